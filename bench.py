@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Decode tokens/s of the Qwen3-8B-shaped Q4_K/Q6_K stack at M = 1 on GB300.
+
+Default arm (ours): one decode token per step through libdq (CUDA graph of
+182 kernels) on synthetic random-init weights (4.65 GB, larger than L2, read
+once per step).  Prints one JSON line with the metric, the roofline of the
+dominant kernel, the end-to-end number through the C ABI with host buffers,
+clock samples and the CPU-oracle baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the token does not shard across GPUs here); the time is the max over ranks.
+The reference arm (--impl reference) times the fp64 CPU oracle on this host's
+cores on the same workload, one token per step; rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantised_gemv_norm_gb300 import ledger, synth  # noqa: E402
+
+METRIC = "decode tokens/s (Qwen3-8B-shaped Q4_K, M=1); achieved HBM GB/s vs GB300 peak"
+SEED = 1
+MAX_CTX = 1024
+WORKLOAD = ("Qwen3-8B-shaped decode token: 36 layers (Q4_K attention q|k|v 6144x4096 and o 4096x4096, "
+            "Q4_K gate/up 12288x4096, down 4096x12288 Q6_K in odd layers / Q4_K in even), final RMSNorm, "
+            "Q6_K vocabulary 151936x4096; empty KV cache (pos 0); M=1")
+# The pages' own number for this workload: llama.cpp, Qwen3-8B Q4_K, empty context, RTX 5090
+# ("The roofline holds on a second GPU", "How I ran it": 248.8 / 253.9 / 255.1 tok/s); median.
+PAGES_BASELINE_TOK_S = 253.9
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_KINDS = ("qkv", "attention", "o_proj", "gate_up", "down", "vocab")
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def aggregate_max(value: float, world: int, device=None) -> float:
+    """Max over ranks (the job's time is its slowest rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return None, "fallback"
+
+
+def hbm_peak_gbs():
+    d, src = measured_peaks()
+    if d:
+        for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+            if key in d and isinstance(d[key], (int, float)):
+                return float(d[key]), "of measured"
+    return FALLBACK_HBM_GBS, "of fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_%d.csv" % gpu_index)
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() in ("active", "1"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def token_bytes(ctx: int) -> int:
+    S = ledger.QWEN3_8B_SHAPE
+    return ledger.token_bytes(S["n_layers"], S["hidden"], S["ffn"], S["n_q"], S["n_kv"], S["hd"], S["vocab"], ctx)
+
+
+def kernel_bytes(kind: str, layer: int, ctx: int) -> int:
+    """Algorithmic bytes of one launch: weights (+ gamma, + K/V read)."""
+    S = ledger.QWEN3_8B_SHAPE
+    H, F = S["hidden"], S["ffn"]
+    qkv_rows = (S["n_q"] + 2 * S["n_kv"]) * S["hd"]
+    if kind == "qkv":
+        return ledger.matrix_bytes(ledger.FMT_Q4K, qkv_rows, H) + 4 * H
+    if kind == "attention":
+        return ledger.kv_read_bytes(1, S["n_kv"], S["hd"], ctx + 1)
+    if kind == "o_proj":
+        return ledger.matrix_bytes(ledger.FMT_Q4K, H, S["n_q"] * S["hd"])
+    if kind == "gate_up":
+        return 2 * ledger.matrix_bytes(ledger.FMT_Q4K, F, H) + 4 * H
+    if kind == "down":
+        fmt = ledger.FMT_Q6K if layer % 2 == 1 else ledger.FMT_Q4K
+        return ledger.matrix_bytes(fmt, H, F)
+    return ledger.matrix_bytes(ledger.FMT_Q6K, S["vocab"], H) + 4 * H
+
+
+# ------------------------------------------------------------------ ours
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    from quantised_gemv_norm_gb300 import build, dq, upload
+
+    build.build()
+    dq.load()
+    t0 = time.time()
+    m = synth.make_model(SEED, max_ctx=MAX_CTX, **synth.QWEN3_8B)
+    kv = synth.make_kv_cache(SEED, m, 0)
+    w = upload.to_device(m, kv, device)
+    model = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=True)
+    setup_s = time.time() - t0
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+
+    K, W = args.steps, args.warmup
+    xs = torch.stack([torch.from_numpy(synth.decode_input(SEED, m.hidden, t)) for t in range(K + W)]).to(device)
+    logits = torch.empty(m.vocab, dtype=torch.float32, device=device)
+
+    # ---- device-timed decode: inputs resident in HBM, pos 0 (empty cache) each step
+    for t in range(W):
+        model.step_raw(xs[t].data_ptr(), 0, logits.data_ptr(), sh)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        torch.cuda.synchronize(device)
+        ev0.record(stream)
+        for t in range(K):
+            model.step_raw(xs[W + t].data_ptr(), 0, logits.data_ptr(), sh)
+        ev1.record(stream)
+        torch.cuda.synchronize(device)
+    barrier(world, device)
+    local_s = ev0.elapsed_time(ev1) / 1e3
+    max_s = aggregate_max(local_s, world, device)
+    err = dq.device_error()
+    tok_s = K * world / max_s
+
+    # ---- end to end through the C ABI with host buffers: pinned x in, logits out, per step
+    x_host = torch.from_numpy(np.stack([synth.decode_input(SEED + 7, m.hidden, t) for t in range(K + W)])).pin_memory()
+    x_dev = torch.empty(m.hidden, dtype=torch.float32, device=device)
+    out_host = torch.empty(m.vocab, dtype=torch.float32).pin_memory()
+
+    def e2e_step(t):
+        x_dev.copy_(x_host[t], non_blocking=True)
+        model.step_raw(x_dev.data_ptr(), 0, logits.data_ptr(), sh)
+        out_host.copy_(logits, non_blocking=True)
+        stream.synchronize()
+
+    for t in range(W):
+        e2e_step(t)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for t in range(K):
+        e2e_step(W + t)
+    torch.cuda.synchronize(device)
+    e2e_local = time.perf_counter() - t0
+    barrier(world, device)
+    e2e_max = aggregate_max(e2e_local, world, device)
+
+    # ---- per-kernel timing (each kind across all 36 layers, alone, CUDA events on this stream)
+    per_kernel = {}
+    for kind_i, kind in enumerate(KERNEL_KINDS):
+        layers = [0] if kind == "vocab" else list(range(m.n_layers))
+        reps = 3 if kind == "vocab" else 1
+        for l in layers[:2]:
+            model.enqueue_kernel(l, kind_i, sh)
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            for l in layers:
+                model.enqueue_kernel(l, kind_i, sh)
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        n = reps * len(layers)
+        us = a.elapsed_time(b) * 1e3 / n
+        byts = sum(kernel_bytes(kind, l, 0) for l in layers) / len(layers)
+        per_kernel[kind] = {"us_per_launch": round(us, 3), "bytes_per_launch": int(byts),
+                            "GBps": round(byts / us / 1e3, 1), "launches_per_token": len(layers)}
+    # dominant kernel: the largest share of a token's summed kernel time
+    share = {k: v["us_per_launch"] * v["launches_per_token"] for k, v in per_kernel.items()}
+    dom = max(share, key=share.get)
+    peak, peak_src = hbm_peak_gbs()
+    dk = per_kernel[dom]
+    achieved = dk["GBps"]
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            traffic = json.load(open(prof)).get(dom)
+        except Exception:
+            traffic = None
+
+    # ---- 512-token context (cache filled with N(0,1) fp16, pos 512)
+    ctx = {}
+    if not args.no_ctx512:
+        kv512 = synth.make_kv_cache(SEED + 1, m, 512)
+        w["kv_cache"].copy_(torch.from_numpy(kv512.view(np.int16)).to(device))
+        del kv512
+        for t in range(W):
+            model.step_raw(xs[t].data_ptr(), 512, logits.data_ptr(), sh)
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for t in range(K):
+            model.step_raw(xs[W + t].data_ptr(), 512, logits.data_ptr(), sh)
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        s512 = aggregate_max(a.elapsed_time(b) / 1e3, world, device)
+        tb512 = token_bytes(512)
+        ctx = {"tokens_per_s": round(K * world / s512, 2), "bytes_per_token": tb512,
+               "GBps": round(tb512 * K / s512 / 1e9, 1)}
+
+    tb = token_bytes(0)
+    out = {
+        "metric": METRIC,
+        "value": round(tok_s, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(max_s / K * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(tok_s / PAGES_BASELINE_TOK_S, 3),
+        "dtype": "f32",
+        "data": "synthetic (seeded random-init Q4_K/Q6_K weights, N(0,1) hidden inputs)",
+        "config": {"workload": WORKLOAD, "bytes_per_token": tb, "ctx": 0,
+                   "l2": "inputs larger than L2: 4.65 GB of weights read per step, no flush needed",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "hbm": {"achieved_GBps_token": round(tb * tok_s / world / 1e9, 1), "peak_GBps": peak,
+                "frac_of_peak": round(tb * tok_s / world / 1e9 / peak, 4), "peak_source": peak_src,
+                "roofline_tokens_per_s": round(peak * 1e9 / tb, 1)},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src},
+        "per_kernel": per_kernel,
+        "ctx512": ctx,
+        "e2e": {"value": round(K * world / e2e_max, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * m.hidden,
+                "d2h_bytes_per_step": 4 * m.vocab},
+        "gpu_launches": model.launches_per_step * K,
+        "clocks": clocks.summary(),
+        "device_error_flag": err,
+        "setup_s": round(setup_s, 1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(m)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    model.close()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+# -------------------------------------------------------------- the oracle
+
+
+def cpu_baseline(m, tokens: int = 1):
+    """The fp64 CPU oracle, as it stands, on this host's cores: `tokens` full decode tokens."""
+    import oracle
+
+    oracle.build()
+    kv = synth.make_kv_cache(SEED, m, 0)
+    t0 = time.perf_counter()
+    for t in range(tokens):
+        oracle.decode_step(m, synth.decode_input(SEED, m.hidden, t), 0, kv)
+    dt = time.perf_counter() - t0
+    return {"value": round(tokens / dt, 4), "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d full decode token(s) of the same workload (pos 0), fp64, %.1f s" % (tokens, dt)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    m = synth.make_model(SEED, max_ctx=MAX_CTX, **synth.QWEN3_8B)
+    import oracle
+
+    oracle.build()
+    kv = synth.make_kv_cache(SEED, m, 0)
+    for t in range(args.warmup):
+        oracle.decode_step(m, synth.decode_input(SEED, m.hidden, t), 0, kv)
+    t0 = time.perf_counter()
+    for t in range(args.steps):
+        oracle.decode_step(m, synth.decode_input(SEED, m.hidden, args.warmup + t), 0, kv)
+    dt = time.perf_counter() - t0
+    v = args.steps / dt
+    cores = oracle.num_threads()
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(v, 4),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(v / PAGES_BASELINE_TOK_S, 5),
+        "dtype": "f64",
+        "data": "synthetic (seeded random-init Q4_K/Q6_K weights, N(0,1) hidden inputs)",
+        "config": {"workload": WORKLOAD, "bytes_per_token": token_bytes(0), "ctx": 0},
+        "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d full decode tokens on the host, fp64" % args.steps},
+        "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--no-ctx512", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if args.steps > 8:
+            args.steps = 8  # bounded sample: ~5-10 s of host time per token
+        if args.warmup > 3:
+            args.warmup = 3
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,252 @@
+/*
+ * dq.h -- C ABI of libdq: the single-token (M = 1) decode hot path of an LLM on
+ * one NVIDIA GB300 (sm_103a): RMSNorm / LayerNorm, matrix-vector products over
+ * bf16, Q4_K and Q6_K weights dequantised in registers, grouped-query decode
+ * attention over an fp16 KV cache, and a whole decode token over a
+ * Qwen3-8B-shaped layer stack.
+ *
+ * Conventions (every entry point):
+ *   - Returns a dq_status: 0 (DQ_OK) or a negative code.  Arguments are checked
+ *     before anything is launched; a failed check launches nothing.
+ *   - Pointers are caller-owned DEVICE pointers unless marked "host".  The
+ *     library never frees caller memory and allocates nothing in the compute
+ *     calls (only dq_model_create allocates, and dq_model_destroy frees).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued asynchronously; nothing synchronises unless
+ *     stated.  A CUDA error at launch returns DQ_ERR_CUDA and
+ *     dq_last_cuda_error() gives the cudaError_t.
+ *   - Kernels bound every internal wait by a wall-clock limit; a timeout sets a
+ *     per-device error flag, readable with dq_device_error().
+ *   - No exception or C++ type crosses this interface.
+ *
+ * Block formats (this library's canonical little-endian layouts; the pages fix
+ * the sizes -- "The roofline holds on a second GPU", sections "The Math" and
+ * "The search space": Q4_K is 4.5 bits per weight, 256 weights in 144 bytes;
+ * Q6_K is 6.5625 bits per weight, 256 weights in 210 bytes -- but not the bit
+ * positions, which are defined here):
+ *
+ *   Q4_K, 144 bytes, weights n = 32 j + i (j = 0..7):
+ *     [0,2) d (binary16)  [2,4) dmin (binary16)
+ *     [4,16) 96-bit little-endian bit string: sc_j at bits 6j..6j+5,
+ *            m_j at bits 48+6j..53+6j (unsigned 6-bit)
+ *     [16,144) byte 16+16j+i: low nibble = code of weight 32j+i,
+ *              high nibble = code of weight 32j+16+i
+ *     w_n = d * sc_j * q_n - dmin * m_j
+ *   Q6_K, 210 bytes, weights n = 32 g + r (g = 0..7):
+ *     [0,128) byte 16g+i: low nibble = low 4 bits of weight 32g+i,
+ *             high nibble = low 4 bits of weight 32g+16+i
+ *     [128,192) high 2 bits of weight 32g+16h+4t+e at bits 2t..2t+1 of byte
+ *               128+8g+4h+e (h in {0,1}; t, e in 0..3)
+ *     [192,208) int8 sc[16], sc[s] for weights 16s..16s+15
+ *     [208,210) d (binary16)
+ *     q_n = low4 | high2 << 4;  w_n = d * sc[n/16] * (q_n - 32)
+ *   A quantised matrix is row-major: row r is the K/256 blocks of that row,
+ *   back to back.  The library requires 16-byte aligned rows, i.e. K % 256 == 0
+ *   for Q4_K and K % 2048 == 0 for Q6_K, and a 16-byte aligned base pointer.
+ *   bf16 matrices are row-major [rows][K], K % 8 == 0, 16-byte aligned.
+ */
+#ifndef DQ_H
+#define DQ_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define DQ_API __declspec(dllexport)
+#else
+#define DQ_API __attribute__((visibility("default")))
+#endif
+
+typedef enum {
+    DQ_OK = 0,
+    DQ_ERR_NULL = -1,        /* a required pointer is NULL */
+    DQ_ERR_SHAPE = -2,       /* a size is zero, negative or inconsistent */
+    DQ_ERR_ALIGN = -3,       /* a pointer or row is not 16-byte aligned */
+    DQ_ERR_UNSUPPORTED = -4, /* a shape this build has no kernel for */
+    DQ_ERR_CUDA = -5,        /* a CUDA runtime call failed: see dq_last_cuda_error() */
+    DQ_ERR_TIMEOUT = -6,     /* a kernel gave up a bounded wait (device flag) */
+    DQ_ERR_ALLOC = -7        /* dq_model_create could not allocate its workspace */
+} dq_status;
+
+/* Weight formats. */
+#define DQ_FMT_BF16 0
+#define DQ_FMT_Q4K 1
+#define DQ_FMT_Q6K 2
+
+/* Static text for a status code (never NULL). */
+DQ_API const char* dq_status_string(int status);
+
+/* cudaError_t of the most recent DQ_ERR_CUDA returned on this host thread. */
+DQ_API int dq_last_cuda_error(void);
+
+/* Synchronises `stream`, then reads and clears the current device's error flag:
+ * 0 if no kernel gave up a bounded wait since the last call, else a bit mask
+ * (1 consumer timeout, 2 producer timeout, 4 copies in flight at exit,
+ * 8 bad argument seen on the device).  Returns DQ_ERR_CUDA on a CUDA error. */
+DQ_API int dq_device_error(void* stream);
+
+/* ------------------------------------------------------------------- norms
+ * "one-serial-kernel" (vocodex.ai), section "One thread": the normalisation
+ * that runs twice per layer and once at the end, reduced by a block of threads
+ * instead of one thread per row; the layer norm in two passes (mean, then the
+ * variance of x - mean).
+ *
+ * dq_rmsnorm:   y[r][i] = x[r][i] / sqrt(mean_i(x[r][i]^2) + eps) * gamma[i]
+ * dq_layernorm: y[r][i] = (x[r][i] - mu_r) / sqrt(var_r + eps) * gamma[i] + beta[i],
+ *               mu_r = mean, var_r = population variance (divide by n).
+ * x, y: fp32 [rows][n] row-major (y may equal x); gamma, beta: fp32 [n].
+ * One thread block of 256 threads per row; fp32 arithmetic.
+ * Errors: NULL pointer -> DQ_ERR_NULL; rows < 1 or n < 1 -> DQ_ERR_SHAPE. */
+DQ_API int dq_rmsnorm(const float* x, const float* gamma, float* y, int rows, int n, float eps, void* stream);
+DQ_API int dq_layernorm(const float* x, const float* gamma, const float* beta, float* y, int rows, int n,
+                        float eps, void* stream);
+
+/* Same computations with an explicit block size (1 .. 1024, a power of two):
+ * threads = 1 is the one-thread-per-row kernel the page measured as the fault;
+ * the sweep over thread counts is the page's "corner control" as a CUDA
+ * block-size sweep.  Errors as above, plus DQ_ERR_SHAPE for a bad count. */
+DQ_API int dq_rmsnorm_threads(const float* x, const float* gamma, float* y, int rows, int n, float eps,
+                              int threads, void* stream);
+DQ_API int dq_layernorm_threads(const float* x, const float* gamma, const float* beta, float* y, int rows,
+                                int n, float eps, int threads, void* stream);
+
+/* -------------------------------------------------------------------- GEMV
+ * "The Mountain Runs" (coderlegion, S-MoE diary #5), section 3: one output per
+ * weight row; the weight stream is read in wide consecutive chunks instead of
+ * one thread per row.  Here rows are streamed into shared memory by bulk (TMA)
+ * copies and dequantised in registers ("The roofline holds on a second GPU",
+ * section "Hiding, fusing...": keep the weights packed, unpack in registers,
+ * accumulate in 32 bits).
+ *
+ *   y[r] = sum_k W[r][k] * x[k],  r < rows, fp32 output.
+ *
+ * dq_gemv_bf16: W bf16 [rows][K], x bf16 [K] (both bit patterns), fp32
+ *   accumulation.  K % 8 == 0, 8 <= K <= 24576.
+ * dq_gemv_q4k / dq_gemv_q6k: W blocks (see the header comment), x fp32 [K].
+ *   The activation is carried as a 15-bit fixed-point vector with one fp32
+ *   scale per 32 elements (relative error <= 2^-15 of each group's largest
+ *   |x|), products are exact 32-bit integer sums, the block scales are applied
+ *   in fp32.  Q4_K: K % 256 == 0, 256 <= K <= 32768.  Q6_K: K % 2048 == 0,
+ *   2048 <= K <= 32768.
+ * W, x 16-byte aligned (DQ_ERR_ALIGN otherwise).  y must not overlap W or x.
+ * Errors: NULL -> DQ_ERR_NULL; rows < 1 or K outside the ranges -> DQ_ERR_SHAPE
+ * or DQ_ERR_UNSUPPORTED. */
+DQ_API int dq_gemv_bf16(const void* W_bf16, const void* x_bf16, float* y, int rows, int K, void* stream);
+DQ_API int dq_gemv_q4k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream);
+DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream);
+
+/* Dequantise nblocks consecutive blocks to fp32 (256 values per block), each
+ * weight computed as the block formula above in fp32.  A test hook: with the
+ * synthetic binades (Q4_K d in [2^-13, 2^-12), dmin in [2^-10, 2^-9); Q6_K d in
+ * [2^-14, 2^-13)) every weight is exact, so the output is bit-exact.
+ * blocks: any alignment; out: fp32 [nblocks * 256].  nblocks >= 1. */
+DQ_API int dq_dequant_q4k(const void* blocks, float* out, long long nblocks, void* stream);
+DQ_API int dq_dequant_q6k(const void* blocks, float* out, long long nblocks, void* stream);
+
+/* -------------------------------------------------------------- attention
+ * Grouped-query decode attention for one token ("The roofline holds on a second
+ * GPU", sections "Said before the run" and "Where the time goes": each new token
+ * also reads the conversation's keys and values; 32 query heads share 8 KV heads
+ * in the Qwen3-8B census).
+ *
+ *   for query head h (KV head g = h / (n_q / n_kv)) and keys j < n_keys:
+ *     s_j = (q_h . k_gj) / sqrt(head_dim);  p = softmax(s);  out_h = sum_j p_j v_gj
+ *
+ * q: fp32 [n_q][head_dim]; k_plane, v_plane: fp16 [n_kv][max_ctx][head_dim]
+ * (one layer of the cache); out: fp32 [n_q][head_dim].  The keys are split into
+ * up to 16 chunks per KV head, one thread block each; the last block to finish
+ * for a KV head merges the chunk partials (max-subtracted log-sum-exp).
+ * workspace: device scratch of dq_attention_workspace_bytes(n_q, n_kv) bytes,
+ * zero-filled by the caller before its first use; the kernel leaves it zeroed
+ * again (its counters) so it can be reused.  Calls that share a workspace must
+ * not overlap in time.
+ * Limits: head_dim == 128, n_q % n_kv == 0, n_q / n_kv <= 8, 1 <= n_keys <= max_ctx.
+ * Errors: NULL -> DQ_ERR_NULL; shapes -> DQ_ERR_SHAPE / DQ_ERR_UNSUPPORTED;
+ * workspace too small -> DQ_ERR_SHAPE. */
+DQ_API size_t dq_attention_workspace_bytes(int n_q, int n_kv);
+DQ_API int dq_attention_decode(const float* q, const void* k_plane, const void* v_plane, float* out, int n_q,
+                               int n_kv, int head_dim, int max_ctx, int n_keys, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------ M-token sweep
+ * "The roofline holds on a second GPU", section "The Math": M tokens share one
+ * read of the weights; below M* = (w/16)(R/BW) memory bounds the product, above
+ * it arithmetic does.  Y[m][r] = sum_k W[r][k] * X[m][k] for m < M.
+ * W: Q4_K blocks [rows][K/256]; X fp32 [M][K]; Y fp32 [M][rows].
+ * 1 <= M <= 64; K as dq_gemv_q4k.  Errors as dq_gemv_q4k. */
+DQ_API int dq_matmul_q4k(const void* W_blocks, const float* X, float* Y, int M, int rows, int K, void* stream);
+
+/* -------------------------------------------------------------- decode step
+ * One decode token over a pre-norm decoder stack ("The roofline holds on a
+ * second GPU", section "The Math": per layer a 4096x4096 attention table plus
+ * 1024x4096 key and value tables, 12288x4096 gate and up tables, a 4096x12288
+ * down table, then a 151936x4096 vocabulary table; "one-serial-kernel",
+ * section "One thread": the norm twice per layer and once at the end).
+ *
+ * Per layer l, with x the fp32 residual vector:
+ *   h = RMSNorm(x, attn_norm[l]);  [q|k|v] = Wqkv[l] h
+ *   cache[l][0][:, pos] = fp16(k);  cache[l][1][:, pos] = fp16(v)
+ *   a = GQA attention of q over keys 0..pos;  x += Wo[l] a
+ *   h = RMSNorm(x, ffn_norm[l]);  x += Wdown[l] (SiLU(Wgate[l] h) * (Wup[l] h))
+ * then logits = Wvocab RMSNorm(x, out_norm).
+ * Each layer runs as five kernels (norm+QKV with the cache append, attention
+ * with its merge, O projection + residual, norm+gate/up+SwiGLU, down + residual)
+ * chained with programmatic dependent launch and captured in one CUDA graph, so
+ * each kernel streams its weights while the previous one finishes.
+ */
+typedef struct dq_model dq_model; /* opaque: owns workspace + graph, BORROWS weights */
+
+typedef struct {
+    int n_layers, hidden, ffn, n_q_heads, n_kv_heads, head_dim, vocab, max_ctx;
+    float eps;
+    /* host arrays of n_layers DEVICE pointers each (copied at create time): */
+    const float* const* attn_norm; /* fp32 [hidden] */
+    const void* const* wqkv;       /* Q4_K [(n_q + 2 n_kv) head_dim][hidden], rows q | k | v */
+    const void* const* wo;         /* Q4_K [hidden][n_q head_dim] */
+    const float* const* ffn_norm;  /* fp32 [hidden] */
+    const void* const* wgate;      /* Q4_K [ffn][hidden] */
+    const void* const* wup;        /* Q4_K [ffn][hidden] */
+    const void* const* wdown;      /* DQ_FMT_Q4K or DQ_FMT_Q6K [hidden][ffn] */
+    const int* down_fmt;           /* host int[n_layers]: format of wdown[l] */
+    const float* out_norm;         /* device fp32 [hidden] */
+    const void* wvocab;            /* device Q6_K [vocab][hidden] */
+    void* kv_cache;                /* device fp16 [n_layers][2][n_kv][max_ctx][head_dim] */
+    int use_graph;                 /* 1: capture the token in a CUDA graph (default); 0: eager launches */
+} dq_model_desc;
+
+/* Validates the description, allocates the workspace (activations, attention
+ * scratch) and captures the token graph on the current device.  Host call;
+ * synchronises the device.  *out receives the handle (NULL on error).
+ * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE, DQ_ERR_ALIGN, DQ_ERR_UNSUPPORTED,
+ * DQ_ERR_ALLOC, DQ_ERR_CUDA. */
+DQ_API int dq_model_create(const dq_model_desc* desc, dq_model** out);
+
+/* Enqueues one token on `stream`: x_in fp32 [hidden] (read), position pos
+ * (0 <= pos < max_ctx; the cache must hold keys 0..pos-1), logits fp32 [vocab]
+ * (written).  Writes this token's k and v into the cache at pos.  Calls on one
+ * model must not overlap in time.  Errors: DQ_ERR_NULL, DQ_ERR_SHAPE, DQ_ERR_CUDA. */
+DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits, void* stream);
+
+/* Number of kernels one dq_decode_step launches. */
+DQ_API int dq_model_launches_per_step(const dq_model* m);
+
+/* Diagnostics for per-kernel timing: enqueues one of the token's kernels on
+ * its own (no programmatic dependency), with the position and logits pointer
+ * of the most recent dq_decode_step on this model.  kind: 0 norm+QKV+append,
+ * 1 attention, 2 O projection + residual, 3 norm+gate/up+SwiGLU, 4 down +
+ * residual, 5 final norm + vocabulary (layer ignored).  It updates the model's
+ * activations and cache row like the token does.
+ * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE (layer or kind out of range), DQ_ERR_CUDA. */
+DQ_API int dq_model_enqueue_kernel(dq_model* m, int layer, int kind, void* stream);
+
+/* Frees the workspace and graph (synchronises the device).  NULL is a no-op. */
+DQ_API int dq_model_destroy(dq_model* m);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DQ_H */

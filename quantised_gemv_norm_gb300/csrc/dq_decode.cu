@@ -1,0 +1,335 @@
+// dq_decode.cu -- one decode token over a pre-norm decoder stack.
+//
+// Per layer five kernels, chained with programmatic dependent launch:
+//   1. RMSNorm(x) fused into the Q|K|V GEMV (Q4_K); the epilogue writes q and
+//      appends k, v to the fp16 cache at pos;
+//   2. grouped-query attention over keys 0..pos, merged by its last block;
+//   3. O projection (Q4_K) + residual add into x;
+//   4. RMSNorm(x) fused into the gate and up GEMVs (Q4_K, streamed together),
+//      epilogue SiLU(gate) * up;
+//   5. down projection (Q4_K or Q6_K) + residual add into x;
+// then RMSNorm(x) fused into the vocabulary GEMV (Q6_K).  The 5 L + 1 launches
+// are captured once in a CUDA graph.  A small kernel before the graph copies
+// x_in and records pos and the logits pointer in device memory, because the
+// graph's arguments are fixed.
+//
+// Layout follows the Qwen3-8B census of "The roofline holds on a second GPU",
+// section "The Math"; the norm placement follows "one-serial-kernel", section
+// "One thread" (twice per layer and once at the end).
+#include <new>
+#include <vector>
+
+#include "dq_attn.cuh"
+#include "dq_gemv_host.h"
+
+namespace dq {
+
+__global__ void step_begin_kernel(const float* __restrict__ x_in, float* __restrict__ x, int n, StepArgs* step,
+                                  int pos, float* logits)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n)
+        x[i] = x_in[i];
+    if (i == 0) {
+        step->pos = pos;
+        step->logits = logits;
+    }
+}
+
+}  // namespace dq
+
+struct dq_model {
+    int n_layers, hidden, ffn, n_q, n_kv, hd, vocab, max_ctx;
+    float eps;
+    std::vector<const float*> attn_norm, ffn_norm;
+    std::vector<const uint8_t*> wqkv, wo, wgate, wup, wdown;
+    std::vector<int> down_fmt;
+    const float* out_norm;
+    const uint8_t* wvocab;
+    __half* kv;
+    // workspace (one allocation)
+    void* ws;
+    float* x;
+    float* q;
+    float* attn;
+    float* act;
+    dq::StepArgs* step;
+    void* attn_ws;
+    // plans
+    dqhost::GemvPlan p_qkv, p_o, p_gateup, p_down_q4, p_down_q6, p_vocab;
+    bool have_down_q4, have_down_q6;
+    // graph
+    int use_graph;
+    cudaStream_t cap_stream;
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+enum { K_QKV = 0, K_ATTN = 1, K_O = 2, K_GATEUP = 3, K_DOWN = 4, K_VOCAB = 5 };
+
+static cudaError_t launch_kernel(dq_model* m, int l, int kind, cudaStream_t s, bool pdl)
+{
+    const int qdim = m->n_q * m->hd, kvdim = m->n_kv * m->hd;
+    const size_t plane = static_cast<size_t>(m->n_kv) * m->max_ctx * m->hd;
+    __half* kc = m->kv + static_cast<size_t>(l) * 2 * plane;
+    __half* vc = kc + plane;
+    int* err = dqhost::device_error_flag();
+    dq::GemvArgs a{};
+    a.err = err;
+    switch (kind) {
+    case K_QKV:  // norm + QKV + cache append
+        a.W = m->wqkv[l];
+        a.pro = dq::PRO_RMS;
+        a.x = m->x;
+        a.gamma = m->attn_norm[l];
+        a.eps = m->eps;
+        a.epi = dq::EPI_QKV;
+        a.y = m->q;
+        a.step = m->step;
+        a.kv_k = kc;
+        a.kv_v = vc;
+        a.qdim = qdim;
+        a.kvdim = kvdim;
+        a.hd = m->hd;
+        a.max_ctx = m->max_ctx;
+        return dqhost::launch_gemv(m->p_qkv, a, s, pdl);
+    case K_ATTN: {
+        dq::AttnArgs t{};
+        t.q = m->q;
+        t.kc = kc;
+        t.vc = vc;
+        t.out = m->attn;
+        dqhost::attention_bind_workspace(t, m->attn_ws);
+        t.n_q = m->n_q;
+        t.n_kv = m->n_kv;
+        t.max_ctx = m->max_ctx;
+        t.step = m->step;
+        t.err = err;
+        return dqhost::launch_attention(t, s, pdl);
+    }
+    case K_O:  // O projection + residual
+        a.W = m->wo[l];
+        a.pro = dq::PRO_F32;
+        a.x = m->attn;
+        a.epi = dq::EPI_RESID;
+        a.y = m->x;
+        return dqhost::launch_gemv(m->p_o, a, s, pdl);
+    case K_GATEUP:  // norm + gate/up + SwiGLU
+        a.W = m->wgate[l];
+        a.W2 = m->wup[l];
+        a.pro = dq::PRO_RMS;
+        a.x = m->x;
+        a.gamma = m->ffn_norm[l];
+        a.eps = m->eps;
+        a.epi = dq::EPI_SWIGLU;
+        a.y = m->act;
+        return dqhost::launch_gemv(m->p_gateup, a, s, pdl);
+    case K_DOWN:  // down + residual
+        a.W = m->wdown[l];
+        a.pro = dq::PRO_F32;
+        a.x = m->act;
+        a.epi = dq::EPI_RESID;
+        a.y = m->x;
+        return dqhost::launch_gemv(m->down_fmt[l] == DQ_FMT_Q6K ? m->p_down_q6 : m->p_down_q4, a, s, pdl);
+    default:  // final norm + vocabulary
+        a.W = m->wvocab;
+        a.pro = dq::PRO_RMS;
+        a.x = m->x;
+        a.gamma = m->out_norm;
+        a.eps = m->eps;
+        a.epi = dq::EPI_STORE;
+        a.y_from_step = 1;
+        a.step = m->step;
+        return dqhost::launch_gemv(m->p_vocab, a, s, pdl);
+    }
+}
+
+static cudaError_t enqueue_token(dq_model* m, cudaStream_t s)
+{
+    cudaError_t e;
+    for (int l = 0; l < m->n_layers; ++l)
+        for (int kind = K_QKV; kind <= K_DOWN; ++kind)
+            if ((e = launch_kernel(m, l, kind, s, true)) != cudaSuccess)
+                return e;
+    return launch_kernel(m, 0, K_VOCAB, s, true);
+}
+
+static void free_model(dq_model* m)
+{
+    if (!m)
+        return;
+    if (m->exec)
+        cudaGraphExecDestroy(m->exec);
+    if (m->graph)
+        cudaGraphDestroy(m->graph);
+    if (m->cap_stream)
+        cudaStreamDestroy(m->cap_stream);
+    if (m->ws)
+        cudaFree(m->ws);
+    delete m;
+}
+
+extern "C" {
+
+DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
+{
+    if (!out)
+        return DQ_ERR_NULL;
+    *out = nullptr;
+    if (!d || !d->attn_norm || !d->wqkv || !d->wo || !d->ffn_norm || !d->wgate || !d->wup || !d->wdown ||
+        !d->down_fmt || !d->out_norm || !d->wvocab || !d->kv_cache)
+        return DQ_ERR_NULL;
+    if (d->n_layers < 1 || d->hidden < 1 || d->ffn < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1 ||
+        d->head_dim < 1 || d->vocab < 1 || d->max_ctx < 1 || d->n_q_heads % d->n_kv_heads)
+        return DQ_ERR_SHAPE;
+    if (d->head_dim != dq::ATT_HD || d->n_q_heads / d->n_kv_heads > 8 || d->n_kv_heads > dq::ATT_COUNTER_BYTES / 4)
+        return DQ_ERR_UNSUPPORTED;
+    const int qdim = d->n_q_heads * d->head_dim, kvdim = d->n_kv_heads * d->head_dim;
+    if (d->hidden % 256 || d->ffn % 256 || qdim % 256)
+        return DQ_ERR_SHAPE;
+    for (int l = 0; l < d->n_layers; ++l) {
+        if (!d->attn_norm[l] || !d->wqkv[l] || !d->wo[l] || !d->ffn_norm[l] || !d->wgate[l] || !d->wup[l] ||
+            !d->wdown[l])
+            return DQ_ERR_NULL;
+        if (d->down_fmt[l] != DQ_FMT_Q4K && d->down_fmt[l] != DQ_FMT_Q6K)
+            return DQ_ERR_SHAPE;
+        if (!dqhost::aligned16(d->attn_norm[l]) || !dqhost::aligned16(d->wqkv[l]) || !dqhost::aligned16(d->wo[l]) ||
+            !dqhost::aligned16(d->ffn_norm[l]) || !dqhost::aligned16(d->wgate[l]) || !dqhost::aligned16(d->wup[l]) ||
+            !dqhost::aligned16(d->wdown[l]))
+            return DQ_ERR_ALIGN;
+    }
+    if (!dqhost::aligned16(d->out_norm) || !dqhost::aligned16(d->wvocab) || !dqhost::aligned16(d->kv_cache))
+        return DQ_ERR_ALIGN;
+
+    dq_model* m = new (std::nothrow) dq_model();
+    if (!m)
+        return DQ_ERR_ALLOC;
+    m->n_layers = d->n_layers;
+    m->hidden = d->hidden;
+    m->ffn = d->ffn;
+    m->n_q = d->n_q_heads;
+    m->n_kv = d->n_kv_heads;
+    m->hd = d->head_dim;
+    m->vocab = d->vocab;
+    m->max_ctx = d->max_ctx;
+    m->eps = d->eps;
+    m->use_graph = d->use_graph;
+    for (int l = 0; l < d->n_layers; ++l) {
+        m->attn_norm.push_back(d->attn_norm[l]);
+        m->ffn_norm.push_back(d->ffn_norm[l]);
+        m->wqkv.push_back(static_cast<const uint8_t*>(d->wqkv[l]));
+        m->wo.push_back(static_cast<const uint8_t*>(d->wo[l]));
+        m->wgate.push_back(static_cast<const uint8_t*>(d->wgate[l]));
+        m->wup.push_back(static_cast<const uint8_t*>(d->wup[l]));
+        m->wdown.push_back(static_cast<const uint8_t*>(d->wdown[l]));
+        m->down_fmt.push_back(d->down_fmt[l]);
+        if (d->down_fmt[l] == DQ_FMT_Q6K)
+            m->have_down_q6 = true;
+        else
+            m->have_down_q4 = true;
+    }
+    m->out_norm = d->out_norm;
+    m->wvocab = static_cast<const uint8_t*>(d->wvocab);
+    m->kv = static_cast<__half*>(d->kv_cache);
+
+    int st;
+    const int ring = dqhost::GEMV_RING_DEFAULT;
+    if ((st = dqhost::plan_gemv(DQ_FMT_Q4K, qdim + 2 * kvdim, d->hidden, 1, ring, &m->p_qkv)) != DQ_OK ||
+        (st = dqhost::plan_gemv(DQ_FMT_Q4K, d->hidden, qdim, 1, ring, &m->p_o)) != DQ_OK ||
+        (st = dqhost::plan_gemv(DQ_FMT_Q4K, d->ffn, d->hidden, 2, ring, &m->p_gateup)) != DQ_OK ||
+        (m->have_down_q4 && (st = dqhost::plan_gemv(DQ_FMT_Q4K, d->hidden, d->ffn, 1, ring, &m->p_down_q4)) != DQ_OK) ||
+        (m->have_down_q6 && (st = dqhost::plan_gemv(DQ_FMT_Q6K, d->hidden, d->ffn, 1, ring, &m->p_down_q6)) != DQ_OK) ||
+        (st = dqhost::plan_gemv(DQ_FMT_Q6K, d->vocab, d->hidden, 1, ring, &m->p_vocab)) != DQ_OK) {
+        free_model(m);
+        return st;
+    }
+
+    // workspace: x | q | attn | act | step | attention scratch, each 256-byte aligned
+    auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+    const size_t bx = up(sizeof(float) * d->hidden), bq = up(sizeof(float) * qdim), ba = bq,
+                 bf = up(sizeof(float) * d->ffn), bs = up(sizeof(dq::StepArgs)),
+                 bw = up(dqhost::attention_workspace_bytes(d->n_q_heads, d->n_kv_heads));
+    cudaError_t e = cudaMalloc(&m->ws, bx + bq + ba + bf + bs + bw);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        free_model(m);
+        return DQ_ERR_ALLOC;
+    }
+    char* base = static_cast<char*>(m->ws);
+    m->x = reinterpret_cast<float*>(base);
+    m->q = reinterpret_cast<float*>(base + bx);
+    m->attn = reinterpret_cast<float*>(base + bx + bq);
+    m->act = reinterpret_cast<float*>(base + bx + bq + ba);
+    m->step = reinterpret_cast<dq::StepArgs*>(base + bx + bq + ba + bf);
+    m->attn_ws = base + bx + bq + ba + bf + bs;
+    if ((e = cudaMemset(m->ws, 0, bx + bq + ba + bf + bs + bw)) != cudaSuccess) {
+        free_model(m);
+        return dqhost::set_cuda_error(e);
+    }
+    if (m->use_graph) {
+        if ((e = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeRelaxed)) != cudaSuccess) {
+            free_model(m);
+            return dqhost::set_cuda_error(e);
+        }
+        cudaError_t e1 = enqueue_token(m, m->cap_stream);
+        cudaError_t e2 = cudaStreamEndCapture(m->cap_stream, &m->graph);
+        if (e1 != cudaSuccess || e2 != cudaSuccess) {
+            free_model(m);
+            return dqhost::set_cuda_error(e1 != cudaSuccess ? e1 : e2);
+        }
+        if ((e = cudaGraphInstantiate(&m->exec, m->graph, 0)) != cudaSuccess) {
+            free_model(m);
+            return dqhost::set_cuda_error(e);
+        }
+    }
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) {
+        free_model(m);
+        return dqhost::set_cuda_error(e);
+    }
+    *out = m;
+    return DQ_OK;
+}
+
+DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits, void* stream)
+{
+    if (!m || !x_in || !logits)
+        return DQ_ERR_NULL;
+    if (pos < 0 || pos >= m->max_ctx)
+        return DQ_ERR_SHAPE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int threads = 256;
+    dq::step_begin_kernel<<<(m->hidden + threads - 1) / threads, threads, 0, s>>>(x_in, m->x, m->hidden, m->step,
+                                                                                  pos, logits);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return dqhost::set_cuda_error(e);
+    e = m->use_graph ? cudaGraphLaunch(m->exec, s) : enqueue_token(m, s);
+    return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
+}
+
+DQ_API int dq_model_launches_per_step(const dq_model* m)
+{
+    return m ? 2 + 5 * m->n_layers : 0;
+}
+
+DQ_API int dq_model_enqueue_kernel(dq_model* m, int layer, int kind, void* stream)
+{
+    if (!m)
+        return DQ_ERR_NULL;
+    if (kind < K_QKV || kind > K_VOCAB || layer < 0 || layer >= m->n_layers)
+        return DQ_ERR_SHAPE;
+    cudaError_t e = launch_kernel(m, layer, kind, static_cast<cudaStream_t>(stream), false);
+    return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
+}
+
+DQ_API int dq_model_destroy(dq_model* m)
+{
+    if (!m)
+        return DQ_OK;
+    cudaDeviceSynchronize();
+    free_model(m);
+    return DQ_OK;
+}
+
+}  // extern "C"

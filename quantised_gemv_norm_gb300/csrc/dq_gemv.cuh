@@ -1,0 +1,484 @@
+// dq_gemv.cuh -- the weight-streaming matrix-vector kernel (sm_103a).
+//
+// y[r] = sum_k W[r][k] x[k] for bf16, Q4_K and Q6_K rows ("The Mountain Runs",
+// section 3: one output per weight row, the weights read in wide consecutive
+// chunks; "The roofline holds on a second GPU", section "Hiding, fusing...":
+// packed weights unpacked in registers, 32-bit accumulation, enough bytes in
+// flight to cover the memory latency).
+//
+// Structure of one thread block (1 per SM, 288 threads):
+//   * warp 8 is the producer: one elected lane streams the block's rows, R rows
+//     per stage, into a ring of shared-memory stages with 1-D bulk (TMA) copies
+//     that complete on an mbarrier (L2 evict-first: weights are read once);
+//   * warps 0-7 (256 threads) consume.  They are split into RG row groups of P
+//     threads; within a group each thread owns UL fixed 32-weight units of the
+//     K axis (16-byte bf16 units for bf16), so its slice of the activation is
+//     loaded, normalised and quantised once, into registers, in the prologue;
+//   * per stage each thread forms its unit dot products for RPT rows, the group
+//     reduces them (transpose-reduce in the warp, then shared memory across the
+//     group's warps) and one thread per row runs the epilogue.
+// The producer starts before griddepcontrol.wait: weights never depend on the
+// previous kernel, so under programmatic dependent launch the ring fills while
+// the previous kernel drains.  Consumers read activations only after the wait.
+#pragma once
+
+#include "dq_common.cuh"
+
+namespace dq {
+
+constexpr int NCONS = 256;
+constexpr int NCONS_WARPS = NCONS / 32;
+constexpr int GEMV_THREADS = NCONS + 32;
+constexpr int MAX_STAGES = 8;
+constexpr int MAX_RPT = 4;
+constexpr int CONS_BAR = 1;  // named barrier id of the consumer warps
+
+enum { PRO_F32 = 0, PRO_RMS = 1, PRO_BF16 = 2 };
+enum { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SWIGLU = 3 };
+
+// Per-token arguments of the decode graph, in device memory.
+struct StepArgs {
+    int pos;
+    int pad;
+    float* logits;
+};
+
+struct GemvArgs {
+    const uint8_t* W;   // matrix 0, row-major rows of row_bytes
+    const uint8_t* W2;  // matrix 1 (EPI_SWIGLU: the up table), else null
+    int rows;           // rows of each matrix
+    int K;
+    int row_bytes;
+    int P;              // consumer threads per row group
+    int RG;             // row groups (NCONS / P)
+    int nstage;
+    int stage_bytes;    // RG * RPT * row_bytes * NMAT
+    int pro;            // PRO_*
+    int epi;            // EPI_*
+    const float* x;     // fp32 activation [K] (PRO_F32, PRO_RMS)
+    const uint16_t* xb; // bf16 activation [K] (PRO_BF16)
+    const float* gamma; // RMSNorm weight [K] (PRO_RMS)
+    float eps;
+    float* y;           // output [rows] (EPI_STORE/RESID/SWIGLU), q output (EPI_QKV)
+    int y_from_step;    // EPI_STORE: write to step->logits instead of y
+    const StepArgs* step;
+    __half* kv_k;       // EPI_QKV: this layer's K plane [n_kv][max_ctx][hd]
+    __half* kv_v;
+    int qdim, kvdim, hd, max_ctx;
+    int* err;
+};
+
+// ---------------------------------------------------------- activation units
+
+// One 32-element slice of the activation as 15-bit fixed point.
+struct XQ {
+    uint32_t q[16];  // q[p] = xi[2p] (low 16 bits) | xi[2p+1] << 16, |xi| <= 16383
+    float s;         // x ~= s * xi
+    float f;         // Q4_K: s / 16;          Q6_K: unused
+    float hsum;      // Q4_K: sum of the 32 fp32 values
+    int s32a, s32b;  // Q6_K: 32 * sum xi[0..15], 32 * sum xi[16..31]
+};
+
+constexpr float XQ_MAX = 16383.0f;
+
+// Natural unit index -> first k of the unit.  Q6_K units are permuted within
+// spans of 8 blocks so that the 4 blocks a warp touches have distinct
+// shared-memory bank phases (block stride 210 B).
+template <int FMT>
+__device__ __forceinline__ int unit_k0(int n)
+{
+    if (FMT == FMT_Q6K) {
+        const int B = n >> 3, i = B & 7;
+        const int Bp = (B & ~7) + (i < 4 ? 2 * i : 2 * (i - 4) + 1);
+        return 256 * Bp + 32 * (n & 7);
+    }
+    return 32 * n;
+}
+
+__device__ __forceinline__ void quantise_unit(const float (&h)[32], XQ& u)
+{
+    float amax = 0.f, hs = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        amax = fmaxf(amax, fabsf(h[e]));
+        hs += h[e];
+    }
+    const float inv = amax > 0.f ? XQ_MAX / amax : 0.f;
+    u.s = amax / XQ_MAX;
+    u.f = u.s * 0.0625f;
+    u.hsum = hs;
+    int sa = 0, sb = 0;
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+        const int a = __float2int_rn(h[2 * p] * inv);
+        const int b = __float2int_rn(h[2 * p + 1] * inv);
+        u.q[p] = (static_cast<uint32_t>(a) & 0xffffu) | (static_cast<uint32_t>(b) << 16);
+        if (p < 8)
+            sa += a + b;
+        else
+            sb += a + b;
+    }
+    u.s32a = 32 * sa;
+    u.s32b = 32 * sb;
+}
+
+// ------------------------------------------------------------- unit products
+
+// Q4_K unit n of a row: 32 weights of sub-block j = n & 7 of block n >> 3.
+__device__ __forceinline__ float q4k_unit(const uint8_t* rp, int n, const XQ& u)
+{
+    const int j = n & 7;
+    const uint8_t* bp = rp + Q4K_BYTES * (n >> 3);
+    const uint4 hd = lds128(bp);
+    const uint4 c = lds128(bp + 16 + 16 * j);
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    int lo = 0, hi = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint32_t l = cw[t] & 0x0F0F0F0Fu;  // codes of weights 4t .. 4t+3
+        const uint32_t h = cw[t] & 0xF0F0F0F0u;  // 16 x codes of weights 16+4t .. 16+4t+3
+        lo = dp2a_lo(u.q[2 * t], l, lo);
+        lo = dp2a_hi(u.q[2 * t + 1], l, lo);
+        hi = dp2a_lo(u.q[8 + 2 * t], h, hi);
+        hi = dp2a_hi(u.q[8 + 2 * t + 1], h, hi);
+    }
+    const int dot16 = lo * 16 + hi;  // 16 * sum q * xi
+    // scale j: bits 6j.. of the 96-bit string (hd.y, hd.z, hd.w); min j: bits 48+6j..
+    const uint32_t s_lo = j < 6 ? hd.y : hd.z, s_hi = j < 6 ? hd.z : hd.w;
+    const uint32_t m_lo = j < 3 ? hd.z : hd.w, m_hi = j < 3 ? hd.w : 0u;
+    const int sc = static_cast<int>(__funnelshift_r(s_lo, s_hi, (6 * j) & 31) & 63u);
+    const int mn = static_cast<int>(__funnelshift_r(m_lo, m_hi, (48 + 6 * j) & 31) & 63u);
+    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+    return (d * static_cast<float>(sc)) * (u.f * static_cast<float>(dot16)) -
+           (dmin * static_cast<float>(mn)) * u.hsum;
+}
+
+// Q6_K unit: 32 weights of group g of (permuted) block Bp; fields start at
+// even byte offsets, so they are read as aligned words and re-aligned.
+__device__ __forceinline__ float q6k_unit(const uint8_t* rp, int n, const XQ& u)
+{
+    const int B = n >> 3, i = B & 7;
+    const int Bp = (B & ~7) + (i < 4 ? 2 * i : 2 * (i - 4) + 1);
+    const int g = n & 7;
+    const uint8_t* bp = rp + Q6K_BYTES * Bp;
+    const uint32_t sh = (Bp & 1) ? 16u : 0u;       // rows are 16-byte aligned
+    const uint8_t* pl = bp + 16 * g - (sh >> 3);    // aligned word at or before ql
+    const uint8_t* ph = bp + 128 + 8 * g - (sh >> 3);
+    const uint32_t w0 = lds32(pl), w1 = lds32(pl + 4), w2 = lds32(pl + 8), w3 = lds32(pl + 12),
+                   w4 = lds32(pl + 16);
+    const uint32_t ql[4] = {__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
+                            __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh)};
+    const uint32_t h0 = lds32(ph), h1 = lds32(ph + 4), h2 = lds32(ph + 8);
+    const uint32_t H0 = __funnelshift_r(h0, h1, sh), H1 = __funnelshift_r(h1, h2, sh);
+    const uint32_t scw = *reinterpret_cast<const uint16_t*>(bp + 192 + 2 * g);
+    const uint32_t dbits = *reinterpret_cast<const uint16_t*>(bp + 208);
+    int da = 0, db = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        // high two bits of weights 4t+e sit at bits 2t of byte e: move them to bits 4-5
+        const uint32_t ha = (t < 2 ? (H0 << (4 - 2 * t)) : (H0 >> (2 * t - 4))) & 0x30303030u;
+        const uint32_t hb = (t < 2 ? (H1 << (4 - 2 * t)) : (H1 >> (2 * t - 4))) & 0x30303030u;
+        const uint32_t qa = (ql[t] & 0x0F0F0F0Fu) | ha;         // q of weights 4t+e
+        const uint32_t qb = ((ql[t] >> 4) & 0x0F0F0F0Fu) | hb;  // q of weights 16+4t+e
+        da = dp2a_lo(u.q[2 * t], qa, da);
+        da = dp2a_hi(u.q[2 * t + 1], qa, da);
+        db = dp2a_lo(u.q[8 + 2 * t], qb, db);
+        db = dp2a_hi(u.q[8 + 2 * t + 1], qb, db);
+    }
+    const int sca = static_cast<int>(static_cast<int8_t>(scw & 0xffu));
+    const int scb = static_cast<int>(static_cast<int8_t>(scw >> 8));
+    const int v = sca * (da - u.s32a) + scb * (db - u.s32b);  // sum sc (q - 32) xi, |v| < 2^31
+    return (half_bits_to_float(dbits) * u.s) * static_cast<float>(v);
+}
+
+// bf16 unit n: 8 weights at byte 16n of the row; xb holds the 8 bf16 activations.
+__device__ __forceinline__ float bf16_unit(const uint8_t* rp, int n, const uint32_t (&xb)[4])
+{
+    const uint4 w = lds128(rp + 16 * n);
+    float a0 = bf16lo(w.x) * bf16lo(xb[0]);
+    float a1 = bf16hi(w.x) * bf16hi(xb[0]);
+    a0 = fmaf(bf16lo(w.y), bf16lo(xb[1]), a0);
+    a1 = fmaf(bf16hi(w.y), bf16hi(xb[1]), a1);
+    a0 = fmaf(bf16lo(w.z), bf16lo(xb[2]), a0);
+    a1 = fmaf(bf16hi(w.z), bf16hi(xb[2]), a1);
+    a0 = fmaf(bf16lo(w.w), bf16lo(xb[3]), a0);
+    a1 = fmaf(bf16hi(w.w), bf16hi(xb[3]), a1);
+    return a0 + a1;
+}
+
+// -------------------------------------------------------- warp reductions
+
+// Reduce NV values per lane across the warp.  Afterwards the lanes with
+// (lane % (32 / NV)) == 0 hold the total of value index
+// sum_s bit(lane, 16 >> s) * (NV >> (s + 1)), i.e. lane 32/NV * v holds value v.
+template <int NV>
+__device__ __forceinline__ void warp_transpose_reduce(float (&v)[NV], int lane)
+{
+    int n = NV;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        if (n > 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int k = 0; k < NV / 2; ++k) {
+                if (k < n / 2) {
+                    const float send = up ? v[k] : v[k + n / 2];
+                    const float keep = up ? v[k + n / 2] : v[k];
+                    v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            n >>= 1;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int FMT>
+struct UnitState;
+template <>
+struct UnitState<FMT_Q4K> {
+    XQ x;
+};
+template <>
+struct UnitState<FMT_Q6K> {
+    XQ x;
+};
+template <>
+struct UnitState<FMT_BF16> {
+    uint32_t xb[4];
+};
+
+template <int FMT, int UL, int RPT, int NMAT>
+__global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? 80 : (UL == 2 ? 128 : 144)) gemv_stream_kernel(const __grid_constant__ GemvArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int ring_bytes = a.nstage * a.stage_bytes;
+    float* red = reinterpret_cast<float*>(smem + ring_bytes);             // [2][8][RPT*NMAT]
+    float* nred = red + 2 * NCONS_WARPS * RPT * NMAT;                      // [8]
+    int* abort_flag = reinterpret_cast<int*>(nred + NCONS_WARPS);          // [2]
+    uint64_t* full = reinterpret_cast<uint64_t*>(abort_flag + 2);          // [MAX_STAGES]
+    uint64_t* empty = full + MAX_STAGES;                                   // [MAX_STAGES]
+
+    pdl_trigger();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * a.rows / gridDim.x);
+    const int r1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * a.rows / gridDim.x);
+    const int R = a.RG * RPT;
+    const int ntiles = (r1 - r0 + R - 1) / R;
+
+    if (tid == 0) {
+        for (int s = 0; s < a.nstage; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NCONS_WARPS);
+        }
+        abort_flag[0] = 0;
+        abort_flag[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ producer
+    if (warp == NCONS_WARPS) {
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            int issued = 0;
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % a.nstage;
+                if (t >= a.nstage && !mbar_wait(&empty[s], ((t / a.nstage) - 1) & 1)) {
+                    set_error(a.err, DEVERR_TIMEOUT_EMPTY);
+                    break;
+                }
+                const int row = r0 + t * R;
+                const int nr = min(R, r1 - row);
+                const uint32_t bytes = static_cast<uint32_t>(nr * a.row_bytes);
+                uint8_t* dst = smem + static_cast<size_t>(s) * a.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], bytes * NMAT);
+                bulk_g2s(dst, a.W + static_cast<size_t>(row) * a.row_bytes, bytes, &full[s], pol);
+                if (NMAT == 2)
+                    bulk_g2s(dst + static_cast<size_t>(R) * a.row_bytes, a.W2 + static_cast<size_t>(row) * a.row_bytes,
+                             bytes, &full[s], pol);
+                ++issued;
+            }
+            // do not leave the block with copies in flight
+            for (int t = max(0, issued - a.nstage); t < issued; ++t)
+                if (!mbar_wait(&full[t % a.nstage], (t / a.nstage) & 1))
+                    set_error(a.err, DEVERR_TIMEOUT_DRAIN);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers
+    pdl_wait();
+    const int g = tid / a.P;
+    const int p = tid - g * a.P;
+    const int U = (FMT == FMT_BF16) ? a.K / 8 : a.K / 32;
+
+    UnitState<FMT> us[UL];
+    bool have[UL];
+#pragma unroll
+    for (int k = 0; k < UL; ++k)
+        have[k] = (p + a.P * k) < U;
+
+    if (FMT == FMT_BF16) {
+#pragma unroll
+        for (int k = 0; k < UL; ++k) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (have[k])
+                v = __ldcg(reinterpret_cast<const uint4*>(a.xb) + (p + a.P * k));
+            uint32_t* xb = reinterpret_cast<uint32_t*>(&us[k]);
+            xb[0] = v.x; xb[1] = v.y; xb[2] = v.z; xb[3] = v.w;
+        }
+    } else {
+        float rstd = 1.f;
+        if (a.pro == PRO_RMS) {
+            float ss = 0.f;
+#pragma unroll
+            for (int k = 0; k < UL; ++k) {
+                if (have[k]) {
+                    const float* xp = a.x + unit_k0<FMT>(p + a.P * k);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 v = ldg_cg_f4(xp + 4 * e);
+                        ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
+                        ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+                    }
+                }
+            }
+            ss = warp_sum(ss);
+            if (lane == 0)
+                nred[warp] = ss;
+            named_bar_sync(CONS_BAR, NCONS);
+            float tot = 0.f;
+            const int w0 = (g * a.P) >> 5, nw = a.P >> 5;
+            for (int w = 0; w < nw; ++w)
+                tot += nred[w0 + w];
+            rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
+        }
+#pragma unroll
+        for (int k = 0; k < UL; ++k) {
+            float h[32];
+            if (have[k]) {
+                const int k0 = unit_k0<FMT>(p + a.P * k);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 v = ldg_cg_f4(a.x + k0 + 4 * e);
+                    h[4 * e] = v.x; h[4 * e + 1] = v.y; h[4 * e + 2] = v.z; h[4 * e + 3] = v.w;
+                }
+                if (a.pro == PRO_RMS) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 gm = __ldg(reinterpret_cast<const float4*>(a.gamma + k0) + e);
+                        h[4 * e] = h[4 * e] * rstd * gm.x;
+                        h[4 * e + 1] = h[4 * e + 1] * rstd * gm.y;
+                        h[4 * e + 2] = h[4 * e + 2] * rstd * gm.z;
+                        h[4 * e + 3] = h[4 * e + 3] * rstd * gm.w;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    h[e] = 0.f;
+            }
+            quantise_unit(h, reinterpret_cast<XQ&>(us[k]));
+        }
+    }
+
+    constexpr int NV = RPT * NMAT;
+    for (int t = 0; t < ntiles; ++t) {
+        const int s = t % a.nstage;
+        if (!mbar_wait(&full[s], (t / a.nstage) & 1)) {
+            set_error(a.err, DEVERR_TIMEOUT_FULL);
+            atomicExch(&abort_flag[t & 1], 1);
+        }
+        const uint8_t* tile = smem + static_cast<size_t>(s) * a.stage_bytes;
+        const int row0 = r0 + t * R;
+        const int nr = min(R, r1 - row0);
+        float acc[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+            acc[v] = 0.f;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            const int row = g + a.RG * i;
+            if (row < nr) {
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) {
+                    const uint8_t* rp = tile + static_cast<size_t>(m * R + row) * a.row_bytes;
+                    float sum = 0.f;
+#pragma unroll
+                    for (int k = 0; k < UL; ++k) {
+                        if (have[k]) {
+                            const int n = p + a.P * k;
+                            if (FMT == FMT_Q4K)
+                                sum += q4k_unit(rp, n, reinterpret_cast<const XQ&>(us[k]));
+                            else if (FMT == FMT_Q6K)
+                                sum += q6k_unit(rp, n, reinterpret_cast<const XQ&>(us[k]));
+                            else
+                                sum += bf16_unit(rp, n, reinterpret_cast<const uint32_t(&)[4]>(us[k]));
+                        }
+                    }
+                    acc[m * RPT + i] = sum;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[s]);  // this warp is done with the stage
+
+        warp_transpose_reduce<NV>(acc, lane);
+        float* rb = red + (t & 1) * NCONS_WARPS * NV;
+        if ((lane & (32 / NV - 1)) == 0)
+            rb[warp * NV + lane / (32 / NV)] = acc[0];
+        named_bar_sync(CONS_BAR, NCONS);
+        if (tid < R) {
+            const int rg = tid % a.RG, i = tid / a.RG;
+            if (tid < nr) {
+                const int w0 = (rg * a.P) >> 5, nw = a.P >> 5;
+                float v0 = 0.f, v1 = 0.f;
+                for (int w = 0; w < nw; ++w) {
+                    v0 += rb[(w0 + w) * NV + i];
+                    if (NMAT == 2)
+                        v1 += rb[(w0 + w) * NV + RPT + i];
+                }
+                const int r = row0 + tid;
+                if (a.epi == EPI_STORE) {
+                    float* out = a.y_from_step ? a.step->logits : a.y;
+                    out[r] = v0;
+                } else if (a.epi == EPI_RESID) {
+                    a.y[r] += v0;
+                } else if (a.epi == EPI_SWIGLU) {
+                    a.y[r] = v0 / (1.0f + expf(-v0)) * v1;
+                } else {  // EPI_QKV
+                    if (r < a.qdim) {
+                        a.y[r] = v0;
+                    } else {
+                        const int idx = r - a.qdim;
+                        const int which = idx / a.kvdim, rem = idx - which * a.kvdim;
+                        const int kvh = rem / a.hd, dd = rem - kvh * a.hd;
+                        __half* plane = which ? a.kv_v : a.kv_k;
+                        const int pos = a.step->pos;
+                        if (pos >= 0 && pos < a.max_ctx)
+                            plane[(static_cast<size_t>(kvh) * a.max_ctx + pos) * a.hd + dd] = __float2half_rn(v0);
+                        else
+                            set_error(a.err, DEVERR_BAD_ARG);
+                    }
+                }
+            }
+        }
+        // uniform: every consumer reads this tile's flag after the same barrier; a
+        // flag for tile t+1 goes to the other slot, so a fast thread cannot race it
+        if (*reinterpret_cast<volatile int*>(&abort_flag[t & 1]))
+            break;
+    }
+}
+
+// Shared-memory bytes the kernel needs beyond the ring.
+__host__ __device__ constexpr int gemv_extra_smem(int rpt, int nmat)
+{
+    return 2 * NCONS_WARPS * rpt * nmat * 4 + NCONS_WARPS * 4 + 2 * 4 + 2 * MAX_STAGES * 8 + 16;
+}
+
+}  // namespace dq

@@ -1,0 +1,288 @@
+// dq_gemv_host.cu -- plans and launches the streaming GEMV; the GEMV and
+// dequantisation entry points of the C ABI.
+#include <mutex>
+
+#include "dq_gemv_host.h"
+
+namespace dqhost {
+
+static int row_bytes_of(int fmt, int K)
+{
+    if (fmt == DQ_FMT_BF16)
+        return 2 * K;
+    return (K / 256) * (fmt == DQ_FMT_Q4K ? dq::Q4K_BYTES : dq::Q6K_BYTES);
+}
+
+static GemvKernel kernel_for(int fmt, int ul, int rpt, int nmat)
+{
+    if (fmt == DQ_FMT_Q4K)
+        return gemv_kernel_q4k(ul, rpt, nmat);
+    if (fmt == DQ_FMT_Q6K)
+        return gemv_kernel_q6k(ul, rpt, nmat);
+    return gemv_kernel_bf16(ul, rpt, nmat);
+}
+
+static cudaError_t ensure_smem_attr(GemvKernel k, int bytes)
+{
+    static std::mutex mu;
+    static GemvKernel keys[256];
+    static int vals[256];
+    static int n = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (keys[i] == k) {
+            if (vals[i] >= bytes)
+                return cudaSuccess;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+            if (e == cudaSuccess)
+                vals[i] = bytes;
+            return e;
+        }
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && n < 256) {
+        keys[n] = k;
+        vals[n] = bytes;
+        ++n;
+    }
+    return e;
+}
+
+int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, GemvPlan* plan)
+{
+    if (rows < 1 || K < 1)
+        return DQ_ERR_SHAPE;
+    const int unit_w = fmt == DQ_FMT_BF16 ? 8 : 32;
+    if (fmt == DQ_FMT_BF16 && K % 8)
+        return DQ_ERR_SHAPE;
+    if (fmt == DQ_FMT_Q4K && K % 256)
+        return DQ_ERR_SHAPE;
+    if (fmt == DQ_FMT_Q6K && K % 2048)
+        return DQ_ERR_ALIGN;  // 210-byte blocks: rows are 16-byte aligned only when K % 2048 == 0
+    const int U = K / unit_w;
+    const int rb = row_bytes_of(fmt, K);
+    static const int ul_q[] = {1, 2, 3, 4};
+    static const int ul_b[] = {1, 2, 4, 8, 12};
+    const int* uls = fmt == DQ_FMT_BF16 ? ul_b : ul_q;
+    const int nul = fmt == DQ_FMT_BF16 ? 5 : 4;
+    static const int Ps[] = {128, 256, 64, 32};
+    int best_P = 0, best_UL = 0, best_waste = 1 << 30;
+    for (int pi = 0; pi < 4; ++pi) {
+        const int P = Ps[pi];
+        const int need = (U + P - 1) / P;
+        int UL = 0;
+        for (int i = 0; i < nul; ++i)
+            if (uls[i] >= need) {
+                UL = uls[i];
+                break;
+            }
+        if (!UL)
+            continue;
+        const int RG = dq::NCONS / P;
+        if (static_cast<long long>(RG) * rb * nmat > GEMV_STAGE_MAX)
+            continue;
+        const int waste = UL * P - U;
+        if (waste < best_waste) {
+            best_waste = waste;
+            best_P = P;
+            best_UL = UL;
+        }
+    }
+    if (!best_P)
+        return DQ_ERR_UNSUPPORTED;
+    GemvPlan p{};
+    p.fmt = fmt;
+    p.rows = rows;
+    p.K = K;
+    p.nmat = nmat;
+    p.row_bytes = rb;
+    p.P = best_P;
+    p.RG = dq::NCONS / best_P;
+    p.UL = best_UL;
+    p.RPT = 1;
+    for (int r = 4; r >= 1; r >>= 1)
+        if (static_cast<long long>(p.RG) * r * rb * nmat <= GEMV_STAGE_TARGET) {
+            p.RPT = r;
+            break;
+        }
+    p.stage_bytes = p.RG * p.RPT * rb * nmat;
+    p.nstage = ring_bytes / p.stage_bytes;
+    if (p.nstage < 2)
+        p.nstage = 2;
+    if (p.nstage > dq::MAX_STAGES)
+        p.nstage = dq::MAX_STAGES;
+    p.smem_bytes = p.nstage * p.stage_bytes + dq::gemv_extra_smem(p.RPT, nmat);
+    const int sms = sm_count();
+    p.grid = rows < sms ? rows : sms;
+    p.kernel = kernel_for(fmt, p.UL, p.RPT, nmat);
+    if (!p.kernel)
+        return DQ_ERR_UNSUPPORTED;
+    cudaError_t e = ensure_smem_attr(p.kernel, p.smem_bytes);
+    if (e != cudaSuccess)
+        return set_cuda_error(e);
+    *plan = p;
+    return DQ_OK;
+}
+
+cudaError_t launch_gemv(const GemvPlan& plan, dq::GemvArgs a, cudaStream_t stream, bool pdl)
+{
+    a.rows = plan.rows;
+    a.K = plan.K;
+    a.row_bytes = plan.row_bytes;
+    a.P = plan.P;
+    a.RG = plan.RG;
+    a.nstage = plan.nstage;
+    a.stage_bytes = plan.stage_bytes;
+    if (!a.err)
+        a.err = device_error_flag();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(dq::GEMV_THREADS);
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, plan.kernel, a);
+}
+
+}  // namespace dqhost
+
+// ------------------------------------------------------------ dequantisers
+
+namespace dq {
+
+__device__ __forceinline__ uint32_t ldb(const uint8_t* p) { return *p; }
+
+// One thread per 32 weights of Q4_K: w = d * sc_j * q - dmin * m_j in fp32.
+__global__ void dequant_q4k_kernel(const uint8_t* __restrict__ blocks, float* __restrict__ out, long long nunits)
+{
+    const long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (u >= nunits)
+        return;
+    const uint8_t* b = blocks + (u >> 3) * Q4K_BYTES;
+    const int j = static_cast<int>(u & 7);
+    const float d = half_bits_to_float(ldb(b) | ldb(b + 1) << 8);
+    const float dmin = half_bits_to_float(ldb(b + 2) | ldb(b + 3) << 8);
+    int sc = 0, mn = 0;
+    for (int k = 0; k < 6; ++k) {
+        const int bs = 6 * j + k, bm = 48 + 6 * j + k;
+        sc |= ((ldb(b + 4 + (bs >> 3)) >> (bs & 7)) & 1) << k;
+        mn |= ((ldb(b + 4 + (bm >> 3)) >> (bm & 7)) & 1) << k;
+    }
+    const float ds = d * static_cast<float>(sc), dm = dmin * static_cast<float>(mn);
+    float* o = out + u * 32;
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t c = ldb(b + 16 + 16 * j + i);
+        o[i] = ds * static_cast<float>(c & 15u) - dm;
+        o[16 + i] = ds * static_cast<float>(c >> 4) - dm;
+    }
+}
+
+// One thread per 32 weights of Q6_K: w = d * sc[n/16] * (q - 32) in fp32.
+__global__ void dequant_q6k_kernel(const uint8_t* __restrict__ blocks, float* __restrict__ out, long long nunits)
+{
+    const long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (u >= nunits)
+        return;
+    const uint8_t* b = blocks + (u >> 3) * Q6K_BYTES;
+    const int g = static_cast<int>(u & 7);
+    const float d = half_bits_to_float(ldb(b + 208) | ldb(b + 209) << 8);
+    const float sa = d * static_cast<float>(static_cast<int8_t>(b[192 + 2 * g]));
+    const float sb = d * static_cast<float>(static_cast<int8_t>(b[192 + 2 * g + 1]));
+    float* o = out + u * 32;
+    for (int h = 0; h < 2; ++h)
+        for (int t = 0; t < 4; ++t)
+            for (int e = 0; e < 4; ++e) {
+                const int r = 16 * h + 4 * t + e;
+                const uint32_t lo = (ldb(b + 16 * g + 4 * t + e) >> (4 * h)) & 15u;
+                const uint32_t hi = (ldb(b + 128 + 8 * g + 4 * h + e) >> (2 * t)) & 3u;
+                const int q = static_cast<int>(lo | hi << 4);
+                o[r] = (h ? sb : sa) * static_cast<float>(q - 32);
+            }
+}
+
+}  // namespace dq
+
+// ------------------------------------------------------------------- C ABI
+
+static int gemv_entry(int fmt, const void* W, const void* x, float* y, int rows, int K, void* stream)
+{
+    if (!W || !x || !y)
+        return DQ_ERR_NULL;
+    if (!dqhost::aligned16(W) || !dqhost::aligned16(x))
+        return DQ_ERR_ALIGN;
+    dqhost::GemvPlan plan;
+    int st = dqhost::plan_gemv(fmt, rows, K, 1, dqhost::GEMV_RING_DEFAULT, &plan);
+    if (st != DQ_OK)
+        return st;
+    dq::GemvArgs a{};
+    a.W = static_cast<const uint8_t*>(W);
+    a.pro = fmt == DQ_FMT_BF16 ? dq::PRO_BF16 : dq::PRO_F32;
+    a.epi = dq::EPI_STORE;
+    if (fmt == DQ_FMT_BF16)
+        a.xb = static_cast<const uint16_t*>(x);
+    else
+        a.x = static_cast<const float*>(x);
+    a.y = y;
+    cudaError_t e = dqhost::launch_gemv(plan, a, static_cast<cudaStream_t>(stream), false);
+    return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
+}
+
+extern "C" {
+
+DQ_API int dq_gemv_bf16(const void* W_bf16, const void* x_bf16, float* y, int rows, int K, void* stream)
+{
+    if (K > 24576)
+        return DQ_ERR_UNSUPPORTED;
+    return gemv_entry(DQ_FMT_BF16, W_bf16, x_bf16, y, rows, K, stream);
+}
+
+DQ_API int dq_gemv_q4k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream)
+{
+    if (K > 32768)
+        return DQ_ERR_UNSUPPORTED;
+    return gemv_entry(DQ_FMT_Q4K, W_blocks, x, y, rows, K, stream);
+}
+
+DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream)
+{
+    if (K > 32768)
+        return DQ_ERR_UNSUPPORTED;
+    return gemv_entry(DQ_FMT_Q6K, W_blocks, x, y, rows, K, stream);
+}
+
+static int dequant_entry(bool q6, const void* blocks, float* out, long long nblocks, void* stream)
+{
+    if (!blocks || !out)
+        return DQ_ERR_NULL;
+    if (nblocks < 1)
+        return DQ_ERR_SHAPE;
+    const long long nunits = nblocks * 8;
+    const int threads = 256;
+    const long long grid = (nunits + threads - 1) / threads;
+    if (grid > 0x7fffffffLL)
+        return DQ_ERR_SHAPE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (q6)
+        dq::dequant_q6k_kernel<<<static_cast<unsigned>(grid), threads, 0, s>>>(static_cast<const uint8_t*>(blocks), out,
+                                                                              nunits);
+    else
+        dq::dequant_q4k_kernel<<<static_cast<unsigned>(grid), threads, 0, s>>>(static_cast<const uint8_t*>(blocks), out,
+                                                                              nunits);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
+}
+
+DQ_API int dq_dequant_q4k(const void* blocks, float* out, long long nblocks, void* stream)
+{
+    return dequant_entry(false, blocks, out, nblocks, stream);
+}
+
+DQ_API int dq_dequant_q6k(const void* blocks, float* out, long long nblocks, void* stream)
+{
+    return dequant_entry(true, blocks, out, nblocks, stream);
+}
+
+}  // extern "C"

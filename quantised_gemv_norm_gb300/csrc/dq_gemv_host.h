@@ -1,0 +1,40 @@
+// dq_gemv_host.h -- host-side planning and launching of the streaming GEMV kernel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "dq_gemv.cuh"
+
+namespace dqhost {
+
+using GemvKernel = void (*)(dq::GemvArgs);
+
+// Kernel tables, one translation unit per format (null when not instantiated).
+GemvKernel gemv_kernel_q4k(int ul, int rpt, int nmat);
+GemvKernel gemv_kernel_q6k(int ul, int rpt, int nmat);
+GemvKernel gemv_kernel_bf16(int ul, int rpt, int nmat);
+
+struct GemvPlan {
+    int fmt, rows, K, nmat;
+    int row_bytes;
+    int P, RG, UL, RPT;
+    int nstage, stage_bytes;
+    int smem_bytes;
+    int grid;
+    GemvKernel kernel;
+};
+
+constexpr int GEMV_STAGE_TARGET = 32 * 1024;   // bytes per ring stage (target)
+constexpr int GEMV_STAGE_MAX = 64 * 1024;      // largest stage accepted
+constexpr int GEMV_RING_DEFAULT = 96 * 1024;   // ring bytes: two blocks of two kernels fit one SM
+
+// Chooses the thread layout, tile and ring for one matrix shape.  Returns
+// DQ_OK, DQ_ERR_SHAPE or DQ_ERR_UNSUPPORTED.  Sets the kernel's shared-memory
+// attribute (host call, not a stream operation).
+int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, GemvPlan* plan);
+
+// Fills the layout fields of `a` from the plan and launches on `stream`;
+// `pdl` adds the programmatic-stream-serialisation launch attribute.
+cudaError_t launch_gemv(const GemvPlan& plan, dq::GemvArgs a, cudaStream_t stream, bool pdl);
+
+}  // namespace dqhost

@@ -1,0 +1,79 @@
+"""The C-ABI library: builds, loads and exports every symbol include/dq.h declares;
+argument checks that return before any CUDA call.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dq.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"DQ_API\s+[\w\s\*]+?\b(dq_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantised_gemv_norm_gb300 import build
+
+    build.build()
+    from quantised_gemv_norm_gb300 import dq
+
+    return dq.load()
+
+
+def test_header_declares_the_hot_path():
+    names = declared_symbols()
+    for required in ("dq_rmsnorm", "dq_layernorm", "dq_gemv_bf16", "dq_gemv_q4k", "dq_gemv_q6k",
+                     "dq_dequant_q4k", "dq_dequant_q6k", "dq_attention_decode", "dq_matmul_q4k",
+                     "dq_model_create", "dq_decode_step", "dq_model_destroy"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_declared_symbol():
+    from quantised_gemv_norm_gb300 import dq
+
+    assert sorted(dq.SIGNATURES) == declared_symbols()
+
+
+def test_status_strings(lib):
+    for code in range(0, -8, -1):
+        s = lib.dq_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.dq_status_string(-99) == b"unknown status"
+
+
+def test_argument_errors_return_before_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(16)  # never dereferenced: checks fail first
+    assert lib.dq_gemv_q4k(None, fake, fake, 4, 256, None) == -1
+    assert lib.dq_gemv_q4k(P(17), fake, fake, 4, 256, None) == -3          # misaligned W
+    assert lib.dq_gemv_q4k(fake, fake, fake, 4, 40000, None) == -4        # K too large
+    assert lib.dq_gemv_q6k(fake, fake, fake, 4, 40000, None) == -4
+    assert lib.dq_gemv_bf16(fake, fake, fake, 4, 30000, None) == -4
+    assert lib.dq_rmsnorm(None, fake, fake, 1, 8, 1e-6, None) == -1
+    assert lib.dq_rmsnorm(fake, fake, fake, 0, 8, 1e-6, None) == -2
+    assert lib.dq_rmsnorm_threads(fake, fake, fake, 1, 8, 1e-6, 3, None) == -2  # not a power of two
+    assert lib.dq_layernorm(fake, fake, None, fake, 1, 8, 1e-6, None) == -1
+    assert lib.dq_dequant_q4k(fake, fake, 0, None) == -2
+    assert lib.dq_attention_decode(fake, fake, fake, fake, 32, 8, 64, 16, 1, fake, 1 << 20, None) == -4
+    assert lib.dq_attention_decode(fake, fake, fake, fake, 32, 8, 128, 16, 17, fake, 1 << 20, None) == -2
+    assert lib.dq_attention_decode(fake, fake, fake, fake, 32, 8, 128, 16, 4, fake, 8, None) == -2
+    assert lib.dq_matmul_q4k(fake, fake, fake, 65, 4, 256, None) == -2
+    assert lib.dq_decode_step(None, fake, 0, fake, None) == -1
+    h = P()
+    assert lib.dq_model_create(None, ctypes.byref(h)) == -1
+    assert lib.dq_model_destroy(None) == 0
+
+
+def test_attention_workspace_size(lib):
+    assert lib.dq_attention_workspace_bytes(32, 8) == 256 + 32 * 16 * 132 * 4
+    assert lib.dq_attention_workspace_bytes(0, 8) == 0

@@ -1,0 +1,251 @@
+"""GPU parity: every C-ABI entry point against the CPU oracle on the same seeded
+inputs, at sizes that span several tiles with ragged tails and at the full
+configuration sizes.  Tolerances:
+  norms      |y - r| <= 1e-5 * max(1, |r|) elementwise
+  GEMV       max|y - r| / max|r| <= 2e-3 (bf16 in / fp32 accumulate bar)
+  dequant    bit-exact
+  attention  max|o - r| / max|r| <= 1e-4 (fp16 data, fp32 arithmetic)
+  decode     logits max|y - r| / max|r| <= 2e-3
+"""
+import numpy as np
+import pytest
+import torch
+
+from quantised_gemv_norm_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+GEMV_TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def dq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantised_gemv_norm_gb300 import build, dq as dqmod
+
+    build.build()
+    dqmod.load()
+    yield dqmod
+    assert dqmod.device_error() == 0
+
+
+def cuda(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def normwise(y, r):
+    y = np.asarray(y, np.float64)
+    r = np.asarray(r, np.float64)
+    return float(np.max(np.abs(y - r)) / max(np.max(np.abs(r)), 1e-300))
+
+
+# ---------------------------------------------------------------- norms
+
+
+@pytest.mark.parametrize("rows,n", [(64, 2048), (3, 1000), (5, 4097), (2, 1), (1, 12288)])
+def test_rmsnorm(dq, orc, rows, n):
+    x, g, _ = synth.norm_inputs(0, rows, n)
+    y = dq.rmsnorm(cuda(x), cuda(g), 1e-6).cpu().numpy()
+    r = orc.rmsnorm(x, g, 1e-6)
+    assert np.all(np.abs(y - r) <= 1e-5 * np.maximum(1.0, np.abs(r)))
+
+
+@pytest.mark.parametrize("rows,n", [(64, 2048), (3, 1000), (5, 4097), (1, 12288)])
+def test_layernorm(dq, orc, rows, n):
+    x, g, b = synth.norm_inputs(1, rows, n)
+    y = dq.layernorm(cuda(x), cuda(g), cuda(b), 1e-6).cpu().numpy()
+    r = orc.layernorm(x, g, b, 1e-6)
+    assert np.all(np.abs(y - r) <= 1e-5 * np.maximum(1.0, np.abs(r)))
+
+
+@pytest.mark.parametrize("threads", [1, 2, 8, 32, 64, 256, 1024])
+def test_norm_thread_sweep(dq, orc, threads):
+    x, g, b = synth.norm_inputs(2, 4, 2048)
+    y = dq.rmsnorm(cuda(x), cuda(g), 1e-6, threads=threads).cpu().numpy()
+    r = orc.rmsnorm(x, g, 1e-6)
+    assert np.all(np.abs(y - r) <= 1e-5 * np.maximum(1.0, np.abs(r)))
+    y = dq.layernorm(cuda(x), cuda(g), cuda(b), 1e-6, threads=threads).cpu().numpy()
+    r = orc.layernorm(x, g, b, 1e-6)
+    assert np.all(np.abs(y - r) <= 1e-5 * np.maximum(1.0, np.abs(r)))
+
+
+def test_rmsnorm_in_place(dq, orc):
+    x, g, _ = synth.norm_inputs(3, 8, 2048)
+    t = cuda(x)
+    dq.rmsnorm(t, cuda(g), 1e-6, out=t)
+    r = orc.rmsnorm(x, g, 1e-6)
+    assert np.all(np.abs(t.cpu().numpy() - r) <= 1e-5 * np.maximum(1.0, np.abs(r)))
+
+
+# ------------------------------------------------------------ dequant
+
+
+def test_dequant_bit_exact(dq, orc):
+    rng = np.random.default_rng(11)
+    b4 = synth.q4k_blocks(rng, 3001)
+    b6 = synth.q6k_blocks(rng, 3001)
+    y4 = dq.dequant_q4k(cuda(b4)).cpu().numpy()
+    y6 = dq.dequant_q6k(cuda(b6)).cpu().numpy()
+    r4 = orc.dequant_q4k(b4).astype(np.float32)
+    r6 = orc.dequant_q6k(b6).astype(np.float32)
+    assert np.array_equal(y4.view(np.uint32), r4.view(np.uint32))
+    assert np.array_equal(y6.view(np.uint32), r6.view(np.uint32))
+
+
+def test_dequant_hand_built(dq, orc):
+    blk = orc.pack_q6k(0x0400, [-128] * 16, [63] * 256)
+    assert np.all(dq.dequant_q6k(cuda(blk)).cpu().numpy() == -0.2421875)
+    blk = orc.pack_q4k(0x3C00, 0x3800, [5] * 8, [63] * 8, [0] * 256)
+    assert np.all(dq.dequant_q4k(cuda(blk)).cpu().numpy() == -31.5)
+
+
+# --------------------------------------------------------------- GEMV
+
+
+BF16_SHAPES = [(512, 4096), (1003, 4096), (7, 8), (33, 1024), (1024, 4096), (4096, 4096), (12288, 4096),
+               (4096, 12288), (151936, 4096)]
+
+
+@pytest.mark.parametrize("rows,K", BF16_SHAPES)
+def test_gemv_bf16(dq, orc, rows, K):
+    W, x = synth.bf16_gemv_inputs(4, rows, K)
+    y = dq.gemv_bf16(cuda(W.view(np.int16)), cuda(x.view(np.int16))).cpu().numpy()
+    r = orc.gemv_bf16(W, x)
+    assert normwise(y, r) <= GEMV_TOL
+
+
+Q4K_SHAPES = [(300, 4096), (1, 4096), (37, 256), (129, 768), (257, 2048), (64, 12288), (8, 32768),
+              (12288, 4096), (4096, 4096), (6144, 4096), (4096, 12288)]
+
+
+@pytest.mark.parametrize("rows,K", Q4K_SHAPES)
+def test_gemv_q4k(dq, orc, rows, K):
+    W = synth.quant_matrix(5, synth.FMT_Q4K, rows, K)
+    x = synth.activation(5, K)
+    y = dq.gemv_q4k(cuda(W), cuda(x)).cpu().numpy()
+    r = orc.gemv_q4k(W, x, rows, K)
+    assert normwise(y, r) <= GEMV_TOL
+
+
+Q6K_SHAPES = [(300, 4096), (1, 2048), (77, 6144), (4096, 12288), (151936, 4096), (5, 32768)]
+
+
+@pytest.mark.parametrize("rows,K", Q6K_SHAPES)
+def test_gemv_q6k(dq, orc, rows, K):
+    W = synth.quant_matrix(6, synth.FMT_Q6K, rows, K)
+    x = synth.activation(6, K)
+    y = dq.gemv_q6k(cuda(W), cuda(x)).cpu().numpy()
+    r = orc.gemv_q6k(W, x, rows, K)
+    assert normwise(y, r) <= GEMV_TOL
+
+
+def test_gemv_quant_condition_aware(dq, orc):
+    # error against sum_k |W_rk x_k|, per row (well inside the bar for 15-bit activations)
+    rows, K = 513, 4096
+    for fmt, fn, deq in ((synth.FMT_Q4K, dq.gemv_q4k, orc.dequant_q4k), (synth.FMT_Q6K, dq.gemv_q6k, orc.dequant_q6k)):
+        W = synth.quant_matrix(7, fmt, rows, K)
+        x = synth.activation(7, K)
+        y = fn(cuda(W), cuda(x)).cpu().numpy().astype(np.float64)
+        Wd = deq(W).reshape(rows, K)
+        r = Wd @ x.astype(np.float64)
+        cond = np.abs(Wd) @ np.abs(x.astype(np.float64))
+        assert np.max(np.abs(y - r) / cond) <= 1e-4
+
+
+def test_gemv_extreme_activation(dq, orc):
+    # a group whose values span 12 orders of magnitude, a zero group and an outlier
+    rows, K = 40, 4096
+    W = synth.quant_matrix(8, synth.FMT_Q4K, rows, K)
+    x = synth.activation(8, K)
+    x[:32] = 0.0
+    x[32:64] *= 1e-6
+    x[100] = 1e4
+    y = dq.gemv_q4k(cuda(W), cuda(x)).cpu().numpy()
+    assert normwise(y, orc.gemv_q4k(W, x, rows, K)) <= GEMV_TOL
+
+
+# ---------------------------------------------------------- attention
+
+
+def _attn_inputs(seed, n_q, n_kv, max_ctx, n_keys):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((n_q, 128)).astype(np.float32)
+    k = rng.standard_normal((n_kv, max_ctx, 128)).astype(np.float16)
+    v = rng.standard_normal((n_kv, max_ctx, 128)).astype(np.float16)
+    return q, k, v
+
+
+@pytest.mark.parametrize("n_q,n_kv,n_keys", [(32, 8, 1), (32, 8, 7), (32, 8, 32), (32, 8, 33), (32, 8, 513),
+                                             (32, 8, 1024), (16, 2, 100), (8, 8, 17)])
+def test_attention(dq, orc, n_q, n_kv, n_keys):
+    q, k, v = _attn_inputs(n_keys, n_q, n_kv, 1024, n_keys)
+    ws = dq.attention_workspace(n_q, n_kv)
+    qt, kt, vt = cuda(q), cuda(k), cuda(v)
+    for _ in range(2):  # the workspace must come back zeroed and reusable
+        o = dq.attention_decode(qt, kt, vt, n_keys, workspace=ws).cpu().numpy()
+        r = orc.attention(q.astype(np.float64), k.view(np.uint16), v.view(np.uint16), n_keys)
+        assert normwise(o, r) <= 1e-4
+
+
+# ------------------------------------------------------------- M-sweep
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 64])
+def test_matmul_q4k(dq, orc, M):
+    rows, K = 12288, 4096
+    W = synth.quant_matrix(9, synth.FMT_Q4K, rows, K)
+    X = np.stack([synth.activation(9, K, m) for m in range(M)])
+    Y = dq.matmul_q4k(cuda(W), cuda(X)).cpu().numpy()
+    R = orc.matmul_q4k(W, X, rows, K)
+    for m in range(M):
+        assert normwise(Y[m], R[m]) <= GEMV_TOL
+
+
+# -------------------------------------------------------------- decode
+
+
+def _run_decode(dq, orc, m, kv, positions, use_graph=True, seed=0):
+    from quantised_gemv_norm_gb300 import upload
+
+    w = upload.to_device(m, kv)
+    model = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=use_graph)
+    kv_host = kv.copy()
+    for t, pos in enumerate(positions):
+        x = synth.decode_input(seed, m.hidden, t)
+        logits = model.step(cuda(x), pos).cpu().numpy()
+        ref = orc.decode_step(m, x, pos, kv_host)
+        err = normwise(logits, ref)
+        assert err <= GEMV_TOL, (pos, err)
+        # the cache rows this token appended: fp16 values of k and v
+        got = w["kv_cache"].cpu().numpy().view(np.float16)[:, :, :, pos, :].astype(np.float64)
+        want = kv_host.view(np.float16)[:, :, :, pos, :].astype(np.float64)
+        assert normwise(got, want) <= GEMV_TOL
+    model.close()
+    assert dq.device_error() == 0
+
+
+def test_decode_small_model_steps(dq, orc):
+    m = synth.make_model(21, n_layers=2, hidden=2048, ffn=4096, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                         vocab=1000, max_ctx=64)
+    kv = synth.make_kv_cache(21, m, 0)
+    _run_decode(dq, orc, m, kv, [0, 1, 2, 3])
+
+
+def test_decode_small_model_eager_equals_graph(dq, orc):
+    m = synth.make_model(22, n_layers=2, hidden=2048, ffn=4096, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                         vocab=777, max_ctx=40)
+    kv = synth.make_kv_cache(22, m, 30)
+    _run_decode(dq, orc, m, kv, [30, 31], use_graph=False)
+
+
+def test_decode_qwen3_8b_shape_empty_cache(dq, orc):
+    m = synth.make_model(1, max_ctx=1024, **synth.QWEN3_8B)
+    kv = synth.make_kv_cache(1, m, 0)
+    _run_decode(dq, orc, m, kv, [0])
+
+
+def test_decode_qwen3_8b_shape_512_context(dq, orc):
+    m = synth.make_model(1, max_ctx=1024, **synth.QWEN3_8B)
+    kv = synth.make_kv_cache(2, m, 512)
+    _run_decode(dq, orc, m, kv, [512])
