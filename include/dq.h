@@ -242,6 +242,13 @@ DQ_API int dq_model_launches_per_step(const dq_model* m);
  * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE (layer or kind out of range), DQ_ERR_CUDA. */
 DQ_API int dq_model_enqueue_kernel(dq_model* m, int layer, int kind, void* stream);
 
+/* Diagnostics: device pointer of one of the model's activation buffers, for
+ * checking a kernel's output in isolation.  which: 0 the fp32 residual x
+ * [hidden], 1 q [n_q head_dim], 2 the attention output [n_q head_dim], 3 the
+ * SwiGLU activation [ffn].  The buffers are owned by the model.
+ * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE. */
+DQ_API int dq_model_buffer(const dq_model* m, int which, void** ptr);
+
 /* Frees the workspace and graph (synchronises the device).  NULL is a no-op. */
 DQ_API int dq_model_destroy(dq_model* m);
 

@@ -323,6 +323,19 @@ DQ_API int dq_model_enqueue_kernel(dq_model* m, int layer, int kind, void* strea
     return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
 }
 
+DQ_API int dq_model_buffer(const dq_model* m, int which, void** ptr)
+{
+    if (!m || !ptr)
+        return DQ_ERR_NULL;
+    switch (which) {
+    case 0: *ptr = m->x; return DQ_OK;
+    case 1: *ptr = m->q; return DQ_OK;
+    case 2: *ptr = m->attn; return DQ_OK;
+    case 3: *ptr = m->act; return DQ_OK;
+    default: return DQ_ERR_SHAPE;
+    }
+}
+
 DQ_API int dq_model_destroy(dq_model* m)
 {
     if (!m)

@@ -41,6 +41,7 @@ SIGNATURES = {
     "dq_decode_step": (I, [P, P, I, P, P]),
     "dq_model_launches_per_step": (I, [P]),
     "dq_model_enqueue_kernel": (I, [P, I, I, P]),
+    "dq_model_buffer": (I, [P, I, P]),
     "dq_model_destroy": (I, [P]),
 }
 
@@ -219,6 +220,14 @@ def attention_decode(q: torch.Tensor, k_plane: torch.Tensor, v_plane: torch.Tens
 # --------------------------------------------------------------- model
 
 
+def _wrap_device_f32(ptr: int, numel: int) -> torch.Tensor:
+    """A torch tensor over existing device memory (no copy, no ownership)."""
+    class _CAI:
+        __cuda_array_interface__ = {"shape": (numel,), "typestr": "<f4", "data": (ptr, False), "version": 3,
+                                    "strides": None}
+    return torch.as_tensor(_CAI(), device="cuda")
+
+
 class _Desc(ctypes.Structure):
     _fields_ = [
         ("n_layers", I), ("hidden", I), ("ffn", I), ("n_q_heads", I), ("n_kv_heads", I), ("head_dim", I),
@@ -279,6 +288,12 @@ class Model:
         """Launch one of the token's kernels alone (diagnostics / per-kernel timing)."""
         s = ctypes.c_void_p(stream_handle) if stream_handle is not None else _stream()
         _check("dq_model_enqueue_kernel", _lib.dq_model_enqueue_kernel(self._h, int(layer), int(kind), s))
+
+    def buffer(self, which: int, numel: int) -> torch.Tensor:
+        """A torch view (fp32) of one model activation buffer: 0 x, 1 q, 2 attn, 3 act."""
+        p = ctypes.c_void_p()
+        _check("dq_model_buffer", _lib.dq_model_buffer(self._h, int(which), ctypes.byref(p)))
+        return _wrap_device_f32(p.value, numel)
 
     def close(self):
         if getattr(self, "_h", None):
