@@ -70,13 +70,18 @@ struct GemvArgs {
 
 // ---------------------------------------------------------- activation units
 
-// One 32-element slice of the activation as 15-bit fixed point.
+// One 32-element slice of the activation as fixed point: x ~= s * xi with 15-bit
+// integers xi (PL = 1), or x ~= s * (xi + xl / 2^15) with a second 16-bit plane of
+// the remainder (PL = 2, about 30 bits, fp32-level) for the inputs whose errors
+// the attention amplifies.
+template <int PL>
 struct XQ {
-    uint32_t q[16];  // q[p] = xi[2p] (low 16 bits) | xi[2p+1] << 16, |xi| <= 16383
-    float s;         // x ~= s * xi
-    float f;         // Q4_K: s / 16;          Q6_K: unused
-    float hsum;      // Q4_K: sum of the 32 fp32 values
-    int s32a, s32b;  // Q6_K: 32 * sum xi[0..15], 32 * sum xi[16..31]
+    uint32_t q[16];               // q[p] = xi[2p] (low 16 bits) | xi[2p+1] << 16, |xi| <= 16383
+    uint32_t l[PL == 2 ? 16 : 1]; // PL = 2: the remainder plane, same packing, |xl| <= 16384
+    float s;                      // group scale
+    float f;                      // Q4_K: s / 16
+    float hsum;                   // Q4_K: sum of the 32 fp32 values
+    int s32a, s32b;               // Q6_K: 32 * sum xi[0..15], 32 * sum xi[16..31]
 };
 
 constexpr float XQ_MAX = 16383.0f;
@@ -95,7 +100,13 @@ __device__ __forceinline__ int unit_k0(int n)
     return 32 * n;
 }
 
-__device__ __forceinline__ void quantise_unit(const float (&h)[32], XQ& u)
+__device__ __forceinline__ uint32_t pack16x2(int a, int b)
+{
+    return (static_cast<uint32_t>(a) & 0xffffu) | (static_cast<uint32_t>(b) << 16);
+}
+
+template <int PL>
+__device__ __forceinline__ void quantise_unit(const float (&h)[32], XQ<PL>& u)
 {
     float amax = 0.f, hs = 0.f;
 #pragma unroll
@@ -110,9 +121,12 @@ __device__ __forceinline__ void quantise_unit(const float (&h)[32], XQ& u)
     int sa = 0, sb = 0;
 #pragma unroll
     for (int p = 0; p < 16; ++p) {
-        const int a = __float2int_rn(h[2 * p] * inv);
-        const int b = __float2int_rn(h[2 * p + 1] * inv);
-        u.q[p] = (static_cast<uint32_t>(a) & 0xffffu) | (static_cast<uint32_t>(b) << 16);
+        const float ta = h[2 * p] * inv, tb = h[2 * p + 1] * inv;
+        const int a = __float2int_rn(ta), b = __float2int_rn(tb);
+        u.q[p] = pack16x2(a, b);
+        if (PL == 2)  // ta - a is exact in fp32 (|ta - a| <= 1/2)
+            u.l[p] = pack16x2(__float2int_rn((ta - static_cast<float>(a)) * 32768.0f),
+                              __float2int_rn((tb - static_cast<float>(b)) * 32768.0f));
         if (p < 8)
             sa += a + b;
         else
@@ -125,14 +139,15 @@ __device__ __forceinline__ void quantise_unit(const float (&h)[32], XQ& u)
 // ------------------------------------------------------------- unit products
 
 // Q4_K unit n of a row: 32 weights of sub-block j = n & 7 of block n >> 3.
-__device__ __forceinline__ float q4k_unit(const uint8_t* rp, int n, const XQ& u)
+template <int PL>
+__device__ __forceinline__ float q4k_unit(const uint8_t* rp, int n, const XQ<PL>& u)
 {
     const int j = n & 7;
     const uint8_t* bp = rp + Q4K_BYTES * (n >> 3);
     const uint4 hd = lds128(bp);
     const uint4 c = lds128(bp + 16 + 16 * j);
     const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-    int lo = 0, hi = 0;
+    int lo = 0, hi = 0, lo2 = 0, hi2 = 0;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         const uint32_t l = cw[t] & 0x0F0F0F0Fu;  // codes of weights 4t .. 4t+3
@@ -141,21 +156,28 @@ __device__ __forceinline__ float q4k_unit(const uint8_t* rp, int n, const XQ& u)
         lo = dp2a_hi(u.q[2 * t + 1], l, lo);
         hi = dp2a_lo(u.q[8 + 2 * t], h, hi);
         hi = dp2a_hi(u.q[8 + 2 * t + 1], h, hi);
+        if (PL == 2) {
+            lo2 = dp2a_lo(u.l[2 * t], l, lo2);
+            lo2 = dp2a_hi(u.l[2 * t + 1], l, lo2);
+            hi2 = dp2a_lo(u.l[8 + 2 * t], h, hi2);
+            hi2 = dp2a_hi(u.l[8 + 2 * t + 1], h, hi2);
+        }
     }
-    const int dot16 = lo * 16 + hi;  // 16 * sum q * xi
+    float dot16 = static_cast<float>(lo * 16 + hi);  // 16 * sum q * xi
+    if (PL == 2)
+        dot16 += static_cast<float>(lo2 * 16 + hi2) * (1.0f / 32768.0f);
     // scale j: bits 6j.. of the 96-bit string (hd.y, hd.z, hd.w); min j: bits 48+6j..
     const uint32_t s_lo = j < 6 ? hd.y : hd.z, s_hi = j < 6 ? hd.z : hd.w;
     const uint32_t m_lo = j < 3 ? hd.z : hd.w, m_hi = j < 3 ? hd.w : 0u;
     const int sc = static_cast<int>(__funnelshift_r(s_lo, s_hi, (6 * j) & 31) & 63u);
     const int mn = static_cast<int>(__funnelshift_r(m_lo, m_hi, (48 + 6 * j) & 31) & 63u);
     const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
-    return (d * static_cast<float>(sc)) * (u.f * static_cast<float>(dot16)) -
-           (dmin * static_cast<float>(mn)) * u.hsum;
+    return (d * static_cast<float>(sc)) * (u.f * dot16) - (dmin * static_cast<float>(mn)) * u.hsum;
 }
 
 // Q6_K unit: 32 weights of group g of (permuted) block Bp; fields start at
 // even byte offsets, so they are read as aligned words and re-aligned.
-__device__ __forceinline__ float q6k_unit(const uint8_t* rp, int n, const XQ& u)
+__device__ __forceinline__ float q6k_unit(const uint8_t* rp, int n, const XQ<1>& u)
 {
     const int B = n >> 3, i = B & 7;
     const int Bp = (B & ~7) + (i < 4 ? 2 * i : 2 * (i - 4) + 1);
@@ -236,23 +258,20 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[NV], int lane)
 
 // ------------------------------------------------------------------ kernel
 
-template <int FMT>
-struct UnitState;
-template <>
-struct UnitState<FMT_Q4K> {
-    XQ x;
+template <int FMT, int PL>
+struct UnitState {
+    XQ<PL> x;
 };
-template <>
-struct UnitState<FMT_Q6K> {
-    XQ x;
-};
-template <>
-struct UnitState<FMT_BF16> {
+template <int PL>
+struct UnitState<FMT_BF16, PL> {
     uint32_t xb[4];
 };
 
-template <int FMT, int UL, int RPT, int NMAT>
-__global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? 80 : (UL == 2 ? 128 : 144)) gemv_stream_kernel(const __grid_constant__ GemvArgs a)
+// Register caps keep two blocks of neighbouring kernels of the decode chain on
+// one SM (288 threads x (cap_a + cap_b) <= 64K registers).
+template <int FMT, int UL, int RPT, int NMAT, int PL>
+__global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? (PL == 2 ? 96 : 80) : (UL <= 3 ? 128 : (UL == 4 ? 144 : 168)))
+    gemv_stream_kernel(const __grid_constant__ GemvArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int ring_bytes = a.nstage * a.stage_bytes;
@@ -316,7 +335,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? 80 : (U
     const int p = tid - g * a.P;
     const int U = (FMT == FMT_BF16) ? a.K / 8 : a.K / 32;
 
-    UnitState<FMT> us[UL];
+    UnitState<FMT, PL> us[UL];
     bool have[UL];
 #pragma unroll
     for (int k = 0; k < UL; ++k)
@@ -382,7 +401,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? 80 : (U
                 for (int e = 0; e < 32; ++e)
                     h[e] = 0.f;
             }
-            quantise_unit(h, reinterpret_cast<XQ&>(us[k]));
+            quantise_unit<PL>(h, reinterpret_cast<XQ<PL>&>(us[k]));
         }
     }
 
@@ -413,9 +432,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? 80 : (U
                         if (have[k]) {
                             const int n = p + a.P * k;
                             if (FMT == FMT_Q4K)
-                                sum += q4k_unit(rp, n, reinterpret_cast<const XQ&>(us[k]));
+                                sum += q4k_unit<PL>(rp, n, reinterpret_cast<const XQ<PL>&>(us[k]));
                             else if (FMT == FMT_Q6K)
-                                sum += q6k_unit(rp, n, reinterpret_cast<const XQ&>(us[k]));
+                                sum += q6k_unit(rp, n, reinterpret_cast<const XQ<1>&>(us[k]));
                             else
                                 sum += bf16_unit(rp, n, reinterpret_cast<const uint32_t(&)[4]>(us[k]));
                         }

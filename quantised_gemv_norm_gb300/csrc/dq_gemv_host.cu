@@ -13,13 +13,13 @@ static int row_bytes_of(int fmt, int K)
     return (K / 256) * (fmt == DQ_FMT_Q4K ? dq::Q4K_BYTES : dq::Q6K_BYTES);
 }
 
-static GemvKernel kernel_for(int fmt, int ul, int rpt, int nmat)
+static GemvKernel kernel_for(int fmt, int ul, int rpt, int nmat, int pl)
 {
     if (fmt == DQ_FMT_Q4K)
-        return gemv_kernel_q4k(ul, rpt, nmat);
+        return gemv_kernel_q4k(ul, rpt, nmat, pl);
     if (fmt == DQ_FMT_Q6K)
-        return gemv_kernel_q6k(ul, rpt, nmat);
-    return gemv_kernel_bf16(ul, rpt, nmat);
+        return gemv_kernel_q6k(ul, rpt, nmat, pl);
+    return gemv_kernel_bf16(ul, rpt, nmat, pl);
 }
 
 static cudaError_t ensure_smem_attr(GemvKernel k, int bytes)
@@ -47,7 +47,7 @@ static cudaError_t ensure_smem_attr(GemvKernel k, int bytes)
     return e;
 }
 
-int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, GemvPlan* plan)
+int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, int planes, GemvPlan* plan)
 {
     if (rows < 1 || K < 1)
         return DQ_ERR_SHAPE;
@@ -113,7 +113,8 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, GemvPlan* plan
     p.smem_bytes = p.nstage * p.stage_bytes + dq::gemv_extra_smem(p.RPT, nmat);
     const int sms = sm_count();
     p.grid = rows < sms ? rows : sms;
-    p.kernel = kernel_for(fmt, p.UL, p.RPT, nmat);
+    p.planes = (planes == 2 && fmt == DQ_FMT_Q4K && p.UL <= 2) ? 2 : 1;
+    p.kernel = kernel_for(fmt, p.UL, p.RPT, nmat, p.planes);
     if (!p.kernel)
         return DQ_ERR_UNSUPPORTED;
     cudaError_t e = ensure_smem_attr(p.kernel, p.smem_bytes);
@@ -214,7 +215,7 @@ static int gemv_entry(int fmt, const void* W, const void* x, float* y, int rows,
     if (!dqhost::aligned16(W) || !dqhost::aligned16(x))
         return DQ_ERR_ALIGN;
     dqhost::GemvPlan plan;
-    int st = dqhost::plan_gemv(fmt, rows, K, 1, dqhost::GEMV_RING_DEFAULT, &plan);
+    int st = dqhost::plan_gemv(fmt, rows, K, 1, dqhost::GEMV_RING_DEFAULT, 1, &plan);
     if (st != DQ_OK)
         return st;
     dq::GemvArgs a{};

@@ -10,14 +10,15 @@ namespace dqhost {
 using GemvKernel = void (*)(dq::GemvArgs);
 
 // Kernel tables, one translation unit per format (null when not instantiated).
-GemvKernel gemv_kernel_q4k(int ul, int rpt, int nmat);
-GemvKernel gemv_kernel_q6k(int ul, int rpt, int nmat);
-GemvKernel gemv_kernel_bf16(int ul, int rpt, int nmat);
+GemvKernel gemv_kernel_q4k(int ul, int rpt, int nmat, int pl);
+GemvKernel gemv_kernel_q6k(int ul, int rpt, int nmat, int pl);
+GemvKernel gemv_kernel_bf16(int ul, int rpt, int nmat, int pl);
 
 struct GemvPlan {
     int fmt, rows, K, nmat;
     int row_bytes;
     int P, RG, UL, RPT;
+    int planes;      // activation planes: 1 (15-bit) or 2 (about 30-bit, Q4_K with UL <= 2)
     int nstage, stage_bytes;
     int smem_bytes;
     int grid;
@@ -28,10 +29,11 @@ constexpr int GEMV_STAGE_TARGET = 32 * 1024;   // bytes per ring stage (target)
 constexpr int GEMV_STAGE_MAX = 64 * 1024;      // largest stage accepted
 constexpr int GEMV_RING_DEFAULT = 96 * 1024;   // ring bytes: two blocks of two kernels fit one SM
 
-// Chooses the thread layout, tile and ring for one matrix shape.  Returns
-// DQ_OK, DQ_ERR_SHAPE or DQ_ERR_UNSUPPORTED.  Sets the kernel's shared-memory
-// attribute (host call, not a stream operation).
-int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, GemvPlan* plan);
+// Chooses the thread layout, tile and ring for one matrix shape.  `planes` = 2
+// asks for the two-plane activation where the format and layout allow it (else
+// one plane).  Returns DQ_OK, DQ_ERR_SHAPE or DQ_ERR_UNSUPPORTED.  Sets the
+// kernel's shared-memory attribute (host call, not a stream operation).
+int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, int planes, GemvPlan* plan);
 
 // Fills the layout fields of `a` from the plan and launches on `stream`;
 // `pdl` adds the programmatic-stream-serialisation launch attribute.

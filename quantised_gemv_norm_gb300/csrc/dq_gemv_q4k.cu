@@ -3,35 +3,47 @@
 
 namespace dqhost {
 
-GemvKernel gemv_kernel_q4k(int ul, int rpt, int nmat)
+GemvKernel gemv_kernel_q4k(int ul, int rpt, int nmat, int pl)
 {
-#define DQ_K(UL, RPT, NM) \
-    if (ul == UL && rpt == RPT && nmat == NM) \
-        return &dq::gemv_stream_kernel<dq::FMT_Q4K, UL, RPT, NM>;
-    DQ_K(1, 1, 1)
-    DQ_K(1, 1, 2)
-    DQ_K(1, 2, 1)
-    DQ_K(1, 2, 2)
-    DQ_K(1, 4, 1)
-    DQ_K(1, 4, 2)
-    DQ_K(2, 1, 1)
-    DQ_K(2, 1, 2)
-    DQ_K(2, 2, 1)
-    DQ_K(2, 2, 2)
-    DQ_K(2, 4, 1)
-    DQ_K(2, 4, 2)
-    DQ_K(3, 1, 1)
-    DQ_K(3, 1, 2)
-    DQ_K(3, 2, 1)
-    DQ_K(3, 2, 2)
-    DQ_K(3, 4, 1)
-    DQ_K(3, 4, 2)
-    DQ_K(4, 1, 1)
-    DQ_K(4, 1, 2)
-    DQ_K(4, 2, 1)
-    DQ_K(4, 2, 2)
-    DQ_K(4, 4, 1)
-    DQ_K(4, 4, 2)
+#define DQ_K(UL, RPT, NM, PL) \
+    if (ul == UL && rpt == RPT && nmat == NM && pl == PL) \
+        return &dq::gemv_stream_kernel<dq::FMT_Q4K, UL, RPT, NM, PL>;
+    DQ_K(1, 1, 1, 1)
+    DQ_K(1, 1, 2, 1)
+    DQ_K(1, 1, 1, 2)
+    DQ_K(1, 1, 2, 2)
+    DQ_K(1, 2, 1, 1)
+    DQ_K(1, 2, 2, 1)
+    DQ_K(1, 2, 1, 2)
+    DQ_K(1, 2, 2, 2)
+    DQ_K(1, 4, 1, 1)
+    DQ_K(1, 4, 2, 1)
+    DQ_K(1, 4, 1, 2)
+    DQ_K(1, 4, 2, 2)
+    DQ_K(2, 1, 1, 1)
+    DQ_K(2, 1, 2, 1)
+    DQ_K(2, 1, 1, 2)
+    DQ_K(2, 1, 2, 2)
+    DQ_K(2, 2, 1, 1)
+    DQ_K(2, 2, 2, 1)
+    DQ_K(2, 2, 1, 2)
+    DQ_K(2, 2, 2, 2)
+    DQ_K(2, 4, 1, 1)
+    DQ_K(2, 4, 2, 1)
+    DQ_K(2, 4, 1, 2)
+    DQ_K(2, 4, 2, 2)
+    DQ_K(3, 1, 1, 1)
+    DQ_K(3, 1, 2, 1)
+    DQ_K(3, 2, 1, 1)
+    DQ_K(3, 2, 2, 1)
+    DQ_K(3, 4, 1, 1)
+    DQ_K(3, 4, 2, 1)
+    DQ_K(4, 1, 1, 1)
+    DQ_K(4, 1, 2, 1)
+    DQ_K(4, 2, 1, 1)
+    DQ_K(4, 2, 2, 1)
+    DQ_K(4, 4, 1, 1)
+    DQ_K(4, 4, 2, 1)
 #undef DQ_K
     return nullptr;
 }
