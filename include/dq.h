@@ -215,7 +215,13 @@ typedef struct {
     const void* wvocab;            /* device Q6_K [vocab][hidden] */
     void* kv_cache;                /* device fp16 [n_layers][2][n_kv][max_ctx][head_dim] */
     int use_graph;                 /* 1: capture the token in a CUDA graph (default); 0: eager launches */
+    int flags;                     /* DQ_MODEL_* bits; 0 for the default behaviour */
 } dq_model_desc;
+
+/* dq_model_desc.flags: launch the token's kernels without programmatic
+ * dependent launch (each kernel waits for the previous one to finish before it
+ * starts streaming); for measuring what the overlap is worth. */
+#define DQ_MODEL_NO_PDL 1
 
 /* Validates the description, allocates the workspace (activations, attention
  * scratch) and captures the token graph on the current device.  Host call;

@@ -60,6 +60,7 @@ struct dq_model {
     bool have_down_q4, have_down_q6;
     // graph
     int use_graph;
+    bool pdl;
     cudaStream_t cap_stream;
     cudaGraph_t graph;
     cudaGraphExec_t exec;
@@ -149,9 +150,9 @@ static cudaError_t enqueue_token(dq_model* m, cudaStream_t s)
     cudaError_t e;
     for (int l = 0; l < m->n_layers; ++l)
         for (int kind = K_QKV; kind <= K_DOWN; ++kind)
-            if ((e = launch_kernel(m, l, kind, s, true)) != cudaSuccess)
+            if ((e = launch_kernel(m, l, kind, s, m->pdl)) != cudaSuccess)
                 return e;
-    return launch_kernel(m, 0, K_VOCAB, s, true);
+    return launch_kernel(m, 0, K_VOCAB, s, m->pdl);
 }
 
 static void free_model(dq_model* m)
@@ -214,6 +215,7 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
     m->max_ctx = d->max_ctx;
     m->eps = d->eps;
     m->use_graph = d->use_graph;
+    m->pdl = (d->flags & DQ_MODEL_NO_PDL) == 0;
     for (int l = 0; l < d->n_layers; ++l) {
         m->attn_norm.push_back(d->attn_norm[l]);
         m->ffn_norm.push_back(d->ffn_norm[l]);

@@ -233,8 +233,11 @@ class _Desc(ctypes.Structure):
         ("n_layers", I), ("hidden", I), ("ffn", I), ("n_q_heads", I), ("n_kv_heads", I), ("head_dim", I),
         ("vocab", I), ("max_ctx", I), ("eps", F),
         ("attn_norm", P), ("wqkv", P), ("wo", P), ("ffn_norm", P), ("wgate", P), ("wup", P), ("wdown", P),
-        ("down_fmt", P), ("out_norm", P), ("wvocab", P), ("kv_cache", P), ("use_graph", I),
+        ("down_fmt", P), ("out_norm", P), ("wvocab", P), ("kv_cache", P), ("use_graph", I), ("flags", I),
     ]
+
+
+MODEL_NO_PDL = 1
 
 
 class Model:
@@ -248,7 +251,7 @@ class Model:
     """
 
     def __init__(self, n_layers, hidden, ffn, n_q_heads, n_kv_heads, head_dim, vocab, max_ctx, eps, weights,
-                 use_graph: bool = True):
+                 use_graph: bool = True, flags: int = 0):
         lib = load()
         self.weights = weights
         self.hidden, self.vocab, self.max_ctx = hidden, vocab, max_ctx
@@ -265,7 +268,7 @@ class Model:
                   arr(weights["attn_norm"]), arr(weights["wqkv"]), arr(weights["wo"]), arr(weights["ffn_norm"]),
                   arr(weights["wgate"]), arr(weights["wup"]), arr(weights["wdown"]),
                   ctypes.cast(fmts, ctypes.c_void_p), weights["out_norm"].data_ptr(), weights["wvocab"].data_ptr(),
-                  weights["kv_cache"].data_ptr(), 1 if use_graph else 0)
+                  weights["kv_cache"].data_ptr(), 1 if use_graph else 0, int(flags))
         h = ctypes.c_void_p()
         _check("dq_model_create", lib.dq_model_create(ctypes.byref(d), ctypes.byref(h)))
         self._h = h
