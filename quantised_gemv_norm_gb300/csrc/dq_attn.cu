@@ -30,7 +30,8 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(const __grid_constant_
     const int nthr = blockDim.x;
     // step->pos was written before the token's first kernel: safe before the wait
     const int n_keys = a.step ? a.step->pos + 1 : a.n_keys;
-    const int L = (n_keys + ATT_CHUNKS - 1) / ATT_CHUNKS;
+    // chunks of at least ATT_MIN_CHUNK keys: short contexts take one block per KV head
+    const int L = max((n_keys + ATT_CHUNKS - 1) / ATT_CHUNKS, ATT_MIN_CHUNK);
     const int j0 = c * L, j1 = min(n_keys, j0 + L);
     const int nact = (n_keys + L - 1) / L;
     pdl_wait();
@@ -100,6 +101,12 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(const __grid_constant_
         m = mnew;
     }
 
+    if (nact == 1) {  // the only block of this KV head: normalise and write directly
+        const float inv = 1.0f / l;
+        *reinterpret_cast<float4*>(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane) =
+            make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv);
+        return;
+    }
     float* pp = a.part + (static_cast<size_t>(h) * ATT_CHUNKS + c) * ATT_PART;
     if (lane == 0) {
         pp[0] = m;

@@ -6,17 +6,19 @@
 // packed weights unpacked in registers, 32-bit accumulation, enough bytes in
 // flight to cover the memory latency).
 //
-// Structure of one thread block (1 per SM, 288 threads):
-//   * warp 8 is the producer: one elected lane streams the block's rows, R rows
+// Structure of one thread block (1 per SM, 544 threads):
+//   * warp 16 is the producer: one elected lane streams the block's rows, R rows
 //     per stage, into a ring of shared-memory stages with 1-D bulk (TMA) copies
 //     that complete on an mbarrier (L2 evict-first: weights are read once);
-//   * warps 0-7 (256 threads) consume.  They are split into RG row groups of P
-//     threads; within a group each thread owns UL fixed 32-weight units of the
-//     K axis (16-byte bf16 units for bf16), so its slice of the activation is
-//     loaded, normalised and quantised once, into registers, in the prologue;
-//   * per stage each thread forms its unit dot products for RPT rows, the group
-//     reduces them (transpose-reduce in the warp, then shared memory across the
-//     group's warps) and one thread per row runs the epilogue.
+//   * warps 0-15 (512 threads) consume.  They are split into RG independent row
+//     groups of P threads; within a group each thread owns UL fixed 32-weight
+//     units of the K axis (16-byte units for bf16), so its slice of the
+//     activation is loaded, normalised and quantised once, into registers;
+//   * per stage each thread forms its unit dot products for RPT rows of its
+//     group, the group reduces them (transpose-reduce in the warp, then shared
+//     memory across the group's warps behind a named barrier of the group only)
+//     and lanes of the group's first warp run the epilogue.  Groups never wait
+//     for each other; each warp releases a stage on its own.
 // The producer starts before griddepcontrol.wait: weights never depend on the
 // previous kernel, so under programmatic dependent launch the ring fills while
 // the previous kernel drains.  Consumers read activations only after the wait.
@@ -26,12 +28,12 @@
 
 namespace dq {
 
-constexpr int NCONS = 256;
+constexpr int NCONS = 512;
 constexpr int NCONS_WARPS = NCONS / 32;
 constexpr int GEMV_THREADS = NCONS + 32;
 constexpr int MAX_STAGES = 8;
 constexpr int MAX_RPT = 4;
-constexpr int CONS_BAR = 1;  // named barrier id of the consumer warps
+constexpr int MAX_RG = 8;  // row groups of >= 64 threads use named barriers 1..8
 
 enum { PRO_F32 = 0, PRO_RMS = 1, PRO_BF16 = 2 };
 enum { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SWIGLU = 3 };
@@ -147,25 +149,26 @@ __device__ __forceinline__ float q4k_unit(const uint8_t* rp, int n, const XQ<PL>
     const uint4 hd = lds128(bp);
     const uint4 c = lds128(bp + 16 + 16 * j);
     const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-    int lo = 0, hi = 0, lo2 = 0, hi2 = 0;
+    // four independent accumulators per plane keep the dependent chains short
+    int la = 0, lb = 0, ha = 0, hb = 0, la2 = 0, lb2 = 0, ha2 = 0, hb2 = 0;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         const uint32_t l = cw[t] & 0x0F0F0F0Fu;  // codes of weights 4t .. 4t+3
         const uint32_t h = cw[t] & 0xF0F0F0F0u;  // 16 x codes of weights 16+4t .. 16+4t+3
-        lo = dp2a_lo(u.q[2 * t], l, lo);
-        lo = dp2a_hi(u.q[2 * t + 1], l, lo);
-        hi = dp2a_lo(u.q[8 + 2 * t], h, hi);
-        hi = dp2a_hi(u.q[8 + 2 * t + 1], h, hi);
+        la = dp2a_lo(u.q[2 * t], l, la);
+        lb = dp2a_hi(u.q[2 * t + 1], l, lb);
+        ha = dp2a_lo(u.q[8 + 2 * t], h, ha);
+        hb = dp2a_hi(u.q[8 + 2 * t + 1], h, hb);
         if (PL == 2) {
-            lo2 = dp2a_lo(u.l[2 * t], l, lo2);
-            lo2 = dp2a_hi(u.l[2 * t + 1], l, lo2);
-            hi2 = dp2a_lo(u.l[8 + 2 * t], h, hi2);
-            hi2 = dp2a_hi(u.l[8 + 2 * t + 1], h, hi2);
+            la2 = dp2a_lo(u.l[2 * t], l, la2);
+            lb2 = dp2a_hi(u.l[2 * t + 1], l, lb2);
+            ha2 = dp2a_lo(u.l[8 + 2 * t], h, ha2);
+            hb2 = dp2a_hi(u.l[8 + 2 * t + 1], h, hb2);
         }
     }
-    float dot16 = static_cast<float>(lo * 16 + hi);  // 16 * sum q * xi
+    float dot16 = static_cast<float>((la + lb) * 16 + (ha + hb));  // 16 * sum q * xi
     if (PL == 2)
-        dot16 += static_cast<float>(lo2 * 16 + hi2) * (1.0f / 32768.0f);
+        dot16 += static_cast<float>((la2 + lb2) * 16 + (ha2 + hb2)) * (1.0f / 32768.0f);
     // scale j: bits 6j.. of the 96-bit string (hd.y, hd.z, hd.w); min j: bits 48+6j..
     const uint32_t s_lo = j < 6 ? hd.y : hd.z, s_hi = j < 6 ? hd.z : hd.w;
     const uint32_t m_lo = j < 3 ? hd.z : hd.w, m_hi = j < 3 ? hd.w : 0u;
@@ -194,7 +197,7 @@ __device__ __forceinline__ float q6k_unit(const uint8_t* rp, int n, const XQ<1>&
     const uint32_t H0 = __funnelshift_r(h0, h1, sh), H1 = __funnelshift_r(h1, h2, sh);
     const uint32_t scw = *reinterpret_cast<const uint16_t*>(bp + 192 + 2 * g);
     const uint32_t dbits = *reinterpret_cast<const uint16_t*>(bp + 208);
-    int da = 0, db = 0;
+    int da = 0, db = 0, da2 = 0, db2 = 0;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         // high two bits of weights 4t+e sit at bits 2t of byte e: move them to bits 4-5
@@ -203,10 +206,12 @@ __device__ __forceinline__ float q6k_unit(const uint8_t* rp, int n, const XQ<1>&
         const uint32_t qa = (ql[t] & 0x0F0F0F0Fu) | ha;         // q of weights 4t+e
         const uint32_t qb = ((ql[t] >> 4) & 0x0F0F0F0Fu) | hb;  // q of weights 16+4t+e
         da = dp2a_lo(u.q[2 * t], qa, da);
-        da = dp2a_hi(u.q[2 * t + 1], qa, da);
+        da2 = dp2a_hi(u.q[2 * t + 1], qa, da2);
         db = dp2a_lo(u.q[8 + 2 * t], qb, db);
-        db = dp2a_hi(u.q[8 + 2 * t + 1], qb, db);
+        db2 = dp2a_hi(u.q[8 + 2 * t + 1], qb, db2);
     }
+    da += da2;
+    db += db2;
     const int sca = static_cast<int>(static_cast<int8_t>(scw & 0xffu));
     const int scb = static_cast<int>(static_cast<int8_t>(scw >> 8));
     const int v = sca * (da - u.s32a) + scb * (db - u.s32b);  // sum sc (q - 32) xi, |v| < 2^31
@@ -267,19 +272,26 @@ struct UnitState<FMT_BF16, PL> {
     uint32_t xb[4];
 };
 
-// Register caps keep two blocks of neighbouring kernels of the decode chain on
-// one SM (288 threads x (cap_a + cap_b) <= 64K registers).
-template <int FMT, int UL, int RPT, int NMAT, int PL>
-__global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? (PL == 2 ? 96 : 80) : (UL <= 3 ? 128 : (UL == 4 ? 144 : 168)))
-    gemv_stream_kernel(const __grid_constant__ GemvArgs a)
+// Synchronise the P threads of row group g (a single warp needs only __syncwarp).
+__device__ __forceinline__ void group_sync(int g, int P)
 {
+    if (P == 32)
+        __syncwarp();
+    else
+        named_bar_sync(1 + g, P);
+}
+
+template <int FMT, int UL, int RPT, int NMAT, int PL>
+__global__ void __maxnreg__(120) gemv_stream_kernel(const __grid_constant__ GemvArgs a)
+{
+    constexpr int NV = RPT * NMAT;
     extern __shared__ __align__(128) uint8_t smem[];
     const int ring_bytes = a.nstage * a.stage_bytes;
-    float* red = reinterpret_cast<float*>(smem + ring_bytes);             // [2][8][RPT*NMAT]
-    float* nred = red + 2 * NCONS_WARPS * RPT * NMAT;                      // [8]
-    int* abort_flag = reinterpret_cast<int*>(nred + NCONS_WARPS);          // [2]
-    uint64_t* full = reinterpret_cast<uint64_t*>(abort_flag + 2);          // [MAX_STAGES]
-    uint64_t* empty = full + MAX_STAGES;                                   // [MAX_STAGES]
+    float* red = reinterpret_cast<float*>(smem + ring_bytes);              // [2][16 warps][NV]
+    float* gred = red + 2 * NCONS_WARPS * NV;                               // [16 warps]
+    int* abort_flag = reinterpret_cast<int*>(gred + NCONS_WARPS);           // [MAX_RG][2]
+    uint64_t* full = reinterpret_cast<uint64_t*>(abort_flag + 2 * MAX_RG);  // [MAX_STAGES]
+    uint64_t* empty = full + MAX_STAGES;                                    // [MAX_STAGES]
 
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -293,8 +305,8 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? (PL == 
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], NCONS_WARPS);
         }
-        abort_flag[0] = 0;
-        abort_flag[1] = 0;
+        for (int i = 0; i < 2 * MAX_RG; ++i)
+            abort_flag[i] = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -331,69 +343,50 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? (PL == 
 
     // ------------------------------------------------------------ consumers
     pdl_wait();
-    const int g = tid / a.P;
-    const int p = tid - g * a.P;
+    const int P = a.P;
+    const int g = tid / P;
+    const int p = tid - g * P;
+    const int gw0 = (g * P) >> 5, nwg = P >> 5;  // the group's first warp and warp count
     const int U = (FMT == FMT_BF16) ? a.K / 8 : a.K / 32;
 
     UnitState<FMT, PL> us[UL];
     bool have[UL];
 #pragma unroll
     for (int k = 0; k < UL; ++k)
-        have[k] = (p + a.P * k) < U;
+        have[k] = (p + P * k) < U;
 
     if (FMT == FMT_BF16) {
 #pragma unroll
         for (int k = 0; k < UL; ++k) {
             uint4 v = make_uint4(0, 0, 0, 0);
             if (have[k])
-                v = __ldcg(reinterpret_cast<const uint4*>(a.xb) + (p + a.P * k));
+                v = __ldcg(reinterpret_cast<const uint4*>(a.xb) + (p + P * k));
             uint32_t* xb = reinterpret_cast<uint32_t*>(&us[k]);
             xb[0] = v.x; xb[1] = v.y; xb[2] = v.z; xb[3] = v.w;
         }
     } else {
-        float rstd = 1.f;
-        if (a.pro == PRO_RMS) {
-            float ss = 0.f;
-#pragma unroll
-            for (int k = 0; k < UL; ++k) {
-                if (have[k]) {
-                    const float* xp = a.x + unit_k0<FMT>(p + a.P * k);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float4 v = ldg_cg_f4(xp + 4 * e);
-                        ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
-                        ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
-                    }
-                }
-            }
-            ss = warp_sum(ss);
-            if (lane == 0)
-                nred[warp] = ss;
-            named_bar_sync(CONS_BAR, NCONS);
-            float tot = 0.f;
-            const int w0 = (g * a.P) >> 5, nw = a.P >> 5;
-            for (int w = 0; w < nw; ++w)
-                tot += nred[w0 + w];
-            rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
-        }
+        // One pass: quantise x (x * gamma under RMSNorm) and sum x^2; RMSNorm's
+        // 1/rms is one scalar, applied to the group scales afterwards.
+        const bool rms = a.pro == PRO_RMS;
+        float ss = 0.f;
 #pragma unroll
         for (int k = 0; k < UL; ++k) {
             float h[32];
             if (have[k]) {
-                const int k0 = unit_k0<FMT>(p + a.P * k);
+                const int k0 = unit_k0<FMT>(p + P * k);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const float4 v = ldg_cg_f4(a.x + k0 + 4 * e);
                     h[4 * e] = v.x; h[4 * e + 1] = v.y; h[4 * e + 2] = v.z; h[4 * e + 3] = v.w;
                 }
-                if (a.pro == PRO_RMS) {
+                if (rms) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        ss = fmaf(h[e], h[e], ss);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const float4 gm = __ldg(reinterpret_cast<const float4*>(a.gamma + k0) + e);
-                        h[4 * e] = h[4 * e] * rstd * gm.x;
-                        h[4 * e + 1] = h[4 * e + 1] * rstd * gm.y;
-                        h[4 * e + 2] = h[4 * e + 2] * rstd * gm.z;
-                        h[4 * e + 3] = h[4 * e + 3] * rstd * gm.w;
+                        h[4 * e] *= gm.x; h[4 * e + 1] *= gm.y; h[4 * e + 2] *= gm.z; h[4 * e + 3] *= gm.w;
                     }
                 }
             } else {
@@ -403,14 +396,31 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? (PL == 
             }
             quantise_unit<PL>(h, reinterpret_cast<XQ<PL>&>(us[k]));
         }
+        if (rms) {
+            ss = warp_sum(ss);
+            if (lane == 0)
+                gred[warp] = ss;
+            group_sync(g, P);
+            float tot = 0.f;
+            for (int w = 0; w < nwg; ++w)
+                tot += gred[gw0 + w];
+            const float rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
+#pragma unroll
+            for (int k = 0; k < UL; ++k) {
+                XQ<PL>& u = reinterpret_cast<XQ<PL>&>(us[k]);
+                u.s *= rstd;
+                u.f *= rstd;
+                u.hsum *= rstd;
+            }
+        }
     }
 
-    constexpr int NV = RPT * NMAT;
+    int* my_abort = abort_flag + 2 * g;
     for (int t = 0; t < ntiles; ++t) {
         const int s = t % a.nstage;
         if (!mbar_wait(&full[s], (t / a.nstage) & 1)) {
             set_error(a.err, DEVERR_TIMEOUT_FULL);
-            atomicExch(&abort_flag[t & 1], 1);
+            atomicExch(&my_abort[t & 1], 1);
         }
         const uint8_t* tile = smem + static_cast<size_t>(s) * a.stage_bytes;
         const int row0 = r0 + t * R;
@@ -430,7 +440,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? (PL == 
 #pragma unroll
                     for (int k = 0; k < UL; ++k) {
                         if (have[k]) {
-                            const int n = p + a.P * k;
+                            const int n = p + P * k;
                             if (FMT == FMT_Q4K)
                                 sum += q4k_unit<PL>(rp, n, reinterpret_cast<const XQ<PL>&>(us[k]));
                             else if (FMT == FMT_Q6K)
@@ -451,18 +461,18 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? (PL == 
         float* rb = red + (t & 1) * NCONS_WARPS * NV;
         if ((lane & (32 / NV - 1)) == 0)
             rb[warp * NV + lane / (32 / NV)] = acc[0];
-        named_bar_sync(CONS_BAR, NCONS);
-        if (tid < R) {
-            const int rg = tid % a.RG, i = tid / a.RG;
-            if (tid < nr) {
-                const int w0 = (rg * a.P) >> 5, nw = a.P >> 5;
+        group_sync(g, P);
+        if (warp == gw0 && lane < RPT) {
+            const int i = lane;
+            const int row = g + a.RG * i;
+            if (row < nr) {
                 float v0 = 0.f, v1 = 0.f;
-                for (int w = 0; w < nw; ++w) {
-                    v0 += rb[(w0 + w) * NV + i];
+                for (int w = 0; w < nwg; ++w) {
+                    v0 += rb[(gw0 + w) * NV + i];
                     if (NMAT == 2)
-                        v1 += rb[(w0 + w) * NV + RPT + i];
+                        v1 += rb[(gw0 + w) * NV + RPT + i];
                 }
-                const int r = row0 + tid;
+                const int r = row0 + row;
                 if (a.epi == EPI_STORE) {
                     float* out = a.y_from_step ? a.step->logits : a.y;
                     out[r] = v0;
@@ -487,9 +497,9 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? (PL == 
                 }
             }
         }
-        // uniform: every consumer reads this tile's flag after the same barrier; a
-        // flag for tile t+1 goes to the other slot, so a fast thread cannot race it
-        if (*reinterpret_cast<volatile int*>(&abort_flag[t & 1]))
+        // Uniform within the group: its threads read this tile's flag after the same
+        // group barrier; a flag for tile t+1 goes to the other slot.
+        if (*reinterpret_cast<volatile int*>(&my_abort[t & 1]))
             break;
     }
 }
@@ -497,7 +507,7 @@ __global__ void __launch_bounds__(GEMV_THREADS, 1) __maxnreg__(UL == 1 ? (PL == 
 // Shared-memory bytes the kernel needs beyond the ring.
 __host__ __device__ constexpr int gemv_extra_smem(int rpt, int nmat)
 {
-    return 2 * NCONS_WARPS * rpt * nmat * 4 + NCONS_WARPS * 4 + 2 * 4 + 2 * MAX_STAGES * 8 + 16;
+    return 2 * NCONS_WARPS * rpt * nmat * 4 + NCONS_WARPS * 4 + 2 * MAX_RG * 4 + 2 * MAX_STAGES * 8 + 16;
 }
 
 }  // namespace dq

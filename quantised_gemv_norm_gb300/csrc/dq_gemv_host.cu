@@ -60,11 +60,15 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, int planes, Ge
         return DQ_ERR_ALIGN;  // 210-byte blocks: rows are 16-byte aligned only when K % 2048 == 0
     const int U = K / unit_w;
     const int rb = row_bytes_of(fmt, K);
+    const int pl = (planes == 2 && fmt == DQ_FMT_Q4K) ? 2 : 1;
     static const int ul_q[] = {1, 2, 3, 4};
+    static const int ul_q2[] = {1, 2};
     static const int ul_b[] = {1, 2, 4, 8, 12};
-    const int* uls = fmt == DQ_FMT_BF16 ? ul_b : ul_q;
-    const int nul = fmt == DQ_FMT_BF16 ? 5 : 4;
-    static const int Ps[] = {128, 256, 64, 32};
+    const int* uls = fmt == DQ_FMT_BF16 ? ul_b : (pl == 2 ? ul_q2 : ul_q);
+    const int nul = fmt == DQ_FMT_BF16 ? 5 : (pl == 2 ? 2 : 4);
+    // Row groups of P threads (P >= 64 so that the groups' named barriers fit).
+    // Least masked lanes first, then more groups (smaller P).
+    static const int Ps[] = {64, 128, 256, 512};
     int best_P = 0, best_UL = 0, best_waste = 1 << 30;
     for (int pi = 0; pi < 4; ++pi) {
         const int P = Ps[pi];
@@ -98,9 +102,18 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, int planes, Ge
     p.P = best_P;
     p.RG = dq::NCONS / best_P;
     p.UL = best_UL;
+    const int sms = sm_count();
+    p.grid = rows < sms ? rows : sms;
+    // Stage size: at most GEMV_STAGE_TARGET, and about a quarter of one block's
+    // bytes so small matrices still pipeline; rows per thread RPT in {1, 2, 4}.
+    const long long per_block = static_cast<long long>((rows + p.grid - 1) / p.grid) * rb * nmat;
+    const long long unit_stage = static_cast<long long>(p.RG) * rb * nmat;
+    long long cap = per_block / 4;
+    if (cap > GEMV_STAGE_TARGET)
+        cap = GEMV_STAGE_TARGET;
     p.RPT = 1;
     for (int r = 4; r >= 1; r >>= 1)
-        if (static_cast<long long>(p.RG) * r * rb * nmat <= GEMV_STAGE_TARGET) {
+        if (unit_stage * r <= cap) {
             p.RPT = r;
             break;
         }
@@ -111,15 +124,19 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, int planes, Ge
     if (p.nstage > dq::MAX_STAGES)
         p.nstage = dq::MAX_STAGES;
     p.smem_bytes = p.nstage * p.stage_bytes + dq::gemv_extra_smem(p.RPT, nmat);
-    const int sms = sm_count();
-    p.grid = rows < sms ? rows : sms;
-    p.planes = (planes == 2 && fmt == DQ_FMT_Q4K && p.UL <= 2) ? 2 : 1;
+    p.planes = pl;
     p.kernel = kernel_for(fmt, p.UL, p.RPT, nmat, p.planes);
     if (!p.kernel)
         return DQ_ERR_UNSUPPORTED;
     cudaError_t e = ensure_smem_attr(p.kernel, p.smem_bytes);
     if (e != cudaSuccess)
         return set_cuda_error(e);
+    int blocks = 0;  // one block of GEMV_THREADS threads must fit on an SM
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, p.kernel, dq::GEMV_THREADS, p.smem_bytes);
+    if (e != cudaSuccess)
+        return set_cuda_error(e);
+    if (blocks < 1)
+        return DQ_ERR_UNSUPPORTED;
     *plan = p;
     return DQ_OK;
 }

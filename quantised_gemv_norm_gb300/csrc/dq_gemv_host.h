@@ -25,9 +25,9 @@ struct GemvPlan {
     GemvKernel kernel;
 };
 
-constexpr int GEMV_STAGE_TARGET = 32 * 1024;   // bytes per ring stage (target)
+constexpr int GEMV_STAGE_TARGET = 48 * 1024;   // bytes per ring stage (upper target)
 constexpr int GEMV_STAGE_MAX = 64 * 1024;      // largest stage accepted
-constexpr int GEMV_RING_DEFAULT = 96 * 1024;   // ring bytes: two blocks of two kernels fit one SM
+constexpr int GEMV_RING_DEFAULT = 176 * 1024;  // ring bytes: one block per SM
 
 // Chooses the thread layout, tile and ring for one matrix shape.  `planes` = 2
 // asks for the two-plane activation where the format and layout allow it (else

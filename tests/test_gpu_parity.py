@@ -176,7 +176,7 @@ def _attn_inputs(seed, n_q, n_kv, max_ctx, n_keys):
     return q, k, v
 
 
-@pytest.mark.parametrize("n_q,n_kv,n_keys", [(32, 8, 1), (32, 8, 7), (32, 8, 32), (32, 8, 33), (32, 8, 513),
+@pytest.mark.parametrize("n_q,n_kv,n_keys", [(32, 8, 1), (32, 8, 7), (32, 8, 32), (32, 8, 33), (32, 8, 64), (32, 8, 65), (32, 8, 513),
                                              (32, 8, 1024), (16, 2, 100), (8, 8, 17)])
 def test_attention(dq, orc, n_q, n_kv, n_keys):
     q, k, v = _attn_inputs(n_keys, n_q, n_kv, 1024, n_keys)
