@@ -6,11 +6,13 @@
 // packed weights unpacked in registers, 32-bit accumulation, enough bytes in
 // flight to cover the memory latency).
 //
-// Structure of one thread block (1 per SM, 544 threads):
-//   * warp 16 is the producer: one elected lane streams the block's rows, R rows
-//     per stage, into a ring of shared-memory stages with 1-D bulk (TMA) copies
-//     that complete on an mbarrier (L2 evict-first: weights are read once);
-//   * warps 0-15 (512 threads) consume.  They are split into RG independent row
+// Structure of one thread block (1 per SM, 512 threads, 16 warps):
+//   * the block's rows stream, R rows per stage, into a ring of shared-memory
+//     stages with 1-D bulk (TMA) copies that complete on an mbarrier (L2
+//     evict-first: weights are read once).  Thread 0 issues the first ring-full
+//     at kernel start; afterwards the last warp to release a stage refills it
+//     (an mbarrier counts the releases, a shared counter elects the refiller);
+//   * all 16 warps consume.  They are split into RG independent row
 //     groups of P threads; within a group each thread owns UL fixed 32-weight
 //     units of the K axis (16-byte units for bf16), so its slice of the
 //     activation is loaded, normalised and quantised once, into registers;
@@ -19,9 +21,9 @@
 //     memory across the group's warps behind a named barrier of the group only)
 //     and lanes of the group's first warp run the epilogue.  Groups never wait
 //     for each other; each warp releases a stage on its own.
-// The producer starts before griddepcontrol.wait: weights never depend on the
-// previous kernel, so under programmatic dependent launch the ring fills while
-// the previous kernel drains.  Consumers read activations only after the wait.
+// The first ring-full is issued before griddepcontrol.wait: weights never depend
+// on the previous kernel, so under programmatic dependent launch the ring fills
+// while the previous kernel drains.  Activations are read only after the wait.
 #pragma once
 
 #include "dq_common.cuh"
@@ -30,7 +32,7 @@ namespace dq {
 
 constexpr int NCONS = 512;
 constexpr int NCONS_WARPS = NCONS / 32;
-constexpr int GEMV_THREADS = NCONS + 32;
+constexpr int GEMV_THREADS = NCONS;
 constexpr int MAX_STAGES = 8;
 constexpr int MAX_RPT = 4;
 constexpr int MAX_RG = 8;  // row groups of >= 64 threads use named barriers 1..8
@@ -282,7 +284,23 @@ __device__ __forceinline__ void group_sync(int g, int P)
 }
 
 template <int FMT, int UL, int RPT, int NMAT, int PL>
-__global__ void __maxnreg__(120) gemv_stream_kernel(const __grid_constant__ GemvArgs a)
+__device__ __forceinline__ void issue_tile(const GemvArgs& a, uint8_t* smem, uint64_t* full, int t, int r0, int r1,
+                                           int R, uint64_t pol)
+{
+    const int s = t % a.nstage;
+    const int row = r0 + t * R;
+    const int nr = min(R, r1 - row);
+    const uint32_t bytes = static_cast<uint32_t>(nr * a.row_bytes);
+    uint8_t* dst = smem + static_cast<size_t>(s) * a.stage_bytes;
+    mbar_arrive_expect_tx(&full[s], bytes * NMAT);
+    bulk_g2s(dst, a.W + static_cast<size_t>(row) * a.row_bytes, bytes, &full[s], pol);
+    if (NMAT == 2)
+        bulk_g2s(dst + static_cast<size_t>(R) * a.row_bytes, a.W2 + static_cast<size_t>(row) * a.row_bytes, bytes,
+                 &full[s], pol);
+}
+
+template <int FMT, int UL, int RPT, int NMAT, int PL>
+__global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ GemvArgs a)
 {
     constexpr int NV = RPT * NMAT;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -290,7 +308,8 @@ __global__ void __maxnreg__(120) gemv_stream_kernel(const __grid_constant__ Gemv
     float* red = reinterpret_cast<float*>(smem + ring_bytes);              // [2][16 warps][NV]
     float* gred = red + 2 * NCONS_WARPS * NV;                               // [16 warps]
     int* abort_flag = reinterpret_cast<int*>(gred + NCONS_WARPS);           // [MAX_RG][2]
-    uint64_t* full = reinterpret_cast<uint64_t*>(abort_flag + 2 * MAX_RG);  // [MAX_STAGES]
+    int* release = abort_flag + 2 * MAX_RG;                                 // [MAX_STAGES]
+    uint64_t* full = reinterpret_cast<uint64_t*>(release + MAX_STAGES);     // [MAX_STAGES]
     uint64_t* empty = full + MAX_STAGES;                                    // [MAX_STAGES]
 
     pdl_trigger();
@@ -299,47 +318,21 @@ __global__ void __maxnreg__(120) gemv_stream_kernel(const __grid_constant__ Gemv
     const int r1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * a.rows / gridDim.x);
     const int R = a.RG * RPT;
     const int ntiles = (r1 - r0 + R - 1) / R;
+    const uint64_t pol = l2_evict_first_policy();
 
     if (tid == 0) {
         for (int s = 0; s < a.nstage; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], NCONS_WARPS);
+            release[s] = 0;
         }
         for (int i = 0; i < 2 * MAX_RG; ++i)
             abort_flag[i] = 0;
         fence_mbar_init();
+        for (int t = 0; t < min(a.nstage, ntiles); ++t)
+            issue_tile<FMT, UL, RPT, NMAT, PL>(a, smem, full, t, r0, r1, R, pol);
     }
     __syncthreads();
-
-    // ------------------------------------------------------------ producer
-    if (warp == NCONS_WARPS) {
-        if (lane == 0) {
-            const uint64_t pol = l2_evict_first_policy();
-            int issued = 0;
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t % a.nstage;
-                if (t >= a.nstage && !mbar_wait(&empty[s], ((t / a.nstage) - 1) & 1)) {
-                    set_error(a.err, DEVERR_TIMEOUT_EMPTY);
-                    break;
-                }
-                const int row = r0 + t * R;
-                const int nr = min(R, r1 - row);
-                const uint32_t bytes = static_cast<uint32_t>(nr * a.row_bytes);
-                uint8_t* dst = smem + static_cast<size_t>(s) * a.stage_bytes;
-                mbar_arrive_expect_tx(&full[s], bytes * NMAT);
-                bulk_g2s(dst, a.W + static_cast<size_t>(row) * a.row_bytes, bytes, &full[s], pol);
-                if (NMAT == 2)
-                    bulk_g2s(dst + static_cast<size_t>(R) * a.row_bytes, a.W2 + static_cast<size_t>(row) * a.row_bytes,
-                             bytes, &full[s], pol);
-                ++issued;
-            }
-            // do not leave the block with copies in flight
-            for (int t = max(0, issued - a.nstage); t < issued; ++t)
-                if (!mbar_wait(&full[t % a.nstage], (t / a.nstage) & 1))
-                    set_error(a.err, DEVERR_TIMEOUT_DRAIN);
-        }
-        return;
-    }
 
     // ------------------------------------------------------------ consumers
     pdl_wait();
@@ -454,8 +447,18 @@ __global__ void __maxnreg__(120) gemv_stream_kernel(const __grid_constant__ Gemv
             }
         }
         __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&empty[s]);  // this warp is done with the stage
+        if (lane == 0) {  // this warp is done with the stage; the last one refills it
+            mbar_arrive(&empty[s]);
+            if (atomicAdd(&release[s], 1) == NCONS_WARPS - 1) {
+                release[s] = 0;
+                if (t + a.nstage < ntiles) {
+                    if (mbar_wait(&empty[s], (t / a.nstage) & 1))
+                        issue_tile<FMT, UL, RPT, NMAT, PL>(a, smem, full, t + a.nstage, r0, r1, R, pol);
+                    else
+                        set_error(a.err, DEVERR_TIMEOUT_EMPTY);
+                }
+            }
+        }
 
         warp_transpose_reduce<NV>(acc, lane);
         float* rb = red + (t & 1) * NCONS_WARPS * NV;
@@ -507,7 +510,8 @@ __global__ void __maxnreg__(120) gemv_stream_kernel(const __grid_constant__ Gemv
 // Shared-memory bytes the kernel needs beyond the ring.
 __host__ __device__ constexpr int gemv_extra_smem(int rpt, int nmat)
 {
-    return 2 * NCONS_WARPS * rpt * nmat * 4 + NCONS_WARPS * 4 + 2 * MAX_RG * 4 + 2 * MAX_STAGES * 8 + 16;
+    return 2 * NCONS_WARPS * rpt * nmat * 4 + NCONS_WARPS * 4 + 2 * MAX_RG * 4 + MAX_STAGES * 4 +
+           2 * MAX_STAGES * 8 + 16;
 }
 
 }  // namespace dq
