@@ -274,16 +274,47 @@ struct UnitState<FMT_BF16, PL> {
     uint32_t xb[4];
 };
 
-// Synchronise the P threads of row group g (a single warp needs only __syncwarp).
-__device__ __forceinline__ void group_sync(int g, int P)
+// ------------------------------------------------------- shared-memory layout
+
+constexpr int XQ_WORDS_PL1 = 24;  // q[16], s, f, hsum, s32a, s32b, pad: 96 bytes
+constexpr int XQ_WORDS_PL2 = 40;  // q[16], l[16], s, f, hsum, s32a, s32b, pad: 160 bytes
+constexpr int GEMV_MISC_BYTES = 256;
+
+__host__ __device__ constexpr int xq_words(int pl) { return pl == 2 ? XQ_WORDS_PL2 : XQ_WORDS_PL1; }
+
+// Offsets of the block's shared-memory regions: the weight ring, the staged
+// activation and RMSNorm weight, the quantised activation (one entry per
+// 32-element unit), the per-warp partial sums and the barriers.
+struct GemvSmem {
+    int x, g, xq, red, misc, total;
+};
+
+__host__ __device__ inline GemvSmem gemv_smem_layout(int fmt, int K, int nstage, int stage_bytes, int rpt, int nmat,
+                                                     int pl, bool norm)
 {
-    if (P == 32)
-        __syncwarp();
-    else
-        named_bar_sync(1 + g, P);
+    GemvSmem L;
+    int o = nstage * stage_bytes;
+    L.x = L.g = L.xq = o;
+    if (fmt != FMT_BF16) {
+        L.x = o;
+        o += K * 4;
+        L.g = o;
+        if (norm)
+            o += K * 4;
+        L.xq = o;
+        o += (K / 32) * xq_words(pl) * 4;
+    }
+    L.red = o;
+    o += 2 * nstage * NCONS_WARPS * rpt * nmat * 4;
+    L.misc = o;
+    o += GEMV_MISC_BYTES;
+    L.total = o;
+    return L;
 }
 
-template <int FMT, int UL, int RPT, int NMAT, int PL>
+// ------------------------------------------------------------------ kernel
+
+template <int NMAT>
 __device__ __forceinline__ void issue_tile(const GemvArgs& a, uint8_t* smem, uint64_t* full, int t, int r0, int r1,
                                            int R, uint64_t pol)
 {
@@ -299,18 +330,77 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, uint8_t* smem, uin
                  &full[s], pol);
 }
 
+// Quantise the staged activation (times gamma under RMSNorm) once per block:
+// eight lanes share one 32-element unit, four elements each.  Returns this
+// thread's partial sum of x^2.
+template <int FMT, int PL>
+__device__ __forceinline__ float quantise_block(const float* xs, const float* gs, bool norm, uint32_t* xq, int K,
+                                                int tid)
+{
+    float ss = 0.f;
+    const int nchunks = K / 4;  // a multiple of 64: whole warps take part in each pass
+    for (int c = tid; c < nchunks; c += NCONS) {
+        float4 v = reinterpret_cast<const float4*>(xs)[c];
+        if (norm) {
+            ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+            const float4 gv = reinterpret_cast<const float4*>(gs)[c];
+            v.x *= gv.x; v.y *= gv.y; v.z *= gv.z; v.w *= gv.w;
+        }
+        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        float hs = (v.x + v.y) + (v.z + v.w);
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            hs += __shfl_xor_sync(0xffffffffu, hs, o);
+        }
+        const float inv = amax > 0.f ? XQ_MAX / amax : 0.f;
+        const float t0 = v.x * inv, t1 = v.y * inv, t2 = v.z * inv, t3 = v.w * inv;
+        const int a0 = __float2int_rn(t0), a1 = __float2int_rn(t1), a2 = __float2int_rn(t2), a3 = __float2int_rn(t3);
+        const int e = c & 7;
+        uint32_t* q = xq + (c >> 3) * xq_words(PL);
+        q[2 * e] = pack16x2(a0, a1);
+        q[2 * e + 1] = pack16x2(a2, a3);
+        if (PL == 2) {  // remainders: t - a is exact in fp32
+            q[16 + 2 * e] = pack16x2(__float2int_rn((t0 - static_cast<float>(a0)) * 32768.0f),
+                                     __float2int_rn((t1 - static_cast<float>(a1)) * 32768.0f));
+            q[16 + 2 * e + 1] = pack16x2(__float2int_rn((t2 - static_cast<float>(a2)) * 32768.0f),
+                                         __float2int_rn((t3 - static_cast<float>(a3)) * 32768.0f));
+        }
+        int isum = (a0 + a1) + (a2 + a3);  // the two 16-element halves of the unit (Q6_K offsets)
+        isum += __shfl_xor_sync(0xffffffffu, isum, 1);
+        isum += __shfl_xor_sync(0xffffffffu, isum, 2);
+        float* meta = reinterpret_cast<float*>(q + 16 * PL);
+        if (e == 0) {
+            const float sc = amax / XQ_MAX;
+            meta[0] = sc;
+            meta[1] = sc * 0.0625f;
+            meta[2] = hs;
+            reinterpret_cast<int*>(meta)[3] = 32 * isum;
+        } else if (e == 4) {
+            reinterpret_cast<int*>(meta)[4] = 32 * isum;
+        }
+    }
+    return ss;
+}
+
 template <int FMT, int UL, int RPT, int NMAT, int PL>
 __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ GemvArgs a)
 {
     constexpr int NV = RPT * NMAT;
     extern __shared__ __align__(128) uint8_t smem[];
-    const int ring_bytes = a.nstage * a.stage_bytes;
-    float* red = reinterpret_cast<float*>(smem + ring_bytes);              // [2][16 warps][NV]
-    float* gred = red + 2 * NCONS_WARPS * NV;                               // [16 warps]
-    int* abort_flag = reinterpret_cast<int*>(gred + NCONS_WARPS);           // [MAX_RG][2]
-    int* release = abort_flag + 2 * MAX_RG;                                 // [MAX_STAGES]
-    uint64_t* full = reinterpret_cast<uint64_t*>(release + MAX_STAGES);     // [MAX_STAGES]
-    uint64_t* empty = full + MAX_STAGES;                                    // [MAX_STAGES]
+    const bool norm = a.pro == PRO_RMS;
+    const GemvSmem L = gemv_smem_layout(FMT, a.K, a.nstage, a.stage_bytes, RPT, NMAT, PL, norm);
+    float* xs = reinterpret_cast<float*>(smem + L.x);
+    float* gs = reinterpret_cast<float*>(smem + L.g);
+    uint32_t* xq = reinterpret_cast<uint32_t*>(smem + L.xq);
+    float* red = reinterpret_cast<float*>(smem + L.red);            // [2 nstage][16 warps][NV]
+    int* release = reinterpret_cast<int*>(smem + L.misc);           // [MAX_STAGES]
+    int* abort_flag = release + MAX_STAGES;                         // [4]
+    float* gred = reinterpret_cast<float*>(abort_flag + 4);         // [16]
+    uint64_t* full = reinterpret_cast<uint64_t*>(gred + NCONS_WARPS);  // [MAX_STAGES]
+    uint64_t* empty = full + MAX_STAGES;                            // [MAX_STAGES]
+    uint64_t* xbar = empty + MAX_STAGES;
+    uint64_t* gbar = xbar + 1;
 
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -319,6 +409,7 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
     const int R = a.RG * RPT;
     const int ntiles = (r1 - r0 + R - 1) / R;
     const uint64_t pol = l2_evict_first_policy();
+    const bool quant = FMT != FMT_BF16;
 
     if (tid == 0) {
         for (int s = 0; s < a.nstage; ++s) {
@@ -326,16 +417,21 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             mbar_init(&empty[s], NCONS_WARPS);
             release[s] = 0;
         }
-        for (int i = 0; i < 2 * MAX_RG; ++i)
-            abort_flag[i] = 0;
+        mbar_init(xbar, 1);
+        mbar_init(gbar, 1);
+        abort_flag[0] = 0;
         fence_mbar_init();
+        // weights and the norm weight never depend on the previous kernel
         for (int t = 0; t < min(a.nstage, ntiles); ++t)
-            issue_tile<FMT, UL, RPT, NMAT, PL>(a, smem, full, t, r0, r1, R, pol);
+            issue_tile<NMAT>(a, smem, full, t, r0, r1, R, pol);
+        if (quant && norm) {
+            mbar_arrive_expect_tx(gbar, static_cast<uint32_t>(a.K * 4));
+            bulk_g2s_plain(gs, a.gamma, static_cast<uint32_t>(a.K * 4), gbar);
+        }
     }
     __syncthreads();
+    pdl_wait();  // the activation is the previous kernel's output
 
-    // ------------------------------------------------------------ consumers
-    pdl_wait();
     const int P = a.P;
     const int g = tid / P;
     const int p = tid - g * P;
@@ -358,62 +454,66 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             xb[0] = v.x; xb[1] = v.y; xb[2] = v.z; xb[3] = v.w;
         }
     } else {
-        // One pass: quantise x (x * gamma under RMSNorm) and sum x^2; RMSNorm's
-        // 1/rms is one scalar, applied to the group scales afterwards.
-        const bool rms = a.pro == PRO_RMS;
-        float ss = 0.f;
-#pragma unroll
-        for (int k = 0; k < UL; ++k) {
-            float h[32];
-            if (have[k]) {
-                const int k0 = unit_k0<FMT>(p + P * k);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float4 v = ldg_cg_f4(a.x + k0 + 4 * e);
-                    h[4 * e] = v.x; h[4 * e + 1] = v.y; h[4 * e + 2] = v.z; h[4 * e + 3] = v.w;
-                }
-                if (rms) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        ss = fmaf(h[e], h[e], ss);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float4 gm = __ldg(reinterpret_cast<const float4*>(a.gamma + k0) + e);
-                        h[4 * e] *= gm.x; h[4 * e + 1] *= gm.y; h[4 * e + 2] *= gm.z; h[4 * e + 3] *= gm.w;
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    h[e] = 0.f;
-            }
-            quantise_unit<PL>(h, reinterpret_cast<XQ<PL>&>(us[k]));
+        if (tid == 0) {
+            mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(a.K * 4));
+            bulk_g2s_plain(xs, a.x, static_cast<uint32_t>(a.K * 4), xbar);
         }
-        if (rms) {
+        bool ok = mbar_wait(xbar, 0);
+        if (norm)
+            ok = mbar_wait(gbar, 0) && ok;
+        if (!ok) {
+            set_error(a.err, DEVERR_TIMEOUT_FULL);
+            abort_flag[0] = 1;
+        }
+        float ss = quantise_block<FMT, PL>(xs, gs, norm, xq, a.K, tid);
+        float rstd = 1.f;
+        if (norm) {
             ss = warp_sum(ss);
             if (lane == 0)
                 gred[warp] = ss;
-            group_sync(g, P);
+        }
+        __syncthreads();  // xq and gred complete
+        if (norm) {
             float tot = 0.f;
-            for (int w = 0; w < nwg; ++w)
-                tot += gred[gw0 + w];
-            const float rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
+            for (int w = 0; w < NCONS_WARPS; ++w)
+                tot += gred[w];
+            rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
+        }
 #pragma unroll
-            for (int k = 0; k < UL; ++k) {
+        for (int k = 0; k < UL; ++k) {
+            if (have[k]) {
                 XQ<PL>& u = reinterpret_cast<XQ<PL>&>(us[k]);
-                u.s *= rstd;
-                u.f *= rstd;
-                u.hsum *= rstd;
+                const uint32_t* src = xq + (unit_k0<FMT>(p + P * k) >> 5) * xq_words(PL);
+#pragma unroll
+                for (int w = 0; w < 16; w += 4) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(src + w);
+                    u.q[w] = v.x; u.q[w + 1] = v.y; u.q[w + 2] = v.z; u.q[w + 3] = v.w;
+                }
+                if (PL == 2) {
+#pragma unroll
+                    for (int w = 0; w < 16; w += 4) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(src + 16 + w);
+                        u.l[w] = v.x; u.l[w + 1] = v.y; u.l[w + 2] = v.z; u.l[w + 3] = v.w;
+                    }
+                }
+                const float* meta = reinterpret_cast<const float*>(src + 16 * PL);
+                u.s = meta[0] * rstd;
+                u.f = meta[1] * rstd;
+                u.hsum = meta[2] * rstd;
+                u.s32a = reinterpret_cast<const int*>(meta)[3];
+                u.s32b = reinterpret_cast<const int*>(meta)[4];
             }
         }
     }
 
-    int* my_abort = abort_flag + 2 * g;
     for (int t = 0; t < ntiles; ++t) {
+        if (*reinterpret_cast<volatile int*>(abort_flag))
+            break;  // no block-wide barrier follows: warps may leave independently
         const int s = t % a.nstage;
         if (!mbar_wait(&full[s], (t / a.nstage) & 1)) {
             set_error(a.err, DEVERR_TIMEOUT_FULL);
-            atomicExch(&my_abort[t & 1], 1);
+            abort_flag[0] = 1;
+            break;
         }
         const uint8_t* tile = smem + static_cast<size_t>(s) * a.stage_bytes;
         const int row0 = r0 + t * R;
@@ -446,72 +546,68 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) {  // this warp is done with the stage; the last one refills it
-            mbar_arrive(&empty[s]);
-            if (atomicAdd(&release[s], 1) == NCONS_WARPS - 1) {
-                release[s] = 0;
-                if (t + a.nstage < ntiles) {
-                    if (mbar_wait(&empty[s], (t / a.nstage) & 1))
-                        issue_tile<FMT, UL, RPT, NMAT, PL>(a, smem, full, t + a.nstage, r0, r1, R, pol);
-                    else
-                        set_error(a.err, DEVERR_TIMEOUT_EMPTY);
-                }
-            }
-        }
-
+        // warp partial sums of this tile's rows -> shared memory
         warp_transpose_reduce<NV>(acc, lane);
-        float* rb = red + (t & 1) * NCONS_WARPS * NV;
+        float* rb = red + (t % (2 * a.nstage)) * NCONS_WARPS * NV;
         if ((lane & (32 / NV - 1)) == 0)
             rb[warp * NV + lane / (32 / NV)] = acc[0];
-        group_sync(g, P);
-        if (warp == gw0 && lane < RPT) {
-            const int i = lane;
-            const int row = g + a.RG * i;
-            if (row < nr) {
-                float v0 = 0.f, v1 = 0.f;
-                for (int w = 0; w < nwg; ++w) {
-                    v0 += rb[(gw0 + w) * NV + i];
-                    if (NMAT == 2)
-                        v1 += rb[(gw0 + w) * NV + RPT + i];
-                }
-                const int r = row0 + row;
-                if (a.epi == EPI_STORE) {
-                    float* out = a.y_from_step ? a.step->logits : a.y;
-                    out[r] = v0;
-                } else if (a.epi == EPI_RESID) {
-                    a.y[r] += v0;
-                } else if (a.epi == EPI_SWIGLU) {
-                    a.y[r] = v0 / (1.0f + expf(-v0)) * v1;
-                } else {  // EPI_QKV
-                    if (r < a.qdim) {
-                        a.y[r] = v0;
-                    } else {
-                        const int idx = r - a.qdim;
-                        const int which = idx / a.kvdim, rem = idx - which * a.kvdim;
-                        const int kvh = rem / a.hd, dd = rem - kvh * a.hd;
-                        __half* plane = which ? a.kv_v : a.kv_k;
-                        const int pos = a.step->pos;
-                        if (pos >= 0 && pos < a.max_ctx)
-                            plane[(static_cast<size_t>(kvh) * a.max_ctx + pos) * a.hd + dd] = __float2half_rn(v0);
-                        else
-                            set_error(a.err, DEVERR_BAD_ARG);
-                    }
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {  // release the stage (mbarrier arrive = release); count the releases
+            mbar_arrive(&empty[s]);
+            last = atomicAdd(&release[s], 1) == NCONS_WARPS - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (!last)
+            continue;
+        // The last warp to release: every warp has arrived, so acquire the stage's
+        // phase (this also makes the other warps' partial sums visible), refill the
+        // slot, then finish the tile's rows.
+        if (!mbar_wait(&empty[s], (t / a.nstage) & 1)) {
+            set_error(a.err, DEVERR_TIMEOUT_EMPTY);
+            abort_flag[0] = 1;
+            break;
+        }
+        if (lane == 0) {
+            release[s] = 0;
+            if (t + a.nstage < ntiles)
+                issue_tile<NMAT>(a, smem, full, t + a.nstage, r0, r1, R, pol);
+        }
+        for (int row = lane; row < nr; row += 32) {
+            const int rg = row % a.RG, i = row / a.RG;
+            const int w0 = (rg * P) >> 5;
+            float v0 = 0.f, v1 = 0.f;
+            for (int w = 0; w < nwg; ++w) {
+                v0 += rb[(w0 + w) * NV + i];
+                if (NMAT == 2)
+                    v1 += rb[(w0 + w) * NV + RPT + i];
+            }
+            const int r = row0 + row;
+            if (a.epi == EPI_STORE) {
+                float* out = a.y_from_step ? a.step->logits : a.y;
+                out[r] = v0;
+            } else if (a.epi == EPI_RESID) {
+                a.y[r] += v0;
+            } else if (a.epi == EPI_SWIGLU) {
+                a.y[r] = v0 / (1.0f + expf(-v0)) * v1;
+            } else {  // EPI_QKV
+                if (r < a.qdim) {
+                    a.y[r] = v0;
+                } else {
+                    const int idx = r - a.qdim;
+                    const int which = idx / a.kvdim, rem = idx - which * a.kvdim;
+                    const int kvh = rem / a.hd, dd = rem - kvh * a.hd;
+                    __half* plane = which ? a.kv_v : a.kv_k;
+                    const int pos = a.step->pos;
+                    if (pos >= 0 && pos < a.max_ctx)
+                        plane[(static_cast<size_t>(kvh) * a.max_ctx + pos) * a.hd + dd] = __float2half_rn(v0);
+                    else
+                        set_error(a.err, DEVERR_BAD_ARG);
                 }
             }
         }
-        // Uniform within the group: its threads read this tile's flag after the same
-        // group barrier; a flag for tile t+1 goes to the other slot.
-        if (*reinterpret_cast<volatile int*>(&my_abort[t & 1]))
-            break;
     }
-}
-
-// Shared-memory bytes the kernel needs beyond the ring.
-__host__ __device__ constexpr int gemv_extra_smem(int rpt, int nmat)
-{
-    return 2 * NCONS_WARPS * rpt * nmat * 4 + NCONS_WARPS * 4 + 2 * MAX_RG * 4 + MAX_STAGES * 4 +
-           2 * MAX_STAGES * 8 + 16;
+    (void)gw0;
 }
 
 }  // namespace dq

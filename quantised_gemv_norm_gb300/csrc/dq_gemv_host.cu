@@ -47,7 +47,7 @@ static cudaError_t ensure_smem_attr(GemvKernel k, int bytes)
     return e;
 }
 
-int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, int planes, GemvPlan* plan)
+int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool norm, GemvPlan* plan)
 {
     if (rows < 1 || K < 1)
         return DQ_ERR_SHAPE;
@@ -118,12 +118,18 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, int planes, Ge
             break;
         }
     p.stage_bytes = p.RG * p.RPT * rb * nmat;
-    p.nstage = ring_bytes / p.stage_bytes;
-    if (p.nstage < 2)
-        p.nstage = 2;
-    if (p.nstage > dq::MAX_STAGES)
-        p.nstage = dq::MAX_STAGES;
-    p.smem_bytes = p.nstage * p.stage_bytes + dq::gemv_extra_smem(p.RPT, nmat);
+    // as many stages as fit next to the activation buffers (2 .. MAX_STAGES)
+    const dq::GemvSmem base = dq::gemv_smem_layout(fmt, K, 0, p.stage_bytes, p.RPT, nmat, pl, norm);
+    const int per_stage = p.stage_bytes + 2 * dq::NCONS_WARPS * p.RPT * nmat * 4;
+    int ns = (GEMV_SMEM_MAX - base.total) / per_stage;
+    if (ns > GEMV_RING_MAX / p.stage_bytes)
+        ns = GEMV_RING_MAX / p.stage_bytes;
+    if (ns > dq::MAX_STAGES)
+        ns = dq::MAX_STAGES;
+    if (ns < 2)
+        return DQ_ERR_UNSUPPORTED;
+    p.nstage = ns;
+    p.smem_bytes = dq::gemv_smem_layout(fmt, K, p.nstage, p.stage_bytes, p.RPT, nmat, pl, norm).total;
     p.planes = pl;
     p.kernel = kernel_for(fmt, p.UL, p.RPT, nmat, p.planes);
     if (!p.kernel)
@@ -232,7 +238,7 @@ static int gemv_entry(int fmt, const void* W, const void* x, float* y, int rows,
     if (!dqhost::aligned16(W) || !dqhost::aligned16(x))
         return DQ_ERR_ALIGN;
     dqhost::GemvPlan plan;
-    int st = dqhost::plan_gemv(fmt, rows, K, 1, dqhost::GEMV_RING_DEFAULT, 1, &plan);
+    int st = dqhost::plan_gemv(fmt, rows, K, 1, 1, false, &plan);
     if (st != DQ_OK)
         return st;
     dq::GemvArgs a{};

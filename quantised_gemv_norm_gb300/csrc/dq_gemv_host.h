@@ -27,13 +27,15 @@ struct GemvPlan {
 
 constexpr int GEMV_STAGE_TARGET = 48 * 1024;   // bytes per ring stage (upper target)
 constexpr int GEMV_STAGE_MAX = 64 * 1024;      // largest stage accepted
-constexpr int GEMV_RING_DEFAULT = 176 * 1024;  // ring bytes: one block per SM
+constexpr int GEMV_RING_MAX = 176 * 1024;      // ring bytes at most (one block per SM)
+constexpr int GEMV_SMEM_MAX = 227 * 1024;      // shared memory one block may use
 
 // Chooses the thread layout, tile and ring for one matrix shape.  `planes` = 2
 // asks for the two-plane activation where the format and layout allow it (else
-// one plane).  Returns DQ_OK, DQ_ERR_SHAPE or DQ_ERR_UNSUPPORTED.  Sets the
-// kernel's shared-memory attribute (host call, not a stream operation).
-int plan_gemv(int fmt, int rows, int K, int nmat, int ring_bytes, int planes, GemvPlan* plan);
+// one plane); `norm` reserves room for the RMSNorm weight.  Returns DQ_OK,
+// DQ_ERR_SHAPE or DQ_ERR_UNSUPPORTED.  Sets the kernel's shared-memory
+// attribute (host call, not a stream operation).
+int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool norm, GemvPlan* plan);
 
 // Fills the layout fields of `a` from the plan and launches on `stream`;
 // `pdl` adds the programmatic-stream-serialisation launch attribute.

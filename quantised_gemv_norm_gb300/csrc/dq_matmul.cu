@@ -21,7 +21,7 @@ DQ_API int dq_matmul_q4k(const void* W_blocks, const float* X, float* Y, int M, 
     if (!dqhost::aligned16(W_blocks) || !dqhost::aligned16(X) || (K % 4))
         return DQ_ERR_ALIGN;
     dqhost::GemvPlan plan;
-    int st = dqhost::plan_gemv(DQ_FMT_Q4K, rows, K, 1, dqhost::GEMV_RING_DEFAULT, 1, &plan);
+    int st = dqhost::plan_gemv(DQ_FMT_Q4K, rows, K, 1, 1, false, &plan);
     if (st != DQ_OK)
         return st;
     for (int m = 0; m < M; ++m) {
