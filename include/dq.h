@@ -129,14 +129,24 @@ DQ_API int dq_layernorm_threads(const float* x, const float* gamma, const float*
  *   The activation is carried as a 15-bit fixed-point vector with one fp32
  *   scale per 32 elements (relative error <= 2^-15 of each group's largest
  *   |x|), products are exact 32-bit integer sums, the block scales are applied
- *   in fp32.  Q4_K: K % 256 == 0, 256 <= K <= 32768.  Q6_K: K % 2048 == 0,
- *   2048 <= K <= 32768.
+ *   in fp32.  Q4_K: K % 256 == 0, 256 <= K <= 16384.  Q6_K: K % 2048 == 0,
+ *   2048 <= K <= 16384.
  * W, x 16-byte aligned (DQ_ERR_ALIGN otherwise).  y must not overlap W or x.
  * Errors: NULL -> DQ_ERR_NULL; rows < 1 or K outside the ranges -> DQ_ERR_SHAPE
  * or DQ_ERR_UNSUPPORTED. */
 DQ_API int dq_gemv_bf16(const void* W_bf16, const void* x_bf16, float* y, int rows, int K, void* stream);
 DQ_API int dq_gemv_q4k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream);
 DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream);
+
+/* Diagnostics: when `buffer` is not NULL, every later GEMV launch in this
+ * process writes 8 unsigned 64-bit values per thread block at
+ * buffer[8 * block]: global-timer ns at start, after set-up, after the
+ * dependency wait, after the activation is staged, after it is quantised,
+ * when the first weight stage is ready; then the latest warp end time and the
+ * count of finished warps (both accumulated: zero the buffer before a launch).
+ * The buffer needs 64 bytes per block (at most one block per SM).  NULL turns
+ * tracing off.  Not for use while another thread launches GEMVs. */
+DQ_API int dq_debug_trace(void* buffer);
 
 /* Dequantise nblocks consecutive blocks to fp32 (256 values per block), each
  * weight computed as the block formula above in fp32.  A test hook: with the

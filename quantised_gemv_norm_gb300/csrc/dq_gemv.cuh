@@ -70,6 +70,7 @@ struct GemvArgs {
     __half* kv_v;
     int qdim, kvdim, hd, max_ctx;
     int* err;
+    unsigned long long* trace;  // diagnostics: per-block timestamps when not null
 };
 
 // ---------------------------------------------------------- activation units
@@ -276,8 +277,10 @@ struct UnitState<FMT_BF16, PL> {
 
 // ------------------------------------------------------- shared-memory layout
 
-constexpr int XQ_WORDS_PL1 = 24;  // q[16], s, f, hsum, s32a, s32b, pad: 96 bytes
-constexpr int XQ_WORDS_PL2 = 40;  // q[16], l[16], s, f, hsum, s32a, s32b, pad: 160 bytes
+// Entry strides are odd multiples of 16 bytes so that 8 lanes reading 8
+// consecutive entries with 16-byte loads hit distinct banks.
+constexpr int XQ_WORDS_PL1 = 28;  // q[16], s, f, hsum, s32a, s32b, pad: 112 bytes
+constexpr int XQ_WORDS_PL2 = 44;  // q[16], l[16], s, f, hsum, s32a, s32b, pad: 176 bytes
 constexpr int GEMV_MISC_BYTES = 256;
 
 __host__ __device__ constexpr int xq_words(int pl) { return pl == 2 ? XQ_WORDS_PL2 : XQ_WORDS_PL1; }
@@ -404,6 +407,9 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
 
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned long long* trace = a.trace ? a.trace + 8 * blockIdx.x : nullptr;
+    if (trace && tid == 0)
+        trace[0] = globaltimer_ns();
     const int r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * a.rows / gridDim.x);
     const int r1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * a.rows / gridDim.x);
     const int R = a.RG * RPT;
@@ -430,7 +436,11 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         }
     }
     __syncthreads();
+    if (trace && tid == 0)
+        trace[1] = globaltimer_ns();
     pdl_wait();  // the activation is the previous kernel's output
+    if (trace && tid == 0)
+        trace[2] = globaltimer_ns();
 
     const int P = a.P;
     const int g = tid / P;
@@ -461,6 +471,8 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         bool ok = mbar_wait(xbar, 0);
         if (norm)
             ok = mbar_wait(gbar, 0) && ok;
+        if (trace && tid == 0)
+            trace[3] = globaltimer_ns();
         if (!ok) {
             set_error(a.err, DEVERR_TIMEOUT_FULL);
             abort_flag[0] = 1;
@@ -473,6 +485,8 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
                 gred[warp] = ss;
         }
         __syncthreads();  // xq and gred complete
+        if (trace && tid == 0)
+            trace[4] = globaltimer_ns();
         if (norm) {
             float tot = 0.f;
             for (int w = 0; w < NCONS_WARPS; ++w)
@@ -515,6 +529,8 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             abort_flag[0] = 1;
             break;
         }
+        if (trace && t == 0 && tid == 0)
+            trace[5] = globaltimer_ns();
         const uint8_t* tile = smem + static_cast<size_t>(s) * a.stage_bytes;
         const int row0 = r0 + t * R;
         const int nr = min(R, r1 - row0);
@@ -608,6 +624,10 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         }
     }
     (void)gw0;
+    if (trace && lane == 0) {  // the last warp of the block to finish records the end
+        atomicMax(trace + 6, globaltimer_ns());
+        atomicAdd(trace + 7, 1ull);
+    }
 }
 
 }  // namespace dq

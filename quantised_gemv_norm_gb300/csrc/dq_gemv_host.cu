@@ -147,8 +147,13 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool norm, GemvPla
     return DQ_OK;
 }
 
+static unsigned long long* g_trace = nullptr;
+
+void set_gemv_trace(void* buf) { g_trace = static_cast<unsigned long long*>(buf); }
+
 cudaError_t launch_gemv(const GemvPlan& plan, dq::GemvArgs a, cudaStream_t stream, bool pdl)
 {
+    a.trace = g_trace;
     a.rows = plan.rows;
     a.K = plan.K;
     a.row_bytes = plan.row_bytes;
@@ -256,6 +261,12 @@ static int gemv_entry(int fmt, const void* W, const void* x, float* y, int rows,
 
 extern "C" {
 
+DQ_API int dq_debug_trace(void* buffer)
+{
+    dqhost::set_gemv_trace(buffer);
+    return DQ_OK;
+}
+
 DQ_API int dq_gemv_bf16(const void* W_bf16, const void* x_bf16, float* y, int rows, int K, void* stream)
 {
     if (K > 24576)
@@ -265,14 +276,14 @@ DQ_API int dq_gemv_bf16(const void* W_bf16, const void* x_bf16, float* y, int ro
 
 DQ_API int dq_gemv_q4k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream)
 {
-    if (K > 32768)
+    if (K > 16384)
         return DQ_ERR_UNSUPPORTED;
     return gemv_entry(DQ_FMT_Q4K, W_blocks, x, y, rows, K, stream);
 }
 
 DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream)
 {
-    if (K > 32768)
+    if (K > 16384)
         return DQ_ERR_UNSUPPORTED;
     return gemv_entry(DQ_FMT_Q6K, W_blocks, x, y, rows, K, stream);
 }

@@ -41,4 +41,9 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool norm, GemvPla
 // `pdl` adds the programmatic-stream-serialisation launch attribute.
 cudaError_t launch_gemv(const GemvPlan& plan, dq::GemvArgs a, cudaStream_t stream, bool pdl);
 
+// Diagnostics: GEMV launches record per-block timestamps into `buf` (8 x 64-bit
+// per block: start, set-up done, dependency released, activation staged,
+// activation quantised, first stage ready, end, blocks finished); NULL stops.
+void set_gemv_trace(void* buf);
+
 }  // namespace dqhost

@@ -16,7 +16,7 @@ DQ_API int dq_matmul_q4k(const void* W_blocks, const float* X, float* Y, int M, 
         return DQ_ERR_NULL;
     if (M < 1 || M > 64 || rows < 1)
         return DQ_ERR_SHAPE;
-    if (K > 32768)
+    if (K > 16384)
         return DQ_ERR_UNSUPPORTED;
     if (!dqhost::aligned16(W_blocks) || !dqhost::aligned16(X) || (K % 4))
         return DQ_ERR_ALIGN;

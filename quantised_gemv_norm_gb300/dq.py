@@ -29,6 +29,7 @@ SIGNATURES = {
     "dq_layernorm": (I, [P, P, P, P, I, I, F, P]),
     "dq_rmsnorm_threads": (I, [P, P, P, I, I, F, I, P]),
     "dq_layernorm_threads": (I, [P, P, P, P, I, I, F, I, P]),
+    "dq_debug_trace": (I, [P]),
     "dq_gemv_bf16": (I, [P, P, P, I, I, P]),
     "dq_gemv_q4k": (I, [P, P, P, I, I, P]),
     "dq_gemv_q6k": (I, [P, P, P, I, I, P]),

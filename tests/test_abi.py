@@ -56,7 +56,7 @@ def test_argument_errors_return_before_launch(lib):
     fake = P(16)  # never dereferenced: checks fail first
     assert lib.dq_gemv_q4k(None, fake, fake, 4, 256, None) == -1
     assert lib.dq_gemv_q4k(P(17), fake, fake, 4, 256, None) == -3          # misaligned W
-    assert lib.dq_gemv_q4k(fake, fake, fake, 4, 40000, None) == -4        # K too large
+    assert lib.dq_gemv_q4k(fake, fake, fake, 4, 16640, None) == -4        # K too large
     assert lib.dq_gemv_q6k(fake, fake, fake, 4, 40000, None) == -4
     assert lib.dq_gemv_bf16(fake, fake, fake, 4, 30000, None) == -4
     assert lib.dq_rmsnorm(None, fake, fake, 1, 8, 1e-6, None) == -1

@@ -115,7 +115,7 @@ def test_gemv_bf16(dq, orc, rows, K):
     assert normwise(y, r) <= GEMV_TOL
 
 
-Q4K_SHAPES = [(300, 4096), (1, 4096), (37, 256), (129, 768), (257, 2048), (64, 12288), (8, 32768),
+Q4K_SHAPES = [(300, 4096), (1, 4096), (37, 256), (129, 768), (257, 2048), (64, 12288), (8, 16384),
               (12288, 4096), (4096, 4096), (6144, 4096), (4096, 12288)]
 
 
@@ -128,7 +128,7 @@ def test_gemv_q4k(dq, orc, rows, K):
     assert normwise(y, r) <= GEMV_TOL
 
 
-Q6K_SHAPES = [(300, 4096), (1, 2048), (77, 6144), (4096, 12288), (151936, 4096), (5, 32768)]
+Q6K_SHAPES = [(300, 4096), (1, 2048), (77, 6144), (4096, 12288), (151936, 4096), (5, 16384)]
 
 
 @pytest.mark.parametrize("rows,K", Q6K_SHAPES)
