@@ -237,14 +237,14 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
     int st;
     // The q|k|v and O projections feed the attention, which amplifies input
     // errors: they take the two-plane (about 30-bit) activation.
-    if ((st = dqhost::plan_gemv(DQ_FMT_Q4K, qdim + 2 * kvdim, d->hidden, 1, 2, true, &m->p_qkv)) != DQ_OK ||
-        (st = dqhost::plan_gemv(DQ_FMT_Q4K, d->hidden, qdim, 1, 2, false, &m->p_o)) != DQ_OK ||
-        (st = dqhost::plan_gemv(DQ_FMT_Q4K, d->ffn, d->hidden, 2, 1, true, &m->p_gateup)) != DQ_OK ||
+    if ((st = dqhost::plan_gemv(DQ_FMT_Q4K, qdim + 2 * kvdim, d->hidden, 1, 2, false, &m->p_qkv)) != DQ_OK ||
+        (st = dqhost::plan_gemv(DQ_FMT_Q4K, d->hidden, qdim, 1, 2, true, &m->p_o)) != DQ_OK ||
+        (st = dqhost::plan_gemv(DQ_FMT_Q4K, d->ffn, d->hidden, 2, 1, false, &m->p_gateup)) != DQ_OK ||
         (m->have_down_q4 &&
-         (st = dqhost::plan_gemv(DQ_FMT_Q4K, d->hidden, d->ffn, 1, 1, false, &m->p_down_q4)) != DQ_OK) ||
+         (st = dqhost::plan_gemv(DQ_FMT_Q4K, d->hidden, d->ffn, 1, 1, true, &m->p_down_q4)) != DQ_OK) ||
         (m->have_down_q6 &&
-         (st = dqhost::plan_gemv(DQ_FMT_Q6K, d->hidden, d->ffn, 1, 1, false, &m->p_down_q6)) != DQ_OK) ||
-        (st = dqhost::plan_gemv(DQ_FMT_Q6K, d->vocab, d->hidden, 1, 1, true, &m->p_vocab)) != DQ_OK) {
+         (st = dqhost::plan_gemv(DQ_FMT_Q6K, d->hidden, d->ffn, 1, 1, true, &m->p_down_q6)) != DQ_OK) ||
+        (st = dqhost::plan_gemv(DQ_FMT_Q6K, d->vocab, d->hidden, 1, 1, false, &m->p_vocab)) != DQ_OK) {
         free_model(m);
         return st;
     }

@@ -69,6 +69,7 @@ struct GemvArgs {
     __half* kv_k;       // EPI_QKV: this layer's K plane [n_kv][max_ctx][hd]
     __half* kv_v;
     int qdim, kvdim, hd, max_ctx;
+    int resid_rows;             // EPI_RESID: shared-memory slots for the block's residual rows
     int* err;
     unsigned long long* trace;  // diagnostics: per-block timestamps when not null
 };
@@ -285,6 +286,56 @@ constexpr int GEMV_MISC_BYTES = 256;
 
 __host__ __device__ constexpr int xq_words(int pl) { return pl == 2 ? XQ_WORDS_PL2 : XQ_WORDS_PL1; }
 
+// Offsets of the block's shared-memory regions: the weight ring, the quantised
+// activation (one entry per 32-element unit), the block's residual rows, the
+// per-warp partial sums and the barriers.
+struct GemvSmem {
+    int xq, resid, red, misc, total;
+};
+
+__host__ __device__ inline GemvSmem gemv_smem_layout(int fmt, int K, int nstage, int stage_bytes, int rpt, int nmat,
+                                                     int pl, int resid_rows)
+{
+    GemvSmem L;
+    int o = nstage * stage_bytes;
+    L.xq = o;
+    if (fmt != FMT_BF16)
+        o += (K / 32) * xq_words(pl) * 4;
+    L.resid = o;
+    o += ((resid_rows * 4 + 15) / 16) * 16;
+    L.red = o;
+    o += 2 * nstage * NCONS_WARPS * rpt * nmat * 4;
+    L.misc = o;
+    o += GEMV_MISC_BYTES;
+    L.total = o;
+    return L;
+}
+
+// Largest number of 4-element activation chunks one thread quantises (K <= 16384).
+constexpr int GEMV_MAX_K = 16384;
+constexpr int QCHUNKS = GEMV_MAX_K / 4 / NCONS;
+
+// ------------------------------------------------------------------ kernel
+
+template <int FMT, int PL>
+struct UnitState {
+    XQ<PL> x;
+};
+template <int PL>
+struct UnitState<FMT_BF16, PL> {
+    uint32_t xb[4];
+};
+
+// ------------------------------------------------------- shared-memory layout
+
+// Entry strides are odd multiples of 16 bytes so that 8 lanes reading 8
+// consecutive entries with 16-byte loads hit distinct banks.
+constexpr int XQ_WORDS_PL1 = 28;  // q[16], s, f, hsum, s32a, s32b, pad: 112 bytes
+constexpr int XQ_WORDS_PL2 = 44;  // q[16], l[16], s, f, hsum, s32a, s32b, pad: 176 bytes
+constexpr int GEMV_MISC_BYTES = 256;
+
+__host__ __device__ constexpr int xq_words(int pl) { return pl == 2 ? XQ_WORDS_PL2 : XQ_WORDS_PL1; }
+
 // Offsets of the block's shared-memory regions: the weight ring, the staged
 // activation and RMSNorm weight, the quantised activation (one entry per
 // 32-element unit), the per-warp partial sums and the barriers.
@@ -333,42 +384,44 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, uint8_t* smem, uin
                  &full[s], pol);
 }
 
-// Quantise the staged activation (times gamma under RMSNorm) once per block:
-// eight lanes share one 32-element unit, four elements each.  Returns this
-// thread's partial sum of x^2.
+// Quantise the activation (times gamma under RMSNorm) once per block: eight
+// lanes share one 32-element unit, four elements each; chunk c = tid + NCONS i
+// of the vector is v[i].  Returns this thread's partial sum of x^2.
 template <int FMT, int PL>
-__device__ __forceinline__ float quantise_block(const float* xs, const float* gs, bool norm, uint32_t* xq, int K,
-                                                int tid)
+__device__ __forceinline__ float quantise_block(float4 (&v)[QCHUNKS], const float4 (&gv)[QCHUNKS], bool norm,
+                                                uint32_t* xq, int K, int tid)
 {
     float ss = 0.f;
     const int nchunks = K / 4;  // a multiple of 64: whole warps take part in each pass
-    for (int c = tid; c < nchunks; c += NCONS) {
-        float4 v = reinterpret_cast<const float4*>(xs)[c];
+#pragma unroll
+    for (int i = 0; i < QCHUNKS; ++i) {
+        const int c = tid + NCONS * i;
+        if (c >= nchunks)
+            break;
+        float4 h = v[i];
         if (norm) {
-            ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
-            const float4 gv = reinterpret_cast<const float4*>(gs)[c];
-            v.x *= gv.x; v.y *= gv.y; v.z *= gv.z; v.w *= gv.w;
+            ss = fmaf(h.x, h.x, ss); ss = fmaf(h.y, h.y, ss); ss = fmaf(h.z, h.z, ss); ss = fmaf(h.w, h.w, ss);
+            h.x *= gv[i].x; h.y *= gv[i].y; h.z *= gv[i].z; h.w *= gv[i].w;
         }
-        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-        float hs = (v.x + v.y) + (v.z + v.w);
+        float amax = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
+        float hs = (h.x + h.y) + (h.z + h.w);
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) {
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
             hs += __shfl_xor_sync(0xffffffffu, hs, o);
         }
         const float inv = amax > 0.f ? XQ_MAX / amax : 0.f;
-        const float t0 = v.x * inv, t1 = v.y * inv, t2 = v.z * inv, t3 = v.w * inv;
+        const float t0 = h.x * inv, t1 = h.y * inv, t2 = h.z * inv, t3 = h.w * inv;
         const int a0 = __float2int_rn(t0), a1 = __float2int_rn(t1), a2 = __float2int_rn(t2), a3 = __float2int_rn(t3);
         const int e = c & 7;
         uint32_t* q = xq + (c >> 3) * xq_words(PL);
-        q[2 * e] = pack16x2(a0, a1);
-        q[2 * e + 1] = pack16x2(a2, a3);
-        if (PL == 2) {  // remainders: t - a is exact in fp32
-            q[16 + 2 * e] = pack16x2(__float2int_rn((t0 - static_cast<float>(a0)) * 32768.0f),
-                                     __float2int_rn((t1 - static_cast<float>(a1)) * 32768.0f));
-            q[16 + 2 * e + 1] = pack16x2(__float2int_rn((t2 - static_cast<float>(a2)) * 32768.0f),
-                                         __float2int_rn((t3 - static_cast<float>(a3)) * 32768.0f));
-        }
+        *reinterpret_cast<uint2*>(q + 2 * e) = make_uint2(pack16x2(a0, a1), pack16x2(a2, a3));
+        if (PL == 2)  // remainders: t - a is exact in fp32
+            *reinterpret_cast<uint2*>(q + 16 + 2 * e) =
+                make_uint2(pack16x2(__float2int_rn((t0 - static_cast<float>(a0)) * 32768.0f),
+                                    __float2int_rn((t1 - static_cast<float>(a1)) * 32768.0f)),
+                           pack16x2(__float2int_rn((t2 - static_cast<float>(a2)) * 32768.0f),
+                                    __float2int_rn((t3 - static_cast<float>(a3)) * 32768.0f)));
         int isum = (a0 + a1) + (a2 + a3);  // the two 16-element halves of the unit (Q6_K offsets)
         isum += __shfl_xor_sync(0xffffffffu, isum, 1);
         isum += __shfl_xor_sync(0xffffffffu, isum, 2);
@@ -392,18 +445,17 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
     constexpr int NV = RPT * NMAT;
     extern __shared__ __align__(128) uint8_t smem[];
     const bool norm = a.pro == PRO_RMS;
-    const GemvSmem L = gemv_smem_layout(FMT, a.K, a.nstage, a.stage_bytes, RPT, NMAT, PL, norm);
-    float* xs = reinterpret_cast<float*>(smem + L.x);
-    float* gs = reinterpret_cast<float*>(smem + L.g);
+    const GemvSmem L = gemv_smem_layout(FMT, a.K, a.nstage, a.stage_bytes, RPT, NMAT, PL, a.resid_rows);
     uint32_t* xq = reinterpret_cast<uint32_t*>(smem + L.xq);
+    float* resid = reinterpret_cast<float*>(smem + L.resid);
     float* red = reinterpret_cast<float*>(smem + L.red);            // [2 nstage][16 warps][NV]
     int* release = reinterpret_cast<int*>(smem + L.misc);           // [MAX_STAGES]
     int* abort_flag = release + MAX_STAGES;                         // [4]
     float* gred = reinterpret_cast<float*>(abort_flag + 4);         // [16]
     uint64_t* full = reinterpret_cast<uint64_t*>(gred + NCONS_WARPS);  // [MAX_STAGES]
     uint64_t* empty = full + MAX_STAGES;                            // [MAX_STAGES]
-    uint64_t* xbar = empty + MAX_STAGES;
-    uint64_t* gbar = xbar + 1;
+    float** step_logits = reinterpret_cast<float**>(empty + MAX_STAGES);
+    int* step_pos = reinterpret_cast<int*>(step_logits + 1);
 
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -423,16 +475,21 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             mbar_init(&empty[s], NCONS_WARPS);
             release[s] = 0;
         }
-        mbar_init(xbar, 1);
-        mbar_init(gbar, 1);
         abort_flag[0] = 0;
         fence_mbar_init();
         // weights and the norm weight never depend on the previous kernel
         for (int t = 0; t < min(a.nstage, ntiles); ++t)
             issue_tile<NMAT>(a, smem, full, t, r0, r1, R, pol);
-        if (quant && norm) {
-            mbar_arrive_expect_tx(gbar, static_cast<uint32_t>(a.K * 4));
-            bulk_g2s_plain(gs, a.gamma, static_cast<uint32_t>(a.K * 4), gbar);
+    }
+    // the norm weight never depends on the previous kernel either
+    float4 gv[QCHUNKS], xv[QCHUNKS];
+    if (quant) {
+#pragma unroll
+        for (int i = 0; i < QCHUNKS; ++i) {
+            const int c = tid + NCONS * i;
+            gv[i] = make_float4(1.f, 1.f, 1.f, 1.f);
+            if (norm && c < a.K / 4)
+                gv[i] = __ldg(reinterpret_cast<const float4*>(a.gamma) + c);
         }
     }
     __syncthreads();
@@ -441,6 +498,15 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
     pdl_wait();  // the activation is the previous kernel's output
     if (trace && tid == 0)
         trace[2] = globaltimer_ns();
+
+    // everything the epilogue needs from global memory, loaded once
+    if (tid == 0) {
+        *step_logits = a.y_from_step ? a.step->logits : a.y;
+        *step_pos = a.epi == EPI_QKV ? a.step->pos : 0;
+    }
+    if (a.epi == EPI_RESID)
+        for (int r = tid; r < r1 - r0; r += NCONS)
+            resid[r] = __ldcg(a.y + r0 + r);
 
     const int P = a.P;
     const int g = tid / P;
@@ -463,21 +529,17 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             uint32_t* xb = reinterpret_cast<uint32_t*>(&us[k]);
             xb[0] = v.x; xb[1] = v.y; xb[2] = v.z; xb[3] = v.w;
         }
+        __syncthreads();  // step fields and residual rows
     } else {
-        if (tid == 0) {
-            mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(a.K * 4));
-            bulk_g2s_plain(xs, a.x, static_cast<uint32_t>(a.K * 4), xbar);
+#pragma unroll
+        for (int i = 0; i < QCHUNKS; ++i) {
+            const int c = tid + NCONS * i;
+            if (c < a.K / 4)
+                xv[i] = __ldcg(reinterpret_cast<const float4*>(a.x) + c);
         }
-        bool ok = mbar_wait(xbar, 0);
-        if (norm)
-            ok = mbar_wait(gbar, 0) && ok;
         if (trace && tid == 0)
             trace[3] = globaltimer_ns();
-        if (!ok) {
-            set_error(a.err, DEVERR_TIMEOUT_FULL);
-            abort_flag[0] = 1;
-        }
-        float ss = quantise_block<FMT, PL>(xs, gs, norm, xq, a.K, tid);
+        float ss = quantise_block<FMT, PL>(xv, gv, norm, xq, a.K, tid);
         float rstd = 1.f;
         if (norm) {
             ss = warp_sum(ss);
@@ -600,10 +662,9 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             }
             const int r = row0 + row;
             if (a.epi == EPI_STORE) {
-                float* out = a.y_from_step ? a.step->logits : a.y;
-                out[r] = v0;
+                (*step_logits)[r] = v0;
             } else if (a.epi == EPI_RESID) {
-                a.y[r] += v0;
+                a.y[r] = resid[r - r0] + v0;
             } else if (a.epi == EPI_SWIGLU) {
                 a.y[r] = v0 / (1.0f + expf(-v0)) * v1;
             } else {  // EPI_QKV
@@ -614,7 +675,7 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
                     const int which = idx / a.kvdim, rem = idx - which * a.kvdim;
                     const int kvh = rem / a.hd, dd = rem - kvh * a.hd;
                     __half* plane = which ? a.kv_v : a.kv_k;
-                    const int pos = a.step->pos;
+                    const int pos = *step_pos;
                     if (pos >= 0 && pos < a.max_ctx)
                         plane[(static_cast<size_t>(kvh) * a.max_ctx + pos) * a.hd + dd] = __float2half_rn(v0);
                     else

@@ -47,7 +47,7 @@ static cudaError_t ensure_smem_attr(GemvKernel k, int bytes)
     return e;
 }
 
-int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool norm, GemvPlan* plan)
+int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool resid, GemvPlan* plan)
 {
     if (rows < 1 || K < 1)
         return DQ_ERR_SHAPE;
@@ -58,6 +58,8 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool norm, GemvPla
         return DQ_ERR_SHAPE;
     if (fmt == DQ_FMT_Q6K && K % 2048)
         return DQ_ERR_ALIGN;  // 210-byte blocks: rows are 16-byte aligned only when K % 2048 == 0
+    if (fmt != DQ_FMT_BF16 && K > dq::GEMV_MAX_K)
+        return DQ_ERR_UNSUPPORTED;
     const int U = K / unit_w;
     const int rb = row_bytes_of(fmt, K);
     const int pl = (planes == 2 && fmt == DQ_FMT_Q4K) ? 2 : 1;
@@ -119,7 +121,8 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool norm, GemvPla
         }
     p.stage_bytes = p.RG * p.RPT * rb * nmat;
     // as many stages as fit next to the activation buffers (2 .. MAX_STAGES)
-    const dq::GemvSmem base = dq::gemv_smem_layout(fmt, K, 0, p.stage_bytes, p.RPT, nmat, pl, norm);
+    p.resid_rows = resid ? (rows + p.grid - 1) / p.grid : 0;
+    const dq::GemvSmem base = dq::gemv_smem_layout(fmt, K, 0, p.stage_bytes, p.RPT, nmat, pl, p.resid_rows);
     const int per_stage = p.stage_bytes + 2 * dq::NCONS_WARPS * p.RPT * nmat * 4;
     int ns = (GEMV_SMEM_MAX - base.total) / per_stage;
     if (ns > GEMV_RING_MAX / p.stage_bytes)
@@ -129,7 +132,7 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool norm, GemvPla
     if (ns < 2)
         return DQ_ERR_UNSUPPORTED;
     p.nstage = ns;
-    p.smem_bytes = dq::gemv_smem_layout(fmt, K, p.nstage, p.stage_bytes, p.RPT, nmat, pl, norm).total;
+    p.smem_bytes = dq::gemv_smem_layout(fmt, K, p.nstage, p.stage_bytes, p.RPT, nmat, pl, p.resid_rows).total;
     p.planes = pl;
     p.kernel = kernel_for(fmt, p.UL, p.RPT, nmat, p.planes);
     if (!p.kernel)
@@ -161,6 +164,7 @@ cudaError_t launch_gemv(const GemvPlan& plan, dq::GemvArgs a, cudaStream_t strea
     a.RG = plan.RG;
     a.nstage = plan.nstage;
     a.stage_bytes = plan.stage_bytes;
+    a.resid_rows = plan.resid_rows;
     if (!a.err)
         a.err = device_error_flag();
     cudaLaunchConfig_t cfg = {};

@@ -22,6 +22,7 @@ struct GemvPlan {
     int nstage, stage_bytes;
     int smem_bytes;
     int grid;
+    int resid_rows;  // shared-memory slots for residual rows (EPI_RESID), else 0
     GemvKernel kernel;
 };
 
@@ -32,10 +33,10 @@ constexpr int GEMV_SMEM_MAX = 227 * 1024;      // shared memory one block may us
 
 // Chooses the thread layout, tile and ring for one matrix shape.  `planes` = 2
 // asks for the two-plane activation where the format and layout allow it (else
-// one plane); `norm` reserves room for the RMSNorm weight.  Returns DQ_OK,
-// DQ_ERR_SHAPE or DQ_ERR_UNSUPPORTED.  Sets the kernel's shared-memory
-// attribute (host call, not a stream operation).
-int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool norm, GemvPlan* plan);
+// one plane); `resid` reserves room for the block's residual rows (the
+// EPI_RESID epilogue).  Returns DQ_OK, DQ_ERR_SHAPE or DQ_ERR_UNSUPPORTED.
+// Sets the kernel's shared-memory attribute (host call, not a stream operation).
+int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool resid, GemvPlan* plan);
 
 // Fills the layout fields of `a` from the plan and launches on `stream`;
 // `pdl` adds the programmatic-stream-serialisation launch attribute.
