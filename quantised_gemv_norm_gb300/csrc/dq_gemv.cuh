@@ -317,57 +317,6 @@ constexpr int QCHUNKS = GEMV_MAX_K / 4 / NCONS;
 
 // ------------------------------------------------------------------ kernel
 
-template <int FMT, int PL>
-struct UnitState {
-    XQ<PL> x;
-};
-template <int PL>
-struct UnitState<FMT_BF16, PL> {
-    uint32_t xb[4];
-};
-
-// ------------------------------------------------------- shared-memory layout
-
-// Entry strides are odd multiples of 16 bytes so that 8 lanes reading 8
-// consecutive entries with 16-byte loads hit distinct banks.
-constexpr int XQ_WORDS_PL1 = 28;  // q[16], s, f, hsum, s32a, s32b, pad: 112 bytes
-constexpr int XQ_WORDS_PL2 = 44;  // q[16], l[16], s, f, hsum, s32a, s32b, pad: 176 bytes
-constexpr int GEMV_MISC_BYTES = 256;
-
-__host__ __device__ constexpr int xq_words(int pl) { return pl == 2 ? XQ_WORDS_PL2 : XQ_WORDS_PL1; }
-
-// Offsets of the block's shared-memory regions: the weight ring, the staged
-// activation and RMSNorm weight, the quantised activation (one entry per
-// 32-element unit), the per-warp partial sums and the barriers.
-struct GemvSmem {
-    int x, g, xq, red, misc, total;
-};
-
-__host__ __device__ inline GemvSmem gemv_smem_layout(int fmt, int K, int nstage, int stage_bytes, int rpt, int nmat,
-                                                     int pl, bool norm)
-{
-    GemvSmem L;
-    int o = nstage * stage_bytes;
-    L.x = L.g = L.xq = o;
-    if (fmt != FMT_BF16) {
-        L.x = o;
-        o += K * 4;
-        L.g = o;
-        if (norm)
-            o += K * 4;
-        L.xq = o;
-        o += (K / 32) * xq_words(pl) * 4;
-    }
-    L.red = o;
-    o += 2 * nstage * NCONS_WARPS * rpt * nmat * 4;
-    L.misc = o;
-    o += GEMV_MISC_BYTES;
-    L.total = o;
-    return L;
-}
-
-// ------------------------------------------------------------------ kernel
-
 template <int NMAT>
 __device__ __forceinline__ void issue_tile(const GemvArgs& a, uint8_t* smem, uint64_t* full, int t, int r0, int r1,
                                            int R, uint64_t pol)
