@@ -317,19 +317,21 @@ constexpr int QCHUNKS = GEMV_MAX_K / 4 / NCONS;
 
 // ------------------------------------------------------------------ kernel
 
+// Stream tile t (rows r0 + t R .. ) of the block's rows into its ring slot.
 template <int NMAT>
-__device__ __forceinline__ void issue_tile(const GemvArgs& a, uint8_t* smem, uint64_t* full, int t, int r0, int r1,
+__device__ __forceinline__ void issue_tile(const uint8_t* W, const uint8_t* W2, int row_bytes, int nstage,
+                                           int stage_bytes, uint8_t* smem, uint64_t* full, int t, int r0, int r1,
                                            int R, uint64_t pol)
 {
-    const int s = t % a.nstage;
+    const int s = t % nstage;
     const int row = r0 + t * R;
     const int nr = min(R, r1 - row);
-    const uint32_t bytes = static_cast<uint32_t>(nr * a.row_bytes);
-    uint8_t* dst = smem + static_cast<size_t>(s) * a.stage_bytes;
+    const uint32_t bytes = static_cast<uint32_t>(nr * row_bytes);
+    uint8_t* dst = smem + static_cast<size_t>(s) * stage_bytes;
     mbar_arrive_expect_tx(&full[s], bytes * NMAT);
-    bulk_g2s(dst, a.W + static_cast<size_t>(row) * a.row_bytes, bytes, &full[s], pol);
+    bulk_g2s(dst, W + static_cast<size_t>(row) * row_bytes, bytes, &full[s], pol);
     if (NMAT == 2)
-        bulk_g2s(dst + static_cast<size_t>(R) * a.row_bytes, a.W2 + static_cast<size_t>(row) * a.row_bytes, bytes,
+        bulk_g2s(dst + static_cast<size_t>(R) * row_bytes, W2 + static_cast<size_t>(row) * row_bytes, bytes,
                  &full[s], pol);
 }
 
@@ -389,8 +391,11 @@ __device__ __forceinline__ float quantise_block(float4 (&v)[QCHUNKS], const floa
 }
 
 template <int FMT, int UL, int RPT, int NMAT, int PL>
-__global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ GemvArgs a)
+__global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ GemvArgs args)
 {
+    // A private copy: its fields live in registers.  (Taking the address of the
+    // parameter would turn every field access into a memory load.)
+    const GemvArgs a = args;
     constexpr int NV = RPT * NMAT;
     extern __shared__ __align__(128) uint8_t smem[];
     const bool norm = a.pro == PRO_RMS;
@@ -428,7 +433,7 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         fence_mbar_init();
         // weights and the norm weight never depend on the previous kernel
         for (int t = 0; t < min(a.nstage, ntiles); ++t)
-            issue_tile<NMAT>(a, smem, full, t, r0, r1, R, pol);
+            issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, t, r0, r1, R, pol);
     }
     // the norm weight never depends on the previous kernel either
     float4 gv[QCHUNKS], xv[QCHUNKS];
@@ -598,7 +603,8 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         if (lane == 0) {
             release[s] = 0;
             if (t + a.nstage < ntiles)
-                issue_tile<NMAT>(a, smem, full, t + a.nstage, r0, r1, R, pol);
+                issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, t + a.nstage, r0, r1,
+                                 R, pol);
         }
         for (int row = lane; row < nr; row += 32) {
             const int rg = row % a.RG, i = row / a.RG;
