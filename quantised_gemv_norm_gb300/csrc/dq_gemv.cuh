@@ -9,18 +9,20 @@
 // Structure of one thread block (1 per SM, 512 threads, 16 warps):
 //   * the block's rows stream, R rows per stage, into a ring of shared-memory
 //     stages with 1-D bulk (TMA) copies that complete on an mbarrier (L2
-//     evict-first: weights are read once).  Thread 0 issues the first ring-full
-//     at kernel start; afterwards the last warp to release a stage refills it
-//     (an mbarrier counts the releases, a shared counter elects the refiller);
-//   * all 16 warps consume.  They are split into RG independent row
-//     groups of P threads; within a group each thread owns UL fixed 32-weight
-//     units of the K axis (16-byte units for bf16), so its slice of the
-//     activation is loaded, normalised and quantised once, into registers;
+//     evict-first: weights are read once).  Thread 0 issues the first
+//     ring-full at kernel start;
+//   * all 16 warps consume every stage.  They are split into RG row groups of
+//     P threads; within a group each thread owns UL fixed 32-weight units of
+//     the K axis (16-byte units for bf16), so its slice of the activation is
+//     held in registers, quantised once per block;
 //   * per stage each thread forms its unit dot products for RPT rows of its
-//     group, the group reduces them (transpose-reduce in the warp, then shared
-//     memory across the group's warps behind a named barrier of the group only)
-//     and lanes of the group's first warp run the epilogue.  Groups never wait
-//     for each other; each warp releases a stage on its own.
+//     group, the warp reduces them (transpose-reduce) into shared memory and
+//     releases the stage with an mbarrier arrive (no waiting);
+//   * stage t is completed by warp t % 16 a couple of stages later: it waits
+//     for the stage's release phase (normally already complete), refills the
+//     slot with stage t + nstage and runs the epilogue of the stage's rows
+//     from the warps' partial sums.  No warp waits for another on the common
+//     path, and the extra work rotates over the warps.
 // The first ring-full is issued before griddepcontrol.wait: weights never depend
 // on the previous kernel, so under programmatic dependent launch the ring fills
 // while the previous kernel drains.  Activations are read only after the wait.
@@ -403,9 +405,7 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
     uint32_t* xq = reinterpret_cast<uint32_t*>(smem + L.xq);
     float* resid = reinterpret_cast<float*>(smem + L.resid);
     float* red = reinterpret_cast<float*>(smem + L.red);            // [2 nstage][16 warps][NV]
-    int* release = reinterpret_cast<int*>(smem + L.misc);           // [MAX_STAGES]
-    int* abort_flag = release + MAX_STAGES;                         // [4]
-    float* gred = reinterpret_cast<float*>(abort_flag + 4);         // [16]
+    float* gred = reinterpret_cast<float*>(smem + L.misc + 48);     // [16] (48 bytes reserved)
     uint64_t* full = reinterpret_cast<uint64_t*>(gred + NCONS_WARPS);  // [MAX_STAGES]
     uint64_t* empty = full + MAX_STAGES;                            // [MAX_STAGES]
     float** step_logits = reinterpret_cast<float**>(empty + MAX_STAGES);
@@ -427,9 +427,7 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         for (int s = 0; s < a.nstage; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], NCONS_WARPS);
-            release[s] = 0;
         }
-        abort_flag[0] = 0;
         fence_mbar_init();
         // weights and the norm weight never depend on the previous kernel
         for (int t = 0; t < min(a.nstage, ntiles); ++t)
@@ -536,76 +534,22 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         }
     }
 
-    for (int t = 0; t < ntiles; ++t) {
-        if (*reinterpret_cast<volatile int*>(abort_flag))
-            break;  // no block-wide barrier follows: warps may leave independently
-        const int s = t % a.nstage;
-        if (!mbar_wait(&full[s], (t / a.nstage) & 1)) {
-            set_error(a.err, DEVERR_TIMEOUT_FULL);
-            abort_flag[0] = 1;
-            break;
-        }
-        if (trace && t == 0 && tid == 0)
-            trace[5] = globaltimer_ns();
-        const uint8_t* tile = smem + static_cast<size_t>(s) * a.stage_bytes;
-        const int row0 = r0 + t * R;
-        const int nr = min(R, r1 - row0);
-        float acc[NV];
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-            acc[v] = 0.f;
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-            const int row = g + a.RG * i;
-            if (row < nr) {
-#pragma unroll
-                for (int m = 0; m < NMAT; ++m) {
-                    const uint8_t* rp = tile + static_cast<size_t>(m * R + row) * a.row_bytes;
-                    float sum = 0.f;
-#pragma unroll
-                    for (int k = 0; k < UL; ++k) {
-                        if (have[k]) {
-                            const int n = p + P * k;
-                            if (FMT == FMT_Q4K)
-                                sum += q4k_unit<PL>(rp, n, reinterpret_cast<const XQ<PL>&>(us[k]));
-                            else if (FMT == FMT_Q6K)
-                                sum += q6k_unit(rp, n, reinterpret_cast<const XQ<1>&>(us[k]));
-                            else
-                                sum += bf16_unit(rp, n, reinterpret_cast<const uint32_t(&)[4]>(us[k]));
-                        }
-                    }
-                    acc[m * RPT + i] = sum;
-                }
-            }
-        }
-        // warp partial sums of this tile's rows -> shared memory
-        warp_transpose_reduce<NV>(acc, lane);
-        float* rb = red + (t % (2 * a.nstage)) * NCONS_WARPS * NV;
-        if ((lane & (32 / NV - 1)) == 0)
-            rb[warp * NV + lane / (32 / NV)] = acc[0];
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {  // release the stage (mbarrier arrive = release); count the releases
-            mbar_arrive(&empty[s]);
-            last = atomicAdd(&release[s], 1) == NCONS_WARPS - 1;
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (!last)
-            continue;
-        // The last warp to release: every warp has arrived, so acquire the stage's
-        // phase (this also makes the other warps' partial sums visible), refill the
-        // slot, then finish the tile's rows.
-        if (!mbar_wait(&empty[s], (t / a.nstage) & 1)) {
+    // Tile t is completed (its slot refilled, its rows' epilogue run) by warp
+    // t % 16, DEFER tiles later, when every warp has normally released it: no
+    // warp waits for another on the common path.
+    const int DEFER = a.nstage >= 4 ? 2 : 1;
+    auto complete = [&](int tc) -> bool {
+        const int sc = tc % a.nstage;
+        if (!mbar_wait(&empty[sc], (tc / a.nstage) & 1)) {  // all warps done with tile tc
             set_error(a.err, DEVERR_TIMEOUT_EMPTY);
-            abort_flag[0] = 1;
-            break;
+            return false;
         }
-        if (lane == 0) {
-            release[s] = 0;
-            if (t + a.nstage < ntiles)
-                issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, t + a.nstage, r0, r1,
-                                 R, pol);
-        }
+        if (lane == 0 && tc + a.nstage < ntiles)
+            issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, tc + a.nstage, r0, r1, R,
+                             pol);
+        const float* rb = red + (tc % (2 * a.nstage)) * NCONS_WARPS * NV;
+        const int row0 = r0 + tc * R;
+        const int nr = min(R, r1 - row0);
         for (int row = lane; row < nr; row += 32) {
             const int rg = row % a.RG, i = row / a.RG;
             const int w0 = (rg * P) >> 5;
@@ -638,7 +582,67 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
                 }
             }
         }
+        return true;
+    };
+
+    bool ok = true;
+    int t = 0;
+    for (; t < ntiles && ok; ++t) {
+        const int s = t % a.nstage;
+        if (!mbar_wait(&full[s], (t / a.nstage) & 1)) {
+            set_error(a.err, DEVERR_TIMEOUT_FULL);
+            ok = false;
+            break;
+        }
+        if (trace && t == 0 && tid == 0)
+            trace[5] = globaltimer_ns();
+        const uint8_t* tile = smem + static_cast<size_t>(s) * a.stage_bytes;
+        const int nr = min(R, r1 - (r0 + t * R));
+        float acc[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+            acc[v] = 0.f;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            const int row = g + a.RG * i;
+            if (row < nr) {
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) {
+                    const uint8_t* rp = tile + static_cast<size_t>(m * R + row) * a.row_bytes;
+                    float sum = 0.f;
+#pragma unroll
+                    for (int k = 0; k < UL; ++k) {
+                        if (have[k]) {
+                            const int n = p + P * k;
+                            if (FMT == FMT_Q4K)
+                                sum += q4k_unit<PL>(rp, n, reinterpret_cast<const XQ<PL>&>(us[k]));
+                            else if (FMT == FMT_Q6K)
+                                sum += q6k_unit(rp, n, reinterpret_cast<const XQ<1>&>(us[k]));
+                            else
+                                sum += bf16_unit(rp, n, reinterpret_cast<const uint32_t(&)[4]>(us[k]));
+                        }
+                    }
+                    acc[m * RPT + i] = sum;
+                }
+            }
+        }
+        // this warp's partial sums of the tile's rows -> shared memory, then release
+        warp_transpose_reduce<NV>(acc, lane);
+        float* rb = red + (t % (2 * a.nstage)) * NCONS_WARPS * NV;
+        if ((lane & (32 / NV - 1)) == 0)
+            rb[warp * NV + lane / (32 / NV)] = acc[0];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[s]);  // release semantics: the partial sums are visible to the completer
+        const int tc = t - DEFER;
+        if (tc >= 0 && tc % NCONS_WARPS == warp)
+            ok = complete(tc);
     }
+    // tiles still to complete: the last DEFER (or all, after a timeout: none are refilled then)
+    if (ok)
+        for (int tc = max(0, ntiles - DEFER); tc < ntiles; ++tc)
+            if (tc % NCONS_WARPS == warp && !complete(tc))
+                break;
     (void)gw0;
     if (trace && lane == 0) {  // the last warp of the block to finish records the end
         atomicMax(trace + 6, globaltimer_ns());
