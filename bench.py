@@ -92,7 +92,7 @@ def hbm_peak_gbs():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms during the timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -108,7 +108,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -272,7 +272,7 @@ def run_ours(args):
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(prof):
         try:
-            traffic = json.load(open(prof)).get(dom)
+            traffic = json.load(open(prof)).get(dom, {}).get("dram_bytes_per_launch")
         except Exception:
             traffic = None
 
@@ -338,6 +338,34 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_kernel_probe(args):
+    """One decode token of a 2-layer full-width stack (9 GEMV launches), then the
+    chosen kernel kind on layer 1 (a Q6_K down layer), alone, `probe_reps` times."""
+    import torch
+
+    from quantised_gemv_norm_gb300 import build, dq, upload
+
+    build.build()
+    dq.load()
+    S = synth.QWEN3_8B
+    m = synth.make_model(SEED, n_layers=2, hidden=S["hidden"], ffn=S["ffn"], n_q_heads=S["n_q_heads"],
+                         n_kv_heads=S["n_kv_heads"], head_dim=S["head_dim"], vocab=S["vocab"], max_ctx=MAX_CTX)
+    w = upload.to_device(m, synth.make_kv_cache(SEED, m, 0))
+    model = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=False)
+    x = torch.from_numpy(synth.decode_input(SEED, m.hidden)).cuda()
+    logits = model.step(x, 0)
+    kind = KERNEL_KINDS.index(args.kernel_probe)
+    for _ in range(args.probe_reps):
+        model.enqueue_kernel(1, kind)
+    torch.cuda.synchronize()
+    err = dq.device_error()
+    model.close()
+    print(json.dumps({"kernel_probe": args.kernel_probe, "reps": args.probe_reps, "device_error_flag": err,
+                      "logits_finite": bool(torch.isfinite(logits).all().item())}))
+    if err:
+        sys.exit(1)
+
+
 # -------------------------------------------------------------- the oracle
 
 
@@ -397,12 +425,19 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--no-ctx512", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-probe", choices=KERNEL_KINDS, default=None,
+                    help="profiling aid: build a 2-layer full-width stack, run one token, then launch this "
+                         "kernel kind alone --probe-reps times (for ncu -k ... -s 9 -c 1)")
+    ap.add_argument("--probe-reps", type=int, default=3)
     args = ap.parse_args()
+    if args.kernel_probe:
+        run_kernel_probe(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
