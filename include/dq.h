@@ -181,6 +181,23 @@ DQ_API int dq_attention_decode(const float* q, const void* k_plane, const void* 
                                int n_kv, int head_dim, int max_ctx, int n_keys, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/* The same attention without any allocation.  The pages have no counterpart:
+ * this serves callers that cannot call cudaMalloc (code running while a stream
+ * is captured under a mode that forbids allocation, server plugins whose host
+ * owns all device memory, deployments that fix device memory at start-up).
+ * The scratch is one static device array of the library, sized for
+ * n_q <= 64 and n_kv <= 64 (about 529 KB, held on every device that loads the
+ * library until the process exits).  The first call on a device looks up that
+ * array's address; make that first call before any stream capture.  Each call
+ * clears the array's merge counters on `stream` first.  All calls share the
+ * array: calls whose executions overlap in time (on any streams) race and give
+ * wrong results.  Arguments as dq_attention_decode without the workspace.
+ * Errors: NULL -> DQ_ERR_NULL; shapes, and n_q > 64 or n_kv > 64 ->
+ * DQ_ERR_SHAPE; head_dim != 128 or n_q / n_kv > 8 -> DQ_ERR_UNSUPPORTED;
+ * misaligned pointers -> DQ_ERR_ALIGN; a CUDA error -> DQ_ERR_CUDA. */
+DQ_API int dq_attention_decode_static(const float* q, const void* k_plane, const void* v_plane, float* out, int n_q,
+                                      int n_kv, int head_dim, int max_ctx, int n_keys, void* stream);
+
 /* ------------------------------------------------------------ M-token sweep
  * "The roofline holds on a second GPU", section "The Math": M tokens share one
  * read of the weights; below M* = (w/16)(R/BW) memory bounds the product, above

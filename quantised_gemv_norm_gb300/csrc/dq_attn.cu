@@ -12,6 +12,8 @@
 // max / sum / output (4 dims per lane).  Each block writes (m, l, o) partials;
 // the last block of a KV head to finish (a device-scope counter, no waiting)
 // merges them and resets the counter for the next call.
+#include <mutex>
+
 #include "dq_attn.cuh"
 
 namespace dq {
@@ -214,6 +216,87 @@ DQ_API int dq_attention_decode(const float* q, const void* k_plane, const void* 
     a.n_keys = n_keys;
     a.step = nullptr;
     cudaError_t e = dqhost::launch_attention(a, static_cast<cudaStream_t>(stream), false);
+    return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------- attention without allocation
+//
+// Some callers cannot call cudaMalloc: code that runs while a stream is being
+// captured into a CUDA graph under a capture mode that forbids allocation,
+// inference-server plugins whose host owns all device memory through its own
+// pool, and embedded or real-time deployments that fix their device memory at
+// start-up.  For them the attention scratch (the merge counters and the chunk
+// partials) lives in one file-scope device array, sized for up to
+// DQ_STATIC_ATT_MAX_Q query heads and DQ_STATIC_ATT_MAX_KV KV heads.  Every
+// device that loads this library holds the array until the process exits.
+
+namespace {
+
+constexpr int STATIC_ATT_MAX_Q = 64;
+constexpr int STATIC_ATT_MAX_KV = 64;
+constexpr size_t STATIC_ATT_BYTES =
+    dq::ATT_COUNTER_BYTES + static_cast<size_t>(STATIC_ATT_MAX_Q) * dq::ATT_CHUNKS * dq::ATT_PART * sizeof(float);
+
+static __device__ __align__(256) unsigned char g_static_att_scratch[STATIC_ATT_BYTES];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current); null if the lookup fails.
+void* static_att_scratch()
+{
+    static std::mutex mu;
+    static void* ptrs[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_att_scratch) != cudaSuccess)
+            return nullptr;
+        ptrs[dev] = p;
+    }
+    return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+DQ_API int dq_attention_decode_static(const float* q, const void* k_plane, const void* v_plane, float* out, int n_q,
+                                      int n_kv, int head_dim, int max_ctx, int n_keys, void* stream)
+{
+    if (!q || !k_plane || !v_plane || !out)
+        return DQ_ERR_NULL;
+    if (n_q < 1 || n_kv < 1 || max_ctx < 1 || n_keys < 1 || n_keys > max_ctx || n_q % n_kv)
+        return DQ_ERR_SHAPE;
+    if (n_q > STATIC_ATT_MAX_Q || n_kv > STATIC_ATT_MAX_KV)
+        return DQ_ERR_SHAPE;  // beyond the fixed scratch array
+    if (head_dim != dq::ATT_HD || n_q / n_kv > 8)
+        return DQ_ERR_UNSUPPORTED;
+    if (!dqhost::aligned16(q) || !dqhost::aligned16(k_plane) || !dqhost::aligned16(v_plane) || !dqhost::aligned16(out))
+        return DQ_ERR_ALIGN;
+    void* scratch = static_att_scratch();
+    if (!scratch)
+        return dqhost::set_cuda_error(cudaGetLastError());
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the merge counters must start at zero whatever an earlier call left behind
+    cudaError_t e = cudaMemsetAsync(scratch, 0, dq::ATT_COUNTER_BYTES, s);
+    if (e != cudaSuccess)
+        return dqhost::set_cuda_error(e);
+    dq::AttnArgs a{};
+    a.q = q;
+    a.kc = static_cast<const __half*>(k_plane);
+    a.vc = static_cast<const __half*>(v_plane);
+    a.out = out;
+    dqhost::attention_bind_workspace(a, scratch);
+    a.n_q = n_q;
+    a.n_kv = n_kv;
+    a.max_ctx = max_ctx;
+    a.n_keys = n_keys;
+    a.step = nullptr;
+    e = dqhost::launch_attention(a, s, false);
     return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
 }
 

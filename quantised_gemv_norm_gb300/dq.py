@@ -37,6 +37,7 @@ SIGNATURES = {
     "dq_dequant_q6k": (I, [P, P, LL, P]),
     "dq_attention_workspace_bytes": (SZ, [I, I]),
     "dq_attention_decode": (I, [P, P, P, P, I, I, I, I, I, P, SZ, P]),
+    "dq_attention_decode_static": (I, [P, P, P, P, I, I, I, I, I, P]),
     "dq_matmul_q4k": (I, [P, P, P, I, I, I, P]),
     "dq_model_create": (I, [P, P]),
     "dq_decode_step": (I, [P, P, I, P, P]),
@@ -215,6 +216,18 @@ def attention_decode(q: torch.Tensor, k_plane: torch.Tensor, v_plane: torch.Tens
     st = lib.dq_attention_decode(_ptr(q), _ptr(k_plane), _ptr(v_plane), _ptr(out), n_q, n_kv, hd, max_ctx,
                                  n_keys, _ptr(ws), ws.numel(), _stream())
     _check("dq_attention_decode", st)
+    return out
+
+
+def attention_decode_static(q: torch.Tensor, k_plane: torch.Tensor, v_plane: torch.Tensor, n_keys: int, out=None):
+    """As attention_decode, with the library's static scratch (no allocation by the library)."""
+    lib = load()
+    n_q, hd = q.shape
+    n_kv, max_ctx, _ = k_plane.shape
+    out = torch.empty_like(q) if out is None else out
+    st = lib.dq_attention_decode_static(_ptr(q), _ptr(k_plane), _ptr(v_plane), _ptr(out), n_q, n_kv, hd, max_ctx,
+                                        n_keys, _stream())
+    _check("dq_attention_decode_static", st)
     return out
 
 
