@@ -88,7 +88,7 @@ struct XQ {
     uint32_t l[PL == 2 ? 16 : 1]; // PL = 2: the remainder plane, same packing, |xl| <= 16384
     float s;                      // group scale
     float f;                      // Q4_K: s / 16
-    float hsum;                   // Q4_K: sum of the 32 fp32 values
+    float hsum;                   // Q4_K: s * (sum of the rounded values): the min term
     int s32a, s32b;               // Q6_K: 32 * sum xi[0..15], 32 * sum xi[16..31]
 };
 
@@ -334,36 +334,49 @@ __device__ __forceinline__ float quantise_block(float4 (&v)[QCHUNKS], const floa
             h.x *= gv[i].x; h.y *= gv[i].y; h.z *= gv[i].z; h.w *= gv[i].w;
         }
         float amax = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
-        float hs = (h.x + h.y) + (h.z + h.w);
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
+        for (int o = 1; o < 8; o <<= 1)
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            hs += __shfl_xor_sync(0xffffffffu, hs, o);
-        }
         const float inv = amax > 0.f ? XQ_MAX / amax : 0.f;
         const float t0 = h.x * inv, t1 = h.y * inv, t2 = h.z * inv, t3 = h.w * inv;
         const int a0 = round_small(t0), a1 = round_small(t1), a2 = round_small(t2), a3 = round_small(t3);
         const int e = c & 7;
         uint32_t* q = xq + (c >> 3) * xq_words(PL);
         *reinterpret_cast<uint2*>(q + 2 * e) = make_uint2(pack16x2(a0, a1), pack16x2(a2, a3));
-        if (PL == 2)  // remainders: t - a is exact in fp32
-            *reinterpret_cast<uint2*>(q + 16 + 2 * e) =
-                make_uint2(pack16x2(round_small((t0 - static_cast<float>(a0)) * 32768.0f),
-                                    round_small((t1 - static_cast<float>(a1)) * 32768.0f)),
-                           pack16x2(round_small((t2 - static_cast<float>(a2)) * 32768.0f),
-                                    round_small((t3 - static_cast<float>(a3)) * 32768.0f)));
-        int isum = (a0 + a1) + (a2 + a3);  // the two 16-element halves of the unit (Q6_K offsets)
+        int lsum = 0;
+        if (PL == 2) {  // remainders: t - a is exact in fp32
+            const int b0 = round_small((t0 - static_cast<float>(a0)) * 32768.0f);
+            const int b1 = round_small((t1 - static_cast<float>(a1)) * 32768.0f);
+            const int b2 = round_small((t2 - static_cast<float>(a2)) * 32768.0f);
+            const int b3 = round_small((t3 - static_cast<float>(a3)) * 32768.0f);
+            *reinterpret_cast<uint2*>(q + 16 + 2 * e) = make_uint2(pack16x2(b0, b1), pack16x2(b2, b3));
+            lsum = (b0 + b1) + (b2 + b3);
+        }
+        // Integer sums of the rounded values: per 16-element half (Q6_K's -32 offset)
+        // and over the unit (Q4_K's min term).  Taking the min term from the same
+        // rounded values keeps the product exactly sum_k W_k x^_k, so the rounding
+        // error meets the full (zero-mean) weights, not only their positive part.
+        int isum = (a0 + a1) + (a2 + a3);
         isum += __shfl_xor_sync(0xffffffffu, isum, 1);
         isum += __shfl_xor_sync(0xffffffffu, isum, 2);
+        const int ihalf = isum;  // this 16-element half
+        isum += __shfl_xor_sync(0xffffffffu, isum, 4);
+        if (PL == 2) {
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1)
+                lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+        }
         float* meta = reinterpret_cast<float*>(q + 16 * PL);
-        if (e == 0) {
+        if (e == 0 || e == 4) {
             const float sc = amax / XQ_MAX;
-            meta[0] = sc;
-            meta[1] = sc * 0.0625f;
-            meta[2] = hs;
-            reinterpret_cast<int*>(meta)[3] = 32 * isum;
-        } else if (e == 4) {
-            reinterpret_cast<int*>(meta)[4] = 32 * isum;
+            if (e == 0) {
+                meta[0] = sc;
+                meta[1] = sc * 0.0625f;
+                meta[2] = sc * (static_cast<float>(isum) + static_cast<float>(lsum) * (1.0f / 32768.0f));
+                reinterpret_cast<int*>(meta)[3] = 32 * ihalf;
+            } else {
+                reinterpret_cast<int*>(meta)[4] = 32 * ihalf;
+            }
         }
     }
     return ss;
