@@ -528,20 +528,22 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
     // t % 16, DEFER tiles later, when every warp has normally released it: no
     // warp waits for another on the common path.
     const int DEFER = a.nstage >= 4 ? 2 : 1;
-    auto complete = [&](int tc) -> bool {
-        const int sc = tc % a.nstage;
-        if (!mbar_wait(&empty[sc], (tc / a.nstage) & 1)) {  // all warps done with tile tc
+    // Counters instead of divisions by the runtime stage count: stage t uses ring
+    // slot t % nstage with phase (t / nstage) & 1 and partial-sum slot t % (2 nstage).
+    const int rg_shift = 31 - __clz(a.RG);  // RG is a power of two
+    auto complete = [&](int tc, int sc, uint32_t phase, int rslot) -> bool {
+        if (!mbar_wait(&empty[sc], phase)) {  // all warps done with tile tc
             set_error(a.err, DEVERR_TIMEOUT_EMPTY);
             return false;
         }
         if (lane == 0 && tc + a.nstage < ntiles)
             issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, tc + a.nstage, r0, r1, R,
                              pol);
-        const float* rb = red + (tc % (2 * a.nstage)) * NCONS_WARPS * NV;
+        const float* rb = red + rslot * NCONS_WARPS * NV;
         const int row0 = r0 + tc * R;
         const int nr = min(R, r1 - row0);
         for (int row = lane; row < nr; row += 32) {
-            const int rg = row % a.RG, i = row / a.RG;
+            const int rg = row & (a.RG - 1), i = row >> rg_shift;
             const int w0 = (rg * P) >> 5;
             float v0 = 0.f, v1 = 0.f;
             for (int w = 0; w < nwg; ++w) {
@@ -576,10 +578,10 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
     };
 
     bool ok = true;
-    int t = 0;
+    int t = 0, s = 0, rslot = 0;
+    uint32_t phase = 0;
     for (; t < ntiles && ok; ++t) {
-        const int s = t % a.nstage;
-        if (!mbar_wait(&full[s], (t / a.nstage) & 1)) {
+        if (!mbar_wait(&full[s], phase)) {
             set_error(a.err, DEVERR_TIMEOUT_FULL);
             ok = false;
             break;
@@ -618,20 +620,36 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         }
         // this warp's partial sums of the tile's rows -> shared memory, then release
         warp_transpose_reduce<NV>(acc, lane);
-        float* rb = red + (t % (2 * a.nstage)) * NCONS_WARPS * NV;
+        float* rb = red + rslot * NCONS_WARPS * NV;
         if ((lane & (32 / NV - 1)) == 0)
             rb[warp * NV + lane / (32 / NV)] = acc[0];
         __syncwarp();
         if (lane == 0)
             mbar_arrive(&empty[s]);  // release semantics: the partial sums are visible to the completer
         const int tc = t - DEFER;
-        if (tc >= 0 && tc % NCONS_WARPS == warp)
-            ok = complete(tc);
+        if (tc >= 0 && (tc & (NCONS_WARPS - 1)) == warp) {
+            int sc = s - DEFER, rc = rslot - DEFER;
+            uint32_t pc = phase;
+            if (sc < 0) {
+                sc += a.nstage;
+                pc ^= 1u;
+            }
+            if (rc < 0)
+                rc += 2 * a.nstage;
+            ok = complete(tc, sc, pc, rc);
+        }
+        if (++s == a.nstage) {
+            s = 0;
+            phase ^= 1u;
+        }
+        if (++rslot == 2 * a.nstage)
+            rslot = 0;
     }
-    // tiles still to complete: the last DEFER (or all, after a timeout: none are refilled then)
+    // tiles still to complete: the last DEFER (after a timeout none are: nothing is refilled then)
     if (ok)
         for (int tc = max(0, ntiles - DEFER); tc < ntiles; ++tc)
-            if (tc % NCONS_WARPS == warp && !complete(tc))
+            if ((tc & (NCONS_WARPS - 1)) == warp &&
+                !complete(tc, tc % a.nstage, (tc / a.nstage) & 1, tc % (2 * a.nstage)))
                 break;
     (void)gw0;
     if (trace && lane == 0) {  // the last warp of the block to finish records the end
