@@ -18,130 +18,12 @@
 
 namespace dq {
 
-__global__ void __launch_bounds__(256) attn_decode_kernel(const __grid_constant__ AttnArgs a)
+__global__ void __launch_bounds__(256) attn_decode_kernel(const __grid_constant__ AttnArgs args)
 {
-    __shared__ __align__(16) __half ks[ATT_BATCH][ATT_HD + 8];
-    __shared__ __align__(16) __half vs[ATT_BATCH][ATT_HD];
-    __shared__ __align__(16) float qs[8][ATT_HD];
-    __shared__ int s_last;
-
+    __shared__ __align__(16) AttnSmem sm;
     pdl_trigger();
-    const int c = blockIdx.x, g = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int group = blockDim.x >> 5;
-    const int nthr = blockDim.x;
-    // step->pos was written before the token's first kernel: safe before the wait
-    const int n_keys = a.step ? a.step->pos + 1 : a.n_keys;
-    // chunks of at least ATT_MIN_CHUNK keys: short contexts take one block per KV head
-    const int L = max((n_keys + ATT_CHUNKS - 1) / ATT_CHUNKS, ATT_MIN_CHUNK);
-    const int j0 = c * L, j1 = min(n_keys, j0 + L);
-    const int nact = (n_keys + L - 1) / L;
-    pdl_wait();
-    if (n_keys < 1 || n_keys > a.max_ctx) {
-        if (tid == 0 && c == 0)
-            set_error(a.err, DEVERR_BAD_ARG);
-        return;
-    }
-    if (j0 >= n_keys)
-        return;
-
-    const int h = g * group + warp;
-    {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.q + static_cast<size_t>(h) * ATT_HD) + lane);
-        *reinterpret_cast<float4*>(&qs[warp][4 * lane]) = v;
-    }
-    const __half* kbase = a.kc + static_cast<size_t>(g) * a.max_ctx * ATT_HD;
-    const __half* vbase = a.vc + static_cast<size_t>(g) * a.max_ctx * ATT_HD;
-    const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
-
-    float m = -INFINITY, l = 0.f;
-    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-    for (int jb = j0; jb < j1; jb += ATT_BATCH) {
-        const int nb = min(ATT_BATCH, j1 - jb);
-        __syncthreads();  // previous batch fully consumed (and qs written on the first)
-        for (int idx = tid; idx < nb * (ATT_HD / 8); idx += nthr) {
-            const int j = idx >> 4, ch = idx & 15;
-            const uint4 kv = __ldcg(reinterpret_cast<const uint4*>(kbase + static_cast<size_t>(jb + j) * ATT_HD) + ch);
-            const uint4 vv = __ldcg(reinterpret_cast<const uint4*>(vbase + static_cast<size_t>(jb + j) * ATT_HD) + ch);
-            *reinterpret_cast<uint4*>(&ks[j][8 * ch]) = kv;
-            *reinterpret_cast<uint4*>(&vs[j][8 * ch]) = vv;
-        }
-        __syncthreads();
-        float s = -INFINITY;
-        if (lane < nb) {
-            float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-            for (int ch = 0; ch < ATT_HD / 8; ++ch) {
-                const uint4 kr = *reinterpret_cast<const uint4*>(&ks[lane][8 * ch]);
-                const float4 qa = *reinterpret_cast<const float4*>(&qs[warp][8 * ch]);
-                const float4 qb = *reinterpret_cast<const float4*>(&qs[warp][8 * ch + 4]);
-                const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(&kr.x));
-                const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(&kr.y));
-                const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(&kr.z));
-                const float2 k3 = __half22float2(*reinterpret_cast<const __half2*>(&kr.w));
-                d0 = fmaf(qa.x, k0.x, d0); d1 = fmaf(qa.y, k0.y, d1);
-                d0 = fmaf(qa.z, k1.x, d0); d1 = fmaf(qa.w, k1.y, d1);
-                d0 = fmaf(qb.x, k2.x, d0); d1 = fmaf(qb.y, k2.y, d1);
-                d0 = fmaf(qb.z, k3.x, d0); d1 = fmaf(qb.w, k3.y, d1);
-            }
-            s = (d0 + d1) * scale;
-        }
-        const float mb = warp_max(s);
-        const float mnew = fmaxf(m, mb);
-        const float p = lane < nb ? expf(s - mnew) : 0.f;
-        const float corr = expf(m - mnew);  // 0 on the first batch (m = -inf)
-        l = l * corr + warp_sum(p);
-        o0 *= corr; o1 *= corr; o2 *= corr; o3 *= corr;
-        for (int j = 0; j < nb; ++j) {
-            const float pj = __shfl_sync(0xffffffffu, p, j);
-            const uint2 vr = *reinterpret_cast<const uint2*>(&vs[j][4 * lane]);
-            const float2 va = __half22float2(*reinterpret_cast<const __half2*>(&vr.x));
-            const float2 vb = __half22float2(*reinterpret_cast<const __half2*>(&vr.y));
-            o0 = fmaf(pj, va.x, o0); o1 = fmaf(pj, va.y, o1);
-            o2 = fmaf(pj, vb.x, o2); o3 = fmaf(pj, vb.y, o3);
-        }
-        m = mnew;
-    }
-
-    if (nact == 1) {  // the only block of this KV head: normalise and write directly
-        const float inv = 1.0f / l;
-        *reinterpret_cast<float4*>(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane) =
-            make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv);
-        return;
-    }
-    float* pp = a.part + (static_cast<size_t>(h) * ATT_CHUNKS + c) * ATT_PART;
-    if (lane == 0) {
-        pp[0] = m;
-        pp[1] = l;
-    }
-    *reinterpret_cast<float4*>(pp + 4 + 4 * lane) = make_float4(o0, o1, o2, o3);
-    __threadfence();
-    __syncthreads();
-    if (tid == 0)
-        s_last = (atomicAdd(&a.counters[g], 1) == nact - 1);
-    __syncthreads();
-    if (!s_last)
-        return;
-    __threadfence();
-    // merge the chunk partials of this warp's head
-    const float* hp = a.part + static_cast<size_t>(h) * ATT_CHUNKS * ATT_PART;
-    float M = -INFINITY;
-    for (int cc = 0; cc < nact; ++cc)
-        M = fmaxf(M, __ldcg(hp + cc * ATT_PART));
-    float Ls = 0.f, r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-    for (int cc = 0; cc < nact; ++cc) {
-        const float w = expf(__ldcg(hp + cc * ATT_PART) - M);
-        Ls = fmaf(__ldcg(hp + cc * ATT_PART + 1), w, Ls);
-        const float4 ov = __ldcg(reinterpret_cast<const float4*>(hp + cc * ATT_PART + 4) + lane);
-        r0 = fmaf(ov.x, w, r0); r1 = fmaf(ov.y, w, r1);
-        r2 = fmaf(ov.z, w, r2); r3 = fmaf(ov.w, w, r3);
-    }
-    const float inv = 1.0f / Ls;
-    *reinterpret_cast<float4*>(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane) =
-        make_float4(r0 * inv, r1 * inv, r2 * inv, r3 * inv);
-    __syncthreads();
-    if (tid == 0)
-        a.counters[g] = 0;
+    const AttnArgs a = args;
+    attn_block(a, blockIdx.x, blockIdx.y, blockDim.x >> 5, sm, true);
 }
 
 }  // namespace dq
