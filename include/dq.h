@@ -144,8 +144,13 @@ DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows,
  * dependency wait, after the activation is staged, after it is quantised,
  * when the first weight stage is ready; then the latest warp end time and the
  * count of finished warps (both accumulated: zero the buffer before a launch).
- * The buffer needs 64 bytes per block (at most one block per SM).  NULL turns
- * tracing off.  Not for use while another thread launches GEMVs. */
+ * The buffer needs 64 bytes per block (at most one block per SM).  A
+ * dq_decode_step that runs the fused token kernel writes instead 4 values per
+ * block and phase at buffer[4 (block * phases + phase)] (phases = 5 n_layers
+ * + 1: per layer Q|K|V, attention, O, gate/up, down; then the vocabulary):
+ * phase entered, grid barrier passed, activation in registers, phase done;
+ * 32 bytes per block and phase.  NULL turns tracing off.  Not for use while
+ * another thread launches kernels of the library. */
 DQ_API int dq_debug_trace(void* buffer);
 
 /* Dequantise nblocks consecutive blocks to fp32 (256 values per block), each
@@ -241,7 +246,7 @@ typedef struct {
     const float* out_norm;         /* device fp32 [hidden] */
     const void* wvocab;            /* device Q6_K [vocab][hidden] */
     void* kv_cache;                /* device fp16 [n_layers][2][n_kv][max_ctx][head_dim] */
-    int use_graph;                 /* 1: capture the token in a CUDA graph (default); 0: eager launches */
+    int use_graph;                 /* separate kernels only: 1 capture them in a CUDA graph, 0 eager launches */
     int flags;                     /* DQ_MODEL_* bits; 0 for the default behaviour */
 } dq_model_desc;
 
@@ -249,9 +254,21 @@ typedef struct {
  * dependent launch (each kernel waits for the previous one to finish before it
  * starts streaming); for measuring what the overlap is worth. */
 #define DQ_MODEL_NO_PDL 1
+/* dq_model_desc.flags: run the token as 5 n_layers + 1 separate kernels (in a
+ * graph when use_graph is set) even where the fused token kernel applies. */
+#define DQ_MODEL_KERNELS 2
 
 /* Validates the description, allocates the workspace (activations, attention
- * scratch) and captures the token graph on the current device.  Host call;
+ * scratch, barrier counter) and prepares the token on the current device.
+ *
+ * Two ways to run a token.  The fused token kernel (the default where the
+ * shape allows: hidden and n_q head_dim at most 4096 and multiples of 2048 and
+ * 256, ffn at most 12288, a multiple of 2048 if a down projection is Q6_K) is
+ * one cooperative launch of one block per SM that runs all phases with grid
+ * barriers between them while the weights stream through each block's ring
+ * without a break.  Otherwise, or with DQ_MODEL_KERNELS, the token is 5
+ * n_layers + 1 kernels chained by programmatic dependent launch, captured once
+ * in a CUDA graph when use_graph is set.  Host call;
  * synchronises the device.  *out receives the handle (NULL on error).
  * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE, DQ_ERR_ALIGN, DQ_ERR_UNSUPPORTED,
  * DQ_ERR_ALLOC, DQ_ERR_CUDA. */
@@ -265,6 +282,12 @@ DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits
 
 /* Number of kernels one dq_decode_step launches. */
 DQ_API int dq_model_launches_per_step(const dq_model* m);
+
+/* 1 when dq_decode_step runs the fused token kernel, 0 when it runs separate
+ * kernels, DQ_ERR_NULL for a NULL handle.  A fused token whose device wait ran
+ * out (dq_device_error reports a timeout) leaves the model's barrier counter
+ * undefined: destroy and re-create the model after such an error. */
+DQ_API int dq_model_fused(const dq_model* m);
 
 /* Diagnostics for per-kernel timing: enqueues one of the token's kernels on
  * its own (no programmatic dependency), with the position and logits pointer

@@ -13,14 +13,18 @@
 // x_in and records pos and the logits pointer in device memory, because the
 // graph's arguments are fixed.
 //
+// Where the shape allows, the same phases run instead as one persistent
+// cooperative kernel (dq_token.cu), launched directly with x_in, pos and the
+// logits pointer as arguments.
+//
 // Layout follows the Qwen3-8B census of "The roofline holds on a second GPU",
 // section "The Math"; the norm placement follows "one-serial-kernel", section
 // "One thread" (twice per layer and once at the end).
 #include <new>
 #include <vector>
 
-#include "dq_attn.cuh"
 #include "dq_gemv_host.h"
+#include "dq_token.cuh"
 
 namespace dq {
 
@@ -55,6 +59,12 @@ struct dq_model {
     float* act;
     dq::StepArgs* step;
     void* attn_ws;
+    // fused token kernel
+    bool fused;
+    dqhost::TokenPlan tplan;
+    dq::TokenLayer* layers_dev;
+    unsigned* bar;
+    unsigned bar_base;
     // plans
     dqhost::GemvPlan p_qkv, p_o, p_gateup, p_down_q4, p_down_q6, p_vocab;
     bool have_down_q4, have_down_q6;
@@ -249,12 +259,19 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
         return st;
     }
 
-    // workspace: x | q | attn | act | step | attention scratch, each 256-byte aligned
+    // the fused token kernel where the shape allows (its absence is not an error)
+    if ((d->flags & DQ_MODEL_KERNELS) == 0)
+        m->fused = dqhost::plan_token(d->n_layers, d->hidden, d->ffn, d->n_q_heads, d->n_kv_heads, d->head_dim,
+                                      m->have_down_q6, &m->tplan) == DQ_OK;
+
+    // workspace: x | q | attn | act | step | attention scratch | layer table | barrier, each 256-byte aligned
     auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     const size_t bx = up(sizeof(float) * d->hidden), bq = up(sizeof(float) * qdim), ba = bq,
                  bf = up(sizeof(float) * d->ffn), bs = up(sizeof(dq::StepArgs)),
-                 bw = up(dqhost::attention_workspace_bytes(d->n_q_heads, d->n_kv_heads));
-    cudaError_t e = cudaMalloc(&m->ws, bx + bq + ba + bf + bs + bw);
+                 bw = up(dqhost::attention_workspace_bytes(d->n_q_heads, d->n_kv_heads)),
+                 bl = up(sizeof(dq::TokenLayer) * d->n_layers), bb = 256;
+    const size_t total = bx + bq + ba + bf + bs + bw + bl + bb;
+    cudaError_t e = cudaMalloc(&m->ws, total);
     if (e != cudaSuccess) {
         cudaGetLastError();
         free_model(m);
@@ -267,11 +284,33 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
     m->act = reinterpret_cast<float*>(base + bx + bq + ba);
     m->step = reinterpret_cast<dq::StepArgs*>(base + bx + bq + ba + bf);
     m->attn_ws = base + bx + bq + ba + bf + bs;
-    if ((e = cudaMemset(m->ws, 0, bx + bq + ba + bf + bs + bw)) != cudaSuccess) {
+    m->layers_dev = reinterpret_cast<dq::TokenLayer*>(base + bx + bq + ba + bf + bs + bw);
+    m->bar = reinterpret_cast<unsigned*>(base + bx + bq + ba + bf + bs + bw + bl);
+    m->bar_base = 0;
+    if ((e = cudaMemset(m->ws, 0, total)) != cudaSuccess) {
         free_model(m);
         return dqhost::set_cuda_error(e);
     }
-    if (m->use_graph) {
+    if (m->fused) {
+        std::vector<dq::TokenLayer> tl(d->n_layers);
+        for (int l = 0; l < d->n_layers; ++l) {
+            tl[l].attn_norm = m->attn_norm[l];
+            tl[l].ffn_norm = m->ffn_norm[l];
+            tl[l].wqkv = m->wqkv[l];
+            tl[l].wo = m->wo[l];
+            tl[l].wgate = m->wgate[l];
+            tl[l].wup = m->wup[l];
+            tl[l].wdown = m->wdown[l];
+            tl[l].down_fmt = m->down_fmt[l];
+            tl[l].pad = 0;
+        }
+        if ((e = cudaMemcpy(m->layers_dev, tl.data(), sizeof(dq::TokenLayer) * d->n_layers,
+                            cudaMemcpyHostToDevice)) != cudaSuccess) {
+            free_model(m);
+            return dqhost::set_cuda_error(e);
+        }
+    }
+    if (m->use_graph && !m->fused) {
         if ((e = cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking)) != cudaSuccess ||
             (e = cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeRelaxed)) != cudaSuccess) {
             free_model(m);
@@ -303,6 +342,44 @@ DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits
     if (pos < 0 || pos >= m->max_ctx)
         return DQ_ERR_SHAPE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (m->fused) {
+        dq::TokenArgs a{};
+        a.layers = m->layers_dev;
+        a.n_layers = m->n_layers;
+        a.hidden = m->hidden;
+        a.ffn = m->ffn;
+        a.n_q = m->n_q;
+        a.n_kv = m->n_kv;
+        a.hd = m->hd;
+        a.vocab = m->vocab;
+        a.max_ctx = m->max_ctx;
+        a.eps = m->eps;
+        a.out_norm = m->out_norm;
+        a.wvocab = m->wvocab;
+        a.kv = m->kv;
+        a.x = m->x;
+        a.q = m->q;
+        a.attn = m->attn;
+        a.act = m->act;
+        dq::AttnArgs t{};
+        dqhost::attention_bind_workspace(t, m->attn_ws);
+        a.part = t.part;
+        a.counters = t.counters;
+        a.step = m->step;
+        a.bar = m->bar;
+        a.bar_base = m->bar_base;
+        a.x_in = x_in;
+        a.logits = logits;
+        a.pos = pos;
+        a.err = dqhost::device_error_flag();
+        a.trace = dqhost::gemv_trace();
+        cudaError_t e = dqhost::launch_token(m->tplan, a, s);
+        if (e != cudaSuccess)
+            return dqhost::set_cuda_error(e);
+        // every block arrives once at each of the nph - 1 barriers
+        m->bar_base += static_cast<unsigned>(m->tplan.nph - 1) * static_cast<unsigned>(m->tplan.grid);
+        return DQ_OK;
+    }
     const int threads = 256;
     dq::step_begin_kernel<<<(m->hidden + threads - 1) / threads, threads, 0, s>>>(x_in, m->x, m->hidden, m->step,
                                                                                   pos, logits);
@@ -315,7 +392,12 @@ DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits
 
 DQ_API int dq_model_launches_per_step(const dq_model* m)
 {
-    return m ? 2 + 5 * m->n_layers : 0;
+    return m ? (m->fused ? 1 : 2 + 5 * m->n_layers) : 0;
+}
+
+DQ_API int dq_model_fused(const dq_model* m)
+{
+    return m ? (m->fused ? 1 : 0) : DQ_ERR_NULL;
 }
 
 DQ_API int dq_model_enqueue_kernel(dq_model* m, int layer, int kind, void* stream)

@@ -317,14 +317,14 @@ __device__ __forceinline__ void issue_tile(const uint8_t* W, const uint8_t* W2, 
 // Quantise the activation (times gamma under RMSNorm) once per block: eight
 // lanes share one 32-element unit, four elements each; chunk c = tid + NCONS i
 // of the vector is v[i].  Returns this thread's partial sum of x^2.
-template <int FMT, int PL>
-__device__ __forceinline__ float quantise_block(float4 (&v)[QCHUNKS], const float4 (&gv)[QCHUNKS], bool norm,
-                                                uint32_t* xq, int K, int tid)
+template <int FMT, int PL, int NCH>
+__device__ __forceinline__ float quantise_block(float4 (&v)[NCH], const float4 (&gv)[NCH], bool norm, uint32_t* xq,
+                                                int K, int tid)
 {
     float ss = 0.f;
     const int nchunks = K / 4;  // a multiple of 64: whole warps take part in each pass
 #pragma unroll
-    for (int i = 0; i < QCHUNKS; ++i) {
+    for (int i = 0; i < NCH; ++i) {
         const int c = tid + NCONS * i;
         if (c >= nchunks)
             break;
@@ -380,6 +380,82 @@ __device__ __forceinline__ float quantise_block(float4 (&v)[QCHUNKS], const floa
         }
     }
     return ss;
+}
+
+// One stage of the consumers: this thread's unit products for rows g, g + RG,
+// ... (RPT of them, each of NMAT matrices) of the tile, reduced over the warp
+// into wred[0 .. RPT NMAT) (the warp's partial sums; matrix m, row i at m RPT + i).
+template <int FMT, int PL, int UL, int RPT, int NMAT>
+__device__ __forceinline__ void consume_tile(const uint8_t* tile, int nr, int R, int RG, int g, int p, int P,
+                                             int row_bytes, const UnitState<FMT, PL> (&us)[UL],
+                                             const bool (&have)[UL], float* wred, int lane)
+{
+    constexpr int NV = RPT * NMAT;
+    float acc[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+        acc[v] = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+        const int row = g + RG * i;
+        if (row < nr) {
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+                const uint8_t* rp = tile + static_cast<size_t>(m * R + row) * row_bytes;
+                float sum = 0.f;
+#pragma unroll
+                for (int k = 0; k < UL; ++k) {
+                    if (have[k]) {
+                        const int n = p + P * k;
+                        if (FMT == FMT_Q4K)
+                            sum += q4k_unit<PL>(rp, n, reinterpret_cast<const XQ<PL>&>(us[k]));
+                        else if (FMT == FMT_Q6K)
+                            sum += q6k_unit(rp, n, reinterpret_cast<const XQ<1>&>(us[k]));
+                        else
+                            sum += bf16_unit(rp, n, reinterpret_cast<const uint32_t(&)[4]>(us[k]));
+                    }
+                }
+                acc[m * RPT + i] = sum;
+            }
+        }
+    }
+    warp_transpose_reduce<NV>(acc, lane);
+    if ((lane & (32 / NV - 1)) == 0)
+        wred[lane / (32 / NV)] = acc[0];
+    __syncwarp();
+}
+
+// Load this thread's activation units (unit p + P k of the K axis) from the
+// quantised table into registers, folding the RMS factor into the scales.
+template <int FMT, int PL, int UL>
+__device__ __forceinline__ void load_units(UnitState<FMT, PL> (&us)[UL], const bool (&have)[UL], const uint32_t* xq,
+                                           int p, int P, float rstd)
+{
+#pragma unroll
+    for (int k = 0; k < UL; ++k) {
+        if (have[k]) {
+            XQ<PL>& u = reinterpret_cast<XQ<PL>&>(us[k]);
+            const uint32_t* src = xq + (unit_k0<FMT>(p + P * k) >> 5) * xq_words(PL);
+#pragma unroll
+            for (int w = 0; w < 16; w += 4) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + w);
+                u.q[w] = v.x; u.q[w + 1] = v.y; u.q[w + 2] = v.z; u.q[w + 3] = v.w;
+            }
+            if (PL == 2) {
+#pragma unroll
+                for (int w = 0; w < 16; w += 4) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(src + 16 + w);
+                    u.l[w] = v.x; u.l[w + 1] = v.y; u.l[w + 2] = v.z; u.l[w + 3] = v.w;
+                }
+            }
+            const float* meta = reinterpret_cast<const float*>(src + 16 * PL);
+            u.s = meta[0] * rstd;
+            u.f = meta[1] * rstd;
+            u.hsum = meta[2] * rstd;
+            u.s32a = reinterpret_cast<const int*>(meta)[3];
+            u.s32b = reinterpret_cast<const int*>(meta)[4];
+        }
+    }
 }
 
 template <int FMT, int UL, int RPT, int NMAT, int PL>
@@ -481,7 +557,7 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         }
         if (trace && tid == 0)
             trace[3] = globaltimer_ns();
-        float ss = quantise_block<FMT, PL>(xv, gv, norm, xq, a.K, tid);
+        float ss = quantise_block<FMT, PL, QCHUNKS>(xv, gv, norm, xq, a.K, tid);
         float rstd = 1.f;
         if (norm) {
             ss = warp_sum(ss);
@@ -497,31 +573,7 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
                 tot += gred[w];
             rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
         }
-#pragma unroll
-        for (int k = 0; k < UL; ++k) {
-            if (have[k]) {
-                XQ<PL>& u = reinterpret_cast<XQ<PL>&>(us[k]);
-                const uint32_t* src = xq + (unit_k0<FMT>(p + P * k) >> 5) * xq_words(PL);
-#pragma unroll
-                for (int w = 0; w < 16; w += 4) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(src + w);
-                    u.q[w] = v.x; u.q[w + 1] = v.y; u.q[w + 2] = v.z; u.q[w + 3] = v.w;
-                }
-                if (PL == 2) {
-#pragma unroll
-                    for (int w = 0; w < 16; w += 4) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(src + 16 + w);
-                        u.l[w] = v.x; u.l[w + 1] = v.y; u.l[w + 2] = v.z; u.l[w + 3] = v.w;
-                    }
-                }
-                const float* meta = reinterpret_cast<const float*>(src + 16 * PL);
-                u.s = meta[0] * rstd;
-                u.f = meta[1] * rstd;
-                u.hsum = meta[2] * rstd;
-                u.s32a = reinterpret_cast<const int*>(meta)[3];
-                u.s32b = reinterpret_cast<const int*>(meta)[4];
-            }
-        }
+        load_units<FMT, PL, UL>(us, have, xq, p, P, rstd);
     }
 
     // Tile t is completed (its slot refilled, its rows' epilogue run) by warp
@@ -590,40 +642,8 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             trace[5] = globaltimer_ns();
         const uint8_t* tile = smem + static_cast<size_t>(s) * a.stage_bytes;
         const int nr = min(R, r1 - (r0 + t * R));
-        float acc[NV];
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-            acc[v] = 0.f;
-#pragma unroll
-        for (int i = 0; i < RPT; ++i) {
-            const int row = g + a.RG * i;
-            if (row < nr) {
-#pragma unroll
-                for (int m = 0; m < NMAT; ++m) {
-                    const uint8_t* rp = tile + static_cast<size_t>(m * R + row) * a.row_bytes;
-                    float sum = 0.f;
-#pragma unroll
-                    for (int k = 0; k < UL; ++k) {
-                        if (have[k]) {
-                            const int n = p + P * k;
-                            if (FMT == FMT_Q4K)
-                                sum += q4k_unit<PL>(rp, n, reinterpret_cast<const XQ<PL>&>(us[k]));
-                            else if (FMT == FMT_Q6K)
-                                sum += q6k_unit(rp, n, reinterpret_cast<const XQ<1>&>(us[k]));
-                            else
-                                sum += bf16_unit(rp, n, reinterpret_cast<const uint32_t(&)[4]>(us[k]));
-                        }
-                    }
-                    acc[m * RPT + i] = sum;
-                }
-            }
-        }
-        // this warp's partial sums of the tile's rows -> shared memory, then release
-        warp_transpose_reduce<NV>(acc, lane);
-        float* rb = red + rslot * NCONS_WARPS * NV;
-        if ((lane & (32 / NV - 1)) == 0)
-            rb[warp * NV + lane / (32 / NV)] = acc[0];
-        __syncwarp();
+        consume_tile<FMT, PL, UL, RPT, NMAT>(tile, nr, R, a.RG, g, p, P, a.row_bytes, us, have,
+                                             red + rslot * NCONS_WARPS * NV + warp * NV, lane);
         if (lane == 0)
             mbar_arrive(&empty[s]);  // release semantics: the partial sums are visible to the completer
         const int tc = t - DEFER;

@@ -153,6 +153,7 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool resid, GemvPl
 static unsigned long long* g_trace = nullptr;
 
 void set_gemv_trace(void* buf) { g_trace = static_cast<unsigned long long*>(buf); }
+unsigned long long* gemv_trace() { return g_trace; }
 
 cudaError_t launch_gemv(const GemvPlan& plan, dq::GemvArgs a, cudaStream_t stream, bool pdl)
 {

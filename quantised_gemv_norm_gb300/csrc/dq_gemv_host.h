@@ -46,5 +46,6 @@ cudaError_t launch_gemv(const GemvPlan& plan, dq::GemvArgs a, cudaStream_t strea
 // per block: start, set-up done, dependency released, activation staged,
 // activation quantised, first stage ready, end, blocks finished); NULL stops.
 void set_gemv_trace(void* buf);
+unsigned long long* gemv_trace();  // the buffer set by set_gemv_trace (null when off)
 
 }  // namespace dqhost

@@ -1,0 +1,118 @@
+// dq_token.cuh -- arguments and host interface of the persistent decode-token kernel.
+#pragma once
+
+#include "dq_attn.cuh"
+
+namespace dq {
+
+constexpr int TK_NSTAGE = 4;       // weight ring slots per block
+constexpr int TK_SLOT = 40960;     // bytes per slot (largest tile: 4 Q6_K rows of K = 12288)
+constexpr int TK_P = 128;          // threads per row group
+constexpr int TK_RG = NCONS / TK_P;
+constexpr int TK_DEFER = 2;        // a stage is completed this many stages after it is consumed
+constexpr int TK_RED_STRIDE = 4;   // floats per warp in one partial-sum slot
+
+// Phase kinds.  Per layer: QKV, ATTN, O, GATEUP, DOWN (Q4_K or Q6_K); then VOCAB.
+enum { PH_QKV = 0, PH_ATTN, PH_O, PH_GATEUP, PH_DOWN_Q4, PH_DOWN_Q6, PH_VOCAB, PH_KINDS };
+
+// Rows streamed per tile and matrix, by kind (row groups x rows per thread).
+__host__ __device__ constexpr int tk_rpt(int kind)
+{
+    return kind == PH_QKV || kind == PH_O ? 4 : kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 1 : 2;
+}
+
+struct TokenLayer {
+    const float* attn_norm;
+    const float* ffn_norm;
+    const uint8_t* wqkv;
+    const uint8_t* wo;
+    const uint8_t* wgate;
+    const uint8_t* wup;
+    const uint8_t* wdown;
+    int down_fmt;
+    int pad;
+};
+
+struct TokenArgs {
+    const TokenLayer* layers;  // device [n_layers]
+    int n_layers, hidden, ffn, n_q, n_kv, hd, vocab, max_ctx;
+    float eps;
+    const float* out_norm;
+    const uint8_t* wvocab;
+    __half* kv;                // [n_layers][2][n_kv][max_ctx][hd]
+    float* x;                  // residual stream [hidden]
+    float* q;                  // [n_q hd]
+    float* attn;               // [n_q hd]
+    float* act;                // [ffn]
+    float* part;               // attention partials
+    int* counters;             // attention merge counters (zero between phases)
+    StepArgs* step;            // pos and logits recorded for the diagnostics entry points
+    unsigned* bar;             // grid barrier arrival counter (monotonic)
+    unsigned bar_base;         // its value when this launch starts
+    const float* x_in;
+    float* logits;
+    int pos;
+    int* err;
+    unsigned long long* trace; // diagnostics: 4 timestamps per block and phase when not null
+};
+
+struct PhaseEnt {
+    const uint8_t* W;
+    const uint8_t* W2;
+    int T0;    // the block's first tile of the phase (tiles numbered over the whole token)
+    int kind;
+};
+
+struct KindEnt {
+    int rows, K, row_bytes, R, nmat, pad[3];
+};
+
+// Shared memory of one block, at fixed offsets: the weight ring, the per-warp
+// partial sums, barriers and flags, the kind table, the block's residual rows,
+// the quantised activation (aliased by the attention staging), then the phase
+// table, whose length depends on the layer count.
+constexpr int TK_RESID_MAX = 64;  // residual rows of one block at most
+constexpr int TK_OFF_RED = TK_NSTAGE * TK_SLOT;
+constexpr int TK_OFF_MISC = TK_OFF_RED + 2 * TK_NSTAGE * NCONS_WARPS * TK_RED_STRIDE * 4;
+constexpr int TK_OFF_KTAB = TK_OFF_MISC + 256;
+constexpr int TK_OFF_RESID = TK_OFF_KTAB + 256;
+constexpr int TK_OFF_XQ = TK_OFF_RESID + TK_RESID_MAX * 4;
+
+__host__ __device__ constexpr int tk_max(int x, int y) { return x > y ? x : y; }
+
+// Bytes of the quantised-activation region: K <= 4096 with two planes (Q|K|V,
+// O), K <= 4096 ULF with one plane (down), and the attention staging.
+__host__ __device__ constexpr int tk_xq_bytes(int ulf)
+{
+    return (tk_max(tk_max(TK_P * xq_words(2) * 4, ulf * TK_P * xq_words(1) * 4), static_cast<int>(sizeof(AttnSmem))) +
+            127) / 128 * 128;
+}
+__host__ __device__ constexpr int tk_off_ptab(int ulf) { return TK_OFF_XQ + tk_xq_bytes(ulf); }
+__host__ __device__ constexpr int tk_smem_bytes(int ulf, int nph)
+{
+    return tk_off_ptab(ulf) + (nph + 1) * static_cast<int>(sizeof(PhaseEnt));
+}
+
+}  // namespace dq
+
+namespace dqhost {
+
+using TokenKernel = void (*)(dq::TokenArgs);
+
+struct TokenPlan {
+    int ulf;          // activation units per thread of the down projection
+    int nph;          // phases per token (5 per layer + 1)
+    int grid;         // one block per SM
+    int smem_bytes;
+    TokenKernel kernel;
+};
+
+// Whether the persistent token kernel covers this model shape (DQ_OK) or not
+// (DQ_ERR_UNSUPPORTED): hidden and n_q head_dim <= 4096, ffn <= 16384 (12288
+// with a Q6_K down projection), and the block's shared memory fits.
+int plan_token(int n_layers, int hidden, int ffn, int n_q, int n_kv, int hd, bool any_q6_down, TokenPlan* plan);
+
+// Cooperative launch of one token on `stream` (grid barriers need every block resident).
+cudaError_t launch_token(const TokenPlan& plan, const dq::TokenArgs& a, cudaStream_t stream);
+
+}  // namespace dqhost

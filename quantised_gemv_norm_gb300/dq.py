@@ -42,6 +42,7 @@ SIGNATURES = {
     "dq_model_create": (I, [P, P]),
     "dq_decode_step": (I, [P, P, I, P, P]),
     "dq_model_launches_per_step": (I, [P]),
+    "dq_model_fused": (I, [P]),
     "dq_model_enqueue_kernel": (I, [P, I, I, P]),
     "dq_model_buffer": (I, [P, I, P]),
     "dq_model_destroy": (I, [P]),
@@ -252,6 +253,7 @@ class _Desc(ctypes.Structure):
 
 
 MODEL_NO_PDL = 1
+MODEL_KERNELS = 2  # run the token as separate kernels even where the fused token kernel applies
 
 
 class Model:
@@ -287,6 +289,7 @@ class Model:
         _check("dq_model_create", lib.dq_model_create(ctypes.byref(d), ctypes.byref(h)))
         self._h = h
         self.launches_per_step = lib.dq_model_launches_per_step(h)
+        self.fused = bool(lib.dq_model_fused(h))
 
     def step(self, x_in: torch.Tensor, pos: int, logits: torch.Tensor | None = None) -> torch.Tensor:
         lib = load()

@@ -205,19 +205,26 @@ def test_matmul_q4k(dq, orc, M):
 # -------------------------------------------------------------- decode
 
 
-def _run_decode(dq, orc, m, kv, positions, use_graph=True, seed=0, emulate=False):
+def _run_decode(dq, orc, m, kv, positions, use_graph=True, seed=0, emulate=False, flags=0, fused=None, w=None):
     """Decode `positions` on the GPU and in the oracle; returns the GPU logits per step.
 
     Bar per step: max|gpu - oracle| / max|oracle| <= 2e-3.  With `emulate`, the
     bar is widened to 4x the deviation that the documented activation format
     alone produces on this model (tests/decode_emulation.py), for random models
     whose logits amplify input rounding far more than a trained model's would.
+    `fused` (when not None) is the expected execution mode of the model.
     """
     from quantised_gemv_norm_gb300 import upload
     import decode_emulation as emu
 
-    w = upload.to_device(m, kv)
-    model = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=use_graph)
+    if w is None:
+        w = upload.to_device(m, kv)
+    else:
+        w["kv_cache"].copy_(torch.from_numpy(kv.view(np.int16)).to("cuda"))
+    model = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=use_graph, flags=flags)
+    if fused is not None:
+        assert model.fused == fused
+        assert model.launches_per_step == (1 if fused else 2 + 5 * m.n_layers)
     kv_host = kv.copy()
     kv_emu = kv.copy()
     Wd = emu.dequantised(orc, m) if emulate else None
@@ -241,11 +248,26 @@ def _run_decode(dq, orc, m, kv, positions, use_graph=True, seed=0, emulate=False
     return outs
 
 
-def test_decode_small_model_steps(dq, orc):
+MODES = {"fused": (0, True), "kernels": (2, False)}  # flags (DQ_MODEL_KERNELS = 2), expected fused
+
+
+@pytest.mark.parametrize("mode", ["fused", "kernels"])
+def test_decode_small_model_steps(dq, orc, mode):
     m = synth.make_model(21, n_layers=2, hidden=2048, ffn=4096, n_q_heads=8, n_kv_heads=2, head_dim=128,
                          vocab=1000, max_ctx=64)
     kv = synth.make_kv_cache(21, m, 0)
-    _run_decode(dq, orc, m, kv, [0, 1, 2, 3], emulate=True)
+    flags, fused = MODES[mode]
+    _run_decode(dq, orc, m, kv, [0, 1, 2, 3], emulate=True, flags=flags, fused=fused)
+
+
+@pytest.mark.parametrize("mode", ["fused", "kernels"])
+def test_decode_small_model_attention_chunks(dq, orc, mode):
+    # contexts around the attention's chunking: one chunk (64 keys), two, and 16 chunks of 69 keys
+    m = synth.make_model(23, n_layers=2, hidden=2048, ffn=4096, n_q_heads=16, n_kv_heads=4, head_dim=128,
+                         vocab=300, max_ctx=1200)
+    kv = synth.make_kv_cache(23, m, 1100)
+    flags, fused = MODES[mode]
+    _run_decode(dq, orc, m, kv, [63, 64, 1100], emulate=True, flags=flags, fused=fused)
 
 
 def test_decode_small_model_eager_equals_graph(dq, orc):
@@ -253,19 +275,54 @@ def test_decode_small_model_eager_equals_graph(dq, orc):
     m = synth.make_model(22, n_layers=2, hidden=2048, ffn=4096, n_q_heads=8, n_kv_heads=2, head_dim=128,
                          vocab=777, max_ctx=40)
     kv = synth.make_kv_cache(22, m, 30)
-    eager = _run_decode(dq, orc, m, kv, [30, 31], use_graph=False, emulate=True)
-    graph = _run_decode(dq, orc, m, kv, [30, 31], use_graph=True, emulate=True)
+    eager = _run_decode(dq, orc, m, kv, [30, 31], use_graph=False, emulate=True, flags=2, fused=False)
+    graph = _run_decode(dq, orc, m, kv, [30, 31], use_graph=True, emulate=True, flags=2, fused=False)
     for a, b in zip(eager, graph):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
-def test_decode_qwen3_8b_shape_empty_cache(dq, orc):
-    m = synth.make_model(1, max_ctx=1024, **synth.QWEN3_8B)
+def test_decode_fused_is_deterministic(dq, orc):
+    # the fused token kernel reduces in a fixed order: two runs agree bit for bit
+    m = synth.make_model(24, n_layers=2, hidden=2048, ffn=4096, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                         vocab=500, max_ctx=80)
+    kv = synth.make_kv_cache(24, m, 70)
+    a = _run_decode(dq, orc, m, kv, [70, 71], emulate=True, fused=True)
+    b = _run_decode(dq, orc, m, kv, [70, 71], emulate=True, fused=True)
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+
+
+def test_decode_shape_outside_fused_kernel_runs_kernels(dq, orc):
+    # hidden 6144 is beyond the fused kernel's activation registers: separate kernels run
+    m = synth.make_model(25, n_layers=1, hidden=6144, ffn=2048, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                         vocab=256, max_ctx=16)
+    kv = synth.make_kv_cache(25, m, 3)
+    _run_decode(dq, orc, m, kv, [3], emulate=True, fused=False)
+
+
+_QWEN = {}
+
+
+def _qwen3():
+    if "m" not in _QWEN:
+        from quantised_gemv_norm_gb300 import upload
+        m = synth.make_model(1, max_ctx=1024, **synth.QWEN3_8B)
+        _QWEN["m"] = m
+        _QWEN["w"] = upload.to_device(m, synth.make_kv_cache(1, m, 0))
+    return _QWEN["m"], _QWEN["w"]
+
+
+@pytest.mark.parametrize("mode", ["fused", "kernels"])
+def test_decode_qwen3_8b_shape_empty_cache(dq, orc, mode):
+    m, w = _qwen3()
     kv = synth.make_kv_cache(1, m, 0)
-    _run_decode(dq, orc, m, kv, [0])
+    flags, fused = MODES[mode]
+    _run_decode(dq, orc, m, kv, [0], flags=flags, fused=fused, w=w)
 
 
-def test_decode_qwen3_8b_shape_512_context(dq, orc):
-    m = synth.make_model(1, max_ctx=1024, **synth.QWEN3_8B)
+@pytest.mark.parametrize("mode", ["fused", "kernels"])
+def test_decode_qwen3_8b_shape_512_context(dq, orc, mode):
+    m, w = _qwen3()
     kv = synth.make_kv_cache(2, m, 512)
-    _run_decode(dq, orc, m, kv, [512])
+    flags, fused = MODES[mode]
+    _run_decode(dq, orc, m, kv, [512], flags=flags, fused=fused, w=w)
