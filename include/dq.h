@@ -254,21 +254,22 @@ typedef struct {
  * dependent launch (each kernel waits for the previous one to finish before it
  * starts streaming); for measuring what the overlap is worth. */
 #define DQ_MODEL_NO_PDL 1
-/* dq_model_desc.flags: run the token as 5 n_layers + 1 separate kernels (in a
- * graph when use_graph is set) even where the fused token kernel applies. */
-#define DQ_MODEL_KERNELS 2
+/* dq_model_desc.flags: run the token as one persistent cooperative kernel
+ * (the fused token kernel) where the shape allows; otherwise the flag is
+ * ignored and the separate kernels run.  See dq_model_create. */
+#define DQ_MODEL_FUSED 2
 
 /* Validates the description, allocates the workspace (activations, attention
  * scratch, barrier counter) and prepares the token on the current device.
  *
- * Two ways to run a token.  The fused token kernel (the default where the
- * shape allows: hidden and n_q head_dim at most 4096 and multiples of 2048 and
- * 256, ffn at most 12288, a multiple of 2048 if a down projection is Q6_K) is
+ * Two ways to run a token.  By default it is 5 n_layers + 1 kernels chained
+ * by programmatic dependent launch, captured once in a CUDA graph when
+ * use_graph is set.  With DQ_MODEL_FUSED, where the shape allows (at most 64
+ * layers; hidden and n_q head_dim at most 4096, hidden a multiple of 2048;
+ * ffn at most 12288, a multiple of 2048 if a down projection is Q6_K), it is
  * one cooperative launch of one block per SM that runs all phases with grid
  * barriers between them while the weights stream through each block's ring
- * without a break.  Otherwise, or with DQ_MODEL_KERNELS, the token is 5
- * n_layers + 1 kernels chained by programmatic dependent launch, captured once
- * in a CUDA graph when use_graph is set.  Host call;
+ * without a break.  Host call;
  * synchronises the device.  *out receives the handle (NULL on error).
  * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE, DQ_ERR_ALIGN, DQ_ERR_UNSUPPORTED,
  * DQ_ERR_ALLOC, DQ_ERR_CUDA. */

@@ -259,8 +259,8 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
         return st;
     }
 
-    // the fused token kernel where the shape allows (its absence is not an error)
-    if ((d->flags & DQ_MODEL_KERNELS) == 0)
+    // the fused token kernel on request, where the shape allows (its absence is not an error)
+    if (d->flags & DQ_MODEL_FUSED)
         m->fused = dqhost::plan_token(d->n_layers, d->hidden, d->ffn, d->n_q_heads, d->n_kv_heads, d->head_dim,
                                       m->have_down_q6, &m->tplan) == DQ_OK;
 

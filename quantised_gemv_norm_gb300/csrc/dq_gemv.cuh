@@ -314,18 +314,18 @@ __device__ __forceinline__ void issue_tile(const uint8_t* W, const uint8_t* W2, 
                  &full[s], pol);
 }
 
-// Quantise the activation (times gamma under RMSNorm) once per block: eight
-// lanes share one 32-element unit, four elements each; chunk c = tid + NCONS i
-// of the vector is v[i].  Returns this thread's partial sum of x^2.
-template <int FMT, int PL, int NCH>
+// Quantise the activation (times gamma under RMSNorm) once per block of NT
+// threads: eight lanes share one 32-element unit, four elements each; chunk
+// c = tid + NT i of the vector is v[i].  Returns this thread's partial sum of x^2.
+template <int FMT, int PL, int NCH, int NT = NCONS>
 __device__ __forceinline__ float quantise_block(float4 (&v)[NCH], const float4 (&gv)[NCH], bool norm, uint32_t* xq,
                                                 int K, int tid)
 {
     float ss = 0.f;
-    const int nchunks = K / 4;  // a multiple of 64: whole warps take part in each pass
+    const int nchunks = K / 4;  // a multiple of 32: whole warps take part in each pass
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
-        const int c = tid + NCONS * i;
+        const int c = tid + NT * i;
         if (c >= nchunks)
             break;
         float4 h = v[i];

@@ -13,10 +13,12 @@
 // a second GPU", section "Hiding, fusing...": keep the bytes in flight across
 // the whole token; "The Mountain Runs", section 3: one output per weight row).
 //
-// The consumers are those of the streaming GEMV kernel (dq_gemv.cuh): 512
-// threads in four row groups of 128, each thread holding its slice of the
-// quantised activation in registers; stage t is completed by warp t % 16 two
-// stages later.  The attention phase runs one (key chunk, KV head) item per
+// The consumers are those of the streaming GEMV kernel (dq_gemv.cuh), with
+// 384 threads (12 warps, so each thread may hold 168 registers: the code of
+// all phase kinds shares one allocation): row groups of 128 threads for the
+// K <= 4096 phases and one group of 384 for the down projection, each thread
+// holding one 32-element unit of the quantised activation in registers; stage
+// t is completed by warp t % 12 two stages later.  The attention phase runs one (key chunk, KV head) item per
 // block on the first n_q / n_kv warps (dq_attn.cuh).
 //
 // Every wait is bounded.  A block whose wait runs out records the error, stops
@@ -46,46 +48,39 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v)
 extern __shared__ __align__(128) uint8_t tk_smem[];
 
 struct TkMisc {
-    float gred[NCONS_WARPS];   // norm partial sums
+    float gred[TK_WARPS];      // norm partial sums
     uint64_t full[TK_NSTAGE];  // stage loaded
     uint64_t empty[TK_NSTAGE]; // stage released by all warps
     int dead;                  // a wait of this block ran out
     int issued_hi;             // one past the highest tile issued
     int sync_ok;
     int ttotal;                // the block's tiles over the token
-    // Epilogue pointers of phase p in slot p & 1: thread 0 writes the next
-    // phase's while warps may still complete the current phase's last tiles.
-    float* y[2];               // output rows
-    __half* kc[2];             // EPI_QKV: the layer's K and V planes
-    __half* vc[2];
 };
 static_assert(sizeof(TkMisc) <= 256, "misc region");
 
 __device__ __forceinline__ TkMisc& tk_misc() { return *reinterpret_cast<TkMisc*>(tk_smem + TK_OFF_MISC); }
+// The launch arguments, copied to shared memory at kernel start: the phase
+// functions read them there instead of holding them in registers.
+__device__ __forceinline__ const TokenArgs& tk_args() { return *reinterpret_cast<const TokenArgs*>(tk_smem + TK_OFF_ARGS); }
 __device__ __forceinline__ KindEnt* tk_ktab() { return reinterpret_cast<KindEnt*>(tk_smem + TK_OFF_KTAB); }
 __device__ __forceinline__ float* tk_resid() { return reinterpret_cast<float*>(tk_smem + TK_OFF_RESID); }
 __device__ __forceinline__ uint32_t* tk_xq() { return reinterpret_cast<uint32_t*>(tk_smem + TK_OFF_XQ); }
 __device__ __forceinline__ float* tk_red() { return reinterpret_cast<float*>(tk_smem + TK_OFF_RED); }
-template <int ULF>
-__device__ __forceinline__ PhaseEnt* tk_ptab() { return reinterpret_cast<PhaseEnt*>(tk_smem + tk_off_ptab(ULF)); }
+__device__ __forceinline__ PhaseEnt* tk_ptab() { return reinterpret_cast<PhaseEnt*>(tk_smem + TK_OFF_PTAB); }
 
-__device__ __forceinline__ int tk_row0(int rows) { return static_cast<int>(static_cast<long long>(blockIdx.x) * rows / gridDim.x); }
-__device__ __forceinline__ int tk_row1(int rows) { return static_cast<int>(static_cast<long long>(blockIdx.x + 1) * rows / gridDim.x); }
 
 // Stream tile T (numbered over the token) into its ring slot.  `cur` is the
 // calling thread's cursor into the phase table (each thread issues tiles in
 // increasing order, so it only moves forward).
-template <int ULF>
 __device__ __forceinline__ void tk_issue(int T, int& cur)
 {
-    const PhaseEnt* ptab = tk_ptab<ULF>();
+    const PhaseEnt* ptab = tk_ptab();
     while (T >= ptab[cur + 1].T0)
         ++cur;
     const PhaseEnt& e = ptab[cur];
     const KindEnt& k = tk_ktab()[e.kind];
-    const int r0 = tk_row0(k.rows), r1 = tk_row1(k.rows);
-    const int row = r0 + (T - e.T0) * k.R;
-    const int nr = min(k.R, r1 - row);
+    const int row = k.r0 + (T - e.T0) * k.R;
+    const int nr = min(k.R, k.r1 - row);
     const uint32_t bytes = static_cast<uint32_t>(nr * k.row_bytes);
     const int s = T & (TK_NSTAGE - 1);
     uint8_t* dst = tk_smem + s * TK_SLOT;
@@ -98,22 +93,24 @@ __device__ __forceinline__ void tk_issue(int T, int& cur)
     atomicMax(&m.issued_hi, T + 1);
 }
 
-// Grid barrier on a monotonic arrival counter: the block arrives, then waits
-// until the counter reaches `target` (all gridDim.x blocks have arrived as
-// often as this one).  A dead block arrives without waiting.  Returns false
-// when the block is (or has just become) dead.
-__device__ __forceinline__ bool tk_sync(const TokenArgs& a, unsigned target)
+// Grid barrier before phase p (p >= 1) on a monotonic arrival counter: the
+// block arrives, then waits until the counter reaches bar_base + p gridDim.x
+// (every block has arrived p times).  A dead block arrives without waiting.
+// Returns false when the block is (or has just become) dead.
+__device__ __forceinline__ bool tk_sync(int p)
 {
+    const TokenArgs& A = tk_args();
     TkMisc& m = tk_misc();
     __syncthreads();  // the block's phase outputs are written
     if (threadIdx.x == 0) {
+        const unsigned target = A.bar_base + static_cast<unsigned>(p) * gridDim.x;
         int ok = *reinterpret_cast<volatile int*>(&m.dead) == 0;
-        red_release_add(a.bar, 1u);  // release, cumulative over the block's writes through bar.sync
-        if (ok && static_cast<int>(ld_acquire_u32(a.bar) - target) < 0) {
+        red_release_add(A.bar, 1u);  // release, cumulative over the block's writes through bar.sync
+        if (ok && static_cast<int>(ld_acquire_u32(A.bar) - target) < 0) {
             const unsigned long long t0 = globaltimer_ns();
-            while (static_cast<int>(ld_acquire_u32(a.bar) - target) < 0) {
+            while (static_cast<int>(ld_acquire_u32(A.bar) - target) < 0) {
                 if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-                    set_error(a.err, DEVERR_TIMEOUT_BARRIER);
+                    set_error(A.err, DEVERR_TIMEOUT_BARRIER);
                     m.dead = 1;
                     ok = 0;
                     break;
@@ -126,81 +123,67 @@ __device__ __forceinline__ bool tk_sync(const TokenArgs& a, unsigned target)
     return m.sync_ok != 0;
 }
 
-__device__ __forceinline__ void tk_trace(const TokenArgs& a, int nph, int p, int i)
+__device__ __forceinline__ void tk_trace(int p, int i)
 {
-    if (a.trace && threadIdx.x == 0)
-        a.trace[(static_cast<size_t>(blockIdx.x) * nph + p) * 4 + i] = globaltimer_ns();
+    const TokenArgs& A = tk_args();
+    if (A.trace && threadIdx.x == 0)
+        A.trace[(static_cast<size_t>(blockIdx.x) * (5 * A.n_layers + 1) + p) * 4 + i] = globaltimer_ns();
 }
 
-// Epilogue of one output row r (value v0, and v1 of the second matrix).
-template <int EPI>
-__device__ __forceinline__ void tk_epilogue(const TokenArgs& a, int slot, int r, int r0, float v0, float v1)
+// One matrix phase p of kind KIND: prefetch the norm weight, pass the barrier,
+// quantise the activation, consume the phase's tiles and complete them (refill
+// + epilogue).  T is the block's next tile, icur the caller's issue cursor;
+// returns both advanced.
+template <int KIND, int FMT, int PL, int NMAT, int EPI, bool NORM>
+__device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
 {
-    const TkMisc& m = tk_misc();
-    float* y = m.y[slot];
-    if (EPI == EPI_STORE) {
-        y[r] = v0;
-    } else if (EPI == EPI_RESID) {
-        y[r] = tk_resid()[r - r0] + v0;
-    } else if (EPI == EPI_SWIGLU) {
-        y[r] = v0 / (1.0f + expf(-v0)) * v1;
-    } else {  // EPI_QKV: q rows, then k and v rows appended to the cache at pos
-        const int qdim = a.n_q * a.hd, kvdim = a.n_kv * a.hd;
-        if (r < qdim) {
-            y[r] = v0;
-        } else {
-            const int idx = r - qdim;
-            const int which = idx / kvdim, rem = idx - which * kvdim;
-            const int kvh = rem / a.hd, dd = rem - kvh * a.hd;
-            __half* plane = which ? m.vc[slot] : m.kc[slot];
-            plane[(static_cast<size_t>(kvh) * a.max_ctx + a.pos) * a.hd + dd] = __float2half_rn(v0);
-        }
-    }
-}
-
-// One matrix phase: prefetch the norm weight, pass the barrier, quantise the
-// activation, consume the phase's tiles and complete them (refill + epilogue).
-template <int ULF, int KIND, int FMT, int PL, int UL, int NMAT, int EPI, bool NORM>
-__device__ __forceinline__ void tk_gemv(const TokenArgs& a, int nph, int p, bool barrier, unsigned target,
-                                        const float* x, const float* gamma, const float* rsrc, int& T, int& icur)
-{
+    constexpr int P = tk_p(KIND);     // threads per row group, one activation unit each
+    constexpr int RG = tk_rg(KIND);   // row groups
     constexpr int RP = tk_rpt(KIND);  // rows per thread and matrix
-    constexpr int R = TK_RG * RP;     // rows per tile and matrix
-    constexpr int NCH = 2 * UL;       // 4-element activation chunks per thread: K <= 4096 UL
+    constexpr int R = RG * RP;        // rows per tile and matrix
+    constexpr int UL = 1;
+    constexpr int NCH = (8 * P + TK_THREADS - 1) / TK_THREADS;  // 4-element chunks a thread quantises: K <= 32 P
     static_assert(RP * NMAT <= TK_RED_STRIDE, "partial sums per warp");
+    const TokenArgs& A = tk_args();
     const KindEnt& ke = tk_ktab()[KIND];
     const int K = ke.K;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const PhaseEnt* ptab = tk_ptab<ULF>();
+    const PhaseEnt* ptab = tk_ptab();
     const int T0 = ptab[p].T0, ntiles = ptab[p + 1].T0 - T0;
-    const int r0 = tk_row0(ke.rows), r1 = tk_row1(ke.rows);
+    const int r0 = ke.r0, r1 = ke.r1;
     TkMisc& m = tk_misc();
+    const int l = p / 5;
+    const float* x0 = l == 0 ? A.x_in : A.x;  // the residual stream entering layer l
+    const float* x = KIND == PH_QKV ? x0 : KIND == PH_O ? A.attn : KIND == PH_GATEUP || KIND == PH_VOCAB ? A.x : A.act;
+    const float* gamma = KIND == PH_QKV ? A.layers[l].attn_norm : KIND == PH_GATEUP ? A.layers[l].ffn_norm : A.out_norm;
 
-    tk_trace(a, nph, p, 0);
+    tk_trace(p, 0);
     float4 gv[NCH];
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
-        const int ch = tid + NCONS * i;
+        const int ch = tid + TK_THREADS * i;
         gv[i] = make_float4(1.f, 1.f, 1.f, 1.f);
         if (NORM && ch < K / 4)
             gv[i] = __ldg(reinterpret_cast<const float4*>(gamma) + ch);
     }
-    if (barrier ? !tk_sync(a, target) : m.dead != 0)
-        return;
-    tk_trace(a, nph, p, 1);
+    if (p > 0 ? !tk_sync(p) : m.dead != 0)
+        return make_int2(T, icur);
+    tk_trace(p, 1);
 
     float4 xv[NCH];
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
-        const int ch = tid + NCONS * i;
+        const int ch = tid + TK_THREADS * i;
         xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (ch < K / 4)
             xv[i] = __ldcg(reinterpret_cast<const float4*>(x) + ch);
     }
-    if (EPI == EPI_RESID)
-        for (int r = tid; r < r1 - r0; r += NCONS)
+    if (EPI == EPI_RESID) {
+        const float* rsrc = KIND == PH_O ? x0 : A.x;
+        for (int r = tid; r < r1 - r0; r += TK_THREADS)
             tk_resid()[r] = __ldcg(rsrc + r0 + r);
-    float ss = quantise_block<FMT, PL, NCH>(xv, gv, NORM, tk_xq(), K, tid);
+    }
+    float ss = quantise_block<FMT, PL, NCH, TK_THREADS>(xv, gv, NORM, tk_xq(), K, tid);
     if (NORM) {
         ss = warp_sum(ss);
         if (lane == 0)
@@ -211,43 +194,60 @@ __device__ __forceinline__ void tk_gemv(const TokenArgs& a, int nph, int p, bool
     if (NORM) {
         float tot = 0.f;
 #pragma unroll
-        for (int w = 0; w < NCONS_WARPS; ++w)
+        for (int w = 0; w < TK_WARPS; ++w)
             tot += m.gred[w];
-        rstd = 1.0f / sqrtf(tot / static_cast<float>(K) + a.eps);
+        rstd = 1.0f / sqrtf(tot / static_cast<float>(K) + A.eps);
     }
-    const int g = tid / TK_P, pp = tid % TK_P;
+    const int g = tid / P, pp = tid % P;
     UnitState<FMT, PL> us[UL];
     bool have[UL];
-#pragma unroll
-    for (int k = 0; k < UL; ++k)
-        have[k] = (pp + TK_P * k) < K / 32;
-    load_units<FMT, PL, UL>(us, have, tk_xq(), pp, TK_P, rstd);
-    tk_trace(a, nph, p, 2);
+    have[0] = pp < K / 32;
+    load_units<FMT, PL, UL>(us, have, tk_xq(), pp, P, rstd);
+    tk_trace(p, 2);
 
     // Complete tile tc (token tile Tc): wait until every warp released it,
     // refill its slot with tile Tc + TK_NSTAGE, run the epilogue of its rows.
     auto complete = [&](int tc, int Tc) -> bool {
         const int sc = Tc & (TK_NSTAGE - 1);
         if (!mbar_wait(&m.empty[sc], (Tc / TK_NSTAGE) & 1)) {
-            set_error(a.err, DEVERR_TIMEOUT_EMPTY);
+            set_error(A.err, DEVERR_TIMEOUT_EMPTY);
             return false;
         }
         if (lane == 0 && Tc + TK_NSTAGE < m.ttotal)
-            tk_issue<ULF>(Tc + TK_NSTAGE, icur);
-        const float* rb = tk_red() + (Tc & (2 * TK_NSTAGE - 1)) * NCONS_WARPS * TK_RED_STRIDE;
+            tk_issue(Tc + TK_NSTAGE, icur);
+        const float* rb = tk_red() + (Tc & (2 * TK_NSTAGE - 1)) * TK_WARPS * TK_RED_STRIDE;
         const int row0 = r0 + tc * R;
         const int nr = min(R, r1 - row0);
         for (int row = lane; row < nr; row += 32) {
-            const int rg = row % TK_RG, i = row / TK_RG;
-            const float* wb = rb + rg * (TK_P / 32) * TK_RED_STRIDE;
+            const int rg = row % RG, i = row / RG;
+            const float* wb = rb + rg * (P / 32) * TK_RED_STRIDE;
             float v0 = 0.f, v1 = 0.f;
 #pragma unroll
-            for (int w = 0; w < TK_P / 32; ++w) {
+            for (int w = 0; w < P / 32; ++w) {
                 v0 += wb[w * TK_RED_STRIDE + i];
                 if (NMAT == 2)
                     v1 += wb[w * TK_RED_STRIDE + RP + i];
             }
-            tk_epilogue<EPI>(a, p & 1, row0 + row, r0, v0, v1);
+            const int r = row0 + row;
+            if (EPI == EPI_STORE) {
+                A.logits[r] = v0;
+            } else if (EPI == EPI_RESID) {
+                A.x[r] = tk_resid()[r - r0] + v0;
+            } else if (EPI == EPI_SWIGLU) {
+                A.act[r] = v0 / (1.0f + expf(-v0)) * v1;
+            } else {  // EPI_QKV: q rows, then k and v rows appended to the cache at pos
+                const int qdim = A.n_q * A.hd, kvdim = A.n_kv * A.hd;
+                if (r < qdim) {
+                    A.q[r] = v0;
+                } else {
+                    const int idx = r - qdim;
+                    const int which = idx / kvdim, rem = idx - which * kvdim;
+                    const int kvh = rem / A.hd, dd = rem - kvh * A.hd;
+                    const size_t plane = static_cast<size_t>(A.n_kv) * A.max_ctx * A.hd;
+                    __half* kc = A.kv + static_cast<size_t>(l) * 2 * plane + (which ? plane : 0);
+                    kc[(static_cast<size_t>(kvh) * A.max_ctx + A.pos) * A.hd + dd] = __float2half_rn(v0);
+                }
+            }
         }
         return true;
     };
@@ -256,83 +256,90 @@ __device__ __forceinline__ void tk_gemv(const TokenArgs& a, int nph, int p, bool
     for (int t = 0; t < ntiles; ++t, ++T) {
         const int s = T & (TK_NSTAGE - 1);
         if (!mbar_wait(&m.full[s], (T / TK_NSTAGE) & 1)) {
-            set_error(a.err, DEVERR_TIMEOUT_FULL);
+            set_error(A.err, DEVERR_TIMEOUT_FULL);
             ok = false;
             break;
         }
         const int nr = min(R, r1 - (r0 + t * R));
         consume_tile<FMT, PL, UL, RP, NMAT>(
-            tk_smem + s * TK_SLOT, nr, R, TK_RG, g, pp, TK_P, ke.row_bytes, us, have,
-            tk_red() + ((T & (2 * TK_NSTAGE - 1)) * NCONS_WARPS + warp) * TK_RED_STRIDE, lane);
+            tk_smem + s * TK_SLOT, nr, R, RG, g, pp, P, ke.row_bytes, us, have,
+            tk_red() + ((T & (2 * TK_NSTAGE - 1)) * TK_WARPS + warp) * TK_RED_STRIDE, lane);
         if (lane == 0)
             mbar_arrive(&m.empty[s]);
-        if (t >= TK_DEFER && ((T - TK_DEFER) & (NCONS_WARPS - 1)) == warp && !complete(t - TK_DEFER, T - TK_DEFER)) {
+        if (t >= TK_DEFER && (T - TK_DEFER) % TK_WARPS == warp && !complete(t - TK_DEFER, T - TK_DEFER)) {
             ok = false;
             break;
         }
     }
     if (ok)
         for (int tc = max(0, ntiles - TK_DEFER); tc < ntiles; ++tc)
-            if (((T0 + tc) & (NCONS_WARPS - 1)) == warp && !complete(tc, T0 + tc)) {
+            if ((T0 + tc) % TK_WARPS == warp && !complete(tc, T0 + tc)) {
                 ok = false;
                 break;
             }
     if (!ok)
         m.dead = 1;
-    tk_trace(a, nph, p, 3);
+    tk_trace(p, 3);
+    return make_int2(T0 + ntiles, icur);
 }
 
-// Attention phase: items (key chunk, KV head) spread over the blocks.
-__device__ __forceinline__ void tk_attention(const TokenArgs& a, int nph, int p, int l, unsigned target)
+// Attention phase p: items (key chunk, KV head) spread over the blocks.
+__device__ __forceinline__ void tk_attention(int p)
 {
-    tk_trace(a, nph, p, 0);
-    if (!tk_sync(a, target))
+    const TokenArgs& A = tk_args();
+    tk_trace(p, 0);
+    if (!tk_sync(p))
         return;
-    tk_trace(a, nph, p, 1);
-    const int group = a.n_q / a.n_kv;
+    tk_trace(p, 1);
+    const int group = A.n_q / A.n_kv;
     if ((threadIdx.x >> 5) < group) {
-        const size_t plane = static_cast<size_t>(a.n_kv) * a.max_ctx * a.hd;
+        const int l = p / 5;
+        const size_t plane = static_cast<size_t>(A.n_kv) * A.max_ctx * A.hd;
         AttnArgs t;
-        t.q = a.q;
-        t.kc = a.kv + static_cast<size_t>(l) * 2 * plane;
+        t.q = A.q;
+        t.kc = A.kv + static_cast<size_t>(l) * 2 * plane;
         t.vc = t.kc + plane;
-        t.out = a.attn;
-        t.part = a.part;
-        t.counters = a.counters;
-        t.n_q = a.n_q;
-        t.n_kv = a.n_kv;
-        t.max_ctx = a.max_ctx;
-        t.n_keys = a.pos + 1;
+        t.out = A.attn;
+        t.part = A.part;
+        t.counters = A.counters;
+        t.n_q = A.n_q;
+        t.n_kv = A.n_kv;
+        t.max_ctx = A.max_ctx;
+        t.n_keys = A.pos + 1;
         t.step = nullptr;
-        t.err = a.err;
-        const int n_keys = a.pos + 1;
+        t.err = A.err;
+        const int n_keys = A.pos + 1;
         const int L = max((n_keys + ATT_CHUNKS - 1) / ATT_CHUNKS, ATT_MIN_CHUNK);
         const int nact = (n_keys + L - 1) / L;
         AttnSmem& sm = *reinterpret_cast<AttnSmem*>(tk_xq());
-        for (int item = blockIdx.x; item < nact * a.n_kv; item += gridDim.x) {
+        for (int item = blockIdx.x; item < nact * A.n_kv; item += gridDim.x) {
             attn_block(t, item % nact, item / nact, group, sm, false);
             named_bar_sync(ATT_BAR, 32 * group);  // staging free before the next item
         }
     }
-    tk_trace(a, nph, p, 3);
+    tk_trace(p, 3);
 }
 
-template <int ULF>
-__global__ void __launch_bounds__(NCONS, 1) token_kernel(const __grid_constant__ TokenArgs a)
+__global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_constant__ TokenArgs a)
 {
     const int nph = 5 * a.n_layers + 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int G = gridDim.x;
-    PhaseEnt* ptab = tk_ptab<ULF>();
+    PhaseEnt* ptab = tk_ptab();
     KindEnt* ktab = tk_ktab();
     TkMisc& m = tk_misc();
 
+    {  // the arguments to shared memory
+        const int* src = reinterpret_cast<const int*>(&a);
+        int* dst = reinterpret_cast<int*>(tk_smem + TK_OFF_ARGS);
+        for (int i = tid; i < static_cast<int>(sizeof(TokenArgs) / 4); i += TK_THREADS)
+            dst[i] = src[i];
+    }
     if (tid < PH_KINDS) {
         const int qdim = a.n_q * a.hd, kvdim = a.n_kv * a.hd;
         const int q4h = a.hidden / 256 * Q4K_BYTES;
         KindEnt k{};
         k.nmat = 1;
-        k.R = TK_RG * tk_rpt(tid);
+        k.R = tk_rows_per_tile(tid);
         switch (tid) {
         case PH_QKV: k.rows = qdim + 2 * kvdim; k.K = a.hidden; k.row_bytes = q4h; break;
         case PH_ATTN: k.R = 1; break;
@@ -342,11 +349,13 @@ __global__ void __launch_bounds__(NCONS, 1) token_kernel(const __grid_constant__
         case PH_DOWN_Q6: k.rows = a.hidden; k.K = a.ffn; k.row_bytes = a.ffn / 256 * Q6K_BYTES; break;
         default: k.rows = a.vocab; k.K = a.hidden; k.row_bytes = a.hidden / 256 * Q6K_BYTES; break;
         }
+        k.r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * k.rows / gridDim.x);
+        k.r1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * k.rows / gridDim.x);
         ktab[tid] = k;
     }
     __syncthreads();
     // phase table: kind, weights and this block's tile count, then a prefix sum
-    for (int p = tid; p < nph; p += NCONS) {
+    for (int p = tid; p < nph; p += TK_THREADS) {
         PhaseEnt e{a.wvocab, nullptr, 0, PH_VOCAB};
         if (p < nph - 1) {
             const TokenLayer& ly = a.layers[p / 5];
@@ -359,7 +368,7 @@ __global__ void __launch_bounds__(NCONS, 1) token_kernel(const __grid_constant__
             }
         }
         const KindEnt& k = ktab[e.kind];
-        e.T0 = (tk_row1(k.rows) - tk_row0(k.rows) + k.R - 1) / k.R;
+        e.T0 = (k.r1 - k.r0 + k.R - 1) / k.R;
         ptab[p] = e;
     }
     __syncthreads();
@@ -389,13 +398,13 @@ __global__ void __launch_bounds__(NCONS, 1) token_kernel(const __grid_constant__
     if (tid == 0) {
         for (int s = 0; s < TK_NSTAGE; ++s) {
             mbar_init(&m.full[s], 1);
-            mbar_init(&m.empty[s], NCONS_WARPS);
+            mbar_init(&m.empty[s], TK_WARPS);
         }
         fence_mbar_init();
         m.dead = 0;
         m.issued_hi = 0;
         for (int T = 0; T < min(TK_NSTAGE, m.ttotal); ++T)
-            tk_issue<ULF>(T, icur);
+            tk_issue(T, icur);
         if (blockIdx.x == 0) {
             a.step->pos = a.pos;
             a.step->logits = a.logits;
@@ -403,52 +412,23 @@ __global__ void __launch_bounds__(NCONS, 1) token_kernel(const __grid_constant__
     }
     __syncthreads();
 
-    int T = 0;
-    unsigned target = a.bar_base;
-    const size_t plane = static_cast<size_t>(a.n_kv) * a.max_ctx * a.hd;
-    for (int p = 0; p < nph; ++p) {
-        const int l = p / 5;
-        const bool barrier = p > 0;
-        if (barrier)
-            target += static_cast<unsigned>(G);
-        const int kind = ptab[p].kind;
-        // the epilogue's pointers: written before the phase's barrier, read after it
-        if (tid == 0) {
-            m.y[p & 1] = kind == PH_QKV ? a.q : kind == PH_GATEUP ? a.act : kind == PH_VOCAB ? a.logits : a.x;
-            m.kc[p & 1] = a.kv + static_cast<size_t>(l) * 2 * plane;
-            m.vc[p & 1] = m.kc[p & 1] + plane;
-        }
-        const float* x0 = l == 0 ? a.x_in : a.x;  // the residual stream entering layer l
-        switch (kind) {
-        case PH_QKV:
-            tk_gemv<ULF, PH_QKV, FMT_Q4K, 2, 1, 1, EPI_QKV, true>(a, nph, p, barrier, target, x0,
-                                                                  a.layers[l].attn_norm, nullptr, T, icur);
-            break;
-        case PH_ATTN:
-            tk_attention(a, nph, p, l, target);
-            break;
-        case PH_O:
-            tk_gemv<ULF, PH_O, FMT_Q4K, 2, 1, 1, EPI_RESID, false>(a, nph, p, barrier, target, a.attn, nullptr, x0, T,
-                                                                   icur);
-            break;
-        case PH_GATEUP:
-            tk_gemv<ULF, PH_GATEUP, FMT_Q4K, 1, 1, 2, EPI_SWIGLU, true>(a, nph, p, barrier, target, a.x,
-                                                                        a.layers[l].ffn_norm, nullptr, T, icur);
-            break;
-        case PH_DOWN_Q4:
-            tk_gemv<ULF, PH_DOWN_Q4, FMT_Q4K, 1, ULF, 1, EPI_RESID, false>(a, nph, p, barrier, target, a.act, nullptr,
-                                                                           a.x, T, icur);
-            break;
-        case PH_DOWN_Q6:
-            tk_gemv<ULF, PH_DOWN_Q6, FMT_Q6K, 1, ULF, 1, EPI_RESID, false>(a, nph, p, barrier, target, a.act, nullptr,
-                                                                           a.x, T, icur);
-            break;
-        default:
-            tk_gemv<ULF, PH_VOCAB, FMT_Q6K, 1, 1, 1, EPI_STORE, true>(a, nph, p, barrier, target, a.x, a.out_norm,
-                                                                      nullptr, T, icur);
-            break;
-        }
+    // The phases in token order: per layer a straight sequence (a loop over a
+    // switch on the phase kind makes the register allocator keep every kind's
+    // values live at once).
+    int2 st = make_int2(0, icur);  // the block's next tile, this thread's issue cursor
+#pragma unroll 1
+    for (int l = 0; l < a.n_layers; ++l) {
+        const int p = 5 * l;
+        st = tk_gemv<PH_QKV, FMT_Q4K, 2, 1, EPI_QKV, true>(p, st.x, st.y);
+        tk_attention(p + 1);
+        st = tk_gemv<PH_O, FMT_Q4K, 2, 1, EPI_RESID, false>(p + 2, st.x, st.y);
+        st = tk_gemv<PH_GATEUP, FMT_Q4K, 1, 2, EPI_SWIGLU, true>(p + 3, st.x, st.y);
+        if (ptab[p + 4].kind == PH_DOWN_Q6)
+            st = tk_gemv<PH_DOWN_Q6, FMT_Q6K, 1, 1, EPI_RESID, false>(p + 4, st.x, st.y);
+        else
+            st = tk_gemv<PH_DOWN_Q4, FMT_Q4K, 1, 1, EPI_RESID, false>(p + 4, st.x, st.y);
     }
+    st = tk_gemv<PH_VOCAB, FMT_Q6K, 1, 1, EPI_STORE, true>(nph - 1, st.x, st.y);
     // A block that stopped early may still have copies in flight into its
     // shared memory: wait (bounded) for the last ring-full it issued.
     __syncthreads();
@@ -469,59 +449,45 @@ __global__ void __launch_bounds__(NCONS, 1) token_kernel(const __grid_constant__
 
 namespace dqhost {
 
-static TokenKernel token_kernel_for(int ulf)
-{
-    switch (ulf) {
-    case 1: return dq::token_kernel<1>;
-    case 3: return dq::token_kernel<3>;
-    default: return nullptr;
-    }
-}
-
 int plan_token(int n_layers, int hidden, int ffn, int n_q, int n_kv, int hd, bool any_q6_down, TokenPlan* plan)
 {
     using namespace dq;
     const int qdim = n_q * hd;
-    if (hidden > TK_P * 32 || qdim > TK_P * 32 || hidden % 2048 || qdim % 256 || ffn % 256 || hd != ATT_HD ||
-        n_q % n_kv || n_q / n_kv > 8)
+    if (n_layers > TK_MAX_LAYERS || hidden > 32 * tk_p(PH_QKV) || qdim > 32 * tk_p(PH_O) ||
+        ffn > 32 * tk_p(PH_DOWN_Q4) || hidden % 2048 || qdim % 256 || ffn % 256 || hd != ATT_HD || n_q % n_kv ||
+        n_q / n_kv > 8)
         return DQ_ERR_UNSUPPORTED;
     if (any_q6_down && ffn % 2048)
-        return DQ_ERR_UNSUPPORTED;
-    const int ulf = (ffn + TK_P * 32 - 1) / (TK_P * 32);
-    TokenKernel k = token_kernel_for(ulf);
-    if (!k)
         return DQ_ERR_UNSUPPORTED;
     // tiles fit a ring slot
     const int q4h = hidden / 256 * Q4K_BYTES, q4q = qdim / 256 * Q4K_BYTES;
     const int down_rb = ffn / 256 * (any_q6_down ? Q6K_BYTES : Q4K_BYTES);
-    if (TK_RG * tk_rpt(PH_QKV) * q4h > TK_SLOT || TK_RG * tk_rpt(PH_O) * q4q > TK_SLOT ||
-        2 * TK_RG * tk_rpt(PH_GATEUP) * q4h > TK_SLOT || TK_RG * tk_rpt(PH_DOWN_Q6) * down_rb > TK_SLOT ||
-        TK_RG * tk_rpt(PH_VOCAB) * (hidden / 256 * Q6K_BYTES) > TK_SLOT)
+    if (tk_rows_per_tile(PH_QKV) * q4h > TK_SLOT || tk_rows_per_tile(PH_O) * q4q > TK_SLOT ||
+        2 * tk_rows_per_tile(PH_GATEUP) * q4h > TK_SLOT || tk_rows_per_tile(PH_DOWN_Q6) * down_rb > TK_SLOT ||
+        tk_rows_per_tile(PH_VOCAB) * (hidden / 256 * Q6K_BYTES) > TK_SLOT)
         return DQ_ERR_UNSUPPORTED;
     const int grid = sm_count();
     if ((hidden + grid - 1) / grid + 1 > TK_RESID_MAX)
         return DQ_ERR_UNSUPPORTED;
-    const int nph = 5 * n_layers + 1;
-    const int smem = tk_smem_bytes(ulf, nph);
+    const int smem = tk_smem_bytes(hidden, qdim, ffn);
     if (smem > 227 * 1024)
         return DQ_ERR_UNSUPPORTED;
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem);
+    const void* k = reinterpret_cast<const void*>(token_kernel);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return DQ_ERR_UNSUPPORTED;
     }
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void*>(k), NCONS, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, TK_THREADS, smem);
     if (e != cudaSuccess || per_sm < 1) {
         cudaGetLastError();
         return DQ_ERR_UNSUPPORTED;
     }
-    plan->ulf = ulf;
-    plan->nph = nph;
+    plan->nph = 5 * n_layers + 1;
     plan->grid = grid;
     plan->smem_bytes = smem;
-    plan->kernel = k;
+    plan->kernel = token_kernel;
     return DQ_OK;
 }
 
@@ -529,7 +495,7 @@ cudaError_t launch_token(const TokenPlan& plan, const dq::TokenArgs& a, cudaStre
 {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(plan.grid);
-    cfg.blockDim = dim3(dq::NCONS);
+    cfg.blockDim = dim3(dq::TK_THREADS);
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

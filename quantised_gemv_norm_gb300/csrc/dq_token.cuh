@@ -5,21 +5,23 @@
 
 namespace dq {
 
+constexpr int TK_THREADS = 384;    // 12 warps: 168 registers a thread for the phases' activation slices
+constexpr int TK_WARPS = TK_THREADS / 32;
 constexpr int TK_NSTAGE = 4;       // weight ring slots per block
 constexpr int TK_SLOT = 40960;     // bytes per slot (largest tile: 4 Q6_K rows of K = 12288)
-constexpr int TK_P = 128;          // threads per row group
-constexpr int TK_RG = NCONS / TK_P;
 constexpr int TK_DEFER = 2;        // a stage is completed this many stages after it is consumed
 constexpr int TK_RED_STRIDE = 4;   // floats per warp in one partial-sum slot
 
 // Phase kinds.  Per layer: QKV, ATTN, O, GATEUP, DOWN (Q4_K or Q6_K); then VOCAB.
 enum { PH_QKV = 0, PH_ATTN, PH_O, PH_GATEUP, PH_DOWN_Q4, PH_DOWN_Q6, PH_VOCAB, PH_KINDS };
 
-// Rows streamed per tile and matrix, by kind (row groups x rows per thread).
-__host__ __device__ constexpr int tk_rpt(int kind)
-{
-    return kind == PH_QKV || kind == PH_O ? 4 : kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 1 : 2;
-}
+// Consumer layout by kind: row groups of tk_p threads (each thread holds one
+// 32-element unit of the activation, so K <= 32 tk_p), tk_rpt rows per thread
+// and matrix; a tile holds TK_THREADS / tk_p * tk_rpt rows of each matrix.
+__host__ __device__ constexpr int tk_p(int kind) { return kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? TK_THREADS : 128; }
+__host__ __device__ constexpr int tk_rg(int kind) { return TK_THREADS / tk_p(kind); }
+__host__ __device__ constexpr int tk_rpt(int kind) { return kind == PH_GATEUP ? 2 : 4; }
+__host__ __device__ constexpr int tk_rows_per_tile(int kind) { return tk_rg(kind) * tk_rpt(kind); }
 
 struct TokenLayer {
     const float* attn_norm;
@@ -64,33 +66,34 @@ struct PhaseEnt {
 };
 
 struct KindEnt {
-    int rows, K, row_bytes, R, nmat, pad[3];
+    int rows, K, row_bytes, R, nmat;
+    int r0, r1;  // this block's rows [r0, r1) of each matrix
+    int pad;
 };
 
 // Shared memory of one block, at fixed offsets: the weight ring, the per-warp
 // partial sums, barriers and flags, the kind table, the block's residual rows,
-// the quantised activation (aliased by the attention staging), then the phase
-// table, whose length depends on the layer count.
-constexpr int TK_RESID_MAX = 64;  // residual rows of one block at most
+// the phase table, then the quantised activation (aliased by the attention
+// staging), whose size depends on the model shape.
+constexpr int TK_RESID_MAX = 64;   // residual rows of one block at most
+constexpr int TK_MAX_LAYERS = 64;
 constexpr int TK_OFF_RED = TK_NSTAGE * TK_SLOT;
-constexpr int TK_OFF_MISC = TK_OFF_RED + 2 * TK_NSTAGE * NCONS_WARPS * TK_RED_STRIDE * 4;
-constexpr int TK_OFF_KTAB = TK_OFF_MISC + 256;
+constexpr int TK_OFF_MISC = TK_OFF_RED + 2 * TK_NSTAGE * TK_WARPS * TK_RED_STRIDE * 4;
+constexpr int TK_OFF_ARGS = TK_OFF_MISC + 256;
+constexpr int TK_OFF_KTAB = TK_OFF_ARGS + (static_cast<int>(sizeof(TokenArgs)) + 127) / 128 * 128;
 constexpr int TK_OFF_RESID = TK_OFF_KTAB + 256;
-constexpr int TK_OFF_XQ = TK_OFF_RESID + TK_RESID_MAX * 4;
+constexpr int TK_OFF_PTAB = TK_OFF_RESID + TK_RESID_MAX * 4;
+constexpr int TK_OFF_XQ = TK_OFF_PTAB + ((5 * TK_MAX_LAYERS + 2) * static_cast<int>(sizeof(PhaseEnt)) + 127) / 128 * 128;
 
-__host__ __device__ constexpr int tk_max(int x, int y) { return x > y ? x : y; }
-
-// Bytes of the quantised-activation region: K <= 4096 with two planes (Q|K|V,
-// O), K <= 4096 ULF with one plane (down), and the attention staging.
-__host__ __device__ constexpr int tk_xq_bytes(int ulf)
+// Shared-memory bytes of the block for a model shape: the quantised
+// activation of the largest input (two planes for Q|K|V and O, one for the
+// down projection) or the attention staging, whichever is larger.
+__host__ __device__ inline int tk_smem_bytes(int hidden, int qdim, int ffn)
 {
-    return (tk_max(tk_max(TK_P * xq_words(2) * 4, ulf * TK_P * xq_words(1) * 4), static_cast<int>(sizeof(AttnSmem))) +
-            127) / 128 * 128;
-}
-__host__ __device__ constexpr int tk_off_ptab(int ulf) { return TK_OFF_XQ + tk_xq_bytes(ulf); }
-__host__ __device__ constexpr int tk_smem_bytes(int ulf, int nph)
-{
-    return tk_off_ptab(ulf) + (nph + 1) * static_cast<int>(sizeof(PhaseEnt));
+    int xq = (hidden > qdim ? hidden : qdim) / 32 * xq_words(2) * 4;
+    xq = xq > ffn / 32 * xq_words(1) * 4 ? xq : ffn / 32 * xq_words(1) * 4;
+    xq = xq > static_cast<int>(sizeof(AttnSmem)) ? xq : static_cast<int>(sizeof(AttnSmem));
+    return TK_OFF_XQ + xq;
 }
 
 }  // namespace dq
@@ -100,7 +103,6 @@ namespace dqhost {
 using TokenKernel = void (*)(dq::TokenArgs);
 
 struct TokenPlan {
-    int ulf;          // activation units per thread of the down projection
     int nph;          // phases per token (5 per layer + 1)
     int grid;         // one block per SM
     int smem_bytes;
@@ -108,8 +110,8 @@ struct TokenPlan {
 };
 
 // Whether the persistent token kernel covers this model shape (DQ_OK) or not
-// (DQ_ERR_UNSUPPORTED): hidden and n_q head_dim <= 4096, ffn <= 16384 (12288
-// with a Q6_K down projection), and the block's shared memory fits.
+// (DQ_ERR_UNSUPPORTED): at most 64 layers, hidden and n_q head_dim <= 4096,
+// ffn <= 12288, and the block's shared memory fits.
 int plan_token(int n_layers, int hidden, int ffn, int n_q, int n_kv, int hd, bool any_q6_down, TokenPlan* plan);
 
 // Cooperative launch of one token on `stream` (grid barriers need every block resident).

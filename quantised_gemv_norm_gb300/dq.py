@@ -253,7 +253,7 @@ class _Desc(ctypes.Structure):
 
 
 MODEL_NO_PDL = 1
-MODEL_KERNELS = 2  # run the token as separate kernels even where the fused token kernel applies
+MODEL_FUSED = 2  # run the token as one persistent kernel where the shape allows
 
 
 class Model:

@@ -248,7 +248,7 @@ def _run_decode(dq, orc, m, kv, positions, use_graph=True, seed=0, emulate=False
     return outs
 
 
-MODES = {"fused": (0, True), "kernels": (2, False)}  # flags (DQ_MODEL_KERNELS = 2), expected fused
+MODES = {"fused": (2, True), "kernels": (0, False)}  # flags (DQ_MODEL_FUSED = 2), expected fused
 
 
 @pytest.mark.parametrize("mode", ["fused", "kernels"])
@@ -275,8 +275,8 @@ def test_decode_small_model_eager_equals_graph(dq, orc):
     m = synth.make_model(22, n_layers=2, hidden=2048, ffn=4096, n_q_heads=8, n_kv_heads=2, head_dim=128,
                          vocab=777, max_ctx=40)
     kv = synth.make_kv_cache(22, m, 30)
-    eager = _run_decode(dq, orc, m, kv, [30, 31], use_graph=False, emulate=True, flags=2, fused=False)
-    graph = _run_decode(dq, orc, m, kv, [30, 31], use_graph=True, emulate=True, flags=2, fused=False)
+    eager = _run_decode(dq, orc, m, kv, [30, 31], use_graph=False, emulate=True, fused=False)
+    graph = _run_decode(dq, orc, m, kv, [30, 31], use_graph=True, emulate=True, fused=False)
     for a, b in zip(eager, graph):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
@@ -286,8 +286,8 @@ def test_decode_fused_is_deterministic(dq, orc):
     m = synth.make_model(24, n_layers=2, hidden=2048, ffn=4096, n_q_heads=8, n_kv_heads=2, head_dim=128,
                          vocab=500, max_ctx=80)
     kv = synth.make_kv_cache(24, m, 70)
-    a = _run_decode(dq, orc, m, kv, [70, 71], emulate=True, fused=True)
-    b = _run_decode(dq, orc, m, kv, [70, 71], emulate=True, fused=True)
+    a = _run_decode(dq, orc, m, kv, [70, 71], emulate=True, flags=2, fused=True)
+    b = _run_decode(dq, orc, m, kv, [70, 71], emulate=True, flags=2, fused=True)
     for x, y in zip(a, b):
         assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
 
@@ -297,7 +297,7 @@ def test_decode_shape_outside_fused_kernel_runs_kernels(dq, orc):
     m = synth.make_model(25, n_layers=1, hidden=6144, ffn=2048, n_q_heads=8, n_kv_heads=2, head_dim=128,
                          vocab=256, max_ctx=16)
     kv = synth.make_kv_cache(25, m, 3)
-    _run_decode(dq, orc, m, kv, [3], emulate=True, fused=False)
+    _run_decode(dq, orc, m, kv, [3], emulate=True, flags=2, fused=False)
 
 
 _QWEN = {}
