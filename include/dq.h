@@ -85,7 +85,9 @@ DQ_API int dq_last_cuda_error(void);
 /* Synchronises `stream`, then reads and clears the current device's error flag:
  * 0 if no kernel gave up a bounded wait since the last call, else a bit mask
  * (1 consumer timeout, 2 producer timeout, 4 copies in flight at exit,
- * 8 bad argument seen on the device).  Returns DQ_ERR_CUDA on a CUDA error. */
+ * 8 bad argument seen on the device, 16 grid-barrier timeout in the fused
+ * token kernel, 32 tensor-core completion timeout).  Returns DQ_ERR_CUDA on a
+ * CUDA error. */
 DQ_API int dq_device_error(void* stream);
 
 /* ------------------------------------------------------------------- norms
@@ -207,8 +209,24 @@ DQ_API int dq_attention_decode_static(const float* q, const void* k_plane, const
  * "The roofline holds on a second GPU", section "The Math": M tokens share one
  * read of the weights; below M* = (w/16)(R/BW) memory bounds the product, above
  * it arithmetic does.  Y[m][r] = sum_k W[r][k] * X[m][k] for m < M.
- * W: Q4_K blocks [rows][K/256]; X fp32 [M][K]; Y fp32 [M][rows].
- * 1 <= M <= 64; K as dq_gemv_q4k.  Errors as dq_gemv_q4k. */
+ * W: Q4_K blocks [rows][K/256] (16-byte aligned); X fp32 [M][K] (16-byte
+ * aligned); Y fp32 [M][rows].  1 <= M <= 64, K a positive multiple of 256.
+ *
+ * Paths: DQ_MATMUL_CUDA_CORE runs the streaming GEMV once per token (reads W
+ * M times; K <= 16384).  DQ_MATMUL_TENSOR reads W once for all tokens on the
+ * tensor cores (tcgen05.mma, fp16 operands: each weight and activation is
+ * rounded to fp16, |X| must stay below 65504; fp32 accumulation).
+ * DQ_MATMUL_AUTO picks CUDA cores for M = 1 and tensor cores for M >= 2.
+ * Errors: NULL -> DQ_ERR_NULL; M, rows, K or path out of range ->
+ * DQ_ERR_SHAPE; misaligned W or X -> DQ_ERR_ALIGN; CUDA-core path with
+ * K > 16384 -> DQ_ERR_UNSUPPORTED; a CUDA error -> DQ_ERR_CUDA. */
+#define DQ_MATMUL_AUTO 0
+#define DQ_MATMUL_CUDA_CORE 1
+#define DQ_MATMUL_TENSOR 2
+DQ_API int dq_matmul_q4k_path(const void* W_blocks, const float* X, float* Y, int M, int rows, int K, int path,
+                              void* stream);
+
+/* dq_matmul_q4k_path with DQ_MATMUL_AUTO. */
 DQ_API int dq_matmul_q4k(const void* W_blocks, const float* X, float* Y, int M, int rows, int K, void* stream);
 
 /* -------------------------------------------------------------- decode step

@@ -1,0 +1,93 @@
+// dq_tc.cuh -- 5th-generation tensor core (tcgen05) helpers: tensor-memory
+// allocation, the UMMA shared-memory and instruction descriptors, the MMA
+// issue and commit, and tensor-memory loads.  Inline PTX for sm_103a.
+#pragma once
+
+#include "dq_common.cuh"
+
+namespace dq {
+
+// ------------------------------------------------------------ tensor memory
+
+// Allocate `ncols` (a power of two >= 32) columns of tensor memory for this
+// block; the base address is written to *dst (shared).  Executed by one
+// whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Generic-proxy writes to shared memory made visible to the async proxy (the
+// tensor core reads its operands through it).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// -------------------------------------------------------------- descriptors
+
+// Shared-memory matrix descriptor, K-major operand without swizzling: the
+// operand is tiled by 8-row x 16-byte core matrices (each 128 contiguous
+// bytes); core matrices adjacent along K are `lbo` bytes apart, those
+// adjacent along M (or N) `sbo` bytes apart.  Bits 46-48 hold the fixed
+// descriptor version 0b001; base offset, stride mode and swizzle are 0.
+__device__ __forceinline__ uint64_t umma_desc_kmajor(const void* smem_ptr, uint32_t lbo, uint32_t sbo)
+{
+    const uint64_t start = (smem_addr(smem_ptr) >> 4) & 0x3FFFu;
+    return start | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of kind::f16 with fp16 A and B, fp32 accumulator,
+// both operands K-major, dense: D format at bits 4-5 (1 = F32), A and B
+// formats at 7-9 and 10-12 (0 = F16), N / 8 at bits 17-22, M / 16 at 24-28.
+__host__ __device__ constexpr uint32_t umma_idesc_f16_f32(int M, int N)
+{
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D (tensor memory) [+]= A (shared, M x 16) * B (shared, 16 x N): one MMA of
+// K = 16, issued by one thread.  `accum` = 0 overwrites D.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accum)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+// Arrive once on `bar` when every MMA this thread issued before has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+// 16 consecutive 32-bit columns of the warp's 32 tensor-memory lanes: thread
+// `lane` receives lane (taddr's lane + lane), columns taddr's column + 0..15.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+}  // namespace dq

@@ -39,6 +39,7 @@ SIGNATURES = {
     "dq_attention_decode": (I, [P, P, P, P, I, I, I, I, I, P, SZ, P]),
     "dq_attention_decode_static": (I, [P, P, P, P, I, I, I, I, I, P]),
     "dq_matmul_q4k": (I, [P, P, P, I, I, I, P]),
+    "dq_matmul_q4k_path": (I, [P, P, P, I, I, I, I, P]),
     "dq_model_create": (I, [P, P]),
     "dq_decode_step": (I, [P, P, I, P, P]),
     "dq_model_launches_per_step": (I, [P]),
@@ -186,14 +187,21 @@ def dequant_q6k(blocks: torch.Tensor, out=None):
     return out
 
 
-def matmul_q4k(W: torch.Tensor, X: torch.Tensor, out=None):
-    """W: uint8 [rows, K/256*144]; X: fp32 [M, K] -> fp32 [M, rows]."""
+MATMUL_AUTO, MATMUL_CUDA_CORE, MATMUL_TENSOR = 0, 1, 2
+
+
+def matmul_q4k(W: torch.Tensor, X: torch.Tensor, out=None, path: int = MATMUL_AUTO):
+    """W: uint8 [rows, K/256*144]; X: fp32 [M, K] -> fp32 [M, rows].
+
+    ``path``: MATMUL_AUTO (CUDA cores at M = 1, tensor cores above),
+    MATMUL_CUDA_CORE (one GEMV per token) or MATMUL_TENSOR (one read of W)."""
     lib = load()
     rows = W.shape[0]
     K = quant_K(FMT_Q4K, W.shape[1])
     M = X.shape[0]
     out = torch.empty((M, rows), dtype=torch.float32, device=W.device) if out is None else out
-    _check("dq_matmul_q4k", lib.dq_matmul_q4k(_ptr(W), _ptr(X), _ptr(out), M, rows, K, _stream()))
+    _check("dq_matmul_q4k_path",
+           lib.dq_matmul_q4k_path(_ptr(W), _ptr(X), _ptr(out), M, rows, K, int(path), _stream()))
     return out
 
 

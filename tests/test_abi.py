@@ -68,6 +68,10 @@ def test_argument_errors_return_before_launch(lib):
     assert lib.dq_attention_decode(fake, fake, fake, fake, 32, 8, 128, 16, 17, fake, 1 << 20, None) == -2
     assert lib.dq_attention_decode(fake, fake, fake, fake, 32, 8, 128, 16, 4, fake, 8, None) == -2
     assert lib.dq_matmul_q4k(fake, fake, fake, 65, 4, 256, None) == -2
+    assert lib.dq_matmul_q4k(fake, fake, fake, 2, 4, 300, None) == -2         # K not a multiple of 256
+    assert lib.dq_matmul_q4k_path(fake, fake, fake, 2, 4, 256, 3, None) == -2  # no such path
+    assert lib.dq_matmul_q4k_path(P(17), fake, fake, 2, 4, 256, 2, None) == -3
+    assert lib.dq_matmul_q4k_path(fake, fake, fake, 2, 4, 32768, 1, None) == -4
     assert lib.dq_decode_step(None, fake, 0, fake, None) == -1
     h = P()
     assert lib.dq_model_create(None, ctypes.byref(h)) == -1

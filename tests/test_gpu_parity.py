@@ -196,10 +196,23 @@ def test_matmul_q4k(dq, orc, M):
     rows, K = 12288, 4096
     W = synth.quant_matrix(9, synth.FMT_Q4K, rows, K)
     X = np.stack([synth.activation(9, K, m) for m in range(M)])
-    Y = dq.matmul_q4k(cuda(W), cuda(X)).cpu().numpy()
     R = orc.matmul_q4k(W, X, rows, K)
+    for path in (dq.MATMUL_AUTO, dq.MATMUL_CUDA_CORE, dq.MATMUL_TENSOR):
+        Y = dq.matmul_q4k(cuda(W), cuda(X), path=path).cpu().numpy()
+        for m in range(M):
+            assert normwise(Y[m], R[m]) <= GEMV_TOL, (path, m)
+
+
+@pytest.mark.parametrize("rows,K,M", [(1000, 256, 3), (20000, 512, 17), (152, 1024, 33), (77, 2048, 64)])
+def test_matmul_q4k_tensor_shapes(dq, orc, rows, K, M):
+    # ragged row tiles, a single block column, several 128-row tiles per block, one row per block
+    W = synth.quant_matrix(11, synth.FMT_Q4K, rows, K)
+    X = np.stack([synth.activation(11, K, m) for m in range(M)])
+    R = orc.matmul_q4k(W, X, rows, K)
+    Y = dq.matmul_q4k(cuda(W), cuda(X), path=dq.MATMUL_TENSOR).cpu().numpy()
     for m in range(M):
-        assert normwise(Y[m], R[m]) <= GEMV_TOL
+        assert normwise(Y[m], R[m]) <= GEMV_TOL, m
+    assert dq.device_error() == 0
 
 
 # -------------------------------------------------------------- decode
