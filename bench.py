@@ -41,6 +41,7 @@ WORKLOAD = ("Qwen3-8B-shaped decode token: 36 layers (Q4_K attention q|k|v 6144x
 # ("The roofline holds on a second GPU", "How I ran it": 248.8 / 253.9 / 255.1 tok/s); median.
 PAGES_BASELINE_TOK_S = 253.9
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0  # dense, burst; fp16 runs at the same tensor rate
 KERNEL_KINDS = ("qkv", "attention", "o_proj", "gate_up", "down", "vocab")
 
 
@@ -80,6 +81,15 @@ def measured_peaks():
         except Exception:
             pass
     return None, "fallback"
+
+
+def tensor_peak_tflops():
+    d, _ = measured_peaks()
+    if d:
+        for key in ("bf16_tflops", "bf16_TFLOPs"):
+            if key in d and isinstance(d[key], (int, float)):
+                return float(d[key]), "of measured"
+    return FALLBACK_BF16_TFLOPS, "of fallback"
 
 
 def hbm_peak_gbs():
@@ -296,6 +306,28 @@ def run_ours(args):
         ctx = {"tokens_per_s": round(K * world / s512, 2), "bytes_per_token": tb512,
                "GBps": round(tb512 * K / s512 / 1e9, 1)}
 
+    # ---- the same token as one persistent kernel (opt-in mode), for comparison
+    fused = {}
+    if not args.no_fused:
+        fmodel = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=True, flags=dq.MODEL_FUSED)
+        if fmodel.fused:
+            for t in range(W):
+                fmodel.step_raw(xs[t].data_ptr(), 0, logits.data_ptr(), sh)
+            torch.cuda.synchronize(device)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for t in range(K):
+                fmodel.step_raw(xs[W + t].data_ptr(), 0, logits.data_ptr(), sh)
+            b.record(stream)
+            torch.cuda.synchronize(device)
+            fs = aggregate_max(a.elapsed_time(b) / 1e3, world, device)
+            fused = {"tokens_per_s": round(K * world / fs, 2), "ms_per_step": round(fs / K * 1e3, 4),
+                     "launches_per_step": fmodel.launches_per_step}
+        fmodel.close()
+
+    # ---- M-token sweep of one Q4_K matrix (tensor cores vs one GEMV per token)
+    msweep = run_msweep(device) if not args.no_msweep else {}
+
     tb = token_bytes(0)
     out = {
         "metric": METRIC,
@@ -320,6 +352,8 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src},
         "per_kernel": per_kernel,
         "ctx512": ctx,
+        "fused_token_kernel": fused,
+        "msweep": msweep,
         "e2e": {"value": round(K * world / e2e_max, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * m.hidden,
                 "d2h_bytes_per_step": 4 * m.vocab},
         "gpu_launches": model.launches_per_step * K,
@@ -336,6 +370,52 @@ def run_ours(args):
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+SWEEP_ROWS, SWEEP_K = 12288, 4096
+SWEEP_M = (1, 2, 4, 8, 16, 64)
+
+
+def run_msweep(device, reps: int = 20) -> dict:
+    """Y[M x 12288] = X[M x 4096] W^T over one Q4_K matrix for M in SWEEP_M, both
+    paths, each call on the next of enough device copies of W to exceed L2
+    (every call reads W from HBM).  Time per call from CUDA events."""
+    import torch
+
+    from quantised_gemv_norm_gb300 import dq
+
+    W = torch.from_numpy(synth.quant_matrix(SEED, synth.FMT_Q4K, SWEEP_ROWS, SWEEP_K)).to(device)
+    wbytes = W.numel()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    copies = [W] + [W.clone() for _ in range(max(1, (3 * l2) // wbytes))]
+    X = torch.from_numpy(np.stack([synth.activation(SEED, SWEEP_K, m) for m in range(max(SWEEP_M))])).to(device)
+    Y = torch.empty((max(SWEEP_M), SWEEP_ROWS), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    out = {"rows": SWEEP_ROWS, "K": SWEEP_K, "weight_bytes": wbytes, "copies_rotated": len(copies)}
+    for name, path in (("tensor", dq.MATMUL_TENSOR), ("cuda_core", dq.MATMUL_CUDA_CORE)):
+        res = {}
+        for M in SWEEP_M:
+            Xm, Ym = X[:M], Y[:M]
+            for i in range(3):
+                dq.matmul_q4k(copies[i % len(copies)], Xm, out=Ym, path=path)
+            torch.cuda.synchronize(device)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(reps):
+                dq.matmul_q4k(copies[i % len(copies)], Xm, out=Ym, path=path)
+            b.record(stream)
+            torch.cuda.synchronize(device)
+            us = a.elapsed_time(b) * 1e3 / reps
+            res[str(M)] = {"us": round(us, 2), "GBps": round(wbytes / us / 1e3, 1),
+                           "TFLOPs": round(2.0 * M * SWEEP_ROWS * SWEEP_K / us / 1e6, 2)}
+        out[name] = res
+    R, rsrc = tensor_peak_tflops()
+    bw, bsrc = hbm_peak_gbs()
+    out["predicted_M_star"] = round(ledger.m_star(4.5, R * 1e12, bw * 1e9), 1)
+    out["M_star_inputs"] = {"R_TFLOPs": R, "R_source": rsrc, "BW_GBps": bw, "BW_source": bsrc}
+    t1 = out["tensor"]["1"]["us"]
+    out["tensor_cost_ratio_vs_M1"] = {k: round(v["us"] / t1, 3) for k, v in out["tensor"].items()}
+    return out
 
 
 def run_kernel_probe(args):
@@ -430,6 +510,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--no-ctx512", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fused", action="store_true", help="skip the fused-token-kernel comparison")
+    ap.add_argument("--no-msweep", action="store_true", help="skip the M-token sweep")
+    ap.add_argument("--msweep-only", action="store_true", help="print only the M-token sweep")
     ap.add_argument("--kernel-probe", choices=KERNEL_KINDS, default=None,
                     help="profiling aid: build a 2-layer full-width stack, run one token, then launch this "
                          "kernel kind alone --probe-reps times (for ncu -k ... -s 9 -c 1)")
@@ -437,6 +520,15 @@ def main():
     args = ap.parse_args()
     if args.kernel_probe:
         run_kernel_probe(args)
+        return
+    if args.msweep_only:
+        import torch
+
+        from quantised_gemv_norm_gb300 import build, dq
+
+        build.build()
+        dq.load()
+        print(json.dumps({"msweep": run_msweep(torch.device("cuda", 0))}), flush=True)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -151,7 +151,11 @@ DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows,
  * block and phase at buffer[4 (block * phases + phase)] (phases = 5 n_layers
  * + 1: per layer Q|K|V, attention, O, gate/up, down; then the vocabulary):
  * phase entered, grid barrier passed, activation in registers, phase done;
- * 32 bytes per block and phase.  NULL turns tracing off.  Not for use while
+ * 32 bytes per block and phase.  A tensor-core dq_matmul_q4k_path writes, for
+ * block 0 and its first 32 half-block stages, 8 SM clock stamps per stage at
+ * buffer[8 stage]: operands seen ready and MMAs issued (control thread), stage
+ * start, weights landed, operand buffer free and stage written (thread 0).
+ * NULL turns tracing off.  Not for use while
  * another thread launches kernels of the library. */
 DQ_API int dq_debug_trace(void* buffer);
 
@@ -216,7 +220,8 @@ DQ_API int dq_attention_decode_static(const float* q, const void* k_plane, const
  * M times; K <= 16384).  DQ_MATMUL_TENSOR reads W once for all tokens on the
  * tensor cores (tcgen05.mma, fp16 operands: each weight and activation is
  * rounded to fp16, |X| must stay below 65504; fp32 accumulation).
- * DQ_MATMUL_AUTO picks CUDA cores for M = 1 and tensor cores for M >= 2.
+ * DQ_MATMUL_AUTO picks CUDA cores for M <= 2 and tensor cores for M >= 3 (the
+ * measured crossover on the 12288 x 4096 table).
  * Errors: NULL -> DQ_ERR_NULL; M, rows, K or path out of range ->
  * DQ_ERR_SHAPE; misaligned W or X -> DQ_ERR_ALIGN; CUDA-core path with
  * K > 16384 -> DQ_ERR_UNSUPPORTED; a CUDA error -> DQ_ERR_CUDA. */

@@ -7,20 +7,27 @@
 //   * CUDA cores: the single-vector streaming GEMV once per token (reads the
 //     weights M times; the M = 1 path and the comparison point);
 //   * tensor cores (M >= 2): every weight is read once for all M tokens.  Each
-//     block takes a contiguous range of rows (at most 128 per tile) and walks
-//     K in Q4_K block columns: the blocks' bytes stream into a shared-memory
-//     ring with 1-D bulk copies, all threads dequantise one half block (128 K)
-//     at a time to fp16 in the UMMA K-major core-matrix layout, the tokens'
-//     activations are staged beside it as fp16, and one thread issues eight
-//     tcgen05.mma (M = 128, N = tokens rounded up to 16, K = 16) accumulating
-//     in fp32 in tensor memory.  Dequantisation of the next half block
-//     overlaps the MMAs of the current one (double-buffered operands; the
-//     MMAs' commit releases a buffer).  The epilogue reads the accumulator
-//     with tcgen05.ld and writes Y.
+//     block takes a contiguous range of rows (at most 128 per tile: one row
+//     per tensor-memory lane) and walks K in Q4_K block columns.  Each block
+//     column of the tile's rows (one 144-byte block per row, rows row_bytes
+//     apart) streams into a shared-memory ring with one 2-D tensor (TMA) copy.
+//     Per half block (128 K) every thread dequantises 64 weights of one row to
+//     fp16 in registers and stores them straight into an A buffer in tensor
+//     memory (tcgen05.st); the tokens' activations are staged in shared memory
+//     as fp16 in the UMMA K-major core-matrix layout; one thread issues eight
+//     tcgen05.mma (M = 128, N = tokens rounded up to 16, K = 16, A from tensor
+//     memory) accumulating in fp32 in tensor memory.  Two A/B buffers: the
+//     next half block is dequantised while the MMAs run; their commit releases
+//     a buffer.  The epilogue reads the accumulator with tcgen05.ld.
+//     A in tensor memory keeps the dequantised weights out of shared memory,
+//     whose bandwidth the MMAs would otherwise share with the dequantisation.
 //
 // fp16 and not bf16 operands: a dequantised Q4_K weight d sc q - dmin m has up
 // to 21 significant bits; fp16 keeps 11 (relative error 2^-12 per weight,
 // about 1e-4 normwise on a row), bf16 only 8 (about 1e-3, half the tolerance).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "dq_gemv_host.h"
@@ -28,26 +35,56 @@
 
 namespace dq {
 
-constexpr int MM_THREADS = 256;
+constexpr int MM_DQ_WARPS = 16;                // dequantisation / staging / epilogue warps
+constexpr int MM_CTRL = MM_DQ_WARPS;           // the control warp: copies and MMAs
+constexpr int MM_THREADS = 32 * (MM_DQ_WARPS + 1);
 constexpr int MM_ROWS = 128;                   // rows per tile = UMMA M
 constexpr int MM_KC = 128;                     // K per MMA stage: half a Q4_K block
-constexpr int MM_NS = 4;                       // ring slots, one Q4_K block column of the tile's rows each
-constexpr int MM_SLOT = MM_ROWS * Q4K_BYTES;   // 18432 bytes
-constexpr int MM_A_BYTES = MM_ROWS * MM_KC * 2;
+constexpr int MM_BPS = 4;                      // Q4_K block columns per ring slot
+constexpr int MM_ROWB = MM_BPS * Q4K_BYTES + 16;  // 592: a slot row (4 blocks and 16 bytes of the next;
+                                                  // the odd 16-byte stride keeps 8 rows on distinct banks)
+constexpr int MM_NS_MAX = 4;
+constexpr int MM_ACC = 4;                      // independent accumulators (MMA s of a stage adds into s % 4)
+constexpr int MM_TA_COLS = MM_KC / 2;          // columns of one A buffer (two fp16 per column)
+// Tensor memory: accumulator i in columns [i NT, (i + 1) NT), then the two A buffers.
+__host__ __device__ constexpr int mm_ta_col(int nt) { return MM_ACC * nt; }
+__host__ __device__ constexpr uint32_t mm_tmem_cols(int nt)
+{
+    return MM_ACC * nt + 2 * MM_TA_COLS <= 256 ? 256u : 512u;
+}
 constexpr int MM_LBO = 128;                    // bytes between core matrices adjacent along K
 constexpr int MM_SBO = (MM_KC / 8) * 128;      // bytes between 8-row (8-token) groups
 constexpr int DEVERR_TIMEOUT_MMA = 32;
 
 __host__ __device__ constexpr int mm_b_bytes(int nt) { return nt * MM_KC * 2; }
-__host__ __device__ constexpr int mm_smem_bytes(int nt) { return MM_NS * MM_SLOT + 2 * MM_A_BYTES + 2 * mm_b_bytes(nt) + 128; }
+// A ring slot: box_rows rows of MM_ROWB bytes, the slot start 128-byte aligned (tensor copy destination).
+__host__ __device__ constexpr int mm_slot_bytes(int box_rows) { return (box_rows * MM_ROWB + 127) / 128 * 128; }
+__host__ __device__ constexpr int mm_smem_bytes(int nt, int ns, int box_rows)
+{
+    return ns * mm_slot_bytes(box_rows) + 2 * mm_b_bytes(nt) + 128;
+}
 
 struct MmArgs {
-    const uint8_t* W;  // Q4_K rows of row_bytes
+    CUtensorMap tmap;  // W as a 2-D array of 8-byte words [rows][row_bytes / 8], box MM_ROWB bytes x box_rows
     const float* X;    // [M][K]
     float* Y;          // [M][rows]
     int M, rows, K;
+    int box_rows;      // rows one tensor copy brings (>= the rows of any tile of a block)
+    int ns;            // ring slots (2 or 4)
+    unsigned long long* trace;  // diagnostics: block 0's per-stage cycle stamps when not null
     int* err;
 };
+
+// 2-D tensor copy global -> shared of the box at (x bytes, y rows), completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
 
 // Byte offset of element (r, k) in a K-major core-matrix tile with MM_KC columns.
 __device__ __forceinline__ int mm_off(int r, int k)
@@ -80,15 +117,16 @@ template <int NT>
 __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __grid_constant__ MmArgs a)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
+    const int slot_bytes = mm_slot_bytes(a.box_rows);
     uint8_t* ring = sm;
-    uint8_t* Abuf = sm + MM_NS * MM_SLOT;
-    uint8_t* Bbuf = Abuf + 2 * MM_A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(Bbuf + 2 * mm_b_bytes(NT));  // [MM_NS]
-    uint64_t* mmad = full + MM_NS;                                            // [2]: buffer's MMAs done
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mmad + 2);
+    uint8_t* Bbuf = sm + a.ns * slot_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(Bbuf + 2 * mm_b_bytes(NT));  // [MM_NS_MAX] slot landed
+    uint64_t* opready = full + MM_NS_MAX;                                     // [2] operands of a stage written
+    uint64_t* opfree = opready + 2;                                           // [2] a stage's MMAs done
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(opfree + 2);
     volatile int* fail = reinterpret_cast<volatile int*>(tslot + 1);
     int* issued = const_cast<int*>(fail) + 1;   // one past the last block column issued (over the block's tiles)
-    int* committed = issued + 1;                // one past the last half-chunk committed
+    int* committed = issued + 1;                // one past the last stage committed
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, b = blockIdx.x;
@@ -97,17 +135,16 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
     if (r1b <= r0b)
         return;
     const int nblk = a.K / 256;
-    const size_t row_bytes = static_cast<size_t>(nblk) * Q4K_BYTES;
-    constexpr uint32_t NCOLS = NT < 32 ? 32 : NT;
-    const uint64_t pol = l2_evict_first_policy();
 
     if (warp == 0)
-        tmem_alloc(tslot, NCOLS);
+        tmem_alloc(tslot, mm_tmem_cols(NT));
     if (tid == 0) {
-        for (int s = 0; s < MM_NS; ++s)
+        for (int s = 0; s < a.ns; ++s)
             mbar_init(&full[s], 1);
-        mbar_init(&mmad[0], 1);
-        mbar_init(&mmad[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&opready[i], MM_DQ_WARPS);
+            mbar_init(&opfree[i], 1);
+        }
         fence_mbar_init();
         *fail = 0;
         *issued = 0;
@@ -117,8 +154,8 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tbase = *tslot;
-    constexpr uint32_t idesc = umma_idesc_f16_f32(MM_ROWS, NT);
 
+    // a bounded wait; false once this block has given up
     auto wait = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
         if (*fail)
             return false;
@@ -129,143 +166,220 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
         }
         return true;
     };
+    // the same by a whole warp, with one outcome for all its lanes (tcgen05.ld/st are warp-collective)
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
+        return __all_sync(0xffffffffu, wait(bar, parity, code)) != 0;
+    };
 
-    int bg0 = 0;  // block columns of earlier tiles (ring slot and phase continue)
-    int g0 = 0;   // half-chunks of earlier tiles (operand buffer and phase continue)
-    for (int rt0 = r0b; rt0 < r1b && !*fail; rt0 += MM_ROWS) {
-        const int nrows = min(MM_ROWS, r1b - rt0);
-        const uint8_t* Wt = a.W + static_cast<size_t>(rt0) * row_bytes;
-        // warp 0 streams block column c of the tile's rows into its ring slot
-        auto issue = [&](int c) {
-            const int bg = bg0 + c;
-            const int s = bg % MM_NS;
-            if (lane == 0)
-                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nrows * Q4K_BYTES));
-            __syncwarp();
-            for (int r = lane; r < nrows; r += 32)
-                bulk_g2s(ring + s * MM_SLOT + r * Q4K_BYTES, Wt + r * row_bytes + static_cast<size_t>(c) * Q4K_BYTES,
-                         Q4K_BYTES, &full[s], pol);
-            if (lane == 0)
-                *issued = bg + 1;
-        };
-        if (warp == 0)
-            for (int c = 0; c < min(MM_NS, nblk); ++c)
-                issue(c);
-
-        for (int hc = 0; hc < 2 * nblk; ++hc) {
-            const int c = hc >> 1, half = hc & 1;
-            const int g = g0 + hc, buf = g & 1;
-            const int bg = bg0 + c;
-            if (half == 0 && !wait(&full[bg % MM_NS], (bg / MM_NS) & 1, DEVERR_TIMEOUT_FULL))
-                break;
-            if (g >= 2 && !wait(&mmad[buf], ((g - 2) >> 1) & 1, DEVERR_TIMEOUT_MMA))
-                break;
-            uint8_t* At = Abuf + buf * MM_A_BYTES;
-            uint8_t* Bt = Bbuf + buf * mm_b_bytes(NT);
-            const uint8_t* slot = ring + (bg % MM_NS) * MM_SLOT;
-            // weights: 128 rows x 4 sub-blocks of 32 of this half block, two units a thread
-#pragma unroll
-            for (int i = 0; i < (MM_ROWS * 4) / MM_THREADS; ++i) {
-                const int u = tid + MM_THREADS * i;
-                const int row = u >> 2, jj = u & 3, j = 4 * half + jj;
-                if (row < nrows) {
-                    const uint8_t* bp = slot + row * Q4K_BYTES;
-                    const uint4 hd = lds128(bp);
-                    const uint4 cw = lds128(bp + 16 + 16 * j);
-                    const uint32_t s_lo = j < 6 ? hd.y : hd.z, s_hi = j < 6 ? hd.z : hd.w;
-                    const uint32_t m_lo = j < 3 ? hd.z : hd.w, m_hi = j < 3 ? hd.w : 0u;
-                    const int sc = static_cast<int>(__funnelshift_r(s_lo, s_hi, (6 * j) & 31) & 63u);
-                    const int mn = static_cast<int>(__funnelshift_r(m_lo, m_hi, (48 + 6 * j) & 31) & 63u);
-                    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
-                    const __half2 A = __float2half2_rn(d * static_cast<float>(sc));
-                    const __half2 B = __float2half2_rn(dmin * static_cast<float>(mn));
-                    // byte i of the 16: low nibble weight 32j + i, high nibble weight 32j + 16 + i
-                    uint32_t lo[8], hi[8];
-                    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const uint32_t t = __byte_perm(words[w], 0u, 0x3120);  // b0 b2 b1 b3
-                        mm_dequant_word(t, A, B, lo[2 * w], lo[2 * w + 1], hi[2 * w], hi[2 * w + 1]);
-                    }
-                    const int k0 = 32 * jj;  // within the 128-wide stage
-                    *reinterpret_cast<uint4*>(At + mm_off(row, k0)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    *reinterpret_cast<uint4*>(At + mm_off(row, k0 + 8)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-                    *reinterpret_cast<uint4*>(At + mm_off(row, k0 + 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(At + mm_off(row, k0 + 24)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-                }
-            }
-            // activations: tokens x 16 groups of 8 K, fp32 -> fp16
-            const int kbase = c * 256 + half * MM_KC;
-            for (int it = tid; it < a.M * (MM_KC / 8); it += MM_THREADS) {
-                const int n = it >> 4, kg = it & 15;
-                const float4* xp = reinterpret_cast<const float4*>(a.X + static_cast<size_t>(n) * a.K + kbase + 8 * kg);
-                const float4 x0 = __ldg(xp), x1 = __ldg(xp + 1);
-                const uint4 v = make_uint4(h2_bits(__floats2half2_rn(x0.x, x0.y)), h2_bits(__floats2half2_rn(x0.z, x0.w)),
-                                           h2_bits(__floats2half2_rn(x1.x, x1.y)), h2_bits(__floats2half2_rn(x1.z, x1.w)));
-                *reinterpret_cast<uint4*>(Bt + mm_off(n, 8 * kg)) = v;
-            }
-            fence_proxy_async_smem();
-            __syncthreads();
-            if (*fail)
-                break;
-            if (warp == 0) {
-                if (lane == 0) {
+    if (warp == MM_CTRL) {
+        // ---- control: the ring's copies and the MMAs (one thread)
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_f16_f32(MM_ROWS, NT);
+            const uint64_t pol = l2_evict_first_policy();
+            const int ngrp = (nblk + MM_BPS - 1) / MM_BPS;  // slot loads per tile
+            int bg0 = 0, g0 = 0;
+            bool ok = true;
+            for (int rt0 = r0b; rt0 < r1b && ok; rt0 += MM_ROWS) {
+                // block columns [4 q, 4 q + 4) of the tile's rows into a ring slot (box_rows >=
+                // the tile's rows: extra rows are the next block's or zero fill, as are the
+                // bytes past the end of a row)
+                auto issue = [&](int q) {
+                    const int bg = bg0 + q;
+                    const int s = bg % a.ns;
+                    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(a.box_rows * MM_ROWB));
+                    tma_load_2d(ring + s * slot_bytes, &a.tmap, q * (MM_BPS * Q4K_BYTES / 8), rt0, &full[s], pol);
+                    *issued = bg + 1;
+                };
+                for (int q = 0; q < min(a.ns, ngrp); ++q)
+                    issue(q);
+                for (int hc = 0; hc < 2 * nblk; ++hc) {
+                    const int g = g0 + hc, buf = g & 1, c = hc >> 1;
+                    if (!(ok = wait(&opready[buf], (g >> 1) & 1, DEVERR_TIMEOUT_FULL)))
+                        break;
+                    unsigned long long* tr = (a.trace && b == 0 && hc < 32) ? a.trace + 8 * hc : nullptr;
+                    if (tr)
+                        tr[0] = clock64();
                     tc_fence_after_sync();
+                    const uint32_t ta = tbase + mm_ta_col(NT) + MM_TA_COLS * buf;
+                    const uint64_t bd = umma_desc_kmajor(Bbuf + buf * mm_b_bytes(NT), MM_LBO, MM_SBO);
+                    // K = 16 per MMA: 8 columns of A, two core matrices of B.  MMA s adds
+                    // into accumulator s % MM_ACC, so consecutive MMAs do not wait on each other.
 #pragma unroll
                     for (int s = 0; s < MM_KC / 16; ++s)
-                        umma_f16(tbase, umma_desc_kmajor(At + s * 2 * MM_LBO, MM_LBO, MM_SBO),
-                                 umma_desc_kmajor(Bt + s * 2 * MM_LBO, MM_LBO, MM_SBO), idesc, (hc > 0 || s > 0) ? 1u : 0u);
-                    umma_commit(&mmad[buf]);
+                        umma_f16_ta(tbase + NT * (s % MM_ACC), ta + 8 * s,
+                                    bd + static_cast<uint64_t>((2 * MM_LBO * s) >> 4), idesc,
+                                    (hc > 0 || s >= MM_ACC) ? 1u : 0u);
+                    umma_commit(&opfree[buf]);
                     *committed = g + 1;
+                    if (tr)
+                        tr[1] = clock64();
+                    // the last stage of a slot's block columns is dequantised: refill the slot
+                    const int q = c / MM_BPS;
+                    if ((hc + 1 == 2 * nblk || (hc + 1) % (2 * MM_BPS) == 0) && q + a.ns < ngrp)
+                        issue(q + a.ns);
                 }
-                __syncwarp();
-                // the slot's block column is dequantised: refill it
-                if (half == 1 && c + MM_NS < nblk)
-                    issue(c + MM_NS);
+                bg0 += ngrp;
+                g0 += 2 * nblk;
             }
         }
-        if (*fail)
-            break;
-        // accumulator complete -> Y
-        const int glast = g0 + 2 * nblk - 1;
-        wait(&mmad[glast & 1], (glast >> 1) & 1, DEVERR_TIMEOUT_MMA);
-        __syncthreads();  // the flag is read uniformly: tcgen05.ld is warp-collective
-        tc_fence_after_sync();
-        const bool ok = !*fail;
-        if (warp < 4 && ok) {
-            const int row = 32 * warp + lane;
+        __syncwarp();  // the warp reconverges before the block-wide barrier below
+    } else {
+        // ---- dequantisation, activation staging and the epilogue (8 warps)
+        constexpr int NDQ = 32 * MM_DQ_WARPS;
+        constexpr int NXI = (NT * (MM_KC / 8) + NDQ - 1) / NDQ;  // activation items a thread stages
+        const int ngrp = (nblk + MM_BPS - 1) / MM_BPS;
+        int bg0 = 0, g0 = 0;
+        for (int rt0 = r0b; rt0 < r1b; rt0 += MM_ROWS) {
+            const int nrows = min(MM_ROWS, r1b - rt0);
+            // the tokens' activations of stage hc + 1 are loaded while stage hc is
+            // processed (item t = tid + 256 i: token t % NT, 8-element group t / NT)
+            float4 xn[NXI][2];
+            auto load_x = [&](int hcn) {
+                const int kb = (hcn >> 1) * 256 + (hcn & 1) * MM_KC;
 #pragma unroll
-            for (int cc = 0; cc < NT / 16; ++cc) {
-                uint32_t v[16];
-                tmem_ld16(tbase + (static_cast<uint32_t>(32 * warp) << 16) + 16 * cc, v);
-                tmem_ld_wait();
-                if (row < nrows) {
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const int n = 16 * cc + q;
-                        if (n < a.M)
-                            a.Y[static_cast<size_t>(n) * a.rows + rt0 + row] = __uint_as_float(v[q]);
+                for (int i = 0; i < NXI; ++i) {
+                    const int it = tid + NDQ * i;
+                    const int n = it % NT, kg = it / NT;
+                    if (it < NT * (MM_KC / 8) && n < a.M && hcn < 2 * nblk) {
+                        const float4* xp =
+                            reinterpret_cast<const float4*>(a.X + static_cast<size_t>(n) * a.K + kb + 8 * kg);
+                        xn[i][0] = __ldg(xp);
+                        xn[i][1] = __ldg(xp + 1);
                     }
                 }
+            };
+            load_x(0);
+            bool ok = true;
+            for (int hc = 0; hc < 2 * nblk; ++hc) {
+                const int c = hc >> 1, half = hc & 1;
+                const int g = g0 + hc, buf = g & 1;
+                const int bg = bg0 + c / MM_BPS;
+                unsigned long long* tr = (a.trace && b == 0 && tid == 0 && hc < 32) ? a.trace + 8 * hc : nullptr;
+                if (tr)
+                    tr[2] = clock64();
+                if (hc % (2 * MM_BPS) == 0 && !(ok = warp_wait(&full[bg % a.ns], (bg / a.ns) & 1, DEVERR_TIMEOUT_FULL)))
+                    break;
+                if (tr)
+                    tr[3] = clock64();
+                if (g >= 2 && !(ok = warp_wait(&opfree[buf], ((g - 2) >> 1) & 1, DEVERR_TIMEOUT_MMA)))
+                    break;
+                if (tr)
+                    tr[4] = clock64();
+                uint8_t* Bt = Bbuf + buf * mm_b_bytes(NT);
+                const uint8_t* slot = ring + (bg % a.ns) * slot_bytes + (c % MM_BPS) * Q4K_BYTES;
+                // weights: thread (warp w, lane) dequantises row 32 (w % 4) + lane,
+                // sub-block 4 half + w / 4 of this half block, into the A buffer in tensor
+                // memory (one lane per row, two fp16 per column; the four warps of a lane
+                // quarter take the four sub-blocks)
+                {
+                    const int row = 32 * (warp & 3) + lane;
+                    const int j = 4 * half + (warp >> 2);
+                    uint32_t v[16];
+                    if (row < nrows) {
+                        const uint8_t* bp = slot + row * MM_ROWB;
+                        const uint4 hd = lds128(bp);
+                        const uint4 cw = lds128(bp + 16 + 16 * j);
+                        const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+                        const uint32_t s_lo = j < 6 ? hd.y : hd.z, s_hi = j < 6 ? hd.z : hd.w;
+                        const uint32_t m_lo = j < 3 ? hd.z : hd.w, m_hi = j < 3 ? hd.w : 0u;
+                        const int sc = static_cast<int>(__funnelshift_r(s_lo, s_hi, (6 * j) & 31) & 63u);
+                        const int mn = static_cast<int>(__funnelshift_r(m_lo, m_hi, (48 + 6 * j) & 31) & 63u);
+                        const __half2 A = __float2half2_rn(d * static_cast<float>(sc));
+                        const __half2 B = __float2half2_rn(dmin * static_cast<float>(mn));
+                        // byte i of the 16: low nibble weight 32j + i, high nibble weight
+                        // 32j + 16 + i; column c of the sub-block holds weights 2c, 2c + 1
+                        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const uint32_t t = __byte_perm(words[w], 0u, 0x3120);  // b0 b2 b1 b3
+                            mm_dequant_word(t, A, B, v[2 * w], v[2 * w + 1], v[8 + 2 * w], v[8 + 2 * w + 1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            v[i] = 0u;
+                    }
+                    tmem_st16(tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + mm_ta_col(NT) +
+                                  MM_TA_COLS * buf + 16 * (warp >> 2),
+                              v);
+                }
+                // activations: fp32 -> fp16 into the B buffer (consecutive threads take
+                // consecutive tokens), then the next stage's loads
+#pragma unroll
+                for (int i = 0; i < NXI; ++i) {
+                    const int it = tid + NDQ * i;
+                    const int n = it % NT, kg = it / NT;
+                    if (it < NT * (MM_KC / 8) && n < a.M) {
+                        const float4 x0 = xn[i][0], x1 = xn[i][1];
+                        const uint4 v = make_uint4(
+                            h2_bits(__floats2half2_rn(x0.x, x0.y)), h2_bits(__floats2half2_rn(x0.z, x0.w)),
+                            h2_bits(__floats2half2_rn(x1.x, x1.y)), h2_bits(__floats2half2_rn(x1.z, x1.w)));
+                        *reinterpret_cast<uint4*>(Bt + mm_off(n, 8 * kg)) = v;
+                    }
+                }
+                load_x(hc + 1);
+                tmem_st_wait();
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                if (tr)
+                    tr[5] = clock64();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&opready[buf]);  // release: this warp's part of stage g is written
             }
+            if (!ok)
+                break;
+            // accumulator complete -> Y (warps 0-3: one lane quarter each)
+            if (warp < 4) {
+                const int glast = g0 + 2 * nblk - 1;
+                if (!warp_wait(&opfree[glast & 1], (glast >> 1) & 1, DEVERR_TIMEOUT_MMA))
+                    break;
+                tc_fence_after_sync();
+                const int row = 32 * warp + lane;
+#pragma unroll
+                for (int cc = 0; cc < NT / 16; ++cc) {
+                    float y[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        y[q] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < MM_ACC; ++i) {  // the accumulators' sum, in a fixed order
+                        uint32_t v[16];
+                        tmem_ld16(tbase + (static_cast<uint32_t>(32 * warp) << 16) + NT * i + 16 * cc, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            y[q] += __uint_as_float(v[q]);
+                    }
+                    if (row < nrows) {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const int n = 16 * cc + q;
+                            if (n < a.M)
+                                a.Y[static_cast<size_t>(n) * a.rows + rt0 + row] = y[q];
+                        }
+                    }
+                }
+                // The next tile's first MMAs overwrite the accumulator only after this
+                // warp's arrival on that tile's first stage, which follows these reads.
+                tc_fence_before_sync();
+            }
+            bg0 += ngrp;
+            g0 += 2 * nblk;
         }
-        tc_fence_before_sync();
-        __syncthreads();  // accumulator read before the next tile's MMAs overwrite it
-        bg0 += nblk;
-        g0 += 2 * nblk;
     }
     // After a failed wait: let this block's copies and MMAs in flight finish (bounded).
     __syncthreads();
     if (tid == 0 && *fail) {
         const int hi = *issued, gc = *committed;
-        for (int bg = max(0, hi - MM_NS); bg < hi; ++bg) {
+        for (int bg = max(0, hi - a.ns); bg < hi; ++bg) {
             const unsigned long long t0 = globaltimer_ns();
-            while (!mbar_try_wait(&full[bg % MM_NS], (bg / MM_NS) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+            while (!mbar_try_wait(&full[bg % a.ns], (bg / a.ns) & 1) && globaltimer_ns() - t0 < 100000000ull) {
             }
         }
         for (int g = max(0, gc - 2); g < gc; ++g) {
             const unsigned long long t0 = globaltimer_ns();
-            while (!mbar_try_wait(&mmad[g & 1], (g >> 1) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+            while (!mbar_try_wait(&opfree[g & 1], (g >> 1) & 1) && globaltimer_ns() - t0 < 100000000ull) {
             }
         }
     }
@@ -273,7 +387,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
     __syncthreads();
     if (warp == 0) {
         tc_fence_after_sync();
-        tmem_dealloc(tbase, NCOLS);
+        tmem_dealloc(tbase, mm_tmem_cols(NT));
     }
 }
 
@@ -282,6 +396,24 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
 namespace dqhost {
 
 static int mm_nt(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+static EncodeTiled encode_tiled()
+{
+    static std::once_flag once;
+    static EncodeTiled fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
 
 static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, int rows, int K, cudaStream_t s)
 {
@@ -292,15 +424,38 @@ static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, i
     void (*k)(dq::MmArgs) = nt == 16 ? dq::matmul_q4k_tc_kernel<16>
                           : nt == 32 ? dq::matmul_q4k_tc_kernel<32>
                                      : dq::matmul_q4k_tc_kernel<64>;
-    const int smem = dq::mm_smem_bytes(nt);
     std::call_once(once[idx], [&] {
         attr_err[idx] = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (attr_err[idx] != cudaSuccess)
         return set_cuda_error(attr_err[idx]);
-    dq::MmArgs a{W, X, Y, M, rows, K, device_error_flag()};
+    EncodeTiled enc = encode_tiled();
+    if (!enc)
+        return DQ_ERR_UNSUPPORTED;
     const int grid = std::min(sm_count(), rows);
+    const int per_block = (rows + grid - 1) / grid;
+    dq::MmArgs a{};
+    a.X = X;
+    a.Y = Y;
+    a.M = M;
+    a.rows = rows;
+    a.K = K;
+    a.box_rows = std::min(dq::MM_ROWS, per_block);
+    a.err = device_error_flag();
+    a.trace = gemv_trace();
+    // as many ring slots as fit (4, else 2)
+    a.ns = dq::mm_smem_bytes(nt, 4, a.box_rows) <= 227 * 1024 ? 4 : 2;
+    const int smem = dq::mm_smem_bytes(nt, a.ns, a.box_rows);
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(K / 256) * dq::Q4K_BYTES;
+    const cuuint64_t dims[2] = {row_bytes / 8, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(dq::MM_ROWB / 8), static_cast<cuuint32_t>(a.box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&a.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(W), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return DQ_ERR_UNSUPPORTED;
     k<<<grid, dq::MM_THREADS, smem, s>>>(a);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DQ_OK : set_cuda_error(e);
@@ -319,7 +474,8 @@ DQ_API int dq_matmul_q4k_path(const void* W_blocks, const float* X, float* Y, in
         return DQ_ERR_SHAPE;
     if (!dqhost::aligned16(W_blocks) || !dqhost::aligned16(X))
         return DQ_ERR_ALIGN;
-    const bool tensor = path == DQ_MATMUL_TENSOR || (path == DQ_MATMUL_AUTO && M >= 2);
+    // measured crossover: one GEMV per token is faster up to M = 2
+    const bool tensor = path == DQ_MATMUL_TENSOR || (path == DQ_MATMUL_AUTO && M >= 3);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (tensor)
         return dqhost::launch_matmul_tc(static_cast<const uint8_t*>(W_blocks), X, Y, M, rows, K, s);
