@@ -146,12 +146,17 @@ DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows,
  * dependency wait, after the activation is staged, after it is quantised,
  * when the first weight stage is ready; then the latest warp end time and the
  * count of finished warps (both accumulated: zero the buffer before a launch).
- * The buffer needs 64 bytes per block (at most one block per SM).  A
- * dq_decode_step that runs the fused token kernel writes instead 4 values per
- * block and phase at buffer[4 (block * phases + phase)] (phases = 5 n_layers
+ * Block 0 also writes SM clock stamps for its first 64 stages after the
+ * per-block values, at buffer[8 * blocks + i]: [2t] stage t ready, [2t + 1]
+ * thread 0 done with it, [128 + t] stage t's copy issued.  The buffer needs
+ * 64 bytes per block (at most one block per SM) plus 1536 bytes.  A
+ * dq_decode_step that runs the fused token kernel writes instead 8 values per
+ * block and phase at buffer[8 (block * phases + phase)] (phases = 5 n_layers
  * + 1: per layer Q|K|V, attention, O, gate/up, down; then the vocabulary):
- * phase entered, grid barrier passed, activation in registers, phase done;
- * 32 bytes per block and phase.  A tensor-core dq_matmul_q4k_path writes, for
+ * global-timer ns at [0] phase entered, [6] this block's barrier arrival,
+ * [2] grid barrier passed, [4] phase done; SM clock cycles at [3] barrier passed, [5] activation quantised,
+ * [7] activation in registers, [1] first weight tile ready; 64 bytes per
+ * block and phase.  A tensor-core dq_matmul_q4k_path writes, for
  * block 0 and its first 32 half-block stages, 8 SM clock stamps per stage at
  * buffer[8 stage]: operands seen ready and MMAs issued (control thread), stage
  * start, weights landed, operand buffer free and stage written (thread 0).

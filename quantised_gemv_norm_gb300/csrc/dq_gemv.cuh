@@ -385,38 +385,34 @@ __device__ __forceinline__ float quantise_block(float4 (&v)[NCH], const float4 (
 // One stage of the consumers: this thread's unit products for rows g, g + RG,
 // ... (RPT of them, each of NMAT matrices) of the tile, reduced over the warp
 // into wred[0 .. RPT NMAT) (the warp's partial sums; matrix m, row i at m RPT + i).
+// nidx[k] is the unit thread k-slot k reads: its own unit, or a valid stand-in
+// whose activation is zero (load_units) when the thread has none.  Rows past
+// the tile's last (a partial last tile) are computed from stale stage bytes and
+// never stored, so the loop has no branches.
 template <int FMT, int PL, int UL, int RPT, int NMAT>
-__device__ __forceinline__ void consume_tile(const uint8_t* tile, int nr, int R, int RG, int g, int p, int P,
-                                             int row_bytes, const UnitState<FMT, PL> (&us)[UL],
-                                             const bool (&have)[UL], float* wred, int lane)
+__device__ __forceinline__ void consume_tile(const uint8_t* tile, int R, int RG, int g, int row_bytes,
+                                             const UnitState<FMT, PL> (&us)[UL], const int (&nidx)[UL], float* wred,
+                                             int lane)
 {
     constexpr int NV = RPT * NMAT;
     float acc[NV];
 #pragma unroll
-    for (int v = 0; v < NV; ++v)
-        acc[v] = 0.f;
-#pragma unroll
     for (int i = 0; i < RPT; ++i) {
         const int row = g + RG * i;
-        if (row < nr) {
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m) {
-                const uint8_t* rp = tile + static_cast<size_t>(m * R + row) * row_bytes;
-                float sum = 0.f;
+        for (int m = 0; m < NMAT; ++m) {
+            const uint8_t* rp = tile + static_cast<size_t>(m * R + row) * row_bytes;
+            float sum = 0.f;
 #pragma unroll
-                for (int k = 0; k < UL; ++k) {
-                    if (have[k]) {
-                        const int n = p + P * k;
-                        if (FMT == FMT_Q4K)
-                            sum += q4k_unit<PL>(rp, n, reinterpret_cast<const XQ<PL>&>(us[k]));
-                        else if (FMT == FMT_Q6K)
-                            sum += q6k_unit(rp, n, reinterpret_cast<const XQ<1>&>(us[k]));
-                        else
-                            sum += bf16_unit(rp, n, reinterpret_cast<const uint32_t(&)[4]>(us[k]));
-                    }
-                }
-                acc[m * RPT + i] = sum;
+            for (int k = 0; k < UL; ++k) {
+                if (FMT == FMT_Q4K)
+                    sum += q4k_unit<PL>(rp, nidx[k], reinterpret_cast<const XQ<PL>&>(us[k]));
+                else if (FMT == FMT_Q6K)
+                    sum += q6k_unit(rp, nidx[k], reinterpret_cast<const XQ<1>&>(us[k]));
+                else
+                    sum += bf16_unit(rp, nidx[k], reinterpret_cast<const uint32_t(&)[4]>(us[k]));
             }
+            acc[m * RPT + i] = sum;
         }
     }
     warp_transpose_reduce<NV>(acc, lane);
@@ -433,8 +429,18 @@ __device__ __forceinline__ void load_units(UnitState<FMT, PL> (&us)[UL], const b
 {
 #pragma unroll
     for (int k = 0; k < UL; ++k) {
-        if (have[k]) {
-            XQ<PL>& u = reinterpret_cast<XQ<PL>&>(us[k]);
+        XQ<PL>& u = reinterpret_cast<XQ<PL>&>(us[k]);
+        if (!have[k]) {  // no unit: a zero activation (its products vanish)
+#pragma unroll
+            for (int w = 0; w < 16; ++w)
+                u.q[w] = 0u;
+            if (PL == 2)
+#pragma unroll
+                for (int w = 0; w < 16; ++w)
+                    u.l[w] = 0u;
+            u.s = u.f = u.hsum = 0.f;
+            u.s32a = u.s32b = 0;
+        } else {
             const uint32_t* src = xq + (unit_k0<FMT>(p + P * k) >> 5) * xq_words(PL);
 #pragma unroll
             for (int w = 0; w < 16; w += 4) {
@@ -480,6 +486,9 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
     pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     unsigned long long* trace = a.trace ? a.trace + 8 * blockIdx.x : nullptr;
+    // block 0 also records SM clocks per stage: [2t] stage t ready (thread 0), [2t + 1]
+    // thread 0 done with it, [128 + t] stage t issued (t < 64)
+    unsigned long long* ttile = (a.trace && blockIdx.x == 0) ? a.trace + 8 * gridDim.x : nullptr;
     if (trace && tid == 0)
         trace[0] = globaltimer_ns();
     const int r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * a.rows / gridDim.x);
@@ -496,8 +505,11 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         }
         fence_mbar_init();
         // weights and the norm weight never depend on the previous kernel
-        for (int t = 0; t < min(a.nstage, ntiles); ++t)
+        for (int t = 0; t < min(a.nstage, ntiles); ++t) {
             issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, t, r0, r1, R, pol);
+            if (ttile)
+                ttile[128 + t] = clock64();
+        }
     }
     // the norm weight never depends on the previous kernel either
     float4 gv[QCHUNKS], xv[QCHUNKS];
@@ -534,9 +546,12 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
 
     UnitState<FMT, PL> us[UL];
     bool have[UL];
+    int nidx[UL];
 #pragma unroll
-    for (int k = 0; k < UL; ++k)
+    for (int k = 0; k < UL; ++k) {
         have[k] = (p + P * k) < U;
+        nidx[k] = have[k] ? p + P * k : U - 1;  // a stand-in for a missing unit (zero activation)
+    }
 
     if (FMT == FMT_BF16) {
 #pragma unroll
@@ -588,9 +603,12 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             set_error(a.err, DEVERR_TIMEOUT_EMPTY);
             return false;
         }
-        if (lane == 0 && tc + a.nstage < ntiles)
+        if (lane == 0 && tc + a.nstage < ntiles) {
             issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, tc + a.nstage, r0, r1, R,
                              pol);
+            if (ttile && tc + a.nstage < 64)
+                ttile[128 + tc + a.nstage] = clock64();
+        }
         const float* rb = red + rslot * NCONS_WARPS * NV;
         const int row0 = r0 + tc * R;
         const int nr = min(R, r1 - row0);
@@ -640,12 +658,15 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         }
         if (trace && t == 0 && tid == 0)
             trace[5] = globaltimer_ns();
+        if (ttile && tid == 0 && t < 64)
+            ttile[2 * t] = clock64();
         const uint8_t* tile = smem + static_cast<size_t>(s) * a.stage_bytes;
-        const int nr = min(R, r1 - (r0 + t * R));
-        consume_tile<FMT, PL, UL, RPT, NMAT>(tile, nr, R, a.RG, g, p, P, a.row_bytes, us, have,
+        consume_tile<FMT, PL, UL, RPT, NMAT>(tile, R, a.RG, g, a.row_bytes, us, nidx,
                                              red + rslot * NCONS_WARPS * NV + warp * NV, lane);
         if (lane == 0)
             mbar_arrive(&empty[s]);  // release semantics: the partial sums are visible to the completer
+        if (ttile && tid == 0 && t < 64)
+            ttile[2 * t + 1] = clock64();
         const int tc = t - DEFER;
         if (tc >= 0 && (tc & (NCONS_WARPS - 1)) == warp) {
             int sc = s - DEFER, rc = rslot - DEFER;

@@ -32,12 +32,15 @@ namespace dq {
 
 constexpr int DEVERR_TIMEOUT_BARRIER = 16;
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
+
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p)
 {
     unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v)
 {
@@ -97,6 +100,8 @@ __device__ __forceinline__ void tk_issue(int T, int& cur)
 // block arrives, then waits until the counter reaches bar_base + p gridDim.x
 // (every block has arrived p times).  A dead block arrives without waiting.
 // Returns false when the block is (or has just become) dead.
+__device__ __forceinline__ void tk_trace(int p, int i);
+
 __device__ __forceinline__ bool tk_sync(int p)
 {
     const TokenArgs& A = tk_args();
@@ -105,10 +110,11 @@ __device__ __forceinline__ bool tk_sync(int p)
     if (threadIdx.x == 0) {
         const unsigned target = A.bar_base + static_cast<unsigned>(p) * gridDim.x;
         int ok = *reinterpret_cast<volatile int*>(&m.dead) == 0;
+        tk_trace(p, 6);
         red_release_add(A.bar, 1u);  // release, cumulative over the block's writes through bar.sync
-        if (ok && static_cast<int>(ld_acquire_u32(A.bar) - target) < 0) {
+        if (ok && static_cast<int>(ld_relaxed_u32(A.bar) - target) < 0) {
             const unsigned long long t0 = globaltimer_ns();
-            while (static_cast<int>(ld_acquire_u32(A.bar) - target) < 0) {
+            while (static_cast<int>(ld_relaxed_u32(A.bar) - target) < 0) {
                 if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
                     set_error(A.err, DEVERR_TIMEOUT_BARRIER);
                     m.dead = 1;
@@ -117,17 +123,21 @@ __device__ __forceinline__ bool tk_sync(int p)
                 }
             }
         }
+        fence_acquire_gpu();  // the relaxed polls plus this fence acquire the other blocks' writes
         m.sync_ok = ok;
     }
     __syncthreads();
     return m.sync_ok != 0;
 }
 
+// Diagnostics: stamp i (0..7) of phase p of this block; even stamps are the global
+// timer (ns), odd ones the SM clock (cycles).
 __device__ __forceinline__ void tk_trace(int p, int i)
 {
     const TokenArgs& A = tk_args();
     if (A.trace && threadIdx.x == 0)
-        A.trace[(static_cast<size_t>(blockIdx.x) * (5 * A.n_layers + 1) + p) * 4 + i] = globaltimer_ns();
+        A.trace[(static_cast<size_t>(blockIdx.x) * (5 * A.n_layers + 1) + p) * 8 + i] =
+            (i & 1) ? clock64() : globaltimer_ns();
 }
 
 // One matrix phase p of kind KIND: prefetch the norm weight, pass the barrier,
@@ -168,7 +178,8 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
     }
     if (p > 0 ? !tk_sync(p) : m.dead != 0)
         return make_int2(T, icur);
-    tk_trace(p, 1);
+    tk_trace(p, 2);
+    tk_trace(p, 3);
 
     float4 xv[NCH];
 #pragma unroll
@@ -190,6 +201,7 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
             m.gred[warp] = ss;
     }
     __syncthreads();  // quantised activation, residual rows and norm partials complete
+    tk_trace(p, 5);
     float rstd = 1.f;
     if (NORM) {
         float tot = 0.f;
@@ -202,8 +214,9 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
     UnitState<FMT, PL> us[UL];
     bool have[UL];
     have[0] = pp < K / 32;
+    const int nidx[UL] = {have[0] ? pp : K / 32 - 1};
     load_units<FMT, PL, UL>(us, have, tk_xq(), pp, P, rstd);
-    tk_trace(p, 2);
+    tk_trace(p, 7);
 
     // Complete tile tc (token tile Tc): wait until every warp released it,
     // refill its slot with tile Tc + TK_NSTAGE, run the epilogue of its rows.
@@ -260,9 +273,10 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
             ok = false;
             break;
         }
-        const int nr = min(R, r1 - (r0 + t * R));
+        if (t == 0)
+            tk_trace(p, 1);
         consume_tile<FMT, PL, UL, RP, NMAT>(
-            tk_smem + s * TK_SLOT, nr, R, RG, g, pp, P, ke.row_bytes, us, have,
+            tk_smem + s * TK_SLOT, R, RG, g, ke.row_bytes, us, nidx,
             tk_red() + ((T & (2 * TK_NSTAGE - 1)) * TK_WARPS + warp) * TK_RED_STRIDE, lane);
         if (lane == 0)
             mbar_arrive(&m.empty[s]);
@@ -279,7 +293,7 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
             }
     if (!ok)
         m.dead = 1;
-    tk_trace(p, 3);
+    tk_trace(p, 4);
     return make_int2(T0 + ntiles, icur);
 }
 
@@ -290,7 +304,7 @@ __device__ __forceinline__ void tk_attention(int p)
     tk_trace(p, 0);
     if (!tk_sync(p))
         return;
-    tk_trace(p, 1);
+    tk_trace(p, 2);
     const int group = A.n_q / A.n_kv;
     if ((threadIdx.x >> 5) < group) {
         const int l = p / 5;
@@ -317,7 +331,7 @@ __device__ __forceinline__ void tk_attention(int p)
             named_bar_sync(ATT_BAR, 32 * group);  // staging free before the next item
         }
     }
-    tk_trace(p, 3);
+    tk_trace(p, 4);
 }
 
 __global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_constant__ TokenArgs a)
