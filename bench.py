@@ -252,7 +252,9 @@ def run_ours(args):
     barrier(world, device)
     e2e_max = aggregate_max(e2e_local, world, device)
 
-    # ---- per-kernel timing (each kind across all 36 layers, alone, CUDA events on this stream)
+    # ---- per-kernel timing (each kind across all 36 layers, alone, CUDA events on this stream).
+    # The launches are queued behind a short device-side sleep before the first event, so
+    # the events time the GPU running them back to back, not the host issuing them.
     per_kernel = {}
     for kind_i, kind in enumerate(KERNEL_KINDS):
         layers = [0] if kind == "vocab" else list(range(m.n_layers))
@@ -261,6 +263,7 @@ def run_ours(args):
             model.enqueue_kernel(l, kind_i, sh)
         torch.cuda.synchronize(device)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(20_000_000)  # about 10 ms at 2 GHz: longer than queuing the launches takes
         a.record(stream)
         for _ in range(reps):
             for l in layers:

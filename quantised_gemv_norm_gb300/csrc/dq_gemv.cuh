@@ -9,8 +9,8 @@
 // Structure of one thread block (1 per SM, 512 threads, 16 warps):
 //   * the block's rows stream, R rows per stage, into a ring of shared-memory
 //     stages with 1-D bulk (TMA) copies that complete on an mbarrier (L2
-//     evict-first: weights are read once).  Thread 0 issues the first
-//     ring-full at kernel start;
+//     evict-first: weights are read once).  The first ring-full is issued
+//     right after the set-up barrier, one stage per lane of warp 0;
 //   * all 16 warps consume every stage.  They are split into RG row groups of
 //     P threads; within a group each thread owns UL fixed 32-weight units of
 //     the K axis (16-byte units for bf16), so its slice of the activation is
@@ -504,12 +504,6 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             mbar_init(&empty[s], NCONS_WARPS);
         }
         fence_mbar_init();
-        // weights and the norm weight never depend on the previous kernel
-        for (int t = 0; t < min(a.nstage, ntiles); ++t) {
-            issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, t, r0, r1, R, pol);
-            if (ttile)
-                ttile[128 + t] = clock64();
-        }
     }
     // the norm weight never depends on the previous kernel either
     float4 gv[QCHUNKS], xv[QCHUNKS];
@@ -523,6 +517,13 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         }
     }
     __syncthreads();
+    // weights never depend on the previous kernel: the first ring-full, one stage per
+    // lane of warp 0 (the copies start in parallel)
+    if (tid < min(a.nstage, ntiles)) {
+        issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, tid, r0, r1, R, pol);
+        if (ttile)
+            ttile[128 + tid] = clock64();
+    }
     if (trace && tid == 0)
         trace[1] = globaltimer_ns();
     pdl_wait();  // the activation is the previous kernel's output
@@ -586,7 +587,7 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             float tot = 0.f;
             for (int w = 0; w < NCONS_WARPS; ++w)
                 tot += gred[w];
-            rstd = 1.0f / sqrtf(tot / static_cast<float>(a.K) + a.eps);
+            rstd = rsqrtf(tot / static_cast<float>(a.K) + a.eps);
         }
         load_units<FMT, PL, UL>(us, have, xq, p, P, rstd);
     }

@@ -208,7 +208,7 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
 #pragma unroll
         for (int w = 0; w < TK_WARPS; ++w)
             tot += m.gred[w];
-        rstd = 1.0f / sqrtf(tot / static_cast<float>(K) + A.eps);
+        rstd = rsqrtf(tot / static_cast<float>(K) + A.eps);
     }
     const int g = tid / P, pp = tid % P;
     UnitState<FMT, PL> us[UL];
