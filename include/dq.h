@@ -148,8 +148,9 @@ DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows,
  * count of finished warps (both accumulated: zero the buffer before a launch).
  * Block 0 also writes SM clock stamps for its first 64 stages after the
  * per-block values, at buffer[8 * blocks + i]: [2t] stage t ready, [2t + 1]
- * thread 0 done with it, [128 + t] stage t's copy issued.  The buffer needs
- * 64 bytes per block (at most one block per SM) plus 1536 bytes.  A
+ * thread 0 done with it, [128 + t] stage t's copy issued.  The i-th GEMV
+ * launch after this call writes its values at word offset i (8 blocks + 192),
+ * so the buffer needs (64 bytes per block + 1536 bytes) per traced launch.  A
  * dq_decode_step that runs the fused token kernel writes instead 8 values per
  * block and phase at buffer[8 (block * phases + phase)] (phases = 5 n_layers
  * + 1: per layer Q|K|V, attention, O, gate/up, down; then the vocabulary):

@@ -151,13 +151,21 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool resid, GemvPl
 }
 
 static unsigned long long* g_trace = nullptr;
+static size_t g_trace_next = 0;  // 64-bit words of the buffer used by earlier GEMV launches
 
-void set_gemv_trace(void* buf) { g_trace = static_cast<unsigned long long*>(buf); }
+void set_gemv_trace(void* buf)
+{
+    g_trace = static_cast<unsigned long long*>(buf);
+    g_trace_next = 0;
+}
 unsigned long long* gemv_trace() { return g_trace; }
 
 cudaError_t launch_gemv(const GemvPlan& plan, dq::GemvArgs a, cudaStream_t stream, bool pdl)
 {
-    a.trace = g_trace;
+    // each traced launch takes the next slot: 8 words per block, 192 for block 0's stages
+    a.trace = g_trace ? g_trace + g_trace_next : nullptr;
+    if (g_trace)
+        g_trace_next += 8 * static_cast<size_t>(plan.grid) + 192;
     a.rows = plan.rows;
     a.K = plan.K;
     a.row_bytes = plan.row_bytes;
