@@ -252,9 +252,11 @@ def run_ours(args):
     barrier(world, device)
     e2e_max = aggregate_max(e2e_local, world, device)
 
-    # ---- per-kernel timing (each kind across all 36 layers, alone, CUDA events on this stream).
+    # ---- per-kernel timing (each kind across all 36 layers, CUDA events on this stream).
     # The launches are queued behind a short device-side sleep before the first event, so
-    # the events time the GPU running them back to back, not the host issuing them.
+    # the events time the GPU running them back to back, not the host issuing them; they
+    # are chained with programmatic dependent launch as in the token, so each launch's
+    # start-up overlaps the previous one's end as it does in the token.
     per_kernel = {}
     for kind_i, kind in enumerate(KERNEL_KINDS):
         layers = [0] if kind == "vocab" else list(range(m.n_layers))

@@ -295,7 +295,8 @@ typedef struct {
  * by programmatic dependent launch, captured once in a CUDA graph when
  * use_graph is set.  With DQ_MODEL_FUSED, where the shape allows (at most 64
  * layers; hidden and n_q head_dim at most 4096, hidden a multiple of 2048;
- * ffn at most 12288, a multiple of 2048 if a down projection is Q6_K), it is
+ * ffn at most 12288 with a Q6_K down projection (a multiple of 2048), else as
+ * far as the block's shared memory allows), it is
  * one cooperative launch of one block per SM that runs all phases with grid
  * barriers between them while the weights stream through each block's ring
  * without a break.  Host call;
@@ -320,8 +321,10 @@ DQ_API int dq_model_launches_per_step(const dq_model* m);
 DQ_API int dq_model_fused(const dq_model* m);
 
 /* Diagnostics for per-kernel timing: enqueues one of the token's kernels on
- * its own (no programmatic dependency), with the position and logits pointer
- * of the most recent dq_decode_step on this model.  kind: 0 norm+QKV+append,
+ * its own, launched as in the token (with programmatic dependent launch unless
+ * the model has DQ_MODEL_NO_PDL: back-to-back calls overlap one kernel's
+ * start-up with the previous one's end, as the token's kernels do), with the
+ * position and logits pointer of the most recent dq_decode_step on this model.  kind: 0 norm+QKV+append,
  * 1 attention, 2 O projection + residual, 3 norm+gate/up+SwiGLU, 4 down +
  * residual, 5 final norm + vocabulary (layer ignored).  It updates the model's
  * activations and cache row like the token does.

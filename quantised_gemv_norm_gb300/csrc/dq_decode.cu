@@ -406,7 +406,7 @@ DQ_API int dq_model_enqueue_kernel(dq_model* m, int layer, int kind, void* strea
         return DQ_ERR_NULL;
     if (kind < K_QKV || kind > K_VOCAB || layer < 0 || layer >= m->n_layers)
         return DQ_ERR_SHAPE;
-    cudaError_t e = launch_kernel(m, layer, kind, static_cast<cudaStream_t>(stream), false);
+    cudaError_t e = launch_kernel(m, layer, kind, static_cast<cudaStream_t>(stream), m->pdl);
     return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
 }
 

@@ -13,12 +13,11 @@
 // a second GPU", section "Hiding, fusing...": keep the bytes in flight across
 // the whole token; "The Mountain Runs", section 3: one output per weight row).
 //
-// The consumers are those of the streaming GEMV kernel (dq_gemv.cuh), with
-// 384 threads (12 warps, so each thread may hold 168 registers: the code of
-// all phase kinds shares one allocation): row groups of 128 threads for the
-// K <= 4096 phases and one group of 384 for the down projection, each thread
-// holding one 32-element unit of the quantised activation in registers; stage
-// t is completed by warp t % 12 two stages later.  The attention phase runs one (key chunk, KV head) item per
+// The consumers are those of the streaming GEMV kernel (dq_gemv.cuh): 512
+// threads in row groups of 128 for the K <= 4096 phases and one group of 512
+// for the down projection, each thread holding one 32-element unit of the
+// quantised activation in registers; stage t is completed by warp t % 16 two
+// stages later.  The attention phase runs one (key chunk, KV head) item per
 // block on the first n_q / n_kv warps (dq_attn.cuh).
 //
 // Every wait is bounded.  A block whose wait runs out records the error, stops

@@ -5,7 +5,7 @@
 
 namespace dq {
 
-constexpr int TK_THREADS = 384;    // 12 warps: 168 registers a thread for the phases' activation slices
+constexpr int TK_THREADS = 512;    // 16 warps, 128 registers a thread
 constexpr int TK_WARPS = TK_THREADS / 32;
 constexpr int TK_NSTAGE = 4;       // weight ring slots per block
 constexpr int TK_SLOT = 40960;     // bytes per slot (largest tile: 4 Q6_K rows of K = 12288)
@@ -20,7 +20,7 @@ enum { PH_QKV = 0, PH_ATTN, PH_O, PH_GATEUP, PH_DOWN_Q4, PH_DOWN_Q6, PH_VOCAB, P
 // and matrix; a tile holds TK_THREADS / tk_p * tk_rpt rows of each matrix.
 __host__ __device__ constexpr int tk_p(int kind) { return kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? TK_THREADS : 128; }
 __host__ __device__ constexpr int tk_rg(int kind) { return TK_THREADS / tk_p(kind); }
-__host__ __device__ constexpr int tk_rpt(int kind) { return kind == PH_GATEUP ? 2 : 4; }
+__host__ __device__ constexpr int tk_rpt(int kind) { return kind == PH_GATEUP || kind == PH_VOCAB ? 2 : 4; }
 __host__ __device__ constexpr int tk_rows_per_tile(int kind) { return tk_rg(kind) * tk_rpt(kind); }
 
 struct TokenLayer {
@@ -111,7 +111,8 @@ struct TokenPlan {
 
 // Whether the persistent token kernel covers this model shape (DQ_OK) or not
 // (DQ_ERR_UNSUPPORTED): at most 64 layers, hidden and n_q head_dim <= 4096,
-// ffn <= 12288, and the block's shared memory fits.
+// ffn <= 16384 (12288 with a Q6_K down projection), and the block's shared
+// memory fits.
 int plan_token(int n_layers, int hidden, int ffn, int n_q, int n_kv, int hd, bool any_q6_down, TokenPlan* plan);
 
 // Cooperative launch of one token on `stream` (grid barriers need every block resident).
