@@ -60,6 +60,8 @@ def _load():
         "oracle_layernorm": (None, [P, P, P, P, i32, i32, f64]),
         "oracle_attention": (None, [P, P, P, P, i32, i32, i32, i32, i32]),
         "oracle_silu": (f64, [f64]),
+        "oracle_head_rmsnorm": (None, [P, P, i32, f64]),
+        "oracle_rope": (None, [P, i32, i32, f64]),
         "oracle_decode_step": (None, [P, P, i32, P, P]),
         "oracle_num_threads": (i32, []),
     }
@@ -252,7 +254,22 @@ class _Model(ctypes.Structure):
         ("ffn_norm", ctypes.c_void_p), ("wgate", ctypes.c_void_p), ("wup", ctypes.c_void_p),
         ("wdown", ctypes.c_void_p), ("down_fmt", ctypes.c_void_p), ("out_norm", ctypes.c_void_p),
         ("wvocab", ctypes.c_void_p), ("kv_cache", ctypes.c_void_p),
+        ("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p), ("rope_theta", ctypes.c_double),
     ]
+
+
+def head_rmsnorm(v: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    """Per-head RMSNorm of one head vector (Qwen3 QK-norm); returns a new array."""
+    out = np.array(v, dtype=np.float64, copy=True)
+    _load().oracle_head_rmsnorm(_p(out), _p(_c(w, np.float32)), out.size, float(eps))
+    return out
+
+
+def rope(v: np.ndarray, pos: int, theta: float) -> np.ndarray:
+    """Rotary position embedding of one head vector (rotate-half pairing); new array."""
+    out = np.array(v, dtype=np.float64, copy=True)
+    _load().oracle_rope(_p(out), out.size, int(pos), float(theta))
+    return out
 
 
 def decode_step(model, x_in: np.ndarray, pos: int, kv_cache: np.ndarray, want_hidden: bool = False):
@@ -261,7 +278,8 @@ def decode_step(model, x_in: np.ndarray, pos: int, kv_cache: np.ndarray, want_hi
     ``model`` is any object with the attributes of a synthetic model (see the
     input generator): n_layers, hidden, ffn, n_q_heads, n_kv_heads, head_dim,
     vocab, max_ctx, eps, and per-layer lists attn_norm, wqkv, wo, ffn_norm,
-    wgate, wup, wdown, down_fmt, plus out_norm and wvocab, all numpy arrays.
+    wgate, wup, wdown, down_fmt, plus out_norm and wvocab, all numpy arrays;
+    optionally per-layer q_norm and k_norm and rope_theta (Qwen3 attention inputs).
     ``kv_cache`` (uint16 fp16 bits [L, 2, n_kv, max_ctx, hd]) is updated in place
     at ``pos``.  Returns float64 logits (and the final hidden state if asked).
     """
@@ -286,7 +304,10 @@ def decode_step(model, x_in: np.ndarray, pos: int, kv_cache: np.ndarray, want_hi
                ptr_array(model.wo, np.uint8), ptr_array(model.ffn_norm, np.float32),
                ptr_array(model.wgate, np.uint8), ptr_array(model.wup, np.uint8),
                ptr_array(model.wdown, np.uint8), down_fmt.ctypes.data, out_norm.ctypes.data,
-               wvocab.ctypes.data, kv_cache.ctypes.data)
+               wvocab.ctypes.data, kv_cache.ctypes.data,
+               ptr_array(model.q_norm, np.float32) if getattr(model, "q_norm", None) else None,
+               ptr_array(model.k_norm, np.float32) if getattr(model, "k_norm", None) else None,
+               float(getattr(model, "rope_theta", 0.0) or 0.0))
     xin = _c(x_in, np.float32).reshape(-1)
     assert xin.size == model.hidden
     logits = np.empty(model.vocab, np.float64)

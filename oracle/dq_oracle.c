@@ -410,6 +410,37 @@ ORACLE_API void oracle_attention(const double *q, const uint16_t *kc, const uint
 
 ORACLE_API double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* ------------------------------------------------ Qwen3 attention inputs -- */
+/* The pages name the model (Qwen3-8B) but not its attention's input transforms;
+ * these are the model family's own, written from their definitions:
+ *   - per-head RMSNorm ("QK-norm"): each head's vector v (hd values) becomes
+ *     v / sqrt(mean(v^2) + eps) * w, with one weight vector w[hd] per layer for
+ *     all query heads and one for all key heads;
+ *   - rotary position embedding, rotate-half pairing: for i < hd/2 the pair
+ *     (v[i], v[i + hd/2]) turns by the angle pos * theta^(-2i/hd). */
+
+ORACLE_API void oracle_head_rmsnorm(double *v, const float *w, int hd, double eps)
+{
+    double ss = 0.0;
+    for (int i = 0; i < hd; i++)
+        ss += v[i] * v[i];
+    double r = 1.0 / sqrt(ss / hd + eps);
+    for (int i = 0; i < hd; i++)
+        v[i] = v[i] * r * (double)w[i];
+}
+
+ORACLE_API void oracle_rope(double *v, int hd, int pos, double theta)
+{
+    int half = hd / 2;
+    for (int i = 0; i < half; i++) {
+        double ang = (double)pos * pow(theta, -2.0 * i / hd);
+        double c = cos(ang), sn = sin(ang);
+        double a = v[i], b = v[i + half];
+        v[i] = a * c - b * sn;
+        v[i + half] = b * c + a * sn;
+    }
+}
+
 /* ---------------------------------------------------------- decode step -- */
 
 typedef struct {
@@ -426,9 +457,14 @@ typedef struct {
     const float *out_norm;          /* fp32[hidden] */
     const uint8_t *wvocab;          /* Q6_K [vocab][hidden] */
     uint16_t *kv_cache;             /* fp16 [L][2][n_kv][max_ctx][hd] */
+    /* Qwen3 attention inputs; q_norm NULL: plain attention on the projections */
+    const float *const *q_norm;     /* [L] -> fp32[hd] */
+    const float *const *k_norm;     /* [L] -> fp32[hd] */
+    double rope_theta;
 } oracle_model;
 
-/* One token: x_in (fp32 hidden) at position pos.  Appends this token's k and v
+/* One token: x_in (fp32 hidden) at position pos.  With Qwen3 attention inputs,
+ * q and k are head-normalised and rotated first.  Appends this token's k and v
  * (rounded to fp16) to the cache, then attends over keys 0..pos.  Writes the
  * final hidden state (double) when x_out is not NULL, and the logits. */
 ORACLE_API void oracle_decode_step(const oracle_model *mdl, const float *x_in, int pos, double *logits, double *x_out)
@@ -449,6 +485,16 @@ ORACLE_API void oracle_decode_step(const oracle_model *mdl, const float *x_in, i
     for (int l = 0; l < mdl->n_layers; l++) {
         rmsnorm_row(x, mdl->attn_norm[l], h, H, mdl->eps);
         gemv_any(FMT_Q4K, mdl->wqkv[l], h, qkv, qdim + 2 * kvdim, H);
+        if (mdl->q_norm) { /* QK-norm, then RoPE at pos, on every q and k head */
+            for (int hh = 0; hh < nq; hh++) {
+                oracle_head_rmsnorm(qkv + hh * hd, mdl->q_norm[l], hd, mdl->eps);
+                oracle_rope(qkv + hh * hd, hd, pos, mdl->rope_theta);
+            }
+            for (int kvh = 0; kvh < nkv; kvh++) {
+                oracle_head_rmsnorm(qkv + qdim + kvh * hd, mdl->k_norm[l], hd, mdl->eps);
+                oracle_rope(qkv + qdim + kvh * hd, hd, pos, mdl->rope_theta);
+            }
+        }
         uint16_t *kc = mdl->kv_cache + (size_t)l * 2 * plane;
         uint16_t *vc = kc + plane;
         for (int kvh = 0; kvh < nkv; kvh++)

@@ -35,7 +35,7 @@ FMT_BF16, FMT_Q4K, FMT_Q6K = 0, 1, 2
 # Role ids keep every tensor on its own random stream.
 _ROLES = {"x": 1, "gamma": 2, "beta": 3, "w": 4, "wqkv": 10, "wo": 11, "wgate": 12, "wup": 13,
           "wdown": 14, "attn_norm": 15, "ffn_norm": 16, "out_norm": 17, "wvocab": 18, "kv": 19,
-          "xin": 20}
+          "xin": 20, "q_norm": 21, "k_norm": 22}
 
 
 def rng_for(seed: int, *key: int) -> np.random.Generator:
@@ -155,6 +155,10 @@ class SyntheticModel:
     down_fmt: list = field(default_factory=list)
     out_norm: np.ndarray = None
     wvocab: np.ndarray = None
+    # Qwen3 attention inputs (empty: plain attention on the projections)
+    q_norm: list = field(default_factory=list)
+    k_norm: list = field(default_factory=list)
+    rope_theta: float = 0.0
 
     @property
     def qkv_rows(self) -> int:
@@ -168,8 +172,14 @@ class SyntheticModel:
         return n + self.wvocab.nbytes
 
 
+QWEN3_ROPE_THETA = 1.0e6
+
+
 def make_model(seed: int, n_layers: int, hidden: int, ffn: int, n_q_heads: int, n_kv_heads: int,
-               head_dim: int, vocab: int, max_ctx: int, eps: float = 1e-6) -> SyntheticModel:
+               head_dim: int, vocab: int, max_ctx: int, eps: float = 1e-6,
+               qwen3_attention: bool = False) -> SyntheticModel:
+    """``qwen3_attention`` adds per-layer q/k head-norm weights ~ N(1, 0.1) and the
+    rotary base 1e6 (Qwen3's); the other tensors do not depend on it."""
     m = SyntheticModel(n_layers, hidden, ffn, n_q_heads, n_kv_heads, head_dim, vocab, max_ctx, eps)
     qdim = n_q_heads * head_dim
     for l in range(n_layers):
@@ -183,6 +193,11 @@ def make_model(seed: int, n_layers: int, hidden: int, ffn: int, n_q_heads: int, 
         m.down_fmt.append(fmt)
         gen = q6k_blocks if fmt == FMT_Q6K else q4k_blocks
         m.wdown.append(gen(rng_for(seed, _role("wdown"), l), hidden * ffn // 256).reshape(hidden, -1))
+    if qwen3_attention:
+        for l in range(n_layers):
+            m.q_norm.append(normal_f32(rng_for(seed, _role("q_norm"), l), (head_dim,), 1.0, 0.1))
+            m.k_norm.append(normal_f32(rng_for(seed, _role("k_norm"), l), (head_dim,), 1.0, 0.1))
+        m.rope_theta = QWEN3_ROPE_THETA
     m.out_norm = normal_f32(rng_for(seed, _role("out_norm")), (hidden,), 1.0, 0.1)
     m.wvocab = q6k_blocks(rng_for(seed, _role("wvocab")), vocab * hidden // 256).reshape(vocab, -1)
     return m

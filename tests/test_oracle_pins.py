@@ -487,3 +487,88 @@ def test_decode_emulation_group_round():
         err = np.abs(emu.group_round(w, planes) - w).reshape(-1, 32).max(axis=1)
         amax = np.abs(w).reshape(-1, 32).max(axis=1)
         assert np.all(err <= bound * amax * (1 + 1e-9))
+
+
+# ------------------------------------------------- Qwen3 attention inputs
+
+
+def test_rope_is_identity_at_position_zero(orc):
+    v = synth.normal_f32(synth.rng_for(31, 1), (128,)).astype(np.float64)
+    assert np.array_equal(orc.rope(v, 0, 1.0e6), v)
+
+
+def test_rope_turns_the_first_pair_by_the_position(orc):
+    # dimension 0 pairs with dimension 64 and turns by pos * theta^0 = pos radians
+    for pos in (1, 7, 511, 4097):
+        e0 = np.zeros(128)
+        e0[0] = 1.0
+        r = orc.rope(e0, pos, 1.0e6)
+        assert abs(r[0] - np.cos(pos)) < 1e-12 and abs(r[64] - np.sin(pos)) < 1e-12
+        assert np.count_nonzero(np.delete(r, [0, 64])) == 0
+
+
+def test_rope_last_pair_angle(orc):
+    # pair (63, 127) turns by pos * theta^(-126/128): with theta = 2^128 that is pos * 2^-126
+    pos = 3
+    e = np.zeros(128)
+    e[63] = 1.0
+    r = orc.rope(e, pos, 2.0 ** 128)
+    ang = pos * 2.0 ** -126
+    assert abs(r[63] - np.cos(ang)) < 1e-15 and abs(r[127] - np.sin(ang)) < 1e-15
+
+
+def test_rope_keeps_pair_norms_and_relative_positions(orc):
+    rng = synth.rng_for(32, 1)
+    q = rng.standard_normal(128)
+    k = rng.standard_normal(128)
+    for pos in (5, 300):
+        r = orc.rope(q, pos, 1.0e6)
+        assert np.allclose(np.hypot(r[:64], r[64:]), np.hypot(q[:64], q[64:]), rtol=0, atol=1e-12)
+    # a rotation by position: the score depends only on the distance between positions
+    a = np.dot(orc.rope(q, 40, 1.0e6), orc.rope(k, 10, 1.0e6))
+    b = np.dot(orc.rope(q, 130, 1.0e6), orc.rope(k, 100, 1.0e6))
+    assert abs(a - b) < 1e-9 * max(1.0, abs(a))
+
+
+def test_head_rmsnorm_closed_forms(orc):
+    w = synth.normal_f32(synth.rng_for(33, 1), (128,), 1.0, 0.1)
+    c = 3.0
+    out = orc.head_rmsnorm(np.full(128, c), w, 1e-6)
+    assert np.allclose(out, c / np.sqrt(c * c + 1e-6) * w.astype(np.float64), rtol=1e-14, atol=0)
+    v = synth.normal_f32(synth.rng_for(33, 2), (128,)).astype(np.float64)
+    ones = np.ones(128, np.float32)
+    n1 = orc.head_rmsnorm(v, ones, 0.0)
+    assert abs(np.sqrt(np.mean(n1 ** 2)) - 1.0) < 1e-14     # unit RMS with unit weights, eps 0
+    assert np.allclose(orc.head_rmsnorm(v * 7.5, ones, 0.0), n1, rtol=1e-14, atol=0)  # scale invariant
+
+
+def test_qwen3_attention_does_not_change_the_first_token(orc):
+    # with one key the softmax is 1: the output is that key's value, whatever q and k are,
+    # and v is not transformed: the logits at pos 0 equal those of plain attention
+    plain = synth.make_model(34, n_layers=2, hidden=256, ffn=512, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                             vocab=300, max_ctx=8)
+    qwen = synth.make_model(34, n_layers=2, hidden=256, ffn=512, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                            vocab=300, max_ctx=8, qwen3_attention=True)
+    x = synth.decode_input(34, 256)
+    a = orc.decode_step(plain, x, 0, synth.make_kv_cache(34, plain, 0))
+    b = orc.decode_step(qwen, x, 0, synth.make_kv_cache(34, qwen, 0))
+    assert np.array_equal(a, b)
+
+
+def test_qwen3_attention_changes_later_tokens_and_caches_rotated_keys(orc):
+    qwen = synth.make_model(35, n_layers=1, hidden=256, ffn=512, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                            vocab=64, max_ctx=8, qwen3_attention=True)
+    plain = synth.make_model(35, n_layers=1, hidden=256, ffn=512, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                             vocab=64, max_ctx=8)
+    kv_q = synth.make_kv_cache(35, qwen, 0)
+    kv_p = synth.make_kv_cache(35, plain, 0)
+    x = synth.decode_input(35, 256)
+    orc.decode_step(qwen, x, 3, kv_q)
+    orc.decode_step(plain, x, 3, kv_p)
+    # the cached key at pos 3 is the normalised, rotated projection; the value is unchanged
+    kq = kv_q.view(np.float16)[0, 0, :, 3, :].astype(np.float64)
+    kp = kv_p.view(np.float16)[0, 0, :, 3, :].astype(np.float64)
+    for h in range(2):
+        want = orc.rope(orc.head_rmsnorm(kp[h], qwen.k_norm[0], qwen.eps), 3, qwen.rope_theta)
+        assert np.max(np.abs(kq[h] - want)) <= 2e-3 * np.max(np.abs(want))  # fp16 rounding of both
+    assert np.array_equal(kv_q.view(np.uint16)[0, 1], kv_p.view(np.uint16)[0, 1])
