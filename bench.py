@@ -36,7 +36,8 @@ SEED = 1
 MAX_CTX = 1024
 WORKLOAD = ("Qwen3-8B-shaped decode token: 36 layers (Q4_K attention q|k|v 6144x4096 and o 4096x4096, "
             "Q4_K gate/up 12288x4096, down 4096x12288 Q6_K in odd layers / Q4_K in even), final RMSNorm, "
-            "Q6_K vocabulary 151936x4096; empty KV cache (pos 0); M=1")
+            "Q6_K vocabulary 151936x4096; Qwen3 attention inputs (per-head q/k RMSNorm, rotary base 1e6); "
+            "empty KV cache (pos 0); M=1")
 # The pages' own number for this workload: llama.cpp, Qwen3-8B Q4_K, empty context, RTX 5090
 # ("The roofline holds on a second GPU", "How I ran it": 248.8 / 253.9 / 255.1 tok/s); median.
 PAGES_BASELINE_TOK_S = 253.9
@@ -198,7 +199,7 @@ def run_ours(args):
     build.build()
     dq.load()
     t0 = time.time()
-    m = synth.make_model(SEED, max_ctx=MAX_CTX, **synth.QWEN3_8B)
+    m = synth.make_model(SEED, max_ctx=MAX_CTX, qwen3_attention=True, **synth.QWEN3_8B)
     kv = synth.make_kv_cache(SEED, m, 0)
     w = upload.to_device(m, kv, device)
     model = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=True)
@@ -434,7 +435,8 @@ def run_kernel_probe(args):
     dq.load()
     S = synth.QWEN3_8B
     m = synth.make_model(SEED, n_layers=2, hidden=S["hidden"], ffn=S["ffn"], n_q_heads=S["n_q_heads"],
-                         n_kv_heads=S["n_kv_heads"], head_dim=S["head_dim"], vocab=S["vocab"], max_ctx=MAX_CTX)
+                         n_kv_heads=S["n_kv_heads"], head_dim=S["head_dim"], vocab=S["vocab"], max_ctx=MAX_CTX,
+                         qwen3_attention=True)
     w = upload.to_device(m, synth.make_kv_cache(SEED, m, 0))
     model = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=False)
     x = torch.from_numpy(synth.decode_input(SEED, m.hidden)).cuda()
@@ -472,7 +474,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    m = synth.make_model(SEED, max_ctx=MAX_CTX, **synth.QWEN3_8B)
+    m = synth.make_model(SEED, max_ctx=MAX_CTX, qwen3_attention=True, **synth.QWEN3_8B)
     import oracle
 
     oracle.build()

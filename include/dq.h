@@ -215,6 +215,35 @@ DQ_API int dq_attention_decode(const float* q, const void* k_plane, const void* 
 DQ_API int dq_attention_decode_static(const float* q, const void* k_plane, const void* v_plane, float* out, int n_q,
                                       int n_kv, int head_dim, int max_ctx, int n_keys, void* stream);
 
+/* Qwen3 attention inputs.  The pages name the model (Qwen3-8B, "The roofline
+ * holds on a second GPU", section "The Math") but not its attention's input
+ * transforms; these are the model family's own:
+ *   head_rmsnorm(v, w) = v / sqrt(mean(v^2) + eps) * w   (per 128-dim head)
+ *   rope(v, pos): for i < 64, (v[i], v[i + 64]) turns by pos / theta^(i / 64)
+ * with one weight vector for all query heads and one for all key heads.
+ *
+ * dq_rope_table fills table, fp32 (cos, sin) pairs [max_ctx][head_dim / 2][2]
+ * (device, 16-byte aligned, written), with the angle p / theta^(2i / head_dim)
+ * for row p and pair i, computed in double precision and rounded once to fp32.
+ * Enqueued on `stream`.  Errors: NULL -> DQ_ERR_NULL; max_ctx < 1, head_dim
+ * odd or < 2, theta <= 1 -> DQ_ERR_SHAPE; misaligned -> DQ_ERR_ALIGN. */
+DQ_API int dq_rope_table(float* table, int max_ctx, int head_dim, double theta, void* stream);
+
+/* dq_attention_decode with the Qwen3 inputs, for the token at pos = n_keys - 1:
+ *   q_h <- rope(head_rmsnorm(q_h, q_norm), pos) for every query head;
+ *   k_plane[g][pos] = fp16(rope(head_rmsnorm(k_new[g], k_norm), pos));
+ * then the attention of q over keys 0..pos.  q: fp32 [n_q][128] as projected
+ * (read, not modified); k_new: fp32 [n_kv][128] as projected (read); k_plane:
+ * fp16 [n_kv][max_ctx][128] (row pos written, rows < pos read); v_plane as in
+ * dq_attention_decode (row pos must already hold the token's value);
+ * q_norm, k_norm: fp32 [128]; rope_table: a dq_rope_table of at least n_keys
+ * rows for head_dim 128.  All device pointers, 16-byte aligned.  Workspace,
+ * limits and errors as dq_attention_decode. */
+DQ_API int dq_attention_decode_rope(const float* q, const float* k_new, void* k_plane, const void* v_plane, float* out,
+                                    const float* q_norm, const float* k_norm, const float* rope_table, float eps,
+                                    int n_q, int n_kv, int head_dim, int max_ctx, int n_keys, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------ M-token sweep
  * "The roofline holds on a second GPU", section "The Math": M tokens share one
  * read of the weights; below M* = (w/16)(R/BW) memory bounds the product, above
@@ -249,6 +278,7 @@ DQ_API int dq_matmul_q4k(const void* W_blocks, const float* X, float* Y, int M, 
  *
  * Per layer l, with x the fp32 residual vector:
  *   h = RMSNorm(x, attn_norm[l]);  [q|k|v] = Wqkv[l] h
+ *   (Qwen3 inputs: each q and k head <- rope(head_rmsnorm(., q_norm/k_norm[l]), pos))
  *   cache[l][0][:, pos] = fp16(k);  cache[l][1][:, pos] = fp16(v)
  *   a = GQA attention of q over keys 0..pos;  x += Wo[l] a
  *   h = RMSNorm(x, ffn_norm[l]);  x += Wdown[l] (SiLU(Wgate[l] h) * (Wup[l] h))
@@ -277,6 +307,11 @@ typedef struct {
     void* kv_cache;                /* device fp16 [n_layers][2][n_kv][max_ctx][head_dim] */
     int use_graph;                 /* separate kernels only: 1 capture them in a CUDA graph, 0 eager launches */
     int flags;                     /* DQ_MODEL_* bits; 0 for the default behaviour */
+    /* Qwen3 attention inputs (see dq_attention_decode_rope); q_norm NULL: plain
+     * attention and the next two fields are ignored. */
+    const float* const* q_norm;    /* host array of n_layers DEVICE pointers: fp32 [head_dim], query heads */
+    const float* const* k_norm;    /* the same for the key heads */
+    double rope_theta;             /* rotary base, > 1 (Qwen3: 1e6) */
 } dq_model_desc;
 
 /* dq_model_desc.flags: launch the token's kernels without programmatic

@@ -26,9 +26,34 @@ __global__ void __launch_bounds__(256) attn_decode_kernel(const __grid_constant_
     attn_block(a, blockIdx.x, blockIdx.y, blockDim.x >> 5, sm, true);
 }
 
+// (cos, sin) of p / theta^(2i / hd) for p < max_ctx, i < hd / 2, in double
+// precision, rounded once to fp32.
+__global__ void rope_table_kernel(float2* __restrict__ tab, int max_ctx, int hd, double theta)
+{
+    const int half = hd / 2;
+    const size_t n = static_cast<size_t>(max_ctx) * half;
+    for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
+         idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const int p = static_cast<int>(idx / half), i = static_cast<int>(idx % half);
+        const double ang = static_cast<double>(p) * pow(theta, -2.0 * i / hd);
+        double sn, cs;
+        sincos(ang, &sn, &cs);
+        tab[idx] = make_float2(static_cast<float>(cs), static_cast<float>(sn));
+    }
+}
+
 }  // namespace dq
 
 namespace dqhost {
+
+cudaError_t launch_rope_table(float2* tab, int max_ctx, int hd, double theta, cudaStream_t stream)
+{
+    const size_t n = static_cast<size_t>(max_ctx) * (hd / 2);
+    const int threads = 256;
+    const int blocks = static_cast<int>(n / threads + 1 < 4096 ? n / threads + 1 : 4096);
+    dq::rope_table_kernel<<<blocks, threads, 0, stream>>>(tab, max_ctx, hd, theta);
+    return cudaGetLastError();
+}
 
 size_t attention_workspace_bytes(int n_q, int n_kv)
 {
@@ -97,6 +122,56 @@ DQ_API int dq_attention_decode(const float* q, const void* k_plane, const void* 
     a.max_ctx = max_ctx;
     a.n_keys = n_keys;
     a.step = nullptr;
+    cudaError_t e = dqhost::launch_attention(a, static_cast<cudaStream_t>(stream), false);
+    return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
+}
+
+DQ_API int dq_rope_table(float* table, int max_ctx, int head_dim, double theta, void* stream)
+{
+    if (!table)
+        return DQ_ERR_NULL;
+    if (max_ctx < 1 || head_dim < 2 || head_dim % 2 || !(theta > 1.0))
+        return DQ_ERR_SHAPE;
+    if (!dqhost::aligned16(table))
+        return DQ_ERR_ALIGN;
+    cudaError_t e = dqhost::launch_rope_table(reinterpret_cast<float2*>(table), max_ctx, head_dim, theta,
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
+}
+
+DQ_API int dq_attention_decode_rope(const float* q, const float* k_new, void* k_plane, const void* v_plane, float* out,
+                                    const float* q_norm, const float* k_norm, const float* rope_table, float eps,
+                                    int n_q, int n_kv, int head_dim, int max_ctx, int n_keys, void* workspace,
+                                    size_t workspace_bytes, void* stream)
+{
+    if (!q || !k_new || !k_plane || !v_plane || !out || !q_norm || !k_norm || !rope_table || !workspace)
+        return DQ_ERR_NULL;
+    if (n_q < 1 || n_kv < 1 || max_ctx < 1 || n_keys < 1 || n_keys > max_ctx || n_q % n_kv)
+        return DQ_ERR_SHAPE;
+    if (head_dim != dq::ATT_HD || n_q / n_kv > 8 || n_kv > dq::ATT_COUNTER_BYTES / 4)
+        return DQ_ERR_UNSUPPORTED;
+    if (workspace_bytes < dqhost::attention_workspace_bytes(n_q, n_kv))
+        return DQ_ERR_SHAPE;
+    if (!dqhost::aligned16(q) || !dqhost::aligned16(k_new) || !dqhost::aligned16(k_plane) ||
+        !dqhost::aligned16(v_plane) || !dqhost::aligned16(out) || !dqhost::aligned16(q_norm) ||
+        !dqhost::aligned16(k_norm) || !dqhost::aligned16(rope_table) || !dqhost::aligned16(workspace))
+        return DQ_ERR_ALIGN;
+    dq::AttnArgs a{};
+    a.q = q;
+    a.kc = static_cast<const __half*>(k_plane);
+    a.vc = static_cast<const __half*>(v_plane);
+    a.out = out;
+    dqhost::attention_bind_workspace(a, workspace);
+    a.n_q = n_q;
+    a.n_kv = n_kv;
+    a.max_ctx = max_ctx;
+    a.n_keys = n_keys;
+    a.step = nullptr;
+    a.k_new = k_new;
+    a.q_norm = q_norm;
+    a.k_norm = k_norm;
+    a.rope = reinterpret_cast<const float2*>(rope_table);
+    a.eps = eps;
     cudaError_t e = dqhost::launch_attention(a, static_cast<cudaStream_t>(stream), false);
     return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
 }

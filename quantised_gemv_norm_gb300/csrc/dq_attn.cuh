@@ -23,6 +23,13 @@ struct AttnArgs {
     int n_keys;            // used when step == null
     const StepArgs* step;  // decode graph: n_keys = step->pos + 1
     int* err;
+    // Qwen3 attention (k_new not null): q and this token's key are normalised
+    // per head and rotated before use; the key is written to kc at n_keys - 1.
+    const float* k_new;    // [n_kv][128] the token's keys as projected (fp32)
+    const float* q_norm;   // [128] RMSNorm weight shared by the query heads
+    const float* k_norm;   // [128] RMSNorm weight shared by the key heads
+    const float2* rope;    // [max_ctx][64] (cos, sin) of pos / theta^(2i / 128)
+    float eps;
 };
 
 constexpr int ATT_BAR = 15;  // named barrier id of the attention warps
@@ -33,6 +40,33 @@ struct AttnSmem {
     float qs[8][ATT_HD];
     int last;
 };
+
+// RMSNorm of one 128-dim head (4 dims per lane, weight w) followed by the
+// rotate-half rotary embedding: dims i and i + 64 turn by the angle whose
+// (cos, sin) is cs[i].  These are the Qwen3 family's attention inputs (the
+// decode census of "The roofline holds on a second GPU" names the model, not
+// these transforms): one weight vector for all query heads, one for all key
+// heads, rotary base 1e6.
+__device__ __forceinline__ float4 head_norm_rope(float4 v, const float* __restrict__ w,
+                                                 const float2* __restrict__ cs, float eps, int lane)
+{
+    const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+    const float r = rsqrtf(ss * (1.0f / ATT_HD) + eps);
+    const float4 g = __ldg(reinterpret_cast<const float4*>(w) + lane);
+    v = make_float4(v.x * r * g.x, v.y * r * g.y, v.z * r * g.z, v.w * r * g.w);
+    // the partner dims (i + 64 for the first half, i - 64 for the second) sit 16 lanes away
+    float4 o;
+    o.x = __shfl_xor_sync(0xffffffffu, v.x, 16);
+    o.y = __shfl_xor_sync(0xffffffffu, v.y, 16);
+    o.z = __shfl_xor_sync(0xffffffffu, v.z, 16);
+    o.w = __shfl_xor_sync(0xffffffffu, v.w, 16);
+    const int i0 = (4 * lane) & (ATT_HD / 2 - 1);
+    const float4 c01 = __ldg(reinterpret_cast<const float4*>(cs + i0));
+    const float4 c23 = __ldg(reinterpret_cast<const float4*>(cs + i0 + 2));
+    const float sg = lane < 16 ? -1.0f : 1.0f;  // first half: a cos - b sin; second: b cos + a sin
+    return make_float4(fmaf(v.x, c01.x, sg * o.x * c01.y), fmaf(v.y, c01.z, sg * o.y * c01.w),
+                       fmaf(v.z, c23.x, sg * o.z * c23.y), fmaf(v.w, c23.z, sg * o.w * c23.w));
+}
 
 // Block (c, g) of the decode attention, run by the first `group` warps of the
 // calling block (threads 0 .. 32 group - 1, synchronised by named barrier
@@ -62,11 +96,28 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
         return;
 
     const int h = g * group + warp;
+    const __half* kbase = a.kc + static_cast<size_t>(g) * a.max_ctx * ATT_HD;
     {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.q + static_cast<size_t>(h) * ATT_HD) + lane);
+        float4 v = __ldcg(reinterpret_cast<const float4*>(a.q + static_cast<size_t>(h) * ATT_HD) + lane);
+        if (a.k_new) {
+            const int pos = n_keys - 1;
+            const float2* cs = a.rope + static_cast<size_t>(pos) * (ATT_HD / 2);
+            if (c == nact - 1 && warp == 0) {
+                // the block whose chunk holds pos finalises the token's key before
+                // staging it (the batch loop's first barrier orders the store)
+                float4 k = __ldcg(reinterpret_cast<const float4*>(a.k_new + static_cast<size_t>(g) * ATT_HD) + lane);
+                k = head_norm_rope(k, a.k_norm, cs, a.eps, lane);
+                const __half2 k01 = __floats2half2_rn(k.x, k.y), k23 = __floats2half2_rn(k.z, k.w);
+                uint2 u;
+                u.x = *reinterpret_cast<const uint32_t*>(&k01);
+                u.y = *reinterpret_cast<const uint32_t*>(&k23);
+                *reinterpret_cast<uint2*>(const_cast<__half*>(kbase) + static_cast<size_t>(pos) * ATT_HD + 4 * lane) = u;
+                __threadfence_block();
+            }
+            v = head_norm_rope(v, a.q_norm, cs, a.eps, lane);
+        }
         *reinterpret_cast<float4*>(&qs[warp][4 * lane]) = v;
     }
-    const __half* kbase = a.kc + static_cast<size_t>(g) * a.max_ctx * ATT_HD;
     const __half* vbase = a.vc + static_cast<size_t>(g) * a.max_ctx * ATT_HD;
     const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
 
@@ -166,6 +217,9 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
 namespace dqhost {
 
 size_t attention_workspace_bytes(int n_q, int n_kv);
+// Fills tab [max_ctx][hd / 2] with (cos, sin) of p / theta^(2i / hd), computed
+// in double precision and rounded once.
+cudaError_t launch_rope_table(float2* tab, int max_ctx, int hd, double theta, cudaStream_t stream);
 // Splits a workspace into the counters and the partials.
 void attention_bind_workspace(dq::AttnArgs& a, void* ws);
 cudaError_t launch_attention(const dq::AttnArgs& a, cudaStream_t stream, bool pdl);

@@ -48,6 +48,7 @@ struct dq_model {
     std::vector<const float*> attn_norm, ffn_norm;
     std::vector<const uint8_t*> wqkv, wo, wgate, wup, wdown;
     std::vector<int> down_fmt;
+    std::vector<const float*> q_norm, k_norm;  // Qwen3 attention inputs (empty: plain attention)
     const float* out_norm;
     const uint8_t* wvocab;
     __half* kv;
@@ -59,6 +60,8 @@ struct dq_model {
     float* act;
     dq::StepArgs* step;
     void* attn_ws;
+    float* k_new;       // Qwen3 attention inputs: the token's projected keys, else null
+    float2* rope;       // (cos, sin) [max_ctx][hd / 2] when k_new is set
     // fused token kernel
     bool fused;
     dqhost::TokenPlan tplan;
@@ -99,6 +102,7 @@ static cudaError_t launch_kernel(dq_model* m, int l, int kind, cudaStream_t s, b
         a.step = m->step;
         a.kv_k = kc;
         a.kv_v = vc;
+        a.k_new = m->k_new;
         a.qdim = qdim;
         a.kvdim = kvdim;
         a.hd = m->hd;
@@ -116,6 +120,13 @@ static cudaError_t launch_kernel(dq_model* m, int l, int kind, cudaStream_t s, b
         t.max_ctx = m->max_ctx;
         t.step = m->step;
         t.err = err;
+        if (m->k_new) {
+            t.k_new = m->k_new;
+            t.q_norm = m->q_norm[l];
+            t.k_norm = m->k_norm[l];
+            t.rope = m->rope;
+            t.eps = m->eps;
+        }
         return dqhost::launch_attention(t, s, pdl);
     }
     case K_O:  // O projection + residual
@@ -211,6 +222,19 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
     }
     if (!dqhost::aligned16(d->out_norm) || !dqhost::aligned16(d->wvocab) || !dqhost::aligned16(d->kv_cache))
         return DQ_ERR_ALIGN;
+    const bool qwen3 = d->q_norm != nullptr;
+    if (qwen3) {
+        if (!d->k_norm)
+            return DQ_ERR_NULL;
+        if (!(d->rope_theta > 1.0))
+            return DQ_ERR_SHAPE;
+        for (int l = 0; l < d->n_layers; ++l) {
+            if (!d->q_norm[l] || !d->k_norm[l])
+                return DQ_ERR_NULL;
+            if (!dqhost::aligned16(d->q_norm[l]) || !dqhost::aligned16(d->k_norm[l]))
+                return DQ_ERR_ALIGN;
+        }
+    }
 
     dq_model* m = new (std::nothrow) dq_model();
     if (!m)
@@ -235,6 +259,10 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
         m->wup.push_back(static_cast<const uint8_t*>(d->wup[l]));
         m->wdown.push_back(static_cast<const uint8_t*>(d->wdown[l]));
         m->down_fmt.push_back(d->down_fmt[l]);
+        if (qwen3) {
+            m->q_norm.push_back(d->q_norm[l]);
+            m->k_norm.push_back(d->k_norm[l]);
+        }
         if (d->down_fmt[l] == DQ_FMT_Q6K)
             m->have_down_q6 = true;
         else
@@ -264,13 +292,16 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
         m->fused = dqhost::plan_token(d->n_layers, d->hidden, d->ffn, d->n_q_heads, d->n_kv_heads, d->head_dim,
                                       m->have_down_q6, &m->tplan) == DQ_OK;
 
-    // workspace: x | q | attn | act | step | attention scratch | layer table | barrier, each 256-byte aligned
+    // workspace: x | q | attn | act | step | attention scratch | layer table | barrier
+    // [| new keys | rotary table], each 256-byte aligned
     auto up = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     const size_t bx = up(sizeof(float) * d->hidden), bq = up(sizeof(float) * qdim), ba = bq,
                  bf = up(sizeof(float) * d->ffn), bs = up(sizeof(dq::StepArgs)),
                  bw = up(dqhost::attention_workspace_bytes(d->n_q_heads, d->n_kv_heads)),
-                 bl = up(sizeof(dq::TokenLayer) * d->n_layers), bb = 256;
-    const size_t total = bx + bq + ba + bf + bs + bw + bl + bb;
+                 bl = up(sizeof(dq::TokenLayer) * d->n_layers), bb = 256,
+                 bk = qwen3 ? up(sizeof(float) * kvdim) : 0,
+                 br = qwen3 ? up(sizeof(float2) * static_cast<size_t>(d->max_ctx) * (d->head_dim / 2)) : 0;
+    const size_t total = bx + bq + ba + bf + bs + bw + bl + bb + bk + br;
     cudaError_t e = cudaMalloc(&m->ws, total);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -287,7 +318,12 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
     m->layers_dev = reinterpret_cast<dq::TokenLayer*>(base + bx + bq + ba + bf + bs + bw);
     m->bar = reinterpret_cast<unsigned*>(base + bx + bq + ba + bf + bs + bw + bl);
     m->bar_base = 0;
-    if ((e = cudaMemset(m->ws, 0, total)) != cudaSuccess) {
+    if (qwen3) {
+        m->k_new = reinterpret_cast<float*>(base + bx + bq + ba + bf + bs + bw + bl + bb);
+        m->rope = reinterpret_cast<float2*>(base + bx + bq + ba + bf + bs + bw + bl + bb + bk);
+    }
+    if ((e = cudaMemset(m->ws, 0, total)) != cudaSuccess ||
+        (qwen3 && (e = dqhost::launch_rope_table(m->rope, d->max_ctx, d->head_dim, d->rope_theta, 0)) != cudaSuccess)) {
         free_model(m);
         return dqhost::set_cuda_error(e);
     }
@@ -301,6 +337,8 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
             tl[l].wgate = m->wgate[l];
             tl[l].wup = m->wup[l];
             tl[l].wdown = m->wdown[l];
+            tl[l].q_norm = qwen3 ? m->q_norm[l] : nullptr;
+            tl[l].k_norm = qwen3 ? m->k_norm[l] : nullptr;
             tl[l].down_fmt = m->down_fmt[l];
             tl[l].pad = 0;
         }
@@ -365,6 +403,8 @@ DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits
         dqhost::attention_bind_workspace(t, m->attn_ws);
         a.part = t.part;
         a.counters = t.counters;
+        a.k_new = m->k_new;
+        a.rope = m->rope;
         a.step = m->step;
         a.bar = m->bar;
         a.bar_base = m->bar_base;

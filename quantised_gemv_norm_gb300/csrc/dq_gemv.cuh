@@ -70,6 +70,7 @@ struct GemvArgs {
     const StepArgs* step;
     __half* kv_k;       // EPI_QKV: this layer's K plane [n_kv][max_ctx][hd]
     __half* kv_v;
+    float* k_new;       // EPI_QKV: when not null, k rows go here (fp32 [kvdim]) for the attention to finish
     int qdim, kvdim, hd, max_ctx;
     int resid_rows;             // EPI_RESID: shared-memory slots for the block's residual rows
     int* err;
@@ -638,7 +639,9 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
                     const int kvh = rem / a.hd, dd = rem - kvh * a.hd;
                     __half* plane = which ? a.kv_v : a.kv_k;
                     const int pos = *step_pos;
-                    if (pos >= 0 && pos < a.max_ctx)
+                    if (!which && a.k_new)
+                        a.k_new[rem] = v0;
+                    else if (pos >= 0 && pos < a.max_ctx)
                         plane[(static_cast<size_t>(kvh) * a.max_ctx + pos) * a.hd + dd] = __float2half_rn(v0);
                     else
                         set_error(a.err, DEVERR_BAD_ARG);

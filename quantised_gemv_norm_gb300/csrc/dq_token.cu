@@ -257,7 +257,10 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
                     const int kvh = rem / A.hd, dd = rem - kvh * A.hd;
                     const size_t plane = static_cast<size_t>(A.n_kv) * A.max_ctx * A.hd;
                     __half* kc = A.kv + static_cast<size_t>(l) * 2 * plane + (which ? plane : 0);
-                    kc[(static_cast<size_t>(kvh) * A.max_ctx + A.pos) * A.hd + dd] = __float2half_rn(v0);
+                    if (!which && A.k_new)  // the attention normalises and rotates it first
+                        A.k_new[rem] = v0;
+                    else
+                        kc[(static_cast<size_t>(kvh) * A.max_ctx + A.pos) * A.hd + dd] = __float2half_rn(v0);
                 }
             }
         }
@@ -321,6 +324,11 @@ __device__ __forceinline__ void tk_attention(int p)
         t.n_keys = A.pos + 1;
         t.step = nullptr;
         t.err = A.err;
+        t.k_new = A.k_new;
+        t.q_norm = A.layers[l].q_norm;
+        t.k_norm = A.layers[l].k_norm;
+        t.rope = A.rope;
+        t.eps = A.eps;
         const int n_keys = A.pos + 1;
         const int L = max((n_keys + ATT_CHUNKS - 1) / ATT_CHUNKS, ATT_MIN_CHUNK);
         const int nact = (n_keys + L - 1) / L;

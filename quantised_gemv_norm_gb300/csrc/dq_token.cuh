@@ -31,6 +31,8 @@ struct TokenLayer {
     const uint8_t* wgate;
     const uint8_t* wup;
     const uint8_t* wdown;
+    const float* q_norm;  // Qwen3 attention inputs: per-head RMSNorm weights [hd] (null: plain attention)
+    const float* k_norm;
     int down_fmt;
     int pad;
 };
@@ -48,6 +50,8 @@ struct TokenArgs {
     float* act;                // [ffn]
     float* part;               // attention partials
     int* counters;             // attention merge counters (zero between phases)
+    float* k_new;              // Qwen3 attention inputs: the token's keys as projected [n_kv hd], else null
+    const float2* rope;        // (cos, sin) table [max_ctx][hd / 2] when k_new is set
     StepArgs* step;            // pos and logits recorded for the diagnostics entry points
     unsigned* bar;             // grid barrier arrival counter (monotonic)
     unsigned bar_base;         // its value when this launch starts

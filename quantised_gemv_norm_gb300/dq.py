@@ -21,6 +21,7 @@ Q4K_BLOCK_BYTES, Q6K_BLOCK_BYTES = 144, 210
 
 # name -> (restype, argtypes); the same names as include/dq.h
 P, I, LL, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_size_t
+D = ctypes.c_double
 SIGNATURES = {
     "dq_status_string": (ctypes.c_char_p, [I]),
     "dq_last_cuda_error": (I, []),
@@ -38,6 +39,8 @@ SIGNATURES = {
     "dq_attention_workspace_bytes": (SZ, [I, I]),
     "dq_attention_decode": (I, [P, P, P, P, I, I, I, I, I, P, SZ, P]),
     "dq_attention_decode_static": (I, [P, P, P, P, I, I, I, I, I, P]),
+    "dq_rope_table": (I, [P, I, I, D, P]),
+    "dq_attention_decode_rope": (I, [P, P, P, P, P, P, P, P, F, I, I, I, I, I, P, SZ, P]),
     "dq_matmul_q4k": (I, [P, P, P, I, I, I, P]),
     "dq_matmul_q4k_path": (I, [P, P, P, I, I, I, I, P]),
     "dq_model_create": (I, [P, P]),
@@ -240,6 +243,31 @@ def attention_decode_static(q: torch.Tensor, k_plane: torch.Tensor, v_plane: tor
     return out
 
 
+def rope_table(max_ctx: int, head_dim: int = 128, theta: float = 1.0e6, device=None) -> torch.Tensor:
+    """fp32 [max_ctx, head_dim // 2, 2]: (cos, sin) of p / theta^(2i / head_dim)."""
+    lib = load()
+    t = torch.empty((max_ctx, head_dim // 2, 2), dtype=torch.float32, device=device or "cuda")
+    _check("dq_rope_table", lib.dq_rope_table(_ptr(t), int(max_ctx), int(head_dim), float(theta), _stream()))
+    return t
+
+
+def attention_decode_rope(q: torch.Tensor, k_new: torch.Tensor, k_plane: torch.Tensor, v_plane: torch.Tensor,
+                          q_norm: torch.Tensor, k_norm: torch.Tensor, rope: torch.Tensor, n_keys: int,
+                          eps: float = 1e-6, workspace: torch.Tensor | None = None, out=None):
+    """Qwen3 attention inputs: q fp32 [n_q, 128] and k_new fp32 [n_kv, 128] as projected are
+    head-normalised and rotated to position n_keys - 1; k_plane row n_keys - 1 is written."""
+    lib = load()
+    n_q, hd = q.shape
+    n_kv, max_ctx, _ = k_plane.shape
+    ws = attention_workspace(n_q, n_kv, q.device) if workspace is None else workspace
+    out = torch.empty_like(q) if out is None else out
+    st = lib.dq_attention_decode_rope(_ptr(q), _ptr(k_new), _ptr(k_plane), _ptr(v_plane), _ptr(out), _ptr(q_norm),
+                                      _ptr(k_norm), _ptr(rope), float(eps), n_q, n_kv, hd, max_ctx, int(n_keys),
+                                      _ptr(ws), ws.numel(), _stream())
+    _check("dq_attention_decode_rope", st)
+    return out
+
+
 # --------------------------------------------------------------- model
 
 
@@ -257,6 +285,7 @@ class _Desc(ctypes.Structure):
         ("vocab", I), ("max_ctx", I), ("eps", F),
         ("attn_norm", P), ("wqkv", P), ("wo", P), ("ffn_norm", P), ("wgate", P), ("wup", P), ("wdown", P),
         ("down_fmt", P), ("out_norm", P), ("wvocab", P), ("kv_cache", P), ("use_graph", I), ("flags", I),
+        ("q_norm", P), ("k_norm", P), ("rope_theta", D),
     ]
 
 
@@ -271,11 +300,13 @@ class Model:
     ``wqkv``, ``wo``, ``ffn_norm``, ``wgate``, ``wup``, ``wdown`` and the list
     ``down_fmt`` (ints), plus ``out_norm``, ``wvocab`` and ``kv_cache``
     (fp16/int16 [L, 2, n_kv, max_ctx, hd]).  The handle borrows them: keep
-    them alive (this object holds references).
+    them alive (this object holds references).  With the Qwen3 attention
+    inputs, ``weights`` also holds per-layer lists ``q_norm`` and ``k_norm``
+    (fp32 [hd]) and ``rope_theta`` is the rotary base (> 1).
     """
 
     def __init__(self, n_layers, hidden, ffn, n_q_heads, n_kv_heads, head_dim, vocab, max_ctx, eps, weights,
-                 use_graph: bool = True, flags: int = 0):
+                 use_graph: bool = True, flags: int = 0, rope_theta: float = 0.0):
         lib = load()
         self.weights = weights
         self.hidden, self.vocab, self.max_ctx = hidden, vocab, max_ctx
@@ -293,6 +324,10 @@ class Model:
                   arr(weights["wgate"]), arr(weights["wup"]), arr(weights["wdown"]),
                   ctypes.cast(fmts, ctypes.c_void_p), weights["out_norm"].data_ptr(), weights["wvocab"].data_ptr(),
                   weights["kv_cache"].data_ptr(), 1 if use_graph else 0, int(flags))
+        if weights.get("q_norm"):
+            d.q_norm = arr(weights["q_norm"])
+            d.k_norm = arr(weights["k_norm"])
+            d.rope_theta = float(rope_theta)
         h = ctypes.c_void_p()
         _check("dq_model_create", lib.dq_model_create(ctypes.byref(d), ctypes.byref(h)))
         self._h = h

@@ -22,9 +22,13 @@ def to_device(m, kv_cache: np.ndarray, device="cuda") -> dict:
         "wvocab": t(m.wvocab),
         "kv_cache": torch.from_numpy(kv_cache.view(np.int16)).to(device),
     }
+    if getattr(m, "q_norm", None):
+        w["q_norm"] = [t(a) for a in m.q_norm]
+        w["k_norm"] = [t(a) for a in m.k_norm]
     return w
 
 
 def model_kwargs(m) -> dict:
     return dict(n_layers=m.n_layers, hidden=m.hidden, ffn=m.ffn, n_q_heads=m.n_q_heads, n_kv_heads=m.n_kv_heads,
-                head_dim=m.head_dim, vocab=m.vocab, max_ctx=m.max_ctx, eps=m.eps)
+                head_dim=m.head_dim, vocab=m.vocab, max_ctx=m.max_ctx, eps=m.eps,
+                rope_theta=float(getattr(m, "rope_theta", 0.0) or 0.0))

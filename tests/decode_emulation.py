@@ -54,6 +54,13 @@ def decode(orc, m, Wd, x_in, pos, kv):
     x = np.asarray(x_in, np.float64)
     for l in range(m.n_layers):
         qkv = Wd["qkv"][l] @ group_round(_rms(x, m.attn_norm[l], m.eps), 2)
+        if getattr(m, "q_norm", None):  # Qwen3 attention inputs, exact (fp64) as in the oracle
+            for h in range(nq):
+                qkv[h * hd:(h + 1) * hd] = orc.rope(orc.head_rmsnorm(qkv[h * hd:(h + 1) * hd], m.q_norm[l], m.eps),
+                                                    pos, m.rope_theta)
+            for g in range(nkv):
+                sl = slice(qdim + g * hd, qdim + (g + 1) * hd)
+                qkv[sl] = orc.rope(orc.head_rmsnorm(qkv[sl], m.k_norm[l], m.eps), pos, m.rope_theta)
         kvf[l, 0, :, pos, :] = qkv[qdim:qdim + kvdim].reshape(nkv, hd).astype(np.float16)
         kvf[l, 1, :, pos, :] = qkv[qdim + kvdim:].reshape(nkv, hd).astype(np.float16)
         att = orc.attention(qkv[:qdim].reshape(nq, hd), kv[l, 0], kv[l, 1], pos + 1).reshape(-1)

@@ -72,6 +72,15 @@ def test_argument_errors_return_before_launch(lib):
     assert lib.dq_matmul_q4k_path(fake, fake, fake, 2, 4, 256, 3, None) == -2  # no such path
     assert lib.dq_matmul_q4k_path(P(17), fake, fake, 2, 4, 256, 2, None) == -3
     assert lib.dq_matmul_q4k_path(fake, fake, fake, 2, 4, 32768, 1, None) == -4
+    assert lib.dq_rope_table(None, 16, 128, 1e6, None) == -1
+    assert lib.dq_rope_table(fake, 16, 127, 1e6, None) == -2              # odd head_dim
+    assert lib.dq_rope_table(fake, 16, 128, 1.0, None) == -2              # theta must exceed 1
+    assert lib.dq_rope_table(P(24), 16, 128, 1e6, None) == -3
+    r = lib.dq_attention_decode_rope
+    assert r(fake, None, fake, fake, fake, fake, fake, fake, 1e-6, 32, 8, 128, 16, 1, fake, 1 << 20, None) == -1
+    assert r(fake, fake, fake, fake, fake, fake, fake, fake, 1e-6, 32, 8, 64, 16, 1, fake, 1 << 20, None) == -4
+    assert r(fake, fake, fake, fake, fake, fake, fake, fake, 1e-6, 32, 8, 128, 16, 0, fake, 1 << 20, None) == -2
+    assert r(fake, fake, fake, fake, fake, fake, fake, P(24), 1e-6, 32, 8, 128, 16, 1, fake, 1 << 20, None) == -3
     assert lib.dq_decode_step(None, fake, 0, fake, None) == -1
     h = P()
     assert lib.dq_model_create(None, ctypes.byref(h)) == -1
@@ -81,3 +90,34 @@ def test_argument_errors_return_before_launch(lib):
 def test_attention_workspace_size(lib):
     assert lib.dq_attention_workspace_bytes(32, 8) == 256 + 32 * 16 * 132 * 4
     assert lib.dq_attention_workspace_bytes(0, 8) == 0
+
+
+def test_model_create_checks_qwen3_inputs_before_allocating(lib):
+    # q_norm set: k_norm, every layer's weights and the rotary base are checked first
+    from quantised_gemv_norm_gb300 import dq
+
+    L = 2
+    fake = [16 * (i + 1) for i in range(L)]
+
+    def arr(vals):
+        a = (ctypes.c_void_p * L)(*vals)
+        keep.append(a)
+        return ctypes.cast(a, ctypes.c_void_p)
+
+    keep = []
+    fmts = (ctypes.c_int * L)(1, 2)
+
+    def desc(q_norm, k_norm, theta):
+        d = dq._Desc(L, 2048, 4096, 8, 2, 128, 1000, 64, 1e-6, arr(fake), arr(fake), arr(fake), arr(fake),
+                     arr(fake), arr(fake), arr(fake), ctypes.cast(fmts, ctypes.c_void_p), 16, 16, 16, 0, 0)
+        d.q_norm = q_norm
+        d.k_norm = k_norm
+        d.rope_theta = theta
+        return d
+
+    h = ctypes.c_void_p()
+    assert lib.dq_model_create(ctypes.byref(desc(arr(fake), None, 1e6)), ctypes.byref(h)) == -1
+    assert lib.dq_model_create(ctypes.byref(desc(arr(fake), arr(fake), 0.5)), ctypes.byref(h)) == -2
+    assert lib.dq_model_create(ctypes.byref(desc(arr(fake), arr([16, 0]), 1e6)), ctypes.byref(h)) == -1
+    assert lib.dq_model_create(ctypes.byref(desc(arr(fake), arr([16, 40]), 1e6)), ctypes.byref(h)) == -3
+    assert h.value is None

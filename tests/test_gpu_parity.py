@@ -188,6 +188,49 @@ def test_attention(dq, orc, n_q, n_kv, n_keys):
         assert normwise(o, r) <= 1e-4
 
 
+def test_rope_table(dq, orc):
+    # row p, pair i: the rotation the oracle applies to the unit vector e_i is (cos, sin) of that angle
+    max_ctx, hd, theta = 40960, 128, 1.0e6
+    tab = dq.rope_table(max_ctx, hd, theta).cpu().numpy().astype(np.float64)
+    for p in (0, 1, 7, 1000, 32767, 40959):
+        for i in range(hd // 2):
+            e = np.zeros(hd)
+            e[i] = 1.0
+            r = orc.rope(e, p, theta)
+            assert abs(tab[p, i, 0] - r[i]) <= 1.2e-7 and abs(tab[p, i, 1] - r[i + hd // 2]) <= 1.2e-7, (p, i)
+    assert np.all(tab[0, :, 0] == 1.0) and np.all(tab[0, :, 1] == 0.0)
+
+
+@pytest.mark.parametrize("n_q,n_kv,n_keys", [(32, 8, 1), (32, 8, 64), (32, 8, 65), (16, 2, 1100), (8, 8, 3000)])
+def test_attention_decode_rope(dq, orc, n_q, n_kv, n_keys):
+    max_ctx, theta, eps = 3072, 1.0e6, 1e-6
+    rng = np.random.default_rng(700 + n_keys)
+    q = (rng.standard_normal((n_q, 128)) * 3.0).astype(np.float32)
+    k_new = (rng.standard_normal((n_kv, 128)) * 3.0).astype(np.float32)
+    q_norm = rng.normal(1.0, 0.1, 128).astype(np.float32)
+    k_norm = rng.normal(1.0, 0.1, 128).astype(np.float32)
+    k = rng.standard_normal((n_kv, max_ctx, 128)).astype(np.float16)
+    v = rng.standard_normal((n_kv, max_ctx, 128)).astype(np.float16)
+    pos = n_keys - 1
+    k[:, pos, :] = 0  # written by the call
+    rope = dq.rope_table(max_ctx, 128, theta)
+    kt = cuda(k)
+    o = dq.attention_decode_rope(cuda(q), cuda(k_new), kt, cuda(v), cuda(q_norm), cuda(k_norm), rope, n_keys,
+                                 eps=eps).cpu().numpy()
+    # oracle: normalise and rotate each head, append the key in fp16, attend
+    qr = np.stack([orc.rope(orc.head_rmsnorm(q[h], q_norm, eps), pos, theta) for h in range(n_q)])
+    kref = np.stack([orc.rope(orc.head_rmsnorm(k_new[g], k_norm, eps), pos, theta) for g in range(n_kv)])
+    k_ref = k.copy()
+    k_ref[:, pos, :] = kref.astype(np.float16)
+    r = orc.attention(qr, k_ref.view(np.uint16), v.view(np.uint16), n_keys)
+    assert normwise(o, r) <= 1e-4
+    got = kt.cpu().numpy()
+    # the appended key: the fp16 rounding of a value within fp32 arithmetic of the exact one
+    assert np.max(np.abs(got[:, pos, :].astype(np.float64) - kref)) <= np.max(np.abs(kref)) * 2.0 ** -10
+    assert np.array_equal(np.delete(got, pos, axis=1).view(np.uint16), np.delete(k, pos, axis=1).view(np.uint16))
+    assert dq.device_error() == 0
+
+
 # ------------------------------------------------------------- M-sweep
 
 
@@ -313,13 +356,35 @@ def test_decode_shape_outside_fused_kernel_runs_kernels(dq, orc):
     _run_decode(dq, orc, m, kv, [3], emulate=True, flags=2, fused=False)
 
 
+@pytest.mark.parametrize("mode", ["fused", "kernels"])
+def test_decode_small_model_qwen3_attention(dq, orc, mode):
+    # per-head q/k RMSNorm and rotary embedding: the first positions, one and two chunks, 16 chunks
+    m = synth.make_model(26, n_layers=2, hidden=2048, ffn=4096, n_q_heads=16, n_kv_heads=4, head_dim=128,
+                         vocab=300, max_ctx=1200, qwen3_attention=True)
+    kv = synth.make_kv_cache(26, m, 1100)
+    flags, fused = MODES[mode]
+    _run_decode(dq, orc, m, kv, [0, 1, 2, 63, 64, 1100], emulate=True, flags=flags, fused=fused)
+
+
+def test_decode_qwen3_attention_modes_agree(dq, orc):
+    # the fused kernel and the separate kernels compute the same norm, rotation and cache row
+    m = synth.make_model(27, n_layers=2, hidden=2048, ffn=4096, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                         vocab=500, max_ctx=300, qwen3_attention=True)
+    kv = synth.make_kv_cache(27, m, 257)
+    a = _run_decode(dq, orc, m, kv, [257, 258], emulate=True, flags=2, fused=True)
+    b = _run_decode(dq, orc, m, kv, [257, 258], emulate=True, flags=0, fused=False)
+    for x, y in zip(a, b):
+        assert normwise(x, y) <= GEMV_TOL
+
+
 _QWEN = {}
 
 
 def _qwen3():
+    # the Qwen3-8B shape with Qwen3's attention inputs (q/k head norms, rotary base 1e6)
     if "m" not in _QWEN:
         from quantised_gemv_norm_gb300 import upload
-        m = synth.make_model(1, max_ctx=1024, **synth.QWEN3_8B)
+        m = synth.make_model(1, max_ctx=1024, qwen3_attention=True, **synth.QWEN3_8B)
         _QWEN["m"] = m
         _QWEN["w"] = upload.to_device(m, synth.make_kv_cache(1, m, 0))
     return _QWEN["m"], _QWEN["w"]
