@@ -594,17 +594,12 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
     }
 
     // Tile t is completed (its slot refilled, its rows' epilogue run) by warp
-    // t % 16, DEFER tiles later, when every warp has normally released it: no
-    // warp waits for another on the common path.
-    const int DEFER = a.nstage >= 4 ? 2 : 1;
-    // Counters instead of divisions by the runtime stage count: stage t uses ring
-    // slot t % nstage with phase (t / nstage) & 1 and partial-sum slot t % (2 nstage).
+    // t % 16 as soon as that warp sees every warp release it: it tests the
+    // slot's `empty` barrier after each of its stages and keeps testing while it
+    // waits for its next stage, so the refill leaves without a fixed delay and a
+    // warp only ever waits on another when its next stage needs that refill.
     const int rg_shift = 31 - __clz(a.RG);  // RG is a power of two
-    auto complete = [&](int tc, int sc, uint32_t phase, int rslot) -> bool {
-        if (!mbar_wait(&empty[sc], phase)) {  // all warps done with tile tc
-            set_error(a.err, DEVERR_TIMEOUT_EMPTY);
-            return false;
-        }
+    auto complete = [&](int tc, int rslot) {
         if (lane == 0 && tc + a.nstage < ntiles) {
             issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, tc + a.nstage, r0, r1, R,
                              pol);
@@ -648,17 +643,45 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
                 }
             }
         }
-        return true;
     };
 
+    // Counters instead of divisions by the runtime stage count: stage t uses ring
+    // slot t % nstage with phase (t / nstage) & 1 and partial-sum slot t % (2 nstage).
+    int pend = -1, pend_s = 0, pend_r = 0;  // the tile this warp completes next (-1: none)
+    uint32_t pend_ph = 0;
     bool ok = true;
     int t = 0, s = 0, rslot = 0;
     uint32_t phase = 0;
     for (; t < ntiles && ok; ++t) {
-        if (!mbar_wait(&full[s], phase)) {
-            set_error(a.err, DEVERR_TIMEOUT_FULL);
-            ok = false;
-            break;
+        if (pend < 0) {
+            if (!mbar_wait(&full[s], phase)) {
+                set_error(a.err, DEVERR_TIMEOUT_FULL);
+                ok = false;
+                break;
+            }
+        } else if (!mbar_test_wait(&full[s], phase)) {  // wait for the stage, completing the pending tile meanwhile
+            const unsigned long long t0 = globaltimer_ns();
+            bool got = false;
+            while (pend >= 0) {
+                if (mbar_test_wait(&empty[pend_s], pend_ph)) {
+                    complete(pend, pend_r);
+                    pend = -1;
+                } else if (mbar_test_wait(&full[s], phase)) {
+                    got = true;
+                    break;
+                } else if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                    set_error(a.err, DEVERR_TIMEOUT_EMPTY);
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok)
+                break;
+            if (!got && !mbar_wait(&full[s], phase)) {
+                set_error(a.err, DEVERR_TIMEOUT_FULL);
+                ok = false;
+                break;
+            }
         }
         if (trace && t == 0 && tid == 0)
             trace[5] = globaltimer_ns();
@@ -671,17 +694,15 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             mbar_arrive(&empty[s]);  // release semantics: the partial sums are visible to the completer
         if (ttile && tid == 0 && t < 64)
             ttile[2 * t + 1] = clock64();
-        const int tc = t - DEFER;
-        if (tc >= 0 && (tc & (NCONS_WARPS - 1)) == warp) {
-            int sc = s - DEFER, rc = rslot - DEFER;
-            uint32_t pc = phase;
-            if (sc < 0) {
-                sc += a.nstage;
-                pc ^= 1u;
-            }
-            if (rc < 0)
-                rc += 2 * a.nstage;
-            ok = complete(tc, sc, pc, rc);
+        if ((t & (NCONS_WARPS - 1)) == warp) {  // this warp's tile (a previous one was completed before
+            pend = t;                           // its stage t - 16 + nstage < t could be waited for)
+            pend_s = s;
+            pend_ph = phase;
+            pend_r = rslot;
+        }
+        if (pend >= 0 && mbar_test_wait(&empty[pend_s], pend_ph)) {
+            complete(pend, pend_r);
+            pend = -1;
         }
         if (++s == a.nstage) {
             s = 0;
@@ -690,12 +711,13 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         if (++rslot == 2 * a.nstage)
             rslot = 0;
     }
-    // tiles still to complete: the last DEFER (after a timeout none are: nothing is refilled then)
-    if (ok)
-        for (int tc = max(0, ntiles - DEFER); tc < ntiles; ++tc)
-            if ((tc & (NCONS_WARPS - 1)) == warp &&
-                !complete(tc, tc % a.nstage, (tc / a.nstage) & 1, tc % (2 * a.nstage)))
-                break;
+    // the tile still pending (after a timeout nothing is: no refill is owed then)
+    if (ok && pend >= 0) {
+        if (mbar_wait(&empty[pend_s], pend_ph))
+            complete(pend, pend_r);
+        else
+            set_error(a.err, DEVERR_TIMEOUT_EMPTY);
+    }
     (void)gw0;
     if (trace && lane == 0) {  // the last warp of the block to finish records the end
         atomicMax(trace + 6, globaltimer_ns());

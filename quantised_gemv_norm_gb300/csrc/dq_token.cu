@@ -217,14 +217,12 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
     load_units<FMT, PL, UL>(us, have, tk_xq(), pp, P, rstd);
     tk_trace(p, 7);
 
-    // Complete tile tc (token tile Tc): wait until every warp released it,
-    // refill its slot with tile Tc + TK_NSTAGE, run the epilogue of its rows.
-    auto complete = [&](int tc, int Tc) -> bool {
-        const int sc = Tc & (TK_NSTAGE - 1);
-        if (!mbar_wait(&m.empty[sc], (Tc / TK_NSTAGE) & 1)) {
-            set_error(A.err, DEVERR_TIMEOUT_EMPTY);
-            return false;
-        }
+    // Complete tile tc (token tile Tc) once every warp has released it: refill
+    // its slot with tile Tc + TK_NSTAGE, run the epilogue of its rows.  Tile Tc
+    // belongs to warp Tc % 16, which tests the slot's `empty` barrier after each
+    // of its stages and while it waits for its next one (no fixed delay; a warp
+    // only waits on another when its next stage needs that very refill).
+    auto complete = [&](int tc, int Tc) {
         if (lane == 0 && Tc + TK_NSTAGE < m.ttotal)
             tk_issue(Tc + TK_NSTAGE, icur);
         const float* rb = tk_red() + (Tc & (2 * TK_NSTAGE - 1)) * TK_WARPS * TK_RED_STRIDE;
@@ -264,13 +262,36 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
                 }
             }
         }
-        return true;
     };
+    auto released = [&](int Tc) { return mbar_test_wait(&m.empty[Tc & (TK_NSTAGE - 1)], (Tc / TK_NSTAGE) & 1); };
 
     bool ok = true;
+    int pend = -1;  // this warp's tile (phase-local index) still to complete
     for (int t = 0; t < ntiles; ++t, ++T) {
         const int s = T & (TK_NSTAGE - 1);
-        if (!mbar_wait(&m.full[s], (T / TK_NSTAGE) & 1)) {
+        const uint32_t ph = (T / TK_NSTAGE) & 1;
+        bool got = false;
+        if (pend >= 0 && !mbar_test_wait(&m.full[s], ph)) {  // complete the pending tile while waiting
+            const unsigned long long t0 = globaltimer_ns();
+            while (pend >= 0) {
+                if (released(T0 + pend)) {
+                    complete(pend, T0 + pend);
+                    pend = -1;
+                } else if (mbar_test_wait(&m.full[s], ph)) {
+                    got = true;
+                    break;
+                } else if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                    set_error(A.err, DEVERR_TIMEOUT_EMPTY);
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok)
+                break;
+        } else if (pend >= 0) {
+            got = true;
+        }
+        if (!got && !mbar_wait(&m.full[s], ph)) {
             set_error(A.err, DEVERR_TIMEOUT_FULL);
             ok = false;
             break;
@@ -282,17 +303,21 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
             tk_red() + ((T & (2 * TK_NSTAGE - 1)) * TK_WARPS + warp) * TK_RED_STRIDE, lane);
         if (lane == 0)
             mbar_arrive(&m.empty[s]);
-        if (t >= TK_DEFER && (T - TK_DEFER) % TK_WARPS == warp && !complete(t - TK_DEFER, T - TK_DEFER)) {
-            ok = false;
-            break;
+        if (T % TK_WARPS == warp)
+            pend = t;
+        if (pend >= 0 && released(T0 + pend)) {
+            complete(pend, T0 + pend);
+            pend = -1;
         }
     }
-    if (ok)
-        for (int tc = max(0, ntiles - TK_DEFER); tc < ntiles; ++tc)
-            if ((T0 + tc) % TK_WARPS == warp && !complete(tc, T0 + tc)) {
-                ok = false;
-                break;
-            }
+    if (ok && pend >= 0) {  // the phase's epilogue must be done before the next barrier
+        if (mbar_wait(&m.empty[(T0 + pend) & (TK_NSTAGE - 1)], ((T0 + pend) / TK_NSTAGE) & 1))
+            complete(pend, T0 + pend);
+        else {
+            set_error(A.err, DEVERR_TIMEOUT_EMPTY);
+            ok = false;
+        }
+    }
     if (!ok)
         m.dead = 1;
     tk_trace(p, 4);

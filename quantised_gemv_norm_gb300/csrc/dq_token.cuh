@@ -9,7 +9,6 @@ constexpr int TK_THREADS = 512;    // 16 warps, 128 registers a thread
 constexpr int TK_WARPS = TK_THREADS / 32;
 constexpr int TK_NSTAGE = 4;       // weight ring slots per block
 constexpr int TK_SLOT = 40960;     // bytes per slot (largest tile: 4 Q6_K rows of K = 12288)
-constexpr int TK_DEFER = 2;        // a stage is completed this many stages after it is consumed
 constexpr int TK_RED_STRIDE = 4;   // floats per warp in one partial-sum slot
 
 // Phase kinds.  Per layer: QKV, ATTN, O, GATEUP, DOWN (Q4_K or Q6_K); then VOCAB.
