@@ -23,6 +23,7 @@ _lib = None
 
 Q4K_BLOCK_BYTES = 144
 Q6K_BLOCK_BYTES = 210
+Q2K_BLOCK_BYTES = 84
 
 
 def build(force: bool = False) -> str:
@@ -51,6 +52,10 @@ def _load():
         "oracle_unpack_q6k": (None, [P, P, P, P]),
         "oracle_pack_q6k": (None, [ctypes.c_uint16, P, P, P]),
         "oracle_dequant_q4k": (None, [P, i64, P]),
+        "oracle_unpack_q2k": (None, [P, P, P, P, P, P]),
+        "oracle_pack_q2k": (None, [ctypes.c_uint16, ctypes.c_uint16, P, P, P, P]),
+        "oracle_dequant_q2k": (None, [P, i64, P]),
+        "oracle_gemv_q2k": (None, [P, P, P, i32, i32]),
         "oracle_dequant_q6k": (None, [P, i64, P]),
         "oracle_gemv_bf16": (None, [P, P, P, i32, i32]),
         "oracle_gemv_q4k": (None, [P, P, P, i32, i32]),
@@ -128,6 +133,35 @@ def pack_q4k(d_bits: int, dmin_bits: int, sc, m, q) -> np.ndarray:
     return out
 
 
+def unpack_q2k(block: np.ndarray):
+    """-> (d, dmin, sc[16], m[16], q[256]) of one 84-byte Q2_K block."""
+    blk = _c(block, np.uint8)
+    assert blk.size == Q2K_BLOCK_BYTES
+    d = ctypes.c_double()
+    dmin = ctypes.c_double()
+    sc = np.zeros(16, np.int32)
+    m = np.zeros(16, np.int32)
+    q = np.zeros(256, np.int32)
+    _load().oracle_unpack_q2k(_p(blk), ctypes.byref(d), ctypes.byref(dmin), _p(sc), _p(m), _p(q))
+    return d.value, dmin.value, sc, m, q
+
+
+def pack_q2k(d_bits: int, dmin_bits: int, sc, m, q) -> np.ndarray:
+    out = np.zeros(Q2K_BLOCK_BYTES, np.uint8)
+    _load().oracle_pack_q2k(int(d_bits), int(dmin_bits), _p(_c(sc, np.int32)), _p(_c(m, np.int32)),
+                            _p(_c(q, np.int32)), _p(out))
+    return out
+
+
+def dequant_q2k(blocks: np.ndarray) -> np.ndarray:
+    b = _c(blocks, np.uint8).reshape(-1)
+    assert b.size % Q2K_BLOCK_BYTES == 0
+    n = b.size // Q2K_BLOCK_BYTES
+    out = np.empty(n * 256, np.float64)
+    _load().oracle_dequant_q2k(_p(b), n, _p(out))
+    return out
+
+
 def unpack_q6k(block: np.ndarray):
     """-> (d, sc[16], q[256]) of one 210-byte Q6_K block."""
     blk = _c(block, np.uint8)
@@ -189,6 +223,10 @@ def _gemv_quant(fn, bpb, W, x, rows, K):
 
 def gemv_q4k(W: np.ndarray, x: np.ndarray, rows: int, K: int) -> np.ndarray:
     return _gemv_quant(_load().oracle_gemv_q4k, Q4K_BLOCK_BYTES, W, x, rows, K)
+
+
+def gemv_q2k(W: np.ndarray, x: np.ndarray, rows: int, K: int) -> np.ndarray:
+    return _gemv_quant(_load().oracle_gemv_q2k, Q2K_BLOCK_BYTES, W, x, rows, K)
 
 
 def gemv_q6k(W: np.ndarray, x: np.ndarray, rows: int, K: int) -> np.ndarray:

@@ -53,6 +53,18 @@
  *     [208,210) d: IEEE binary16
  *     q_n = low4 | high2 << 4 (0..63); weight n = d * sc[n/16] * (q_n - 32)
  *
+ *   Q2_K super-block, 84 bytes, 256 weights n = 16*j + i (sub-block j = 0..15):
+ *     [0,2)    d     IEEE binary16
+ *     [2,4)    dmin  IEEE binary16
+ *     [4,20)   byte 4 + j: sc_j in its low nibble, m_j in its high nibble (unsigned 4-bit)
+ *     [20,84)  codes: byte 20 + 4*j + b (b = 0..3) holds the 2-bit codes of
+ *              weights 16j + 4k + b (k = 0..3) at bits [2k, 2k+2)
+ *     weight n = d * sc_j * q_n - dmin * m_j
+ *   (The pages name 2-bit codes as the next bytes-halving step -- "The Mountain
+ *   Runs", its closing section: expert kernels that dequantise 2/4-bit codes in
+ *   registers -- without a layout; this one is Q4_K's scale/min scheme with
+ *   2-bit codes and 4-bit scales over 16-weight sub-blocks: 2.625 bits/weight.)
+ *
  *   bf16 matrix: row-major, K contiguous, bfloat16 = top 16 bits of an fp32.
  *   fp16 KV cache: [layer][2 (k, v)][kv_head][max_ctx][head_dim] binary16.
  */
@@ -234,6 +246,50 @@ static void dequant_q6k_block(const uint8_t *blk, double *w)
         w[n] = d * sc[n / 16] * (q[n] - 32);
 }
 
+ORACLE_API void oracle_unpack_q2k(const uint8_t *blk, double *d, double *dmin, int sc[16], int m[16], int q[256])
+{
+    *d = oracle_half_to_double(rd16(blk + 0));
+    *dmin = oracle_half_to_double(rd16(blk + 2));
+    for (int j = 0; j < 16; j++) {
+        sc[j] = blk[4 + j] & 15;
+        m[j] = blk[4 + j] >> 4;
+    }
+    for (int j = 0; j < 16; j++)
+        for (int k = 0; k < 4; k++)
+            for (int b = 0; b < 4; b++)
+                q[16 * j + 4 * k + b] = (blk[20 + 4 * j + b] >> (2 * k)) & 3;
+}
+
+ORACLE_API void oracle_pack_q2k(uint16_t d_bits, uint16_t dmin_bits, const int sc[16], const int m[16], const int q[256], uint8_t *blk)
+{
+    memset(blk, 0, 84);
+    blk[0] = d_bits & 255;    blk[1] = d_bits >> 8;
+    blk[2] = dmin_bits & 255; blk[3] = dmin_bits >> 8;
+    for (int j = 0; j < 16; j++)
+        blk[4 + j] = (uint8_t)((sc[j] & 15) | ((m[j] & 15) << 4));
+    for (int j = 0; j < 16; j++)
+        for (int k = 0; k < 4; k++)
+            for (int b = 0; b < 4; b++)
+                blk[20 + 4 * j + b] |= (uint8_t)((q[16 * j + 4 * k + b] & 3) << (2 * k));
+}
+
+/* weight n = d * sc[n/16] * q_n - dmin * m[n/16], evaluated in double. */
+static void dequant_q2k_block(const uint8_t *blk, double *w)
+{
+    double d, dmin;
+    int sc[16], m[16], q[256];
+    oracle_unpack_q2k(blk, &d, &dmin, sc, m, q);
+    for (int n = 0; n < 256; n++)
+        w[n] = d * sc[n / 16] * q[n] - dmin * m[n / 16];
+}
+
+ORACLE_API void oracle_dequant_q2k(const uint8_t *blocks, long long nblocks, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (long long b = 0; b < nblocks; b++)
+        dequant_q2k_block(blocks + 84 * b, out + 256 * b);
+}
+
 ORACLE_API void oracle_dequant_q4k(const uint8_t *blocks, long long nblocks, double *out)
 {
 #pragma omp parallel for schedule(static)
@@ -250,7 +306,7 @@ ORACLE_API void oracle_dequant_q6k(const uint8_t *blocks, long long nblocks, dou
 
 /* ----------------------------------------------------------------- GEMV -- */
 
-enum { FMT_BF16 = 0, FMT_Q4K = 1, FMT_Q6K = 2 };
+enum { FMT_BF16 = 0, FMT_Q4K = 1, FMT_Q6K = 2, FMT_Q2K = 3 };
 
 static size_t row_bytes(int fmt, int K)
 {
@@ -258,6 +314,8 @@ static size_t row_bytes(int fmt, int K)
         return (size_t)K * 2;
     if (fmt == FMT_Q4K)
         return (size_t)(K / 256) * 144;
+    if (fmt == FMT_Q2K)
+        return (size_t)(K / 256) * 84;
     return (size_t)(K / 256) * 210;
 }
 
@@ -277,6 +335,8 @@ static void gemv_any(int fmt, const uint8_t *W, const double *x, double *y, int 
             for (int b = 0; b < K / 256; b++) {
                 if (fmt == FMT_Q4K)
                     dequant_q4k_block(row + 144 * (size_t)b, w);
+                else if (fmt == FMT_Q2K)
+                    dequant_q2k_block(row + 84 * (size_t)b, w);
                 else
                     dequant_q6k_block(row + 210 * (size_t)b, w);
                 for (int n = 0; n < 256; n++)
@@ -311,6 +371,15 @@ ORACLE_API void oracle_gemv_q6k(const uint8_t *W, const float *x, double *y, int
     for (int k = 0; k < K; k++)
         xd[k] = x[k];
     gemv_any(FMT_Q6K, W, xd, y, rows, K);
+    free(xd);
+}
+
+ORACLE_API void oracle_gemv_q2k(const uint8_t *W, const float *x, double *y, int rows, int K)
+{
+    double *xd = (double *)malloc(sizeof(double) * (size_t)K);
+    for (int k = 0; k < K; k++)
+        xd[k] = x[k];
+    gemv_any(FMT_Q2K, W, xd, y, rows, K);
     free(xd);
 }
 

@@ -30,7 +30,8 @@ import numpy as np
 
 Q4K_BLOCK_BYTES = 144
 Q6K_BLOCK_BYTES = 210
-FMT_BF16, FMT_Q4K, FMT_Q6K = 0, 1, 2
+Q2K_BLOCK_BYTES = 84
+FMT_BF16, FMT_Q4K, FMT_Q6K, FMT_Q2K = 0, 1, 2, 3
 
 # Role ids keep every tensor on its own random stream.
 _ROLES = {"x": 1, "gamma": 2, "beta": 3, "w": 4, "wqkv": 10, "wo": 11, "wgate": 12, "wup": 13,
@@ -100,8 +101,17 @@ def q6k_blocks(rng: np.random.Generator, nblocks: int) -> np.ndarray:
     return b
 
 
+def q2k_blocks(rng: np.random.Generator, nblocks: int) -> np.ndarray:
+    # d and dmin in Q4_K's binades: d sc q (< 2^17 units of 2^-23) minus dmin m
+    # (< 2^18 units) is an fp32 number
+    b = random_bytes(rng, nblocks * Q2K_BLOCK_BYTES).reshape(nblocks, Q2K_BLOCK_BYTES)
+    b[:, 1] = (b[:, 1] & 0x03) | (2 << 2)
+    b[:, 3] = (b[:, 3] & 0x03) | (5 << 2)
+    return b
+
+
 def quant_matrix(seed: int, fmt: int, rows: int, K: int, *key: int) -> np.ndarray:
-    """A [rows, K] matrix in Q4_K or Q6_K blocks, as uint8 [rows, row_bytes]."""
+    """A [rows, K] matrix in Q4_K, Q6_K or Q2_K blocks, as uint8 [rows, row_bytes]."""
     assert K % 256 == 0
     rng = rng_for(seed, _role("w"), fmt, rows, K, *key)
     nb = rows * (K // 256)
@@ -109,6 +119,8 @@ def quant_matrix(seed: int, fmt: int, rows: int, K: int, *key: int) -> np.ndarra
         return q4k_blocks(rng, nb).reshape(rows, -1)
     if fmt == FMT_Q6K:
         return q6k_blocks(rng, nb).reshape(rows, -1)
+    if fmt == FMT_Q2K:
+        return q2k_blocks(rng, nb).reshape(rows, -1)
     raise ValueError(fmt)
 
 
@@ -119,7 +131,7 @@ def activation(seed: int, K: int, *key: int) -> np.ndarray:
 def row_bytes(fmt: int, K: int) -> int:
     if fmt == FMT_BF16:
         return 2 * K
-    return (K // 256) * (Q4K_BLOCK_BYTES if fmt == FMT_Q4K else Q6K_BLOCK_BYTES)
+    return (K // 256) * {FMT_Q4K: Q4K_BLOCK_BYTES, FMT_Q6K: Q6K_BLOCK_BYTES, FMT_Q2K: Q2K_BLOCK_BYTES}[fmt]
 
 
 # ----------------------------------------------------------------- models

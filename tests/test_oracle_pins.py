@@ -190,6 +190,95 @@ def test_generator_binades_make_dequant_exact_in_fp32(orc):
     assert 0.01 < np.std(w6) < 0.2
 
 
+# ----------------------------------------------------------------- Q2_K blocks
+
+
+def _q2k_bytes_by_hand(d_bits, dmin_bits, sc, m, q):
+    # the layout as one little-endian integer: byte 4 + j = sc_j | m_j << 4; the code of
+    # weight 16j + 4k + b sits at bit 2k of byte 20 + 4j + b
+    v = d_bits | dmin_bits << 16
+    for j in range(16):
+        v |= (int(sc[j]) | int(m[j]) << 4) << (8 * (4 + j))
+    for n in range(256):
+        j, r = divmod(n, 16)
+        k, b = divmod(r, 4)
+        v |= int(q[n]) << (8 * (20 + 4 * j + b) + 2 * k)
+    return np.frombuffer(v.to_bytes(84, "little"), np.uint8)
+
+
+def test_q2k_layout_matches_independent_encoder(orc):
+    rng = np.random.default_rng(11)
+    for _ in range(20):
+        sc, m, q = rng.integers(0, 16, 16), rng.integers(0, 16, 16), rng.integers(0, 4, 256)
+        d_bits, dmin_bits = int(rng.integers(0, 0x7C00)), int(rng.integers(0, 0x7C00))
+        ref = _q2k_bytes_by_hand(d_bits, dmin_bits, sc, m, q)
+        assert np.array_equal(orc.pack_q2k(d_bits, dmin_bits, sc, m, q), ref)
+        d, dmin, sc2, m2, q2 = orc.unpack_q2k(ref)
+        assert d == orc.half_to_double(d_bits) and dmin == orc.half_to_double(dmin_bits)
+        assert np.array_equal(sc2, sc) and np.array_equal(m2, m) and np.array_equal(q2, q)
+
+
+def test_q2k_bytes_by_hand(orc):
+    # weight 0 is bits 0-1 of byte 20, weight 4 bits 2-3, weight 1 bits 0-1 of byte 21,
+    # weight 16 (sub-block 1) bits 0-1 of byte 24; sc_3 = 5 and m_3 = 9 make byte 7 = 0x95
+    q = np.zeros(256, int)
+    q[0], q[4], q[1], q[16] = 3, 1, 2, 1
+    sc, m = np.zeros(16, int), np.zeros(16, int)
+    sc[3], m[3] = 5, 9
+    blk = orc.pack_q2k(0x3C00, 0x3800, sc, m, q)
+    assert blk[20] == 0b0111 and blk[21] == 0b10 and blk[24] == 1 and blk[7] == 0x95
+    assert blk[0] == 0x00 and blk[1] == 0x3C and blk[2] == 0x00 and blk[3] == 0x38
+    assert int(blk[22]) == int(blk[23]) == 0 and np.count_nonzero(blk[25:]) == 0
+
+
+def test_q2k_dequant_special_cases(orc):
+    one, half = 0x3C00, 0x3800
+    # all codes 3, scale 1, min 0, d = 1 -> every weight 3
+    assert np.all(orc.dequant_q2k(orc.pack_q2k(one, 0, [1] * 16, [0] * 16, [3] * 256)) == 3.0)
+    # codes 0, min 15, dmin 0.5 -> -7.5
+    assert np.all(orc.dequant_q2k(orc.pack_q2k(one, half, [7] * 16, [15] * 16, [0] * 256)) == -7.5)
+    # per-sub-block scale and min on their own 16 weights, sign of the min term
+    sc = [j % 16 for j in range(16)]
+    m = [15 - j for j in range(16)]
+    q = [n % 4 for n in range(256)]
+    w = orc.dequant_q2k(orc.pack_q2k(one, half, sc, m, q))
+    want = [1.0 * sc[n // 16] * (n % 4) - 0.5 * m[n // 16] for n in range(256)]
+    assert np.array_equal(w, np.array(want))
+
+
+def test_q2k_single_code_moves_single_weight(orc):
+    base = np.zeros(256, int)
+    ref = orc.dequant_q2k(orc.pack_q2k(0x3C00, 0, [1] * 16, [0] * 16, base))
+    for n in (0, 1, 3, 4, 15, 16, 17, 100, 255):
+        q = base.copy()
+        q[n] = 2
+        w = orc.dequant_q2k(orc.pack_q2k(0x3C00, 0, [1] * 16, [0] * 16, q))
+        assert list(np.nonzero(w != ref)[0]) == [n] and w[n] == 2.0
+
+
+def test_q2k_generator_exact_in_fp32_and_ledger(orc):
+    w2 = orc.dequant_q2k(synth.q2k_blocks(np.random.default_rng(12), 400))
+    assert np.array_equal(w2.astype(np.float32).astype(np.float64), w2)
+    assert 0.001 < np.std(w2) < 0.2
+    # 84 bytes per 256 weights: 2.625 bits per weight, 7/12 of Q4_K's bytes
+    assert synth.Q2K_BLOCK_BYTES * 8 / 256 == 2.625 and synth.row_bytes(synth.FMT_Q2K, 4096) == 1344
+
+
+def test_gemv_q2k_brute_force_integers(orc):
+    rng = np.random.default_rng(13)
+    rows, K = 4, 768
+    blocks, Wint = [], np.zeros((rows, K), np.int64)
+    for r in range(rows):
+        for b in range(K // 256):
+            sc, m, q = rng.integers(0, 16, 16), rng.integers(0, 16, 16), rng.integers(0, 4, 256)
+            blocks.append(orc.pack_q2k(0x3C00, 0x3C00, sc, m, q))
+            for n in range(256):
+                Wint[r, 256 * b + n] = sc[n // 16] * q[n] - m[n // 16]
+    x = rng.integers(-9, 10, K).astype(np.float32)
+    want = [sum(int(Wint[r, k]) * int(x[k]) for k in range(K)) for r in range(rows)]
+    assert np.array_equal(orc.gemv_q2k(np.concatenate(blocks), x, rows, K), np.array(want, np.float64))
+
+
 # ----------------------------------------------------------------------- GEMV
 
 
@@ -229,7 +318,8 @@ def test_gemv_quant_matches_numpy_matmul(orc):
     # GEMV = (dequantised matrix) @ x: numpy's float64 matmul as the library special case.
     rows, K = 37, 1024
     for fmt, deq, gemv in ((synth.FMT_Q4K, orc.dequant_q4k, orc.gemv_q4k),
-                           (synth.FMT_Q6K, orc.dequant_q6k, orc.gemv_q6k)):
+                           (synth.FMT_Q6K, orc.dequant_q6k, orc.gemv_q6k),
+                           (synth.FMT_Q2K, orc.dequant_q2k, orc.gemv_q2k)):
         W = synth.quant_matrix(7, fmt, rows, K)
         x = synth.activation(7, K)
         Wd = deq(W).reshape(rows, K)
