@@ -333,6 +333,7 @@ def run_ours(args):
 
     # ---- M-token sweep of one Q4_K matrix (tensor cores vs one GEMV per token)
     msweep = run_msweep(device) if not args.no_msweep else {}
+    lowbit = run_lowbit(device) if not args.no_msweep else {}
 
     tb = token_bytes(0)
     out = {
@@ -360,6 +361,7 @@ def run_ours(args):
         "ctx512": ctx,
         "fused_token_kernel": fused,
         "msweep": msweep,
+        "lowbit_gemv": lowbit,
         "e2e": {"value": round(K * world / e2e_max, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * m.hidden,
                 "d2h_bytes_per_step": 4 * m.vocab},
         "gpu_launches": model.launches_per_step * K,
@@ -421,6 +423,46 @@ def run_msweep(device, reps: int = 20) -> dict:
     out["M_star_inputs"] = {"R_TFLOPs": R, "R_source": rsrc, "BW_GBps": bw, "BW_source": bsrc}
     t1 = out["tensor"]["1"]["us"]
     out["tensor_cost_ratio_vs_M1"] = {k: round(v["us"] / t1, 3) for k, v in out["tensor"].items()}
+    return out
+
+
+def run_lowbit(device, reps: int = 20) -> dict:
+    """The 2-bit (Q2_K) GEMV against the 4- and 6-bit ones on the same shapes:
+    per call time from CUDA events, each call on the next of enough device
+    copies to exceed L2 (weights read from HBM every call)."""
+    import torch
+
+    from quantised_gemv_norm_gb300 import dq
+
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    stream = torch.cuda.current_stream(device)
+    bw, bsrc = hbm_peak_gbs()
+    out = {}
+    for rows, K in ((12288, 4096), (151936, 4096)):
+        x = torch.from_numpy(synth.activation(SEED, K)).to(device)
+        y = torch.empty(rows, dtype=torch.float32, device=device)
+        res = {}
+        for name, fmt, fn in (("q2k", synth.FMT_Q2K, dq.gemv_q2k), ("q4k", synth.FMT_Q4K, dq.gemv_q4k),
+                              ("q6k", synth.FMT_Q6K, dq.gemv_q6k)):
+            W = torch.from_numpy(synth.quant_matrix(SEED, fmt, rows, K)).to(device)
+            wbytes = W.numel()
+            copies = [W] + [W.clone() for _ in range(max(0, -(-(3 * l2) // wbytes) - 1))]
+            for i in range(3):
+                fn(copies[i % len(copies)], x, out=y)
+            torch.cuda.synchronize(device)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(reps):
+                fn(copies[i % len(copies)], x, out=y)
+            b.record(stream)
+            torch.cuda.synchronize(device)
+            us = a.elapsed_time(b) * 1e3 / reps
+            res[name] = {"weight_bytes": wbytes, "us": round(us, 2), "GBps": round(wbytes / us / 1e3, 1),
+                         "frac_of_peak": round(wbytes / us / 1e3 / bw, 4), "weights_per_ns": round(rows * K / us / 1e3, 1)}
+            del copies, W
+        out["%dx%d" % (rows, K)] = res
+    out["peak_GBps"] = bw
+    out["peak_source"] = bsrc
     return out
 
 

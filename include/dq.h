@@ -40,9 +40,18 @@
  *     [192,208) int8 sc[16], sc[s] for weights 16s..16s+15
  *     [208,210) d (binary16)
  *     q_n = low4 | high2 << 4;  w_n = d * sc[n/16] * (q_n - 32)
+ *   Q2_K, 84 bytes, weights n = 16 j + i (j = 0..15): 2-bit codes, the step
+ *   below 4 bits that "The Mountain Runs" names (its closing section: the
+ *   expert kernels dequantise 2/4-bit codes in registers) without a layout:
+ *     [0,2) d (binary16)  [2,4) dmin (binary16)
+ *     [4,20) byte 4+j: low nibble sc_j, high nibble m_j (unsigned 4-bit)
+ *     [20,84) byte 20+4j+b (b = 0..3): the code of weight 16j+4k+b at bits
+ *             2k..2k+1 (k = 0..3)
+ *     w_n = d * sc_j * q_n - dmin * m_j      (2.625 bits per weight)
  *   A quantised matrix is row-major: row r is the K/256 blocks of that row,
  *   back to back.  The library requires 16-byte aligned rows, i.e. K % 256 == 0
- *   for Q4_K and K % 2048 == 0 for Q6_K, and a 16-byte aligned base pointer.
+ *   for Q4_K, K % 2048 == 0 for Q6_K and K % 1024 == 0 for Q2_K, and a
+ *   16-byte aligned base pointer.
  *   bf16 matrices are row-major [rows][K], K % 8 == 0, 16-byte aligned.
  */
 #ifndef DQ_H
@@ -75,6 +84,7 @@ typedef enum {
 #define DQ_FMT_BF16 0
 #define DQ_FMT_Q4K 1
 #define DQ_FMT_Q6K 2
+#define DQ_FMT_Q2K 3
 
 /* Static text for a status code (never NULL). */
 DQ_API const char* dq_status_string(int status);
@@ -133,12 +143,16 @@ DQ_API int dq_layernorm_threads(const float* x, const float* gamma, const float*
  *   |x|), products are exact 32-bit integer sums, the block scales are applied
  *   in fp32.  Q4_K: K % 256 == 0, 256 <= K <= 16384.  Q6_K: K % 2048 == 0,
  *   2048 <= K <= 16384.
+ * dq_gemv_q2k: the same with Q2_K blocks (the min term uses the integer sums
+ *   of the fixed-point activation over each 16-element sub-block).
+ *   K % 1024 == 0, 1024 <= K <= 16384.
  * W, x 16-byte aligned (DQ_ERR_ALIGN otherwise).  y must not overlap W or x.
  * Errors: NULL -> DQ_ERR_NULL; rows < 1 or K outside the ranges -> DQ_ERR_SHAPE
  * or DQ_ERR_UNSUPPORTED. */
 DQ_API int dq_gemv_bf16(const void* W_bf16, const void* x_bf16, float* y, int rows, int K, void* stream);
 DQ_API int dq_gemv_q4k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream);
 DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream);
+DQ_API int dq_gemv_q2k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream);
 
 /* Diagnostics: when `buffer` is not NULL, every later GEMV launch in this
  * process writes 8 unsigned 64-bit values per thread block at
@@ -167,11 +181,12 @@ DQ_API int dq_debug_trace(void* buffer);
 
 /* Dequantise nblocks consecutive blocks to fp32 (256 values per block), each
  * weight computed as the block formula above in fp32.  A test hook: with the
- * synthetic binades (Q4_K d in [2^-13, 2^-12), dmin in [2^-10, 2^-9); Q6_K d in
- * [2^-14, 2^-13)) every weight is exact, so the output is bit-exact.
+ * synthetic binades (Q4_K and Q2_K d in [2^-13, 2^-12), dmin in [2^-10, 2^-9);
+ * Q6_K d in [2^-14, 2^-13)) every weight is exact, so the output is bit-exact.
  * blocks: any alignment; out: fp32 [nblocks * 256].  nblocks >= 1. */
 DQ_API int dq_dequant_q4k(const void* blocks, float* out, long long nblocks, void* stream);
 DQ_API int dq_dequant_q6k(const void* blocks, float* out, long long nblocks, void* stream);
+DQ_API int dq_dequant_q2k(const void* blocks, float* out, long long nblocks, void* stream);
 
 /* -------------------------------------------------------------- attention
  * Grouped-query decode attention for one token ("The roofline holds on a second

@@ -19,9 +19,11 @@ namespace dq {
 constexpr int FMT_BF16 = DQ_FMT_BF16;
 constexpr int FMT_Q4K = DQ_FMT_Q4K;
 constexpr int FMT_Q6K = DQ_FMT_Q6K;
+constexpr int FMT_Q2K = DQ_FMT_Q2K;
 
 constexpr int Q4K_BYTES = 144;
 constexpr int Q6K_BYTES = 210;
+constexpr int Q2K_BYTES = 84;
 
 // Device error codes written to the flag (bit mask).
 constexpr int DEVERR_TIMEOUT_FULL = 1;   // a consumer waited too long for a stage

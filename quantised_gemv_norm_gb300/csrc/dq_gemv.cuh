@@ -202,6 +202,34 @@ __device__ __forceinline__ float q6k_unit(const uint8_t* rp, int n, const XQ<1>&
     return (half_bits_to_float(dbits) * u.s) * static_cast<float>(v);
 }
 
+// Q2_K unit n of a row: sub-blocks 2(n & 7) and 2(n & 7) + 1 of block n >> 3
+// (32 weights).  Each sub-block's 16 codes are one 32-bit word: shifting it by
+// 2k and masking leaves weights 4k..4k+3 in the four bytes, in activation order.
+__device__ __forceinline__ float q2k_unit(const uint8_t* rp, int n, const XQ<1>& u)
+{
+    const uint8_t* bp = rp + Q2K_BYTES * (n >> 3);  // 4-byte aligned (84 = 4 * 21)
+    const int ja = 2 * (n & 7);
+    const uint32_t hd = lds32(bp);
+    const uint32_t scm = *reinterpret_cast<const uint16_t*>(bp + 4 + ja);  // sc|m of sub-blocks ja, ja + 1
+    const uint32_t wa = lds32(bp + 20 + 4 * ja), wb = lds32(bp + 24 + 4 * ja);
+    int da = 0, da2 = 0, db = 0, db2 = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t ca = (wa >> (2 * k)) & 0x03030303u;
+        const uint32_t cb = (wb >> (2 * k)) & 0x03030303u;
+        da = dp2a_lo(u.q[2 * k], ca, da);
+        da2 = dp2a_hi(u.q[2 * k + 1], ca, da2);
+        db = dp2a_lo(u.q[8 + 2 * k], cb, db);
+        db2 = dp2a_hi(u.q[8 + 2 * k + 1], cb, db2);
+    }
+    const int sca = static_cast<int>(scm & 15u), ma = static_cast<int>((scm >> 4) & 15u);
+    const int scb = static_cast<int>((scm >> 8) & 15u), mb = static_cast<int>(scm >> 12);
+    const int v = sca * (da + da2) + scb * (db + db2);  // |v| < 2 * 15 * 16 * 3 * 16383
+    const int mn32 = ma * u.s32a + mb * u.s32b;        // 32 * sum_j m_j * (sum of that half's xi)
+    const float d = half_bits_to_float(hd), dmin = half_bits_to_float(hd >> 16);
+    return (d * u.s) * static_cast<float>(v) - (dmin * u.s * (1.0f / 32.0f)) * static_cast<float>(mn32);
+}
+
 // bf16 unit n: 8 weights at byte 16n of the row; xb holds the 8 bf16 activations.
 __device__ __forceinline__ float bf16_unit(const uint8_t* rp, int n, const uint32_t (&xb)[4])
 {
@@ -410,6 +438,8 @@ __device__ __forceinline__ void consume_tile(const uint8_t* tile, int R, int RG,
                     sum += q4k_unit<PL>(rp, nidx[k], reinterpret_cast<const XQ<PL>&>(us[k]));
                 else if (FMT == FMT_Q6K)
                     sum += q6k_unit(rp, nidx[k], reinterpret_cast<const XQ<1>&>(us[k]));
+                else if (FMT == FMT_Q2K)
+                    sum += q2k_unit(rp, nidx[k], reinterpret_cast<const XQ<1>&>(us[k]));
                 else
                     sum += bf16_unit(rp, nidx[k], reinterpret_cast<const uint32_t(&)[4]>(us[k]));
             }

@@ -10,7 +10,7 @@ static int row_bytes_of(int fmt, int K)
 {
     if (fmt == DQ_FMT_BF16)
         return 2 * K;
-    return (K / 256) * (fmt == DQ_FMT_Q4K ? dq::Q4K_BYTES : dq::Q6K_BYTES);
+    return (K / 256) * (fmt == DQ_FMT_Q4K ? dq::Q4K_BYTES : fmt == DQ_FMT_Q2K ? dq::Q2K_BYTES : dq::Q6K_BYTES);
 }
 
 static GemvKernel kernel_for(int fmt, int ul, int rpt, int nmat, int pl)
@@ -19,6 +19,8 @@ static GemvKernel kernel_for(int fmt, int ul, int rpt, int nmat, int pl)
         return gemv_kernel_q4k(ul, rpt, nmat, pl);
     if (fmt == DQ_FMT_Q6K)
         return gemv_kernel_q6k(ul, rpt, nmat, pl);
+    if (fmt == DQ_FMT_Q2K)
+        return gemv_kernel_q2k(ul, rpt, nmat, pl);
     return gemv_kernel_bf16(ul, rpt, nmat, pl);
 }
 
@@ -58,6 +60,8 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool resid, GemvPl
         return DQ_ERR_SHAPE;
     if (fmt == DQ_FMT_Q6K && K % 2048)
         return DQ_ERR_ALIGN;  // 210-byte blocks: rows are 16-byte aligned only when K % 2048 == 0
+    if (fmt == DQ_FMT_Q2K && K % 1024)
+        return DQ_ERR_ALIGN;  // 84-byte blocks: rows are 16-byte aligned only when K % 1024 == 0
     if (fmt != DQ_FMT_BF16 && K > dq::GEMV_MAX_K)
         return DQ_ERR_UNSUPPORTED;
     const int U = K / unit_w;
@@ -222,6 +226,28 @@ __global__ void dequant_q4k_kernel(const uint8_t* __restrict__ blocks, float* __
     }
 }
 
+// One thread per 32 weights of Q2_K: w = d * sc_j * q - dmin * m_j in fp32.
+__global__ void dequant_q2k_kernel(const uint8_t* __restrict__ blocks, float* __restrict__ out, long long nunits)
+{
+    const long long u = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (u >= nunits)
+        return;
+    const uint8_t* b = blocks + (u >> 3) * Q2K_BYTES;
+    const int h = static_cast<int>(u & 7);
+    const float d = half_bits_to_float(ldb(b) | ldb(b + 1) << 8);
+    const float dmin = half_bits_to_float(ldb(b + 2) | ldb(b + 3) << 8);
+    float* o = out + u * 32;
+    for (int s = 0; s < 2; ++s) {
+        const int j = 2 * h + s;
+        const uint32_t sm = ldb(b + 4 + j);
+        const float ds = d * static_cast<float>(sm & 15u), dm = dmin * static_cast<float>(sm >> 4);
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t c = (ldb(b + 20 + 4 * j + (i & 3)) >> (2 * (i >> 2))) & 3u;
+            o[16 * s + i] = ds * static_cast<float>(c) - dm;
+        }
+    }
+}
+
 // One thread per 32 weights of Q6_K: w = d * sc[n/16] * (q - 32) in fp32.
 __global__ void dequant_q6k_kernel(const uint8_t* __restrict__ blocks, float* __restrict__ out, long long nunits)
 {
@@ -301,7 +327,14 @@ DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows,
     return gemv_entry(DQ_FMT_Q6K, W_blocks, x, y, rows, K, stream);
 }
 
-static int dequant_entry(bool q6, const void* blocks, float* out, long long nblocks, void* stream)
+DQ_API int dq_gemv_q2k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream)
+{
+    if (K > 16384)
+        return DQ_ERR_UNSUPPORTED;
+    return gemv_entry(DQ_FMT_Q2K, W_blocks, x, y, rows, K, stream);
+}
+
+static int dequant_entry(int fmt, const void* blocks, float* out, long long nblocks, void* stream)
 {
     if (!blocks || !out)
         return DQ_ERR_NULL;
@@ -313,8 +346,11 @@ static int dequant_entry(bool q6, const void* blocks, float* out, long long nblo
     if (grid > 0x7fffffffLL)
         return DQ_ERR_SHAPE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (q6)
+    if (fmt == DQ_FMT_Q6K)
         dq::dequant_q6k_kernel<<<static_cast<unsigned>(grid), threads, 0, s>>>(static_cast<const uint8_t*>(blocks), out,
+                                                                              nunits);
+    else if (fmt == DQ_FMT_Q2K)
+        dq::dequant_q2k_kernel<<<static_cast<unsigned>(grid), threads, 0, s>>>(static_cast<const uint8_t*>(blocks), out,
                                                                               nunits);
     else
         dq::dequant_q4k_kernel<<<static_cast<unsigned>(grid), threads, 0, s>>>(static_cast<const uint8_t*>(blocks), out,
@@ -325,12 +361,17 @@ static int dequant_entry(bool q6, const void* blocks, float* out, long long nblo
 
 DQ_API int dq_dequant_q4k(const void* blocks, float* out, long long nblocks, void* stream)
 {
-    return dequant_entry(false, blocks, out, nblocks, stream);
+    return dequant_entry(DQ_FMT_Q4K, blocks, out, nblocks, stream);
 }
 
 DQ_API int dq_dequant_q6k(const void* blocks, float* out, long long nblocks, void* stream)
 {
-    return dequant_entry(true, blocks, out, nblocks, stream);
+    return dequant_entry(DQ_FMT_Q6K, blocks, out, nblocks, stream);
+}
+
+DQ_API int dq_dequant_q2k(const void* blocks, float* out, long long nblocks, void* stream)
+{
+    return dequant_entry(DQ_FMT_Q2K, blocks, out, nblocks, stream);
 }
 
 }  // extern "C"

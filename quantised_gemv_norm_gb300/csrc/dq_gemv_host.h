@@ -12,6 +12,7 @@ using GemvKernel = void (*)(dq::GemvArgs);
 // Kernel tables, one translation unit per format (null when not instantiated).
 GemvKernel gemv_kernel_q4k(int ul, int rpt, int nmat, int pl);
 GemvKernel gemv_kernel_q6k(int ul, int rpt, int nmat, int pl);
+GemvKernel gemv_kernel_q2k(int ul, int rpt, int nmat, int pl);
 GemvKernel gemv_kernel_bf16(int ul, int rpt, int nmat, int pl);
 
 struct GemvPlan {

@@ -16,8 +16,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdq.so")
 
-FMT_BF16, FMT_Q4K, FMT_Q6K = 0, 1, 2
-Q4K_BLOCK_BYTES, Q6K_BLOCK_BYTES = 144, 210
+FMT_BF16, FMT_Q4K, FMT_Q6K, FMT_Q2K = 0, 1, 2, 3
+Q4K_BLOCK_BYTES, Q6K_BLOCK_BYTES, Q2K_BLOCK_BYTES = 144, 210, 84
 
 # name -> (restype, argtypes); the same names as include/dq.h
 P, I, LL, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float, ctypes.c_size_t
@@ -34,8 +34,10 @@ SIGNATURES = {
     "dq_gemv_bf16": (I, [P, P, P, I, I, P]),
     "dq_gemv_q4k": (I, [P, P, P, I, I, P]),
     "dq_gemv_q6k": (I, [P, P, P, I, I, P]),
+    "dq_gemv_q2k": (I, [P, P, P, I, I, P]),
     "dq_dequant_q4k": (I, [P, P, LL, P]),
     "dq_dequant_q6k": (I, [P, P, LL, P]),
+    "dq_dequant_q2k": (I, [P, P, LL, P]),
     "dq_attention_workspace_bytes": (SZ, [I, I]),
     "dq_attention_decode": (I, [P, P, P, P, I, I, I, I, I, P, SZ, P]),
     "dq_attention_decode_static": (I, [P, P, P, P, I, I, I, I, I, P]),
@@ -140,7 +142,7 @@ def layernorm(x, gamma, beta, eps: float, out=None, threads: int | None = None):
 
 
 def quant_K(fmt: int, row_bytes: int) -> int:
-    bpb = Q4K_BLOCK_BYTES if fmt == FMT_Q4K else Q6K_BLOCK_BYTES
+    bpb = {FMT_Q4K: Q4K_BLOCK_BYTES, FMT_Q6K: Q6K_BLOCK_BYTES, FMT_Q2K: Q2K_BLOCK_BYTES}[fmt]
     if row_bytes % bpb:
         raise ValueError("row bytes %d is not a whole number of blocks" % row_bytes)
     return row_bytes // bpb * 256
@@ -187,6 +189,23 @@ def dequant_q6k(blocks: torch.Tensor, out=None):
     n = blocks.numel() // Q6K_BLOCK_BYTES
     out = torch.empty(n * 256, dtype=torch.float32, device=blocks.device) if out is None else out
     _check("dq_dequant_q6k", lib.dq_dequant_q6k(_ptr(blocks), _ptr(out), n, _stream()))
+    return out
+
+
+def gemv_q2k(W: torch.Tensor, x: torch.Tensor, out=None):
+    lib = load()
+    rows = W.shape[0]
+    K = quant_K(FMT_Q2K, W.shape[1])
+    out = torch.empty(rows, dtype=torch.float32, device=W.device) if out is None else out
+    _check("dq_gemv_q2k", lib.dq_gemv_q2k(_ptr(W), _ptr(x), _ptr(out), rows, K, _stream()))
+    return out
+
+
+def dequant_q2k(blocks: torch.Tensor, out=None):
+    lib = load()
+    n = blocks.numel() // Q2K_BLOCK_BYTES
+    out = torch.empty(n * 256, dtype=torch.float32, device=blocks.device) if out is None else out
+    _check("dq_dequant_q2k", lib.dq_dequant_q2k(_ptr(blocks), _ptr(out), n, _stream()))
     return out
 
 

@@ -64,6 +64,9 @@ def test_argument_errors_return_before_launch(lib):
     assert lib.dq_rmsnorm_threads(fake, fake, fake, 1, 8, 1e-6, 3, None) == -2  # not a power of two
     assert lib.dq_layernorm(fake, fake, None, fake, 1, 8, 1e-6, None) == -1
     assert lib.dq_dequant_q4k(fake, fake, 0, None) == -2
+    assert lib.dq_dequant_q2k(fake, fake, 0, None) == -2
+    assert lib.dq_gemv_q2k(fake, fake, fake, 4, 1536, None) == -3         # 84-byte blocks: K % 1024
+    assert lib.dq_gemv_q2k(fake, fake, fake, 4, 17408, None) == -4
     assert lib.dq_attention_decode(fake, fake, fake, fake, 32, 8, 64, 16, 1, fake, 1 << 20, None) == -4
     assert lib.dq_attention_decode(fake, fake, fake, fake, 32, 8, 128, 16, 17, fake, 1 << 20, None) == -2
     assert lib.dq_attention_decode(fake, fake, fake, fake, 32, 8, 128, 16, 4, fake, 8, None) == -2

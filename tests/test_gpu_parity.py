@@ -93,6 +93,18 @@ def test_dequant_bit_exact(dq, orc):
     assert np.array_equal(y6.view(np.uint32), r6.view(np.uint32))
 
 
+def test_dequant_q2k_bit_exact_and_hand_built(dq, orc):
+    b2 = synth.q2k_blocks(np.random.default_rng(12), 3001)
+    y2 = dq.dequant_q2k(cuda(b2)).cpu().numpy()
+    r2 = orc.dequant_q2k(b2).astype(np.float32)
+    assert np.array_equal(y2.view(np.uint32), r2.view(np.uint32))
+    blk = orc.pack_q2k(0x3C00, 0x3800, [7] * 16, [15] * 16, [0] * 256)
+    assert np.all(dq.dequant_q2k(cuda(blk)).cpu().numpy() == -7.5)
+    q = [n % 4 for n in range(256)]
+    blk = orc.pack_q2k(0x3C00, 0x3800, list(range(16)), [15 - j for j in range(16)], q)
+    assert np.array_equal(dq.dequant_q2k(cuda(blk)).cpu().numpy().astype(np.float64), orc.dequant_q2k(blk))
+
+
 def test_dequant_hand_built(dq, orc):
     blk = orc.pack_q6k(0x0400, [-128] * 16, [63] * 256)
     assert np.all(dq.dequant_q6k(cuda(blk)).cpu().numpy() == -0.2421875)
@@ -140,10 +152,39 @@ def test_gemv_q6k(dq, orc, rows, K):
     assert normwise(y, r) <= GEMV_TOL
 
 
+Q2K_SHAPES = [(300, 4096), (1, 1024), (77, 3072), (12288, 4096), (4096, 12288), (151936, 4096), (5, 16384)]
+
+
+@pytest.mark.parametrize("rows,K", Q2K_SHAPES)
+def test_gemv_q2k(dq, orc, rows, K):
+    W = synth.quant_matrix(8, synth.FMT_Q2K, rows, K)
+    x = synth.activation(8, K)
+    y = dq.gemv_q2k(cuda(W), cuda(x)).cpu().numpy()
+    r = orc.gemv_q2k(W, x, rows, K)
+    assert normwise(y, r) <= GEMV_TOL
+
+
+def test_gemv_q2k_integer_weights_and_extreme_activation(dq, orc):
+    # d = dmin = 1: integer weights; a zero group, a tiny group and an outlier in x
+    rng = np.random.default_rng(14)
+    rows, K = 40, 2048
+    blocks = [orc.pack_q2k(0x3C00, 0x3C00, rng.integers(0, 16, 16), rng.integers(0, 16, 16), rng.integers(0, 4, 256))
+              for _ in range(rows * K // 256)]
+    W = np.concatenate(blocks).reshape(rows, -1)
+    x = synth.activation(14, K)
+    x[:32] = 0.0
+    x[32:64] *= 1e-6
+    x[100] = 1e4
+    y = dq.gemv_q2k(cuda(W), cuda(x)).cpu().numpy()
+    assert normwise(y, orc.gemv_q2k(W, x, rows, K)) <= GEMV_TOL
+    assert dq.device_error() == 0
+
+
 def test_gemv_quant_condition_aware(dq, orc):
     # error against sum_k |W_rk x_k|, per row (well inside the bar for 15-bit activations)
     rows, K = 513, 4096
-    for fmt, fn, deq in ((synth.FMT_Q4K, dq.gemv_q4k, orc.dequant_q4k), (synth.FMT_Q6K, dq.gemv_q6k, orc.dequant_q6k)):
+    for fmt, fn, deq in ((synth.FMT_Q4K, dq.gemv_q4k, orc.dequant_q4k), (synth.FMT_Q6K, dq.gemv_q6k, orc.dequant_q6k),
+                         (synth.FMT_Q2K, dq.gemv_q2k, orc.dequant_q2k)):
         W = synth.quant_matrix(7, fmt, rows, K)
         x = synth.activation(7, K)
         y = fn(cuda(W), cuda(x)).cpu().numpy().astype(np.float64)
