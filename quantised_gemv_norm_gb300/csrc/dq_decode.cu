@@ -411,13 +411,15 @@ DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits
         a.x_in = x_in;
         a.logits = logits;
         a.pos = pos;
+        a.fold = pos + 1 <= dq::TK_FOLD_KEYS ? 1 : 0;
         a.err = dqhost::device_error_flag();
         a.trace = dqhost::gemv_trace();
         cudaError_t e = dqhost::launch_token(m->tplan, a, s);
         if (e != cudaSuccess)
             return dqhost::set_cuda_error(e);
-        // every block arrives once at each of the nph - 1 barriers
-        m->bar_base += static_cast<unsigned>(m->tplan.nph - 1) * static_cast<unsigned>(m->tplan.grid);
+        // every block arrives once at each barrier: nph - 1, less one per layer when the attention is folded
+        const int nbar = m->tplan.nph - 1 - (a.fold ? m->n_layers : 0);
+        m->bar_base += static_cast<unsigned>(nbar) * static_cast<unsigned>(m->tplan.grid);
         return DQ_OK;
     }
     const int threads = 256;

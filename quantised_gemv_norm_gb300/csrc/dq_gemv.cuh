@@ -343,6 +343,59 @@ __device__ __forceinline__ void issue_tile(const uint8_t* W, const uint8_t* W2, 
                  &full[s], pol);
 }
 
+// Quantise one 4-element chunk c of the activation into the unit table xq: the
+// 8 lanes c & ~7 .. c | 7 of the calling warp hold one 32-element unit (and all
+// take part), four elements each.
+template <int FMT, int PL>
+__device__ __forceinline__ void quantise_chunk(float4 h, int c, uint32_t* xq)
+{
+    float amax = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float inv = amax > 0.f ? XQ_MAX / amax : 0.f;
+    const float t0 = h.x * inv, t1 = h.y * inv, t2 = h.z * inv, t3 = h.w * inv;
+    const int a0 = round_small(t0), a1 = round_small(t1), a2 = round_small(t2), a3 = round_small(t3);
+    const int e = c & 7;
+    uint32_t* q = xq + (c >> 3) * xq_words(PL);
+    *reinterpret_cast<uint2*>(q + 2 * e) = make_uint2(pack16x2(a0, a1), pack16x2(a2, a3));
+    int lsum = 0;
+    if (PL == 2) {  // remainders: t - a is exact in fp32
+        const int b0 = round_small((t0 - static_cast<float>(a0)) * 32768.0f);
+        const int b1 = round_small((t1 - static_cast<float>(a1)) * 32768.0f);
+        const int b2 = round_small((t2 - static_cast<float>(a2)) * 32768.0f);
+        const int b3 = round_small((t3 - static_cast<float>(a3)) * 32768.0f);
+        *reinterpret_cast<uint2*>(q + 16 + 2 * e) = make_uint2(pack16x2(b0, b1), pack16x2(b2, b3));
+        lsum = (b0 + b1) + (b2 + b3);
+    }
+    // Integer sums of the rounded values: per 16-element half (Q6_K's -32 offset,
+    // Q2_K's mins) and over the unit (Q4_K's min term).  Taking the min term from
+    // the same rounded values keeps the product exactly sum_k W_k x^_k, so the
+    // rounding error meets the full (zero-mean) weights, not only their positive part.
+    int isum = (a0 + a1) + (a2 + a3);
+    isum += __shfl_xor_sync(0xffffffffu, isum, 1);
+    isum += __shfl_xor_sync(0xffffffffu, isum, 2);
+    const int ihalf = isum;  // this 16-element half
+    isum += __shfl_xor_sync(0xffffffffu, isum, 4);
+    if (PL == 2) {
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1)
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    }
+    float* meta = reinterpret_cast<float*>(q + 16 * PL);
+    if (e == 0 || e == 4) {
+        const float sc = amax / XQ_MAX;
+        if (e == 0) {
+            meta[0] = sc;
+            meta[1] = sc * 0.0625f;
+            meta[2] = sc * (static_cast<float>(isum) + static_cast<float>(lsum) * (1.0f / 32768.0f));
+            reinterpret_cast<int*>(meta)[3] = 32 * ihalf;
+        } else {
+            reinterpret_cast<int*>(meta)[4] = 32 * ihalf;
+        }
+    }
+}
+
 // Quantise the activation (times gamma under RMSNorm) once per block of NT
 // threads: eight lanes share one 32-element unit, four elements each; chunk
 // c = tid + NT i of the vector is v[i].  Returns this thread's partial sum of x^2.
@@ -362,51 +415,7 @@ __device__ __forceinline__ float quantise_block(float4 (&v)[NCH], const float4 (
             ss = fmaf(h.x, h.x, ss); ss = fmaf(h.y, h.y, ss); ss = fmaf(h.z, h.z, ss); ss = fmaf(h.w, h.w, ss);
             h.x *= gv[i].x; h.y *= gv[i].y; h.z *= gv[i].z; h.w *= gv[i].w;
         }
-        float amax = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float inv = amax > 0.f ? XQ_MAX / amax : 0.f;
-        const float t0 = h.x * inv, t1 = h.y * inv, t2 = h.z * inv, t3 = h.w * inv;
-        const int a0 = round_small(t0), a1 = round_small(t1), a2 = round_small(t2), a3 = round_small(t3);
-        const int e = c & 7;
-        uint32_t* q = xq + (c >> 3) * xq_words(PL);
-        *reinterpret_cast<uint2*>(q + 2 * e) = make_uint2(pack16x2(a0, a1), pack16x2(a2, a3));
-        int lsum = 0;
-        if (PL == 2) {  // remainders: t - a is exact in fp32
-            const int b0 = round_small((t0 - static_cast<float>(a0)) * 32768.0f);
-            const int b1 = round_small((t1 - static_cast<float>(a1)) * 32768.0f);
-            const int b2 = round_small((t2 - static_cast<float>(a2)) * 32768.0f);
-            const int b3 = round_small((t3 - static_cast<float>(a3)) * 32768.0f);
-            *reinterpret_cast<uint2*>(q + 16 + 2 * e) = make_uint2(pack16x2(b0, b1), pack16x2(b2, b3));
-            lsum = (b0 + b1) + (b2 + b3);
-        }
-        // Integer sums of the rounded values: per 16-element half (Q6_K's -32 offset)
-        // and over the unit (Q4_K's min term).  Taking the min term from the same
-        // rounded values keeps the product exactly sum_k W_k x^_k, so the rounding
-        // error meets the full (zero-mean) weights, not only their positive part.
-        int isum = (a0 + a1) + (a2 + a3);
-        isum += __shfl_xor_sync(0xffffffffu, isum, 1);
-        isum += __shfl_xor_sync(0xffffffffu, isum, 2);
-        const int ihalf = isum;  // this 16-element half
-        isum += __shfl_xor_sync(0xffffffffu, isum, 4);
-        if (PL == 2) {
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1)
-                lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-        }
-        float* meta = reinterpret_cast<float*>(q + 16 * PL);
-        if (e == 0 || e == 4) {
-            const float sc = amax / XQ_MAX;
-            if (e == 0) {
-                meta[0] = sc;
-                meta[1] = sc * 0.0625f;
-                meta[2] = sc * (static_cast<float>(isum) + static_cast<float>(lsum) * (1.0f / 32768.0f));
-                reinterpret_cast<int*>(meta)[3] = 32 * ihalf;
-            } else {
-                reinterpret_cast<int*>(meta)[4] = 32 * ihalf;
-            }
-        }
+        quantise_chunk<FMT, PL>(h, c, xq);
     }
     return ss;
 }
@@ -566,9 +575,6 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         *step_logits = a.y_from_step ? a.step->logits : a.y;
         *step_pos = a.epi == EPI_QKV ? a.step->pos : 0;
     }
-    if (a.epi == EPI_RESID)
-        for (int r = tid; r < r1 - r0; r += NCONS)
-            resid[r] = __ldcg(a.y + r0 + r);
 
     const int P = a.P;
     const int g = tid / P;
@@ -594,6 +600,9 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             uint32_t* xb = reinterpret_cast<uint32_t*>(&us[k]);
             xb[0] = v.x; xb[1] = v.y; xb[2] = v.z; xb[3] = v.w;
         }
+        if (a.epi == EPI_RESID)
+            for (int r = tid; r < r1 - r0; r += NCONS)
+                resid[r] = __ldcg(a.y + r0 + r);
         __syncthreads();  // step fields and residual rows
     } else {
 #pragma unroll
@@ -602,6 +611,10 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
             if (c < a.K / 4)
                 xv[i] = __ldcg(reinterpret_cast<const float4*>(a.x) + c);
         }
+        // the residual rows after the activation's loads are out: the round trips overlap
+        if (a.epi == EPI_RESID)
+            for (int r = tid; r < r1 - r0; r += NCONS)
+                resid[r] = __ldcg(a.y + r0 + r);
         if (trace && tid == 0)
             trace[3] = globaltimer_ns();
         float ss = quantise_block<FMT, PL, QCHUNKS>(xv, gv, norm, xq, a.K, tid);

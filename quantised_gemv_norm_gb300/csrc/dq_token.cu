@@ -107,7 +107,9 @@ __device__ __forceinline__ bool tk_sync(int p)
     TkMisc& m = tk_misc();
     __syncthreads();  // the block's phase outputs are written
     if (threadIdx.x == 0) {
-        const unsigned target = A.bar_base + static_cast<unsigned>(p) * gridDim.x;
+        // barriers passed before this one: one per phase, minus the folded attention phases
+        const int nb = A.fold ? p - (p + 3) / 5 : p;
+        const unsigned target = A.bar_base + static_cast<unsigned>(nb) * gridDim.x;
         int ok = *reinterpret_cast<volatile int*>(&m.dead) == 0;
         tk_trace(p, 6);
         red_release_add(A.bar, 1u);  // release, cumulative over the block's writes through bar.sync
@@ -137,6 +139,103 @@ __device__ __forceinline__ void tk_trace(int p, int i)
     if (A.trace && threadIdx.x == 0)
         A.trace[(static_cast<size_t>(blockIdx.x) * (5 * A.n_layers + 1) + p) * 8 + i] =
             (i & 1) ? clock64() : globaltimer_ns();
+}
+
+// Attention for a short context (n_keys <= TK_FOLD_KEYS), computed by every
+// block at the start of the O phase of layer l and quantised straight into the
+// O projection's activation table: no attention phase and no barrier of its
+// own.  Warp w takes query heads w and w + 16 together (n_q <= 32), every load
+// of both issued before any arithmetic, so the fold costs one L2 round trip;
+// lane i holds dims 4i..4i+3.  With the Qwen3 inputs each block normalises and
+// rotates q and the new key itself, and block 0 writes the key's fp16 row into
+// the cache (the other blocks use the same rounded values from registers).
+// Same arithmetic as attn_block.
+template <int PL>
+__device__ __forceinline__ void tk_fold_attention(int l)
+{
+    const TokenArgs& A = tk_args();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pos = A.pos, n_keys = pos + 1, group = A.n_q / A.n_kv;
+    const size_t plane = static_cast<size_t>(A.n_kv) * A.max_ctx * A.hd;
+    __half* kc = A.kv + static_cast<size_t>(l) * 2 * plane;
+    const __half* vc = kc + plane;
+    const bool qwen = A.k_new != nullptr;
+    constexpr int NH = 2;  // heads per warp
+    bool on[NH];
+    int hh[NH], gg[NH];
+    float4 q[NH], k[NH];
+    uint2 kr[NH][TK_FOLD_KEYS], vr[NH][TK_FOLD_KEYS];
+#pragma unroll
+    for (int i = 0; i < NH; ++i) {
+        hh[i] = warp + TK_WARPS * i;
+        on[i] = hh[i] < A.n_q;
+        gg[i] = on[i] ? hh[i] / group : 0;
+        const size_t row0 = static_cast<size_t>(gg[i]) * A.max_ctx * ATT_HD;
+        q[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        k[i] = q[i];
+        if (on[i]) {
+            q[i] = __ldcg(reinterpret_cast<const float4*>(A.q + static_cast<size_t>(hh[i]) * ATT_HD) + lane);
+            if (qwen)
+                k[i] = __ldcg(reinterpret_cast<const float4*>(A.k_new + static_cast<size_t>(gg[i]) * ATT_HD) + lane);
+        }
+#pragma unroll
+        for (int j = 0; j < TK_FOLD_KEYS; ++j) {
+            kr[i][j] = vr[i][j] = make_uint2(0u, 0u);
+            if (on[i] && j < n_keys) {
+                kr[i][j] = __ldcg(reinterpret_cast<const uint2*>(kc + row0 + static_cast<size_t>(j) * ATT_HD) + lane);
+                vr[i][j] = __ldcg(reinterpret_cast<const uint2*>(vc + row0 + static_cast<size_t>(j) * ATT_HD) + lane);
+            }
+        }
+    }
+    const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
+#pragma unroll
+    for (int i = 0; i < NH; ++i) {
+        if (!on[i])  // warp-uniform
+            continue;
+        uint2 knew = make_uint2(0u, 0u);
+        float4 qi = q[i];
+        if (qwen) {
+            const float2* cs = A.rope + static_cast<size_t>(pos) * (ATT_HD / 2);
+            qi = head_norm_rope(qi, A.layers[l].q_norm, cs, A.eps, lane);
+            const float4 kk = head_norm_rope(k[i], A.layers[l].k_norm, cs, A.eps, lane);
+            const __half2 k01 = __floats2half2_rn(kk.x, kk.y), k23 = __floats2half2_rn(kk.z, kk.w);
+            knew.x = *reinterpret_cast<const uint32_t*>(&k01);
+            knew.y = *reinterpret_cast<const uint32_t*>(&k23);
+            if (blockIdx.x == 0 && hh[i] % group == 0)
+                *reinterpret_cast<uint2*>(kc + static_cast<size_t>(gg[i]) * A.max_ctx * ATT_HD +
+                                          static_cast<size_t>(pos) * ATT_HD + 4 * lane) = knew;
+        }
+        float sj[TK_FOLD_KEYS];
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < TK_FOLD_KEYS; ++j) {
+            sj[j] = -INFINITY;
+            if (j < n_keys) {
+                const uint2 kb = (qwen && j == pos) ? knew : kr[i][j];
+                const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(&kb.x));
+                const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(&kb.y));
+                float d = fmaf(qi.x, k0.x, qi.y * k0.y) + fmaf(qi.z, k1.x, qi.w * k1.y);
+                d = warp_sum(d) * scale;
+                sj[j] = d;
+                m = fmaxf(m, d);
+            }
+        }
+        float lsum = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < TK_FOLD_KEYS; ++j)
+            if (j < n_keys) {
+                const float pj = expf(sj[j] - m);
+                lsum += pj;
+                const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&vr[i][j].x));
+                const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&vr[i][j].y));
+                o.x = fmaf(pj, v0.x, o.x); o.y = fmaf(pj, v0.y, o.y);
+                o.z = fmaf(pj, v1.x, o.z); o.w = fmaf(pj, v1.y, o.w);
+            }
+        const float inv = 1.0f / lsum;
+        o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+        quantise_chunk<FMT_Q4K, PL>(o, hh[i] * (ATT_HD / 4) + lane, tk_xq());
+    }
 }
 
 // One matrix phase p of kind KIND: prefetch the norm weight, pass the barrier,
@@ -180,20 +279,27 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
     tk_trace(p, 2);
     tk_trace(p, 3);
 
-    float4 xv[NCH];
+    // the block's residual rows (at most TK_RESID_MAX < TK_THREADS): loaded now, stored
+    // after the activation's loads have gone out, so the two round trips overlap
+    float rv = 0.f;
+    if (EPI == EPI_RESID && tid < r1 - r0)
+        rv = __ldcg((KIND == PH_O ? x0 : A.x) + r0 + tid);
+    float ss = 0.f;
+    if (KIND == PH_O && A.fold) {
+        tk_fold_attention<PL>(l);
+    } else {
+        float4 xv[NCH];
 #pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-        const int ch = tid + TK_THREADS * i;
-        xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (ch < K / 4)
-            xv[i] = __ldcg(reinterpret_cast<const float4*>(x) + ch);
+        for (int i = 0; i < NCH; ++i) {
+            const int ch = tid + TK_THREADS * i;
+            xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ch < K / 4)
+                xv[i] = __ldcg(reinterpret_cast<const float4*>(x) + ch);
+        }
+        ss = quantise_block<FMT, PL, NCH, TK_THREADS>(xv, gv, NORM, tk_xq(), K, tid);
     }
-    if (EPI == EPI_RESID) {
-        const float* rsrc = KIND == PH_O ? x0 : A.x;
-        for (int r = tid; r < r1 - r0; r += TK_THREADS)
-            tk_resid()[r] = __ldcg(rsrc + r0 + r);
-    }
-    float ss = quantise_block<FMT, PL, NCH, TK_THREADS>(xv, gv, NORM, tk_xq(), K, tid);
+    if (EPI == EPI_RESID && tid < r1 - r0)
+        tk_resid()[tid] = rv;
     if (NORM) {
         ss = warp_sum(ss);
         if (lane == 0)
@@ -466,7 +572,8 @@ __global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_const
     for (int l = 0; l < a.n_layers; ++l) {
         const int p = 5 * l;
         st = tk_gemv<PH_QKV, FMT_Q4K, 2, 1, EPI_QKV, true>(p, st.x, st.y);
-        tk_attention(p + 1);
+        if (!a.fold)
+            tk_attention(p + 1);
         st = tk_gemv<PH_O, FMT_Q4K, 2, 1, EPI_RESID, false>(p + 2, st.x, st.y);
         st = tk_gemv<PH_GATEUP, FMT_Q4K, 1, 2, EPI_SWIGLU, true>(p + 3, st.x, st.y);
         if (ptab[p + 4].kind == PH_DOWN_Q6)

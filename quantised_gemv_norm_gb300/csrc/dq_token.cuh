@@ -9,6 +9,9 @@ constexpr int TK_THREADS = 512;    // 16 warps, 128 registers a thread
 constexpr int TK_WARPS = TK_THREADS / 32;
 constexpr int TK_NSTAGE = 4;       // weight ring slots per block
 constexpr int TK_SLOT = 40960;     // bytes per slot (largest tile: 4 Q6_K rows of K = 12288)
+// Contexts of at most this many keys skip the attention phase and its barrier:
+// every block computes all query heads at the start of the O phase.
+constexpr int TK_FOLD_KEYS = 4;
 constexpr int TK_RED_STRIDE = 4;   // floats per warp in one partial-sum slot
 
 // Phase kinds.  Per layer: QKV, ATTN, O, GATEUP, DOWN (Q4_K or Q6_K); then VOCAB.
@@ -49,6 +52,7 @@ struct TokenArgs {
     float* act;                // [ffn]
     float* part;               // attention partials
     int* counters;             // attention merge counters (zero between phases)
+    int fold;                  // 1: pos + 1 <= TK_FOLD_KEYS, the attention is folded into the O phase
     float* k_new;              // Qwen3 attention inputs: the token's keys as projected [n_kv hd], else null
     const float2* rope;        // (cos, sin) table [max_ctx][hd / 2] when k_new is set
     StepArgs* step;            // pos and logits recorded for the diagnostics entry points

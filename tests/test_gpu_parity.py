@@ -407,6 +407,19 @@ def test_decode_small_model_qwen3_attention(dq, orc, mode):
     _run_decode(dq, orc, m, kv, [0, 1, 2, 63, 64, 1100], emulate=True, flags=flags, fused=fused)
 
 
+@pytest.mark.parametrize("qwen3", [False, True])
+@pytest.mark.parametrize("mode", ["fused", "kernels"])
+def test_decode_short_context_fold_boundary(dq, orc, mode, qwen3):
+    # the fused kernel folds the attention into the O phase up to 4 keys (pos 3) and
+    # runs the attention phase from 5 keys on; both sides of the boundary, and the
+    # cache rows written by the fold (block 0) are read back by the next steps
+    m = synth.make_model(28, n_layers=2, hidden=2048, ffn=4096, n_q_heads=16, n_kv_heads=4, head_dim=128,
+                         vocab=400, max_ctx=32, qwen3_attention=qwen3)
+    kv = synth.make_kv_cache(28, m, 1)
+    flags, fused = MODES[mode]
+    _run_decode(dq, orc, m, kv, [1, 2, 3, 4, 5], emulate=True, flags=flags, fused=fused)
+
+
 def test_decode_qwen3_attention_modes_agree(dq, orc):
     # the fused kernel and the separate kernels compute the same norm, rotation and cache row
     m = synth.make_model(27, n_layers=2, hidden=2048, ffn=4096, n_q_heads=8, n_kv_heads=2, head_dim=128,
