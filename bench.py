@@ -1,11 +1,12 @@
 #!/usr/bin/env python3
 """Decode tokens/s of the Qwen3-8B-shaped Q4_K/Q6_K stack at M = 1 on GB300.
 
-Default arm (ours): one decode token per step through libdq (CUDA graph of
-182 kernels) on synthetic random-init weights (4.65 GB, larger than L2, read
-once per step).  Prints one JSON line with the metric, the roofline of the
-dominant kernel, the end-to-end number through the C ABI with host buffers,
-clock samples and the CPU-oracle baseline.
+Default arm (ours): one decode token per step through libdq (the persistent
+token kernel: one cooperative launch per token) on synthetic random-init
+weights (4.65 GB, larger than L2, read once per step).  Prints one JSON line
+with the metric, the roofline of the timed kernel, the end-to-end number
+through the C ABI with host buffers, clock samples and the CPU-oracle
+baseline; the separate-kernel CUDA graph (182 kernels) is timed beside it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -202,7 +203,11 @@ def run_ours(args):
     m = synth.make_model(SEED, max_ctx=MAX_CTX, qwen3_attention=True, **synth.QWEN3_8B)
     kv = synth.make_kv_cache(SEED, m, 0)
     w = upload.to_device(m, kv, device)
-    model = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=True)
+    # The token as one persistent cooperative kernel (the library's fastest mode where
+    # the shape allows); the separate-kernel CUDA graph is timed beside it.
+    model = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=True,
+                     flags=0 if args.no_fused else dq.MODEL_FUSED)
+    mode = "fused token kernel" if model.fused else "CUDA graph of separate kernels"
     setup_s = time.time() - t0
     stream = torch.cuda.current_stream(device)
     sh = stream.cuda_stream
@@ -211,22 +216,24 @@ def run_ours(args):
     xs = torch.stack([torch.from_numpy(synth.decode_input(SEED, m.hidden, t)) for t in range(K + W)]).to(device)
     logits = torch.empty(m.vocab, dtype=torch.float32, device=device)
 
-    # ---- device-timed decode: inputs resident in HBM, pos 0 (empty cache) each step
-    for t in range(W):
-        model.step_raw(xs[t].data_ptr(), 0, logits.data_ptr(), sh)
-    torch.cuda.synchronize(device)
-    barrier(world, device)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+    def timed_steps(mdl, pos):
+        for t in range(W):
+            mdl.step_raw(xs[t].data_ptr(), pos, logits.data_ptr(), sh)
         torch.cuda.synchronize(device)
-        ev0.record(stream)
+        barrier(world, device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        a.record(stream)
         for t in range(K):
-            model.step_raw(xs[W + t].data_ptr(), 0, logits.data_ptr(), sh)
-        ev1.record(stream)
+            mdl.step_raw(xs[W + t].data_ptr(), pos, logits.data_ptr(), sh)
+        b.record(stream)
         torch.cuda.synchronize(device)
-    barrier(world, device)
-    local_s = ev0.elapsed_time(ev1) / 1e3
-    max_s = aggregate_max(local_s, world, device)
+        barrier(world, device)
+        return aggregate_max(a.elapsed_time(b) / 1e3, world, device)
+
+    # ---- device-timed decode: inputs resident in HBM, pos 0 (empty cache) each step
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        max_s = timed_steps(model, 0)
     err = dq.device_error()
     tok_s = K * world / max_s
 
@@ -253,24 +260,43 @@ def run_ours(args):
     barrier(world, device)
     e2e_max = aggregate_max(e2e_local, world, device)
 
-    # ---- per-kernel timing (each kind across all 36 layers, CUDA events on this stream).
-    # The launches are queued behind a short device-side sleep before the first event, so
-    # the events time the GPU running them back to back, not the host issuing them; they
-    # are chained with programmatic dependent launch as in the token, so each launch's
-    # start-up overlaps the previous one's end as it does in the token.
+    # ---- roofline of the timed kernel: the whole token's algorithmic bytes per launch over
+    # its launch time (CUDA events on the launching stream, the timed region above)
+    tb = token_bytes(0)
+    peak, peak_src = hbm_peak_gbs()
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            traffic = json.load(open(prof)).get("token_kernel" if model.fused else "gate_up", {}).get(
+                "dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+    if model.fused:
+        rl_kernel, achieved = "token_kernel", round(tb * K / max_s / 1e9, 1)
+    else:
+        rl_kernel, achieved = None, None
+
+    # ---- the separate-kernel path: the CUDA graph of 182 PDL-chained kernels, and each
+    # kernel kind alone (each kind across all 36 layers, CUDA events on this stream).
+    # The per-kind launches are queued behind a short device-side sleep before the first
+    # event, so the events time the GPU running them back to back, not the host issuing
+    # them; they are chained with programmatic dependent launch as in the token.
+    gmodel = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=True)
+    gs = timed_steps(gmodel, 0)
     per_kernel = {}
     for kind_i, kind in enumerate(KERNEL_KINDS):
         layers = [0] if kind == "vocab" else list(range(m.n_layers))
         reps = 3 if kind == "vocab" else 1
         for l in layers[:2]:
-            model.enqueue_kernel(l, kind_i, sh)
+            gmodel.enqueue_kernel(l, kind_i, sh)
         torch.cuda.synchronize(device)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda._sleep(20_000_000)  # about 10 ms at 2 GHz: longer than queuing the launches takes
         a.record(stream)
         for _ in range(reps):
             for l in layers:
-                model.enqueue_kernel(l, kind_i, sh)
+                gmodel.enqueue_kernel(l, kind_i, sh)
         b.record(stream)
         torch.cuda.synchronize(device)
         n = reps * len(layers)
@@ -278,19 +304,14 @@ def run_ours(args):
         byts = sum(kernel_bytes(kind, l, 0) for l in layers) / len(layers)
         per_kernel[kind] = {"us_per_launch": round(us, 3), "bytes_per_launch": int(byts),
                             "GBps": round(byts / us / 1e3, 1), "launches_per_token": len(layers)}
-    # dominant kernel: the largest share of a token's summed kernel time
     share = {k: v["us_per_launch"] * v["launches_per_token"] for k, v in per_kernel.items()}
     dom = max(share, key=share.get)
-    peak, peak_src = hbm_peak_gbs()
-    dk = per_kernel[dom]
-    achieved = dk["GBps"]
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        try:
-            traffic = json.load(open(prof)).get(dom, {}).get("dram_bytes_per_launch")
-        except Exception:
-            traffic = None
+    separate = {"tokens_per_s": round(K * world / gs, 2), "ms_per_step": round(gs / K * 1e3, 4),
+                "launches_per_step": gmodel.launches_per_step, "per_kernel": per_kernel,
+                "dominant_kernel": dom, "dominant_frac": round(per_kernel[dom]["GBps"] / peak, 4)}
+    gmodel.close()
+    if rl_kernel is None:  # the separate kernels are what ran: the dominant one
+        rl_kernel, achieved = dom, per_kernel[dom]["GBps"]
 
     # ---- 512-token context (cache filled with N(0,1) fp16, pos 512)
     ctx = {}
@@ -298,44 +319,15 @@ def run_ours(args):
         kv512 = synth.make_kv_cache(SEED + 1, m, 512)
         w["kv_cache"].copy_(torch.from_numpy(kv512.view(np.int16)).to(device))
         del kv512
-        for t in range(W):
-            model.step_raw(xs[t].data_ptr(), 512, logits.data_ptr(), sh)
-        torch.cuda.synchronize(device)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for t in range(K):
-            model.step_raw(xs[W + t].data_ptr(), 512, logits.data_ptr(), sh)
-        b.record(stream)
-        torch.cuda.synchronize(device)
-        s512 = aggregate_max(a.elapsed_time(b) / 1e3, world, device)
+        s512 = timed_steps(model, 512)
         tb512 = token_bytes(512)
         ctx = {"tokens_per_s": round(K * world / s512, 2), "bytes_per_token": tb512,
                "GBps": round(tb512 * K / s512 / 1e9, 1)}
-
-    # ---- the same token as one persistent kernel (opt-in mode), for comparison
-    fused = {}
-    if not args.no_fused:
-        fmodel = dq.Model(**upload.model_kwargs(m), weights=w, use_graph=True, flags=dq.MODEL_FUSED)
-        if fmodel.fused:
-            for t in range(W):
-                fmodel.step_raw(xs[t].data_ptr(), 0, logits.data_ptr(), sh)
-            torch.cuda.synchronize(device)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for t in range(K):
-                fmodel.step_raw(xs[W + t].data_ptr(), 0, logits.data_ptr(), sh)
-            b.record(stream)
-            torch.cuda.synchronize(device)
-            fs = aggregate_max(a.elapsed_time(b) / 1e3, world, device)
-            fused = {"tokens_per_s": round(K * world / fs, 2), "ms_per_step": round(fs / K * 1e3, 4),
-                     "launches_per_step": fmodel.launches_per_step}
-        fmodel.close()
 
     # ---- M-token sweep of one Q4_K matrix (tensor cores vs one GEMV per token)
     msweep = run_msweep(device) if not args.no_msweep else {}
     lowbit = run_lowbit(device) if not args.no_msweep else {}
 
-    tb = token_bytes(0)
     out = {
         "metric": METRIC,
         "value": round(tok_s, 2),
@@ -349,17 +341,16 @@ def run_ours(args):
         "vs_baseline": round(tok_s / PAGES_BASELINE_TOK_S, 3),
         "dtype": "f32",
         "data": "synthetic (seeded random-init Q4_K/Q6_K weights, N(0,1) hidden inputs)",
-        "config": {"workload": WORKLOAD, "bytes_per_token": tb, "ctx": 0,
+        "config": {"workload": WORKLOAD, "bytes_per_token": tb, "ctx": 0, "mode": mode,
                    "l2": "inputs larger than L2: 4.65 GB of weights read per step, no flush needed",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm": {"achieved_GBps_token": round(tb * tok_s / world / 1e9, 1), "peak_GBps": peak,
                 "frac_of_peak": round(tb * tok_s / world / 1e9 / peak, 4), "peak_source": peak_src,
                 "roofline_tokens_per_s": round(peak * 1e9 / tb, 1)},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "roofline": {"bound": "hbm", "kernel": rl_kernel, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src},
-        "per_kernel": per_kernel,
+        "separate_kernels": separate,
         "ctx512": ctx,
-        "fused_token_kernel": fused,
         "msweep": msweep,
         "lowbit_gemv": lowbit,
         "e2e": {"value": round(K * world / e2e_max, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * m.hidden,
@@ -495,6 +486,36 @@ def run_kernel_probe(args):
         sys.exit(1)
 
 
+def run_token_probe(args):
+    """`probe_reps` decode tokens of a 2-layer full-width stack (the Qwen3-8B layer
+    shapes and vocabulary, 740 MB of weights) through the fused token kernel: a
+    small case of the headline kernel for profilers."""
+    import torch
+
+    from quantised_gemv_norm_gb300 import build, dq, upload
+
+    build.build()
+    dq.load()
+    S = synth.QWEN3_8B
+    m = synth.make_model(SEED, n_layers=2, hidden=S["hidden"], ffn=S["ffn"], n_q_heads=S["n_q_heads"],
+                         n_kv_heads=S["n_kv_heads"], head_dim=S["head_dim"], vocab=S["vocab"], max_ctx=MAX_CTX,
+                         qwen3_attention=True)
+    w = upload.to_device(m, synth.make_kv_cache(SEED, m, 0))
+    model = dq.Model(**upload.model_kwargs(m), weights=w, flags=dq.MODEL_FUSED)
+    x = torch.from_numpy(synth.decode_input(SEED, m.hidden)).cuda()
+    for _ in range(args.probe_reps):
+        logits = model.step(x, 0)
+    torch.cuda.synchronize()
+    err = dq.device_error()
+    fused = model.fused
+    model.close()
+    print(json.dumps({"token_probe": "2 layers", "fused": fused, "reps": args.probe_reps,
+                      "weight_bytes": int(m.weight_bytes()), "device_error_flag": err,
+                      "logits_finite": bool(torch.isfinite(logits).all().item())}))
+    if err or not fused:
+        sys.exit(1)
+
+
 # -------------------------------------------------------------- the oracle
 
 
@@ -559,14 +580,20 @@ def main():
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--no-ctx512", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-fused", action="store_true", help="skip the fused-token-kernel comparison")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="time the separate-kernel CUDA graph as the headline instead of the fused token kernel")
     ap.add_argument("--no-msweep", action="store_true", help="skip the M-token sweep")
     ap.add_argument("--msweep-only", action="store_true", help="print only the M-token sweep")
     ap.add_argument("--kernel-probe", choices=KERNEL_KINDS, default=None,
                     help="profiling aid: build a 2-layer full-width stack, run one token, then launch this "
                          "kernel kind alone --probe-reps times (for ncu -k ... -s 9 -c 1)")
     ap.add_argument("--probe-reps", type=int, default=3)
+    ap.add_argument("--token-probe", action="store_true",
+                    help="run a few fused tokens of a 2-layer full-width stack (for profilers) and exit")
     args = ap.parse_args()
+    if args.token_probe:
+        run_token_probe(args)
+        return
     if args.kernel_probe:
         run_kernel_probe(args)
         return
