@@ -349,7 +349,11 @@ typedef struct {
  * far as the block's shared memory allows), it is
  * one cooperative launch of one block per SM that runs all phases with grid
  * barriers between them while the weights stream through each block's ring
- * without a break.  Host call;
+ * without a break; for contexts of at most 4 keys (pos <= 3) it skips the
+ * attention phase and every block computes the attention at the start of
+ * the O phase (the model buffer of the attention output, dq_model_buffer 2,
+ * is then not written).  With the Qwen3 inputs the workspace also holds the
+ * rotary table (max_ctx x 512 bytes), computed here.  Host call;
  * synchronises the device.  *out receives the handle (NULL on error).
  * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE, DQ_ERR_ALIGN, DQ_ERR_UNSUPPORTED,
  * DQ_ERR_ALLOC, DQ_ERR_CUDA. */
