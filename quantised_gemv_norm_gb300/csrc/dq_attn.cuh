@@ -47,12 +47,27 @@ struct AttnSmem {
 // decode census of "The roofline holds on a second GPU" names the model, not
 // these transforms): one weight vector for all query heads, one for all key
 // heads, rotary base 1e6.
-__device__ __forceinline__ float4 head_norm_rope(float4 v, const float* __restrict__ w,
-                                                 const float2* __restrict__ cs, float eps, int lane)
+// The per-lane operands of head_norm_rope, loaded together ahead of use: the
+// weight's 4 dims and the (cos, sin) of the lane's 4 rotation pairs.
+struct NormRope {
+    float4 w, c01, c23;
+};
+
+__device__ __forceinline__ NormRope load_norm_rope(const float* __restrict__ w, const float2* __restrict__ cs, int lane)
+{
+    const int i0 = (4 * lane) & (ATT_HD / 2 - 1);
+    NormRope r;
+    r.w = __ldg(reinterpret_cast<const float4*>(w) + lane);
+    r.c01 = __ldg(reinterpret_cast<const float4*>(cs + i0));
+    r.c23 = __ldg(reinterpret_cast<const float4*>(cs + i0 + 2));
+    return r;
+}
+
+__device__ __forceinline__ float4 head_norm_rope(float4 v, const NormRope& nr, float eps, int lane)
 {
     const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
     const float r = rsqrtf(ss * (1.0f / ATT_HD) + eps);
-    const float4 g = __ldg(reinterpret_cast<const float4*>(w) + lane);
+    const float4 g = nr.w;
     v = make_float4(v.x * r * g.x, v.y * r * g.y, v.z * r * g.z, v.w * r * g.w);
     // the partner dims (i + 64 for the first half, i - 64 for the second) sit 16 lanes away
     float4 o;
@@ -60,9 +75,7 @@ __device__ __forceinline__ float4 head_norm_rope(float4 v, const float* __restri
     o.y = __shfl_xor_sync(0xffffffffu, v.y, 16);
     o.z = __shfl_xor_sync(0xffffffffu, v.z, 16);
     o.w = __shfl_xor_sync(0xffffffffu, v.w, 16);
-    const int i0 = (4 * lane) & (ATT_HD / 2 - 1);
-    const float4 c01 = __ldg(reinterpret_cast<const float4*>(cs + i0));
-    const float4 c23 = __ldg(reinterpret_cast<const float4*>(cs + i0 + 2));
+    const float4 c01 = nr.c01, c23 = nr.c23;
     const float sg = lane < 16 ? -1.0f : 1.0f;  // first half: a cos - b sin; second: b cos + a sin
     return make_float4(fmaf(v.x, c01.x, sg * o.x * c01.y), fmaf(v.y, c01.z, sg * o.y * c01.w),
                        fmaf(v.z, c23.x, sg * o.z * c23.y), fmaf(v.w, c23.z, sg * o.w * c23.w));
@@ -102,11 +115,13 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
         if (a.k_new) {
             const int pos = n_keys - 1;
             const float2* cs = a.rope + static_cast<size_t>(pos) * (ATT_HD / 2);
+            const NormRope qn = load_norm_rope(a.q_norm, cs, lane);
             if (c == nact - 1 && warp == 0) {
                 // the block whose chunk holds pos finalises the token's key before
                 // staging it (the batch loop's first barrier orders the store)
+                const NormRope kn = load_norm_rope(a.k_norm, cs, lane);
                 float4 k = __ldcg(reinterpret_cast<const float4*>(a.k_new + static_cast<size_t>(g) * ATT_HD) + lane);
-                k = head_norm_rope(k, a.k_norm, cs, a.eps, lane);
+                k = head_norm_rope(k, kn, a.eps, lane);
                 const __half2 k01 = __floats2half2_rn(k.x, k.y), k23 = __floats2half2_rn(k.z, k.w);
                 uint2 u;
                 u.x = *reinterpret_cast<const uint32_t*>(&k01);
@@ -114,7 +129,7 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
                 *reinterpret_cast<uint2*>(const_cast<__half*>(kbase) + static_cast<size_t>(pos) * ATT_HD + 4 * lane) = u;
                 __threadfence_block();
             }
-            v = head_norm_rope(v, a.q_norm, cs, a.eps, lane);
+            v = head_norm_rope(v, qn, a.eps, lane);
         }
         *reinterpret_cast<float4*>(&qs[warp][4 * lane]) = v;
     }

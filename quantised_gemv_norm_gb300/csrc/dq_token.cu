@@ -161,6 +161,12 @@ __device__ __forceinline__ void tk_fold_attention(int l)
     const __half* vc = kc + plane;
     const bool qwen = A.k_new != nullptr;
     constexpr int NH = 2;  // heads per warp
+    NormRope qn{}, kn{};
+    if (qwen) {  // issued with the loads below: one round trip for everything
+        const float2* cs = A.rope + static_cast<size_t>(pos) * (ATT_HD / 2);
+        qn = load_norm_rope(A.layers[l].q_norm, cs, lane);
+        kn = load_norm_rope(A.layers[l].k_norm, cs, lane);
+    }
     bool on[NH];
     int hh[NH], gg[NH];
     float4 q[NH], k[NH];
@@ -195,9 +201,8 @@ __device__ __forceinline__ void tk_fold_attention(int l)
         uint2 knew = make_uint2(0u, 0u);
         float4 qi = q[i];
         if (qwen) {
-            const float2* cs = A.rope + static_cast<size_t>(pos) * (ATT_HD / 2);
-            qi = head_norm_rope(qi, A.layers[l].q_norm, cs, A.eps, lane);
-            const float4 kk = head_norm_rope(k[i], A.layers[l].k_norm, cs, A.eps, lane);
+            qi = head_norm_rope(qi, qn, A.eps, lane);
+            const float4 kk = head_norm_rope(k[i], kn, A.eps, lane);
             const __half2 k01 = __floats2half2_rn(kk.x, kk.y), k23 = __floats2half2_rn(kk.z, kk.w);
             knew.x = *reinterpret_cast<const uint32_t*>(&k01);
             knew.y = *reinterpret_cast<const uint32_t*>(&k23);
