@@ -306,9 +306,16 @@ def run_ours(args):
                             "GBps": round(byts / us / 1e3, 1), "launches_per_token": len(layers)}
     share = {k: v["us_per_launch"] * v["launches_per_token"] for k, v in per_kernel.items()}
     dom = max(share, key=share.get)
+    dom_traffic = None
+    if os.path.exists(prof):
+        try:
+            dom_traffic = json.load(open(prof)).get(dom, {}).get("dram_bytes_per_launch")
+        except Exception:
+            dom_traffic = None
     separate = {"tokens_per_s": round(K * world / gs, 2), "ms_per_step": round(gs / K * 1e3, 4),
                 "launches_per_step": gmodel.launches_per_step, "per_kernel": per_kernel,
-                "dominant_kernel": dom, "dominant_frac": round(per_kernel[dom]["GBps"] / peak, 4)}
+                "dominant_kernel": dom, "dominant_frac": round(per_kernel[dom]["GBps"] / peak, 4),
+                "dominant_traffic": dom_traffic}
     gmodel.close()
     if rl_kernel is None:  # the separate kernels are what ran: the dominant one
         rl_kernel, achieved = dom, per_kernel[dom]["GBps"]
