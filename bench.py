@@ -526,15 +526,18 @@ def run_token_probe(args):
 # -------------------------------------------------------------- the oracle
 
 
-def cpu_baseline(m, tokens: int = 1):
-    """The fp64 CPU oracle, as it stands, on this host's cores: `tokens` full decode tokens."""
+def cpu_baseline(m, budget_s: float = 10.0, max_tokens: int = 30):
+    """The fp64 CPU oracle, as it stands, on this host's cores: full decode tokens of
+    the same workload until about `budget_s` seconds of CPU work (at least one)."""
     import oracle
 
     oracle.build()
     kv = synth.make_kv_cache(SEED, m, 0)
     t0 = time.perf_counter()
-    for t in range(tokens):
-        oracle.decode_step(m, synth.decode_input(SEED, m.hidden, t), 0, kv)
+    tokens = 0
+    while tokens < max_tokens and (tokens == 0 or time.perf_counter() - t0 < budget_s):
+        oracle.decode_step(m, synth.decode_input(SEED, m.hidden, tokens), 0, kv)
+        tokens += 1
     dt = time.perf_counter() - t0
     return {"value": round(tokens / dt, 4), "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "%d full decode token(s) of the same workload (pos 0), fp64, %.1f s" % (tokens, dt)}
