@@ -8,7 +8,7 @@ namespace dq {
 constexpr int ATT_HD = 128;      // head dimension the kernel is written for (4 dims per lane)
 constexpr int ATT_CHUNKS = 16;   // key chunks per KV head (thread blocks per KV head)
 constexpr int ATT_BATCH = 32;    // keys staged in shared memory at a time (one per lane)
-constexpr int ATT_MIN_CHUNK = 64; // fewest keys per block
+constexpr int ATT_MIN_CHUNK = 32; // fewest keys per block (one staging batch)
 constexpr int ATT_PART = 4 + ATT_HD;  // floats per partial: m, l, 2 pad, o[128]
 constexpr int ATT_COUNTER_BYTES = 256;
 
