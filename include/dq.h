@@ -199,7 +199,7 @@ DQ_API int dq_dequant_q2k(const void* blocks, float* out, long long nblocks, voi
  *
  * q: fp32 [n_q][head_dim]; k_plane, v_plane: fp16 [n_kv][max_ctx][head_dim]
  * (one layer of the cache); out: fp32 [n_q][head_dim].  The keys are split into
- * up to 16 chunks per KV head, one thread block each; the last block to finish
+ * up to 32 chunks per KV head, one thread block each; the last block to finish
  * for a KV head merges the chunk partials (max-subtracted log-sum-exp).
  * workspace: device scratch of dq_attention_workspace_bytes(n_q, n_kv) bytes,
  * zero-filled by the caller before its first use; the kernel leaves it zeroed
@@ -218,7 +218,7 @@ DQ_API int dq_attention_decode(const float* q, const void* k_plane, const void* 
  * is captured under a mode that forbids allocation, server plugins whose host
  * owns all device memory, deployments that fix device memory at start-up).
  * The scratch is one static device array of the library, sized for
- * n_q <= 64 and n_kv <= 64 (about 529 KB, held on every device that loads the
+ * n_q <= 64 and n_kv <= 64 (about 1.06 MB, held on every device that loads the
  * library until the process exits).  The first call on a device looks up that
  * array's address; make that first call before any stream capture.  Each call
  * clears the array's merge counters on `stream` first.  All calls share the

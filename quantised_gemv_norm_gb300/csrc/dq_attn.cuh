@@ -6,7 +6,7 @@
 namespace dq {
 
 constexpr int ATT_HD = 128;      // head dimension the kernel is written for (4 dims per lane)
-constexpr int ATT_CHUNKS = 16;   // key chunks per KV head (thread blocks per KV head)
+constexpr int ATT_CHUNKS = 32;   // key chunks per KV head at most (thread blocks per KV head)
 constexpr int ATT_BATCH = 32;    // keys staged in shared memory at a time (one per lane)
 constexpr int ATT_MIN_CHUNK = 32; // fewest keys per block (one staging batch)
 constexpr int ATT_PART = 4 + ATT_HD;  // floats per partial: m, l, 2 pad, o[128]
@@ -81,16 +81,17 @@ __device__ __forceinline__ float4 head_norm_rope(float4 v, const NormRope& nr, f
                        fmaf(v.z, c23.x, sg * o.z * c23.y), fmaf(v.w, c23.z, sg * o.w * c23.w));
 }
 
-// Block (c, g) of the decode attention, run by the first `group` warps of the
-// calling block (threads 0 .. 32 group - 1, synchronised by named barrier
-// ATT_BAR), with `sm` (AttnSmem) as shared staging.  Used by the standalone
-// kernel and by the fused token kernel.
-__device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int group, AttnSmem& sm, bool pdl)
+// Block (c, g) of the decode attention, run by `group` warps of the calling
+// block (threads tbase .. tbase + 32 group - 1, synchronised by named barrier
+// bar), with `sm` (AttnSmem) as shared staging.  Used by the standalone kernel
+// and by the fused token kernel (two items at a time there).
+__device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int group, AttnSmem& sm, bool pdl,
+                                           int bar = ATT_BAR, int tbase = 0)
 {
     auto& ks = sm.ks;
     auto& vs = sm.vs;
     auto& qs = sm.qs;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x - tbase, warp = tid >> 5, lane = tid & 31;
     const int nthr = 32 * group;
     // step->pos was written before the token's first kernel: safe before the wait
     const int n_keys = a.step ? a.step->pos + 1 : a.n_keys;
@@ -140,7 +141,7 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
     float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
     for (int jb = j0; jb < j1; jb += ATT_BATCH) {
         const int nb = min(ATT_BATCH, j1 - jb);
-        named_bar_sync(ATT_BAR, nthr);  // previous batch fully consumed (and qs written on the first)
+        named_bar_sync(bar, nthr);  // previous batch fully consumed (and qs written on the first)
         for (int idx = tid; idx < nb * (ATT_HD / 8); idx += nthr) {
             const int j = idx >> 4, ch = idx & 15;
             const uint4 kv = __ldcg(reinterpret_cast<const uint4*>(kbase + static_cast<size_t>(jb + j) * ATT_HD) + ch);
@@ -148,7 +149,7 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
             *reinterpret_cast<uint4*>(&ks[j][8 * ch]) = kv;
             *reinterpret_cast<uint4*>(&vs[j][8 * ch]) = vv;
         }
-        named_bar_sync(ATT_BAR, nthr);
+        named_bar_sync(bar, nthr);
         float s = -INFINITY;
         if (lane < nb) {
             float d0 = 0.f, d1 = 0.f;
@@ -198,10 +199,10 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
     }
     *reinterpret_cast<float4*>(pp + 4 + 4 * lane) = make_float4(o0, o1, o2, o3);
     __threadfence();
-    named_bar_sync(ATT_BAR, nthr);
+    named_bar_sync(bar, nthr);
     if (tid == 0)
         sm.last = (atomicAdd(&a.counters[g], 1) == nact - 1);
-    named_bar_sync(ATT_BAR, nthr);
+    named_bar_sync(bar, nthr);
     if (!sm.last)
         return;
     __threadfence();
@@ -221,7 +222,7 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
     const float inv = 1.0f / Ls;
     *reinterpret_cast<float4*>(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane) =
         make_float4(r0 * inv, r1 * inv, r2 * inv, r3 * inv);
-    named_bar_sync(ATT_BAR, nthr);
+    named_bar_sync(bar, nthr);
     if (tid == 0)
         a.counters[g] = 0;
 }

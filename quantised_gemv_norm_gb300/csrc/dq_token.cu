@@ -444,7 +444,8 @@ __device__ __forceinline__ void tk_attention(int p)
         return;
     tk_trace(p, 2);
     const int group = A.n_q / A.n_kv;
-    if ((threadIdx.x >> 5) < group) {
+    const int sub = (threadIdx.x >> 5) / group;  // two items at a time: warps [0, group) and [group, 2 group)
+    if (sub < 2) {
         const int l = p / 5;
         const size_t plane = static_cast<size_t>(A.n_kv) * A.max_ctx * A.hd;
         AttnArgs t;
@@ -468,10 +469,11 @@ __device__ __forceinline__ void tk_attention(int p)
         const int n_keys = A.pos + 1;
         const int L = max((n_keys + ATT_CHUNKS - 1) / ATT_CHUNKS, ATT_MIN_CHUNK);
         const int nact = (n_keys + L - 1) / L;
-        AttnSmem& sm = *reinterpret_cast<AttnSmem*>(tk_xq());
-        for (int item = blockIdx.x; item < nact * A.n_kv; item += gridDim.x) {
-            attn_block(t, item % nact, item / nact, group, sm, false);
-            named_bar_sync(ATT_BAR, 32 * group);  // staging free before the next item
+        AttnSmem& sm = *reinterpret_cast<AttnSmem*>(tk_xq() + sub * (TK_ATT_STAGING / 4));
+        const int bar = ATT_BAR - sub;
+        for (int item = 2 * blockIdx.x + sub; item < nact * A.n_kv; item += 2 * gridDim.x) {
+            attn_block(t, item % nact, item / nact, group, sm, false, bar, 32 * group * sub);
+            named_bar_sync(bar, 32 * group);  // staging free before the next item
         }
     }
     tk_trace(p, 4);

@@ -92,14 +92,17 @@ constexpr int TK_OFF_RESID = TK_OFF_KTAB + 256;
 constexpr int TK_OFF_PTAB = TK_OFF_RESID + TK_RESID_MAX * 4;
 constexpr int TK_OFF_XQ = TK_OFF_PTAB + ((5 * TK_MAX_LAYERS + 2) * static_cast<int>(sizeof(PhaseEnt)) + 127) / 128 * 128;
 
+// Bytes of one attention item's staging, rounded to 128: two items run at a time.
+constexpr int TK_ATT_STAGING = (static_cast<int>(sizeof(AttnSmem)) + 127) / 128 * 128;
+
 // Shared-memory bytes of the block for a model shape: the quantised
 // activation of the largest input (two planes for Q|K|V and O, one for the
-// down projection) or the attention staging, whichever is larger.
+// down projection) or the attention staging of two items, whichever is larger.
 __host__ __device__ inline int tk_smem_bytes(int hidden, int qdim, int ffn)
 {
     int xq = (hidden > qdim ? hidden : qdim) / 32 * xq_words(2) * 4;
     xq = xq > ffn / 32 * xq_words(1) * 4 ? xq : ffn / 32 * xq_words(1) * 4;
-    xq = xq > static_cast<int>(sizeof(AttnSmem)) ? xq : static_cast<int>(sizeof(AttnSmem));
+    xq = xq > 2 * TK_ATT_STAGING ? xq : 2 * TK_ATT_STAGING;
     return TK_OFF_XQ + xq;
 }
 

@@ -91,7 +91,7 @@ def test_argument_errors_return_before_launch(lib):
 
 
 def test_attention_workspace_size(lib):
-    assert lib.dq_attention_workspace_bytes(32, 8) == 256 + 32 * 16 * 132 * 4
+    assert lib.dq_attention_workspace_bytes(32, 8) == 256 + 32 * 32 * 132 * 4
     assert lib.dq_attention_workspace_bytes(0, 8) == 0
 
 

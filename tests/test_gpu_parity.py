@@ -359,7 +359,7 @@ def test_decode_small_model_steps(dq, orc, mode):
 
 @pytest.mark.parametrize("mode", ["fused", "kernels"])
 def test_decode_small_model_attention_chunks(dq, orc, mode):
-    # contexts around the attention's chunking: one chunk (64 keys), two, and 16 chunks of 69 keys
+    # contexts around the attention's chunking: two chunks (64 keys), three, and 32 chunks of 35 keys
     m = synth.make_model(23, n_layers=2, hidden=2048, ffn=4096, n_q_heads=16, n_kv_heads=4, head_dim=128,
                          vocab=300, max_ctx=1200)
     kv = synth.make_kv_cache(23, m, 1100)
