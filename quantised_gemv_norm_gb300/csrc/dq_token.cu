@@ -254,8 +254,8 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
     constexpr int RG = tk_rg(KIND);   // row groups
     constexpr int RP = tk_rpt(KIND);  // rows per thread and matrix
     constexpr int R = RG * RP;        // rows per tile and matrix
-    constexpr int UL = 1;
-    constexpr int NCH = (8 * P + TK_THREADS - 1) / TK_THREADS;  // 4-element chunks a thread quantises: K <= 32 P
+    constexpr int UL = tk_ul(KIND);   // activation units a thread holds
+    constexpr int NCH = (8 * P * UL + TK_THREADS - 1) / TK_THREADS;  // 4-element chunks a thread quantises
     static_assert(RP * NMAT <= TK_RED_STRIDE, "partial sums per warp");
     const TokenArgs& A = tk_args();
     const KindEnt& ke = tk_ktab()[KIND];
@@ -323,8 +323,12 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
     const int g = tid / P, pp = tid % P;
     UnitState<FMT, PL> us[UL];
     bool have[UL];
-    have[0] = pp < K / 32;
-    const int nidx[UL] = {have[0] ? pp : K / 32 - 1};
+    int nidx[UL];
+#pragma unroll
+    for (int k = 0; k < UL; ++k) {
+        have[k] = pp + P * k < K / 32;
+        nidx[k] = have[k] ? pp + P * k : K / 32 - 1;  // a stand-in for a missing unit (zero activation)
+    }
     load_units<FMT, PL, UL>(us, have, tk_xq(), pp, P, rstd);
     tk_trace(p, 7);
 
@@ -614,6 +618,7 @@ int plan_token(int n_layers, int hidden, int ffn, int n_q, int n_kv, int hd, boo
     using namespace dq;
     const int qdim = n_q * hd;
     if (n_layers > TK_MAX_LAYERS || hidden > 32 * tk_p(PH_QKV) || qdim > 32 * tk_p(PH_O) ||
+        hidden > 32 * tk_p(PH_GATEUP) * tk_ul(PH_GATEUP) ||
         ffn > 32 * tk_p(PH_DOWN_Q4) || hidden % 2048 || qdim % 256 || ffn % 256 || hd != ATT_HD || n_q % n_kv ||
         n_q / n_kv > 8)
         return DQ_ERR_UNSUPPORTED;
