@@ -420,6 +420,18 @@ def test_decode_short_context_fold_boundary(dq, orc, mode, qwen3):
     _run_decode(dq, orc, m, kv, [1, 2, 3, 4, 5], emulate=True, flags=flags, fused=fused)
 
 
+@pytest.mark.parametrize("n_q,n_kv", [(16, 2), (8, 8)])
+@pytest.mark.parametrize("mode", ["fused", "kernels"])
+def test_decode_group_sizes(dq, orc, mode, n_q, n_kv):
+    # 8 query heads per KV head (two attention items fill the fused block's 16 warps) and
+    # one (two warps work); short, one-chunk and many-chunk contexts
+    m = synth.make_model(29, n_layers=2, hidden=2048, ffn=4096, n_q_heads=n_q, n_kv_heads=n_kv, head_dim=128,
+                         vocab=300, max_ctx=700, qwen3_attention=True)
+    kv = synth.make_kv_cache(29, m, 650)
+    flags, fused = MODES[mode]
+    _run_decode(dq, orc, m, kv, [2, 40, 650], emulate=True, flags=flags, fused=fused)
+
+
 def test_decode_qwen3_attention_modes_agree(dq, orc):
     # the fused kernel and the separate kernels compute the same norm, rotation and cache row
     m = synth.make_model(27, n_layers=2, hidden=2048, ffn=4096, n_q_heads=8, n_kv_heads=2, head_dim=128,
