@@ -7,6 +7,8 @@ configuration sizes.  Tolerances:
   attention  max|o - r| / max|r| <= 1e-4 (fp16 data, fp32 arithmetic)
   decode     logits max|y - r| / max|r| <= 2e-3
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -429,7 +431,29 @@ def test_decode_group_sizes(dq, orc, mode, n_q, n_kv):
                          vocab=300, max_ctx=700, qwen3_attention=True)
     kv = synth.make_kv_cache(29, m, 650)
     flags, fused = MODES[mode]
-    _run_decode(dq, orc, m, kv, [2, 40, 650], emulate=True, flags=flags, fused=fused)
+    _run_decode(dq, orc, m, kv, [2, 40, 650, 699], emulate=True, flags=flags, fused=fused)  # 699: last row
+
+
+@pytest.mark.parametrize("mode", ["fused", "kernels"])
+def test_decode_step_argument_errors(dq, orc, mode):
+    # positions outside the cache and null buffers are refused before any launch
+    from quantised_gemv_norm_gb300 import upload
+
+    m = synth.make_model(30, n_layers=1, hidden=2048, ffn=2048, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                         vocab=256, max_ctx=16)
+    w = upload.to_device(m, synth.make_kv_cache(30, m, 0))
+    model = dq.Model(**upload.model_kwargs(m), weights=w, flags=MODES[mode][0])
+    x = cuda(synth.decode_input(30, m.hidden))
+    for pos in (-1, m.max_ctx, m.max_ctx + 5):
+        with pytest.raises(dq.DQError) as e:
+            model.step(x, pos)
+        assert e.value.status == -2
+    lib = dq.load()
+    assert lib.dq_decode_step(model._h, None, 0, ctypes.c_void_p(x.data_ptr()), None) == -1
+    logits = model.step(x, m.max_ctx - 1)  # the last row is valid
+    assert bool(torch.isfinite(logits).all())
+    model.close()
+    assert dq.device_error() == 0
 
 
 def test_decode_qwen3_attention_modes_agree(dq, orc):
