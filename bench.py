@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -113,7 +114,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_%d.csv" % gpu_index)
+        self.path = os.path.join(tempfile.gettempdir(), "dq_bench_clocks_%d_%d.csv" % (gpu_index, os.getpid()))
 
     def __enter__(self):
         try:
