@@ -335,6 +335,7 @@ def run_ours(args):
     # ---- M-token sweep of one Q4_K matrix (tensor cores vs one GEMV per token)
     msweep = run_msweep(device) if not args.no_msweep else {}
     lowbit = run_lowbit(device) if not args.no_msweep else {}
+    standalone = run_standalone(device) if not args.no_msweep else {}
 
     out = {
         "metric": METRIC,
@@ -361,6 +362,7 @@ def run_ours(args):
         "ctx512": ctx,
         "msweep": msweep,
         "lowbit_gemv": lowbit,
+        "standalone": standalone,
         "e2e": {"value": round(K * world / e2e_max, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4 * m.hidden,
                 "d2h_bytes_per_step": 4 * m.vocab},
         "gpu_launches": model.launches_per_step * K,
@@ -407,6 +409,7 @@ def run_msweep(device, reps: int = 20) -> dict:
                 dq.matmul_q4k(copies[i % len(copies)], Xm, out=Ym, path=path)
             torch.cuda.synchronize(device)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(20_000_000)  # the calls queue behind it: the events time the GPU
             a.record(stream)
             for i in range(reps):
                 dq.matmul_q4k(copies[i % len(copies)], Xm, out=Ym, path=path)
@@ -450,6 +453,7 @@ def run_lowbit(device, reps: int = 20) -> dict:
                 fn(copies[i % len(copies)], x, out=y)
             torch.cuda.synchronize(device)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(20_000_000)  # the calls queue behind it: the events time the GPU
             a.record(stream)
             for i in range(reps):
                 fn(copies[i % len(copies)], x, out=y)
@@ -462,6 +466,64 @@ def run_lowbit(device, reps: int = 20) -> dict:
         out["%dx%d" % (rows, K)] = res
     out["peak_GBps"] = bw
     out["peak_source"] = bsrc
+    return out
+
+
+def run_standalone(device, reps: int = 20) -> dict:
+    """The bf16 GEMV on the shapes of the bf16 configuration (weights larger than L2
+    read from HBM each call: enough rotated copies) and the two norms on the
+    64x2048 norm configuration, with the default block and with one thread per row
+    (the pages' serial norm).  Device-generated seeded inputs; CUDA events."""
+    import torch
+
+    from quantised_gemv_norm_gb300 import dq
+
+    stream = torch.cuda.current_stream(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    bw, bsrc = hbm_peak_gbs()
+    gen = torch.Generator(device=device)
+    gen.manual_seed(SEED)
+
+    def timed(fn, n):
+        # the calls queue behind a device-side sleep, so the events time the GPU running
+        # them back to back rather than the host issuing them
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(20_000_000)
+        a.record(stream)
+        for i in range(n):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) * 1e3 / n
+
+    out = {"bf16_gemv": {}, "norms": {}}
+    for rows, K in ((4096, 4096), (12288, 4096), (4096, 12288), (151936, 4096)):
+        W = (torch.randn((rows, K), generator=gen, device=device) * 0.02).to(torch.bfloat16)
+        x = torch.randn((K,), generator=gen, device=device).to(torch.bfloat16)
+        y = torch.empty(rows, dtype=torch.float32, device=device)
+        wbytes = W.numel() * 2
+        copies = [W] + [W.clone() for _ in range(max(0, -(-(3 * l2) // wbytes) - 1))]
+        us = timed(lambda i: dq.gemv_bf16(copies[i % len(copies)], x, out=y), reps if rows < 100000 else 5)
+        out["bf16_gemv"]["%dx%d" % (rows, K)] = {"weight_bytes": wbytes, "us": round(us, 2),
+                                                 "GBps": round(wbytes / us / 1e3, 1),
+                                                 "frac_of_peak": round(wbytes / us / 1e3 / bw, 4)}
+        del copies, W
+    out["bf16_gemv"]["peak_GBps"], out["bf16_gemv"]["peak_source"] = bw, bsrc
+    rows, n = 64, 2048
+    x = torch.randn((rows, n), generator=gen, device=device)
+    g = 1.0 + 0.1 * torch.randn((n,), generator=gen, device=device)
+    bt = 0.1 * torch.randn((n,), generator=gen, device=device)
+    y = torch.empty_like(x)
+    for threads in (None, 1):
+        key = "default_block" if threads is None else "one_thread_per_row"
+        out["norms"][key] = {
+            "rmsnorm_us": round(timed(lambda i: dq.rmsnorm(x, g, 1e-6, out=y, threads=threads), 100), 2),
+            "layernorm_us": round(timed(lambda i: dq.layernorm(x, g, bt, 1e-6, out=y, threads=threads), 100), 2),
+        }
+    out["norms"]["shape"] = "%dx%d fp32" % (rows, n)
     return out
 
 
