@@ -230,6 +230,45 @@ __device__ __forceinline__ float q2k_unit(const uint8_t* rp, int n, const XQ<1>&
     return (d * u.s) * static_cast<float>(v) - (dmin * u.s * (1.0f / 32.0f)) * static_cast<float>(mn32);
 }
 
+// Q2_K units n and n + 1 (n even: one block, sub-blocks 2(n & 7) .. + 3) of a row
+// at once: the block header, the four scale/min bytes (one word) and the fp16
+// conversions are shared.
+__device__ __forceinline__ float q2k_unit_pair(const uint8_t* rp, int n, const XQ<1>& u0, const XQ<1>& u1)
+{
+    const uint8_t* bp = rp + Q2K_BYTES * (n >> 3);
+    const int ja = 2 * (n & 7);
+    const uint32_t hd = lds32(bp);
+    const uint32_t scm = lds32(bp + 4 + ja);  // sc|m bytes of sub-blocks ja .. ja + 3 (4-byte aligned: ja % 4 == 0)
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        w[q] = lds32(bp + 20 + 4 * (ja + q));
+    int d0[4] = {0, 0, 0, 0}, d1[4] = {0, 0, 0, 0};  // per sub-block: lo and hi dp2a chains
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const XQ<1>& u = q < 2 ? u0 : u1;
+            const int o = (q & 1) * 8;  // sub-block q & 1 of its unit: activation words 0..7 or 8..15
+            const uint32_t c = (w[q] >> (2 * k)) & 0x03030303u;
+            d0[q] = dp2a_lo(u.q[o + 2 * k], c, d0[q]);
+            d1[q] = dp2a_hi(u.q[o + 2 * k + 1], c, d1[q]);
+        }
+    }
+    int v[2], mn[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t sa = (scm >> (16 * h)) & 0xffu, sb = (scm >> (16 * h + 8)) & 0xffu;
+        const XQ<1>& u = h ? u1 : u0;
+        v[h] = static_cast<int>(sa & 15u) * (d0[2 * h] + d1[2 * h]) +
+               static_cast<int>(sb & 15u) * (d0[2 * h + 1] + d1[2 * h + 1]);
+        mn[h] = static_cast<int>(sa >> 4) * u.s32a + static_cast<int>(sb >> 4) * u.s32b;
+    }
+    const float d = half_bits_to_float(hd), dmin = half_bits_to_float(hd >> 16) * (1.0f / 32.0f);
+    return (d * u0.s) * static_cast<float>(v[0]) - (dmin * u0.s) * static_cast<float>(mn[0]) +
+           (d * u1.s) * static_cast<float>(v[1]) - (dmin * u1.s) * static_cast<float>(mn[1]);
+}
+
 // bf16 unit n: 8 weights at byte 16n of the row; xb holds the 8 bf16 activations.
 __device__ __forceinline__ float bf16_unit(const uint8_t* rp, int n, const uint32_t (&xb)[4])
 {
@@ -283,6 +322,17 @@ template <int PL>
 struct UnitState<FMT_BF16, PL> {
     uint32_t xb[4];
 };
+
+// The k-th activation unit of thread p of a P-thread row group holding UL units:
+// p + P k, or, for Q2_K with an even UL, adjacent pairs UL p + k (a pair shares one
+// block of the weight row, see q2k_unit_pair).
+template <int FMT, int UL>
+__host__ __device__ constexpr bool q2k_pairs() { return FMT == FMT_Q2K && UL % 2 == 0; }
+template <int FMT, int UL>
+__device__ __forceinline__ int unit_of(int p, int P, int k)
+{
+    return q2k_pairs<FMT, UL>() ? UL * p + k : p + P * k;
+}
 
 // ------------------------------------------------------- shared-memory layout
 
@@ -441,6 +491,14 @@ __device__ __forceinline__ void consume_tile(const uint8_t* tile, int R, int RG,
         for (int m = 0; m < NMAT; ++m) {
             const uint8_t* rp = tile + static_cast<size_t>(m * R + row) * row_bytes;
             float sum = 0.f;
+            if (FMT == FMT_Q2K && UL % 2 == 0) {  // adjacent unit pairs (q2k_pairs)
+#pragma unroll
+                for (int k = 0; k < UL; k += 2)
+                    sum += q2k_unit_pair(rp, nidx[k], reinterpret_cast<const XQ<1>&>(us[k]),
+                                         reinterpret_cast<const XQ<1>&>(us[k + 1]));
+                acc[m * RPT + i] = sum;
+                continue;
+            }
 #pragma unroll
             for (int k = 0; k < UL; ++k) {
                 if (FMT == FMT_Q4K)
@@ -481,7 +539,7 @@ __device__ __forceinline__ void load_units(UnitState<FMT, PL> (&us)[UL], const b
             u.s = u.f = u.hsum = 0.f;
             u.s32a = u.s32b = 0;
         } else {
-            const uint32_t* src = xq + (unit_k0<FMT>(p + P * k) >> 5) * xq_words(PL);
+            const uint32_t* src = xq + (unit_k0<FMT>(unit_of<FMT, UL>(p, P, k)) >> 5) * xq_words(PL);
 #pragma unroll
             for (int w = 0; w < 16; w += 4) {
                 const uint4 v = *reinterpret_cast<const uint4*>(src + w);
@@ -587,8 +645,9 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
     int nidx[UL];
 #pragma unroll
     for (int k = 0; k < UL; ++k) {
-        have[k] = (p + P * k) < U;
-        nidx[k] = have[k] ? p + P * k : U - 1;  // a stand-in for a missing unit (zero activation)
+        have[k] = unit_of<FMT, UL>(p, P, k) < U;
+        // a stand-in for a missing unit (zero activation); pairs keep their even start
+        nidx[k] = have[k] ? unit_of<FMT, UL>(p, P, k) : (q2k_pairs<FMT, UL>() ? (U - 2 + (k & 1)) : U - 1);
     }
 
     if (FMT == FMT_BF16) {
