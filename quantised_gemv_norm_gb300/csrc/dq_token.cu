@@ -619,7 +619,7 @@ int plan_token(int n_layers, int hidden, int ffn, int n_q, int n_kv, int hd, boo
     const int qdim = n_q * hd;
     if (n_layers > TK_MAX_LAYERS || hidden > 32 * tk_p(PH_QKV) || qdim > 32 * tk_p(PH_O) ||
         hidden > 32 * tk_p(PH_GATEUP) * tk_ul(PH_GATEUP) ||
-        ffn > 32 * tk_p(PH_DOWN_Q4) || hidden % 2048 || qdim % 256 || ffn % 256 || hd != ATT_HD || n_q % n_kv ||
+        ffn > 32 * tk_p(PH_DOWN_Q4) * tk_ul(PH_DOWN_Q4) || hidden % 2048 || qdim % 256 || ffn % 256 || hd != ATT_HD || n_q % n_kv ||
         n_q / n_kv > 8)
         return DQ_ERR_UNSUPPORTED;
     if (any_q6_down && ffn % 2048)

@@ -20,14 +20,17 @@ enum { PH_QKV = 0, PH_ATTN, PH_O, PH_GATEUP, PH_DOWN_Q4, PH_DOWN_Q6, PH_VOCAB, P
 // Consumer layout by kind: row groups of tk_p threads (each thread holds tk_ul
 // 32-element units of the activation, so K <= 32 tk_p tk_ul), tk_rpt rows per
 // thread and matrix; a tile holds TK_THREADS / tk_p * tk_rpt rows of each matrix.
-__host__ __device__ constexpr int tk_p(int kind)
-{
-    return kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? TK_THREADS : kind == PH_GATEUP ? 64 : 128;
-}
+__host__ __device__ constexpr int tk_p(int kind) { return kind == PH_GATEUP ? 64 : 128; }
 // activation units a thread holds (K <= 32 tk_p tk_ul)
-__host__ __device__ constexpr int tk_ul(int kind) { return kind == PH_GATEUP ? 2 : 1; }
+__host__ __device__ constexpr int tk_ul(int kind)
+{
+    return kind == PH_GATEUP ? 2 : kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 3 : 1;
+}
 __host__ __device__ constexpr int tk_rg(int kind) { return TK_THREADS / tk_p(kind); }
-__host__ __device__ constexpr int tk_rpt(int kind) { return kind == PH_GATEUP ? 1 : kind == PH_VOCAB ? 2 : 4; }
+__host__ __device__ constexpr int tk_rpt(int kind)
+{
+    return kind == PH_GATEUP || kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 1 : kind == PH_VOCAB ? 2 : 4;
+}
 __host__ __device__ constexpr int tk_rows_per_tile(int kind) { return tk_rg(kind) * tk_rpt(kind); }
 
 struct TokenLayer {
