@@ -472,7 +472,8 @@ __device__ __forceinline__ float quantise_block(float4 (&v)[NCH], const float4 (
 
 // One stage of the consumers: this thread's unit products for rows g, g + RG,
 // ... (RPT of them, each of NMAT matrices) of the tile, reduced over the warp
-// into wred[0 .. RPT NMAT) (the warp's partial sums; matrix m, row i at m RPT + i).
+// into wred[0 .. RPT NMAT) (the warp's partial sums; matrix m, row i at m RPT + i;
+// three sums are reduced as four, so wred then holds a fourth, zero entry).
 // nidx[k] is the unit thread k-slot k reads: its own unit, or a valid stand-in
 // whose activation is zero (load_units) when the thread has none.  Rows past
 // the tile's last (a partial last tile) are computed from stale stage bytes and
@@ -482,8 +483,10 @@ __device__ __forceinline__ void consume_tile(const uint8_t* tile, int R, int RG,
                                              const UnitState<FMT, PL> (&us)[UL], const int (&nidx)[UL], float* wred,
                                              int lane)
 {
-    constexpr int NV = RPT * NMAT;
+    constexpr int NV = RPT * NMAT == 3 ? 4 : RPT * NMAT;  // the transpose-reduce takes powers of two
     float acc[NV];
+    if (NV != RPT * NMAT)
+        acc[NV - 1] = 0.f;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
         const int row = g + RG * i;

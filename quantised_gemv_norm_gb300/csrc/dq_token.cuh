@@ -29,7 +29,7 @@ __host__ __device__ constexpr int tk_ul(int kind)
 __host__ __device__ constexpr int tk_rg(int kind) { return TK_THREADS / tk_p(kind); }
 __host__ __device__ constexpr int tk_rpt(int kind)
 {
-    return kind == PH_GATEUP || kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 1 : kind == PH_VOCAB ? 2 : 4;
+    return kind == PH_GATEUP || kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 1 : kind == PH_VOCAB ? 3 : 4;
 }
 __host__ __device__ constexpr int tk_rows_per_tile(int kind) { return tk_rg(kind) * tk_rpt(kind); }
 
