@@ -585,7 +585,7 @@ __global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_const
         st = tk_gemv<PH_QKV, FMT_Q4K, 2, 1, EPI_QKV, true>(p, st.x, st.y);
         if (!a.fold)
             tk_attention(p + 1);
-        st = tk_gemv<PH_O, FMT_Q4K, 2, 1, EPI_RESID, false>(p + 2, st.x, st.y);
+        st = tk_gemv<PH_O, FMT_Q4K, 1, 1, EPI_RESID, false>(p + 2, st.x, st.y);
         st = tk_gemv<PH_GATEUP, FMT_Q4K, 1, 2, EPI_SWIGLU, true>(p + 3, st.x, st.y);
         if (ptab[p + 4].kind == PH_DOWN_Q6)
             st = tk_gemv<PH_DOWN_Q6, FMT_Q6K, 1, 1, EPI_RESID, false>(p + 4, st.x, st.y);

@@ -2,7 +2,8 @@
 
 The CUDA path feeds every quantised GEMV a fixed-point copy of its input: per
 32-element group, x ~= s * xi with |xi| <= 16383 (15 bits), or, for the q|k|v
-and O projections, x ~= s * (xi + xl / 2^15) (about 30 bits).  This module
+projection (and the O projection of the separate kernels), x ~= s * (xi + xl / 2^15)
+(about 30 bits).  This module
 re-applies exactly that rounding to GEMV inputs inside a float64 decode built
 from the oracle's dequantised weights and attention, so a test can tell how
 much of a decode's deviation from the exact oracle the documented format
@@ -46,8 +47,9 @@ def dequantised(orc, m):
     }
 
 
-def decode(orc, m, Wd, x_in, pos, kv):
-    """One token with the CUDA path's activation rounding; updates kv (fp16 bits) in place."""
+def decode(orc, m, Wd, x_in, pos, kv, o_planes: int = 2):
+    """One token with the CUDA path's activation rounding; updates kv (fp16 bits) in place.
+    ``o_planes``: the O projection's activation planes (the fused token kernel uses 1)."""
     hd, nq, nkv = m.head_dim, m.n_q_heads, m.n_kv_heads
     qdim, kvdim = nq * hd, nkv * hd
     kvf = kv.view(np.float16)
@@ -64,7 +66,7 @@ def decode(orc, m, Wd, x_in, pos, kv):
         kvf[l, 0, :, pos, :] = qkv[qdim:qdim + kvdim].reshape(nkv, hd).astype(np.float16)
         kvf[l, 1, :, pos, :] = qkv[qdim + kvdim:].reshape(nkv, hd).astype(np.float16)
         att = orc.attention(qkv[:qdim].reshape(nq, hd), kv[l, 0], kv[l, 1], pos + 1).reshape(-1)
-        x = x + Wd["o"][l] @ group_round(att, 2)
+        x = x + Wd["o"][l] @ group_round(att, o_planes)
         h = group_round(_rms(x, m.ffn_norm[l], m.eps), 1)
         g, u = Wd["gate"][l] @ h, Wd["up"][l] @ h
         x = x + Wd["down"][l] @ group_round(g / (1.0 + np.exp(-g)) * u, 1)
