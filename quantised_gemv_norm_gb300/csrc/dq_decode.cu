@@ -273,8 +273,9 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
     m->kv = static_cast<__half*>(d->kv_cache);
 
     int st;
-    // The q|k|v and O projections feed the attention, which amplifies input
-    // errors: they take the two-plane (about 30-bit) activation.
+    // The q|k|v projection feeds the attention, which amplifies input errors: it
+    // takes the two-plane (about 30-bit) activation.  So does O here (in the
+    // fused token kernel O takes one plane: there it measured faster).
     if ((st = dqhost::plan_gemv(DQ_FMT_Q4K, qdim + 2 * kvdim, d->hidden, 1, 2, false, &m->p_qkv)) != DQ_OK ||
         (st = dqhost::plan_gemv(DQ_FMT_Q4K, d->hidden, qdim, 1, 2, true, &m->p_o)) != DQ_OK ||
         (st = dqhost::plan_gemv(DQ_FMT_Q4K, d->ffn, d->hidden, 2, 1, false, &m->p_gateup)) != DQ_OK ||

@@ -104,7 +104,7 @@ constexpr int TK_OFF_XQ = TK_OFF_PTAB + ((5 * TK_MAX_LAYERS + 2) * static_cast<i
 constexpr int TK_ATT_STAGING = (static_cast<int>(sizeof(AttnSmem)) + 127) / 128 * 128;
 
 // Shared-memory bytes of the block for a model shape: the quantised
-// activation of the largest input (two planes for Q|K|V and O, one for the
+// activation of the largest input (two planes for Q|K|V, one for O and the
 // down projection) or the attention staging of two items, whichever is larger.
 __host__ __device__ inline int tk_smem_bytes(int hidden, int qdim, int ffn)
 {
