@@ -17,5 +17,12 @@ def pytest_configure(config):
 def orc():
     import oracle
 
-    oracle.build()
+    mutant = os.environ.get("DQ_ORACLE_MUTANT")
+    if mutant:
+        # a deliberately broken build of the oracle (tests/test_oracle_mutants.py
+        # checks that the pins reject it); loaded instead of the real one
+        oracle.build = lambda force=False: mutant
+        oracle._lib = None
+    else:
+        oracle.build()
     return oracle

@@ -462,6 +462,22 @@ def test_attention_dominant_key_and_scale(orc):
     assert math.isclose(out[0, 0], math.e / (1 + math.e), rel_tol=1e-15)
 
 
+def test_attention_heads_of_a_group_use_their_own_query(orc):
+    # two KV heads of two query heads each; key j of KV head g points along axis j, and
+    # query head h points along axis h % 2 with a large norm: each head picks the value of
+    # "its" key, so head h returns V[h // 2, h % 2]
+    n_q, n_kv, hd, ctx = 4, 2, 16, 2
+    q = np.zeros((n_q, hd))
+    for h in range(n_q):
+        q[h, h % 2] = 100.0
+    K = np.zeros((n_kv, ctx, hd))
+    K[:, 0, 0] = K[:, 1, 1] = 8.0          # scores 200 and 0: weight e^-200 on the other key
+    V = np.arange(n_kv * ctx * hd, dtype=np.float64).reshape(n_kv, ctx, hd) / 64.0
+    out = orc.attention(q, _halves(K), _halves(V), 2)
+    for h in range(n_q):
+        assert np.allclose(out[h], V[h // 2, h % 2], rtol=0, atol=1e-80)
+
+
 def test_silu(orc):
     assert orc.silu(0.0) == 0.0
     assert math.isclose(orc.silu(1.0), 1.0 / (1.0 + math.exp(-1.0)), rel_tol=1e-16)
@@ -539,6 +555,35 @@ def test_decode_attention_path_empty_cache(orc):
     assert np.allclose(hid, x + Wo @ attn, rtol=1e-12, atol=1e-10)
 
 
+def test_decode_attention_path_qwen3_later_token(orc):
+    # FFN switched off, Qwen3 attention inputs, pos 2 over a filled cache: x1 = x + Wo . attn,
+    # with attn rebuilt from the pinned pieces in the layer's order: the q|k|v projection of
+    # rms(x); per-head RMSNorm, then RoPE at pos, on every q head and on the new key; the new
+    # k and v rounded to fp16 into row pos; attention over keys 0..pos (the new key included).
+    m = synth.make_model(36, n_layers=1, hidden=256, ffn=512, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                         vocab=64, max_ctx=8, qwen3_attention=True)
+    m.wdown[0] = _zero_q4k(m.wdown[0])
+    pos, hd, nq, nkv = 2, m.head_dim, m.n_q_heads, m.n_kv_heads
+    qdim, kvdim = nq * hd, nkv * hd
+    kv = synth.make_kv_cache(36, m, pos)
+    k_plane, v_plane = kv[0, 0].copy(), kv[0, 1].copy()
+    x = synth.decode_input(36, m.hidden)
+    _, hid = orc.decode_step(m, x, pos, kv, want_hidden=True)
+    qkv = orc.dequant_q4k(m.wqkv[0]).reshape(m.qkv_rows, m.hidden) @ _rms(x, m.attn_norm[0], m.eps)
+
+    def turn(v, w):
+        return orc.rope(orc.head_rmsnorm(v, w, m.eps), pos, m.rope_theta)
+
+    q = np.stack([turn(qkv[h * hd:(h + 1) * hd], m.q_norm[0]) for h in range(nq)])
+    for g in range(nkv):
+        k = turn(qkv[qdim + g * hd:qdim + (g + 1) * hd], m.k_norm[0])
+        k_plane[g, pos] = k.astype(np.float16).view(np.uint16)
+        v_plane[g, pos] = qkv[qdim + kvdim + g * hd:qdim + kvdim + (g + 1) * hd].astype(np.float16).view(np.uint16)
+    attn = orc.attention(q, k_plane, v_plane, pos + 1).reshape(-1)
+    Wo = orc.dequant_q4k(m.wo[0]).reshape(m.hidden, qdim)
+    assert np.allclose(hid, x + Wo @ attn, rtol=1e-12, atol=1e-10)
+
+
 def test_decode_ffn_path(orc):
     # attention output projection switched off: x1 = x + Wd . (silu(Wg h) * (Wu h)), h = rms(x)
     m = _tiny_model(n_layers=1)
@@ -599,12 +644,25 @@ def test_rope_turns_the_first_pair_by_the_position(orc):
 
 def test_rope_last_pair_angle(orc):
     # pair (63, 127) turns by pos * theta^(-126/128): with theta = 2^128 that is pos * 2^-126
+    # (a tiny angle: its sine is checked relative to itself)
     pos = 3
     e = np.zeros(128)
     e[63] = 1.0
     r = orc.rope(e, pos, 2.0 ** 128)
     ang = pos * 2.0 ** -126
-    assert abs(r[63] - np.cos(ang)) < 1e-15 and abs(r[127] - np.sin(ang)) < 1e-15
+    assert abs(r[63] - np.cos(ang)) < 1e-15 and abs(r[127] - np.sin(ang)) <= 1e-12 * ang
+
+
+def test_rope_middle_pair_angle(orc):
+    # pair (32, 96) turns by pos * theta^(-64/128) = pos / sqrt(theta): one radian at
+    # pos 1000 with theta 1e6; dimension 31 (pair (31, 95)) turns by 1000 * 1e6^(-62/128)
+    e = np.zeros(128)
+    e[32] = 1.0
+    e[31] = 1.0
+    r = orc.rope(e, 1000, 1.0e6)
+    assert abs(r[32] - math.cos(1.0)) < 1e-12 and abs(r[96] - math.sin(1.0)) < 1e-12
+    a31 = 1000 * 1.0e6 ** (-62 / 128)
+    assert abs(r[31] - math.cos(a31)) < 1e-12 and abs(r[95] - math.sin(a31)) < 1e-12
 
 
 def test_rope_keeps_pair_norms_and_relative_positions(orc):
