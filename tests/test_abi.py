@@ -124,3 +124,34 @@ def test_model_create_checks_qwen3_inputs_before_allocating(lib):
     assert lib.dq_model_create(ctypes.byref(desc(arr(fake), arr([16, 0]), 1e6)), ctypes.byref(h)) == -1
     assert lib.dq_model_create(ctypes.byref(desc(arr(fake), arr([16, 40]), 1e6)), ctypes.byref(h)) == -3
     assert h.value is None
+
+
+def test_binding_struct_and_constants_match_the_header(tmp_path):
+    # the header compiled by a C compiler reports the descriptor's layout and the
+    # constants; the ctypes binding must agree field by field
+    import subprocess
+
+    from quantised_gemv_norm_gb300 import dq, synth
+
+    fields = [name for name, _ in dq._Desc._fields_]
+    consts = ["DQ_OK", "DQ_ERR_NULL", "DQ_ERR_SHAPE", "DQ_ERR_ALIGN", "DQ_ERR_UNSUPPORTED", "DQ_ERR_CUDA",
+              "DQ_ERR_TIMEOUT", "DQ_ERR_ALLOC", "DQ_FMT_BF16", "DQ_FMT_Q4K", "DQ_FMT_Q6K", "DQ_FMT_Q2K",
+              "DQ_MODEL_NO_PDL", "DQ_MODEL_FUSED", "DQ_MATMUL_AUTO", "DQ_MATMUL_CUDA_CORE", "DQ_MATMUL_TENSOR"]
+    src = ["#include <stdio.h>", "#include <stddef.h>", '#include "dq.h"', "int main(void) {",
+           '  printf("size %zu\\n", sizeof(dq_model_desc));']
+    src += ['  printf("%s %%zu\\n", offsetof(dq_model_desc, %s));' % (f, f) for f in fields]
+    src += ['  printf("%s %%d\\n", (int)(%s));' % (c, c) for c in consts]
+    src += ["  return 0;", "}"]
+    c = tmp_path / "layout.c"
+    c.write_text("\n".join(src) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(c), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                           text=True).stdout.splitlines())
+    assert int(got["size"]) == ctypes.sizeof(dq._Desc)
+    for f in fields:
+        assert int(got[f]) == getattr(dq._Desc, f).offset, f
+    assert [int(got[c]) for c in consts[:8]] == [0, -1, -2, -3, -4, -5, -6, -7]
+    assert [int(got[c]) for c in consts[8:12]] == [synth.FMT_BF16, synth.FMT_Q4K, synth.FMT_Q6K, synth.FMT_Q2K]
+    assert [int(got[c]) for c in consts[12:14]] == [dq.MODEL_NO_PDL, dq.MODEL_FUSED]
+    assert [int(got[c]) for c in consts[14:]] == [dq.MATMUL_AUTO, dq.MATMUL_CUDA_CORE, dq.MATMUL_TENSOR]
