@@ -21,6 +21,8 @@ MUTANTS = {
     "half_ties_away_from_zero": ("double n = nearbyint(ldexp(a, 10 - E));", "double n = round(ldexp(a, 10 - E));"),
     "bf16_low_half": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b;"),
     "half_subnormal_threshold": ("if (E < -14)", "if (E < -15)"),
+    "half_sign_dropped": ("return sign ? -v : v;", "return v;"),
+    "fields_big_endian": ("return (uint16_t)(p[0] | (p[1] << 8));", "return (uint16_t)(p[1] | (p[0] << 8));"),
     # Q4_K
     "q4k_min_sign": ("w[n] = d * sc[j] * q[n] - dmin * m[j];", "w[n] = d * sc[j] * q[n] + dmin * m[j];"),
     "q4k_nibbles_swapped": ("q[32 * j + i] = byte & 15;\n            q[32 * j + 16 + i] = byte >> 4;",
@@ -34,6 +36,8 @@ MUTANTS = {
                                "*d = oracle_half_to_double(rd16(blk + 2));\n    *dmin = oracle_half_to_double(rd16(blk + 0));\n"
                                "    for (int j = 0; j < 8; j++) {"),
     # Q6_K
+    "q4k_packer_nibbles_swapped": ("(uint8_t)((q[32 * j + i] & 15) | ((q[32 * j + 16 + i] & 15) << 4));",
+                                   "(uint8_t)((q[32 * j + 16 + i] & 15) | ((q[32 * j + i] & 15) << 4));"),
     "q6k_centre": ("w[n] = d * sc[n / 16] * (q[n] - 32);", "w[n] = d * sc[n / 16] * (q[n] - 31);"),
     "q6k_scale_index": ("w[n] = d * sc[n / 16] * (q[n] - 32);", "w[n] = d * sc[n % 16] * (q[n] - 32);"),
     "q6k_high_bits_order": ("q[32 * g + 16 * h + 4 * t + e] |= hi << 4;", "q[32 * g + 16 * h + 4 * e + t] |= hi << 4;"),
@@ -60,6 +64,8 @@ MUTANTS = {
     "rmsnorm_eps_outside_root": ("double inv = 1.0 / sqrt(ss / n + eps);", "double inv = 1.0 / (sqrt(ss / n) + eps);"),
     "rmsnorm_sum_not_mean": ("double inv = 1.0 / sqrt(ss / n + eps);", "double inv = 1.0 / sqrt(ss + eps);"),
     "rmsnorm_gamma_dropped": ("y[i] = x[i] * inv * (double)gamma[i];", "y[i] = x[i] * inv;"),
+    "rmsnorm_eps_dropped": ("double inv = 1.0 / sqrt(ss / n + eps);", "double inv = 1.0 / sqrt(ss / n);"),
+    "layernorm_eps_dropped": ("double inv = 1.0 / sqrt(v / n + eps);", "double inv = 1.0 / sqrt(v / n);"),
     "layernorm_sample_variance": ("double inv = 1.0 / sqrt(v / n + eps);", "double inv = 1.0 / sqrt(v / (n - 1) + eps);"),
     "layernorm_uncentred_moment": ("v += (xr[i] - mean) * (xr[i] - mean);", "v += xr[i] * xr[i];"),
     "layernorm_beta_dropped": ("* (double)gamma[i] + (double)beta[i];", "* (double)gamma[i];"),
@@ -76,6 +82,8 @@ MUTANTS = {
     # Qwen3 attention inputs
     "head_norm_weight_dropped": ("v[i] = v[i] * r * (double)w[i];", "v[i] = v[i] * r;"),
     "head_norm_eps_outside_root": ("double r = 1.0 / sqrt(ss / hd + eps);", "double r = 1.0 / (sqrt(ss / hd) + eps);"),
+    "head_norm_divisor": ("double r = 1.0 / sqrt(ss / hd + eps);", "double r = 1.0 / sqrt(ss / (hd - 1) + eps);"),
+    "rope_position_off_by_one": ("double ang = (double)pos * pow(", "double ang = (double)(pos + 1) * pow("),
     "rope_rotation_sign": ("v[i] = a * c - b * sn;\n        v[i + half] = b * c + a * sn;",
                            "v[i] = a * c + b * sn;\n        v[i + half] = b * c - a * sn;"),
     "rope_frequency": ("pow(theta, -2.0 * i / hd)", "pow(theta, -1.0 * i / hd)"),
@@ -104,6 +112,9 @@ MUTANTS = {
                                   "oracle_rope(qkv + hh * hd, hd, pos, mdl->rope_theta);\n"
                                   "                oracle_head_rmsnorm(qkv + hh * hd, mdl->q_norm[l], hd, mdl->eps);"),
     "decode_key_not_rotated": ("oracle_rope(qkv + qdim + kvh * hd, hd, pos, mdl->rope_theta);", ";"),
+    "decode_query_norm_on_kv_head_count": ("for (int hh = 0; hh < nq; hh++) {", "for (int hh = 0; hh < nkv; hh++) {"),
+    "decode_vocab_as_q4k": ("gemv_any(FMT_Q6K, mdl->wvocab, h, logits, mdl->vocab, H);",
+                            "gemv_any(FMT_Q4K, mdl->wvocab, h, logits, mdl->vocab, H);"),
     "decode_key_uses_query_norm": ("oracle_head_rmsnorm(qkv + qdim + kvh * hd, mdl->k_norm[l], hd, mdl->eps);",
                                    "oracle_head_rmsnorm(qkv + qdim + kvh * hd, mdl->q_norm[l], hd, mdl->eps);"),
 }
