@@ -111,7 +111,8 @@ DQ_API int dq_device_error(void* stream);
  *               mu_r = mean, var_r = population variance (divide by n).
  * x, y: fp32 [rows][n] row-major (y may equal x); gamma, beta: fp32 [n].
  * One thread block of 256 threads per row; fp32 arithmetic.
- * Errors: NULL pointer -> DQ_ERR_NULL; rows < 1 or n < 1 -> DQ_ERR_SHAPE. */
+ * Errors: NULL pointer -> DQ_ERR_NULL; rows < 1, n < 1, or eps negative, NaN or
+ * infinite -> DQ_ERR_SHAPE; gamma or beta not 16-byte aligned -> DQ_ERR_ALIGN. */
 DQ_API int dq_rmsnorm(const float* x, const float* gamma, float* y, int rows, int n, float eps, void* stream);
 DQ_API int dq_layernorm(const float* x, const float* gamma, const float* beta, float* y, int rows, int n,
                         float eps, void* stream);
@@ -252,8 +253,9 @@ DQ_API int dq_rope_table(float* table, int max_ctx, int head_dim, double theta, 
  * fp16 [n_kv][max_ctx][128] (row pos written, rows < pos read); v_plane as in
  * dq_attention_decode (row pos must already hold the token's value);
  * q_norm, k_norm: fp32 [128]; rope_table: a dq_rope_table of at least n_keys
- * rows for head_dim 128.  All device pointers, 16-byte aligned.  Workspace,
- * limits and errors as dq_attention_decode. */
+ * rows for head_dim 128.  All device pointers, 16-byte aligned.  eps: the head
+ * norm's epsilon, finite and >= 0 (else DQ_ERR_SHAPE).  Workspace, limits and
+ * other errors as dq_attention_decode. */
 DQ_API int dq_attention_decode_rope(const float* q, const float* k_new, void* k_plane, const void* v_plane, float* out,
                                     const float* q_norm, const float* k_norm, const float* rope_table, float eps,
                                     int n_q, int n_kv, int head_dim, int max_ctx, int n_keys, void* workspace,
@@ -307,7 +309,7 @@ typedef struct dq_model dq_model; /* opaque: owns workspace + graph, BORROWS wei
 
 typedef struct {
     int n_layers, hidden, ffn, n_q_heads, n_kv_heads, head_dim, vocab, max_ctx;
-    float eps;
+    float eps;                     /* every RMSNorm's epsilon: finite and >= 0 */
     /* host arrays of n_layers DEVICE pointers each (copied at create time): */
     const float* const* attn_norm; /* fp32 [hidden] */
     const void* const* wqkv;       /* Q4_K [(n_q + 2 n_kv) head_dim][hidden], rows q | k | v */

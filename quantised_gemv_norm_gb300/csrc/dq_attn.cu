@@ -146,7 +146,8 @@ DQ_API int dq_attention_decode_rope(const float* q, const float* k_new, void* k_
 {
     if (!q || !k_new || !k_plane || !v_plane || !out || !q_norm || !k_norm || !rope_table || !workspace)
         return DQ_ERR_NULL;
-    if (n_q < 1 || n_kv < 1 || max_ctx < 1 || n_keys < 1 || n_keys > max_ctx || n_q % n_kv)
+    if (n_q < 1 || n_kv < 1 || max_ctx < 1 || n_keys < 1 || n_keys > max_ctx || n_q % n_kv ||
+        !dqhost::valid_eps(eps))
         return DQ_ERR_SHAPE;
     if (head_dim != dq::ATT_HD || n_q / n_kv > 8 || n_kv > dq::ATT_COUNTER_BYTES / 4)
         return DQ_ERR_UNSUPPORTED;

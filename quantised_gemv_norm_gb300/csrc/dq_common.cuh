@@ -213,5 +213,7 @@ int set_cuda_error(cudaError_t e);               // records e, returns DQ_ERR_CU
 int* device_error_flag();                        // this device's error flag (device pointer)
 int sm_count();                                  // SMs of the current device
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// A norm epsilon the entry points accept: finite and >= 0 (NaN fails both tests).
+inline bool valid_eps(double eps) { return eps >= 0.0 && eps <= 1.0e300; }
 
 }  // namespace dqhost

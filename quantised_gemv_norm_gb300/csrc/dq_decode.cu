@@ -202,7 +202,8 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
         !d->down_fmt || !d->out_norm || !d->wvocab || !d->kv_cache)
         return DQ_ERR_NULL;
     if (d->n_layers < 1 || d->hidden < 1 || d->ffn < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1 ||
-        d->head_dim < 1 || d->vocab < 1 || d->max_ctx < 1 || d->n_q_heads % d->n_kv_heads)
+        d->head_dim < 1 || d->vocab < 1 || d->max_ctx < 1 || d->n_q_heads % d->n_kv_heads ||
+        !dqhost::valid_eps(d->eps))
         return DQ_ERR_SHAPE;
     if (d->head_dim != dq::ATT_HD || d->n_q_heads / d->n_kv_heads > 8 || d->n_kv_heads > dq::ATT_COUNTER_BYTES / 4)
         return DQ_ERR_UNSUPPORTED;

@@ -112,7 +112,7 @@ static int norm_entry(bool ln, const float* x, const float* gamma, const float* 
 {
     if (!x || !gamma || !y || (ln && !beta))
         return DQ_ERR_NULL;
-    if (rows < 1 || n < 1)
+    if (rows < 1 || n < 1 || !dqhost::valid_eps(eps))
         return DQ_ERR_SHAPE;
     if (threads < 1 || threads > 1024 || (threads & (threads - 1)))
         return DQ_ERR_SHAPE;

@@ -84,6 +84,12 @@ def test_argument_errors_return_before_launch(lib):
     assert r(fake, fake, fake, fake, fake, fake, fake, fake, 1e-6, 32, 8, 64, 16, 1, fake, 1 << 20, None) == -4
     assert r(fake, fake, fake, fake, fake, fake, fake, fake, 1e-6, 32, 8, 128, 16, 0, fake, 1 << 20, None) == -2
     assert r(fake, fake, fake, fake, fake, fake, fake, P(24), 1e-6, 32, 8, 128, 16, 1, fake, 1 << 20, None) == -3
+    # a norm epsilon must be finite and >= 0
+    for eps in (-1e-6, float("nan"), float("inf")):
+        assert lib.dq_rmsnorm(fake, fake, fake, 1, 8, eps, None) == -2
+        assert lib.dq_layernorm_threads(fake, fake, fake, fake, 1, 8, eps, 64, None) == -2
+        assert r(fake, fake, fake, fake, fake, fake, fake, fake, eps, 32, 8, 128, 16, 1, fake, 1 << 20, None) == -2
+    assert lib.dq_rmsnorm(fake, P(24), fake, 1, 8, 1e-6, None) == -3  # gamma read as float4
     assert lib.dq_decode_step(None, fake, 0, fake, None) == -1
     h = P()
     assert lib.dq_model_create(None, ctypes.byref(h)) == -1
@@ -123,6 +129,10 @@ def test_model_create_checks_qwen3_inputs_before_allocating(lib):
     assert lib.dq_model_create(ctypes.byref(desc(arr(fake), arr(fake), 0.5)), ctypes.byref(h)) == -2
     assert lib.dq_model_create(ctypes.byref(desc(arr(fake), arr([16, 0]), 1e6)), ctypes.byref(h)) == -1
     assert lib.dq_model_create(ctypes.byref(desc(arr(fake), arr([16, 40]), 1e6)), ctypes.byref(h)) == -3
+    for eps in (-1.0, float("nan"), float("inf")):
+        d = desc(arr(fake), arr(fake), 1e6)
+        d.eps = eps
+        assert lib.dq_model_create(ctypes.byref(d), ctypes.byref(h)) == -2
     assert h.value is None
 
 
