@@ -46,6 +46,17 @@ PAGES_BASELINE_TOK_S = 253.9
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0  # dense, burst; fp16 runs at the same tensor rate
 KERNEL_KINDS = ("qkv", "attention", "o_proj", "gate_up", "down", "vocab")
+# The arithmetic of the timed path: 4- and 6-bit integer weight codes times the
+# activation as 15-bit fixed point per 32-element group, integer dot products
+# (dp2a, int32), block and group scales applied and accumulated in fp32.
+DTYPE = "q4k/q6k codes x s16 group fixed-point activations, int32 dot, f32 scale+accumulate"
+
+
+def bench_config(world: int) -> dict:
+    """The workload both arms run (identical keys and values for the same N)."""
+    return {"workload": WORKLOAD, "bytes_per_token": token_bytes(0), "ctx": 0,
+            "l2": "inputs larger than L2: 4.65 GB of weights read per step, no flush needed",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 def dist_env():
@@ -105,7 +116,8 @@ def hbm_peak_gbs():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms while the GPU runs the
+    decode steps (warm-up, timed and end-to-end regions)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -121,11 +133,21 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         return self
+
+    def wait_first_sample(self, timeout_s: float = 3.0):
+        t0 = time.time()
+        while self.proc and time.time() - t0 < timeout_s:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    return
+            except OSError:
+                pass
+            time.sleep(0.02)
 
     def __exit__(self, *exc):
         if self.proc:
@@ -232,9 +254,12 @@ def run_ours(args):
         barrier(world, device)
         return aggregate_max(a.elapsed_time(b) / 1e3, world, device)
 
-    # ---- device-timed decode: inputs resident in HBM, pos 0 (empty cache) each step
-    with ClockSampler(device.index if device.index is not None else 0) as clocks:
-        max_s = timed_steps(model, 0)
+    # ---- device-timed decode: inputs resident in HBM, pos 0 (empty cache) each step.
+    # The clock sampler runs from before the warm-up through the end-to-end steps below
+    # (nvidia-smi takes a moment to start: the first sample is awaited first).
+    clocks = ClockSampler(device.index if device.index is not None else 0).__enter__()
+    clocks.wait_first_sample()
+    max_s = timed_steps(model, 0)
     err = dq.device_error()
     tok_s = K * world / max_s
 
@@ -258,6 +283,7 @@ def run_ours(args):
         e2e_step(W + t)
     torch.cuda.synchronize(device)
     e2e_local = time.perf_counter() - t0
+    clocks.__exit__(None, None, None)
     barrier(world, device)
     e2e_max = aggregate_max(e2e_local, world, device)
 
@@ -348,11 +374,10 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": round(tok_s / PAGES_BASELINE_TOK_S, 3),
-        "dtype": "f32",
+        "dtype": DTYPE,
         "data": "synthetic (seeded random-init Q4_K/Q6_K weights, N(0,1) hidden inputs)",
-        "config": {"workload": WORKLOAD, "bytes_per_token": tb, "ctx": 0, "mode": mode,
-                   "l2": "inputs larger than L2: 4.65 GB of weights read per step, no flush needed",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": bench_config(world),
+        "mode": mode,
         "hbm": {"achieved_GBps_token": round(tb * tok_s / world / 1e9, 1), "peak_GBps": peak,
                 "frac_of_peak": round(tb * tok_s / world / 1e9 / peak, 4), "peak_source": peak_src,
                 "roofline_tokens_per_s": round(peak * 1e9 / tb, 1)},
@@ -669,7 +694,8 @@ def run_reference(args):
         "vs_baseline": round(v / PAGES_BASELINE_TOK_S, 5),
         "dtype": "f64",
         "data": "synthetic (seeded random-init Q4_K/Q6_K weights, N(0,1) hidden inputs)",
-        "config": {"workload": WORKLOAD, "bytes_per_token": token_bytes(0), "ctx": 0},
+        "config": bench_config(world),
+        "mode": "fp64 CPU oracle on the host cores",
         "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
