@@ -100,6 +100,14 @@ DQ_API int dq_last_cuda_error(void);
  * CUDA error. */
 DQ_API int dq_device_error(void* stream);
 
+/* The same check as a dq_status: synchronises `stream`, reads and clears the
+ * current device's error flag, and returns DQ_OK when it was clear,
+ * DQ_ERR_TIMEOUT when a kernel gave up a bounded wait since the last check
+ * (any of the timeout bits above), DQ_ERR_SHAPE when the only bit is a bad
+ * argument seen on the device, or DQ_ERR_CUDA.  Kernels that give up a wait
+ * leave their outputs undefined but return, so the context stays usable. */
+DQ_API int dq_check_device(void* stream);
+
 /* ------------------------------------------------------------------- norms
  * "one-serial-kernel" (vocodex.ai), section "One thread": the normalisation
  * that runs twice per layer and once at the end, reduced by a block of threads
@@ -214,20 +222,29 @@ DQ_API int dq_attention_decode(const float* q, const void* k_plane, const void* 
                                int n_kv, int head_dim, int max_ctx, int n_keys, void* workspace,
                                size_t workspace_bytes, void* stream);
 
-/* The same attention without any allocation.  The pages have no counterpart:
- * this serves callers that cannot call cudaMalloc (code running while a stream
- * is captured under a mode that forbids allocation, server plugins whose host
- * owns all device memory, deployments that fix device memory at start-up).
- * The scratch is one static device array of the library, sized for
- * n_q <= 64 and n_kv <= 64 (about 1.06 MB, held on every device that loads the
- * library until the process exits).  The first call on a device looks up that
- * array's address; make that first call before any stream capture.  Each call
- * clears the array's merge counters on `stream` first.  All calls share the
- * array: calls whose executions overlap in time (on any streams) race and give
- * wrong results.  Arguments as dq_attention_decode without the workspace.
- * Errors: NULL -> DQ_ERR_NULL; shapes, and n_q > 64 or n_kv > 64 ->
- * DQ_ERR_SHAPE; head_dim != 128 or n_q / n_kv > 8 -> DQ_ERR_UNSUPPORTED;
+/* The same attention without any allocation.  The pages have no counterpart.
+ * It serves callers that cannot call cudaMalloc: inference-server plugins
+ * whose host process owns all device memory through its own pool, and
+ * embedded or real-time deployments that fix their device memory at start-up
+ * (where an allocation can fail, or would block the device, in the middle of
+ * serving).  The scratch (merge counters and chunk partials) is one static
+ * device array of the library, sized for n_q <= DQ_STATIC_ATT_MAX_Q and
+ * n_kv <= DQ_STATIC_ATT_MAX_KV: 256 + 64 * 32 * 132 * 4 = 1,081,600 bytes,
+ * held on every device that loads the library until the process exits.
+ * The first call on a device, with that device current, looks up the array's
+ * device address and keeps it for the process; make that first call before any
+ * stream capture.  cudaDeviceReset invalidates the kept address: do not call
+ * this entry point after a device reset.  Each call first clears the array's
+ * merge counters with a cudaMemsetAsync on `stream` (not an allocation).  All
+ * calls share the array, which keeps the last call's partials: calls whose
+ * executions overlap in time (on any streams) race and give wrong results.
+ * Arguments as dq_attention_decode without the workspace.
+ * Errors: NULL -> DQ_ERR_NULL; shapes, and n_q > DQ_STATIC_ATT_MAX_Q or
+ * n_kv > DQ_STATIC_ATT_MAX_KV -> DQ_ERR_SHAPE; head_dim != 128 or n_q / n_kv > 8
+ * -> DQ_ERR_UNSUPPORTED, as is a current device index of 64 or more;
  * misaligned pointers -> DQ_ERR_ALIGN; a CUDA error -> DQ_ERR_CUDA. */
+#define DQ_STATIC_ATT_MAX_Q 64
+#define DQ_STATIC_ATT_MAX_KV 64
 DQ_API int dq_attention_decode_static(const float* q, const void* k_plane, const void* v_plane, float* out, int n_q,
                                       int n_kv, int head_dim, int max_ctx, int n_keys, void* stream);
 
@@ -364,7 +381,11 @@ DQ_API int dq_model_create(const dq_model_desc* desc, dq_model** out);
 /* Enqueues one token on `stream`: x_in fp32 [hidden] (read), position pos
  * (0 <= pos < max_ctx; the cache must hold keys 0..pos-1), logits fp32 [vocab]
  * (written).  Writes this token's k and v into the cache at pos.  Calls on one
- * model must not overlap in time.  Errors: DQ_ERR_NULL, DQ_ERR_SHAPE, DQ_ERR_CUDA. */
+ * model must not overlap in time.  The fused token kernel's arguments depend only
+ * on this call's arguments (the kernel returns its grid-barrier counters to zero
+ * before it exits), so the call may be captured into a CUDA graph and the graph
+ * replayed, one replay at a time per model.
+ * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE, DQ_ERR_CUDA. */
 DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits, void* stream);
 
 /* Number of kernels one dq_decode_step launches. */
@@ -372,9 +393,26 @@ DQ_API int dq_model_launches_per_step(const dq_model* m);
 
 /* 1 when dq_decode_step runs the fused token kernel, 0 when it runs separate
  * kernels, DQ_ERR_NULL for a NULL handle.  A fused token whose device wait ran
- * out (dq_device_error reports a timeout) leaves the model's barrier counter
- * undefined: destroy and re-create the model after such an error. */
+ * out (dq_check_device returns DQ_ERR_TIMEOUT) has undefined logits and cache
+ * row, but the kernel still ends (its blocks stop working and pass the remaining
+ * barriers without waiting) and zeroes its barrier counters: the model stays
+ * usable, and the next token at that position rewrites the cache row. */
 DQ_API int dq_model_fused(const dq_model* m);
+
+/* Diagnostics for the fused token kernel's failure path.  wait_limit_ns bounds
+ * every wait of the model's later fused tokens (1e3 .. 6e10 ns; the default is
+ * 4e9).  barrier_skew > 0 makes the NEXT fused token's grid barriers wait for
+ * that many barriers more than the token has, a target no block can reach: every
+ * block's first barrier wait runs out after wait_limit_ns, the kernel records
+ * the timeout (bit 16) and ends.  The skew applies to one token only.
+ * Errors: DQ_ERR_NULL; DQ_ERR_SHAPE (limit or skew out of range, skew > 1000);
+ * DQ_ERR_UNSUPPORTED when the model does not run the fused kernel. */
+DQ_API int dq_model_debug_waits(dq_model* m, unsigned long long wait_limit_ns, int barrier_skew);
+
+/* Diagnostics: the next n workspace allocations of dq_model_create (in this
+ * process) fail as if the device were out of memory, so the caller sees
+ * DQ_ERR_ALLOC and no handle; n = 0 cancels.  Errors: DQ_ERR_SHAPE for n < 0. */
+DQ_API int dq_debug_fail_next_allocs(int n);
 
 /* Diagnostics for per-kernel timing: enqueues one of the token's kernels on
  * its own, launched as in the token (with programmatic dependent launch unless

@@ -92,4 +92,15 @@ DQ_API int dq_device_error(void* stream)
     return v;
 }
 
+DQ_API int dq_check_device(void* stream)
+{
+    const int v = dq_device_error(stream);
+    if (v < 0)
+        return v;
+    if (v == 0)
+        return DQ_OK;
+    // every bit but "bad argument seen on the device" records a wait that ran out
+    return (v & ~dq::DEVERR_BAD_ARG) ? DQ_ERR_TIMEOUT : DQ_ERR_SHAPE;
+}
+
 }  // extern "C"

@@ -181,41 +181,52 @@ DQ_API int dq_attention_decode_rope(const float* q, const float* k_new, void* k_
 
 // ------------------------------------------------- attention without allocation
 //
-// Some callers cannot call cudaMalloc: code that runs while a stream is being
-// captured into a CUDA graph under a capture mode that forbids allocation,
-// inference-server plugins whose host owns all device memory through its own
-// pool, and embedded or real-time deployments that fix their device memory at
-// start-up.  For them the attention scratch (the merge counters and the chunk
-// partials) lives in one file-scope device array, sized for up to
-// DQ_STATIC_ATT_MAX_Q query heads and DQ_STATIC_ATT_MAX_KV KV heads.  Every
-// device that loads this library holds the array until the process exits.
+// Some callers cannot call cudaMalloc: inference-server plugins whose host
+// process owns all device memory through its own pool, and embedded or
+// real-time deployments that fix their device memory at start-up.  For them
+// the attention scratch (the merge counters and the chunk partials) lives in
+// one file-scope device array, sized for up to DQ_STATIC_ATT_MAX_Q query heads
+// and DQ_STATIC_ATT_MAX_KV KV heads (include/dq.h).  Every device that loads
+// this library holds the array until the process exits.
 
 namespace {
 
-constexpr int STATIC_ATT_MAX_Q = 64;
-constexpr int STATIC_ATT_MAX_KV = 64;
+constexpr int STATIC_ATT_MAX_Q = DQ_STATIC_ATT_MAX_Q;
+constexpr int STATIC_ATT_MAX_KV = DQ_STATIC_ATT_MAX_KV;
+// one merge counter (an int) per KV head in the counter area
+static_assert(STATIC_ATT_MAX_KV <= dq::ATT_COUNTER_BYTES / 4, "a merge counter per KV head");
 constexpr size_t STATIC_ATT_BYTES =
     dq::ATT_COUNTER_BYTES + static_cast<size_t>(STATIC_ATT_MAX_Q) * dq::ATT_CHUNKS * dq::ATT_PART * sizeof(float);
+static_assert(STATIC_ATT_BYTES == 1081600, "the size the header states");
 
 static __device__ __align__(256) unsigned char g_static_att_scratch[STATIC_ATT_BYTES];
 
+constexpr int STATIC_ATT_MAX_DEVICES = 64;
+
 // Device address of the scratch array on the current device, looked up once
-// per device (with that device current); null if the lookup fails.
-void* static_att_scratch()
+// per device (with that device current) and kept for the process.  In host code
+// the array's name stands for a host-side shadow, never for the device memory,
+// so only this address may be handed to a kernel.  Returns DQ_OK, or
+// DQ_ERR_UNSUPPORTED for a device index beyond the table, or DQ_ERR_CUDA.
+int static_att_scratch(void** out)
 {
     static std::mutex mu;
-    static void* ptrs[64] = {};
+    static void* ptrs[STATIC_ATT_MAX_DEVICES] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return nullptr;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return dqhost::set_cuda_error(e);
+    if (dev < 0 || dev >= STATIC_ATT_MAX_DEVICES)
+        return DQ_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(mu);
     if (!ptrs[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_att_scratch) != cudaSuccess)
-            return nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_static_att_scratch)) != cudaSuccess)
+            return dqhost::set_cuda_error(e);
         ptrs[dev] = p;
     }
-    return ptrs[dev];
+    *out = ptrs[dev];
+    return DQ_OK;
 }
 
 }  // namespace
@@ -235,9 +246,10 @@ DQ_API int dq_attention_decode_static(const float* q, const void* k_plane, const
         return DQ_ERR_UNSUPPORTED;
     if (!dqhost::aligned16(q) || !dqhost::aligned16(k_plane) || !dqhost::aligned16(v_plane) || !dqhost::aligned16(out))
         return DQ_ERR_ALIGN;
-    void* scratch = static_att_scratch();
-    if (!scratch)
-        return dqhost::set_cuda_error(cudaGetLastError());
+    void* scratch = nullptr;
+    const int st = static_att_scratch(&scratch);
+    if (st != DQ_OK)
+        return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the merge counters must start at zero whatever an earlier call left behind
     cudaError_t e = cudaMemsetAsync(scratch, 0, dq::ATT_COUNTER_BYTES, s);

@@ -112,14 +112,16 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+// Wait for the phase with the given parity to complete; false once `limit_ns`
+// of wall time has passed without it.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = globaltimer_ns();
     while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
-        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS)
+        if (globaltimer_ns() - t0 > limit_ns)
             return false;
     }
     return true;

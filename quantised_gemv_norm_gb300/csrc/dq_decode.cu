@@ -20,6 +20,7 @@
 // Layout follows the Qwen3-8B census of "The roofline holds on a second GPU",
 // section "The Math"; the norm placement follows "one-serial-kernel", section
 // "One thread" (twice per layer and once at the end).
+#include <atomic>
 #include <new>
 #include <vector>
 
@@ -62,12 +63,15 @@ struct dq_model {
     void* attn_ws;
     float* k_new;       // Qwen3 attention inputs: the token's projected keys, else null
     float2* rope;       // (cos, sin) [max_ctx][hd / 2] when k_new is set
+    float* tk_k;        // fused kernel: tagged copies of the token's keys and values [n_kv hd]
+    float* tk_v;
     // fused token kernel
     bool fused;
     dqhost::TokenPlan tplan;
     dq::TokenLayer* layers_dev;
-    unsigned* bar;
-    unsigned bar_base;
+    unsigned* bar;                 // [0] barrier arrivals, [1] blocks finished (the kernel zeroes both)
+    unsigned long long wait_ns;    // bound on the fused kernel's waits
+    int bar_skew_next;             // diagnostics: extra barriers for the next fused token only
     // plans
     dqhost::GemvPlan p_qkv, p_o, p_gateup, p_down_q4, p_down_q6, p_vocab;
     bool have_down_q4, have_down_q6;
@@ -80,6 +84,9 @@ struct dq_model {
 };
 
 enum { K_QKV = 0, K_ATTN = 1, K_O = 2, K_GATEUP = 3, K_DOWN = 4, K_VOCAB = 5 };
+
+// Workspace allocations of dq_model_create still to fail on purpose (diagnostics).
+static std::atomic<int> g_fail_allocs{0};
 
 static cudaError_t launch_kernel(dq_model* m, int l, int kind, cudaStream_t s, bool pdl)
 {
@@ -301,10 +308,14 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
                  bf = up(sizeof(float) * d->ffn), bs = up(sizeof(dq::StepArgs)),
                  bw = up(dqhost::attention_workspace_bytes(d->n_q_heads, d->n_kv_heads)),
                  bl = up(sizeof(dq::TokenLayer) * d->n_layers), bb = 256,
-                 bk = qwen3 ? up(sizeof(float) * kvdim) : 0,
+                 bk = (qwen3 || m->fused) ? up(sizeof(float) * kvdim) : 0, bv = m->fused ? up(sizeof(float) * kvdim) : 0,
                  br = qwen3 ? up(sizeof(float2) * static_cast<size_t>(d->max_ctx) * (d->head_dim / 2)) : 0;
-    const size_t total = bx + bq + ba + bf + bs + bw + bl + bb + bk + br;
-    cudaError_t e = cudaMalloc(&m->ws, total);
+    const size_t total = bx + bq + ba + bf + bs + bw + bl + bb + bk + bv + br;
+    // diagnostics: an injected allocation failure (dq_debug_fail_next_allocs)
+    int inject = g_fail_allocs.load();
+    while (inject > 0 && !g_fail_allocs.compare_exchange_weak(inject, inject - 1)) {
+    }
+    cudaError_t e = inject > 0 ? cudaErrorMemoryAllocation : cudaMalloc(&m->ws, total);
     if (e != cudaSuccess) {
         cudaGetLastError();
         free_model(m);
@@ -319,10 +330,15 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
     m->attn_ws = base + bx + bq + ba + bf + bs;
     m->layers_dev = reinterpret_cast<dq::TokenLayer*>(base + bx + bq + ba + bf + bs + bw);
     m->bar = reinterpret_cast<unsigned*>(base + bx + bq + ba + bf + bs + bw + bl);
-    m->bar_base = 0;
+    m->wait_ns = dq::WAIT_LIMIT_NS;
+    char* kv_copies = base + bx + bq + ba + bf + bs + bw + bl + bb;
     if (qwen3) {
-        m->k_new = reinterpret_cast<float*>(base + bx + bq + ba + bf + bs + bw + bl + bb);
-        m->rope = reinterpret_cast<float2*>(base + bx + bq + ba + bf + bs + bw + bl + bb + bk);
+        m->k_new = reinterpret_cast<float*>(kv_copies);
+        m->rope = reinterpret_cast<float2*>(kv_copies + bk + bv);
+    }
+    if (m->fused) {  // the fused kernel's tagged copies of the token's keys and values
+        m->tk_k = reinterpret_cast<float*>(kv_copies);
+        m->tk_v = reinterpret_cast<float*>(kv_copies + bk);
     }
     if ((e = cudaMemset(m->ws, 0, total)) != cudaSuccess ||
         (qwen3 && (e = dqhost::launch_rope_table(m->rope, d->max_ctx, d->head_dim, d->rope_theta, 0)) != cudaSuccess)) {
@@ -405,11 +421,14 @@ DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits
         dqhost::attention_bind_workspace(t, m->attn_ws);
         a.part = t.part;
         a.counters = t.counters;
-        a.k_new = m->k_new;
+        a.k_new = m->tk_k;
+        a.v_new = m->tk_v;
+        a.qwen = m->k_new != nullptr;
         a.rope = m->rope;
         a.step = m->step;
         a.bar = m->bar;
-        a.bar_base = m->bar_base;
+        a.wait_ns = m->wait_ns;
+        a.bar_skew = m->bar_skew_next;
         a.x_in = x_in;
         a.logits = logits;
         a.pos = pos;
@@ -419,9 +438,7 @@ DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits
         cudaError_t e = dqhost::launch_token(m->tplan, a, s);
         if (e != cudaSuccess)
             return dqhost::set_cuda_error(e);
-        // every block arrives once at each barrier: nph - 1, less one per layer when the attention is folded
-        const int nbar = m->tplan.nph - 1 - (a.fold ? m->n_layers : 0);
-        m->bar_base += static_cast<unsigned>(nbar) * static_cast<unsigned>(m->tplan.grid);
+        m->bar_skew_next = 0;
         return DQ_OK;
     }
     const int threads = 256;
@@ -465,6 +482,27 @@ DQ_API int dq_model_buffer(const dq_model* m, int which, void** ptr)
     case 3: *ptr = m->act; return DQ_OK;
     default: return DQ_ERR_SHAPE;
     }
+}
+
+DQ_API int dq_model_debug_waits(dq_model* m, unsigned long long wait_limit_ns, int barrier_skew)
+{
+    if (!m)
+        return DQ_ERR_NULL;
+    if (wait_limit_ns < 1000ull || wait_limit_ns > 60000000000ull || barrier_skew < 0 || barrier_skew > 1000)
+        return DQ_ERR_SHAPE;
+    if (!m->fused)
+        return DQ_ERR_UNSUPPORTED;
+    m->wait_ns = wait_limit_ns;
+    m->bar_skew_next = barrier_skew;
+    return DQ_OK;
+}
+
+DQ_API int dq_debug_fail_next_allocs(int n)
+{
+    if (n < 0)
+        return DQ_ERR_SHAPE;
+    g_fail_allocs.store(n);
+    return DQ_OK;
 }
 
 DQ_API int dq_model_destroy(dq_model* m)

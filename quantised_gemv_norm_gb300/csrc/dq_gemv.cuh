@@ -470,6 +470,94 @@ __device__ __forceinline__ float quantise_block(float4 (&v)[NCH], const float4 (
     return ss;
 }
 
+// quantise_block with every chunk's steps interleaved (the shuffles of all
+// chunks in flight together, no early exit) and the scale reciprocal taken by
+// the fast divide (the group's largest element still maps to exactly +-16383;
+// the other values move by at most a few ulp of fp32, far below the rounding
+// step): the chain from the activation load to the stored units is one
+// shuffle-and-round latency, not NCH of them.
+template <int FMT, int PL, int NCH, int NT = NCONS>
+__device__ __forceinline__ float quantise_block_il(float4 (&v)[NCH], const float4 (&gv)[NCH], bool norm,
+                                                   uint32_t* xq, int K, int tid)
+{
+    float ss = 0.f;
+    const int nchunks = K / 4;
+    float am[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        float4 h = v[i];
+        if (norm) {
+            ss = fmaf(h.x, h.x, ss); ss = fmaf(h.y, h.y, ss); ss = fmaf(h.z, h.z, ss); ss = fmaf(h.w, h.w, ss);
+            h.x *= gv[i].x; h.y *= gv[i].y; h.z *= gv[i].z; h.w *= gv[i].w;
+            v[i] = h;
+        }
+        am[i] = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+        for (int i = 0; i < NCH; ++i)
+            am[i] = fmaxf(am[i], __shfl_xor_sync(0xffffffffu, am[i], o));
+    uint2 pk[NCH], pl[NCH];
+    int hs[NCH], hh[NCH], ls[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const float inv = am[i] > 0.f ? __fdividef(XQ_MAX, am[i]) : 0.f;
+        const float t0 = v[i].x * inv, t1 = v[i].y * inv, t2 = v[i].z * inv, t3 = v[i].w * inv;
+        const int a0 = round_small(t0), a1 = round_small(t1), a2 = round_small(t2), a3 = round_small(t3);
+        pk[i] = make_uint2(pack16x2(a0, a1), pack16x2(a2, a3));
+        hs[i] = (a0 + a1) + (a2 + a3);
+        ls[i] = 0;
+        if (PL == 2) {
+            const int b0 = round_small((t0 - static_cast<float>(a0)) * 32768.0f);
+            const int b1 = round_small((t1 - static_cast<float>(a1)) * 32768.0f);
+            const int b2 = round_small((t2 - static_cast<float>(a2)) * 32768.0f);
+            const int b3 = round_small((t3 - static_cast<float>(a3)) * 32768.0f);
+            pl[i] = make_uint2(pack16x2(b0, b1), pack16x2(b2, b3));
+            ls[i] = (b0 + b1) + (b2 + b3);
+        }
+    }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1)
+#pragma unroll
+        for (int i = 0; i < NCH; ++i)
+            hs[i] += __shfl_xor_sync(0xffffffffu, hs[i], o);
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        hh[i] = hs[i];  // this 16-element half
+        hs[i] += __shfl_xor_sync(0xffffffffu, hs[i], 4);
+    }
+    if (PL == 2) {
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < NCH; ++i)
+                ls[i] += __shfl_xor_sync(0xffffffffu, ls[i], o);
+    }
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int c = tid + NT * i;
+        if (c < nchunks) {
+            const int e = c & 7;
+            uint32_t* q = xq + (c >> 3) * xq_words(PL);
+            *reinterpret_cast<uint2*>(q + 2 * e) = pk[i];
+            if (PL == 2)
+                *reinterpret_cast<uint2*>(q + 16 + 2 * e) = pl[i];
+            float* meta = reinterpret_cast<float*>(q + 16 * PL);
+            const float sc = am[i] * (1.0f / XQ_MAX);
+            if (e == 0) {
+                meta[0] = sc;
+                meta[1] = sc * 0.0625f;
+                meta[2] = sc * (static_cast<float>(hs[i]) + static_cast<float>(ls[i]) * (1.0f / 32768.0f));
+                reinterpret_cast<int*>(meta)[3] = 32 * hh[i];
+            } else if (e == 4) {
+                reinterpret_cast<int*>(meta)[4] = 32 * hh[i];
+            }
+        }
+    }
+    return ss;
+}
+
 // One stage of the consumers: this thread's unit products for rows g, g + RG,
 // ... (RPT of them, each of NMAT matrices) of the tile, reduced over the warp
 // into wred[0 .. RPT NMAT) (the warp's partial sums; matrix m, row i at m RPT + i;

@@ -14,15 +14,33 @@
 // the whole token; "The Mountain Runs", section 3: one output per weight row).
 //
 // The consumers are those of the streaming GEMV kernel (dq_gemv.cuh): 512
-// threads in row groups of 128 for the K <= 4096 phases and one group of 512
-// for the down projection, each thread holding one 32-element unit of the
-// quantised activation in registers; stage t is completed by warp t % 16 two
-// stages later.  The attention phase runs one (key chunk, KV head) item per
-// block on the first n_q / n_kv warps (dq_attn.cuh).
+// threads in row groups, each thread holding its 32-element units of the
+// quantised activation in registers; tile t is completed (slot refilled, rows'
+// epilogue run) by warp t % 16 as soon as every warp has released it.  The
+// attention phase runs one (key chunk, KV head) item per block on the first
+// n_q / n_kv warps (dq_attn.cuh); contexts of at most TK_FOLD_KEYS keys fold it
+// into the O phase instead.
+//
+// Tagged activations.  A release fence before every barrier arrival (so that a
+// block's outputs are visible before it counts itself in) measured 0.5-1.3 us
+// per barrier: it waits for the block's outstanding stores under full HBM
+// load.  The barriers between the matrix phases therefore arrive without a
+// fence, and the vectors those phases pass on (the residual x, the SwiGLU
+// activation, q and the new key and value) carry their own validity instead:
+// every value is written with its lowest mantissa bit set to the parity of the
+// write (one fp32 ulp, far below the activation format's rounding), and a
+// reader re-reads any value whose bit does not show the write it waits for.
+// Each location alternates between consecutive writes, and a reader has always
+// seen the previous one (it read the whole vector before its own outputs fed
+// the writer), so one bit suffices.  The barriers around the attention phase,
+// whose cache rows and merge scratch are untagged, keep the release/acquire
+// pair.
 //
 // Every wait is bounded.  A block whose wait runs out records the error, stops
 // working and keeps arriving at the grid barriers without waiting, so the other
-// blocks finish the token (with meaningless output) instead of hanging.
+// blocks finish the token (with meaningless output) instead of hanging; the
+// last block out then puts the counters and the tagged vectors back into their
+// initial state, so the model stays usable.
 #include <algorithm>
 
 #include "dq_token.cuh"
@@ -31,6 +49,11 @@ namespace dq {
 
 constexpr int DEVERR_TIMEOUT_BARRIER = 16;
 
+// Words of the barrier area (TokenArgs::bar).
+constexpr int TB_ARRIVE = 0;  // grid-barrier arrivals of this launch
+constexpr int TB_EXIT = 1;    // blocks finished
+constexpr int TB_TOKEN = 2;   // tokens run since the tagged vectors were reset
+constexpr int TB_FAULT = 3;   // a block of this launch gave up a wait
 
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p)
 {
@@ -39,11 +62,45 @@ __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p)
     return v;
 }
 
-__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ float4 ld_relaxed_f4(const float* p)
+{
+    float4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_f32(float* p, float v)
+{
+    asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v)
 {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v)
+{
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// v with its lowest mantissa bit set to `par`.
+__device__ __forceinline__ float tagged(float v, uint32_t par)
+{
+    return __uint_as_float((__float_as_uint(v) & ~1u) | par);
+}
+
+// Whether all four values carry the tag `par`.
+__device__ __forceinline__ bool tags_ok(float4 v, uint32_t par)
+{
+    const uint32_t x = __float_as_uint(v.x) ^ par, y = __float_as_uint(v.y) ^ par, z = __float_as_uint(v.z) ^ par,
+                   w = __float_as_uint(v.w) ^ par;
+    return ((x | y | z | w) & 1u) == 0u;
 }
 
 // The block's shared memory (layout: dq_token.cuh).
@@ -57,6 +114,8 @@ struct TkMisc {
     int issued_hi;             // one past the highest tile issued
     int sync_ok;
     int ttotal;                // the block's tiles over the token
+    unsigned tokpar;           // parity of the token count (tags of vectors written once per layer)
+    int last_out;              // this block finished last
 };
 static_assert(sizeof(TkMisc) <= 256, "misc region");
 
@@ -70,6 +129,19 @@ __device__ __forceinline__ uint32_t* tk_xq() { return reinterpret_cast<uint32_t*
 __device__ __forceinline__ float* tk_red() { return reinterpret_cast<float*>(tk_smem + TK_OFF_RED); }
 __device__ __forceinline__ PhaseEnt* tk_ptab() { return reinterpret_cast<PhaseEnt*>(tk_smem + TK_OFF_PTAB); }
 
+// Tag of write `idx` (0-based within a token) of a vector written `per_token`
+// times a token.  The count runs on across tokens, so consecutive writes
+// alternate whatever the number of layers; the first write after a reset has
+// tag 1, and the reset state (all zero) tag 0.
+__device__ __forceinline__ uint32_t tk_par(int per_token, int idx)
+{
+    return (tk_misc().tokpar * static_cast<unsigned>(per_token) + static_cast<unsigned>(idx) + 1u) & 1u;
+}
+// The residual x is written twice per layer: by O (idx 2l) and by down (2l + 1).
+__device__ __forceinline__ uint32_t tk_par_x_o(int l) { return tk_par(2 * tk_args().n_layers, 2 * l); }
+__device__ __forceinline__ uint32_t tk_par_x_down(int l) { return tk_par(2 * tk_args().n_layers, 2 * l + 1); }
+// act, q and the new key and value: once per layer.
+__device__ __forceinline__ uint32_t tk_par_layer(int l) { return tk_par(tk_args().n_layers, l); }
 
 // Stream tile T (numbered over the token) into its ring slot.  `cur` is the
 // calling thread's cursor into the phase table (each thread issues tiles in
@@ -95,42 +167,6 @@ __device__ __forceinline__ void tk_issue(int T, int& cur)
     atomicMax(&m.issued_hi, T + 1);
 }
 
-// Grid barrier before phase p (p >= 1) on a monotonic arrival counter: the
-// block arrives, then waits until the counter reaches bar_base + p gridDim.x
-// (every block has arrived p times).  A dead block arrives without waiting.
-// Returns false when the block is (or has just become) dead.
-__device__ __forceinline__ void tk_trace(int p, int i);
-
-__device__ __forceinline__ bool tk_sync(int p)
-{
-    const TokenArgs& A = tk_args();
-    TkMisc& m = tk_misc();
-    __syncthreads();  // the block's phase outputs are written
-    if (threadIdx.x == 0) {
-        // barriers passed before this one: one per phase, minus the folded attention phases
-        const int nb = A.fold ? p - (p + 3) / 5 : p;
-        const unsigned target = A.bar_base + static_cast<unsigned>(nb) * gridDim.x;
-        int ok = *reinterpret_cast<volatile int*>(&m.dead) == 0;
-        tk_trace(p, 6);
-        red_release_add(A.bar, 1u);  // release, cumulative over the block's writes through bar.sync
-        if (ok && static_cast<int>(ld_relaxed_u32(A.bar) - target) < 0) {
-            const unsigned long long t0 = globaltimer_ns();
-            while (static_cast<int>(ld_relaxed_u32(A.bar) - target) < 0) {
-                if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-                    set_error(A.err, DEVERR_TIMEOUT_BARRIER);
-                    m.dead = 1;
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-        fence_acquire_gpu();  // the relaxed polls plus this fence acquire the other blocks' writes
-        m.sync_ok = ok;
-    }
-    __syncthreads();
-    return m.sync_ok != 0;
-}
-
 // Diagnostics: stamp i (0..7) of phase p of this block; even stamps are the global
 // timer (ns), odd ones the SM clock (cycles).
 __device__ __forceinline__ void tk_trace(int p, int i)
@@ -141,17 +177,130 @@ __device__ __forceinline__ void tk_trace(int p, int i)
             (i & 1) ? clock64() : globaltimer_ns();
 }
 
+// A wait of this block ran out: record it for the host and for the launch's
+// last block (which then resets the tagged vectors), and stop working.
+__device__ __forceinline__ void tk_give_up(int code)
+{
+    const TokenArgs& A = tk_args();
+    set_error(A.err, code);
+    atomicExch(A.bar + TB_FAULT, 1u);
+    tk_misc().dead = 1;
+}
+
+// Grid barrier before phase p (p >= 1) on an arrival counter that is zero when
+// the launch starts: the block arrives, then waits until the counter reaches
+// (barriers so far) x gridDim.x (every block has arrived that often).  With
+// `fenced` the arrival releases the block's writes and the wait acquires the
+// others' (the attention phase's untagged data); without, the data carries its
+// tags.  A dead block arrives without waiting.  Returns false when the block is
+// (or has just become) dead.
+__device__ __forceinline__ bool tk_sync(int p, bool fenced)
+{
+    const TokenArgs& A = tk_args();
+    TkMisc& m = tk_misc();
+    __syncthreads();  // the block's phase outputs are written
+    if (threadIdx.x == 0) {
+        // barriers passed before this one: one per phase, minus the folded attention phases
+        const int nb = A.fold ? p - (p + 3) / 5 : p;
+        const unsigned target = static_cast<unsigned>(nb + A.bar_skew) * gridDim.x;
+        int ok = *reinterpret_cast<volatile int*>(&m.dead) == 0;
+        tk_trace(p, 6);
+        if (fenced)
+            red_release_add(A.bar + TB_ARRIVE, 1u);  // cumulative over the block's writes through bar.sync
+        else
+            red_relaxed_add(A.bar + TB_ARRIVE, 1u);
+        if (ok && static_cast<int>(ld_relaxed_u32(A.bar + TB_ARRIVE) - target) < 0) {
+            const unsigned long long t0 = globaltimer_ns();
+            while (static_cast<int>(ld_relaxed_u32(A.bar + TB_ARRIVE) - target) < 0) {
+                if (globaltimer_ns() - t0 > A.wait_ns) {
+                    tk_give_up(DEVERR_TIMEOUT_BARRIER);
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        if (fenced)
+            fence_acq_rel_gpu();  // the relaxed polls plus this fence acquire the other blocks' writes
+        m.sync_ok = ok;
+    }
+    __syncthreads();
+    return m.sync_ok != 0;
+}
+
+// Load chunks c = tid + NT i (float4, c < nchunks) of a tagged vector, re-reading
+// those whose tags do not yet show `par`.  The loop is warp-uniform (the lanes
+// wait for each other, so later shuffles see converged warps).  False when the
+// wait ran out.
+template <int NCH, int NT>
+__device__ __forceinline__ bool tk_load_tagged(float4 (&v)[NCH], const float* x, int nchunks, int tid, uint32_t par)
+{
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int c = tid + NT * i;
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < nchunks)
+            v[i] = ld_relaxed_f4(x + 4 * c);
+    }
+    unsigned long long t0 = 0;
+    while (true) {
+        bool mine = true;
+#pragma unroll
+        for (int i = 0; i < NCH; ++i)
+            if (tid + NT * i < nchunks)
+                mine = mine && tags_ok(v[i], par);
+        if (__all_sync(0xffffffffu, mine))
+            return true;
+        const unsigned long long now = globaltimer_ns();
+        if (t0 == 0)
+            t0 = now;
+        else if (__any_sync(0xffffffffu, now - t0 > tk_args().wait_ns))
+            return false;
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            const int c = tid + NT * i;
+            if (c < nchunks && !tags_ok(v[i], par))
+                v[i] = ld_relaxed_f4(x + 4 * c);
+        }
+    }
+}
+
 // Attention for a short context (n_keys <= TK_FOLD_KEYS), computed by every
 // block at the start of the O phase of layer l and quantised straight into the
 // O projection's activation table: no attention phase and no barrier of its
-// own.  Warp w takes query heads w and w + 16 together (n_q <= 32), every load
-// of both issued before any arithmetic, so the fold costs one L2 round trip;
-// lane i holds dims 4i..4i+3.  With the Qwen3 inputs each block normalises and
+// own.  Warp w takes query heads w and w + 16 together (n_q <= 32); lane i
+// holds dims 4i..4i+3.  With the Qwen3 inputs each block normalises and
 // rotates q and the new key itself, and block 0 writes the key's fp16 row into
 // the cache (the other blocks use the same rounded values from registers).
 // Same arithmetic as attn_block.
+//
+// The head-norm weights and the rotary row do not depend on this token's q|k|v
+// phase, and their addresses take a load of their own: they are loaded before
+// the grid barrier (tk_fold_preload).  After it, one round trip brings q, the
+// new key and value (tagged copies of what the q|k|v phase wrote) and the
+// cache rows of the earlier positions.
+struct FoldPre {
+    NormRope qn, kn;
+};
+
+__device__ __forceinline__ void tk_fold_preload(int l, FoldPre& f)
+{
+    const TokenArgs& A = tk_args();
+    const int lane = threadIdx.x & 31;
+    if (A.qwen) {
+        const float2* cs = A.rope + static_cast<size_t>(A.pos) * (ATT_HD / 2);
+        f.qn = load_norm_rope(A.layers[l].q_norm, cs, lane);
+        f.kn = load_norm_rope(A.layers[l].k_norm, cs, lane);
+    }
+}
+
+__device__ __forceinline__ uint2 half4_bits(float4 v)
+{
+    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
+
 template <int PL>
-__device__ __forceinline__ void tk_fold_attention(int l)
+__device__ __forceinline__ bool tk_fold_attention(int l, const FoldPre& f)
 {
     const TokenArgs& A = tk_args();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -159,64 +308,83 @@ __device__ __forceinline__ void tk_fold_attention(int l)
     const size_t plane = static_cast<size_t>(A.n_kv) * A.max_ctx * A.hd;
     __half* kc = A.kv + static_cast<size_t>(l) * 2 * plane;
     const __half* vc = kc + plane;
-    const bool qwen = A.k_new != nullptr;
+    const uint32_t par = tk_par_layer(l);
     constexpr int NH = 2;  // heads per warp
-    NormRope qn{}, kn{};
-    if (qwen) {  // issued with the loads below: one round trip for everything
-        const float2* cs = A.rope + static_cast<size_t>(pos) * (ATT_HD / 2);
-        qn = load_norm_rope(A.layers[l].q_norm, cs, lane);
-        kn = load_norm_rope(A.layers[l].k_norm, cs, lane);
-    }
     bool on[NH];
     int hh[NH], gg[NH];
-    float4 q[NH], k[NH];
-    uint2 kr[NH][TK_FOLD_KEYS], vr[NH][TK_FOLD_KEYS];
+    float4 q[NH], k[NH], v[NH];
+    uint2 kr[NH][TK_FOLD_KEYS - 1], vr[NH][TK_FOLD_KEYS - 1];  // cache rows j < pos
 #pragma unroll
     for (int i = 0; i < NH; ++i) {
         hh[i] = warp + TK_WARPS * i;
         on[i] = hh[i] < A.n_q;
         gg[i] = on[i] ? hh[i] / group : 0;
         const size_t row0 = static_cast<size_t>(gg[i]) * A.max_ctx * ATT_HD;
-        q[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        k[i] = q[i];
+        q[i] = k[i] = v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (on[i]) {
-            q[i] = __ldcg(reinterpret_cast<const float4*>(A.q + static_cast<size_t>(hh[i]) * ATT_HD) + lane);
-            if (qwen)
-                k[i] = __ldcg(reinterpret_cast<const float4*>(A.k_new + static_cast<size_t>(gg[i]) * ATT_HD) + lane);
+            q[i] = ld_relaxed_f4(A.q + static_cast<size_t>(hh[i]) * ATT_HD + 4 * lane);
+            k[i] = ld_relaxed_f4(A.k_new + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
+            v[i] = ld_relaxed_f4(A.v_new + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
         }
 #pragma unroll
-        for (int j = 0; j < TK_FOLD_KEYS; ++j) {
+        for (int j = 0; j < TK_FOLD_KEYS - 1; ++j) {
             kr[i][j] = vr[i][j] = make_uint2(0u, 0u);
-            if (on[i] && j < n_keys) {
+            if (on[i] && j < pos) {
                 kr[i][j] = __ldcg(reinterpret_cast<const uint2*>(kc + row0 + static_cast<size_t>(j) * ATT_HD) + lane);
                 vr[i][j] = __ldcg(reinterpret_cast<const uint2*>(vc + row0 + static_cast<size_t>(j) * ATT_HD) + lane);
             }
         }
+    }
+    // the tagged values: re-read any that does not yet show this layer's write
+    unsigned long long t0 = 0;
+    while (true) {
+        bool mine = true;
+#pragma unroll
+        for (int i = 0; i < NH; ++i)
+            if (on[i])
+                mine = mine && tags_ok(q[i], par) && tags_ok(k[i], par) && tags_ok(v[i], par);
+        if (__all_sync(0xffffffffu, mine))
+            break;
+        const unsigned long long now = globaltimer_ns();
+        if (t0 == 0)
+            t0 = now;
+        else if (__any_sync(0xffffffffu, now - t0 > A.wait_ns))
+            return false;
+#pragma unroll
+        for (int i = 0; i < NH; ++i)
+            if (on[i]) {
+                if (!tags_ok(q[i], par))
+                    q[i] = ld_relaxed_f4(A.q + static_cast<size_t>(hh[i]) * ATT_HD + 4 * lane);
+                if (!tags_ok(k[i], par))
+                    k[i] = ld_relaxed_f4(A.k_new + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
+                if (!tags_ok(v[i], par))
+                    v[i] = ld_relaxed_f4(A.v_new + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
+            }
     }
     const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
 #pragma unroll
     for (int i = 0; i < NH; ++i) {
         if (!on[i])  // warp-uniform
             continue;
-        uint2 knew = make_uint2(0u, 0u);
         float4 qi = q[i];
-        if (qwen) {
-            qi = head_norm_rope(qi, qn, A.eps, lane);
-            const float4 kk = head_norm_rope(k[i], kn, A.eps, lane);
-            const __half2 k01 = __floats2half2_rn(kk.x, kk.y), k23 = __floats2half2_rn(kk.z, kk.w);
-            knew.x = *reinterpret_cast<const uint32_t*>(&k01);
-            knew.y = *reinterpret_cast<const uint32_t*>(&k23);
+        uint2 knew;  // the current position's key as the cache holds it (fp16)
+        if (A.qwen) {
+            qi = head_norm_rope(qi, f.qn, A.eps, lane);
+            knew = half4_bits(head_norm_rope(k[i], f.kn, A.eps, lane));
             if (blockIdx.x == 0 && hh[i] % group == 0)
                 *reinterpret_cast<uint2*>(kc + static_cast<size_t>(gg[i]) * A.max_ctx * ATT_HD +
                                           static_cast<size_t>(pos) * ATT_HD + 4 * lane) = knew;
+        } else {
+            knew = half4_bits(k[i]);  // the tagged copy of an fp16 value rounds back to it
         }
+        const uint2 vnew = half4_bits(v[i]);
         float sj[TK_FOLD_KEYS];
         float m = -INFINITY;
 #pragma unroll
         for (int j = 0; j < TK_FOLD_KEYS; ++j) {
             sj[j] = -INFINITY;
             if (j < n_keys) {
-                const uint2 kb = (qwen && j == pos) ? knew : kr[i][j];
+                const uint2 kb = j == pos ? knew : kr[i][j < TK_FOLD_KEYS - 1 ? j : 0];
                 const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(&kb.x));
                 const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(&kb.y));
                 float d = fmaf(qi.x, k0.x, qi.y * k0.y) + fmaf(qi.z, k1.x, qi.w * k1.y);
@@ -232,8 +400,9 @@ __device__ __forceinline__ void tk_fold_attention(int l)
             if (j < n_keys) {
                 const float pj = expf(sj[j] - m);
                 lsum += pj;
-                const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&vr[i][j].x));
-                const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&vr[i][j].y));
+                const uint2 vb = j == pos ? vnew : vr[i][j < TK_FOLD_KEYS - 1 ? j : 0];
+                const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&vb.x));
+                const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&vb.y));
                 o.x = fmaf(pj, v0.x, o.x); o.y = fmaf(pj, v0.y, o.y);
                 o.z = fmaf(pj, v1.x, o.z); o.w = fmaf(pj, v1.y, o.w);
             }
@@ -241,6 +410,7 @@ __device__ __forceinline__ void tk_fold_attention(int l)
         o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
         quantise_chunk<FMT_Q4K, PL>(o, hh[i] * (ATT_HD / 4) + lane, tk_xq());
     }
+    return true;
 }
 
 // One matrix phase p of kind KIND: prefetch the norm weight, pass the barrier,
@@ -266,11 +436,13 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
     const int r0 = ke.r0, r1 = ke.r1;
     TkMisc& m = tk_misc();
     const int l = p / 5;
-    const float* x0 = l == 0 ? A.x_in : A.x;  // the residual stream entering layer l
-    const float* x = KIND == PH_QKV ? x0 : KIND == PH_O ? A.attn : KIND == PH_GATEUP || KIND == PH_VOCAB ? A.x : A.act;
+    const bool fold = KIND == PH_O && A.fold;
     const float* gamma = KIND == PH_QKV ? A.layers[l].attn_norm : KIND == PH_GATEUP ? A.layers[l].ffn_norm : A.out_norm;
 
     tk_trace(p, 0);
+    FoldPre fpre;
+    if (fold)
+        tk_fold_preload(l, fpre);
     float4 gv[NCH];
 #pragma unroll
     for (int i = 0; i < NCH; ++i) {
@@ -279,29 +451,49 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
         if (NORM && ch < K / 4)
             gv[i] = __ldg(reinterpret_cast<const float4*>(gamma) + ch);
     }
-    if (p > 0 ? !tk_sync(p) : m.dead != 0)
+    // the O phase after a separate attention phase reads its untagged output
+    if (p > 0 ? !tk_sync(p, KIND == PH_O && !A.fold) : m.dead != 0)
         return make_int2(T, icur);
     tk_trace(p, 2);
     tk_trace(p, 3);
 
-    // the block's residual rows (at most TK_RESID_MAX < TK_THREADS): loaded now, stored
-    // after the activation's loads have gone out, so the two round trips overlap
+    // the block's residual rows (at most TK_RESID_MAX < TK_THREADS): its own
+    // outputs of the previous residual phase (x_in for layer 0's O), loaded now
+    // and stored after the activation's loads have gone out
     float rv = 0.f;
     if (EPI == EPI_RESID && tid < r1 - r0)
-        rv = __ldcg((KIND == PH_O ? x0 : A.x) + r0 + tid);
+        rv = __ldcg((KIND == PH_O && l == 0 ? A.x_in : A.x) + r0 + tid);
     float ss = 0.f;
-    if (KIND == PH_O && A.fold) {
-        tk_fold_attention<PL>(l);
+    bool ok = true;
+    if (fold) {
+        ok = tk_fold_attention<PL>(l, fpre);
     } else {
         float4 xv[NCH];
+        if (KIND == PH_QKV && l == 0) {  // the token's input: written before the launch
 #pragma unroll
-        for (int i = 0; i < NCH; ++i) {
-            const int ch = tid + TK_THREADS * i;
-            xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (ch < K / 4)
-                xv[i] = __ldcg(reinterpret_cast<const float4*>(x) + ch);
+            for (int i = 0; i < NCH; ++i) {
+                const int ch = tid + TK_THREADS * i;
+                xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (ch < K / 4)
+                    xv[i] = __ldcg(reinterpret_cast<const float4*>(A.x_in) + ch);
+            }
+        } else if (KIND == PH_O) {  // the attention phase's output, behind a fenced barrier
+#pragma unroll
+            for (int i = 0; i < NCH; ++i) {
+                const int ch = tid + TK_THREADS * i;
+                xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (ch < K / 4)
+                    xv[i] = __ldcg(reinterpret_cast<const float4*>(A.attn) + ch);
+            }
+        } else {
+            const bool from_act = KIND == PH_DOWN_Q4 || KIND == PH_DOWN_Q6;
+            // x after the O projection (gate/up), after the previous layer's down (q|k|v, vocabulary)
+            const uint32_t par = from_act ? tk_par_layer(l)
+                                 : KIND == PH_GATEUP ? tk_par_x_o(l)
+                                                     : tk_par_x_down(KIND == PH_VOCAB ? A.n_layers - 1 : l - 1);
+            ok = tk_load_tagged<NCH, TK_THREADS>(xv, from_act ? A.act : A.x, K / 4, tid, par);
         }
-        ss = quantise_block<FMT, PL, NCH, TK_THREADS>(xv, gv, NORM, tk_xq(), K, tid);
+        ss = quantise_block_il<FMT, PL, NCH, TK_THREADS>(xv, gv, NORM, tk_xq(), K, tid);
     }
     if (EPI == EPI_RESID && tid < r1 - r0)
         tk_resid()[tid] = rv;
@@ -310,14 +502,20 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
         if (lane == 0)
             m.gred[warp] = ss;
     }
+    if (!ok && lane == 0)
+        tk_give_up(DEVERR_TIMEOUT_BARRIER);
     __syncthreads();  // quantised activation, residual rows and norm partials complete
+    if (m.dead) {
+        tk_trace(p, 4);
+        return make_int2(T, icur);
+    }
     tk_trace(p, 5);
     float rstd = 1.f;
     if (NORM) {
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < TK_WARPS; ++w)
-            tot += m.gred[w];
+        const float4* g4 = reinterpret_cast<const float4*>(m.gred);
+        const float4 ga = g4[0], gb = g4[1], gc = g4[2], gd = g4[3];
+        const float tot = ((ga.x + ga.y) + (ga.z + ga.w)) + ((gb.x + gb.y) + (gb.z + gb.w)) +
+                          (((gc.x + gc.y) + (gc.z + gc.w)) + ((gd.x + gd.y) + (gd.z + gd.w)));
         rstd = rsqrtf(tot / static_cast<float>(K) + A.eps);
     }
     const int g = tid / P, pp = tid % P;
@@ -331,6 +529,9 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
     }
     load_units<FMT, PL, UL>(us, have, tk_xq(), pp, P, rstd);
     tk_trace(p, 7);
+
+    // tags of this phase's outputs
+    const uint32_t opar = EPI == EPI_RESID ? (KIND == PH_O ? tk_par_x_o(l) : tk_par_x_down(l)) : tk_par_layer(l);
 
     // Complete tile tc (token tile Tc) once every warp has released it: refill
     // its slot with tile Tc + TK_NSTAGE, run the epilogue of its rows.  Tile Tc
@@ -357,31 +558,34 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
             if (EPI == EPI_STORE) {
                 A.logits[r] = v0;
             } else if (EPI == EPI_RESID) {
-                A.x[r] = tk_resid()[r - r0] + v0;
+                st_relaxed_f32(A.x + r, tagged(tk_resid()[r - r0] + v0, opar));
             } else if (EPI == EPI_SWIGLU) {
-                A.act[r] = v0 / (1.0f + expf(-v0)) * v1;
-            } else {  // EPI_QKV: q rows, then k and v rows appended to the cache at pos
-                const int qdim = A.n_q * A.hd, kvdim = A.n_kv * A.hd;
+                st_relaxed_f32(A.act + r, tagged(v0 / (1.0f + expf(-v0)) * v1, opar));
+            } else {  // EPI_QKV: q rows; k and v rows to the cache at pos and as tagged fp32 copies
+                const int qdim = A.n_q * ATT_HD, kvdim = A.n_kv * ATT_HD;
                 if (r < qdim) {
-                    A.q[r] = v0;
+                    st_relaxed_f32(A.q + r, tagged(v0, opar));
                 } else {
                     const int idx = r - qdim;
-                    const int which = idx / kvdim, rem = idx - which * kvdim;
-                    const int kvh = rem / A.hd, dd = rem - kvh * A.hd;
-                    const size_t plane = static_cast<size_t>(A.n_kv) * A.max_ctx * A.hd;
-                    __half* kc = A.kv + static_cast<size_t>(l) * 2 * plane + (which ? plane : 0);
-                    if (!which && A.k_new)  // the attention normalises and rotates it first
-                        A.k_new[rem] = v0;
-                    else
-                        kc[(static_cast<size_t>(kvh) * A.max_ctx + A.pos) * A.hd + dd] = __float2half_rn(v0);
+                    const bool is_v = idx >= kvdim;
+                    const int rem = idx - (is_v ? kvdim : 0);
+                    const int kvh = rem / ATT_HD, dd = rem % ATT_HD;
+                    const size_t plane = static_cast<size_t>(A.n_kv) * A.max_ctx * ATT_HD;
+                    __half* kc = A.kv + static_cast<size_t>(l) * 2 * plane + (is_v ? plane : 0);
+                    const __half h = __float2half_rn(v0);
+                    if (is_v || !A.qwen)  // the Qwen3 key is normalised and rotated first (by the attention)
+                        kc[(static_cast<size_t>(kvh) * A.max_ctx + A.pos) * ATT_HD + dd] = h;
+                    // the fold reads these copies: the fp16 value (the projected key for Qwen3)
+                    const float copy = (is_v || !A.qwen) ? __half2float(h) : v0;
+                    st_relaxed_f32((is_v ? A.v_new : A.k_new) + rem, tagged(copy, opar));
                 }
             }
         }
     };
     auto released = [&](int Tc) { return mbar_test_wait(&m.empty[Tc & (TK_NSTAGE - 1)], (Tc / TK_NSTAGE) & 1); };
 
-    bool ok = true;
     int pend = -1;  // this warp's tile (phase-local index) still to complete
+#pragma unroll 1
     for (int t = 0; t < ntiles; ++t, ++T) {
         const int s = T & (TK_NSTAGE - 1);
         const uint32_t ph = (T / TK_NSTAGE) & 1;
@@ -395,7 +599,7 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
                 } else if (mbar_test_wait(&m.full[s], ph)) {
                     got = true;
                     break;
-                } else if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                } else if (globaltimer_ns() - t0 > A.wait_ns) {
                     set_error(A.err, DEVERR_TIMEOUT_EMPTY);
                     ok = false;
                     break;
@@ -406,7 +610,7 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
         } else if (pend >= 0) {
             got = true;
         }
-        if (!got && !mbar_wait(&m.full[s], ph)) {
+        if (!got && !mbar_wait(&m.full[s], ph, A.wait_ns)) {
             set_error(A.err, DEVERR_TIMEOUT_FULL);
             ok = false;
             break;
@@ -426,25 +630,28 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
         }
     }
     if (ok && pend >= 0) {  // the phase's epilogue must be done before the next barrier
-        if (mbar_wait(&m.empty[(T0 + pend) & (TK_NSTAGE - 1)], ((T0 + pend) / TK_NSTAGE) & 1))
+        if (mbar_wait(&m.empty[(T0 + pend) & (TK_NSTAGE - 1)], ((T0 + pend) / TK_NSTAGE) & 1, A.wait_ns))
             complete(pend, T0 + pend);
         else {
             set_error(A.err, DEVERR_TIMEOUT_EMPTY);
             ok = false;
         }
     }
-    if (!ok)
+    if (!ok) {
+        atomicExch(A.bar + TB_FAULT, 1u);
         m.dead = 1;
+    }
     tk_trace(p, 4);
     return make_int2(T0 + ntiles, icur);
 }
 
-// Attention phase p: items (key chunk, KV head) spread over the blocks.
+// Attention phase p: items (key chunk, KV head) spread over the blocks, between
+// two fenced barriers (the cache rows and the merge scratch carry no tags).
 __device__ __forceinline__ void tk_attention(int p)
 {
     const TokenArgs& A = tk_args();
     tk_trace(p, 0);
-    if (!tk_sync(p))
+    if (!tk_sync(p, true))
         return;
     tk_trace(p, 2);
     const int group = A.n_q / A.n_kv;
@@ -465,7 +672,7 @@ __device__ __forceinline__ void tk_attention(int p)
         t.n_keys = A.pos + 1;
         t.step = nullptr;
         t.err = A.err;
-        t.k_new = A.k_new;
+        t.k_new = A.qwen ? A.k_new : nullptr;
         t.q_norm = A.layers[l].q_norm;
         t.k_norm = A.layers[l].k_norm;
         t.rope = A.rope;
@@ -566,6 +773,9 @@ __global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_const
         fence_mbar_init();
         m.dead = 0;
         m.issued_hi = 0;
+        m.last_out = 0;
+        // written only by the previous launch's last block: the same value in every block
+        m.tokpar = ld_relaxed_u32(a.bar + TB_TOKEN) & 1u;
         for (int T = 0; T < min(TK_NSTAGE, m.ttotal); ++T)
             tk_issue(T, icur);
         if (blockIdx.x == 0) {
@@ -582,7 +792,7 @@ __global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_const
 #pragma unroll 1
     for (int l = 0; l < a.n_layers; ++l) {
         const int p = 5 * l;
-        st = tk_gemv<PH_QKV, FMT_Q4K, 2, 1, EPI_QKV, true>(p, st.x, st.y);
+        st = tk_gemv<PH_QKV, FMT_Q4K, 1, 1, EPI_QKV, true>(p, st.x, st.y);
         if (!a.fold)
             tk_attention(p + 1);
         st = tk_gemv<PH_O, FMT_Q4K, 1, 1, EPI_RESID, false>(p + 2, st.x, st.y);
@@ -605,6 +815,44 @@ __global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_const
                     set_error(a.err, DEVERR_TIMEOUT_DRAIN);
                     break;
                 }
+        }
+    }
+    // The last block to finish puts the barrier area back for the next launch:
+    // every block counts itself out only after its last barrier wait and its last
+    // write (dead blocks too), so nothing reads the counters or the tagged vectors
+    // any more.  The arrivals go back to zero and the token count advances (the
+    // tags of the next token follow from it), so a launch's arguments never
+    // depend on host-side state.  After a wait ran out somewhere, writes may be
+    // missing and the tags out of step: the tagged vectors and the token count go
+    // back to zero instead, the state before the first token.
+    if (tid == 0) {
+        fence_acq_rel_gpu();
+        m.last_out = atomicAdd(a.bar + TB_EXIT, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (m.last_out) {
+        fence_acq_rel_gpu();
+        const bool fault = ld_relaxed_u32(a.bar + TB_FAULT) != 0u;
+        if (fault) {
+            const int qdim = a.n_q * a.hd, kvdim = a.n_kv * a.hd;
+            for (int i = tid; i < a.hidden; i += TK_THREADS)
+                a.x[i] = 0.f;
+            for (int i = tid; i < a.ffn; i += TK_THREADS)
+                a.act[i] = 0.f;
+            for (int i = tid; i < qdim; i += TK_THREADS)
+                a.q[i] = 0.f;
+            for (int i = tid; i < kvdim; i += TK_THREADS) {
+                a.k_new[i] = 0.f;
+                a.v_new[i] = 0.f;
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned tok = ld_relaxed_u32(a.bar + TB_TOKEN);
+            atomicExch(a.bar + TB_TOKEN, fault ? 0u : tok + 1u);
+            atomicExch(a.bar + TB_FAULT, 0u);
+            atomicExch(a.bar + TB_ARRIVE, 0u);
+            atomicExch(a.bar + TB_EXIT, 0u);
         }
     }
 }

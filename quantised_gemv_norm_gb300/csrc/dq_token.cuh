@@ -61,11 +61,15 @@ struct TokenArgs {
     float* part;               // attention partials
     int* counters;             // attention merge counters (zero between phases)
     int fold;                  // 1: pos + 1 <= TK_FOLD_KEYS, the attention is folded into the O phase
-    float* k_new;              // Qwen3 attention inputs: the token's keys as projected [n_kv hd], else null
-    const float2* rope;        // (cos, sin) table [max_ctx][hd / 2] when k_new is set
+    float* k_new;              // the token's keys [n_kv hd], tagged: as projected (Qwen3) or their fp16 values
+    float* v_new;              // the token's values [n_kv hd], tagged fp16 values
+    int qwen;                  // Qwen3 attention inputs (per-head norms and rotation)
+    const float2* rope;        // (cos, sin) table [max_ctx][hd / 2] with the Qwen3 inputs
     StepArgs* step;            // pos and logits recorded for the diagnostics entry points
-    unsigned* bar;             // grid barrier arrival counter (monotonic)
-    unsigned bar_base;         // its value when this launch starts
+    unsigned* bar;             // [0] grid-barrier arrivals, [1] blocks finished; both 0 between launches
+    unsigned long long wait_ns;  // bound on every wait of the launch (wall-clock ns)
+    int bar_skew;              // diagnostics: barriers added to every target (0: none), so every wait runs out
+    int pad2;
     const float* x_in;
     float* logits;
     int pos;

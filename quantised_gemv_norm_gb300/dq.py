@@ -26,6 +26,9 @@ SIGNATURES = {
     "dq_status_string": (ctypes.c_char_p, [I]),
     "dq_last_cuda_error": (I, []),
     "dq_device_error": (I, [P]),
+    "dq_check_device": (I, [P]),
+    "dq_model_debug_waits": (I, [P, ctypes.c_ulonglong, I]),
+    "dq_debug_fail_next_allocs": (I, [I]),
     "dq_rmsnorm": (I, [P, P, P, I, I, F, P]),
     "dq_layernorm": (I, [P, P, P, P, I, I, F, P]),
     "dq_rmsnorm_threads": (I, [P, P, P, I, I, F, I, P]),

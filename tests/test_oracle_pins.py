@@ -599,31 +599,6 @@ def test_decode_ffn_path(orc):
     assert np.allclose(hid, x + Wd @ a, rtol=1e-12, atol=1e-9)
 
 
-# ------------------------------------------------ the tests' activation error model
-
-
-def test_decode_emulation_group_round():
-    import decode_emulation as emu
-
-    v = np.zeros(64)
-    v[0], v[1], v[2] = 2.0, 1.0, 1e-4
-    v[32:] = -3.0
-    r1 = emu.group_round(v, 1)
-    # the group max maps to +-16383 exactly; others round to multiples of s = 2/16383
-    step = 2.0 / 16383
-    assert r1[0] == 2.0
-    assert abs(r1[1] - 8192 * step) < 1e-15 and abs(r1[2] - step) < 1e-18  # 1e-4 / s = 0.82 -> 1
-    assert np.all(r1[32:] == -3.0)
-    r2 = emu.group_round(v, 2)
-    assert abs(r2[2] - 1e-4) <= 2.0 / 16383 / 65536
-    rng = np.random.default_rng(0)
-    w = rng.standard_normal(4096)
-    for planes, bound in ((1, 0.5 / 16383), (2, 0.5 / 16383 / 32768)):
-        err = np.abs(emu.group_round(w, planes) - w).reshape(-1, 32).max(axis=1)
-        amax = np.abs(w).reshape(-1, 32).max(axis=1)
-        assert np.all(err <= bound * amax * (1 + 1e-9))
-
-
 # ------------------------------------------------- Qwen3 attention inputs
 
 
