@@ -401,10 +401,12 @@ DQ_API int dq_model_fused(const dq_model* m);
 
 /* Diagnostics for the fused token kernel's failure path.  wait_limit_ns bounds
  * every wait of the model's later fused tokens (1e3 .. 6e10 ns; the default is
- * 4e9).  barrier_skew > 0 makes the NEXT fused token's grid barriers wait for
- * that many barriers more than the token has, a target no block can reach: every
- * block's first barrier wait runs out after wait_limit_ns, the kernel records
- * the timeout (bit 16) and ends.  The skew applies to one token only.
+ * 4e9).  barrier_skew > 0 makes the NEXT fused token wait for something that
+ * never comes: its blocks wait for a write of the activation that is never made,
+ * and its grid barriers (those around the attention phase) for that many
+ * barriers more than the token has.  Every block's first such wait runs out after
+ * wait_limit_ns, the kernel records the timeout (bit 16) and ends.  The skew
+ * applies to one token only.
  * Errors: DQ_ERR_NULL; DQ_ERR_SHAPE (limit or skew out of range, skew > 1000);
  * DQ_ERR_UNSUPPORTED when the model does not run the fused kernel. */
 DQ_API int dq_model_debug_waits(dq_model* m, unsigned long long wait_limit_ns, int barrier_skew);

@@ -44,13 +44,16 @@ constexpr int MM_BPS = 4;                      // Q4_K block columns per ring sl
 constexpr int MM_ROWB = MM_BPS * Q4K_BYTES + 16;  // 592: a slot row (4 blocks and 16 bytes of the next;
                                                   // the odd 16-byte stride keeps 8 rows on distinct banks)
 constexpr int MM_NS_MAX = 4;
+// operand (A in tensor memory, B in shared) buffers at most: 3 and 4 measured no
+// faster than 2 (the dequantising warps, not the MMAs' wait for operands, set the pace)
+constexpr int MM_NAB_MAX = 2;
 constexpr int MM_ACC = 4;                      // independent accumulators (MMA s of a stage adds into s % 4)
 constexpr int MM_TA_COLS = MM_KC / 2;          // columns of one A buffer (two fp16 per column)
-// Tensor memory: accumulator i in columns [i NT, (i + 1) NT), then the two A buffers.
+// Tensor memory: accumulator i in columns [i NT, (i + 1) NT), then the nab A buffers.
 __host__ __device__ constexpr int mm_ta_col(int nt) { return MM_ACC * nt; }
-__host__ __device__ constexpr uint32_t mm_tmem_cols(int nt)
+__host__ __device__ constexpr uint32_t mm_tmem_cols(int nt, int nab)
 {
-    return MM_ACC * nt + 2 * MM_TA_COLS <= 256 ? 256u : 512u;
+    return MM_ACC * nt + nab * MM_TA_COLS <= 256 ? 256u : 512u;
 }
 constexpr int MM_LBO = 128;                    // bytes between core matrices adjacent along K
 constexpr int MM_SBO = (MM_KC / 8) * 128;      // bytes between 8-row (8-token) groups
@@ -59,9 +62,9 @@ constexpr int DEVERR_TIMEOUT_MMA = 32;
 __host__ __device__ constexpr int mm_b_bytes(int nt) { return nt * MM_KC * 2; }
 // A ring slot: box_rows rows of MM_ROWB bytes, the slot start 128-byte aligned (tensor copy destination).
 __host__ __device__ constexpr int mm_slot_bytes(int box_rows) { return (box_rows * MM_ROWB + 127) / 128 * 128; }
-__host__ __device__ constexpr int mm_smem_bytes(int nt, int ns, int box_rows)
+__host__ __device__ constexpr int mm_smem_bytes(int nt, int ns, int nab, int box_rows)
 {
-    return ns * mm_slot_bytes(box_rows) + 2 * mm_b_bytes(nt) + 128;
+    return ns * mm_slot_bytes(box_rows) + nab * mm_b_bytes(nt) + 128;
 }
 
 struct MmArgs {
@@ -70,7 +73,8 @@ struct MmArgs {
     float* Y;          // [M][rows]
     int M, rows, K;
     int box_rows;      // rows one tensor copy brings (>= the rows of any tile of a block)
-    int ns;            // ring slots (2 or 4)
+    int ns;            // ring slots (2 .. 4)
+    int nab;           // operand buffers (2 .. 4): stages whose operands may be written ahead of the MMAs
     unsigned long long* trace;  // diagnostics: block 0's per-stage cycle stamps when not null
     int* err;
 };
@@ -120,10 +124,11 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
     const int slot_bytes = mm_slot_bytes(a.box_rows);
     uint8_t* ring = sm;
     uint8_t* Bbuf = sm + a.ns * slot_bytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(Bbuf + 2 * mm_b_bytes(NT));  // [MM_NS_MAX] slot landed
-    uint64_t* opready = full + MM_NS_MAX;                                     // [2] operands of a stage written
-    uint64_t* opfree = opready + 2;                                           // [2] a stage's MMAs done
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(opfree + 2);
+    const int nab = a.nab;
+    uint64_t* full = reinterpret_cast<uint64_t*>(Bbuf + nab * mm_b_bytes(NT));  // [MM_NS_MAX] slot landed
+    uint64_t* opready = full + MM_NS_MAX;                                       // [nab] operands of a stage written
+    uint64_t* opfree = opready + MM_NAB_MAX;                                    // [nab] a stage's MMAs done
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(opfree + MM_NAB_MAX);
     volatile int* fail = reinterpret_cast<volatile int*>(tslot + 1);
     int* issued = const_cast<int*>(fail) + 1;   // one past the last block column issued (over the block's tiles)
     int* committed = issued + 1;                // one past the last stage committed
@@ -137,11 +142,11 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
     const int nblk = a.K / 256;
 
     if (warp == 0)
-        tmem_alloc(tslot, mm_tmem_cols(NT));
+        tmem_alloc(tslot, mm_tmem_cols(NT, nab));
     if (tid == 0) {
         for (int s = 0; s < a.ns; ++s)
             mbar_init(&full[s], 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < nab; ++i) {
             mbar_init(&opready[i], MM_DQ_WARPS);
             mbar_init(&opfree[i], 1);
         }
@@ -193,8 +198,8 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                 for (int q = 0; q < min(a.ns, ngrp); ++q)
                     issue(q);
                 for (int hc = 0; hc < 2 * nblk; ++hc) {
-                    const int g = g0 + hc, buf = g & 1, c = hc >> 1;
-                    if (!(ok = wait(&opready[buf], (g >> 1) & 1, DEVERR_TIMEOUT_FULL)))
+                    const int g = g0 + hc, buf = g % nab, c = hc >> 1;
+                    if (!(ok = wait(&opready[buf], (g / nab) & 1, DEVERR_TIMEOUT_FULL)))
                         break;
                     unsigned long long* tr = (a.trace && b == 0 && hc < 32) ? a.trace + 8 * hc : nullptr;
                     if (tr)
@@ -252,7 +257,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
             bool ok = true;
             for (int hc = 0; hc < 2 * nblk; ++hc) {
                 const int c = hc >> 1, half = hc & 1;
-                const int g = g0 + hc, buf = g & 1;
+                const int g = g0 + hc, buf = g % nab;
                 const int bg = bg0 + c / MM_BPS;
                 unsigned long long* tr = (a.trace && b == 0 && tid == 0 && hc < 32) ? a.trace + 8 * hc : nullptr;
                 if (tr)
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                     break;
                 if (tr)
                     tr[3] = clock64();
-                if (g >= 2 && !(ok = warp_wait(&opfree[buf], ((g - 2) >> 1) & 1, DEVERR_TIMEOUT_MMA)))
+                if (g >= nab && !(ok = warp_wait(&opfree[buf], ((g - nab) / nab) & 1, DEVERR_TIMEOUT_MMA)))
                     break;
                 if (tr)
                     tr[4] = clock64();
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
             // accumulator complete -> Y (warps 0-3: one lane quarter each)
             if (warp < 4) {
                 const int glast = g0 + 2 * nblk - 1;
-                if (!warp_wait(&opfree[glast & 1], (glast >> 1) & 1, DEVERR_TIMEOUT_MMA))
+                if (!warp_wait(&opfree[glast % nab], (glast / nab) & 1, DEVERR_TIMEOUT_MMA))
                     break;
                 tc_fence_after_sync();
                 const int row = 32 * warp + lane;
@@ -377,9 +382,9 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
             while (!mbar_try_wait(&full[bg % a.ns], (bg / a.ns) & 1) && globaltimer_ns() - t0 < 100000000ull) {
             }
         }
-        for (int g = max(0, gc - 2); g < gc; ++g) {
+        for (int g = max(0, gc - nab); g < gc; ++g) {
             const unsigned long long t0 = globaltimer_ns();
-            while (!mbar_try_wait(&opfree[g & 1], (g >> 1) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+            while (!mbar_try_wait(&opfree[g % nab], (g / nab) & 1) && globaltimer_ns() - t0 < 100000000ull) {
             }
         }
     }
@@ -387,7 +392,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
     __syncthreads();
     if (warp == 0) {
         tc_fence_after_sync();
-        tmem_dealloc(tbase, mm_tmem_cols(NT));
+        tmem_dealloc(tbase, mm_tmem_cols(NT, nab));
     }
 }
 
@@ -444,9 +449,19 @@ static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, i
     a.box_rows = std::min(dq::MM_ROWS, per_block);
     a.err = device_error_flag();
     a.trace = gemv_trace();
-    // as many ring slots as fit (4, else 2)
-    a.ns = dq::mm_smem_bytes(nt, 4, a.box_rows) <= 227 * 1024 ? 4 : 2;
-    const int smem = dq::mm_smem_bytes(nt, a.ns, a.box_rows);
+    // the deepest operand pipeline, then as many ring slots, as shared memory holds
+    a.nab = 2;
+    a.ns = 2;
+    for (int nab = dq::MM_NAB_MAX; nab >= 2 && a.nab == 2; --nab)
+        for (int ns = dq::MM_NS_MAX; ns >= 2; --ns)
+            if (dq::mm_smem_bytes(nt, ns, nab, a.box_rows) <= 227 * 1024) {
+                a.nab = nab;
+                a.ns = ns;
+                break;
+            }
+    if (dq::mm_smem_bytes(nt, a.ns, a.nab, a.box_rows) > 227 * 1024)
+        return DQ_ERR_UNSUPPORTED;
+    const int smem = dq::mm_smem_bytes(nt, a.ns, a.nab, a.box_rows);
     const cuuint64_t row_bytes = static_cast<cuuint64_t>(K / 256) * dq::Q4K_BYTES;
     const cuuint64_t dims[2] = {row_bytes / 8, static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {row_bytes};

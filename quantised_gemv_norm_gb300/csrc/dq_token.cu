@@ -3,15 +3,15 @@
 // The token is the chain of phases of the per-kernel path (per layer: norm +
 // Q|K|V + cache append, attention, O + residual, norm + gate/up + SwiGLU,
 // down + residual; then norm + vocabulary), run by one block per SM that stays
-// resident for the whole token.  Phases are separated by grid barriers (every
-// phase reads the whole output of the one before), but the weight stream is
-// not: each block numbers the weight tiles of all its phases in one sequence
-// and refills its ring slots in that order, so the tiles of the next phase are
-// already in flight while the current phase finishes, the barrier resolves and
-// the next activation is quantised.  That removes the per-kernel start-up and
-// drain cost that dominates a chain of short launches ("The roofline holds on
-// a second GPU", section "Hiding, fusing...": keep the bytes in flight across
-// the whole token; "The Mountain Runs", section 3: one output per weight row).
+// resident for the whole token.  Every phase reads the whole output of the one
+// before, but the weight stream does not wait for it: each block numbers the
+// weight tiles of all its phases in one sequence and refills its ring slots in
+// that order, so the tiles of the next phase are already in flight while the
+// current phase finishes and the next activation arrives and is quantised.
+// That removes the per-kernel start-up and drain cost that dominates a chain
+// of short launches ("The roofline holds on a second GPU", section "Hiding,
+// fusing...": keep the bytes in flight across the whole token; "The Mountain
+// Runs", section 3: one output per weight row).
 //
 // The consumers are those of the streaming GEMV kernel (dq_gemv.cuh): 512
 // threads in row groups, each thread holding its 32-element units of the
@@ -21,26 +21,28 @@
 // n_q / n_kv warps (dq_attn.cuh); contexts of at most TK_FOLD_KEYS keys fold it
 // into the O phase instead.
 //
-// Tagged activations.  A release fence before every barrier arrival (so that a
-// block's outputs are visible before it counts itself in) measured 0.5-1.3 us
-// per barrier: it waits for the block's outstanding stores under full HBM
-// load.  The barriers between the matrix phases therefore arrive without a
-// fence, and the vectors those phases pass on (the residual x, the SwiGLU
-// activation, q and the new key and value) carry their own validity instead:
-// every value is written with its lowest mantissa bit set to the parity of the
-// write (one fp32 ulp, far below the activation format's rounding), and a
-// reader re-reads any value whose bit does not show the write it waits for.
-// Each location alternates between consecutive writes, and a reader has always
-// seen the previous one (it read the whole vector before its own outputs fed
-// the writer), so one bit suffices.  The barriers around the attention phase,
-// whose cache rows and merge scratch are untagged, keep the release/acquire
-// pair.
+// Tagged activations instead of grid barriers.  A grid barrier between two
+// phases cost 1.3-2.5 us: a release fence before each block's arrival (it waits
+// for the block's outstanding stores under full HBM load, 0.5-1.3 us), the
+// counter's round trips, then the activation's load.  The vectors the matrix
+// phases hand on (the residual x, the SwiGLU activation, q and fp32 copies of
+// the new key and value) carry their own validity instead: every value is
+// written with its lowest mantissa bit set to the parity of the write (one fp32
+// ulp, far below the activation format's rounding), and a reader loads the
+// vector straight away, re-reading values whose bit does not yet show the
+// write it waits for.  No barrier is needed between these phases: a phase reads
+// the whole vector the previous one wrote, so a block can only start writing a
+// vector again after every block has read its previous contents (those reads
+// came before the outputs it waited for), and each location alternates between
+// consecutive writes, so one bit tells them apart.  The attention phase, whose
+// cache rows and merge scratch are untagged, sits between two grid barriers
+// with release/acquire.
 //
 // Every wait is bounded.  A block whose wait runs out records the error, stops
-// working and keeps arriving at the grid barriers without waiting, so the other
-// blocks finish the token (with meaningless output) instead of hanging; the
-// last block out then puts the counters and the tagged vectors back into their
-// initial state, so the model stays usable.
+// working and keeps arriving at the grid barriers without waiting; blocks that
+// wait on its outputs run out in turn, so the token ends (with meaningless
+// output) instead of hanging.  The last block out then puts the counters and
+// the tagged vectors back into their initial state, so the model stays usable.
 #include <algorithm>
 
 #include "dq_token.cuh"
@@ -82,11 +84,6 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v)
 {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v)
-{
-    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // v with its lowest mantissa bit set to `par`.
@@ -187,28 +184,23 @@ __device__ __forceinline__ void tk_give_up(int code)
     tk_misc().dead = 1;
 }
 
-// Grid barrier before phase p (p >= 1) on an arrival counter that is zero when
-// the launch starts: the block arrives, then waits until the counter reaches
-// (barriers so far) x gridDim.x (every block has arrived that often).  With
-// `fenced` the arrival releases the block's writes and the wait acquires the
-// others' (the attention phase's untagged data); without, the data carries its
-// tags.  A dead block arrives without waiting.  Returns false when the block is
-// (or has just become) dead.
-__device__ __forceinline__ bool tk_sync(int p, bool fenced)
+// Grid barrier before the attention phase of layer l (p = 5 l + 1) or before
+// the O phase that follows it (p = 5 l + 2), on an arrival counter that is zero
+// when the launch starts: the block arrives (releasing its writes, ordered by
+// bar.sync), then waits until the counter reaches (barriers so far) x gridDim.x
+// and acquires the other blocks' writes.  A dead block arrives without waiting.
+// Returns false when the block is (or has just become) dead.
+__device__ __forceinline__ bool tk_sync(int p)
 {
     const TokenArgs& A = tk_args();
     TkMisc& m = tk_misc();
     __syncthreads();  // the block's phase outputs are written
     if (threadIdx.x == 0) {
-        // barriers passed before this one: one per phase, minus the folded attention phases
-        const int nb = A.fold ? p - (p + 3) / 5 : p;
+        const int nb = 2 * (p / 5) + (p % 5 == 1 ? 1 : 2);
         const unsigned target = static_cast<unsigned>(nb + A.bar_skew) * gridDim.x;
         int ok = *reinterpret_cast<volatile int*>(&m.dead) == 0;
         tk_trace(p, 6);
-        if (fenced)
-            red_release_add(A.bar + TB_ARRIVE, 1u);  // cumulative over the block's writes through bar.sync
-        else
-            red_relaxed_add(A.bar + TB_ARRIVE, 1u);
+        red_release_add(A.bar + TB_ARRIVE, 1u);
         if (ok && static_cast<int>(ld_relaxed_u32(A.bar + TB_ARRIVE) - target) < 0) {
             const unsigned long long t0 = globaltimer_ns();
             while (static_cast<int>(ld_relaxed_u32(A.bar + TB_ARRIVE) - target) < 0) {
@@ -219,8 +211,7 @@ __device__ __forceinline__ bool tk_sync(int p, bool fenced)
                 }
             }
         }
-        if (fenced)
-            fence_acq_rel_gpu();  // the relaxed polls plus this fence acquire the other blocks' writes
+        fence_acq_rel_gpu();  // the relaxed polls plus this fence acquire the other blocks' writes
         m.sync_ok = ok;
     }
     __syncthreads();
@@ -302,13 +293,22 @@ __device__ __forceinline__ uint2 half4_bits(float4 v)
 template <int PL>
 __device__ __forceinline__ bool tk_fold_attention(int l, const FoldPre& f)
 {
-    const TokenArgs& A = tk_args();
+    // the arguments in registers: the table stores below would otherwise make the
+    // compiler reload every field from shared memory inside the chain
+    const TokenArgs& A0 = tk_args();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int pos = A.pos, n_keys = pos + 1, group = A.n_q / A.n_kv;
-    const size_t plane = static_cast<size_t>(A.n_kv) * A.max_ctx * A.hd;
-    __half* kc = A.kv + static_cast<size_t>(l) * 2 * plane;
+    const int pos = A0.pos, n_keys = pos + 1, n_q = A0.n_q, group = n_q / A0.n_kv, max_ctx = A0.max_ctx;
+    const size_t plane = static_cast<size_t>(A0.n_kv) * max_ctx * ATT_HD;
+    __half* kc = A0.kv + static_cast<size_t>(l) * 2 * plane;
     const __half* vc = kc + plane;
-    const uint32_t par = tk_par_layer(l);
+    const float* Aq = A0.q;
+    const float* Ak = A0.k_new;
+    const float* Av = A0.v_new;
+    const bool qwen = A0.qwen != 0;
+    const float eps = A0.eps;
+    const unsigned long long wait_ns = A0.wait_ns;
+    const uint32_t par = tk_par_layer(l) ^ (A0.bar_skew != 0 ? 1u : 0u);  // a skew: a write that never comes
+    uint32_t* xq = tk_xq();
     constexpr int NH = 2;  // heads per warp
     bool on[NH];
     int hh[NH], gg[NH];
@@ -317,14 +317,14 @@ __device__ __forceinline__ bool tk_fold_attention(int l, const FoldPre& f)
 #pragma unroll
     for (int i = 0; i < NH; ++i) {
         hh[i] = warp + TK_WARPS * i;
-        on[i] = hh[i] < A.n_q;
+        on[i] = hh[i] < n_q;
         gg[i] = on[i] ? hh[i] / group : 0;
-        const size_t row0 = static_cast<size_t>(gg[i]) * A.max_ctx * ATT_HD;
+        const size_t row0 = static_cast<size_t>(gg[i]) * max_ctx * ATT_HD;
         q[i] = k[i] = v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (on[i]) {
-            q[i] = ld_relaxed_f4(A.q + static_cast<size_t>(hh[i]) * ATT_HD + 4 * lane);
-            k[i] = ld_relaxed_f4(A.k_new + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
-            v[i] = ld_relaxed_f4(A.v_new + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
+            q[i] = ld_relaxed_f4(Aq + static_cast<size_t>(hh[i]) * ATT_HD + 4 * lane);
+            k[i] = ld_relaxed_f4(Ak + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
+            v[i] = ld_relaxed_f4(Av + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
         }
 #pragma unroll
         for (int j = 0; j < TK_FOLD_KEYS - 1; ++j) {
@@ -348,17 +348,17 @@ __device__ __forceinline__ bool tk_fold_attention(int l, const FoldPre& f)
         const unsigned long long now = globaltimer_ns();
         if (t0 == 0)
             t0 = now;
-        else if (__any_sync(0xffffffffu, now - t0 > A.wait_ns))
+        else if (__any_sync(0xffffffffu, now - t0 > wait_ns))
             return false;
 #pragma unroll
         for (int i = 0; i < NH; ++i)
             if (on[i]) {
                 if (!tags_ok(q[i], par))
-                    q[i] = ld_relaxed_f4(A.q + static_cast<size_t>(hh[i]) * ATT_HD + 4 * lane);
+                    q[i] = ld_relaxed_f4(Aq + static_cast<size_t>(hh[i]) * ATT_HD + 4 * lane);
                 if (!tags_ok(k[i], par))
-                    k[i] = ld_relaxed_f4(A.k_new + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
+                    k[i] = ld_relaxed_f4(Ak + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
                 if (!tags_ok(v[i], par))
-                    v[i] = ld_relaxed_f4(A.v_new + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
+                    v[i] = ld_relaxed_f4(Av + static_cast<size_t>(gg[i]) * ATT_HD + 4 * lane);
             }
     }
     const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
@@ -368,11 +368,11 @@ __device__ __forceinline__ bool tk_fold_attention(int l, const FoldPre& f)
             continue;
         float4 qi = q[i];
         uint2 knew;  // the current position's key as the cache holds it (fp16)
-        if (A.qwen) {
-            qi = head_norm_rope(qi, f.qn, A.eps, lane);
-            knew = half4_bits(head_norm_rope(k[i], f.kn, A.eps, lane));
+        if (qwen) {
+            qi = head_norm_rope(qi, f.qn, eps, lane);
+            knew = half4_bits(head_norm_rope(k[i], f.kn, eps, lane));
             if (blockIdx.x == 0 && hh[i] % group == 0)
-                *reinterpret_cast<uint2*>(kc + static_cast<size_t>(gg[i]) * A.max_ctx * ATT_HD +
+                *reinterpret_cast<uint2*>(kc + static_cast<size_t>(gg[i]) * max_ctx * ATT_HD +
                                           static_cast<size_t>(pos) * ATT_HD + 4 * lane) = knew;
         } else {
             knew = half4_bits(k[i]);  // the tagged copy of an fp16 value rounds back to it
@@ -408,7 +408,7 @@ __device__ __forceinline__ bool tk_fold_attention(int l, const FoldPre& f)
             }
         const float inv = 1.0f / lsum;
         o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-        quantise_chunk<FMT_Q4K, PL>(o, hh[i] * (ATT_HD / 4) + lane, tk_xq());
+        quantise_chunk<FMT_Q4K, PL>(o, hh[i] * (ATT_HD / 4) + lane, xq);
     }
     return true;
 }
@@ -451,9 +451,32 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
         if (NORM && ch < K / 4)
             gv[i] = __ldg(reinterpret_cast<const float4*>(gamma) + ch);
     }
-    // the O phase after a separate attention phase reads its untagged output
-    if (p > 0 ? !tk_sync(p, KIND == PH_O && !A.fold) : m.dead != 0)
-        return make_int2(T, icur);
+    // What the prologue reads, taken from the argument table before the barrier
+    // (after it, every table read would sit in the prologue's dependency chain):
+    // the input vector, whether it carries tags and which, the residual rows.
+    const bool from_act = KIND == PH_DOWN_Q4 || KIND == PH_DOWN_Q6;
+    const bool untagged_in = (KIND == PH_QKV && l == 0) || KIND == PH_O;  // x_in, or attn behind a grid barrier
+    const float* xsrc = KIND == PH_QKV && l == 0 ? A.x_in : KIND == PH_O ? A.attn : from_act ? A.act : A.x;
+    // x after the O projection (gate/up), after the previous layer's down (q|k|v, vocabulary)
+    const uint32_t ipar = from_act ? tk_par_layer(l)
+                          : KIND == PH_GATEUP ? tk_par_x_o(l)
+                                              : tk_par_x_down(KIND == PH_VOCAB ? A.n_layers - 1 : l - 1);
+    const float* rsrc = (KIND == PH_O && l == 0 ? A.x_in : A.x) + r0;
+    // diagnostics: with a barrier skew every tagged read waits for a write that never comes
+    const uint32_t ipar_w = ipar ^ (A.bar_skew != 0 ? 1u : 0u);
+    const float eps = A.eps;
+    // the O phase after a separate attention phase reads its untagged output behind
+    // a grid barrier; the other phases read tagged vectors and need none (the block's
+    // own warps finish the previous phase's epilogue first: the prologue reuses its
+    // shared memory)
+    if (KIND == PH_O && !fold) {
+        if (!tk_sync(p))
+            return make_int2(T, icur);
+    } else {
+        __syncthreads();
+        if (m.dead)
+            return make_int2(T, icur);
+    }
     tk_trace(p, 2);
     tk_trace(p, 3);
 
@@ -462,36 +485,23 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
     // and stored after the activation's loads have gone out
     float rv = 0.f;
     if (EPI == EPI_RESID && tid < r1 - r0)
-        rv = __ldcg((KIND == PH_O && l == 0 ? A.x_in : A.x) + r0 + tid);
+        rv = __ldcg(rsrc + tid);
     float ss = 0.f;
     bool ok = true;
     if (fold) {
         ok = tk_fold_attention<PL>(l, fpre);
     } else {
         float4 xv[NCH];
-        if (KIND == PH_QKV && l == 0) {  // the token's input: written before the launch
+        if (untagged_in) {  // the token's input (written before the launch), or attn behind a grid barrier
 #pragma unroll
             for (int i = 0; i < NCH; ++i) {
                 const int ch = tid + TK_THREADS * i;
                 xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (ch < K / 4)
-                    xv[i] = __ldcg(reinterpret_cast<const float4*>(A.x_in) + ch);
-            }
-        } else if (KIND == PH_O) {  // the attention phase's output, behind a fenced barrier
-#pragma unroll
-            for (int i = 0; i < NCH; ++i) {
-                const int ch = tid + TK_THREADS * i;
-                xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (ch < K / 4)
-                    xv[i] = __ldcg(reinterpret_cast<const float4*>(A.attn) + ch);
+                    xv[i] = __ldcg(reinterpret_cast<const float4*>(xsrc) + ch);
             }
         } else {
-            const bool from_act = KIND == PH_DOWN_Q4 || KIND == PH_DOWN_Q6;
-            // x after the O projection (gate/up), after the previous layer's down (q|k|v, vocabulary)
-            const uint32_t par = from_act ? tk_par_layer(l)
-                                 : KIND == PH_GATEUP ? tk_par_x_o(l)
-                                                     : tk_par_x_down(KIND == PH_VOCAB ? A.n_layers - 1 : l - 1);
-            ok = tk_load_tagged<NCH, TK_THREADS>(xv, from_act ? A.act : A.x, K / 4, tid, par);
+            ok = tk_load_tagged<NCH, TK_THREADS>(xv, xsrc, K / 4, tid, ipar_w);
         }
         ss = quantise_block_il<FMT, PL, NCH, TK_THREADS>(xv, gv, NORM, tk_xq(), K, tid);
     }
@@ -516,7 +526,7 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
         const float4 ga = g4[0], gb = g4[1], gc = g4[2], gd = g4[3];
         const float tot = ((ga.x + ga.y) + (ga.z + ga.w)) + ((gb.x + gb.y) + (gb.z + gb.w)) +
                           (((gc.x + gc.y) + (gc.z + gc.w)) + ((gd.x + gd.y) + (gd.z + gd.w)));
-        rstd = rsqrtf(tot / static_cast<float>(K) + A.eps);
+        rstd = rsqrtf(tot / static_cast<float>(K) + eps);
     }
     const int g = tid / P, pp = tid % P;
     UnitState<FMT, PL> us[UL];
@@ -646,12 +656,12 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
 }
 
 // Attention phase p: items (key chunk, KV head) spread over the blocks, between
-// two fenced barriers (the cache rows and the merge scratch carry no tags).
+// two grid barriers (the cache rows and the merge scratch carry no tags).
 __device__ __forceinline__ void tk_attention(int p)
 {
     const TokenArgs& A = tk_args();
     tk_trace(p, 0);
-    if (!tk_sync(p, true))
+    if (!tk_sync(p))
         return;
     tk_trace(p, 2);
     const int group = A.n_q / A.n_kv;
