@@ -95,8 +95,8 @@ DQ_API int dq_last_cuda_error(void);
 /* Synchronises `stream`, then reads and clears the current device's error flag:
  * 0 if no kernel gave up a bounded wait since the last call, else a bit mask
  * (1 consumer timeout, 2 producer timeout, 4 copies in flight at exit,
- * 8 bad argument seen on the device, 16 grid-barrier timeout in the fused
- * token kernel, 32 tensor-core completion timeout).  Returns DQ_ERR_CUDA on a
+ * 8 bad argument seen on the device, 16 a fused-token wait for another
+ * block's output ran out, 32 tensor-core completion timeout).  Returns DQ_ERR_CUDA on a
  * CUDA error. */
 DQ_API int dq_device_error(void* stream);
 
@@ -177,10 +177,10 @@ DQ_API int dq_gemv_q2k(const void* W_blocks, const float* x, float* y, int rows,
  * dq_decode_step that runs the fused token kernel writes instead 8 values per
  * block and phase at buffer[8 (block * phases + phase)] (phases = 5 n_layers
  * + 1: per layer Q|K|V, attention, O, gate/up, down; then the vocabulary):
- * global-timer ns at [0] phase entered, [6] this block's barrier arrival,
- * [2] grid barrier passed, [4] phase done; SM clock cycles at [3] barrier passed, [5] activation quantised,
- * [7] activation in registers, [1] first weight tile ready; 64 bytes per
- * block and phase.  A tensor-core dq_matmul_q4k_path writes, for
+ * global-timer ns at [0] phase entered, [2] the block's warps done with the
+ * previous phase, [4] phase done; SM clock cycles at [3] the same moment as
+ * [2], [5] activation arrived and quantised, [7] activation in registers, [1]
+ * first weight tile ready; [6] unused; 64 bytes per block and phase.  A tensor-core dq_matmul_q4k_path writes, for
  * block 0 and its first 32 half-block stages, 8 SM clock stamps per stage at
  * buffer[8 stage]: operands seen ready and MMAs issued (control thread), stage
  * start, weights landed, operand buffer free and stage written (thread 0).
@@ -358,7 +358,8 @@ typedef struct {
 #define DQ_MODEL_FUSED 2
 
 /* Validates the description, allocates the workspace (activations, attention
- * scratch, barrier counter) and prepares the token on the current device.
+ * scratch, the fused kernel's launch state) and prepares the token on the
+ * current device.
  *
  * Two ways to run a token.  By default it is 5 n_layers + 1 kernels chained
  * by programmatic dependent launch, captured once in a CUDA graph when
@@ -366,12 +367,15 @@ typedef struct {
  * layers; hidden and n_q head_dim at most 4096, hidden a multiple of 2048;
  * ffn at most 12288 with a Q6_K down projection (a multiple of 2048), else as
  * far as the block's shared memory allows), it is
- * one cooperative launch of one block per SM that runs all phases with grid
- * barriers between them while the weights stream through each block's ring
- * without a break; for contexts of at most 4 keys (pos <= 3) it skips the
+ * one cooperative launch of one block per SM that runs all phases while the
+ * weights stream through each block's ring without a break; a phase starts on
+ * each block as soon as the vector it reads is complete (every value carries a
+ * tag of the write that made it, in its lowest mantissa bit: the activation
+ * buffers of a fused model differ from the computed values by at most that one
+ * fp32 ulp).  For contexts of at most 4 keys (pos <= 3) it skips the
  * attention phase and every block computes the attention at the start of
- * the O phase (the model buffer of the attention output, dq_model_buffer 2,
- * is then not written).  With the Qwen3 inputs the workspace also holds the
+ * the O phase (and writes it to the model buffer of the attention output,
+ * dq_model_buffer 2, one block per head).  With the Qwen3 inputs the workspace also holds the
  * rotary table (max_ctx x 512 bytes), computed here.  Host call;
  * synchronises the device.  *out receives the handle (NULL on error).
  * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE, DQ_ERR_ALIGN, DQ_ERR_UNSUPPORTED,
@@ -382,9 +386,10 @@ DQ_API int dq_model_create(const dq_model_desc* desc, dq_model** out);
  * (0 <= pos < max_ctx; the cache must hold keys 0..pos-1), logits fp32 [vocab]
  * (written).  Writes this token's k and v into the cache at pos.  Calls on one
  * model must not overlap in time.  The fused token kernel's arguments depend only
- * on this call's arguments (the kernel returns its grid-barrier counters to zero
- * before it exits), so the call may be captured into a CUDA graph and the graph
- * replayed, one replay at a time per model.
+ * on this call's arguments (its launch state lives in the model's workspace and
+ * the kernel's last block puts it back before it exits), so the call may be
+ * captured into a CUDA graph and the graph replayed, one replay at a time per
+ * model.
  * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE, DQ_ERR_CUDA. */
 DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits, void* stream);
 
@@ -394,22 +399,22 @@ DQ_API int dq_model_launches_per_step(const dq_model* m);
 /* 1 when dq_decode_step runs the fused token kernel, 0 when it runs separate
  * kernels, DQ_ERR_NULL for a NULL handle.  A fused token whose device wait ran
  * out (dq_check_device returns DQ_ERR_TIMEOUT) has undefined logits and cache
- * row, but the kernel still ends (its blocks stop working and pass the remaining
- * barriers without waiting) and zeroes its barrier counters: the model stays
- * usable, and the next token at that position rewrites the cache row. */
+ * row, but the kernel still ends (its blocks stop working; blocks waiting on
+ * their outputs run out in turn) and its last block resets the launch state
+ * and the tagged activation buffers: the model stays usable, and the next token
+ * at that position rewrites the cache row. */
 DQ_API int dq_model_fused(const dq_model* m);
 
 /* Diagnostics for the fused token kernel's failure path.  wait_limit_ns bounds
  * every wait of the model's later fused tokens (1e3 .. 6e10 ns; the default is
- * 4e9).  barrier_skew > 0 makes the NEXT fused token wait for something that
- * never comes: its blocks wait for a write of the activation that is never made,
- * and its grid barriers (those around the attention phase) for that many
- * barriers more than the token has.  Every block's first such wait runs out after
+ * 4e9).  skew > 0 makes the NEXT fused token wait for something that never
+ * comes: every read of an activation another block writes waits for a write
+ * that is never made.  Every block's first such wait runs out after
  * wait_limit_ns, the kernel records the timeout (bit 16) and ends.  The skew
  * applies to one token only.
- * Errors: DQ_ERR_NULL; DQ_ERR_SHAPE (limit or skew out of range, skew > 1000);
+ * Errors: DQ_ERR_NULL; DQ_ERR_SHAPE (limit out of range, skew < 0 or > 1000);
  * DQ_ERR_UNSUPPORTED when the model does not run the fused kernel. */
-DQ_API int dq_model_debug_waits(dq_model* m, unsigned long long wait_limit_ns, int barrier_skew);
+DQ_API int dq_model_debug_waits(dq_model* m, unsigned long long wait_limit_ns, int skew);
 
 /* Diagnostics: the next n workspace allocations of dq_model_create (in this
  * process) fail as if the device were out of memory, so the caller sees

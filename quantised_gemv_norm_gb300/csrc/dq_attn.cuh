@@ -30,7 +30,70 @@ struct AttnArgs {
     const float* k_norm;   // [128] RMSNorm weight shared by the key heads
     const float2* rope;    // [max_ctx][64] (cos, sin) of pos / theta^(2i / 128)
     float eps;
+    // Tagged mode (the fused token kernel; tag = 1 + parity): q, k_new and v_new carry
+    // the write parity in their lowest mantissa bit and are re-read until they do;
+    // the block whose chunk holds the token's position writes that position's fp16
+    // key and value rows into the cache from k_new (the Qwen3 key, or the key's fp16
+    // value) and v_new (the value's fp16 value); the output is stored with the same
+    // tag; the merge counters are not reset but count on from ctr_base (the launch
+    // zeroes them at its end).  tag = 0 (a zero-initialised AttnArgs): the plain mode.
+    int tag;
+    int ctr_base;
+    const float* v_new;            // [n_kv][128] tagged mode
+    unsigned long long wait_ns;    // tagged mode: bound on the tag waits
 };
+
+__device__ __forceinline__ float4 att_ld_relaxed_f4(const float* p)
+{
+    float4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ bool att_tags_ok(float4 v, uint32_t par)
+{
+    const uint32_t x = __float_as_uint(v.x) ^ par, y = __float_as_uint(v.y) ^ par, z = __float_as_uint(v.z) ^ par,
+                   w = __float_as_uint(v.w) ^ par;
+    return ((x | y | z | w) & 1u) == 0u;
+}
+
+// Load a float4 of a tagged vector, re-reading until its tags show `par`; the
+// loop is warp-uniform.  False when `limit_ns` ran out.
+__device__ __forceinline__ bool att_load_tagged(float4& v, const float* p, uint32_t par, unsigned long long limit_ns)
+{
+    v = att_ld_relaxed_f4(p);
+    unsigned long long t0 = 0;
+    while (!__all_sync(0xffffffffu, att_tags_ok(v, par))) {
+        const unsigned long long now = globaltimer_ns();
+        if (t0 == 0)
+            t0 = now;
+        else if (__any_sync(0xffffffffu, now - t0 > limit_ns))
+            return false;
+        if (!att_tags_ok(v, par))
+            v = att_ld_relaxed_f4(p);
+    }
+    return true;
+}
+
+__device__ __forceinline__ float att_tagged(float v, uint32_t par)
+{
+    return __uint_as_float((__float_as_uint(v) & ~1u) | par);
+}
+
+__device__ __forceinline__ void att_st_out(float* p, float4 v, int tag)
+{
+    if (tag == 0) {
+        *reinterpret_cast<float4*>(p) = v;
+    } else {
+        const uint32_t par = static_cast<uint32_t>(tag - 1) & 1u;
+        asm volatile("st.relaxed.gpu.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(att_tagged(v.x, par)),
+                     "f"(att_tagged(v.y, par)), "f"(att_tagged(v.z, par)), "f"(att_tagged(v.w, par))
+                     : "memory");
+    }
+}
 
 constexpr int ATT_BAR = 15;  // named barrier id of the attention warps
 
@@ -84,8 +147,9 @@ __device__ __forceinline__ float4 head_norm_rope(float4 v, const NormRope& nr, f
 // Block (c, g) of the decode attention, run by `group` warps of the calling
 // block (threads tbase .. tbase + 32 group - 1, synchronised by named barrier
 // bar), with `sm` (AttnSmem) as shared staging.  Used by the standalone kernel
-// and by the fused token kernel (two items at a time there).
-__device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int group, AttnSmem& sm, bool pdl,
+// and by the fused token kernel (two items at a time there, tagged mode).
+// Returns false when a tagged-mode wait ran out (nothing further is written).
+__device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int group, AttnSmem& sm, bool pdl,
                                            int bar = ATT_BAR, int tbase = 0)
 {
     auto& ks = sm.ks;
@@ -104,34 +168,54 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
     if (n_keys < 1 || n_keys > a.max_ctx) {
         if (tid == 0 && c == 0)
             set_error(a.err, DEVERR_BAD_ARG);
-        return;
+        return true;
     }
     if (j0 >= n_keys)
-        return;
+        return true;
 
     const int h = g * group + warp;
+    const bool tagged = a.tag != 0;
+    const uint32_t par = static_cast<uint32_t>(a.tag - 1) & 1u;
     const __half* kbase = a.kc + static_cast<size_t>(g) * a.max_ctx * ATT_HD;
+    const int pos = n_keys - 1;
+    bool ok = true;  // tagged mode: every wait of this thread ended in time
     {
-        float4 v = __ldcg(reinterpret_cast<const float4*>(a.q + static_cast<size_t>(h) * ATT_HD) + lane);
-        if (a.k_new) {
-            const int pos = n_keys - 1;
-            const float2* cs = a.rope + static_cast<size_t>(pos) * (ATT_HD / 2);
-            const NormRope qn = load_norm_rope(a.q_norm, cs, lane);
-            if (c == nact - 1 && warp == 0) {
-                // the block whose chunk holds pos finalises the token's key before
-                // staging it (the batch loop's first barrier orders the store)
-                const NormRope kn = load_norm_rope(a.k_norm, cs, lane);
-                float4 k = __ldcg(reinterpret_cast<const float4*>(a.k_new + static_cast<size_t>(g) * ATT_HD) + lane);
-                k = head_norm_rope(k, kn, a.eps, lane);
-                const __half2 k01 = __floats2half2_rn(k.x, k.y), k23 = __floats2half2_rn(k.z, k.w);
-                uint2 u;
-                u.x = *reinterpret_cast<const uint32_t*>(&k01);
-                u.y = *reinterpret_cast<const uint32_t*>(&k23);
-                *reinterpret_cast<uint2*>(const_cast<__half*>(kbase) + static_cast<size_t>(pos) * ATT_HD + 4 * lane) = u;
-                __threadfence_block();
+        float4 v;
+        if (tagged)
+            ok = att_load_tagged(v, a.q + static_cast<size_t>(h) * ATT_HD + 4 * lane, par, a.wait_ns);
+        else
+            v = __ldcg(reinterpret_cast<const float4*>(a.q + static_cast<size_t>(h) * ATT_HD) + lane);
+        const float2* cs = a.rope + static_cast<size_t>(pos) * (ATT_HD / 2);
+        if (c == nact - 1 && warp == 0 && (a.k_new || tagged)) {
+            // the block whose chunk holds pos writes that position's key (the Qwen3 key
+            // normalised and rotated) -- and in tagged mode its value -- before staging
+            // them (the batch loop's first barrier orders the stores)
+            float4 k = make_float4(0.f, 0.f, 0.f, 0.f), vv = k;
+            if (tagged) {
+                ok = att_load_tagged(k, a.k_new + static_cast<size_t>(g) * ATT_HD + 4 * lane, par, a.wait_ns) && ok;
+                ok = att_load_tagged(vv, a.v_new + static_cast<size_t>(g) * ATT_HD + 4 * lane, par, a.wait_ns) && ok;
+            } else {
+                k = __ldcg(reinterpret_cast<const float4*>(a.k_new + static_cast<size_t>(g) * ATT_HD) + lane);
             }
-            v = head_norm_rope(v, qn, a.eps, lane);
+            if (a.q_norm)  // Qwen3 inputs
+                k = head_norm_rope(k, load_norm_rope(a.k_norm, cs, lane), a.eps, lane);
+            const __half2 k01 = __floats2half2_rn(k.x, k.y), k23 = __floats2half2_rn(k.z, k.w);
+            uint2 u;
+            u.x = *reinterpret_cast<const uint32_t*>(&k01);
+            u.y = *reinterpret_cast<const uint32_t*>(&k23);
+            *reinterpret_cast<uint2*>(const_cast<__half*>(kbase) + static_cast<size_t>(pos) * ATT_HD + 4 * lane) = u;
+            if (tagged) {
+                const __half2 v01 = __floats2half2_rn(vv.x, vv.y), v23 = __floats2half2_rn(vv.z, vv.w);
+                uint2 w;
+                w.x = *reinterpret_cast<const uint32_t*>(&v01);
+                w.y = *reinterpret_cast<const uint32_t*>(&v23);
+                *reinterpret_cast<uint2*>(const_cast<__half*>(a.vc) + (static_cast<size_t>(g) * a.max_ctx + pos) * ATT_HD +
+                                          4 * lane) = w;
+            }
+            __threadfence_block();
         }
+        if (a.q_norm)
+            v = head_norm_rope(v, load_norm_rope(a.q_norm, cs, lane), a.eps, lane);
         *reinterpret_cast<float4*>(&qs[warp][4 * lane]) = v;
     }
     const __half* vbase = a.vc + static_cast<size_t>(g) * a.max_ctx * ATT_HD;
@@ -141,7 +225,14 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
     float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
     for (int jb = j0; jb < j1; jb += ATT_BATCH) {
         const int nb = min(ATT_BATCH, j1 - jb);
-        named_bar_sync(bar, nthr);  // previous batch fully consumed (and qs written on the first)
+        // previous batch fully consumed (and qs written on the first); on the first, in
+        // tagged mode, the item's warps also learn together whether any wait ran out
+        if (tagged && jb == j0) {
+            if (named_bar_red_or(bar, nthr, !ok))
+                return false;
+        } else {
+            named_bar_sync(bar, nthr);
+        }
         for (int idx = tid; idx < nb * (ATT_HD / 8); idx += nthr) {
             const int j = idx >> 4, ch = idx & 15;
             const uint4 kv = __ldcg(reinterpret_cast<const uint4*>(kbase + static_cast<size_t>(jb + j) * ATT_HD) + ch);
@@ -188,9 +279,9 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
 
     if (nact == 1) {  // the only block of this KV head: normalise and write directly
         const float inv = 1.0f / l;
-        *reinterpret_cast<float4*>(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane) =
-            make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv);
-        return;
+        att_st_out(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane, make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv),
+                   a.tag);
+        return true;
     }
     float* pp = a.part + (static_cast<size_t>(h) * ATT_CHUNKS + c) * ATT_PART;
     if (lane == 0) {
@@ -201,10 +292,10 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
     __threadfence();
     named_bar_sync(bar, nthr);
     if (tid == 0)
-        sm.last = (atomicAdd(&a.counters[g], 1) == nact - 1);
+        sm.last = (atomicAdd(&a.counters[g], 1) == (tagged ? a.ctr_base : 0) + nact - 1);
     named_bar_sync(bar, nthr);
     if (!sm.last)
-        return;
+        return true;
     __threadfence();
     // merge the chunk partials of this warp's head
     const float* hp = a.part + static_cast<size_t>(h) * ATT_CHUNKS * ATT_PART;
@@ -220,11 +311,14 @@ __device__ __forceinline__ void attn_block(const AttnArgs& a, int c, int g, int 
         r2 = fmaf(ov.z, w, r2); r3 = fmaf(ov.w, w, r3);
     }
     const float inv = 1.0f / Ls;
-    *reinterpret_cast<float4*>(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane) =
-        make_float4(r0 * inv, r1 * inv, r2 * inv, r3 * inv);
-    named_bar_sync(bar, nthr);
-    if (tid == 0)
-        a.counters[g] = 0;
+    att_st_out(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane, make_float4(r0 * inv, r1 * inv, r2 * inv, r3 * inv),
+               a.tag);
+    if (!tagged) {  // tagged mode: the counters count on across layers; the launch zeroes them at its end
+        named_bar_sync(bar, nthr);
+        if (tid == 0)
+            a.counters[g] = 0;
+    }
+    return true;
 }
 
 

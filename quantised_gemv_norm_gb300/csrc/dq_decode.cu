@@ -69,9 +69,9 @@ struct dq_model {
     bool fused;
     dqhost::TokenPlan tplan;
     dq::TokenLayer* layers_dev;
-    unsigned* bar;                 // [0] barrier arrivals, [1] blocks finished (the kernel zeroes both)
+    unsigned* bar;                 // fused kernel launch state (blocks out, token count, fault; the kernel keeps it)
     unsigned long long wait_ns;    // bound on the fused kernel's waits
-    int bar_skew_next;             // diagnostics: extra barriers for the next fused token only
+    int skew_next;                 // diagnostics: the next fused token waits for writes never made
     // plans
     dqhost::GemvPlan p_qkv, p_o, p_gateup, p_down_q4, p_down_q6, p_vocab;
     bool have_down_q4, have_down_q6;
@@ -428,7 +428,7 @@ DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits
         a.step = m->step;
         a.bar = m->bar;
         a.wait_ns = m->wait_ns;
-        a.bar_skew = m->bar_skew_next;
+        a.skew = m->skew_next;
         a.x_in = x_in;
         a.logits = logits;
         a.pos = pos;
@@ -438,7 +438,7 @@ DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits
         cudaError_t e = dqhost::launch_token(m->tplan, a, s);
         if (e != cudaSuccess)
             return dqhost::set_cuda_error(e);
-        m->bar_skew_next = 0;
+        m->skew_next = 0;
         return DQ_OK;
     }
     const int threads = 256;
@@ -484,16 +484,16 @@ DQ_API int dq_model_buffer(const dq_model* m, int which, void** ptr)
     }
 }
 
-DQ_API int dq_model_debug_waits(dq_model* m, unsigned long long wait_limit_ns, int barrier_skew)
+DQ_API int dq_model_debug_waits(dq_model* m, unsigned long long wait_limit_ns, int skew)
 {
     if (!m)
         return DQ_ERR_NULL;
-    if (wait_limit_ns < 1000ull || wait_limit_ns > 60000000000ull || barrier_skew < 0 || barrier_skew > 1000)
+    if (wait_limit_ns < 1000ull || wait_limit_ns > 60000000000ull || skew < 0 || skew > 1000)
         return DQ_ERR_SHAPE;
     if (!m->fused)
         return DQ_ERR_UNSUPPORTED;
     m->wait_ns = wait_limit_ns;
-    m->bar_skew_next = barrier_skew;
+    m->skew_next = skew;
     return DQ_OK;
 }
 

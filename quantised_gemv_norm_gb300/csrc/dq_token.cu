@@ -24,35 +24,36 @@
 // Tagged activations instead of grid barriers.  A grid barrier between two
 // phases cost 1.3-2.5 us: a release fence before each block's arrival (it waits
 // for the block's outstanding stores under full HBM load, 0.5-1.3 us), the
-// counter's round trips, then the activation's load.  The vectors the matrix
-// phases hand on (the residual x, the SwiGLU activation, q and fp32 copies of
-// the new key and value) carry their own validity instead: every value is
-// written with its lowest mantissa bit set to the parity of the write (one fp32
-// ulp, far below the activation format's rounding), and a reader loads the
-// vector straight away, re-reading values whose bit does not yet show the
-// write it waits for.  No barrier is needed between these phases: a phase reads
-// the whole vector the previous one wrote, so a block can only start writing a
-// vector again after every block has read its previous contents (those reads
-// came before the outputs it waited for), and each location alternates between
-// consecutive writes, so one bit tells them apart.  The attention phase, whose
-// cache rows and merge scratch are untagged, sits between two grid barriers
-// with release/acquire.
+// counter's round trips, then the activation's load.  The vectors the phases
+// hand on (the residual x, the attention output, the SwiGLU activation, q and
+// fp32 copies of the new key and value) carry their own validity instead: every
+// value is written with its lowest mantissa bit set to the parity of the write
+// (one fp32 ulp, far below the activation format's rounding), and a reader
+// loads the vector straight away, re-reading values whose bit does not yet show
+// the write it waits for.  No grid barrier is needed: a phase reads the whole
+// vector the previous one wrote, so a block can only start writing a vector
+// again after every block has read its previous contents (those reads came
+// before the outputs it waited for), and each location alternates between
+// consecutive writes, so one bit tells them apart.  The cache rows of the
+// token's position are written, from the tagged copies, by the block that
+// stages them for the attention (one block per KV head when the attention is
+// folded), and the
+// attention's merge counters count on across the layers of a token.
 //
-// Every wait is bounded.  A block whose wait runs out records the error, stops
-// working and keeps arriving at the grid barriers without waiting; blocks that
-// wait on its outputs run out in turn, so the token ends (with meaningless
-// output) instead of hanging.  The last block out then puts the counters and
-// the tagged vectors back into their initial state, so the model stays usable.
+// Every wait is bounded.  A block whose wait runs out records the error and
+// stops working; blocks that wait on its outputs run out in turn, so the token
+// ends (with meaningless output) instead of hanging.  The last block out then
+// puts the counters and the tagged vectors back into their initial state, so
+// the model stays usable.
 #include <algorithm>
 
 #include "dq_token.cuh"
 
 namespace dq {
 
-constexpr int DEVERR_TIMEOUT_BARRIER = 16;
+constexpr int DEVERR_TIMEOUT_TAG = 16;  // a wait for another block's output ran out
 
-// Words of the barrier area (TokenArgs::bar).
-constexpr int TB_ARRIVE = 0;  // grid-barrier arrivals of this launch
+// Words of the launch-state area (TokenArgs::bar; word 0 unused).
 constexpr int TB_EXIT = 1;    // blocks finished
 constexpr int TB_TOKEN = 2;   // tokens run since the tagged vectors were reset
 constexpr int TB_FAULT = 3;   // a block of this launch gave up a wait
@@ -80,11 +81,6 @@ __device__ __forceinline__ void st_relaxed_f32(float* p, float v)
 }
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v)
-{
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 // v with its lowest mantissa bit set to `par`.
 __device__ __forceinline__ float tagged(float v, uint32_t par)
@@ -184,40 +180,6 @@ __device__ __forceinline__ void tk_give_up(int code)
     tk_misc().dead = 1;
 }
 
-// Grid barrier before the attention phase of layer l (p = 5 l + 1) or before
-// the O phase that follows it (p = 5 l + 2), on an arrival counter that is zero
-// when the launch starts: the block arrives (releasing its writes, ordered by
-// bar.sync), then waits until the counter reaches (barriers so far) x gridDim.x
-// and acquires the other blocks' writes.  A dead block arrives without waiting.
-// Returns false when the block is (or has just become) dead.
-__device__ __forceinline__ bool tk_sync(int p)
-{
-    const TokenArgs& A = tk_args();
-    TkMisc& m = tk_misc();
-    __syncthreads();  // the block's phase outputs are written
-    if (threadIdx.x == 0) {
-        const int nb = 2 * (p / 5) + (p % 5 == 1 ? 1 : 2);
-        const unsigned target = static_cast<unsigned>(nb + A.bar_skew) * gridDim.x;
-        int ok = *reinterpret_cast<volatile int*>(&m.dead) == 0;
-        tk_trace(p, 6);
-        red_release_add(A.bar + TB_ARRIVE, 1u);
-        if (ok && static_cast<int>(ld_relaxed_u32(A.bar + TB_ARRIVE) - target) < 0) {
-            const unsigned long long t0 = globaltimer_ns();
-            while (static_cast<int>(ld_relaxed_u32(A.bar + TB_ARRIVE) - target) < 0) {
-                if (globaltimer_ns() - t0 > A.wait_ns) {
-                    tk_give_up(DEVERR_TIMEOUT_BARRIER);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-        fence_acq_rel_gpu();  // the relaxed polls plus this fence acquire the other blocks' writes
-        m.sync_ok = ok;
-    }
-    __syncthreads();
-    return m.sync_ok != 0;
-}
-
 // Load chunks c = tid + NT i (float4, c < nchunks) of a tagged vector, re-reading
 // those whose tags do not yet show `par`.  The loop is warp-uniform (the lanes
 // wait for each other, so later shuffles see converged warps).  False when the
@@ -257,16 +219,16 @@ __device__ __forceinline__ bool tk_load_tagged(float4 (&v)[NCH], const float* x,
 
 // Attention for a short context (n_keys <= TK_FOLD_KEYS), computed by every
 // block at the start of the O phase of layer l and quantised straight into the
-// O projection's activation table: no attention phase and no barrier of its
-// own.  Warp w takes query heads w and w + 16 together (n_q <= 32); lane i
+// O projection's activation table: no attention phase of its own.  Warp w takes query heads w and w + 16 together (n_q <= 32); lane i
 // holds dims 4i..4i+3.  With the Qwen3 inputs each block normalises and
-// rotates q and the new key itself, and block 0 writes the key's fp16 row into
-// the cache (the other blocks use the same rounded values from registers).
+// rotates q and the new key itself; one block per head writes the head's output
+// and, for a group's first head, the key's and value's fp16 rows into the cache
+// (the other blocks use the same rounded values from registers).
 // Same arithmetic as attn_block.
 //
 // The head-norm weights and the rotary row do not depend on this token's q|k|v
 // phase, and their addresses take a load of their own: they are loaded before
-// the grid barrier (tk_fold_preload).  After it, one round trip brings q, the
+// the phase's block barrier (tk_fold_preload).  After it, one round trip brings q, the
 // new key and value (tagged copies of what the q|k|v phase wrote) and the
 // cache rows of the earlier positions.
 struct FoldPre {
@@ -307,7 +269,9 @@ __device__ __forceinline__ bool tk_fold_attention(int l, const FoldPre& f)
     const bool qwen = A0.qwen != 0;
     const float eps = A0.eps;
     const unsigned long long wait_ns = A0.wait_ns;
-    const uint32_t par = tk_par_layer(l) ^ (A0.bar_skew != 0 ? 1u : 0u);  // a skew: a write that never comes
+    const uint32_t opar_att = tk_par_layer(l);
+    const uint32_t par = opar_att ^ (A0.skew != 0 ? 1u : 0u);  // a skew: a write that never comes
+    float* Aatt = A0.attn;
     uint32_t* xq = tk_xq();
     constexpr int NH = 2;  // heads per warp
     bool on[NH];
@@ -371,13 +335,18 @@ __device__ __forceinline__ bool tk_fold_attention(int l, const FoldPre& f)
         if (qwen) {
             qi = head_norm_rope(qi, f.qn, eps, lane);
             knew = half4_bits(head_norm_rope(k[i], f.kn, eps, lane));
-            if (blockIdx.x == 0 && hh[i] % group == 0)
-                *reinterpret_cast<uint2*>(kc + static_cast<size_t>(gg[i]) * max_ctx * ATT_HD +
-                                          static_cast<size_t>(pos) * ATT_HD + 4 * lane) = knew;
         } else {
             knew = half4_bits(k[i]);  // the tagged copy of an fp16 value rounds back to it
         }
         const uint2 vnew = half4_bits(v[i]);
+        // head h's output (and, for a group's first head, the position's cache rows) is
+        // written by block h % blocks: one block each, spread so no block runs late
+        const bool writer = blockIdx.x == hh[i] % gridDim.x;
+        if (writer && hh[i] % group == 0) {
+            const size_t at = (static_cast<size_t>(gg[i]) * max_ctx + pos) * ATT_HD + 4 * lane;
+            *reinterpret_cast<uint2*>(kc + at) = knew;
+            *reinterpret_cast<uint2*>(const_cast<__half*>(vc) + at) = vnew;
+        }
         float sj[TK_FOLD_KEYS];
         float m = -INFINITY;
 #pragma unroll
@@ -409,12 +378,14 @@ __device__ __forceinline__ bool tk_fold_attention(int l, const FoldPre& f)
         const float inv = 1.0f / lsum;
         o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
         quantise_chunk<FMT_Q4K, PL>(o, hh[i] * (ATT_HD / 4) + lane, xq);
+        if (writer)  // the attention output too (its tags then alternate every layer)
+            att_st_out(Aatt + static_cast<size_t>(hh[i]) * ATT_HD + 4 * lane, o, 1 + static_cast<int>(opar_att));
     }
     return true;
 }
 
-// One matrix phase p of kind KIND: prefetch the norm weight, pass the barrier,
-// quantise the activation, consume the phase's tiles and complete them (refill
+// One matrix phase p of kind KIND: prefetch the norm weight, load the tagged
+// activation as it arrives, quantise it, consume the phase's tiles and complete them (refill
 // + epilogue).  T is the block's next tile, icur the caller's issue cursor;
 // returns both advanced.
 template <int KIND, int FMT, int PL, int NMAT, int EPI, bool NORM>
@@ -451,32 +422,26 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
         if (NORM && ch < K / 4)
             gv[i] = __ldg(reinterpret_cast<const float4*>(gamma) + ch);
     }
-    // What the prologue reads, taken from the argument table before the barrier
-    // (after it, every table read would sit in the prologue's dependency chain):
+    // What the prologue reads, taken from the argument table before the block
+    // barrier (after it, every table read would sit in the prologue's dependency chain):
     // the input vector, whether it carries tags and which, the residual rows.
     const bool from_act = KIND == PH_DOWN_Q4 || KIND == PH_DOWN_Q6;
-    const bool untagged_in = (KIND == PH_QKV && l == 0) || KIND == PH_O;  // x_in, or attn behind a grid barrier
+    const bool untagged_in = KIND == PH_QKV && l == 0;  // x_in, written before the launch
     const float* xsrc = KIND == PH_QKV && l == 0 ? A.x_in : KIND == PH_O ? A.attn : from_act ? A.act : A.x;
-    // x after the O projection (gate/up), after the previous layer's down (q|k|v, vocabulary)
-    const uint32_t ipar = from_act ? tk_par_layer(l)
+    // act and attn: this layer's write; x after the O projection (gate/up), after the
+    // previous layer's down (q|k|v, vocabulary)
+    const uint32_t ipar = from_act || KIND == PH_O ? tk_par_layer(l)
                           : KIND == PH_GATEUP ? tk_par_x_o(l)
                                               : tk_par_x_down(KIND == PH_VOCAB ? A.n_layers - 1 : l - 1);
     const float* rsrc = (KIND == PH_O && l == 0 ? A.x_in : A.x) + r0;
-    // diagnostics: with a barrier skew every tagged read waits for a write that never comes
-    const uint32_t ipar_w = ipar ^ (A.bar_skew != 0 ? 1u : 0u);
+    // diagnostics: with a skew every tagged read waits for a write that never comes
+    const uint32_t ipar_w = ipar ^ (A.skew != 0 ? 1u : 0u);
     const float eps = A.eps;
-    // the O phase after a separate attention phase reads its untagged output behind
-    // a grid barrier; the other phases read tagged vectors and need none (the block's
-    // own warps finish the previous phase's epilogue first: the prologue reuses its
-    // shared memory)
-    if (KIND == PH_O && !fold) {
-        if (!tk_sync(p))
-            return make_int2(T, icur);
-    } else {
-        __syncthreads();
-        if (m.dead)
-            return make_int2(T, icur);
-    }
+    // no grid barrier: the input is tagged; the block's own warps finish the previous
+    // phase's epilogue first (the prologue reuses its shared memory)
+    __syncthreads();
+    if (m.dead)
+        return make_int2(T, icur);
     tk_trace(p, 2);
     tk_trace(p, 3);
 
@@ -492,7 +457,7 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
         ok = tk_fold_attention<PL>(l, fpre);
     } else {
         float4 xv[NCH];
-        if (untagged_in) {  // the token's input (written before the launch), or attn behind a grid barrier
+        if (untagged_in) {  // the token's input, written before the launch
 #pragma unroll
             for (int i = 0; i < NCH; ++i) {
                 const int ch = tid + TK_THREADS * i;
@@ -513,7 +478,7 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
             m.gred[warp] = ss;
     }
     if (!ok && lane == 0)
-        tk_give_up(DEVERR_TIMEOUT_BARRIER);
+        tk_give_up(DEVERR_TIMEOUT_TAG);
     __syncthreads();  // quantised activation, residual rows and norm partials complete
     if (m.dead) {
         tk_trace(p, 4);
@@ -571,22 +536,18 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
                 st_relaxed_f32(A.x + r, tagged(tk_resid()[r - r0] + v0, opar));
             } else if (EPI == EPI_SWIGLU) {
                 st_relaxed_f32(A.act + r, tagged(v0 / (1.0f + expf(-v0)) * v1, opar));
-            } else {  // EPI_QKV: q rows; k and v rows to the cache at pos and as tagged fp32 copies
+            } else {  // EPI_QKV: q rows, then k and v rows
                 const int qdim = A.n_q * ATT_HD, kvdim = A.n_kv * ATT_HD;
                 if (r < qdim) {
                     st_relaxed_f32(A.q + r, tagged(v0, opar));
                 } else {
+                    // k and v: tagged fp32 copies (the key as projected with the Qwen3
+                    // inputs, else the fp16 value the cache will hold); the attention
+                    // (or the fold) writes the cache rows from them
                     const int idx = r - qdim;
                     const bool is_v = idx >= kvdim;
                     const int rem = idx - (is_v ? kvdim : 0);
-                    const int kvh = rem / ATT_HD, dd = rem % ATT_HD;
-                    const size_t plane = static_cast<size_t>(A.n_kv) * A.max_ctx * ATT_HD;
-                    __half* kc = A.kv + static_cast<size_t>(l) * 2 * plane + (is_v ? plane : 0);
-                    const __half h = __float2half_rn(v0);
-                    if (is_v || !A.qwen)  // the Qwen3 key is normalised and rotated first (by the attention)
-                        kc[(static_cast<size_t>(kvh) * A.max_ctx + A.pos) * ATT_HD + dd] = h;
-                    // the fold reads these copies: the fp16 value (the projected key for Qwen3)
-                    const float copy = (is_v || !A.qwen) ? __half2float(h) : v0;
+                    const float copy = (is_v || !A.qwen) ? __half2float(__float2half_rn(v0)) : v0;
                     st_relaxed_f32((is_v ? A.v_new : A.k_new) + rem, tagged(copy, opar));
                 }
             }
@@ -639,7 +600,7 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
             pend = -1;
         }
     }
-    if (ok && pend >= 0) {  // the phase's epilogue must be done before the next barrier
+    if (ok && pend >= 0) {  // the phase's epilogue must be done before the block moves on
         if (mbar_wait(&m.empty[(T0 + pend) & (TK_NSTAGE - 1)], ((T0 + pend) / TK_NSTAGE) & 1, A.wait_ns))
             complete(pend, T0 + pend);
         else {
@@ -655,13 +616,16 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
     return make_int2(T0 + ntiles, icur);
 }
 
-// Attention phase p: items (key chunk, KV head) spread over the blocks, between
-// two grid barriers (the cache rows and the merge scratch carry no tags).
+// Attention phase p: items (key chunk, KV head) spread over the blocks, in the
+// tagged mode of attn_block (q and the new key and value are polled by their
+// tags, the output is tagged, the merge counters count on across layers).
 __device__ __forceinline__ void tk_attention(int p)
 {
     const TokenArgs& A = tk_args();
+    TkMisc& m = tk_misc();
     tk_trace(p, 0);
-    if (!tk_sync(p))
+    __syncthreads();  // the staging below reuses the quantised-activation area
+    if (m.dead)
         return;
     tk_trace(p, 2);
     const int group = A.n_q / A.n_kv;
@@ -669,7 +633,10 @@ __device__ __forceinline__ void tk_attention(int p)
     if (sub < 2) {
         const int l = p / 5;
         const size_t plane = static_cast<size_t>(A.n_kv) * A.max_ctx * A.hd;
-        AttnArgs t;
+        const int n_keys = A.pos + 1;
+        const int L = max((n_keys + ATT_CHUNKS - 1) / ATT_CHUNKS, ATT_MIN_CHUNK);
+        const int nact = (n_keys + L - 1) / L;
+        AttnArgs t{};
         t.q = A.q;
         t.kc = A.kv + static_cast<size_t>(l) * 2 * plane;
         t.vc = t.kc + plane;
@@ -679,21 +646,26 @@ __device__ __forceinline__ void tk_attention(int p)
         t.n_q = A.n_q;
         t.n_kv = A.n_kv;
         t.max_ctx = A.max_ctx;
-        t.n_keys = A.pos + 1;
+        t.n_keys = n_keys;
         t.step = nullptr;
         t.err = A.err;
-        t.k_new = A.qwen ? A.k_new : nullptr;
+        t.k_new = A.k_new;
         t.q_norm = A.layers[l].q_norm;
         t.k_norm = A.layers[l].k_norm;
         t.rope = A.rope;
         t.eps = A.eps;
-        const int n_keys = A.pos + 1;
-        const int L = max((n_keys + ATT_CHUNKS - 1) / ATT_CHUNKS, ATT_MIN_CHUNK);
-        const int nact = (n_keys + L - 1) / L;
+        t.tag = 1 + static_cast<int>(tk_par_layer(l) ^ (A.skew != 0 ? 1u : 0u));
+        t.ctr_base = l * nact;
+        t.v_new = A.v_new;
+        t.wait_ns = A.wait_ns;
         AttnSmem& sm = *reinterpret_cast<AttnSmem*>(tk_xq() + sub * (TK_ATT_STAGING / 4));
         const int bar = ATT_BAR - sub;
         for (int item = 2 * blockIdx.x + sub; item < nact * A.n_kv; item += 2 * gridDim.x) {
-            attn_block(t, item % nact, item / nact, group, sm, false, bar, 32 * group * sub);
+            if (!attn_block(t, item % nact, item / nact, group, sm, false, bar, 32 * group * sub)) {
+                if ((threadIdx.x & 31) == 0)
+                    tk_give_up(DEVERR_TIMEOUT_TAG);
+                break;  // every warp of the item returned false together
+            }
             named_bar_sync(bar, 32 * group);  // staging free before the next item
         }
     }
@@ -827,10 +799,11 @@ __global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_const
                 }
         }
     }
-    // The last block to finish puts the barrier area back for the next launch:
-    // every block counts itself out only after its last barrier wait and its last
+    // The last block to finish puts the launch-state area back for the next launch:
+    // every block counts itself out only after its last wait and its last
     // write (dead blocks too), so nothing reads the counters or the tagged vectors
-    // any more.  The arrivals go back to zero and the token count advances (the
+    // any more.  The exit count and the attention's merge counters go back to zero
+    // and the token count advances (the
     // tags of the next token follow from it), so a launch's arguments never
     // depend on host-side state.  After a wait ran out somewhere, writes may be
     // missing and the tags out of step: the tagged vectors and the token count go
@@ -849,19 +822,22 @@ __global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_const
                 a.x[i] = 0.f;
             for (int i = tid; i < a.ffn; i += TK_THREADS)
                 a.act[i] = 0.f;
-            for (int i = tid; i < qdim; i += TK_THREADS)
+            for (int i = tid; i < qdim; i += TK_THREADS) {
                 a.q[i] = 0.f;
+                a.attn[i] = 0.f;
+            }
             for (int i = tid; i < kvdim; i += TK_THREADS) {
                 a.k_new[i] = 0.f;
                 a.v_new[i] = 0.f;
             }
         }
         __syncthreads();
+        for (int i = tid; i < ATT_COUNTER_BYTES / 4; i += TK_THREADS)  // the attention's merge counters
+            a.counters[i] = 0;
         if (tid == 0) {
             const unsigned tok = ld_relaxed_u32(a.bar + TB_TOKEN);
             atomicExch(a.bar + TB_TOKEN, fault ? 0u : tok + 1u);
             atomicExch(a.bar + TB_FAULT, 0u);
-            atomicExch(a.bar + TB_ARRIVE, 0u);
             atomicExch(a.bar + TB_EXIT, 0u);
         }
     }

@@ -66,9 +66,9 @@ struct TokenArgs {
     int qwen;                  // Qwen3 attention inputs (per-head norms and rotation)
     const float2* rope;        // (cos, sin) table [max_ctx][hd / 2] with the Qwen3 inputs
     StepArgs* step;            // pos and logits recorded for the diagnostics entry points
-    unsigned* bar;             // [0] grid-barrier arrivals, [1] blocks finished; both 0 between launches
+    unsigned* bar;             // launch state: [1] blocks finished, [2] token count, [3] a wait ran out
     unsigned long long wait_ns;  // bound on every wait of the launch (wall-clock ns)
-    int bar_skew;              // diagnostics: barriers added to every target (0: none), so every wait runs out
+    int skew;                  // diagnostics: not 0 -- every tagged read waits for a write never made
     int pad2;
     const float* x_in;
     float* logits;
