@@ -552,6 +552,48 @@ def run_standalone(device, reps: int = 20) -> dict:
     return out
 
 
+OP_PROBES = ("attention_512", "gemv_bf16_4096", "rmsnorm_default", "rmsnorm_one_thread")
+
+
+def run_op_probe(args):
+    """`probe_reps` launches of one standalone entry point on a small case (for
+    profilers): attention over 513 keys of a 32/8-head cache, the bf16 GEMV on
+    4096x4096, or RMSNorm of 64x2048 with the default block or one thread per row."""
+    import torch
+
+    from quantised_gemv_norm_gb300 import build, dq
+
+    build.build()
+    dq.load()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(SEED)
+    kind = args.op_probe
+    if kind == "attention_512":
+        n_q, n_kv, max_ctx, n_keys = 32, 8, 1024, 513
+        q = torch.randn((n_q, 128), generator=gen, device="cuda")
+        k = torch.randn((n_kv, max_ctx, 128), generator=gen, device="cuda").half()
+        v = torch.randn((n_kv, max_ctx, 128), generator=gen, device="cuda").half()
+        ws = dq.attention_workspace(n_q, n_kv)
+        for _ in range(args.probe_reps):
+            y = dq.attention_decode(q, k, v, n_keys, workspace=ws)
+    elif kind == "gemv_bf16_4096":
+        W = (0.02 * torch.randn((4096, 4096), generator=gen, device="cuda")).to(torch.bfloat16)
+        x = torch.randn((4096,), generator=gen, device="cuda").to(torch.bfloat16)
+        for _ in range(args.probe_reps):
+            y = dq.gemv_bf16(W, x)
+    else:
+        x = torch.randn((64, 2048), generator=gen, device="cuda")
+        g = 1.0 + 0.1 * torch.randn((2048,), generator=gen, device="cuda")
+        for _ in range(args.probe_reps):
+            y = dq.rmsnorm(x, g, 1e-6, threads=None if kind == "rmsnorm_default" else 1)
+    torch.cuda.synchronize()
+    err = dq.device_error()
+    print(json.dumps({"op_probe": kind, "reps": args.probe_reps, "device_error_flag": err,
+                      "finite": bool(torch.isfinite(y).all().item())}))
+    if err:
+        sys.exit(1)
+
+
 def run_kernel_probe(args):
     """One decode token of a 2-layer full-width stack (9 GEMV launches), then the
     chosen kernel kind on layer 1 (a Q6_K down layer), alone, `probe_reps` times."""
@@ -718,6 +760,8 @@ def main():
     ap.add_argument("--kernel-probe", choices=KERNEL_KINDS, default=None,
                     help="profiling aid: build a 2-layer full-width stack, run one token, then launch this "
                          "kernel kind alone --probe-reps times (for ncu -k ... -s 9 -c 1)")
+    ap.add_argument("--op-probe", choices=OP_PROBES, default=None,
+                    help="profiling aid: launch one standalone entry point on a small case --probe-reps times")
     ap.add_argument("--probe-reps", type=int, default=3)
     ap.add_argument("--token-probe", action="store_true",
                     help="run a few fused tokens of a 2-layer full-width stack (for profilers) and exit")
@@ -727,6 +771,9 @@ def main():
         return
     if args.kernel_probe:
         run_kernel_probe(args)
+        return
+    if args.op_probe:
+        run_op_probe(args)
         return
     if args.msweep_only:
         import torch
