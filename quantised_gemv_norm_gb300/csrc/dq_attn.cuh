@@ -177,8 +177,23 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
     const bool tagged = a.tag != 0;
     const uint32_t par = static_cast<uint32_t>(a.tag - 1) & 1u;
     const __half* kbase = a.kc + static_cast<size_t>(g) * a.max_ctx * ATT_HD;
+    const __half* vbase = a.vc + static_cast<size_t>(g) * a.max_ctx * ATT_HD;
     const int pos = n_keys - 1;
     bool ok = true;  // tagged mode: every wait of this thread ended in time
+    if (tagged) {
+        // the first batch's cache rows of earlier positions (earlier tokens wrote them)
+        // go to shared memory while q is awaited; the position's own row comes from
+        // the tagged key and value below
+        const int nb = min(ATT_BATCH, j1 - j0);
+        for (int idx = tid; idx < nb * (ATT_HD / 8); idx += nthr) {
+            const int j = idx >> 4, ch = idx & 15;
+            if (j0 + j == pos)
+                continue;
+            cp_async16(&ks[j][8 * ch], kbase + static_cast<size_t>(j0 + j) * ATT_HD + 8 * ch);
+            cp_async16(&vs[j][8 * ch], vbase + static_cast<size_t>(j0 + j) * ATT_HD + 8 * ch);
+        }
+        cp_async_commit();
+    }
     {
         float4 v;
         if (tagged)
@@ -209,8 +224,11 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
                 uint2 w;
                 w.x = *reinterpret_cast<const uint32_t*>(&v01);
                 w.y = *reinterpret_cast<const uint32_t*>(&v23);
-                *reinterpret_cast<uint2*>(const_cast<__half*>(a.vc) + (static_cast<size_t>(g) * a.max_ctx + pos) * ATT_HD +
-                                          4 * lane) = w;
+                *reinterpret_cast<uint2*>(const_cast<__half*>(vbase) + static_cast<size_t>(pos) * ATT_HD + 4 * lane) = w;
+                if (pos - j0 < ATT_BATCH) {  // the row is in the first batch: stage it from here
+                    *reinterpret_cast<uint2*>(&ks[pos - j0][4 * lane]) = u;
+                    *reinterpret_cast<uint2*>(&vs[pos - j0][4 * lane]) = w;
+                }
             }
             __threadfence_block();
         }
@@ -218,7 +236,6 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
             v = head_norm_rope(v, load_norm_rope(a.q_norm, cs, lane), a.eps, lane);
         *reinterpret_cast<float4*>(&qs[warp][4 * lane]) = v;
     }
-    const __half* vbase = a.vc + static_cast<size_t>(g) * a.max_ctx * ATT_HD;
     const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
 
     float m = -INFINITY, l = 0.f;
@@ -228,12 +245,13 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
         // previous batch fully consumed (and qs written on the first); on the first, in
         // tagged mode, the item's warps also learn together whether any wait ran out
         if (tagged && jb == j0) {
+            cp_async_wait_all();  // this thread's staged rows landed
             if (named_bar_red_or(bar, nthr, !ok))
                 return false;
         } else {
             named_bar_sync(bar, nthr);
         }
-        for (int idx = tid; idx < nb * (ATT_HD / 8); idx += nthr) {
+        for (int idx = tid; idx < nb * (ATT_HD / 8) && !(tagged && jb == j0); idx += nthr) {
             const int j = idx >> 4, ch = idx & 15;
             const uint4 kv = __ldcg(reinterpret_cast<const uint4*>(kbase + static_cast<size_t>(jb + j) * ATT_HD) + ch);
             const uint4 vv = __ldcg(reinterpret_cast<const uint4*>(vbase + static_cast<size_t>(jb + j) * ATT_HD) + ch);
@@ -297,18 +315,32 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
     if (!sm.last)
         return true;
     __threadfence();
-    // merge the chunk partials of this warp's head
+    // merge the chunk partials of this warp's head: lane cc holds chunk cc's (m, l)
+    // and weight (nact <= 32), the output rows come 8 chunks at a time, so the
+    // merge costs a few round trips whatever the chunk count
     const float* hp = a.part + static_cast<size_t>(h) * ATT_CHUNKS * ATT_PART;
-    float M = -INFINITY;
-    for (int cc = 0; cc < nact; ++cc)
-        M = fmaxf(M, __ldcg(hp + cc * ATT_PART));
-    float Ls = 0.f, r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-    for (int cc = 0; cc < nact; ++cc) {
-        const float w = expf(__ldcg(hp + cc * ATT_PART) - M);
-        Ls = fmaf(__ldcg(hp + cc * ATT_PART + 1), w, Ls);
-        const float4 ov = __ldcg(reinterpret_cast<const float4*>(hp + cc * ATT_PART + 4) + lane);
-        r0 = fmaf(ov.x, w, r0); r1 = fmaf(ov.y, w, r1);
-        r2 = fmaf(ov.z, w, r2); r3 = fmaf(ov.w, w, r3);
+    float mc = -INFINITY, lc = 0.f;
+    if (lane < nact) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(hp + lane * ATT_PART));
+        mc = ml.x;
+        lc = ml.y;
+    }
+    const float M = warp_max(mc);
+    const float wc = lane < nact ? expf(mc - M) : 0.f;
+    const float Ls = warp_sum(lc * wc);
+    float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+    for (int c0 = 0; c0 < nact; c0 += 8) {
+        float4 ov[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            ov[i] = c0 + i < nact ? __ldcg(reinterpret_cast<const float4*>(hp + (c0 + i) * ATT_PART + 4) + lane)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float w = __shfl_sync(0xffffffffu, wc, (c0 + i) & 31);  // 0 past nact
+            r0 = fmaf(ov[i].x, w, r0); r1 = fmaf(ov[i].y, w, r1);
+            r2 = fmaf(ov[i].z, w, r2); r3 = fmaf(ov[i].w, w, r3);
+        }
     }
     const float inv = 1.0f / Ls;
     att_st_out(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane, make_float4(r0 * inv, r1 * inv, r2 * inv, r3 * inv),

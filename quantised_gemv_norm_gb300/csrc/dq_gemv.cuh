@@ -73,6 +73,8 @@ struct GemvArgs {
     float* k_new;       // EPI_QKV: when not null, k rows go here (fp32 [kvdim]) for the attention to finish
     int qdim, kvdim, hd, max_ctx;
     int resid_rows;             // EPI_RESID: shared-memory slots for the block's residual rows
+    int w_late;                 // 1: the weights may be the previous kernel's output -- before the
+                                // dependency wait only L2 prefetches of them, the copies after it
     int* err;
     unsigned long long* trace;  // diagnostics: per-block timestamps when not null
 };
@@ -393,6 +395,19 @@ __device__ __forceinline__ void issue_tile(const uint8_t* W, const uint8_t* W2, 
                  &full[s], pol);
 }
 
+// Ask L2 for tile t of the block's rows (a hint: nothing is written and nothing
+// waits for it).
+template <int NMAT>
+__device__ __forceinline__ void prefetch_tile(const uint8_t* W, const uint8_t* W2, int row_bytes, int t, int r0,
+                                              int r1, int R)
+{
+    const int row = r0 + t * R;
+    const uint32_t bytes = static_cast<uint32_t>(min(R, r1 - row) * row_bytes);
+    prefetch_l2_bulk(W + static_cast<size_t>(row) * row_bytes, bytes);
+    if (NMAT == 2)
+        prefetch_l2_bulk(W2 + static_cast<size_t>(row) * row_bytes, bytes);
+}
+
 // Quantise one 4-element chunk c of the activation into the unit table xq: the
 // 8 lanes c & ~7 .. c | 7 of the calling warp hold one 32-element unit (and all
 // take part), four elements each.
@@ -558,6 +573,33 @@ __device__ __forceinline__ float quantise_block_il(float4 (&v)[NCH], const float
     return ss;
 }
 
+#ifndef GEMV_QIL
+#define GEMV_QIL 1
+#endif
+
+// The standalone kernel's activation quantiser: the interleaved form for the
+// chunk count K needs (2, 4, 6 or 8 chunks a thread; the chunks past K hold
+// zeros and store nothing).
+template <int FMT, int PL>
+__device__ __forceinline__ float quantise_activation(float4 (&xv)[QCHUNKS], const float4 (&gv)[QCHUNKS], bool norm,
+                                                     uint32_t* xq, int K, int tid)
+{
+    static_assert(QCHUNKS == 8, "chunk counts below");
+    if (!GEMV_QIL)
+        return quantise_block<FMT, PL, QCHUNKS>(xv, gv, norm, xq, K, tid);
+    const int nch = (K / 4 + NCONS - 1) / NCONS;
+    if (nch <= 2)
+        return quantise_block_il<FMT, PL, 2>(*reinterpret_cast<float4(*)[2]>(&xv),
+                                             *reinterpret_cast<const float4(*)[2]>(&gv), norm, xq, K, tid);
+    if (nch <= 4)
+        return quantise_block_il<FMT, PL, 4>(*reinterpret_cast<float4(*)[4]>(&xv),
+                                             *reinterpret_cast<const float4(*)[4]>(&gv), norm, xq, K, tid);
+    if (nch <= 6)
+        return quantise_block_il<FMT, PL, 6>(*reinterpret_cast<float4(*)[6]>(&xv),
+                                             *reinterpret_cast<const float4(*)[6]>(&gv), norm, xq, K, tid);
+    return quantise_block_il<FMT, PL, 8>(xv, gv, norm, xq, K, tid);
+}
+
 // One stage of the consumers: this thread's unit products for rows g, g + RG,
 // ... (RPT of them, each of NMAT matrices) of the tile, reduced over the warp
 // into wred[0 .. RPT NMAT) (the warp's partial sums; matrix m, row i at m RPT + i;
@@ -706,16 +748,25 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
         }
     }
     __syncthreads();
-    // weights never depend on the previous kernel: the first ring-full, one stage per
-    // lane of warp 0 (the copies start in parallel)
-    if (tid < min(a.nstage, ntiles)) {
-        issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, tid, r0, r1, R, pol);
-        if (ttile)
-            ttile[128 + tid] = clock64();
+    // The first ring-full, one stage per lane of warp 0 (the copies start in
+    // parallel).  Weights that never depend on the previous kernel (a model's
+    // tables) are copied before the dependency wait; otherwise only L2 prefetches
+    // go out before it (L2 is where the previous kernel's writes land, so a
+    // prefetch can never leave a stale copy) and the copies follow the wait.
+    const bool first = tid < min(a.nstage, ntiles);
+    if (first) {
+        if (a.w_late)
+            prefetch_tile<NMAT>(a.W, a.W2, a.row_bytes, tid, r0, r1, R);
+        else
+            issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, tid, r0, r1, R, pol);
     }
     if (trace && tid == 0)
         trace[1] = globaltimer_ns();
     pdl_wait();  // the activation is the previous kernel's output
+    if (first && a.w_late)
+        issue_tile<NMAT>(a.W, a.W2, a.row_bytes, a.nstage, a.stage_bytes, smem, full, tid, r0, r1, R, pol);
+    if (first && ttile)
+        ttile[128 + tid] = clock64();
     if (trace && tid == 0)
         trace[2] = globaltimer_ns();
 
@@ -758,6 +809,7 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
 #pragma unroll
         for (int i = 0; i < QCHUNKS; ++i) {
             const int c = tid + NCONS * i;
+            xv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (c < a.K / 4)
                 xv[i] = __ldcg(reinterpret_cast<const float4*>(a.x) + c);
         }
@@ -767,7 +819,7 @@ __global__ void __maxnreg__(128) gemv_stream_kernel(const __grid_constant__ Gemv
                 resid[r] = __ldcg(a.y + r0 + r);
         if (trace && tid == 0)
             trace[3] = globaltimer_ns();
-        float ss = quantise_block<FMT, PL, QCHUNKS>(xv, gv, norm, xq, a.K, tid);
+        float ss = quantise_activation<FMT, PL>(xv, gv, norm, xq, a.K, tid);
         float rstd = 1.f;
         if (norm) {
             ss = warp_sum(ss);

@@ -275,6 +275,10 @@ __global__ void dequant_q6k_kernel(const uint8_t* __restrict__ blocks, float* __
 
 // ------------------------------------------------------------------- C ABI
 
+#ifndef GEMV_PDL
+#define GEMV_PDL 1
+#endif
+
 static int gemv_entry(int fmt, const void* W, const void* x, float* y, int rows, int K, void* stream)
 {
     if (!W || !x || !y)
@@ -294,7 +298,10 @@ static int gemv_entry(int fmt, const void* W, const void* x, float* y, int rows,
     else
         a.x = static_cast<const float*>(x);
     a.y = y;
-    cudaError_t e = dqhost::launch_gemv(plan, a, static_cast<cudaStream_t>(stream), false);
+    // a dependent launch: its set-up and the L2 prefetch of its first tiles overlap
+    // the previous kernel's tail; the weights are copied only after the wait
+    a.w_late = GEMV_PDL;
+    cudaError_t e = dqhost::launch_gemv(plan, a, static_cast<cudaStream_t>(stream), GEMV_PDL != 0);
     return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
 }
 
