@@ -156,6 +156,11 @@ DQ_API int dq_layernorm_threads(const float* x, const float* gamma, const float*
  *   of the fixed-point activation over each 16-element sub-block).
  *   K % 1024 == 0, 1024 <= K <= 16384.
  * W, x 16-byte aligned (DQ_ERR_ALIGN otherwise).  y must not overlap W or x.
+ * Ordering: each call is a programmatic dependent launch on `stream`.  Before
+ * the previous kernel on the stream has completed it only sets up and asks L2
+ * for the first weight tiles (a hint that reads nothing into the SMs); it
+ * reads W and x and writes y only after that kernel's writes are visible, so
+ * stream order holds as for a plain launch.
  * Errors: NULL -> DQ_ERR_NULL; rows < 1 or K outside the ranges -> DQ_ERR_SHAPE
  * or DQ_ERR_UNSUPPORTED. */
 DQ_API int dq_gemv_bf16(const void* W_bf16, const void* x_bf16, float* y, int rows, int K, void* stream);
@@ -180,7 +185,9 @@ DQ_API int dq_gemv_q2k(const void* W_blocks, const float* x, float* y, int rows,
  * global-timer ns at [0] phase entered, [2] the block's warps done with the
  * previous phase, [4] phase done; SM clock cycles at [3] the same moment as
  * [2], [5] activation arrived and quantised, [7] activation in registers, [1]
- * first weight tile ready; [6] unused; 64 bytes per block and phase.  A tensor-core dq_matmul_q4k_path writes, for
+ * first weight tile ready; [6] unused; 64 bytes per block and phase.  In an
+ * attention phase the block's first item writes global-timer ns at [1] q ready,
+ * [3] keys staged, [5] partial computed, [6] merge decided, [7] output stored.  A tensor-core dq_matmul_q4k_path writes, for
  * block 0 and its first 32 half-block stages, 8 SM clock stamps per stage at
  * buffer[8 stage]: operands seen ready and MMAs issued (control thread), stage
  * start, weights landed, operand buffer free and stage written (thread 0).

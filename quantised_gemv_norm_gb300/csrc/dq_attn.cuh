@@ -41,7 +41,17 @@ struct AttnArgs {
     int ctr_base;
     const float* v_new;            // [n_kv][128] tagged mode
     unsigned long long wait_ns;    // tagged mode: bound on the tag waits
+    // diagnostics (the fused token kernel's trace): when not null, the item's first
+    // thread records global-timer ns at [1] q ready, [3] keys staged, [5] partial
+    // computed, [6] merge decided, [7] output stored
+    unsigned long long* trace;
 };
+
+__device__ __forceinline__ void att_stamp(const AttnArgs& a, int i, int tid)
+{
+    if (a.trace && tid == 0)
+        a.trace[i] = globaltimer_ns();
+}
 
 __device__ __forceinline__ float4 att_ld_relaxed_f4(const float* p)
 {
@@ -236,6 +246,7 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
             v = head_norm_rope(v, load_norm_rope(a.q_norm, cs, lane), a.eps, lane);
         *reinterpret_cast<float4*>(&qs[warp][4 * lane]) = v;
     }
+    att_stamp(a, 1, tid);
     const float scale = 0.08838834764831845f;  // 1 / sqrt(128)
 
     float m = -INFINITY, l = 0.f;
@@ -259,6 +270,8 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
             *reinterpret_cast<uint4*>(&vs[j][8 * ch]) = vv;
         }
         named_bar_sync(bar, nthr);
+        if (jb == j0)
+            att_stamp(a, 3, tid);
         float s = -INFINITY;
         if (lane < nb) {
             float d0 = 0.f, d1 = 0.f;
@@ -295,6 +308,7 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
         m = mnew;
     }
 
+    att_stamp(a, 5, tid);
     if (nact == 1) {  // the only block of this KV head: normalise and write directly
         const float inv = 1.0f / l;
         att_st_out(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane, make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv),
@@ -312,6 +326,7 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
     if (tid == 0)
         sm.last = (atomicAdd(&a.counters[g], 1) == (tagged ? a.ctr_base : 0) + nact - 1);
     named_bar_sync(bar, nthr);
+    att_stamp(a, 6, tid);
     if (!sm.last)
         return true;
     __threadfence();
@@ -345,6 +360,7 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
     const float inv = 1.0f / Ls;
     att_st_out(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane, make_float4(r0 * inv, r1 * inv, r2 * inv, r3 * inv),
                a.tag);
+    att_stamp(a, 7, tid);
     if (!tagged) {  // tagged mode: the counters count on across layers; the launch zeroes them at its end
         named_bar_sync(bar, nthr);
         if (tid == 0)

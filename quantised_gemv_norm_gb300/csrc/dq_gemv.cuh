@@ -127,14 +127,32 @@ __device__ __forceinline__ uint32_t pack16x2(int a, int b)
 // ------------------------------------------------------------- unit products
 
 // Q4_K unit n of a row: 32 weights of sub-block j = n & 7 of block n >> 3.
-template <int PL>
-__device__ __forceinline__ float q4k_unit(const uint8_t* rp, int n, const XQ<PL>& u)
+// What a unit product needs of the stage: the sub-block's 16 code bytes, the
+// block's d and dmin (fp16 pair), and the sub-block's 6-bit scale and min
+// (bits 0-5 and 8-13 of smn) taken out of the header as it is read.
+struct Q4KW {
+    uint4 c;
+    uint32_t dd, smn;
+};
+
+__device__ __forceinline__ Q4KW q4k_load(const uint8_t* rp, int n)
 {
     const int j = n & 7;
     const uint8_t* bp = rp + Q4K_BYTES * (n >> 3);
     const uint4 hd = lds128(bp);
-    const uint4 c = lds128(bp + 16 + 16 * j);
-    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    // scale j: bits 6j.. of the 96-bit string (hd.y, hd.z, hd.w); min j: bits 48+6j..
+    const uint32_t s_lo = j < 6 ? hd.y : hd.z, s_hi = j < 6 ? hd.z : hd.w;
+    const uint32_t m_lo = j < 3 ? hd.z : hd.w, m_hi = j < 3 ? hd.w : 0u;
+    const uint32_t sc = __funnelshift_r(s_lo, s_hi, (6 * j) & 31) & 63u;
+    const uint32_t mn = __funnelshift_r(m_lo, m_hi, (48 + 6 * j) & 31) & 63u;
+    return Q4KW{lds128(bp + 16 + 16 * j), hd.x, sc | (mn << 8)};
+}
+
+template <int PL>
+__device__ __forceinline__ float q4k_dot(const Q4KW& w, int n, const XQ<PL>& u)
+{
+    (void)n;
+    const uint32_t cw[4] = {w.c.x, w.c.y, w.c.z, w.c.w};
     // four independent accumulators per plane keep the dependent chains short
     int la = 0, lb = 0, ha = 0, hb = 0, la2 = 0, lb2 = 0, ha2 = 0, hb2 = 0;
 #pragma unroll
@@ -155,21 +173,34 @@ __device__ __forceinline__ float q4k_unit(const uint8_t* rp, int n, const XQ<PL>
     float dot16 = static_cast<float>((la + lb) * 16 + (ha + hb));  // 16 * sum q * xi
     if (PL == 2)
         dot16 += static_cast<float>((la2 + lb2) * 16 + (ha2 + hb2)) * (1.0f / 32768.0f);
-    // scale j: bits 6j.. of the 96-bit string (hd.y, hd.z, hd.w); min j: bits 48+6j..
-    const uint32_t s_lo = j < 6 ? hd.y : hd.z, s_hi = j < 6 ? hd.z : hd.w;
-    const uint32_t m_lo = j < 3 ? hd.z : hd.w, m_hi = j < 3 ? hd.w : 0u;
-    const int sc = static_cast<int>(__funnelshift_r(s_lo, s_hi, (6 * j) & 31) & 63u);
-    const int mn = static_cast<int>(__funnelshift_r(m_lo, m_hi, (48 + 6 * j) & 31) & 63u);
-    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+    const int sc = static_cast<int>(w.smn & 63u), mn = static_cast<int>(w.smn >> 8);
+    const float d = half_bits_to_float(w.dd), dmin = half_bits_to_float(w.dd >> 16);
     return (d * static_cast<float>(sc)) * (u.f * dot16) - (dmin * static_cast<float>(mn)) * u.hsum;
 }
 
+template <int PL>
+__device__ __forceinline__ float q4k_unit(const uint8_t* rp, int n, const XQ<PL>& u)
+{
+    return q4k_dot<PL>(q4k_load(rp, n), n, u);
+}
+
 // Q6_K unit: 32 weights of group g of (permuted) block Bp; fields start at
-// even byte offsets, so they are read as aligned words and re-aligned.
-__device__ __forceinline__ float q6k_unit(const uint8_t* rp, int n, const XQ<1>& u)
+// even byte offsets, so they are read as aligned words and re-aligned as they
+// are read: the 16 low-bit bytes, the 8 high-bit bytes, the two scales (bits
+// 0-15 of sd) and the block's d (bits 16-31).
+struct Q6KW {
+    uint32_t ql[4], H0, H1, sd;
+};
+
+__device__ __forceinline__ int q6k_block(int n)
 {
     const int B = n >> 3, i = B & 7;
-    const int Bp = (B & ~7) + (i < 4 ? 2 * i : 2 * (i - 4) + 1);
+    return (B & ~7) + (i < 4 ? 2 * i : 2 * (i - 4) + 1);
+}
+
+__device__ __forceinline__ Q6KW q6k_load(const uint8_t* rp, int n)
+{
+    const int Bp = q6k_block(n);
     const int g = n & 7;
     const uint8_t* bp = rp + Q6K_BYTES * Bp;
     const uint32_t sh = (Bp & 1) ? 16u : 0u;       // rows are 16-byte aligned
@@ -177,20 +208,30 @@ __device__ __forceinline__ float q6k_unit(const uint8_t* rp, int n, const XQ<1>&
     const uint8_t* ph = bp + 128 + 8 * g - (sh >> 3);
     const uint32_t w0 = lds32(pl), w1 = lds32(pl + 4), w2 = lds32(pl + 8), w3 = lds32(pl + 12),
                    w4 = lds32(pl + 16);
-    const uint32_t ql[4] = {__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh),
-                            __funnelshift_r(w2, w3, sh), __funnelshift_r(w3, w4, sh)};
     const uint32_t h0 = lds32(ph), h1 = lds32(ph + 4), h2 = lds32(ph + 8);
-    const uint32_t H0 = __funnelshift_r(h0, h1, sh), H1 = __funnelshift_r(h1, h2, sh);
-    const uint32_t scw = *reinterpret_cast<const uint16_t*>(bp + 192 + 2 * g);
-    const uint32_t dbits = *reinterpret_cast<const uint16_t*>(bp + 208);
+    Q6KW w;
+    w.ql[0] = __funnelshift_r(w0, w1, sh);
+    w.ql[1] = __funnelshift_r(w1, w2, sh);
+    w.ql[2] = __funnelshift_r(w2, w3, sh);
+    w.ql[3] = __funnelshift_r(w3, w4, sh);
+    w.H0 = __funnelshift_r(h0, h1, sh);
+    w.H1 = __funnelshift_r(h1, h2, sh);
+    w.sd = *reinterpret_cast<const uint16_t*>(bp + 192 + 2 * g) |
+           (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(bp + 208)) << 16);
+    return w;
+}
+
+__device__ __forceinline__ float q6k_dot(const Q6KW& w, int n, const XQ<1>& u)
+{
+    (void)n;
     int da = 0, db = 0, da2 = 0, db2 = 0;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
         // high two bits of weights 4t+e sit at bits 2t of byte e: move them to bits 4-5
-        const uint32_t ha = (t < 2 ? (H0 << (4 - 2 * t)) : (H0 >> (2 * t - 4))) & 0x30303030u;
-        const uint32_t hb = (t < 2 ? (H1 << (4 - 2 * t)) : (H1 >> (2 * t - 4))) & 0x30303030u;
-        const uint32_t qa = (ql[t] & 0x0F0F0F0Fu) | ha;         // q of weights 4t+e
-        const uint32_t qb = ((ql[t] >> 4) & 0x0F0F0F0Fu) | hb;  // q of weights 16+4t+e
+        const uint32_t ha = (t < 2 ? (w.H0 << (4 - 2 * t)) : (w.H0 >> (2 * t - 4))) & 0x30303030u;
+        const uint32_t hb = (t < 2 ? (w.H1 << (4 - 2 * t)) : (w.H1 >> (2 * t - 4))) & 0x30303030u;
+        const uint32_t qa = (w.ql[t] & 0x0F0F0F0Fu) | ha;         // q of weights 4t+e
+        const uint32_t qb = ((w.ql[t] >> 4) & 0x0F0F0F0Fu) | hb;  // q of weights 16+4t+e
         da = dp2a_lo(u.q[2 * t], qa, da);
         da2 = dp2a_hi(u.q[2 * t + 1], qa, da2);
         db = dp2a_lo(u.q[8 + 2 * t], qb, db);
@@ -198,10 +239,15 @@ __device__ __forceinline__ float q6k_unit(const uint8_t* rp, int n, const XQ<1>&
     }
     da += da2;
     db += db2;
-    const int sca = static_cast<int>(static_cast<int8_t>(scw & 0xffu));
-    const int scb = static_cast<int>(static_cast<int8_t>(scw >> 8));
+    const int sca = static_cast<int>(static_cast<int8_t>(w.sd & 0xffu));
+    const int scb = static_cast<int>(static_cast<int8_t>((w.sd >> 8) & 0xffu));
     const int v = sca * (da - u.s32a) + scb * (db - u.s32b);  // sum sc (q - 32) xi, |v| < 2^31
-    return (half_bits_to_float(dbits) * u.s) * static_cast<float>(v);
+    return (half_bits_to_float(w.sd >> 16) * u.s) * static_cast<float>(v);
+}
+
+__device__ __forceinline__ float q6k_unit(const uint8_t* rp, int n, const XQ<1>& u)
+{
+    return q6k_dot(q6k_load(rp, n), n, u);
 }
 
 // Q2_K unit n of a row: sub-blocks 2(n & 7) and 2(n & 7) + 1 of block n >> 3

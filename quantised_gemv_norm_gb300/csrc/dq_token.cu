@@ -658,6 +658,8 @@ __device__ __forceinline__ void tk_attention(int p)
         t.ctr_base = l * nact;
         t.v_new = A.v_new;
         t.wait_ns = A.wait_ns;
+        if (A.trace && sub == 0)  // the block's first item
+            t.trace = A.trace + (static_cast<size_t>(blockIdx.x) * (5 * A.n_layers + 1) + p) * 8;
         AttnSmem& sm = *reinterpret_cast<AttnSmem*>(tk_xq() + sub * (TK_ATT_STAGING / 4));
         const int bar = ATT_BAR - sub;
         for (int item = 2 * blockIdx.x + sub; item < nact * A.n_kv; item += 2 * gridDim.x) {
@@ -667,6 +669,7 @@ __device__ __forceinline__ void tk_attention(int p)
                 break;  // every warp of the item returned false together
             }
             named_bar_sync(bar, 32 * group);  // staging free before the next item
+            t.trace = nullptr;
         }
     }
     tk_trace(p, 4);
