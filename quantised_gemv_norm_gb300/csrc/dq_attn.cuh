@@ -35,17 +35,35 @@ struct AttnArgs {
     // the block whose chunk holds the token's position writes that position's fp16
     // key and value rows into the cache from k_new (the Qwen3 key, or the key's fp16
     // value) and v_new (the value's fp16 value); the output is stored with the same
-    // tag; the merge counters are not reset but count on from ctr_base (the launch
-    // zeroes them at its end).  tag = 0 (a zero-initialised AttnArgs): the plain mode.
+    // tag; the chunks meet through `stamps`, not the merge counters.  tag = 0 (a
+    // zero-initialised AttnArgs): the plain mode.
     int tag;
-    int ctr_base;
     const float* v_new;            // [n_kv][128] tagged mode
     unsigned long long wait_ns;    // tagged mode: bound on the tag waits
+    // Tagged mode with more than one chunk: every chunk but the last stores its
+    // partial and then, with release semantics, `seq` into stamps[g][c]; the
+    // block of the last chunk (the one holding the token's position) merges once
+    // it has acquired every other chunk's stamp.  seq is unique per layer and token
+    // (a stale stamp never matches), so nothing is reset between calls.
+    unsigned* stamps;              // [n_kv][ATT_CHUNKS]
+    unsigned seq;
     // diagnostics (the fused token kernel's trace): when not null, the item's first
     // thread records global-timer ns at [1] q ready, [3] keys staged, [5] partial
     // computed, [6] merge decided, [7] output stored
     unsigned long long* trace;
 };
+
+__device__ __forceinline__ void att_st_release(unsigned* p, unsigned v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned att_ld_acquire(const unsigned* p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ void att_stamp(const AttnArgs& a, int i, int tid)
 {
@@ -316,43 +334,80 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
         return true;
     }
     float* pp = a.part + (static_cast<size_t>(h) * ATT_CHUNKS + c) * ATT_PART;
-    if (lane == 0) {
-        pp[0] = m;
-        pp[1] = l;
+    const float* hp = a.part + static_cast<size_t>(h) * ATT_CHUNKS * ATT_PART;
+    // the chunks whose partials the merge loads: all of them, or in tagged mode all
+    // but the merging (last) chunk, whose partial stays in registers
+    int nload = nact;
+    if (tagged) {
+        if (c != nact - 1) {
+            if (lane == 0) {
+                pp[0] = m;
+                pp[1] = l;
+            }
+            *reinterpret_cast<float4*>(pp + 4 + 4 * lane) = make_float4(o0, o1, o2, o3);
+            named_bar_sync(bar, nthr);  // the item's partial stores come before the stamp
+            if (tid == 0)
+                att_st_release(a.stamps + g * ATT_CHUNKS + c, a.seq);
+            att_stamp(a, 6, tid);
+            return true;
+        }
+        nload = nact - 1;
+        // wait for the other chunks' stamps (lane cc takes chunk cc); the warp
+        // barrier passes each lane's acquire on to the loads of all lanes
+        const unsigned* st = a.stamps + g * ATT_CHUNKS;
+        bool mine = lane >= nload || att_ld_acquire(st + lane) == a.seq;
+        unsigned long long t0 = 0;
+        while (!__all_sync(0xffffffffu, mine)) {
+            const unsigned long long now = globaltimer_ns();
+            if (t0 == 0)
+                t0 = now;
+            else if (__any_sync(0xffffffffu, now - t0 > a.wait_ns))
+                return false;
+            if (!mine)
+                mine = att_ld_acquire(st + lane) == a.seq;
+        }
+        __syncwarp();
+        att_stamp(a, 6, tid);
+    } else {
+        if (lane == 0) {
+            pp[0] = m;
+            pp[1] = l;
+        }
+        *reinterpret_cast<float4*>(pp + 4 + 4 * lane) = make_float4(o0, o1, o2, o3);
+        __threadfence();
+        named_bar_sync(bar, nthr);
+        if (tid == 0)
+            sm.last = (atomicAdd(&a.counters[g], 1) == nact - 1);
+        named_bar_sync(bar, nthr);
+        att_stamp(a, 6, tid);
+        if (!sm.last)
+            return true;
+        __threadfence();
     }
-    *reinterpret_cast<float4*>(pp + 4 + 4 * lane) = make_float4(o0, o1, o2, o3);
-    __threadfence();
-    named_bar_sync(bar, nthr);
-    if (tid == 0)
-        sm.last = (atomicAdd(&a.counters[g], 1) == (tagged ? a.ctr_base : 0) + nact - 1);
-    named_bar_sync(bar, nthr);
-    att_stamp(a, 6, tid);
-    if (!sm.last)
-        return true;
-    __threadfence();
     // merge the chunk partials of this warp's head: lane cc holds chunk cc's (m, l)
     // and weight (nact <= 32), the output rows come 8 chunks at a time, so the
     // merge costs a few round trips whatever the chunk count
-    const float* hp = a.part + static_cast<size_t>(h) * ATT_CHUNKS * ATT_PART;
     float mc = -INFINITY, lc = 0.f;
-    if (lane < nact) {
+    if (lane < nload) {
         const float2 ml = __ldcg(reinterpret_cast<const float2*>(hp + lane * ATT_PART));
         mc = ml.x;
         lc = ml.y;
     }
-    const float M = warp_max(mc);
-    const float wc = lane < nact ? expf(mc - M) : 0.f;
-    const float Ls = warp_sum(lc * wc);
-    float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-    for (int c0 = 0; c0 < nact; c0 += 8) {
+    const float mown = nload < nact ? m : -INFINITY;  // tagged mode: this item's own chunk
+    const float M = fmaxf(warp_max(mc), mown);
+    const float wc = lane < nload ? expf(mc - M) : 0.f;
+    const float wown = nload < nact ? expf(mown - M) : 0.f;
+    const float Ls = warp_sum(lc * wc) + (nload < nact ? l * wown : 0.f);
+    float r0 = o0 * wown, r1 = o1 * wown, r2 = o2 * wown, r3 = o3 * wown;
+    for (int c0 = 0; c0 < nload; c0 += 8) {
         float4 ov[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            ov[i] = c0 + i < nact ? __ldcg(reinterpret_cast<const float4*>(hp + (c0 + i) * ATT_PART + 4) + lane)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            ov[i] = c0 + i < nload ? __ldcg(reinterpret_cast<const float4*>(hp + (c0 + i) * ATT_PART + 4) + lane)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float w = __shfl_sync(0xffffffffu, wc, (c0 + i) & 31);  // 0 past nact
+            const float w = __shfl_sync(0xffffffffu, wc, (c0 + i) & 31);  // 0 past nload
             r0 = fmaf(ov[i].x, w, r0); r1 = fmaf(ov[i].y, w, r1);
             r2 = fmaf(ov[i].z, w, r2); r3 = fmaf(ov[i].w, w, r3);
         }

@@ -65,6 +65,7 @@ struct dq_model {
     float2* rope;       // (cos, sin) [max_ctx][hd / 2] when k_new is set
     float* tk_k;        // fused kernel: tagged copies of the token's keys and values [n_kv hd]
     float* tk_v;
+    unsigned* tk_stamps; // fused kernel: attention chunk stamps [n_kv][ATT_CHUNKS]
     // fused token kernel
     bool fused;
     dqhost::TokenPlan tplan;
@@ -309,8 +310,9 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
                  bw = up(dqhost::attention_workspace_bytes(d->n_q_heads, d->n_kv_heads)),
                  bl = up(sizeof(dq::TokenLayer) * d->n_layers), bb = 256,
                  bk = (qwen3 || m->fused) ? up(sizeof(float) * kvdim) : 0, bv = m->fused ? up(sizeof(float) * kvdim) : 0,
-                 br = qwen3 ? up(sizeof(float2) * static_cast<size_t>(d->max_ctx) * (d->head_dim / 2)) : 0;
-    const size_t total = bx + bq + ba + bf + bs + bw + bl + bb + bk + bv + br;
+                 br = qwen3 ? up(sizeof(float2) * static_cast<size_t>(d->max_ctx) * (d->head_dim / 2)) : 0,
+                 bt = m->fused ? up(sizeof(unsigned) * d->n_kv_heads * dq::ATT_CHUNKS) : 0;
+    const size_t total = bx + bq + ba + bf + bs + bw + bl + bb + bk + bv + br + bt;
     // diagnostics: an injected allocation failure (dq_debug_fail_next_allocs)
     int inject = g_fail_allocs.load();
     while (inject > 0 && !g_fail_allocs.compare_exchange_weak(inject, inject - 1)) {
@@ -336,9 +338,10 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
         m->k_new = reinterpret_cast<float*>(kv_copies);
         m->rope = reinterpret_cast<float2*>(kv_copies + bk + bv);
     }
-    if (m->fused) {  // the fused kernel's tagged copies of the token's keys and values
+    if (m->fused) {  // the fused kernel's tagged copies of the token's keys and values, attention stamps
         m->tk_k = reinterpret_cast<float*>(kv_copies);
         m->tk_v = reinterpret_cast<float*>(kv_copies + bk);
+        m->tk_stamps = reinterpret_cast<unsigned*>(kv_copies + bk + bv + br);
     }
     if ((e = cudaMemset(m->ws, 0, total)) != cudaSuccess ||
         (qwen3 && (e = dqhost::launch_rope_table(m->rope, d->max_ctx, d->head_dim, d->rope_theta, 0)) != cudaSuccess)) {
@@ -421,6 +424,7 @@ DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits
         dqhost::attention_bind_workspace(t, m->attn_ws);
         a.part = t.part;
         a.counters = t.counters;
+        a.stamps = m->tk_stamps;
         a.k_new = m->tk_k;
         a.v_new = m->tk_v;
         a.qwen = m->k_new != nullptr;

@@ -108,6 +108,7 @@ struct TkMisc {
     int sync_ok;
     int ttotal;                // the block's tiles over the token
     unsigned tokpar;           // parity of the token count (tags of vectors written once per layer)
+    unsigned tokseq;           // the token count
     int last_out;              // this block finished last
 };
 static_assert(sizeof(TkMisc) <= 256, "misc region");
@@ -618,7 +619,7 @@ __device__ __forceinline__ int2 tk_gemv(int p, int T, int icur)
 
 // Attention phase p: items (key chunk, KV head) spread over the blocks, in the
 // tagged mode of attn_block (q and the new key and value are polled by their
-// tags, the output is tagged, the merge counters count on across layers).
+// tags, the chunks meet through release/acquire stamps, the output is tagged).
 __device__ __forceinline__ void tk_attention(int p)
 {
     const TokenArgs& A = tk_args();
@@ -655,15 +656,22 @@ __device__ __forceinline__ void tk_attention(int p)
         t.rope = A.rope;
         t.eps = A.eps;
         t.tag = 1 + static_cast<int>(tk_par_layer(l) ^ (A.skew != 0 ? 1u : 0u));
-        t.ctr_base = l * nact;
+        t.stamps = A.stamps;
+        t.seq = tk_misc().tokseq * static_cast<unsigned>(A.n_layers) + static_cast<unsigned>(l) + 1u;
         t.v_new = A.v_new;
         t.wait_ns = A.wait_ns;
         if (A.trace && sub == 0)  // the block's first item
             t.trace = A.trace + (static_cast<size_t>(blockIdx.x) * (5 * A.n_layers + 1) + p) * 8;
         AttnSmem& sm = *reinterpret_cast<AttnSmem*>(tk_xq() + sub * (TK_ATT_STAGING / 4));
         const int bar = ATT_BAR - sub;
+        // Items are numbered chunks first, merging (last) chunks after them: every
+        // pair of warp groups takes its items in increasing order, so a merging item
+        // only ever waits for items that their groups run before any merging one.
+        const int nplain = (nact - 1) * A.n_kv;
         for (int item = 2 * blockIdx.x + sub; item < nact * A.n_kv; item += 2 * gridDim.x) {
-            if (!attn_block(t, item % nact, item / nact, group, sm, false, bar, 32 * group * sub)) {
+            const int c = item < nplain ? item % (nact - 1) : nact - 1;
+            const int g = item < nplain ? item / (nact - 1) : item - nplain;
+            if (!attn_block(t, c, g, group, sm, false, bar, 32 * group * sub)) {
                 if ((threadIdx.x & 31) == 0)
                     tk_give_up(DEVERR_TIMEOUT_TAG);
                 break;  // every warp of the item returned false together
@@ -760,7 +768,8 @@ __global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_const
         m.issued_hi = 0;
         m.last_out = 0;
         // written only by the previous launch's last block: the same value in every block
-        m.tokpar = ld_relaxed_u32(a.bar + TB_TOKEN) & 1u;
+        m.tokseq = ld_relaxed_u32(a.bar + TB_TOKEN);
+        m.tokpar = m.tokseq & 1u;
         for (int T = 0; T < min(TK_NSTAGE, m.ttotal); ++T)
             tk_issue(T, icur);
         if (blockIdx.x == 0) {
@@ -805,8 +814,7 @@ __global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_const
     // The last block to finish puts the launch-state area back for the next launch:
     // every block counts itself out only after its last wait and its last
     // write (dead blocks too), so nothing reads the counters or the tagged vectors
-    // any more.  The exit count and the attention's merge counters go back to zero
-    // and the token count advances (the
+    // any more.  The exit count goes back to zero and the token count advances (the
     // tags of the next token follow from it), so a launch's arguments never
     // depend on host-side state.  After a wait ran out somewhere, writes may be
     // missing and the tags out of step: the tagged vectors and the token count go
@@ -833,10 +841,12 @@ __global__ void __launch_bounds__(TK_THREADS, 1) token_kernel(const __grid_const
                 a.k_new[i] = 0.f;
                 a.v_new[i] = 0.f;
             }
+            // the attention's chunk stamps: the token count restarts, so old stamps
+            // could match a later token's
+            for (int i = tid; i < a.n_kv * ATT_CHUNKS; i += TK_THREADS)
+                a.stamps[i] = 0u;
         }
         __syncthreads();
-        for (int i = tid; i < ATT_COUNTER_BYTES / 4; i += TK_THREADS)  // the attention's merge counters
-            a.counters[i] = 0;
         if (tid == 0) {
             const unsigned tok = ld_relaxed_u32(a.bar + TB_TOKEN);
             atomicExch(a.bar + TB_TOKEN, fault ? 0u : tok + 1u);

@@ -59,7 +59,8 @@ struct TokenArgs {
     float* attn;               // [n_q hd]
     float* act;                // [ffn]
     float* part;               // attention partials
-    int* counters;             // attention merge counters (zero between phases)
+    int* counters;             // attention merge counters (unused here: zero)
+    unsigned* stamps;          // attention chunk stamps [n_kv][ATT_CHUNKS]
     int fold;                  // 1: pos + 1 <= TK_FOLD_KEYS, the attention is folded into the O phase
     float* k_new;              // the token's keys [n_kv hd], tagged: as projected (Qwen3) or their fp16 values
     float* v_new;              // the token's values [n_kv hd], tagged fp16 values

@@ -425,6 +425,17 @@ def test_decode_short_context_fold_boundary(dq, orc, mode, qwen3):
     _run_decode(dq, orc, m, kv, [1, 2, 3, 4, 5], flags=flags, fused=fused)
 
 
+@pytest.mark.parametrize("mode", ["fused", "kernels"])
+def test_decode_many_attention_items_per_block(dq, orc, mode):
+    # 32 KV heads x 32 key chunks = 1024 attention items: in the fused kernel every
+    # pair of warp groups runs several, the merging chunks after the plain ones
+    m = synth.make_model(35, n_layers=2, hidden=2048, ffn=2048, n_q_heads=32, n_kv_heads=32, head_dim=128,
+                         vocab=300, max_ctx=1200, qwen3_attention=True)
+    kv = synth.make_kv_cache(35, m, 1100)
+    flags, fused = MODES[mode]
+    _run_decode(dq, orc, m, kv, [1100, 1101], flags=flags, fused=fused)
+
+
 @pytest.mark.parametrize("n_q,n_kv", [(16, 2), (8, 8)])
 @pytest.mark.parametrize("mode", ["fused", "kernels"])
 def test_decode_group_sizes(dq, orc, mode, n_q, n_kv):
