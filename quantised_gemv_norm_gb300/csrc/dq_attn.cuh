@@ -385,14 +385,23 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
         __threadfence();
     }
     // merge the chunk partials of this warp's head: lane cc holds chunk cc's (m, l)
-    // and weight (nact <= 32), the output rows come 8 chunks at a time, so the
-    // merge costs a few round trips whatever the chunk count
+    // and weight (nact <= 32), the output rows come 8 chunks at a time; the first 8
+    // rows are loaded together with (m, l), so up to 8 chunks cost one round trip
+    // and up to 16 two
+    auto load_rows = [&](float4 (&ov)[8], int c0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            ov[i] = c0 + i < nload ? __ldcg(reinterpret_cast<const float4*>(hp + (c0 + i) * ATT_PART + 4) + lane)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
     float mc = -INFINITY, lc = 0.f;
     if (lane < nload) {
         const float2 ml = __ldcg(reinterpret_cast<const float2*>(hp + lane * ATT_PART));
         mc = ml.x;
         lc = ml.y;
     }
+    float4 ov[8];
+    load_rows(ov, 0);
     const float mown = nload < nact ? m : -INFINITY;  // tagged mode: this item's own chunk
     const float M = fmaxf(warp_max(mc), mown);
     const float wc = lane < nload ? expf(mc - M) : 0.f;
@@ -400,11 +409,8 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
     const float Ls = warp_sum(lc * wc) + (nload < nact ? l * wown : 0.f);
     float r0 = o0 * wown, r1 = o1 * wown, r2 = o2 * wown, r3 = o3 * wown;
     for (int c0 = 0; c0 < nload; c0 += 8) {
-        float4 ov[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            ov[i] = c0 + i < nload ? __ldcg(reinterpret_cast<const float4*>(hp + (c0 + i) * ATT_PART + 4) + lane)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c0 > 0)
+            load_rows(ov, c0);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float w = __shfl_sync(0xffffffffu, wc, (c0 + i) & 31);  // 0 past nload
@@ -416,7 +422,7 @@ __device__ __forceinline__ bool attn_block(const AttnArgs& a, int c, int g, int 
     att_st_out(a.out + static_cast<size_t>(h) * ATT_HD + 4 * lane, make_float4(r0 * inv, r1 * inv, r2 * inv, r3 * inv),
                a.tag);
     att_stamp(a, 7, tid);
-    if (!tagged) {  // tagged mode: the counters count on across layers; the launch zeroes them at its end
+    if (!tagged) {  // the counter goes back to zero for the next call (tagged mode uses stamps)
         named_bar_sync(bar, nthr);
         if (tid == 0)
             a.counters[g] = 0;
