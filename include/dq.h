@@ -187,8 +187,9 @@ DQ_API int dq_gemv_q2k(const void* W_blocks, const float* x, float* y, int rows,
  * [2], [5] activation arrived and quantised, [7] activation in registers, [1]
  * first weight tile ready; [6] unused; 64 bytes per block and phase.  In an
  * attention phase the block's first item writes global-timer ns at [1] q ready,
- * [3] keys staged, [5] partial computed, [6] merge decided, [7] output stored.  A tensor-core dq_matmul_q4k_path writes, for
- * block 0 and its first 32 half-block stages, 8 SM clock stamps per stage at
+ * [3] keys staged, [5] partial computed, [6] merge decided, [7] output
+ * stored.  A tensor-core dq_matmul_q4k_path writes, for block 0 and its first
+ * 32 stages (one Q4_K block column each), 8 SM clock stamps per stage at
  * buffer[8 stage]: operands seen ready and MMAs issued (control thread), stage
  * start, weights landed, operand buffer free and stage written (thread 0).
  * NULL turns tracing off.  Not for use while
@@ -296,7 +297,7 @@ DQ_API int dq_attention_decode_rope(const float* q, const float* k_new, void* k_
  * M times; K <= 16384).  DQ_MATMUL_TENSOR reads W once for all tokens on the
  * tensor cores (tcgen05.mma, fp16 operands: each weight and activation is
  * rounded to fp16, |X| must stay below 65504; fp32 accumulation).
- * DQ_MATMUL_AUTO picks CUDA cores for M <= 2 and tensor cores for M >= 3 (the
+ * DQ_MATMUL_AUTO picks CUDA cores for M <= 3 and tensor cores for M >= 4 (the
  * measured crossover on the 12288 x 4096 table).
  * Errors: NULL -> DQ_ERR_NULL; M, rows, K or path out of range ->
  * DQ_ERR_SHAPE; misaligned W or X -> DQ_ERR_ALIGN; CUDA-core path with

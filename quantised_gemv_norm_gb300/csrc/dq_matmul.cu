@@ -11,13 +11,14 @@
 //     per tensor-memory lane) and walks K in Q4_K block columns.  Each block
 //     column of the tile's rows (one 144-byte block per row, rows row_bytes
 //     apart) streams into a shared-memory ring with one 2-D tensor (TMA) copy.
-//     Per half block (128 K) every thread dequantises 64 weights of one row to
+//     Per block column (256 K) every thread dequantises 64 weights of one row to
 //     fp16 in registers and stores them straight into an A buffer in tensor
 //     memory (tcgen05.st); the tokens' activations are staged in shared memory
-//     as fp16 in the UMMA K-major core-matrix layout; one thread issues eight
-//     tcgen05.mma (M = 128, N = tokens rounded up to 16, K = 16, A from tensor
-//     memory) accumulating in fp32 in tensor memory.  Two A/B buffers: the
-//     next half block is dequantised while the MMAs run; their commit releases
+//     as fp16 in the UMMA K-major core-matrix layout.  Four control warps, one per
+//     scheduler, issue the stage's sixteen tcgen05.mma (M = 128, N = tokens
+//     rounded up to 16, K = 16, A from tensor memory), control warp q those of
+//     fp32 accumulator q in tensor memory: one thread took about 125 cycles an MMA.  Two A/B buffers: the
+//     next block column is dequantised while the MMAs run; their commit releases
 //     a buffer.  The epilogue reads the accumulator with tcgen05.ld.
 //     A in tensor memory keeps the dequantised weights out of shared memory,
 //     whose bandwidth the MMAs would otherwise share with the dequantisation.
@@ -36,18 +37,28 @@
 namespace dq {
 
 constexpr int MM_DQ_WARPS = 16;                // dequantisation / staging / epilogue warps
-constexpr int MM_CTRL = MM_DQ_WARPS;           // the control warp: copies and MMAs
-constexpr int MM_THREADS = 32 * (MM_DQ_WARPS + 1);
+constexpr int MM_CTRL = MM_DQ_WARPS;           // the first control warp (copies and MMAs)
+#ifndef MM_NCTRL_DEF
+#define MM_NCTRL_DEF 4
+#endif
+// control warps, one per scheduler: control warp q issues the MMAs of accumulator q
+constexpr int MM_NCTRL = MM_NCTRL_DEF;
+constexpr int MM_THREADS = 32 * (MM_DQ_WARPS + MM_NCTRL);
 constexpr int MM_ROWS = 128;                   // rows per tile = UMMA M
-constexpr int MM_KC = 128;                     // K per MMA stage: half a Q4_K block
+constexpr int MM_KC = 256;                     // K per MMA stage: one Q4_K block column
 constexpr int MM_BPS = 4;                      // Q4_K block columns per ring slot
 constexpr int MM_ROWB = MM_BPS * Q4K_BYTES + 16;  // 592: a slot row (4 blocks and 16 bytes of the next;
                                                   // the odd 16-byte stride keeps 8 rows on distinct banks)
 constexpr int MM_NS_MAX = 4;
-// operand (A in tensor memory, B in shared) buffers at most: 3 and 4 measured no
-// faster than 2 (the dequantising warps, not the MMAs' wait for operands, set the pace)
-constexpr int MM_NAB_MAX = 2;
+// operand (A in tensor memory, B in shared) buffers at most, where tensor memory
+// holds them (3 measured no faster than 2: the dequantising warps set the pace)
+#ifndef MM_NAB_MAX_DEF
+#define MM_NAB_MAX_DEF 3
+#endif
+constexpr int MM_NAB_MAX = MM_NAB_MAX_DEF;
 constexpr int MM_ACC = 4;                      // independent accumulators (MMA s of a stage adds into s % 4)
+// every accumulator's MMAs come from one thread (one thread's MMAs run in order)
+static_assert(MM_ACC % MM_NCTRL == 0, "control warps per accumulator");
 constexpr int MM_TA_COLS = MM_KC / 2;          // columns of one A buffer (two fp16 per column)
 // Tensor memory: accumulator i in columns [i NT, (i + 1) NT), then the nab A buffers.
 __host__ __device__ constexpr int mm_ta_col(int nt) { return MM_ACC * nt; }
@@ -148,7 +159,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
             mbar_init(&full[s], 1);
         for (int i = 0; i < nab; ++i) {
             mbar_init(&opready[i], MM_DQ_WARPS);
-            mbar_init(&opfree[i], 1);
+            mbar_init(&opfree[i], MM_NCTRL);
         }
         fence_mbar_init();
         *fail = 0;
@@ -176,8 +187,10 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
         return __all_sync(0xffffffffu, wait(bar, parity, code)) != 0;
     };
 
-    if (warp == MM_CTRL) {
-        // ---- control: the ring's copies and the MMAs (one thread)
+    if (warp >= MM_CTRL) {
+        // ---- control: the ring's copies (control warp 0) and the MMAs (one thread
+        // of each control warp: the MMAs of accumulator cq)
+        const int cq = warp - MM_CTRL;
         if (lane == 0) {
             constexpr uint32_t idesc = umma_idesc_f16_f32(MM_ROWS, NT);
             const uint64_t pol = l2_evict_first_policy();
@@ -195,13 +208,14 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                     tma_load_2d(ring + s * slot_bytes, &a.tmap, q * (MM_BPS * Q4K_BYTES / 8), rt0, &full[s], pol);
                     *issued = bg + 1;
                 };
-                for (int q = 0; q < min(a.ns, ngrp); ++q)
-                    issue(q);
-                for (int hc = 0; hc < 2 * nblk; ++hc) {
-                    const int g = g0 + hc, buf = g % nab, c = hc >> 1;
+                if (cq == 0)
+                    for (int q = 0; q < min(a.ns, ngrp); ++q)
+                        issue(q);
+                for (int hc = 0; hc < nblk; ++hc) {
+                    const int g = g0 + hc, buf = g % nab, c = hc;
                     if (!(ok = wait(&opready[buf], (g / nab) & 1, DEVERR_TIMEOUT_FULL)))
                         break;
-                    unsigned long long* tr = (a.trace && b == 0 && hc < 32) ? a.trace + 8 * hc : nullptr;
+                    unsigned long long* tr = (a.trace && b == 0 && cq == 0 && hc < 32) ? a.trace + 8 * hc : nullptr;
                     if (tr)
                         tr[0] = clock64();
                     tc_fence_after_sync();
@@ -211,20 +225,22 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                     // into accumulator s % MM_ACC, so consecutive MMAs do not wait on each other.
 #pragma unroll
                     for (int s = 0; s < MM_KC / 16; ++s)
-                        umma_f16_ta(tbase + NT * (s % MM_ACC), ta + 8 * s,
-                                    bd + static_cast<uint64_t>((2 * MM_LBO * s) >> 4), idesc,
-                                    (hc > 0 || s >= MM_ACC) ? 1u : 0u);
+                        if (s % MM_NCTRL == cq)
+                            umma_f16_ta(tbase + NT * (s % MM_ACC), ta + 8 * s,
+                                        bd + static_cast<uint64_t>((2 * MM_LBO * s) >> 4), idesc,
+                                        (hc > 0 || s >= MM_ACC) ? 1u : 0u);
                     umma_commit(&opfree[buf]);
-                    *committed = g + 1;
+                    if (cq == 0)
+                        *committed = g + 1;
                     if (tr)
                         tr[1] = clock64();
                     // the last stage of a slot's block columns is dequantised: refill the slot
                     const int q = c / MM_BPS;
-                    if ((hc + 1 == 2 * nblk || (hc + 1) % (2 * MM_BPS) == 0) && q + a.ns < ngrp)
+                    if (cq == 0 && (hc + 1 == nblk || (hc + 1) % MM_BPS == 0) && q + a.ns < ngrp)
                         issue(q + a.ns);
                 }
                 bg0 += ngrp;
-                g0 += 2 * nblk;
+                g0 += nblk;
             }
         }
         __syncwarp();  // the warp reconverges before the block-wide barrier below
@@ -240,12 +256,12 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
             // processed (item t = tid + 256 i: token t % NT, 8-element group t / NT)
             float4 xn[NXI][2];
             auto load_x = [&](int hcn) {
-                const int kb = (hcn >> 1) * 256 + (hcn & 1) * MM_KC;
+                const int kb = hcn * MM_KC;
 #pragma unroll
                 for (int i = 0; i < NXI; ++i) {
                     const int it = tid + NDQ * i;
                     const int n = it % NT, kg = it / NT;
-                    if (it < NT * (MM_KC / 8) && n < a.M && hcn < 2 * nblk) {
+                    if (it < NT * (MM_KC / 8) && n < a.M && hcn < nblk) {
                         const float4* xp =
                             reinterpret_cast<const float4*>(a.X + static_cast<size_t>(n) * a.K + kb + 8 * kg);
                         xn[i][0] = __ldg(xp);
@@ -255,14 +271,14 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
             };
             load_x(0);
             bool ok = true;
-            for (int hc = 0; hc < 2 * nblk; ++hc) {
-                const int c = hc >> 1, half = hc & 1;
+            for (int hc = 0; hc < nblk; ++hc) {
+                const int c = hc;
                 const int g = g0 + hc, buf = g % nab;
                 const int bg = bg0 + c / MM_BPS;
                 unsigned long long* tr = (a.trace && b == 0 && tid == 0 && hc < 32) ? a.trace + 8 * hc : nullptr;
                 if (tr)
                     tr[2] = clock64();
-                if (hc % (2 * MM_BPS) == 0 && !(ok = warp_wait(&full[bg % a.ns], (bg / a.ns) & 1, DEVERR_TIMEOUT_FULL)))
+                if (hc % MM_BPS == 0 && !(ok = warp_wait(&full[bg % a.ns], (bg / a.ns) & 1, DEVERR_TIMEOUT_FULL)))
                     break;
                 if (tr)
                     tr[3] = clock64();
@@ -273,40 +289,45 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                 uint8_t* Bt = Bbuf + buf * mm_b_bytes(NT);
                 const uint8_t* slot = ring + (bg % a.ns) * slot_bytes + (c % MM_BPS) * Q4K_BYTES;
                 // weights: thread (warp w, lane) dequantises row 32 (w % 4) + lane,
-                // sub-block 4 half + w / 4 of this half block, into the A buffer in tensor
-                // memory (one lane per row, two fp16 per column; the four warps of a lane
-                // quarter take the four sub-blocks)
+                // sub-blocks w / 4 and w / 4 + 4 of this block column, into the A buffer
+                // in tensor memory (one lane per row, two fp16 per column; the four warps
+                // of a lane quarter take the eight sub-blocks, two each, sharing the header)
                 {
                     const int row = 32 * (warp & 3) + lane;
-                    const int j = 4 * half + (warp >> 2);
-                    uint32_t v[16];
+                    const uint32_t tcol = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + mm_ta_col(NT) +
+                                          MM_TA_COLS * buf;
+                    uint32_t v0[16], v1[16];
                     if (row < nrows) {
                         const uint8_t* bp = slot + row * MM_ROWB;
                         const uint4 hd = lds128(bp);
-                        const uint4 cw = lds128(bp + 16 + 16 * j);
                         const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
-                        const uint32_t s_lo = j < 6 ? hd.y : hd.z, s_hi = j < 6 ? hd.z : hd.w;
-                        const uint32_t m_lo = j < 3 ? hd.z : hd.w, m_hi = j < 3 ? hd.w : 0u;
-                        const int sc = static_cast<int>(__funnelshift_r(s_lo, s_hi, (6 * j) & 31) & 63u);
-                        const int mn = static_cast<int>(__funnelshift_r(m_lo, m_hi, (48 + 6 * j) & 31) & 63u);
-                        const __half2 A = __float2half2_rn(d * static_cast<float>(sc));
-                        const __half2 B = __float2half2_rn(dmin * static_cast<float>(mn));
-                        // byte i of the 16: low nibble weight 32j + i, high nibble weight
-                        // 32j + 16 + i; column c of the sub-block holds weights 2c, 2c + 1
-                        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const uint32_t t = __byte_perm(words[w], 0u, 0x3120);  // b0 b2 b1 b3
-                            mm_dequant_word(t, A, B, v[2 * w], v[2 * w + 1], v[8 + 2 * w], v[8 + 2 * w + 1]);
+                        for (int h = 0; h < 2; ++h) {
+                            const int j = (warp >> 2) + 4 * h;
+                            const uint4 cw = lds128(bp + 16 + 16 * j);
+                            const uint32_t s_lo = j < 6 ? hd.y : hd.z, s_hi = j < 6 ? hd.z : hd.w;
+                            const uint32_t m_lo = j < 3 ? hd.z : hd.w, m_hi = j < 3 ? hd.w : 0u;
+                            const int sc = static_cast<int>(__funnelshift_r(s_lo, s_hi, (6 * j) & 31) & 63u);
+                            const int mn = static_cast<int>(__funnelshift_r(m_lo, m_hi, (48 + 6 * j) & 31) & 63u);
+                            const __half2 A = __float2half2_rn(d * static_cast<float>(sc));
+                            const __half2 B = __float2half2_rn(dmin * static_cast<float>(mn));
+                            // byte i of the 16: low nibble weight 32j + i, high nibble weight
+                            // 32j + 16 + i; column c of the sub-block holds weights 2c, 2c + 1
+                            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+                            uint32_t(&v)[16] = h ? v1 : v0;
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                const uint32_t t = __byte_perm(words[w], 0u, 0x3120);  // b0 b2 b1 b3
+                                mm_dequant_word(t, A, B, v[2 * w], v[2 * w + 1], v[8 + 2 * w], v[8 + 2 * w + 1]);
+                            }
                         }
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            v[i] = 0u;
+                            v0[i] = v1[i] = 0u;
                     }
-                    tmem_st16(tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + mm_ta_col(NT) +
-                                  MM_TA_COLS * buf + 16 * (warp >> 2),
-                              v);
+                    tmem_st16(tcol + 16 * (warp >> 2), v0);
+                    tmem_st16(tcol + 16 * ((warp >> 2) + 4), v1);
                 }
                 // activations: fp32 -> fp16 into the B buffer (consecutive threads take
                 // consecutive tokens), then the next stage's loads
@@ -336,7 +357,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                 break;
             // accumulator complete -> Y (warps 0-3: one lane quarter each)
             if (warp < 4) {
-                const int glast = g0 + 2 * nblk - 1;
+                const int glast = g0 + nblk - 1;
                 if (!warp_wait(&opfree[glast % nab], (glast / nab) & 1, DEVERR_TIMEOUT_MMA))
                     break;
                 tc_fence_after_sync();
@@ -370,7 +391,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                 tc_fence_before_sync();
             }
             bg0 += ngrp;
-            g0 += 2 * nblk;
+            g0 += nblk;
         }
     }
     // After a failed wait: let this block's copies and MMAs in flight finish (bounded).
@@ -454,7 +475,8 @@ static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, i
     a.ns = 2;
     for (int nab = dq::MM_NAB_MAX; nab >= 2 && a.nab == 2; --nab)
         for (int ns = dq::MM_NS_MAX; ns >= 2; --ns)
-            if (dq::mm_smem_bytes(nt, ns, nab, a.box_rows) <= 227 * 1024) {
+            if (dq::mm_smem_bytes(nt, ns, nab, a.box_rows) <= 227 * 1024 &&
+                dq::MM_ACC * nt + nab * dq::MM_TA_COLS <= 512) {  // tensor memory holds it
                 a.nab = nab;
                 a.ns = ns;
                 break;
@@ -489,8 +511,8 @@ DQ_API int dq_matmul_q4k_path(const void* W_blocks, const float* X, float* Y, in
         return DQ_ERR_SHAPE;
     if (!dqhost::aligned16(W_blocks) || !dqhost::aligned16(X))
         return DQ_ERR_ALIGN;
-    // measured crossover: one GEMV per token is faster up to M = 2
-    const bool tensor = path == DQ_MATMUL_TENSOR || (path == DQ_MATMUL_AUTO && M >= 3);
+    // measured crossover: one GEMV per token is faster up to M = 3
+    const bool tensor = path == DQ_MATMUL_TENSOR || (path == DQ_MATMUL_AUTO && M >= 4);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (tensor)
         return dqhost::launch_matmul_tc(static_cast<const uint8_t*>(W_blocks), X, Y, M, rows, K, s);
@@ -507,7 +529,11 @@ DQ_API int dq_matmul_q4k_path(const void* W_blocks, const float* X, float* Y, in
         a.x = X + static_cast<size_t>(m) * K;
         a.epi = dq::EPI_STORE;
         a.y = Y + static_cast<size_t>(m) * rows;
-        cudaError_t e = dqhost::launch_gemv(plan, a, s, false);
+        // dependent launches: the first may follow a kernel that writes W (only L2
+        // prefetches before its wait); the later ones follow this loop's own GEMVs,
+        // which do not, so their first copies leave before the wait
+        a.w_late = m == 0 ? 1 : 0;
+        cudaError_t e = dqhost::launch_gemv(plan, a, s, true);
         if (e != cudaSuccess)
             return dqhost::set_cuda_error(e);
     }
