@@ -552,13 +552,14 @@ def run_standalone(device, reps: int = 20) -> dict:
     return out
 
 
-OP_PROBES = ("attention_512", "gemv_bf16_4096", "rmsnorm_default", "rmsnorm_one_thread")
+OP_PROBES = ("attention_512", "gemv_bf16_4096", "rmsnorm_default", "rmsnorm_one_thread", "matmul_tensor_m16")
 
 
 def run_op_probe(args):
     """`probe_reps` launches of one standalone entry point on a small case (for
     profilers): attention over 513 keys of a 32/8-head cache, the bf16 GEMV on
-    4096x4096, or RMSNorm of 64x2048 with the default block or one thread per row."""
+    4096x4096, RMSNorm of 64x2048 with the default block or one thread per row, or
+    the tensor-core product of 16 tokens over the 12288x4096 Q4_K table."""
     import torch
 
     from quantised_gemv_norm_gb300 import build, dq
@@ -581,6 +582,11 @@ def run_op_probe(args):
         x = torch.randn((4096,), generator=gen, device="cuda").to(torch.bfloat16)
         for _ in range(args.probe_reps):
             y = dq.gemv_bf16(W, x)
+    elif kind == "matmul_tensor_m16":
+        W = torch.from_numpy(synth.quant_matrix(SEED, synth.FMT_Q4K, SWEEP_ROWS, SWEEP_K)).cuda()
+        X = torch.from_numpy(np.stack([synth.activation(SEED, SWEEP_K, m) for m in range(16)])).cuda()
+        for _ in range(args.probe_reps):
+            y = dq.matmul_q4k(W, X, path=dq.MATMUL_TENSOR)
     else:
         x = torch.randn((64, 2048), generator=gen, device="cuda")
         g = 1.0 + 0.1 * torch.randn((2048,), generator=gen, device="cuda")
