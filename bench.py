@@ -265,14 +265,10 @@ def run_ours(args):
 
     # ---- end to end through the C ABI with host buffers: pinned x in, logits out, per step
     x_host = torch.from_numpy(np.stack([synth.decode_input(SEED + 7, m.hidden, t) for t in range(K + W)])).pin_memory()
-    x_dev = torch.empty(m.hidden, dtype=torch.float32, device=device)
     out_host = torch.empty(m.vocab, dtype=torch.float32).pin_memory()
 
-    def e2e_step(t):
-        x_dev.copy_(x_host[t], non_blocking=True)
-        model.step_raw(x_dev.data_ptr(), 0, logits.data_ptr(), sh)
-        out_host.copy_(logits, non_blocking=True)
-        stream.synchronize()
+    def e2e_step(t):  # dq_decode_step_host: copy in, token, copy out, wait
+        model.step_host(x_host[t], 0, out_host)
 
     for t in range(W):
         e2e_step(t)

@@ -401,6 +401,15 @@ DQ_API int dq_model_create(const dq_model_desc* desc, dq_model** out);
  * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE, DQ_ERR_CUDA. */
 DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits, void* stream);
 
+/* dq_decode_step from host memory: copies x_host (fp32 [hidden]) to the
+ * model's own device buffer, enqueues the token on `stream`, copies the logits
+ * (fp32 [vocab]) to logits_host and waits for the stream.  Page-locked host
+ * buffers make the copies asynchronous; pageable ones work and are staged by the
+ * driver.  Synchronises, so it cannot be captured into a CUDA graph.  Calls on one
+ * model must not overlap in time.
+ * Errors: DQ_ERR_NULL, DQ_ERR_SHAPE, DQ_ERR_CUDA. */
+DQ_API int dq_decode_step_host(dq_model* m, const float* x_host, int pos, float* logits_host, void* stream);
+
 /* Number of kernels one dq_decode_step launches. */
 DQ_API int dq_model_launches_per_step(const dq_model* m);
 

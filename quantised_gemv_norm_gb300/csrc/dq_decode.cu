@@ -66,6 +66,8 @@ struct dq_model {
     float* tk_k;        // fused kernel: tagged copies of the token's keys and values [n_kv hd]
     float* tk_v;
     unsigned* tk_stamps; // fused kernel: attention chunk stamps [n_kv][ATT_CHUNKS]
+    float* io_x;         // dq_decode_step_host: the input [hidden] and logits [vocab] on the device
+    float* io_logits;
     // fused token kernel
     bool fused;
     dqhost::TokenPlan tplan;
@@ -311,8 +313,9 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
                  bl = up(sizeof(dq::TokenLayer) * d->n_layers), bb = 256,
                  bk = (qwen3 || m->fused) ? up(sizeof(float) * kvdim) : 0, bv = m->fused ? up(sizeof(float) * kvdim) : 0,
                  br = qwen3 ? up(sizeof(float2) * static_cast<size_t>(d->max_ctx) * (d->head_dim / 2)) : 0,
-                 bt = m->fused ? up(sizeof(unsigned) * d->n_kv_heads * dq::ATT_CHUNKS) : 0;
-    const size_t total = bx + bq + ba + bf + bs + bw + bl + bb + bk + bv + br + bt;
+                 bt = m->fused ? up(sizeof(unsigned) * d->n_kv_heads * dq::ATT_CHUNKS) : 0,
+                 bix = up(sizeof(float) * d->hidden), bil = up(sizeof(float) * d->vocab);
+    const size_t total = bx + bq + ba + bf + bs + bw + bl + bb + bk + bv + br + bt + bix + bil;
     // diagnostics: an injected allocation failure (dq_debug_fail_next_allocs)
     int inject = g_fail_allocs.load();
     while (inject > 0 && !g_fail_allocs.compare_exchange_weak(inject, inject - 1)) {
@@ -343,6 +346,9 @@ DQ_API int dq_model_create(const dq_model_desc* d, dq_model** out)
         m->tk_v = reinterpret_cast<float*>(kv_copies + bk);
         m->tk_stamps = reinterpret_cast<unsigned*>(kv_copies + bk + bv + br);
     }
+    // device copies of dq_decode_step_host's input and logits
+    m->io_x = reinterpret_cast<float*>(kv_copies + bk + bv + br + bt);
+    m->io_logits = reinterpret_cast<float*>(kv_copies + bk + bv + br + bt + bix);
     if ((e = cudaMemset(m->ws, 0, total)) != cudaSuccess ||
         (qwen3 && (e = dqhost::launch_rope_table(m->rope, d->max_ctx, d->head_dim, d->rope_theta, 0)) != cudaSuccess)) {
         free_model(m);
@@ -453,6 +459,26 @@ DQ_API int dq_decode_step(dq_model* m, const float* x_in, int pos, float* logits
         return dqhost::set_cuda_error(e);
     e = m->use_graph ? cudaGraphLaunch(m->exec, s) : enqueue_token(m, s);
     return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
+}
+
+DQ_API int dq_decode_step_host(dq_model* m, const float* x_host, int pos, float* logits_host, void* stream)
+{
+    if (!m || !x_host || !logits_host)
+        return DQ_ERR_NULL;
+    if (pos < 0 || pos >= m->max_ctx)
+        return DQ_ERR_SHAPE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(m->io_x, x_host, sizeof(float) * m->hidden, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess)
+        return dqhost::set_cuda_error(e);
+    const int st = dq_decode_step(m, m->io_x, pos, m->io_logits, s);
+    if (st != DQ_OK)
+        return st;
+    if ((e = cudaMemcpyAsync(logits_host, m->io_logits, sizeof(float) * m->vocab, cudaMemcpyDeviceToHost, s)) !=
+            cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess)
+        return dqhost::set_cuda_error(e);
+    return DQ_OK;
 }
 
 DQ_API int dq_model_launches_per_step(const dq_model* m)

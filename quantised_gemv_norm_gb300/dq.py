@@ -50,6 +50,7 @@ SIGNATURES = {
     "dq_matmul_q4k_path": (I, [P, P, P, I, I, I, I, P]),
     "dq_model_create": (I, [P, P]),
     "dq_decode_step": (I, [P, P, I, P, P]),
+    "dq_decode_step_host": (I, [P, P, I, P, P]),
     "dq_model_launches_per_step": (I, [P]),
     "dq_model_fused": (I, [P]),
     "dq_model_enqueue_kernel": (I, [P, I, I, P]),
@@ -366,6 +367,22 @@ class Model:
         """Pointer-level call (no tensor checks), for timing loops."""
         _check("dq_decode_step", _lib.dq_decode_step(self._h, ctypes.c_void_p(x_ptr), int(pos),
                                                      ctypes.c_void_p(logits_ptr), ctypes.c_void_p(stream_handle)))
+
+    def step_host(self, x_host: torch.Tensor, pos: int, logits_host: torch.Tensor) -> torch.Tensor:
+        """One token from host memory (fp32 CPU tensors, page-locked for asynchronous
+        copies): the C call copies x in, runs the token, copies the logits out and
+        waits for the stream."""
+        if x_host.device.type != "cpu" or logits_host.device.type != "cpu":
+            raise ValueError("step_host takes CPU tensors")
+        if not (x_host.is_contiguous() and logits_host.is_contiguous()):
+            raise ValueError("tensors must be contiguous")
+        if x_host.dtype != torch.float32 or logits_host.dtype != torch.float32:
+            raise ValueError("step_host takes fp32 tensors")
+        if x_host.numel() < self.hidden or logits_host.numel() < self.vocab:
+            raise ValueError("step_host: x needs hidden and logits vocab elements")
+        _check("dq_decode_step_host", _lib.dq_decode_step_host(self._h, ctypes.c_void_p(x_host.data_ptr()), int(pos),
+                                                               ctypes.c_void_p(logits_host.data_ptr()), _stream()))
+        return logits_host
 
     KERNEL_KINDS = ("qkv", "attention", "o_proj", "gate_up", "down", "vocab")
 

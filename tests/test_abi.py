@@ -91,6 +91,7 @@ def test_argument_errors_return_before_launch(lib):
         assert r(fake, fake, fake, fake, fake, fake, fake, fake, eps, 32, 8, 128, 16, 1, fake, 1 << 20, None) == -2
     assert lib.dq_rmsnorm(fake, P(24), fake, 1, 8, 1e-6, None) == -3  # gamma read as float4
     assert lib.dq_decode_step(None, fake, 0, fake, None) == -1
+    assert lib.dq_decode_step_host(None, fake, 0, fake, None) == -1
     h = P()
     assert lib.dq_model_create(None, ctypes.byref(h)) == -1
     assert lib.dq_model_destroy(None) == 0

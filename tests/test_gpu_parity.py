@@ -470,6 +470,37 @@ def test_decode_step_argument_errors(dq, orc, mode):
     assert dq.device_error() == 0
 
 
+@pytest.mark.parametrize("mode", ["fused", "kernels"])
+def test_decode_step_host_matches_device_step(dq, orc, mode):
+    # the host-buffer entry point: same logits bit for bit as the device one, and its
+    # argument errors (pinned and pageable host buffers both work)
+    from quantised_gemv_norm_gb300 import upload
+
+    m = synth.make_model(36, n_layers=2, hidden=2048, ffn=2048, n_q_heads=8, n_kv_heads=2, head_dim=128,
+                         vocab=300, max_ctx=16, qwen3_attention=True)
+    kv = synth.make_kv_cache(36, m, 3)
+    w = upload.to_device(m, kv)
+    model = dq.Model(**upload.model_kwargs(m), weights=w, flags=MODES[mode][0])
+    x = synth.decode_input(36, m.hidden)
+    ref = orc.decode_step(m, x, 3, kv.copy())
+    dev = model.step(cuda(x), 3).cpu().numpy()
+    for pinned in (True, False):
+        xh = torch.from_numpy(x.copy())
+        out = torch.empty(m.vocab, dtype=torch.float32)
+        if pinned:
+            xh, out = xh.pin_memory(), out.pin_memory()
+        got = model.step_host(xh, 3, out).numpy()
+        assert np.array_equal(got.view(np.uint32), dev.view(np.uint32))
+        assert normwise(got, ref) <= GEMV_TOL
+    lib = dq.load()
+    xh = torch.from_numpy(x.copy())
+    assert lib.dq_decode_step_host(model._h, None, 0, ctypes.c_void_p(xh.data_ptr()), None) == -1
+    assert lib.dq_decode_step_host(model._h, ctypes.c_void_p(xh.data_ptr()), m.max_ctx,
+                                   ctypes.c_void_p(xh.data_ptr()), None) == -2
+    model.close()
+    assert dq.device_error() == 0
+
+
 def test_decode_qwen3_attention_modes_agree(dq, orc):
     # the fused kernel and the separate kernels compute the same norm, rotation and cache row
     m = synth.make_model(27, n_layers=2, hidden=2048, ffn=4096, n_q_heads=8, n_kv_heads=2, head_dim=128,
