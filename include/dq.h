@@ -168,6 +168,17 @@ DQ_API int dq_gemv_q4k(const void* W_blocks, const float* x, float* y, int rows,
 DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream);
 DQ_API int dq_gemv_q2k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream);
 
+/* The same four products through one entry point, with flags.  fmt: DQ_FMT_BF16,
+ * DQ_FMT_Q4K, DQ_FMT_Q6K or DQ_FMT_Q2K (x is bf16 for DQ_FMT_BF16, else fp32).
+ * DQ_GEMV_STATIC_WEIGHTS: the kernel that precedes this call on the stream does
+ * not write W (a model's weight table, say), so the GEMV may copy W into shared
+ * memory before that kernel completes; x is still read, and y written, only after
+ * it.  A caller that sets the flag while the preceding kernel writes W gets
+ * undefined results.  flags = 0 is exactly dq_gemv_bf16/q4k/q6k/q2k.
+ * Errors: as those, plus DQ_ERR_SHAPE for an unknown format or flag. */
+#define DQ_GEMV_STATIC_WEIGHTS 1
+DQ_API int dq_gemv_ex(int fmt, const void* W, const void* x, float* y, int rows, int K, int flags, void* stream);
+
 /* Diagnostics: when `buffer` is not NULL, every later GEMV launch in this
  * process writes 8 unsigned 64-bit values per thread block at
  * buffer[8 * block]: global-timer ns at start, after set-up, after the

@@ -275,11 +275,8 @@ __global__ void dequant_q6k_kernel(const uint8_t* __restrict__ blocks, float* __
 
 // ------------------------------------------------------------------- C ABI
 
-#ifndef GEMV_PDL
-#define GEMV_PDL 1
-#endif
-
-static int gemv_entry(int fmt, const void* W, const void* x, float* y, int rows, int K, void* stream)
+static int gemv_entry(int fmt, const void* W, const void* x, float* y, int rows, int K, bool static_w,
+                      void* stream)
 {
     if (!W || !x || !y)
         return DQ_ERR_NULL;
@@ -298,12 +295,15 @@ static int gemv_entry(int fmt, const void* W, const void* x, float* y, int rows,
     else
         a.x = static_cast<const float*>(x);
     a.y = y;
-    // a dependent launch: its set-up and the L2 prefetch of its first tiles overlap
-    // the previous kernel's tail; the weights are copied only after the wait
-    a.w_late = GEMV_PDL;
-    cudaError_t e = dqhost::launch_gemv(plan, a, static_cast<cudaStream_t>(stream), GEMV_PDL != 0);
+    // a dependent launch: its set-up and its first weight requests overlap the
+    // previous kernel's tail.  Weights that kernel may write are only prefetched into
+    // L2 before the wait and copied after it; static weights are copied at once.
+    a.w_late = static_w ? 0 : 1;
+    cudaError_t e = dqhost::launch_gemv(plan, a, static_cast<cudaStream_t>(stream), true);
     return e == cudaSuccess ? DQ_OK : dqhost::set_cuda_error(e);
 }
+
+static int gemv_k_limit(int fmt) { return fmt == DQ_FMT_BF16 ? 24576 : 16384; }
 
 extern "C" {
 
@@ -317,28 +317,39 @@ DQ_API int dq_gemv_bf16(const void* W_bf16, const void* x_bf16, float* y, int ro
 {
     if (K > 24576)
         return DQ_ERR_UNSUPPORTED;
-    return gemv_entry(DQ_FMT_BF16, W_bf16, x_bf16, y, rows, K, stream);
+    return gemv_entry(DQ_FMT_BF16, W_bf16, x_bf16, y, rows, K, false, stream);
 }
 
 DQ_API int dq_gemv_q4k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream)
 {
     if (K > 16384)
         return DQ_ERR_UNSUPPORTED;
-    return gemv_entry(DQ_FMT_Q4K, W_blocks, x, y, rows, K, stream);
+    return gemv_entry(DQ_FMT_Q4K, W_blocks, x, y, rows, K, false, stream);
 }
 
 DQ_API int dq_gemv_q6k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream)
 {
     if (K > 16384)
         return DQ_ERR_UNSUPPORTED;
-    return gemv_entry(DQ_FMT_Q6K, W_blocks, x, y, rows, K, stream);
+    return gemv_entry(DQ_FMT_Q6K, W_blocks, x, y, rows, K, false, stream);
 }
 
 DQ_API int dq_gemv_q2k(const void* W_blocks, const float* x, float* y, int rows, int K, void* stream)
 {
     if (K > 16384)
         return DQ_ERR_UNSUPPORTED;
-    return gemv_entry(DQ_FMT_Q2K, W_blocks, x, y, rows, K, stream);
+    return gemv_entry(DQ_FMT_Q2K, W_blocks, x, y, rows, K, false, stream);
+}
+
+DQ_API int dq_gemv_ex(int fmt, const void* W, const void* x, float* y, int rows, int K, int flags, void* stream)
+{
+    if (fmt != DQ_FMT_BF16 && fmt != DQ_FMT_Q4K && fmt != DQ_FMT_Q6K && fmt != DQ_FMT_Q2K)
+        return DQ_ERR_SHAPE;
+    if (flags & ~DQ_GEMV_STATIC_WEIGHTS)
+        return DQ_ERR_SHAPE;
+    if (K > gemv_k_limit(fmt))
+        return DQ_ERR_UNSUPPORTED;
+    return gemv_entry(fmt, W, x, y, rows, K, (flags & DQ_GEMV_STATIC_WEIGHTS) != 0, stream);
 }
 
 static int dequant_entry(int fmt, const void* blocks, float* out, long long nblocks, void* stream)

@@ -38,6 +38,7 @@ SIGNATURES = {
     "dq_gemv_q4k": (I, [P, P, P, I, I, P]),
     "dq_gemv_q6k": (I, [P, P, P, I, I, P]),
     "dq_gemv_q2k": (I, [P, P, P, I, I, P]),
+    "dq_gemv_ex": (I, [I, P, P, P, I, I, I, P]),
     "dq_dequant_q4k": (I, [P, P, LL, P]),
     "dq_dequant_q6k": (I, [P, P, LL, P]),
     "dq_dequant_q2k": (I, [P, P, LL, P]),
@@ -202,6 +203,21 @@ def gemv_q2k(W: torch.Tensor, x: torch.Tensor, out=None):
     K = quant_K(FMT_Q2K, W.shape[1])
     out = torch.empty(rows, dtype=torch.float32, device=W.device) if out is None else out
     _check("dq_gemv_q2k", lib.dq_gemv_q2k(_ptr(W), _ptr(x), _ptr(out), rows, K, _stream()))
+    return out
+
+
+GEMV_STATIC_WEIGHTS = 1
+
+
+def gemv_ex(fmt: int, W: torch.Tensor, x: torch.Tensor, out=None, flags: int = 0):
+    """The four GEMVs through dq_gemv_ex.  flags: GEMV_STATIC_WEIGHTS when the kernel
+    before this call on the stream does not write W (the copies of W may then start
+    before that kernel completes)."""
+    lib = load()
+    rows = W.shape[0]
+    K = W.shape[1] if fmt == FMT_BF16 else quant_K(fmt, W.shape[1])
+    out = torch.empty(rows, dtype=torch.float32, device=W.device) if out is None else out
+    _check("dq_gemv_ex", lib.dq_gemv_ex(int(fmt), _ptr(W), _ptr(x), _ptr(out), rows, K, int(flags), _stream()))
     return out
 
 

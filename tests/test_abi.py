@@ -67,6 +67,11 @@ def test_argument_errors_return_before_launch(lib):
     assert lib.dq_dequant_q2k(fake, fake, 0, None) == -2
     assert lib.dq_gemv_q2k(fake, fake, fake, 4, 1536, None) == -3         # 84-byte blocks: K % 1024
     assert lib.dq_gemv_q2k(fake, fake, fake, 4, 17408, None) == -4
+    assert lib.dq_gemv_ex(4, fake, fake, fake, 4, 256, 0, None) == -2      # no such format
+    assert lib.dq_gemv_ex(1, fake, fake, fake, 4, 256, 2, None) == -2      # unknown flag
+    assert lib.dq_gemv_ex(1, None, fake, fake, 4, 256, 1, None) == -1
+    assert lib.dq_gemv_ex(1, fake, fake, fake, 4, 16640, 1, None) == -4
+    assert lib.dq_gemv_ex(0, fake, fake, fake, 4, 30000, 0, None) == -4
     assert lib.dq_attention_decode(fake, fake, fake, fake, 32, 8, 64, 16, 1, fake, 1 << 20, None) == -4
     assert lib.dq_attention_decode(fake, fake, fake, fake, 32, 8, 128, 16, 17, fake, 1 << 20, None) == -2
     assert lib.dq_attention_decode(fake, fake, fake, fake, 32, 8, 128, 16, 4, fake, 8, None) == -2

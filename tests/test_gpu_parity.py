@@ -167,6 +167,30 @@ def test_gemv_q2k(dq, orc, rows, K):
     assert normwise(y, r) <= GEMV_TOL
 
 
+@pytest.mark.parametrize("fmt,rows,K", [(0, 4096, 4096), (1, 12288, 4096), (1, 37, 256), (2, 300, 4096),
+                                         (3, 77, 3072)])
+def test_gemv_static_weights_flag(dq, orc, fmt, rows, K):
+    """The static-weights flag only moves the first weight copies before the wait on
+    the previous kernel: the result is the default entry point's, bit for bit, and the
+    oracle's within the GEMV tolerance.  Two calls each, after another GEMV on the
+    stream."""
+    if fmt == dq.FMT_BF16:
+        Wn, xn = synth.bf16_gemv_inputs(4, rows, K)
+        W, x = cuda(Wn.view(np.int16)), cuda(xn.view(np.int16))
+        r = orc.gemv_bf16(Wn, xn)
+    else:
+        Wn = synth.quant_matrix(9, fmt, rows, K)
+        xn = synth.activation(9, K)
+        W, x = cuda(Wn), cuda(xn)
+        r = [None, orc.gemv_q4k, orc.gemv_q6k, orc.gemv_q2k][fmt](Wn, xn, rows, K)
+    base = dq.gemv_ex(fmt, W, x).cpu().numpy()
+    for _ in range(2):
+        dq.gemv_ex(fmt, W, x)
+        y = dq.gemv_ex(fmt, W, x, flags=dq.GEMV_STATIC_WEIGHTS).cpu().numpy()
+        assert np.array_equal(y.view(np.uint32), base.view(np.uint32))
+    assert normwise(base, r) <= GEMV_TOL
+
+
 def test_gemv_q2k_integer_weights_and_extreme_activation(dq, orc):
     # d = dmin = 1: integer weights; a zero group, a tiny group and an outlier in x
     rng = np.random.default_rng(14)
