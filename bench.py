@@ -422,18 +422,26 @@ def run_msweep(device, reps: int = 20) -> dict:
     Y = torch.empty((max(SWEEP_M), SWEEP_ROWS), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     out = {"rows": SWEEP_ROWS, "K": SWEEP_K, "weight_bytes": wbytes, "copies_rotated": len(copies)}
-    for name, path in (("tensor", dq.MATMUL_TENSOR), ("cuda_core", dq.MATMUL_CUDA_CORE)):
+    ws = dq.matmul_split_workspace(max(SWEEP_M), SWEEP_ROWS, SWEEP_K, device)
+
+    def call(path, Wc, Xm, Ym):
+        if path is None:  # tensor cores, K split across blocks
+            dq.matmul_q4k_split(Wc, Xm, ws, out=Ym)
+        else:
+            dq.matmul_q4k(Wc, Xm, out=Ym, path=path)
+
+    for name, path in (("tensor_split", None), ("tensor", dq.MATMUL_TENSOR), ("cuda_core", dq.MATMUL_CUDA_CORE)):
         res = {}
         for M in SWEEP_M:
             Xm, Ym = X[:M], Y[:M]
             for i in range(3):
-                dq.matmul_q4k(copies[i % len(copies)], Xm, out=Ym, path=path)
+                call(path, copies[i % len(copies)], Xm, Ym)
             torch.cuda.synchronize(device)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             torch.cuda._sleep(20_000_000)  # the calls queue behind it: the events time the GPU
             a.record(stream)
             for i in range(reps):
-                dq.matmul_q4k(copies[i % len(copies)], Xm, out=Ym, path=path)
+                call(path, copies[i % len(copies)], Xm, Ym)
             b.record(stream)
             torch.cuda.synchronize(device)
             us = a.elapsed_time(b) * 1e3 / reps
@@ -446,6 +454,8 @@ def run_msweep(device, reps: int = 20) -> dict:
     out["M_star_inputs"] = {"R_TFLOPs": R, "R_source": rsrc, "BW_GBps": bw, "BW_source": bsrc}
     t1 = out["tensor"]["1"]["us"]
     out["tensor_cost_ratio_vs_M1"] = {k: round(v["us"] / t1, 3) for k, v in out["tensor"].items()}
+    t1 = out["tensor_split"]["1"]["us"]
+    out["tensor_split_cost_ratio_vs_M1"] = {k: round(v["us"] / t1, 3) for k, v in out["tensor_split"].items()}
     return out
 
 
@@ -548,14 +558,16 @@ def run_standalone(device, reps: int = 20) -> dict:
     return out
 
 
-OP_PROBES = ("attention_512", "gemv_bf16_4096", "rmsnorm_default", "rmsnorm_one_thread", "matmul_tensor_m16")
+OP_PROBES = ("attention_512", "gemv_bf16_4096", "rmsnorm_default", "rmsnorm_one_thread", "matmul_tensor_m16",
+             "matmul_split_m16")
 
 
 def run_op_probe(args):
     """`probe_reps` launches of one standalone entry point on a small case (for
     profilers): attention over 513 keys of a 32/8-head cache, the bf16 GEMV on
     4096x4096, RMSNorm of 64x2048 with the default block or one thread per row, or
-    the tensor-core product of 16 tokens over the 12288x4096 Q4_K table."""
+    the tensor-core product of 16 tokens over the 12288x4096 Q4_K table (rows per
+    block, or K split across blocks)."""
     import torch
 
     from quantised_gemv_norm_gb300 import build, dq
@@ -583,6 +595,12 @@ def run_op_probe(args):
         X = torch.from_numpy(np.stack([synth.activation(SEED, SWEEP_K, m) for m in range(16)])).cuda()
         for _ in range(args.probe_reps):
             y = dq.matmul_q4k(W, X, path=dq.MATMUL_TENSOR)
+    elif kind == "matmul_split_m16":
+        W = torch.from_numpy(synth.quant_matrix(SEED, synth.FMT_Q4K, SWEEP_ROWS, SWEEP_K)).cuda()
+        X = torch.from_numpy(np.stack([synth.activation(SEED, SWEEP_K, m) for m in range(16)])).cuda()
+        ws = dq.matmul_split_workspace(16, SWEEP_ROWS, SWEEP_K)
+        for _ in range(args.probe_reps):
+            y = dq.matmul_q4k_split(W, X, ws)
     else:
         x = torch.randn((64, 2048), generator=gen, device="cuda")
         g = 1.0 + 0.1 * torch.randn((2048,), generator=gen, device="cuda")

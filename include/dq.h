@@ -199,10 +199,13 @@ DQ_API int dq_gemv_ex(int fmt, const void* W, const void* x, float* y, int rows,
  * first weight tile ready; [6] unused; 64 bytes per block and phase.  In an
  * attention phase the block's first item writes global-timer ns at [1] q ready,
  * [3] keys staged, [5] partial computed, [6] merge decided, [7] output
- * stored.  A tensor-core dq_matmul_q4k_path writes, for block 0 and its first
- * 32 stages (one Q4_K block column each), 8 SM clock stamps per stage at
- * buffer[8 stage]: operands seen ready and MMAs issued (control thread), stage
- * start, weights landed, operand buffer free and stage written (thread 0).
+ * stored.  A tensor-core dq_matmul_q4k_path or dq_matmul_q4k_split writes, for
+ * block 0 and its first 32 stages (one Q4_K block column each), 8 SM clock
+ * stamps per stage at buffer[8 stage]: operands seen ready and MMAs issued
+ * (control thread), stage start, weights landed, operand buffer free and stage
+ * written (thread 0); then global-timer ns per block at buffer[256 + 4 block]:
+ * [0] start, [1] first stage ready, [2] last stage's MMAs done, [3] end
+ * (2304 bytes + 32 bytes per block).
  * NULL turns tracing off.  Not for use while
  * another thread launches kernels of the library. */
 DQ_API int dq_debug_trace(void* buffer);
@@ -321,6 +324,32 @@ DQ_API int dq_matmul_q4k_path(const void* W_blocks, const float* X, float* Y, in
 
 /* dq_matmul_q4k_path with DQ_MATMUL_AUTO. */
 DQ_API int dq_matmul_q4k(const void* W_blocks, const float* X, float* Y, int M, int rows, int K, void* stream);
+
+/* The same product on the tensor cores with K split across blocks.  Without a
+ * split every block takes whole rows: a share of rows / (SM count) rows that
+ * fills only part of a 128-row tile (81 of 128 for 12288 rows on 152 SMs), over
+ * all of K.  Here the (128-row tile, 256-column block) stages are shared out in
+ * contiguous runs, so every tile is full and a block takes 10 or 11 stages
+ * instead of 16 on that table.  A tile whose columns two or three blocks share
+ * is summed from their partial tiles in block order (deterministic: the same
+ * order whichever block finishes last).
+ * Arguments, operand rounding and errors as dq_matmul_q4k_path with
+ * DQ_MATMUL_TENSOR, with rows <= 524288 (else DQ_ERR_UNSUPPORTED); in addition
+ * workspace: a device buffer of at least
+ * dq_matmul_q4k_split_workspace_bytes(M, rows, K) bytes (else DQ_ERR_SHAPE),
+ * 16-byte aligned (else DQ_ERR_ALIGN), owned by the caller, zero-filled before
+ * its first use.  Its first 64 KB hold the tiles' counts, which every call
+ * leaves at zero, the rest the partial tiles: it serves later calls of any shape
+ * whose size fits.  Calls sharing one workspace must not run at the same time
+ * (one workspace per stream).  After a call that reports a device error,
+ * zero-fill it again. */
+DQ_API int dq_matmul_q4k_split(const void* W_blocks, const float* X, float* Y, int M, int rows, int K,
+                               void* workspace, long long workspace_bytes, void* stream);
+
+/* Bytes of the workspace dq_matmul_q4k_split needs for this shape on the
+ * current device (its SM count sets the split), or DQ_ERR_SHAPE /
+ * DQ_ERR_UNSUPPORTED for a shape it does not take. */
+DQ_API long long dq_matmul_q4k_split_workspace_bytes(int M, int rows, int K);
 
 /* -------------------------------------------------------------- decode step
  * One decode token over a pre-norm decoder stack ("The roofline holds on a

@@ -46,10 +46,9 @@ constexpr int MM_NCTRL = MM_NCTRL_DEF;
 constexpr int MM_THREADS = 32 * (MM_DQ_WARPS + MM_NCTRL);
 constexpr int MM_ROWS = 128;                   // rows per tile = UMMA M
 constexpr int MM_KC = 256;                     // K per MMA stage: one Q4_K block column
-constexpr int MM_BPS = 4;                      // Q4_K block columns per ring slot
-constexpr int MM_ROWB = MM_BPS * Q4K_BYTES + 16;  // 592: a slot row (4 blocks and 16 bytes of the next;
-                                                  // the odd 16-byte stride keeps 8 rows on distinct banks)
-constexpr int MM_NS_MAX = 4;
+constexpr int MM_ROWB = Q4K_BYTES;             // a slot row: one block (the 144-byte stride puts the
+                                               // 16-byte header loads of 8 rows on distinct banks)
+constexpr int MM_NS_MAX = 8;
 // operand (A in tensor memory, B in shared) buffers at most, where tensor memory
 // holds them (3 measured no faster than 2: the dequantising warps set the pace)
 #ifndef MM_NAB_MAX_DEF
@@ -83,12 +82,55 @@ struct MmArgs {
     const float* X;    // [M][K]
     float* Y;          // [M][rows]
     int M, rows, K;
-    int box_rows;      // rows one tensor copy brings (>= the rows of any tile of a block)
-    int ns;            // ring slots (2 .. 4)
+    int box_rows;      // rows one tensor copy brings (>= the rows of any tile)
+    int ns;            // ring slots (2 .. MM_NS_MAX), one block column each
     int nab;           // operand buffers (2 .. 4): stages whose operands may be written ahead of the MMAs
+    // K split (cnt not null): the stages (128-row tile, block column) are shared out
+    // in contiguous runs; a tile's partial sums meet in `part`, summed by the block
+    // that completes the tile's count in `cnt` (which it leaves at zero again)
+    unsigned* cnt;     // [row tiles][4 lane quarters]
+    float* part;       // [blocks][2][M][128]: a block's first and last partial tile
     unsigned long long* trace;  // diagnostics: block 0's per-stage cycle stamps when not null
     int* err;
 };
+
+// Segment i of block b (a tile's rows and the block columns [c0, c1) of them that
+// the block takes); false past the block's last.  Without a K split a block takes
+// whole rows (a contiguous share of the rows, in tiles of at most 128), with it a
+// contiguous run of the stages numbered tile-major.
+struct MmSeg {
+    int rt, row0, nrows, c0, c1;
+};
+__device__ __forceinline__ bool mm_seg(const MmArgs& a, int b, int G, int i, MmSeg& sg)
+{
+    const int nblk = a.K / 256;
+    if (!a.cnt) {
+        const int r0b = static_cast<int>(static_cast<long long>(b) * a.rows / G);
+        const int r1b = static_cast<int>(static_cast<long long>(b + 1) * a.rows / G);
+        const int row0 = r0b + MM_ROWS * i;
+        if (row0 >= r1b)
+            return false;
+        sg = MmSeg{i, row0, min(MM_ROWS, r1b - row0), 0, nblk};
+        return true;
+    }
+    const long long S = static_cast<long long>((a.rows + MM_ROWS - 1) / MM_ROWS) * nblk;
+    const long long s0 = S * b / G, s1 = S * (b + 1) / G;
+    const long long rt = s0 / nblk + i;
+    if (rt * nblk >= s1)
+        return false;
+    sg.rt = static_cast<int>(rt);
+    sg.row0 = sg.rt * MM_ROWS;
+    sg.nrows = min(MM_ROWS, a.rows - sg.row0);
+    sg.c0 = static_cast<int>(max(s0, rt * nblk) - rt * nblk);
+    sg.c1 = static_cast<int>(min(s1, (rt + 1) * nblk) - rt * nblk);
+    return true;
+}
+
+// The block whose run of stages holds stage s (K split).
+__device__ __forceinline__ int mm_block_of(long long s, long long S, int G)
+{
+    return static_cast<int>(((s + 1) * G - 1) / S);
+}
 
 // 2-D tensor copy global -> shared of the box at (x bytes, y rows), completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
@@ -109,23 +151,34 @@ __device__ __forceinline__ int mm_off(int r, int k)
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Four fp16 pairs from one word of codes t (bytes b0 b1 b2 b3, already permuted
 // to b0 b2 b1 b3): weights from the low nibbles (b0, b1), (b2, b3) and the high
-// nibbles (b0, b1), (b2, b3), each w = A q - B.
+// nibbles (b0, b1), (b2, b3), each w = A q - B.  A low nibble q in mantissa bits
+// 0-3 under 0x6400 is the fp16 value 1024 + q; a high nibble left in bits 4-7
+// under 0x5400 (64.0, whose mantissa step is 1/16) is 64 + q: one mask and or
+// per pair and one shift per word, and the subtractions are exact.
 __device__ __forceinline__ void mm_dequant_word(uint32_t t, __half2 A, __half2 B, uint32_t& lo01, uint32_t& lo23,
                                                 uint32_t& hi01, uint32_t& hi23)
 {
     const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+    const __half2 k64 = __halves2half2(__ushort_as_half(0x5400), __ushort_as_half(0x5400));
     const __half2 nb = __hneg2(B);
-    // 0x6400 | q is the fp16 value 1024 + q: subtracting 1024 is exact
+    const uint32_t t8 = t >> 8;  // b2, b3 in the low bytes of the halves (b1's bits above are masked off)
     const uint32_t q0 = (t & 0x000F000Fu) | 0x64006400u;
-    const uint32_t q1 = ((t >> 8) & 0x000F000Fu) | 0x64006400u;
-    const uint32_t q2 = ((t >> 4) & 0x000F000Fu) | 0x64006400u;
-    const uint32_t q3 = ((t >> 12) & 0x000F000Fu) | 0x64006400u;
+    const uint32_t q1 = (t8 & 0x000F000Fu) | 0x64006400u;
+    const uint32_t q2 = (t & 0x00F000F0u) | 0x54005400u;
+    const uint32_t q3 = (t8 & 0x00F000F0u) | 0x54005400u;
     lo01 = h2_bits(__hfma2(__hsub2(*reinterpret_cast<const __half2*>(&q0), k1024), A, nb));
     lo23 = h2_bits(__hfma2(__hsub2(*reinterpret_cast<const __half2*>(&q1), k1024), A, nb));
-    hi01 = h2_bits(__hfma2(__hsub2(*reinterpret_cast<const __half2*>(&q2), k1024), A, nb));
-    hi23 = h2_bits(__hfma2(__hsub2(*reinterpret_cast<const __half2*>(&q3), k1024), A, nb));
+    hi01 = h2_bits(__hfma2(__hsub2(*reinterpret_cast<const __half2*>(&q2), k64), A, nb));
+    hi23 = h2_bits(__hfma2(__hsub2(*reinterpret_cast<const __half2*>(&q3), k64), A, nb));
 }
 
 template <int NT>
@@ -141,20 +194,24 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
     uint64_t* opfree = opready + MM_NAB_MAX;                                    // [nab] a stage's MMAs done
     uint32_t* tslot = reinterpret_cast<uint32_t*>(opfree + MM_NAB_MAX);
     volatile int* fail = reinterpret_cast<volatile int*>(tslot + 1);
-    int* issued = const_cast<int*>(fail) + 1;   // one past the last block column issued (over the block's tiles)
+    int* issued = const_cast<int*>(fail) + 1;   // one past the last stage whose copy was issued
     int* committed = issued + 1;                // one past the last stage committed
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, b = blockIdx.x;
-    const int r0b = static_cast<int>(static_cast<long long>(b) * a.rows / G);
-    const int r1b = static_cast<int>(static_cast<long long>(b + 1) * a.rows / G);
-    if (r1b <= r0b)
-        return;
     const int nblk = a.K / 256;
+    unsigned long long* btr = a.trace ? a.trace + 256 + 4 * b : nullptr;  // this block's timeline
+    if (btr && tid == 0)
+        btr[0] = globaltimer_ns();
+    MmSeg sg0;
+    if (!mm_seg(a, b, G, 0, sg0))
+        return;
 
+    pdl_trigger();
     if (warp == 0)
         tmem_alloc(tslot, mm_tmem_cols(NT, nab));
     if (tid == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.tmap)) : "memory");
         for (int s = 0; s < a.ns; ++s)
             mbar_init(&full[s], 1);
         for (int i = 0; i < nab; ++i) {
@@ -170,6 +227,26 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tbase = *tslot;
+    // a dependent launch: the set-up above overlaps the previous kernel's tail.  The
+    // first ring-full of weights is only asked into L2 before the wait (a later write
+    // by the previous kernel lands in L2 as well, so no stale copy can result); every
+    // other global access (the copies, activations, outputs, workspace) follows it.
+    if (warp == MM_CTRL && lane == 0) {
+        MmSeg q = sg0;
+        int i = 0, col = sg0.c0;
+        for (int gi = 0; gi < a.ns; ++gi) {
+            asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                             reinterpret_cast<uint64_t>(&a.tmap)),
+                         "r"(col * (Q4K_BYTES / 8)), "r"(q.row0)
+                         : "memory");
+            if (++col == q.c1) {
+                if (!mm_seg(a, b, G, ++i, q))
+                    break;
+                col = q.c0;
+            }
+        }
+    }
+    pdl_wait();
 
     // a bounded wait; false once this block has given up
     auto wait = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
@@ -189,105 +266,113 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
 
     if (warp >= MM_CTRL) {
         // ---- control: the ring's copies (control warp 0) and the MMAs (one thread
-        // of each control warp: the MMAs of accumulator cq)
+        // of each control warp: the MMAs of accumulator cq).  The block's stages are
+        // numbered g = 0, 1, ... over its segments; stage g uses ring slot g % ns.
         const int cq = warp - MM_CTRL;
         if (lane == 0) {
             constexpr uint32_t idesc = umma_idesc_f16_f32(MM_ROWS, NT);
             const uint64_t pol = l2_evict_first_policy();
-            const int ngrp = (nblk + MM_BPS - 1) / MM_BPS;  // slot loads per tile
-            int bg0 = 0, g0 = 0;
+            int total = 0;
+            MmSeg sg;
+            for (int i = 0; mm_seg(a, b, G, i, sg); ++i)
+                total += sg.c1 - sg.c0;
+            // the next stage to copy: segment iseg, block column icol
+            MmSeg isg = sg0;
+            int iseg = 0, icol = sg0.c0, gnext = 0;
+            // one block column of a tile's rows into slot gnext % ns (box_rows >= the
+            // tile's rows: extra rows are the next tile's or zero fill)
+            auto issue_next = [&]() {
+                const int s = gnext % a.ns;
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(a.box_rows * MM_ROWB));
+                tma_load_2d(ring + s * slot_bytes, &a.tmap, icol * (Q4K_BYTES / 8), isg.row0, &full[s], pol);
+                *issued = ++gnext;
+                if (++icol == isg.c1 && mm_seg(a, b, G, ++iseg, isg))
+                    icol = isg.c0;
+            };
+            if (cq == 0)
+                while (gnext < min(a.ns, total))
+                    issue_next();
+            int g = 0;
             bool ok = true;
-            for (int rt0 = r0b; rt0 < r1b && ok; rt0 += MM_ROWS) {
-                // block columns [4 q, 4 q + 4) of the tile's rows into a ring slot (box_rows >=
-                // the tile's rows: extra rows are the next block's or zero fill, as are the
-                // bytes past the end of a row)
-                auto issue = [&](int q) {
-                    const int bg = bg0 + q;
-                    const int s = bg % a.ns;
-                    mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(a.box_rows * MM_ROWB));
-                    tma_load_2d(ring + s * slot_bytes, &a.tmap, q * (MM_BPS * Q4K_BYTES / 8), rt0, &full[s], pol);
-                    *issued = bg + 1;
-                };
-                if (cq == 0)
-                    for (int q = 0; q < min(a.ns, ngrp); ++q)
-                        issue(q);
-                for (int hc = 0; hc < nblk; ++hc) {
-                    const int g = g0 + hc, buf = g % nab, c = hc;
+            for (int i = 0; ok && mm_seg(a, b, G, i, sg); ++i) {
+                for (int hc = sg.c0; hc < sg.c1; ++hc, ++g) {
+                    const int buf = g % nab;
                     if (!(ok = wait(&opready[buf], (g / nab) & 1, DEVERR_TIMEOUT_FULL)))
                         break;
-                    unsigned long long* tr = (a.trace && b == 0 && cq == 0 && hc < 32) ? a.trace + 8 * hc : nullptr;
+                    unsigned long long* tr = (a.trace && b == 0 && cq == 0 && g < 32) ? a.trace + 8 * g : nullptr;
                     if (tr)
                         tr[0] = clock64();
                     tc_fence_after_sync();
                     const uint32_t ta = tbase + mm_ta_col(NT) + MM_TA_COLS * buf;
                     const uint64_t bd = umma_desc_kmajor(Bbuf + buf * mm_b_bytes(NT), MM_LBO, MM_SBO);
                     // K = 16 per MMA: 8 columns of A, two core matrices of B.  MMA s adds
-                    // into accumulator s % MM_ACC, so consecutive MMAs do not wait on each other.
+                    // into accumulator s % MM_ACC, so consecutive MMAs do not wait on each
+                    // other; the segment's first stage starts the accumulators afresh.
 #pragma unroll
                     for (int s = 0; s < MM_KC / 16; ++s)
                         if (s % MM_NCTRL == cq)
                             umma_f16_ta(tbase + NT * (s % MM_ACC), ta + 8 * s,
                                         bd + static_cast<uint64_t>((2 * MM_LBO * s) >> 4), idesc,
-                                        (hc > 0 || s >= MM_ACC) ? 1u : 0u);
+                                        (hc > sg.c0 || s >= MM_ACC) ? 1u : 0u);
                     umma_commit(&opfree[buf]);
                     if (cq == 0)
                         *committed = g + 1;
                     if (tr)
                         tr[1] = clock64();
-                    // the last stage of a slot's block columns is dequantised: refill the slot
-                    const int q = c / MM_BPS;
-                    if (cq == 0 && (hc + 1 == nblk || (hc + 1) % MM_BPS == 0) && q + a.ns < ngrp)
-                        issue(q + a.ns);
+                    // stage g's slot is free (every dequantising warp read it before its
+                    // opready arrival): the copy of stage g + ns goes into it
+                    if (cq == 0 && g + a.ns < total)
+                        issue_next();
                 }
-                bg0 += ngrp;
-                g0 += nblk;
             }
         }
         __syncwarp();  // the warp reconverges before the block-wide barrier below
     } else {
-        // ---- dequantisation, activation staging and the epilogue (8 warps)
+        // ---- dequantisation, activation staging and the epilogue (16 warps)
         constexpr int NDQ = 32 * MM_DQ_WARPS;
         constexpr int NXI = (NT * (MM_KC / 8) + NDQ - 1) / NDQ;  // activation items a thread stages
-        const int ngrp = (nblk + MM_BPS - 1) / MM_BPS;
-        int bg0 = 0, g0 = 0;
-        for (int rt0 = r0b; rt0 < r1b; rt0 += MM_ROWS) {
-            const int nrows = min(MM_ROWS, r1b - rt0);
-            // the tokens' activations of stage hc + 1 are loaded while stage hc is
-            // processed (item t = tid + 256 i: token t % NT, 8-element group t / NT)
-            float4 xn[NXI][2];
-            auto load_x = [&](int hcn) {
-                const int kb = hcn * MM_KC;
+        // the tokens' activations of the next stage are loaded while a stage is
+        // processed (item t = tid + NDQ i: token t % NT, 8-element group t / NT)
+        float4 xn[NXI][2];
+        auto load_x = [&](int hcn) {
+            const int kb = hcn * MM_KC;
 #pragma unroll
-                for (int i = 0; i < NXI; ++i) {
-                    const int it = tid + NDQ * i;
-                    const int n = it % NT, kg = it / NT;
-                    if (it < NT * (MM_KC / 8) && n < a.M && hcn < nblk) {
-                        const float4* xp =
-                            reinterpret_cast<const float4*>(a.X + static_cast<size_t>(n) * a.K + kb + 8 * kg);
-                        xn[i][0] = __ldg(xp);
-                        xn[i][1] = __ldg(xp + 1);
-                    }
+            for (int i = 0; i < NXI; ++i) {
+                const int it = tid + NDQ * i;
+                const int n = it % NT, kg = it / NT;
+                if (it < NT * (MM_KC / 8) && n < a.M && hcn >= 0 && hcn < nblk) {
+                    const float4* xp =
+                        reinterpret_cast<const float4*>(a.X + static_cast<size_t>(n) * a.K + kb + 8 * kg);
+                    xn[i][0] = __ldg(xp);
+                    xn[i][1] = __ldg(xp + 1);
                 }
-            };
-            load_x(0);
-            bool ok = true;
-            for (int hc = 0; hc < nblk; ++hc) {
-                const int c = hc;
-                const int g = g0 + hc, buf = g % nab;
-                const int bg = bg0 + c / MM_BPS;
-                unsigned long long* tr = (a.trace && b == 0 && tid == 0 && hc < 32) ? a.trace + 8 * hc : nullptr;
+            }
+        };
+        load_x(sg0.c0);
+        int g = 0;
+        bool ok = true;
+        MmSeg sg;
+        for (int si = 0; ok && mm_seg(a, b, G, si, sg); ++si) {
+            const int nrows = sg.nrows;
+            MmSeg nx;
+            const int next_c0 = mm_seg(a, b, G, si + 1, nx) ? nx.c0 : -1;
+            for (int hc = sg.c0; hc < sg.c1; ++hc, ++g) {
+                const int buf = g % nab, s = g % a.ns;
+                unsigned long long* tr = (a.trace && b == 0 && tid == 0 && g < 32) ? a.trace + 8 * g : nullptr;
                 if (tr)
                     tr[2] = clock64();
-                if (hc % MM_BPS == 0 && !(ok = warp_wait(&full[bg % a.ns], (bg / a.ns) & 1, DEVERR_TIMEOUT_FULL)))
+                if (!(ok = warp_wait(&full[s], (g / a.ns) & 1, DEVERR_TIMEOUT_FULL)))
                     break;
                 if (tr)
                     tr[3] = clock64();
+                if (btr && g == 0 && tid == 0)
+                    btr[1] = globaltimer_ns();
                 if (g >= nab && !(ok = warp_wait(&opfree[buf], ((g - nab) / nab) & 1, DEVERR_TIMEOUT_MMA)))
                     break;
                 if (tr)
                     tr[4] = clock64();
                 uint8_t* Bt = Bbuf + buf * mm_b_bytes(NT);
-                const uint8_t* slot = ring + (bg % a.ns) * slot_bytes + (c % MM_BPS) * Q4K_BYTES;
+                const uint8_t* slot = ring + s * slot_bytes;
                 // weights: thread (warp w, lane) dequantises row 32 (w % 4) + lane,
                 // sub-blocks w / 4 and w / 4 + 4 of this block column, into the A buffer
                 // in tensor memory (one lane per row, two fp16 per column; the four warps
@@ -343,7 +428,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                         *reinterpret_cast<uint4*>(Bt + mm_off(n, 8 * kg)) = v;
                     }
                 }
-                load_x(hc + 1);
+                load_x(hc + 1 < sg.c1 ? hc + 1 : next_c0);
                 tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
@@ -355,13 +440,20 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
             }
             if (!ok)
                 break;
-            // accumulator complete -> Y (warps 0-3: one lane quarter each)
+            // accumulator complete (warps 0-3: one lane quarter each) -> Y, or, for a
+            // tile whose block columns other blocks share, -> this block's partial tile
             if (warp < 4) {
-                const int glast = g0 + nblk - 1;
+                const int glast = g - 1;
                 if (!warp_wait(&opfree[glast % nab], (glast / nab) & 1, DEVERR_TIMEOUT_MMA))
                     break;
                 tc_fence_after_sync();
+                if (btr && tid == 0)
+                    btr[2] = globaltimer_ns();
                 const int row = 32 * warp + lane;
+                const bool whole = sg.c0 == 0 && sg.c1 == nblk;
+                float* dst = whole ? a.Y + sg.row0 + row
+                                   : a.part + (static_cast<size_t>(2 * b + (si == 0 ? 0 : 1)) * a.M) * MM_ROWS + row;
+                const size_t dstride = whole ? static_cast<size_t>(a.rows) : static_cast<size_t>(MM_ROWS);
 #pragma unroll
                 for (int cc = 0; cc < NT / 16; ++cc) {
                     float y[16];
@@ -382,30 +474,78 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                         for (int q = 0; q < 16; ++q) {
                             const int n = 16 * cc + q;
                             if (n < a.M)
-                                a.Y[static_cast<size_t>(n) * a.rows + rt0 + row] = y[q];
+                                dst[n * dstride] = y[q];
                         }
                     }
                 }
-                // The next tile's first MMAs overwrite the accumulator only after this
-                // warp's arrival on that tile's first stage, which follows these reads.
+                // The next segment's first MMAs overwrite the accumulator only after this
+                // warp's arrival on that segment's first stage, which follows these reads.
                 tc_fence_before_sync();
+                if (!whole) {
+                    // this warp's 32 rows of the partial tile are written: count them
+                    // (one count per tile and lane quarter, so the four warps never wait
+                    // on each other); the warp that completes a count sums the quarter's
+                    // partials in block order (the same order whichever block comes
+                    // last) and leaves the count at zero
+                    const long long S = static_cast<long long>((a.rows + MM_ROWS - 1) / MM_ROWS) * nblk;
+                    const long long t0 = static_cast<long long>(sg.rt) * nblk;
+                    const int b_lo = mm_block_of(t0, S, G), b_hi = mm_block_of(t0 + nblk - 1, S, G);
+                    const int which_lo = S * b_lo / G == t0 ? 0 : 1;
+                    unsigned* cnt = a.cnt + 4 * sg.rt + warp;
+                    // the warp barrier orders the lanes' stores before lane 0's release
+                    // (cumulative), and lane 0's acquire before the lanes' loads
+                    __syncwarp();
+                    unsigned done = 0;
+                    if (lane == 0)
+                        done = atom_add_acq_rel_gpu(cnt, 1u) == static_cast<unsigned>(b_hi - b_lo) ? 1u : 0u;
+                    done = __shfl_sync(0xffffffffu, done, 0);
+                    __syncwarp();
+                    if (done) {
+                        if (row < nrows)
+                            for (int n0 = 0; n0 < a.M; n0 += 16) {  // 16 tokens' loads in flight at once
+                                float y[16];
+#pragma unroll
+                                for (int q = 0; q < 16; ++q)
+                                    y[q] = 0.f;
+                                for (int bb = b_lo; bb <= b_hi; ++bb) {
+                                    // block bb's partial of this tile: the later blocks' runs start
+                                    // in it (their first segment); block b_lo's run starts in it
+                                    // only when it starts at its column 0
+                                    const int which = bb == b_lo ? which_lo : 0;
+                                    const float* pp =
+                                        a.part + (static_cast<size_t>(2 * bb + which) * a.M + n0) * MM_ROWS + row;
+                                    float v[16];
+#pragma unroll
+                                    for (int q = 0; q < 16; ++q)
+                                        v[q] = n0 + q < a.M ? __ldcg(pp + q * MM_ROWS) : 0.f;
+#pragma unroll
+                                    for (int q = 0; q < 16; ++q)
+                                        y[q] += v[q];
+                                }
+#pragma unroll
+                                for (int q = 0; q < 16; ++q)
+                                    if (n0 + q < a.M)
+                                        a.Y[static_cast<size_t>(n0 + q) * a.rows + sg.row0 + row] = y[q];
+                            }
+                        if (lane == 0)
+                            atomicExch(cnt, 0u);
+                    }
+                }
             }
-            bg0 += ngrp;
-            g0 += nblk;
         }
     }
     // After a failed wait: let this block's copies and MMAs in flight finish (bounded).
     __syncthreads();
     if (tid == 0 && *fail) {
         const int hi = *issued, gc = *committed;
-        for (int bg = max(0, hi - a.ns); bg < hi; ++bg) {
+        for (int gi = max(0, hi - a.ns); gi < hi; ++gi) {
             const unsigned long long t0 = globaltimer_ns();
-            while (!mbar_try_wait(&full[bg % a.ns], (bg / a.ns) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+            while (!mbar_try_wait(&full[gi % a.ns], (gi / a.ns) & 1) && globaltimer_ns() - t0 < 100000000ull) {
             }
         }
-        for (int g = max(0, gc - nab); g < gc; ++g) {
+        for (int gi = max(0, gc - nab); gi < gc; ++gi) {
             const unsigned long long t0 = globaltimer_ns();
-            while (!mbar_try_wait(&opfree[g % nab], (g / nab) & 1) && globaltimer_ns() - t0 < 100000000ull) {
+            while (!mbar_try_wait(&opfree[gi % nab], (gi / nab) & 1) && globaltimer_ns() - t0 < 100000000ull) {
             }
         }
     }
@@ -415,6 +555,8 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
         tc_fence_after_sync();
         tmem_dealloc(tbase, mm_tmem_cols(NT, nab));
     }
+    if (btr && tid == 0)
+        btr[3] = globaltimer_ns();
 }
 
 }  // namespace dq
@@ -441,7 +583,25 @@ static EncodeTiled encode_tiled()
     return fn;
 }
 
-static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, int rows, int K, cudaStream_t s)
+// Workspace of the K-split product: the tiles' counts (zero between calls), then
+// the blocks' partial tiles.
+static long long split_grid(int rows, int K)
+{
+    const long long S = static_cast<long long>((rows + dq::MM_ROWS - 1) / dq::MM_ROWS) * (K / 256);
+    return std::min<long long>(sm_count(), S);
+}
+// The counts take a fixed region (four per 128-row tile, room for 4096 tiles) so
+// that no shape's partial tiles ever overlap another shape's counts: one workspace
+// serves calls of any shapes that fit it.
+constexpr size_t SPLIT_CNT_BYTES = 65536;
+constexpr int SPLIT_MAX_ROWS = static_cast<int>(SPLIT_CNT_BYTES / 16) * dq::MM_ROWS;
+static size_t split_ws_bytes(int M, int rows, int K)
+{
+    return SPLIT_CNT_BYTES + static_cast<size_t>(split_grid(rows, K)) * 2 * M * dq::MM_ROWS * 4;
+}
+
+static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, int rows, int K, void* ws,
+                            cudaStream_t s)
 {
     static std::once_flag once[3];
     static cudaError_t attr_err[3];
@@ -459,7 +619,7 @@ static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, i
     EncodeTiled enc = encode_tiled();
     if (!enc)
         return DQ_ERR_UNSUPPORTED;
-    const int grid = std::min(sm_count(), rows);
+    const int grid = ws ? static_cast<int>(split_grid(rows, K)) : std::min(sm_count(), rows);
     const int per_block = (rows + grid - 1) / grid;
     dq::MmArgs a{};
     a.X = X;
@@ -467,7 +627,11 @@ static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, i
     a.M = M;
     a.rows = rows;
     a.K = K;
-    a.box_rows = std::min(dq::MM_ROWS, per_block);
+    a.box_rows = std::min(dq::MM_ROWS, ws ? rows : per_block);
+    if (ws) {
+        a.cnt = static_cast<unsigned*>(ws);
+        a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + SPLIT_CNT_BYTES);
+    }
     a.err = device_error_flag();
     a.trace = gemv_trace();
     // the deepest operand pipeline, then as many ring slots, as shared memory holds
@@ -493,8 +657,17 @@ static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, i
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return DQ_ERR_UNSUPPORTED;
-    k<<<grid, dq::MM_THREADS, smem, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(dq::MM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, a);
     return e == cudaSuccess ? DQ_OK : set_cuda_error(e);
 }
 
@@ -515,7 +688,7 @@ DQ_API int dq_matmul_q4k_path(const void* W_blocks, const float* X, float* Y, in
     const bool tensor = path == DQ_MATMUL_TENSOR || (path == DQ_MATMUL_AUTO && M >= 4);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (tensor)
-        return dqhost::launch_matmul_tc(static_cast<const uint8_t*>(W_blocks), X, Y, M, rows, K, s);
+        return dqhost::launch_matmul_tc(static_cast<const uint8_t*>(W_blocks), X, Y, M, rows, K, nullptr, s);
     if (K > 16384)
         return DQ_ERR_UNSUPPORTED;
     dqhost::GemvPlan plan;
@@ -543,6 +716,32 @@ DQ_API int dq_matmul_q4k_path(const void* W_blocks, const float* X, float* Y, in
 DQ_API int dq_matmul_q4k(const void* W_blocks, const float* X, float* Y, int M, int rows, int K, void* stream)
 {
     return dq_matmul_q4k_path(W_blocks, X, Y, M, rows, K, DQ_MATMUL_AUTO, stream);
+}
+
+DQ_API long long dq_matmul_q4k_split_workspace_bytes(int M, int rows, int K)
+{
+    if (M < 1 || M > 64 || rows < 1 || K < 256 || K % 256)
+        return DQ_ERR_SHAPE;
+    if (rows > dqhost::SPLIT_MAX_ROWS)
+        return DQ_ERR_UNSUPPORTED;
+    return static_cast<long long>(dqhost::split_ws_bytes(M, rows, K));
+}
+
+DQ_API int dq_matmul_q4k_split(const void* W_blocks, const float* X, float* Y, int M, int rows, int K,
+                               void* workspace, long long workspace_bytes, void* stream)
+{
+    if (!W_blocks || !X || !Y || !workspace)
+        return DQ_ERR_NULL;
+    if (M < 1 || M > 64 || rows < 1 || K < 256 || K % 256)
+        return DQ_ERR_SHAPE;
+    if (!dqhost::aligned16(W_blocks) || !dqhost::aligned16(X) || !dqhost::aligned16(workspace))
+        return DQ_ERR_ALIGN;
+    if (rows > dqhost::SPLIT_MAX_ROWS)
+        return DQ_ERR_UNSUPPORTED;
+    if (workspace_bytes < static_cast<long long>(dqhost::split_ws_bytes(M, rows, K)))
+        return DQ_ERR_SHAPE;
+    return dqhost::launch_matmul_tc(static_cast<const uint8_t*>(W_blocks), X, Y, M, rows, K, workspace,
+                                    static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

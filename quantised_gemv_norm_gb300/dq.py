@@ -49,6 +49,8 @@ SIGNATURES = {
     "dq_attention_decode_rope": (I, [P, P, P, P, P, P, P, P, F, I, I, I, I, I, P, SZ, P]),
     "dq_matmul_q4k": (I, [P, P, P, I, I, I, P]),
     "dq_matmul_q4k_path": (I, [P, P, P, I, I, I, I, P]),
+    "dq_matmul_q4k_split": (I, [P, P, P, I, I, I, P, LL, P]),
+    "dq_matmul_q4k_split_workspace_bytes": (LL, [I, I, I]),
     "dq_model_create": (I, [P, P]),
     "dq_decode_step": (I, [P, P, I, P, P]),
     "dq_decode_step_host": (I, [P, P, I, P, P]),
@@ -244,6 +246,30 @@ def matmul_q4k(W: torch.Tensor, X: torch.Tensor, out=None, path: int = MATMUL_AU
     out = torch.empty((M, rows), dtype=torch.float32, device=W.device) if out is None else out
     _check("dq_matmul_q4k_path",
            lib.dq_matmul_q4k_path(_ptr(W), _ptr(X), _ptr(out), M, rows, K, int(path), _stream()))
+    return out
+
+
+def matmul_split_workspace(M: int, rows: int, K: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace for matmul_q4k_split of this shape (reusable by
+    later calls on the same stream whose shapes fit)."""
+    lib = load()
+    nbytes = lib.dq_matmul_q4k_split_workspace_bytes(M, rows, K)
+    if nbytes < 0:
+        _check("dq_matmul_q4k_split_workspace_bytes", int(nbytes))
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def matmul_q4k_split(W: torch.Tensor, X: torch.Tensor, workspace: torch.Tensor, out=None):
+    """The tensor-core product with K split across blocks (every 128-row tile
+    full); ``workspace`` from matmul_split_workspace."""
+    lib = load()
+    rows = W.shape[0]
+    K = quant_K(FMT_Q4K, W.shape[1])
+    M = X.shape[0]
+    out = torch.empty((M, rows), dtype=torch.float32, device=W.device) if out is None else out
+    _check("dq_matmul_q4k_split",
+           lib.dq_matmul_q4k_split(_ptr(W), _ptr(X), _ptr(out), M, rows, K, _ptr(workspace), workspace.numel(),
+                                   _stream()))
     return out
 
 

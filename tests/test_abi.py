@@ -80,6 +80,14 @@ def test_argument_errors_return_before_launch(lib):
     assert lib.dq_matmul_q4k_path(fake, fake, fake, 2, 4, 256, 3, None) == -2  # no such path
     assert lib.dq_matmul_q4k_path(P(17), fake, fake, 2, 4, 256, 2, None) == -3
     assert lib.dq_matmul_q4k_path(fake, fake, fake, 2, 4, 32768, 1, None) == -4
+    assert lib.dq_matmul_q4k_split(fake, fake, fake, 2, 4, 256, None, 1 << 20, None) == -1
+    assert lib.dq_matmul_q4k_split(fake, fake, fake, 65, 4, 256, fake, 1 << 20, None) == -2
+    assert lib.dq_matmul_q4k_split(fake, fake, fake, 2, 4, 300, fake, 1 << 20, None) == -2
+    assert lib.dq_matmul_q4k_split(fake, fake, fake, 2, 4, 256, P(24), 1 << 20, None) == -3  # misaligned workspace
+    assert lib.dq_matmul_q4k_split_workspace_bytes(0, 4, 256) == -2
+    assert lib.dq_matmul_q4k_split_workspace_bytes(2, 4, 300) == -2
+    assert lib.dq_matmul_q4k_split_workspace_bytes(2, 524289, 256) == -4
+    assert lib.dq_matmul_q4k_split(fake, fake, fake, 2, 524289, 256, fake, 1 << 40, None) == -4
     assert lib.dq_rope_table(None, 16, 128, 1e6, None) == -1
     assert lib.dq_rope_table(fake, 16, 127, 1e6, None) == -2              # odd head_dim
     assert lib.dq_rope_table(fake, 16, 128, 1.0, None) == -2              # theta must exceed 1

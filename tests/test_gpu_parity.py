@@ -326,6 +326,40 @@ def test_matmul_q4k_tensor_shapes(dq, orc, rows, K, M):
     assert dq.device_error() == 0
 
 
+@pytest.mark.parametrize("rows,K,M", [(12288, 4096, 1), (12288, 4096, 16), (12288, 4096, 64), (128, 4096, 3),
+                                      (300, 768, 5), (1000, 2048, 8), (20000, 512, 17), (77, 2048, 2)])
+def test_matmul_q4k_split(dq, orc, rows, K, M):
+    """K split across blocks: the 12288 x 4096 table (tiles shared by two or three
+    blocks), one tile shared by 16 blocks, ragged last tiles, fewer stages than
+    SMs.  Against the oracle at the GEMV bar; a second call on the same workspace
+    (its tile counts left at zero) gives the same bits."""
+    W = synth.quant_matrix(13, synth.FMT_Q4K, rows, K)
+    X = np.stack([synth.activation(13, K, m) for m in range(M)])
+    R = orc.matmul_q4k(W, X, rows, K)
+    Wd, Xd = cuda(W), cuda(X)
+    ws = dq.matmul_split_workspace(M, rows, K)
+    Y = dq.matmul_q4k_split(Wd, Xd, ws).cpu().numpy()
+    for m in range(M):
+        assert normwise(Y[m], R[m]) <= GEMV_TOL, m
+    Y2 = dq.matmul_q4k_split(Wd, Xd, ws).cpu().numpy()
+    assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
+    assert int(ws[:65536].view(torch.int32).abs().sum()) == 0  # the counts are back at zero
+    assert dq.device_error() == 0
+
+
+def test_matmul_q4k_split_workspace_reuse(dq, orc):
+    """One workspace, sized for the largest, serves calls of several shapes in turn."""
+    ws = dq.matmul_split_workspace(64, 12288, 4096)
+    for rows, K, M in ((12288, 4096, 16), (300, 768, 5), (128, 4096, 64), (12288, 4096, 2)):
+        W = synth.quant_matrix(14, synth.FMT_Q4K, rows, K)
+        X = np.stack([synth.activation(14, K, m) for m in range(M)])
+        R = orc.matmul_q4k(W, X, rows, K)
+        Y = dq.matmul_q4k_split(cuda(W), cuda(X), ws).cpu().numpy()
+        for m in range(M):
+            assert normwise(Y[m], R[m]) <= GEMV_TOL, (rows, K, M, m)
+    assert dq.device_error() == 0
+
+
 # -------------------------------------------------------------- decode
 
 
