@@ -459,6 +459,34 @@ def run_msweep(device, reps: int = 20) -> dict:
     return out
 
 
+def graph_us(fn, n: int, device) -> float:
+    """Per-call time of n calls fn(0..n-1) captured in one CUDA graph and replayed
+    (the launch cost of a captured chain instead of a stream's); CUDA events around
+    one replay, after three warm replays."""
+    import torch
+
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        fn(0)  # any first-call set-up happens outside the capture
+        torch.cuda.synchronize(device)
+        with torch.cuda.graph(g, stream=side):
+            for i in range(n):
+                fn(i)
+    torch.cuda.synchronize(device)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize(device)
+    del g
+    return a.elapsed_time(b) * 1e3 / n
+
+
 def run_lowbit(device, reps: int = 20) -> dict:
     """The 2-bit (Q2_K) GEMV against the 4- and 6-bit ones on the same shapes:
     per call time from CUDA events, each call on the next of enough device
@@ -493,6 +521,10 @@ def run_lowbit(device, reps: int = 20) -> dict:
             us = a.elapsed_time(b) * 1e3 / reps
             res[name] = {"weight_bytes": wbytes, "us": round(us, 2), "GBps": round(wbytes / us / 1e3, 1),
                          "frac_of_peak": round(wbytes / us / 1e3 / bw, 4), "weights_per_ns": round(rows * K / us / 1e3, 1)}
+            if rows < 100000:
+                gus = graph_us(lambda i: fn(copies[i % len(copies)], x, out=y), 100, device)
+                res[name]["graph_us"] = round(gus, 2)
+                res[name]["graph_frac_of_peak"] = round(wbytes / gus / 1e3 / bw, 4)
             del copies, W
         out["%dx%d" % (rows, K)] = res
     out["peak_GBps"] = bw
@@ -541,6 +573,10 @@ def run_standalone(device, reps: int = 20) -> dict:
         out["bf16_gemv"]["%dx%d" % (rows, K)] = {"weight_bytes": wbytes, "us": round(us, 2),
                                                  "GBps": round(wbytes / us / 1e3, 1),
                                                  "frac_of_peak": round(wbytes / us / 1e3 / bw, 4)}
+        if rows < 100000:
+            gus = graph_us(lambda i: dq.gemv_bf16(copies[i % len(copies)], x, out=y), 100, device)
+            out["bf16_gemv"]["%dx%d" % (rows, K)]["graph_us"] = round(gus, 2)
+            out["bf16_gemv"]["%dx%d" % (rows, K)]["graph_frac_of_peak"] = round(wbytes / gus / 1e3 / bw, 4)
         del copies, W
     out["bf16_gemv"]["peak_GBps"], out["bf16_gemv"]["peak_source"] = bw, bsrc
     rows, n = 64, 2048
