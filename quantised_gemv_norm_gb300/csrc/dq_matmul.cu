@@ -72,9 +72,12 @@ constexpr int DEVERR_TIMEOUT_MMA = 32;
 __host__ __device__ constexpr int mm_b_bytes(int nt) { return nt * MM_KC * 2; }
 // A ring slot: box_rows rows of MM_ROWB bytes, the slot start 128-byte aligned (tensor copy destination).
 __host__ __device__ constexpr int mm_slot_bytes(int box_rows) { return (box_rows * MM_ROWB + 127) / 128 * 128; }
-__host__ __device__ constexpr int mm_smem_bytes(int nt, int ns, int nab, int box_rows)
+// xs: the activations arrive staged (fp16, UMMA layout) with each slot's weights,
+// so a slot holds the weights and the stage's B tile and there are no B buffers.
+__host__ __device__ constexpr int mm_smem_bytes(int nt, int ns, int nab, int box_rows, bool xs)
 {
-    return ns * mm_slot_bytes(box_rows) + nab * mm_b_bytes(nt) + 128;
+    return xs ? ns * (mm_slot_bytes(box_rows) + mm_b_bytes(nt)) + 128
+              : ns * mm_slot_bytes(box_rows) + nab * mm_b_bytes(nt) + 128;
 }
 
 struct MmArgs {
@@ -90,6 +93,10 @@ struct MmArgs {
     // that completes the tile's count in `cnt` (which it leaves at zero again)
     unsigned* cnt;     // [row tiles][4 lane quarters]
     float* part;       // [blocks][2][M][128]: a block's first and last partial tile
+    // the activations already in fp16 B tiles (mm_stage_x_kernel: [K / 256][NT tokens x
+    // 256] in the UMMA K-major layout), copied with the weights; null: the
+    // dequantising warps stage them from X each stage
+    const uint8_t* xh;
     unsigned long long* trace;  // diagnostics: block 0's per-stage cycle stamps when not null
     int* err;
 };
@@ -151,6 +158,13 @@ __device__ __forceinline__ int mm_off(int r, int k)
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
+__device__ __forceinline__ uint64_t l2_evict_last_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v)
 {
     unsigned old;
@@ -185,11 +199,13 @@ template <int NT>
 __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __grid_constant__ MmArgs a)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
-    const int slot_bytes = mm_slot_bytes(a.box_rows);
+    const bool xs = a.xh != nullptr;  // each slot: weights, then the stage's B tile
+    const int wslot = mm_slot_bytes(a.box_rows);
+    const int slot_bytes = wslot + (xs ? mm_b_bytes(NT) : 0);
     uint8_t* ring = sm;
     uint8_t* Bbuf = sm + a.ns * slot_bytes;
     const int nab = a.nab;
-    uint64_t* full = reinterpret_cast<uint64_t*>(Bbuf + nab * mm_b_bytes(NT));  // [MM_NS_MAX] slot landed
+    uint64_t* full = reinterpret_cast<uint64_t*>(Bbuf + (xs ? 0 : nab * mm_b_bytes(NT)));  // [MM_NS_MAX] slot landed
     uint64_t* opready = full + MM_NS_MAX;                                       // [nab] operands of a stage written
     uint64_t* opfree = opready + MM_NAB_MAX;                                    // [nab] a stage's MMAs done
     uint32_t* tslot = reinterpret_cast<uint32_t*>(opfree + MM_NAB_MAX);
@@ -281,10 +297,15 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
             int iseg = 0, icol = sg0.c0, gnext = 0;
             // one block column of a tile's rows into slot gnext % ns (box_rows >= the
             // tile's rows: extra rows are the next tile's or zero fill)
+            const uint64_t pol_x = l2_evict_last_policy();  // every block reads the B tiles
             auto issue_next = [&]() {
                 const int s = gnext % a.ns;
-                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(a.box_rows * MM_ROWB));
+                mbar_arrive_expect_tx(&full[s],
+                                      static_cast<uint32_t>(a.box_rows * MM_ROWB + (xs ? mm_b_bytes(NT) : 0)));
                 tma_load_2d(ring + s * slot_bytes, &a.tmap, icol * (Q4K_BYTES / 8), isg.row0, &full[s], pol);
+                if (xs)
+                    bulk_g2s(ring + s * slot_bytes + wslot, a.xh + static_cast<size_t>(icol) * mm_b_bytes(NT),
+                             mm_b_bytes(NT), &full[s], pol_x);
                 *issued = ++gnext;
                 if (++icol == isg.c1 && mm_seg(a, b, G, ++iseg, isg))
                     icol = isg.c0;
@@ -304,7 +325,8 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                         tr[0] = clock64();
                     tc_fence_after_sync();
                     const uint32_t ta = tbase + mm_ta_col(NT) + MM_TA_COLS * buf;
-                    const uint64_t bd = umma_desc_kmajor(Bbuf + buf * mm_b_bytes(NT), MM_LBO, MM_SBO);
+                    const uint64_t bd = umma_desc_kmajor(
+                        xs ? ring + (g % a.ns) * slot_bytes + wslot : Bbuf + buf * mm_b_bytes(NT), MM_LBO, MM_SBO);
                     // K = 16 per MMA: 8 columns of A, two core matrices of B.  MMA s adds
                     // into accumulator s % MM_ACC, so consecutive MMAs do not wait on each
                     // other; the segment's first stage starts the accumulators afresh.
@@ -319,10 +341,19 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                         *committed = g + 1;
                     if (tr)
                         tr[1] = clock64();
-                    // stage g's slot is free (every dequantising warp read it before its
-                    // opready arrival): the copy of stage g + ns goes into it
-                    if (cq == 0 && g + a.ns < total)
+                    if (!xs) {
+                        // stage g's slot is free (every dequantising warp read it before its
+                        // opready arrival): the copy of stage g + ns goes into it
+                        if (cq == 0 && g + a.ns < total)
+                            issue_next();
+                    } else if (cq == 0 && g >= 1 && g - 1 + a.ns < total) {
+                        // the MMAs read the B tile from the slot: stage g - 1's slot is free
+                        // once its MMAs are done (committed one stage ago)
+                        const int j = g - 1;
+                        if (!(ok = wait(&opfree[j % nab], (j / nab) & 1, DEVERR_TIMEOUT_MMA)))
+                            break;
                         issue_next();
+                    }
                 }
             }
         }
@@ -348,7 +379,8 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                 }
             }
         };
-        load_x(sg0.c0);
+        if (!xs)
+            load_x(sg0.c0);
         int g = 0;
         bool ok = true;
         MmSeg sg;
@@ -415,20 +447,22 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                     tmem_st16(tcol + 16 * ((warp >> 2) + 4), v1);
                 }
                 // activations: fp32 -> fp16 into the B buffer (consecutive threads take
-                // consecutive tokens), then the next stage's loads
+                // consecutive tokens), then the next stage's loads (unless staged already)
+                if (!xs) {
 #pragma unroll
-                for (int i = 0; i < NXI; ++i) {
-                    const int it = tid + NDQ * i;
-                    const int n = it % NT, kg = it / NT;
-                    if (it < NT * (MM_KC / 8) && n < a.M) {
-                        const float4 x0 = xn[i][0], x1 = xn[i][1];
-                        const uint4 v = make_uint4(
-                            h2_bits(__floats2half2_rn(x0.x, x0.y)), h2_bits(__floats2half2_rn(x0.z, x0.w)),
-                            h2_bits(__floats2half2_rn(x1.x, x1.y)), h2_bits(__floats2half2_rn(x1.z, x1.w)));
-                        *reinterpret_cast<uint4*>(Bt + mm_off(n, 8 * kg)) = v;
+                    for (int i = 0; i < NXI; ++i) {
+                        const int it = tid + NDQ * i;
+                        const int n = it % NT, kg = it / NT;
+                        if (it < NT * (MM_KC / 8) && n < a.M) {
+                            const float4 x0 = xn[i][0], x1 = xn[i][1];
+                            const uint4 v = make_uint4(
+                                h2_bits(__floats2half2_rn(x0.x, x0.y)), h2_bits(__floats2half2_rn(x0.z, x0.w)),
+                                h2_bits(__floats2half2_rn(x1.x, x1.y)), h2_bits(__floats2half2_rn(x1.z, x1.w)));
+                            *reinterpret_cast<uint4*>(Bt + mm_off(n, 8 * kg)) = v;
+                        }
                     }
+                    load_x(hc + 1 < sg.c1 ? hc + 1 : next_c0);
                 }
-                load_x(hc + 1 < sg.c1 ? hc + 1 : next_c0);
                 tmem_st_wait();
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
@@ -559,6 +593,32 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
         btr[3] = globaltimer_ns();
 }
 
+// The M tokens' activations as fp16 B tiles, one per block column: item (column hc,
+// token n, 8-element group kg) converts X[n][256 hc + 8 kg .. + 8) and stores it at
+// mm_off(n, 8 kg) of tile hc; tokens n >= M are zero.  A dependent launch: it waits
+// for X's producer, and the product launched after it waits for it.
+template <int NT>
+__global__ void __launch_bounds__(256) mm_stage_x_kernel(const float* __restrict__ X, uint8_t* __restrict__ xh, int M,
+                                                         int K)
+{
+    pdl_trigger();
+    pdl_wait();
+    const int it = blockIdx.x * 256 + threadIdx.x;
+    const int nblk = K / 256;
+    if (it >= nblk * NT * (MM_KC / 8))
+        return;
+    const int hc = it / (NT * (MM_KC / 8)), rem = it - hc * NT * (MM_KC / 8);
+    const int n = rem % NT, kg = rem / NT;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (n < M) {
+        const float4* xp = reinterpret_cast<const float4*>(X + static_cast<size_t>(n) * K + hc * MM_KC + 8 * kg);
+        const float4 x0 = xp[0], x1 = xp[1];
+        v = make_uint4(h2_bits(__floats2half2_rn(x0.x, x0.y)), h2_bits(__floats2half2_rn(x0.z, x0.w)),
+                       h2_bits(__floats2half2_rn(x1.x, x1.y)), h2_bits(__floats2half2_rn(x1.z, x1.w)));
+    }
+    *reinterpret_cast<uint4*>(xh + static_cast<size_t>(hc) * mm_b_bytes(NT) + mm_off(n, 8 * kg)) = v;
+}
+
 }  // namespace dq
 
 namespace dqhost {
@@ -595,9 +655,17 @@ static long long split_grid(int rows, int K)
 // serves calls of any shapes that fit it.
 constexpr size_t SPLIT_CNT_BYTES = 65536;
 constexpr int SPLIT_MAX_ROWS = static_cast<int>(SPLIT_CNT_BYTES / 16) * dq::MM_ROWS;
+// Above 32 tokens the activations are staged once as fp16 B tiles (after the counts)
+// and copied with the weights; up to 32 the dequantising warps stage them (measured:
+// 64 tokens 52.9 -> 36.4 us on 12288 x 4096, 32 tokens 27.7 -> 29.9 us).
+static bool split_staged_x(int M) { return mm_nt(M) >= 64; }
+static size_t split_xh_bytes(int M, int K)
+{
+    return split_staged_x(M) ? static_cast<size_t>(K / 256) * dq::mm_b_bytes(mm_nt(M)) : 0;
+}
 static size_t split_ws_bytes(int M, int rows, int K)
 {
-    return SPLIT_CNT_BYTES + static_cast<size_t>(split_grid(rows, K)) * 2 * M * dq::MM_ROWS * 4;
+    return SPLIT_CNT_BYTES + split_xh_bytes(M, K) + static_cast<size_t>(split_grid(rows, K)) * 2 * M * dq::MM_ROWS * 4;
 }
 
 static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, int rows, int K, void* ws,
@@ -630,8 +698,11 @@ static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, i
     a.box_rows = std::min(dq::MM_ROWS, ws ? rows : per_block);
     if (ws) {
         a.cnt = static_cast<unsigned*>(ws);
-        a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + SPLIT_CNT_BYTES);
+        if (split_staged_x(M))
+            a.xh = static_cast<uint8_t*>(ws) + SPLIT_CNT_BYTES;
+        a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + SPLIT_CNT_BYTES + split_xh_bytes(M, K));
     }
+    const bool xs = a.xh != nullptr;
     a.err = device_error_flag();
     a.trace = gemv_trace();
     // the deepest operand pipeline, then as many ring slots, as shared memory holds
@@ -639,15 +710,15 @@ static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, i
     a.ns = 2;
     for (int nab = dq::MM_NAB_MAX; nab >= 2 && a.nab == 2; --nab)
         for (int ns = dq::MM_NS_MAX; ns >= 2; --ns)
-            if (dq::mm_smem_bytes(nt, ns, nab, a.box_rows) <= 227 * 1024 &&
+            if (dq::mm_smem_bytes(nt, ns, nab, a.box_rows, xs) <= 227 * 1024 &&
                 dq::MM_ACC * nt + nab * dq::MM_TA_COLS <= 512) {  // tensor memory holds it
                 a.nab = nab;
                 a.ns = ns;
                 break;
             }
-    if (dq::mm_smem_bytes(nt, a.ns, a.nab, a.box_rows) > 227 * 1024)
+    if (dq::mm_smem_bytes(nt, a.ns, a.nab, a.box_rows, xs) > 227 * 1024)
         return DQ_ERR_UNSUPPORTED;
-    const int smem = dq::mm_smem_bytes(nt, a.ns, a.nab, a.box_rows);
+    const int smem = dq::mm_smem_bytes(nt, a.ns, a.nab, a.box_rows, xs);
     const cuuint64_t row_bytes = static_cast<cuuint64_t>(K / 256) * dq::Q4K_BYTES;
     const cuuint64_t dims[2] = {row_bytes / 8, static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {row_bytes};
@@ -657,17 +728,28 @@ static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, i
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return DQ_ERR_UNSUPPORTED;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(dq::MM_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k, a);
+    cudaError_t e;
+    if (xs) {  // the fp16 B tiles first (a dependent launch of its own)
+        const int items = (K / 256) * nt * (dq::MM_KC / 8);
+        cfg.gridDim = dim3((items + 255) / 256);
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
+        void (*sx)(const float*, uint8_t*, int, int) = dq::mm_stage_x_kernel<64>;
+        e = cudaLaunchKernelEx(&cfg, sx, X, const_cast<uint8_t*>(a.xh), M, K);
+        if (e != cudaSuccess)
+            return set_cuda_error(e);
+    }
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(dq::MM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    e = cudaLaunchKernelEx(&cfg, k, a);
     return e == cudaSuccess ? DQ_OK : set_cuda_error(e);
 }
 
