@@ -665,10 +665,13 @@ __device__ __forceinline__ void tk_attention(int p)
         AttnSmem& sm = *reinterpret_cast<AttnSmem*>(tk_xq() + sub * (TK_ATT_STAGING / 4));
         const int bar = ATT_BAR - sub;
         // Items are numbered chunks first, merging (last) chunks after them: every
-        // pair of warp groups takes its items in increasing order, so a merging item
-        // only ever waits for items that their groups run before any merging one.
+        // warp group takes its items in increasing order, so a merging item only ever
+        // waits for items that their groups run before any merging one.
         const int nplain = (nact - 1) * A.n_kv;
-        for (int item = 2 * blockIdx.x + sub; item < nact * A.n_kv; item += 2 * gridDim.x) {
+        // item b of block b's first warp group, then b + blocks of its second: up to one
+        // item a block runs alone (at 512 keys 136 items on 136 blocks rather than two
+        // each on 68)
+        for (int item = static_cast<int>(blockIdx.x + gridDim.x * sub); item < nact * A.n_kv; item += 2 * gridDim.x) {
             const int c = item < nplain ? item % (nact - 1) : nact - 1;
             const int g = item < nplain ? item / (nact - 1) : item - nplain;
             if (!attn_block(t, c, g, group, sm, false, bar, 32 * group * sub)) {
