@@ -20,16 +20,42 @@ enum { PH_QKV = 0, PH_ATTN, PH_O, PH_GATEUP, PH_DOWN_Q4, PH_DOWN_Q6, PH_VOCAB, P
 // Consumer layout by kind: row groups of tk_p threads (each thread holds tk_ul
 // 32-element units of the activation, so K <= 32 tk_p tk_ul), tk_rpt rows per
 // thread and matrix; a tile holds TK_THREADS / tk_p * tk_rpt rows of each matrix.
-__host__ __device__ constexpr int tk_p(int kind) { return kind == PH_GATEUP ? 64 : 128; }
+#ifndef TK_GU_P
+#define TK_GU_P 64
+#define TK_GU_UL 2
+#define TK_GU_RPT 1
+#endif
+#ifndef TK_QKV_P
+#define TK_QKV_P 64
+#define TK_QKV_UL 2
+#define TK_QKV_RPT 2
+#endif
+#ifndef TK_VOC_P
+#define TK_VOC_P 128
+#define TK_VOC_UL 1
+#define TK_VOC_RPT 3
+#endif
+__host__ __device__ constexpr int tk_p(int kind)
+{
+    return kind == PH_GATEUP ? TK_GU_P : kind == PH_QKV ? TK_QKV_P : kind == PH_VOCAB ? TK_VOC_P : 128;
+}
 // activation units a thread holds (K <= 32 tk_p tk_ul)
 __host__ __device__ constexpr int tk_ul(int kind)
 {
-    return kind == PH_GATEUP ? 2 : kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 3 : 1;
+    return kind == PH_GATEUP ? TK_GU_UL
+           : kind == PH_QKV ? TK_QKV_UL
+           : kind == PH_VOCAB ? TK_VOC_UL
+           : kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 3
+                                                      : 1;
 }
 __host__ __device__ constexpr int tk_rg(int kind) { return TK_THREADS / tk_p(kind); }
 __host__ __device__ constexpr int tk_rpt(int kind)
 {
-    return kind == PH_GATEUP || kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 1 : kind == PH_VOCAB ? 3 : 4;
+    return kind == PH_GATEUP ? TK_GU_RPT
+           : kind == PH_QKV ? TK_QKV_RPT
+           : kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 1
+           : kind == PH_VOCAB ? TK_VOC_RPT
+                              : 4;
 }
 __host__ __device__ constexpr int tk_rows_per_tile(int kind) { return tk_rg(kind) * tk_rpt(kind); }
 
