@@ -867,7 +867,7 @@ int plan_token(int n_layers, int hidden, int ffn, int n_q, int n_kv, int hd, boo
 {
     using namespace dq;
     const int qdim = n_q * hd;
-    if (n_layers > TK_MAX_LAYERS || hidden > 32 * tk_p(PH_QKV) * tk_ul(PH_QKV) || qdim > 32 * tk_p(PH_O) ||
+    if (n_layers > TK_MAX_LAYERS || hidden > 32 * tk_p(PH_QKV) * tk_ul(PH_QKV) || qdim > 32 * tk_p(PH_O) * tk_ul(PH_O) ||
         hidden > 32 * tk_p(PH_GATEUP) * tk_ul(PH_GATEUP) || hidden > 32 * tk_p(PH_VOCAB) * tk_ul(PH_VOCAB) ||
         ffn > 32 * tk_p(PH_DOWN_Q4) * tk_ul(PH_DOWN_Q4) || hidden % 2048 || qdim % 256 || ffn % 256 || hd != ATT_HD || n_q % n_kv ||
         n_q / n_kv > 8)

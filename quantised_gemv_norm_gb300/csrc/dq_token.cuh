@@ -30,6 +30,11 @@ enum { PH_QKV = 0, PH_ATTN, PH_O, PH_GATEUP, PH_DOWN_Q4, PH_DOWN_Q6, PH_VOCAB, P
 #define TK_QKV_UL 2
 #define TK_QKV_RPT 2
 #endif
+#ifndef TK_O_P
+#define TK_O_P 128
+#define TK_O_UL 1
+#define TK_O_RPT 4
+#endif
 #ifndef TK_VOC_P
 #define TK_VOC_P 128
 #define TK_VOC_UL 1
@@ -37,13 +42,18 @@ enum { PH_QKV = 0, PH_ATTN, PH_O, PH_GATEUP, PH_DOWN_Q4, PH_DOWN_Q6, PH_VOCAB, P
 #endif
 __host__ __device__ constexpr int tk_p(int kind)
 {
-    return kind == PH_GATEUP ? TK_GU_P : kind == PH_QKV ? TK_QKV_P : kind == PH_VOCAB ? TK_VOC_P : 128;
+    return kind == PH_GATEUP ? TK_GU_P
+           : kind == PH_QKV  ? TK_QKV_P
+           : kind == PH_O    ? TK_O_P
+           : kind == PH_VOCAB ? TK_VOC_P
+                              : 128;
 }
 // activation units a thread holds (K <= 32 tk_p tk_ul)
 __host__ __device__ constexpr int tk_ul(int kind)
 {
     return kind == PH_GATEUP ? TK_GU_UL
            : kind == PH_QKV ? TK_QKV_UL
+           : kind == PH_O ? TK_O_UL
            : kind == PH_VOCAB ? TK_VOC_UL
            : kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 3
                                                       : 1;
@@ -53,6 +63,7 @@ __host__ __device__ constexpr int tk_rpt(int kind)
 {
     return kind == PH_GATEUP ? TK_GU_RPT
            : kind == PH_QKV ? TK_QKV_RPT
+           : kind == PH_O ? TK_O_RPT
            : kind == PH_DOWN_Q4 || kind == PH_DOWN_Q6 ? 1
            : kind == PH_VOCAB ? TK_VOC_RPT
                               : 4;
