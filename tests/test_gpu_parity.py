@@ -347,6 +347,36 @@ def test_matmul_q4k_split(dq, orc, rows, K, M):
     assert dq.device_error() == 0
 
 
+@pytest.mark.parametrize("M", [8, 64])
+def test_matmul_q4k_split_graph_replay(dq, M):
+    """Two calls captured in one CUDA graph (dependent launches, and above 32 tokens
+    the activation pre-pass) and the graph replayed twice: every replay gives the
+    eager call's bits, and the counts are back at zero after each."""
+    rows, K = 12288, 4096
+    W = cuda(synth.quant_matrix(15, synth.FMT_Q4K, rows, K))
+    X = cuda(np.stack([synth.activation(15, K, m) for m in range(M)]))
+    ws = dq.matmul_split_workspace(M, rows, K)
+    ref = dq.matmul_q4k_split(W, X, ws).clone()
+    Y1 = torch.empty_like(ref)
+    Y2 = torch.empty_like(ref)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            dq.matmul_q4k_split(W, X, ws, out=Y1)
+            dq.matmul_q4k_split(W, X, ws, out=Y2)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        Y1.zero_()
+        Y2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(Y1, ref) and torch.equal(Y2, ref)
+        assert int(ws[:65536].view(torch.int32).abs().sum()) == 0
+    assert dq.device_error() == 0
+
+
 def test_matmul_q4k_split_workspace_reuse(dq, orc):
     """One workspace, sized for the largest, serves calls of several shapes in turn."""
     ws = dq.matmul_split_workspace(64, 12288, 4096)
