@@ -332,7 +332,7 @@ DQ_API int dq_matmul_q4k(const void* W_blocks, const float* X, float* Y, int M, 
  * contiguous runs, so every tile is full and a block takes 10 or 11 stages
  * instead of 16 on that table.  A tile whose columns two or three blocks share
  * is summed from their partial tiles in block order (deterministic: the same
- * order whichever block finishes last).  For M > 32 a first kernel converts X
+ * order whichever block finishes last).  For M > 16 a first kernel converts X
  * once into fp16 tiles in the workspace, which each stage then copies beside its
  * weights (instead of every block converting every token's activations).
  * Arguments, operand rounding and errors as dq_matmul_q4k_path with
@@ -341,7 +341,7 @@ DQ_API int dq_matmul_q4k(const void* W_blocks, const float* X, float* Y, int M, 
  * dq_matmul_q4k_split_workspace_bytes(M, rows, K) bytes (else DQ_ERR_SHAPE),
  * 16-byte aligned (else DQ_ERR_ALIGN), owned by the caller, zero-filled before
  * its first use.  Its first 64 KB hold the tiles' counts, which every call
- * leaves at zero, the rest the fp16 activations (M > 32) and the partial tiles:
+ * leaves at zero, the rest the fp16 activations (M > 16) and the partial tiles:
  * it serves later calls of any shape whose size fits.  Calls sharing one workspace must not run at the same time
  * (one workspace per stream).  After a call that reports a device error,
  * zero-fill it again. */

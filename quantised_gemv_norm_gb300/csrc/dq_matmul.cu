@@ -294,12 +294,16 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                 total += sg.c1 - sg.c0;
             // the next stage to copy: segment iseg, block column icol
             MmSeg isg = sg0;
-            int iseg = 0, icol = sg0.c0, gnext = 0;
+            int iseg = 0, icol = sg0.c0, gnext = 0, islot = 0;  // islot = gnext % ns
             // one block column of a tile's rows into slot gnext % ns (box_rows >= the
-            // tile's rows: extra rows are the next tile's or zero fill)
+            // tile's rows: extra rows are the next tile's or zero fill).  Stage and slot
+            // indices advance by counters: a division by the run-time ring or buffer
+            // count costs tens of instructions.
             const uint64_t pol_x = l2_evict_last_policy();  // every block reads the B tiles
             auto issue_next = [&]() {
-                const int s = gnext % a.ns;
+                const int s = islot;
+                if (++islot == a.ns)
+                    islot = 0;
                 mbar_arrive_expect_tx(&full[s],
                                       static_cast<uint32_t>(a.box_rows * MM_ROWB + (xs ? mm_b_bytes(NT) : 0)));
                 tma_load_2d(ring + s * slot_bytes, &a.tmap, icol * (Q4K_BYTES / 8), isg.row0, &full[s], pol);
@@ -314,11 +318,12 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                 while (gnext < min(a.ns, total))
                     issue_next();
             int g = 0;
+            int buf = 0, slot = 0, pbuf = nab - 1;  // g % nab, g % ns, (g - 1) % nab
+            uint32_t bph = 0, pbph = 1;            // (g / nab) & 1, ((g - 1) / nab) & 1
             bool ok = true;
             for (int i = 0; ok && mm_seg(a, b, G, i, sg); ++i) {
                 for (int hc = sg.c0; hc < sg.c1; ++hc, ++g) {
-                    const int buf = g % nab;
-                    if (!(ok = wait(&opready[buf], (g / nab) & 1, DEVERR_TIMEOUT_FULL)))
+                    if (!(ok = wait(&opready[buf], bph, DEVERR_TIMEOUT_FULL)))
                         break;
                     unsigned long long* tr = (a.trace && b == 0 && cq == 0 && g < 32) ? a.trace + 8 * g : nullptr;
                     if (tr)
@@ -326,7 +331,7 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                     tc_fence_after_sync();
                     const uint32_t ta = tbase + mm_ta_col(NT) + MM_TA_COLS * buf;
                     const uint64_t bd = umma_desc_kmajor(
-                        xs ? ring + (g % a.ns) * slot_bytes + wslot : Bbuf + buf * mm_b_bytes(NT), MM_LBO, MM_SBO);
+                        xs ? ring + slot * slot_bytes + wslot : Bbuf + buf * mm_b_bytes(NT), MM_LBO, MM_SBO);
                     // K = 16 per MMA: 8 columns of A, two core matrices of B.  MMA s adds
                     // into accumulator s % MM_ACC, so consecutive MMAs do not wait on each
                     // other; the segment's first stage starts the accumulators afresh.
@@ -349,11 +354,18 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                     } else if (cq == 0 && g >= 1 && g - 1 + a.ns < total) {
                         // the MMAs read the B tile from the slot: stage g - 1's slot is free
                         // once its MMAs are done (committed one stage ago)
-                        const int j = g - 1;
-                        if (!(ok = wait(&opfree[j % nab], (j / nab) & 1, DEVERR_TIMEOUT_MMA)))
+                        if (!(ok = wait(&opfree[pbuf], pbph, DEVERR_TIMEOUT_MMA)))
                             break;
                         issue_next();
                     }
+                    pbuf = buf;
+                    pbph = bph;
+                    if (++buf == nab) {
+                        buf = 0;
+                        bph ^= 1u;
+                    }
+                    if (++slot == a.ns)
+                        slot = 0;
                 }
             }
         }
@@ -382,6 +394,8 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
         if (!xs)
             load_x(sg0.c0);
         int g = 0;
+        int dbuf = 0, dslot = 0;      // g % nab, g % ns
+        uint32_t dbph = 0, dsph = 0;  // (g / nab) & 1, (g / ns) & 1
         bool ok = true;
         MmSeg sg;
         for (int si = 0; ok && mm_seg(a, b, G, si, sg); ++si) {
@@ -389,17 +403,18 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
             MmSeg nx;
             const int next_c0 = mm_seg(a, b, G, si + 1, nx) ? nx.c0 : -1;
             for (int hc = sg.c0; hc < sg.c1; ++hc, ++g) {
-                const int buf = g % nab, s = g % a.ns;
+                const int buf = dbuf, s = dslot;
                 unsigned long long* tr = (a.trace && b == 0 && tid == 0 && g < 32) ? a.trace + 8 * g : nullptr;
                 if (tr)
                     tr[2] = clock64();
-                if (!(ok = warp_wait(&full[s], (g / a.ns) & 1, DEVERR_TIMEOUT_FULL)))
+                if (!(ok = warp_wait(&full[s], dsph, DEVERR_TIMEOUT_FULL)))
                     break;
                 if (tr)
                     tr[3] = clock64();
                 if (btr && g == 0 && tid == 0)
                     btr[1] = globaltimer_ns();
-                if (g >= nab && !(ok = warp_wait(&opfree[buf], ((g - nab) / nab) & 1, DEVERR_TIMEOUT_MMA)))
+                // stage g - nab's MMAs (buffer buf, one use earlier) are done
+                if (g >= nab && !(ok = warp_wait(&opfree[buf], dbph ^ 1u, DEVERR_TIMEOUT_MMA)))
                     break;
                 if (tr)
                     tr[4] = clock64();
@@ -471,6 +486,14 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&opready[buf]);  // release: this warp's part of stage g is written
+                if (++dbuf == nab) {
+                    dbuf = 0;
+                    dbph ^= 1u;
+                }
+                if (++dslot == a.ns) {
+                    dslot = 0;
+                    dsph ^= 1u;
+                }
             }
             if (!ok)
                 break;
@@ -655,10 +678,10 @@ static long long split_grid(int rows, int K)
 // serves calls of any shapes that fit it.
 constexpr size_t SPLIT_CNT_BYTES = 65536;
 constexpr int SPLIT_MAX_ROWS = static_cast<int>(SPLIT_CNT_BYTES / 16) * dq::MM_ROWS;
-// Above 32 tokens the activations are staged once as fp16 B tiles (after the counts)
-// and copied with the weights; up to 32 the dequantising warps stage them (measured:
-// 64 tokens 52.9 -> 36.4 us on 12288 x 4096, 32 tokens 27.7 -> 29.9 us).
-static bool split_staged_x(int M) { return mm_nt(M) >= 64; }
+// Above 16 tokens the activations are staged once as fp16 B tiles (after the counts)
+// and copied with the weights; up to 16 the dequantising warps stage them (measured
+// on 12288 x 4096: 64 tokens 36.4 -> 33.0 us, 32 tokens 29.7 -> 27.2 us).
+static bool split_staged_x(int M) { return mm_nt(M) >= 32; }
 static size_t split_xh_bytes(int M, int K)
 {
     return split_staged_x(M) ? static_cast<size_t>(K / 256) * dq::mm_b_bytes(mm_nt(M)) : 0;
@@ -741,7 +764,7 @@ static int launch_matmul_tc(const uint8_t* W, const float* X, float* Y, int M, i
         cfg.gridDim = dim3((items + 255) / 256);
         cfg.blockDim = dim3(256);
         cfg.dynamicSmemBytes = 0;
-        void (*sx)(const float*, uint8_t*, int, int) = dq::mm_stage_x_kernel<64>;
+        void (*sx)(const float*, uint8_t*, int, int) = nt == 32 ? dq::mm_stage_x_kernel<32> : dq::mm_stage_x_kernel<64>;
         e = cudaLaunchKernelEx(&cfg, sx, X, const_cast<uint8_t*>(a.xh), M, K);
         if (e != cudaSuccess)
             return set_cuda_error(e);

@@ -347,9 +347,9 @@ def test_matmul_q4k_split(dq, orc, rows, K, M):
     assert dq.device_error() == 0
 
 
-@pytest.mark.parametrize("M", [8, 64])
+@pytest.mark.parametrize("M", [8, 32, 64])
 def test_matmul_q4k_split_graph_replay(dq, M):
-    """Two calls captured in one CUDA graph (dependent launches, and above 32 tokens
+    """Two calls captured in one CUDA graph (dependent launches, and above 16 tokens
     the activation pre-pass) and the graph replayed twice: every replay gives the
     eager call's bits, and the counts are back at zero after each."""
     rows, K = 12288, 4096
