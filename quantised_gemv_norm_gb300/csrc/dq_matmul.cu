@@ -266,6 +266,8 @@ __global__ void __launch_bounds__(MM_THREADS, 1) matmul_q4k_tc_kernel(const __gr
 
     // a bounded wait; false once this block has given up
     auto wait = [&](uint64_t* bar, uint32_t parity, int code) -> bool {
+        if (mbar_try_wait(bar, parity))
+            return true;  // complete: the block's failure flag matters only for a wait that blocks
         if (*fail)
             return false;
         if (!mbar_wait(bar, parity)) {
