@@ -311,7 +311,7 @@ DQ_API int dq_attention_decode_rope(const float* q, const float* k_new, void* k_
  * M times; K <= 16384).  DQ_MATMUL_TENSOR reads W once for all tokens on the
  * tensor cores (tcgen05.mma, fp16 operands: each weight and activation is
  * rounded to fp16, |X| must stay below 65504; fp32 accumulation).
- * DQ_MATMUL_AUTO picks CUDA cores for M <= 3 and tensor cores for M >= 4 (the
+ * DQ_MATMUL_AUTO picks CUDA cores for M <= 2 and tensor cores for M >= 3 (the
  * measured crossover on the 12288 x 4096 table).
  * Errors: NULL -> DQ_ERR_NULL; M, rows, K or path out of range ->
  * DQ_ERR_SHAPE; misaligned W or X -> DQ_ERR_ALIGN; CUDA-core path with

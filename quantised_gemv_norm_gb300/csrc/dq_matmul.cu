@@ -791,8 +791,9 @@ DQ_API int dq_matmul_q4k_path(const void* W_blocks, const float* X, float* Y, in
         return DQ_ERR_SHAPE;
     if (!dqhost::aligned16(W_blocks) || !dqhost::aligned16(X))
         return DQ_ERR_ALIGN;
-    // measured crossover: one GEMV per token is faster up to M = 3
-    const bool tensor = path == DQ_MATMUL_TENSOR || (path == DQ_MATMUL_AUTO && M >= 4);
+    // measured crossover on 12288 x 4096: one GEMV per token is faster up to M = 2
+    // (9.3 / 17.7 / about 26 us for M = 1 / 2 / 3 against 21.8 on the tensor cores)
+    const bool tensor = path == DQ_MATMUL_TENSOR || (path == DQ_MATMUL_AUTO && M >= 3);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (tensor)
         return dqhost::launch_matmul_tc(static_cast<const uint8_t*>(W_blocks), X, Y, M, rows, K, nullptr, s);

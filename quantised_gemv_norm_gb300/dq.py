@@ -237,7 +237,7 @@ MATMUL_AUTO, MATMUL_CUDA_CORE, MATMUL_TENSOR = 0, 1, 2
 def matmul_q4k(W: torch.Tensor, X: torch.Tensor, out=None, path: int = MATMUL_AUTO):
     """W: uint8 [rows, K/256*144]; X: fp32 [M, K] -> fp32 [M, rows].
 
-    ``path``: MATMUL_AUTO (CUDA cores up to M = 3, tensor cores above),
+    ``path``: MATMUL_AUTO (CUDA cores up to M = 2, tensor cores above),
     MATMUL_CUDA_CORE (one GEMV per token) or MATMUL_TENSOR (one read of W)."""
     lib = load()
     rows = W.shape[0]

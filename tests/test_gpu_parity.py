@@ -302,7 +302,7 @@ def test_attention_decode_rope(dq, orc, n_q, n_kv, n_keys):
 # ------------------------------------------------------------- M-sweep
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 64])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 16, 64])
 def test_matmul_q4k(dq, orc, M):
     rows, K = 12288, 4096
     W = synth.quant_matrix(9, synth.FMT_Q4K, rows, K)
