@@ -75,11 +75,13 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool resid, GemvPl
     // Row groups of P threads (P >= 64 so that the groups' named barriers fit).
     // Least masked lanes first, then more groups (smaller P).
     static const int Ps[] = {64, 128, 256, 512};
-    // bf16 with at least 64 rows a block: groups of 128 or more (measured on 12288 x
-    // 4096: 16.7 against 18.6 us with 64-thread groups; 4096 x 4096, 27 rows a
-    // block, keeps 64: 7.85 against 7.97)
+    // bf16 and Q4_K with at least 64 rows a block: groups of 128 or more (measured:
+    // bf16 12288 x 4096 16.7 against 18.6 us with 64-thread groups, Q4_K 12288 x 4096
+    // 9.03 against 9.16; bf16 4096 x 4096, 27 rows a block, keeps 64: 7.85 against
+    // 7.97; Q6_K keeps 64: the vocabulary shape 79.5 against 86.1 with 128)
     const int sms = sm_count();
-    const int pmin = (fmt == DQ_FMT_BF16 && (rows + sms - 1) / sms >= 64) ? 128 : 64;
+    const bool tall_fmt = fmt == DQ_FMT_BF16 || fmt == DQ_FMT_Q4K;
+    const int pmin = (tall_fmt && (rows + sms - 1) / sms >= 64) ? 128 : 64;
     int best_P = 0, best_UL = 0, best_waste = 1 << 30;
     for (int pi = 0; pi < 4; ++pi) {
         const int P = Ps[pi];
