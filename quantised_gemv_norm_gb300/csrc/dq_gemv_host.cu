@@ -122,7 +122,10 @@ int plan_gemv(int fmt, int rows, int K, int nmat, int planes, bool resid, GemvPl
     // bytes so small matrices still pipeline; rows per thread RPT in {1, 2, 4}.
     const long long per_block = static_cast<long long>((rows + p.grid - 1) / p.grid) * rb * nmat;
     const long long unit_stage = static_cast<long long>(p.RG) * rb * nmat;
-    long long cap = per_block / 4;
+#ifndef GEMV_CAP_DIV
+#define GEMV_CAP_DIV 4
+#endif
+    long long cap = per_block / GEMV_CAP_DIV;
     if (cap > GEMV_STAGE_TARGET)
         cap = GEMV_STAGE_TARGET;
     p.RPT = 1;

@@ -27,7 +27,10 @@ struct GemvPlan {
     GemvKernel kernel;
 };
 
-constexpr int GEMV_STAGE_TARGET = 48 * 1024;   // bytes per ring stage (upper target)
+#ifndef GEMV_STAGE_TARGET_KB
+#define GEMV_STAGE_TARGET_KB 48
+#endif
+constexpr int GEMV_STAGE_TARGET = GEMV_STAGE_TARGET_KB * 1024;  // bytes per ring stage (upper target)
 constexpr int GEMV_STAGE_MAX = 64 * 1024;      // largest stage accepted
 constexpr int GEMV_RING_MAX = 176 * 1024;      // ring bytes at most (one block per SM)
 constexpr int GEMV_SMEM_MAX = 227 * 1024;      // shared memory one block may use
