@@ -327,11 +327,13 @@ def test_matmul_q4k_tensor_shapes(dq, orc, rows, K, M):
 
 
 @pytest.mark.parametrize("rows,K,M", [(12288, 4096, 1), (12288, 4096, 16), (12288, 4096, 64), (128, 4096, 3),
-                                      (300, 768, 5), (1000, 2048, 8), (20000, 512, 17), (77, 2048, 2)])
+                                      (300, 768, 5), (1000, 2048, 8), (20000, 512, 17), (77, 2048, 2),
+                                      (256, 16384, 4), (40000, 256, 33)])
 def test_matmul_q4k_split(dq, orc, rows, K, M):
     """K split across blocks: the 12288 x 4096 table (tiles shared by two or three
-    blocks), one tile shared by 16 blocks, ragged last tiles, fewer stages than
-    SMs.  Against the oracle at the GEMV bar; a second call on the same workspace
+    blocks), one tile shared by 16 blocks, two tiles of 64 block columns shared by 64
+    blocks each, ragged last tiles, fewer stages than SMs, and single-column rows
+    where every block takes whole tiles.  Against the oracle at the GEMV bar; a second call on the same workspace
     (its tile counts left at zero) gives the same bits."""
     W = synth.quant_matrix(13, synth.FMT_Q4K, rows, K)
     X = np.stack([synth.activation(13, K, m) for m in range(M)])
